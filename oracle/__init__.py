@@ -1,0 +1,47 @@
+"""CPU oracle for certified sparse decode attention -- TEST INFRASTRUCTURE ONLY.
+
+This package is a plain, slow, independent restatement of the decode step of
+"Certified Sparse Attention via Perturbed Retrieval" (arXiv 2610.24991).
+Sources, cited by page and section in every function:
+  * picx.dev summary -- "Methodology / Problem Setup", "Algorithm Components"
+    1-4, "Theoretical Contributions" (Theorems 1-4);
+  * readsearch.ai abstract page -- "Abstract" (GQA-shared scan, fresh
+    perturbations at every decoding step).
+
+It shares no code with the CUDA library under
+``certified_sparse_attention_gb300/``: no headers, kernels, helpers, constants
+or tables.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import it; the product path never does.
+
+Precision: exact scores, weights, statistics and certificates are float64.
+The pieces the GPU must reproduce bit for bit -- the 4-bit key quantiser, the
+deterministic score bounds, the hashed perturbations and the candidate levels
+-- are emulated step by step in IEEE float32 (numpy float32, no fused
+multiply-add), with the operation order written out in ``bounds.py`` and
+``fp32.py``.
+
+Parity status per function (the pins live in ``tests/test_oracle_*.py``):
+  * hashing / log2, quantiser, bounds, inclusion law, nestedness,
+    unbiasedness, exact special cases, Chernoff / Bernstein events,
+    coverage: pinned (closed forms, brute force, Monte Carlo).
+  * which level stops and the exact o / beta values there: parity unpinned by
+    the pages (they print no worked example); pinned only through the
+    statistical and algebraic checks above.
+"""
+from .fp32 import tree_sum_f32, log2_m53_f32
+from .hashing import mix64, group_key, key_hashes, perturb_t
+from .quantize import quantize_keys, vmax_blocks
+from .bounds import query_prep, key_bounds, QM_DEFAULT
+from .certificate import chernoff_interval, certificate_levels
+from .step import (Params, grid_J, oracle_decode_group, dense_attention,
+                   GroupResult, exact_levels, level_sums, score_f32,
+                   cstar_lower_f32, bound_levels_f32)
+
+__all__ = [
+    "tree_sum_f32", "log2_m53_f32", "mix64", "group_key", "key_hashes",
+    "perturb_t", "quantize_keys", "vmax_blocks", "query_prep", "key_bounds",
+    "QM_DEFAULT", "chernoff_interval", "certificate_levels", "Params",
+    "grid_J", "oracle_decode_group", "dense_attention", "GroupResult",
+    "exact_levels", "level_sums", "score_f32", "cstar_lower_f32",
+    "bound_levels_f32",
+]

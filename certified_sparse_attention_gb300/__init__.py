@@ -1,0 +1,280 @@
+"""Certified sparse decode attention on GB300 -- Python binding of libcsa.
+
+Thin ctypes layer over the C ABI in ``include/csa.h``: the functions below
+carry the same names as the C entry points and only marshal arguments (torch
+tensors -> device pointers, Python ints -> host arrays).  Every step of the
+decode path runs in the library's CUDA kernels; there is no Python or CPU
+fallback, and a missing library raises ``CsaLibraryMissing``.
+
+PyTorch supplies device memory and streams only.
+
+Paper: "Certified Sparse Attention via Perturbed Retrieval" (arXiv
+2610.24991), picx.dev summary "Methodology" and "Algorithm Components" 1-4.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libcsa.so")
+
+CSA_OK = 0
+CSA_BF16, CSA_F32 = 0, 1
+CSA_MEASURE_VALUE, CSA_MEASURE_OUTPUT, CSA_MEASURE_DENOM = 0, 1, 2
+WINDOW = 64
+BLOCK = 64
+
+EXPORTED = ("csa_workspace_size", "csa_quantize_keys", "csa_decode_step",
+            "csa_dense_workspace_size", "csa_dense_decode", "csa_check",
+            "csa_status_string", "csa_workspace_layout")
+
+
+class CsaLibraryMissing(RuntimeError):
+    pass
+
+
+class CsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class csa_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int),
+                ("Hkv", ctypes.c_int), ("d", ctypes.c_int),
+                ("n_max", ctypes.c_int64), ("dtype", ctypes.c_int)]
+
+
+class csa_params(ctypes.Structure):
+    _fields_ = [("eps", ctypes.c_float), ("delta", ctypes.c_float),
+                ("r", ctypes.c_int), ("measure", ctypes.c_int),
+                ("J_override", ctypes.c_int)]
+
+
+class csa_head_stats(ctypes.Structure):
+    _fields_ = [("level", ctypes.c_int32), ("keys_read", ctypes.c_int32),
+                ("values_read", ctypes.c_int32),
+                ("n_candidates", ctypes.c_int32),
+                ("n_near_threshold", ctypes.c_int32), ("J", ctypes.c_int32),
+                ("rounds", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class csa_workspace_map(ctypes.Structure):
+    _fields_ = [("ubar", ctypes.c_size_t), ("cmax", ctypes.c_size_t),
+                ("s32", ctypes.c_size_t), ("jr_hist", ctypes.c_size_t),
+                ("total", ctypes.c_size_t), ("J1", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libcsa.so (once).  Raises CsaLibraryMissing if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise CsaLibraryMissing(
+            f"{path} is missing: build it with "
+            "`python -m certified_sparse_attention_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    P = ctypes.POINTER
+    lib.csa_workspace_size.argtypes = [P(csa_shape), P(csa_params)]
+    lib.csa_workspace_size.restype = sz
+    lib.csa_dense_workspace_size.argtypes = [P(csa_shape)]
+    lib.csa_dense_workspace_size.restype = sz
+    lib.csa_quantize_keys.argtypes = [P(csa_shape), vp, vp, P(ctypes.c_int64),
+                                      ctypes.c_int64, vp, vp, vp, vp]
+    lib.csa_quantize_keys.restype = ctypes.c_int
+    lib.csa_decode_step.argtypes = [P(csa_shape), P(csa_params), vp, vp, vp,
+                                    vp, vp, vp, P(ctypes.c_int64),
+                                    P(ctypes.c_uint64), vp, vp, vp, vp, vp,
+                                    vp, sz, vp]
+    lib.csa_decode_step.restype = ctypes.c_int
+    lib.csa_dense_decode.argtypes = [P(csa_shape), vp, vp, vp,
+                                     P(ctypes.c_int64), vp, vp, sz, vp]
+    lib.csa_dense_decode.restype = ctypes.c_int
+    lib.csa_check.argtypes = [vp, vp]
+    lib.csa_check.restype = ctypes.c_int
+    lib.csa_workspace_layout.argtypes = [P(csa_shape), P(csa_params),
+                                         P(csa_workspace_map)]
+    lib.csa_workspace_layout.restype = ctypes.c_int
+    lib.csa_status_string.argtypes = [ctypes.c_int]
+    lib.csa_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(s: int) -> str:
+    return load_library().csa_status_string(int(s)).decode()
+
+
+# ------------------------------------------------------------ marshalling
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _i64(xs: Sequence[int]):
+    return (ctypes.c_int64 * len(xs))(*[int(x) for x in xs])
+
+
+def _u64(xs: Sequence[int]):
+    return (ctypes.c_uint64 * len(xs))(*[int(x) & 0xFFFFFFFFFFFFFFFF
+                                         for x in xs])
+
+
+def make_shape(B, Hq, Hkv, d, n_max, dtype) -> csa_shape:
+    if not isinstance(dtype, int):
+        dtype = CSA_F32 if str(dtype) in ("f32", "float32",
+                                          "torch.float32") else CSA_BF16
+    return csa_shape(int(B), int(Hq), int(Hkv), int(d), int(n_max), dtype)
+
+
+def make_params(eps=0.05, delta=0.05, r=2, measure=CSA_MEASURE_VALUE,
+                J_override=-1) -> csa_params:
+    return csa_params(float(eps), float(delta), int(r), int(measure),
+                      int(J_override))
+
+
+def csa_workspace_size(shape: csa_shape, params: csa_params) -> int:
+    return int(load_library().csa_workspace_size(ctypes.byref(shape),
+                                                 ctypes.byref(params)))
+
+
+def csa_dense_workspace_size(shape: csa_shape) -> int:
+    return int(load_library().csa_dense_workspace_size(ctypes.byref(shape)))
+
+
+def csa_workspace_layout(shape: csa_shape, params: csa_params):
+    m = csa_workspace_map()
+    check(load_library().csa_workspace_layout(ctypes.byref(shape),
+                                              ctypes.byref(params),
+                                              ctypes.byref(m)),
+          "csa_workspace_layout")
+    return m
+
+
+def decode_ordered(u):
+    """Ordered-integer encoding of the maxima (csa_workspace_map.cmax) back
+    to float32 values (numpy uint32 array in, float32 array out)."""
+    import numpy as np
+    u = np.asarray(u, dtype=np.uint32)
+    bits = np.where(u >= np.uint32(0x80000000), u & np.uint32(0x7FFFFFFF),
+                    ~u).astype(np.uint32)
+    return bits.view(np.float32)
+
+
+def csa_quantize_keys(shape, K, V, lens, from_token, K4, bounds, vmax,
+                      stream=None) -> int:
+    return load_library().csa_quantize_keys(
+        ctypes.byref(shape), _ptr(K), _ptr(V), _i64(lens), int(from_token),
+        _ptr(K4), _ptr(bounds), _ptr(vmax), _stream(stream))
+
+
+def csa_decode_step(shape, params, q, K, V, K4, bounds, vmax, lens, seeds,
+                    o, beta, level, keys_read, stats, workspace,
+                    workspace_bytes, stream=None) -> int:
+    return load_library().csa_decode_step(
+        ctypes.byref(shape), ctypes.byref(params), _ptr(q), _ptr(K), _ptr(V),
+        _ptr(K4), _ptr(bounds), _ptr(vmax), _i64(lens), _u64(seeds), _ptr(o),
+        _ptr(beta), _ptr(level), _ptr(keys_read), _ptr(stats),
+        _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def csa_dense_decode(shape, q, K, V, lens, o, workspace, workspace_bytes,
+                     stream=None) -> int:
+    return load_library().csa_dense_decode(
+        ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V), _i64(lens), _ptr(o),
+        _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def csa_check(workspace, stream=None) -> int:
+    return load_library().csa_check(_ptr(workspace), _stream(stream))
+
+
+def check(status: int, where: str = "csa") -> None:
+    if status != CSA_OK:
+        raise CsaError(status, where)
+
+
+# ---------------------------------------------------- tensor conveniences
+
+def meta_buffers(shape: csa_shape, device):
+    """Allocate K4, bounds, vmax (torch, device) for a shape."""
+    import torch
+    nblk = (shape.n_max + BLOCK - 1) // BLOCK
+    K4 = torch.zeros((shape.B, shape.Hkv, nblk * BLOCK, shape.d // 2),
+                     dtype=torch.uint8, device=device)
+    bounds = torch.zeros((shape.B, shape.Hkv, nblk, 2, shape.d),
+                         dtype=torch.float32, device=device)
+    vmax = torch.zeros((shape.B, shape.Hkv, nblk), dtype=torch.float32,
+                       device=device)
+    return K4, bounds, vmax
+
+
+class DecodeStep:
+    """Owns the workspace and output buffers of csa_decode_step for one
+    shape and parameter set; ``__call__`` runs one step on the current
+    stream (asynchronously)."""
+
+    def __init__(self, shape: csa_shape, params: csa_params, device,
+                 with_stats: bool = False):
+        import torch
+        self.shape, self.params = shape, params
+        nbytes = csa_workspace_size(shape, params)
+        if nbytes == 0:
+            raise CsaError(1, "csa_workspace_size")
+        self.ws_bytes = nbytes
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        B, Hq, d = shape.B, shape.Hq, shape.d
+        self.o = torch.empty((B, Hq, d), dtype=torch.float32, device=device)
+        self.beta = torch.empty((B, Hq), dtype=torch.float32, device=device)
+        self.level = torch.empty((B, Hq), dtype=torch.int32, device=device)
+        self.keys_read = torch.empty((B, Hq), dtype=torch.int32,
+                                     device=device)
+        self.stats = (torch.zeros((B, Hq, 8), dtype=torch.int32,
+                                  device=device) if with_stats else None)
+
+    def __call__(self, q, K, V, K4, bounds, vmax, lens, seeds, stream=None):
+        st = csa_decode_step(self.shape, self.params, q, K, V, K4, bounds,
+                             vmax, lens, seeds, self.o, self.beta,
+                             self.level, self.keys_read, self.stats, self.ws,
+                             self.ws_bytes, stream)
+        check(st, "csa_decode_step")
+        return self.o, self.beta, self.level, self.keys_read
+
+
+class DenseDecode:
+    """Owns the workspace of csa_dense_decode for one shape."""
+
+    def __init__(self, shape: csa_shape, device):
+        import torch
+        self.shape = shape
+        self.ws_bytes = csa_dense_workspace_size(shape)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8,
+                              device=device)
+        self.o = torch.empty((shape.B, shape.Hq, shape.d),
+                             dtype=torch.float32, device=device)
+
+    def __call__(self, q, K, V, lens, stream=None):
+        check(csa_dense_decode(self.shape, q, K, V, lens, self.o, self.ws,
+                               self.ws_bytes, stream), "csa_dense_decode")
+        return self.o

@@ -1,0 +1,276 @@
+// Host side of the C ABI declared in include/csa.h: argument checks, the
+// workspace layout, the exact grid size J = ceil(r log2 |pool|), and the
+// launch sequence of one decode step.  No device memory is allocated here.
+#include <cmath>
+#include <cstring>
+
+#include "csa_args.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// J = smallest j with 2^j >= P^r (so tau_J = 2^(-j/r) <= 1/P); exact integers.
+int grid_J(int64_t P, int r) {
+  if (P <= 1) return 0;
+  unsigned __int128 target = 1;
+  for (int i = 0; i < r; ++i) target *= (unsigned __int128)P;
+  int j = 0;
+  while (((unsigned __int128)1 << j) < target) ++j;
+  return j;
+}
+
+bool shape_ok(const csa_shape* s) {
+  return s && s->B >= 1 && s->Hq >= 1 && s->Hkv >= 1 && s->Hq % s->Hkv == 0 && s->n_max >= 1 &&
+         s->n_max <= (int64_t)1 << 31 && (s->dtype == CSA_BF16 || s->dtype == CSA_F32);
+}
+csa_status shape_supported(const csa_shape* s) {
+  const int G = s->Hq / s->Hkv;
+  if (s->d != 64 && s->d != 128) return CSA_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return CSA_ERR_UNSUPPORTED;
+  if (s->B > kMaxB) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+bool params_ok(const csa_params* p) {
+  return p && p->eps > 0.f && std::isfinite(p->eps) && p->delta > 0.f && p->delta < 1.f && p->r >= 1 &&
+         p->r <= 4 && p->measure >= 0 && p->measure <= 2 && p->J_override >= -1 && p->J_override <= kMaxJ;
+}
+
+struct Layout {
+  int J1;
+  int64_t pcap, nblk_max;
+  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, zero_end;
+  size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, s32, win, buckets, dpart, total;
+};
+
+bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
+  const int64_t B = s->B, Hq = s->Hq, Hkv = s->Hkv, D = s->d, G = Hq / Hkv;
+  L.pcap = s->n_max > kWindow ? s->n_max - kWindow : 1;
+  L.nblk_max = (s->n_max + kBlock - 1) / kBlock;
+  const int Jmax = p->J_override >= 0 ? p->J_override : grid_J(L.pcap, p->r);
+  if (Jmax > kMaxJ) return false;
+  L.J1 = Jmax + 1;
+  const int64_t BH = B * Hq, BG = B * Hkv, ACC = 2 * D + 8;
+  size_t o = 0;
+  L.status = o; o += up(64);
+  L.cmax = o; o += up((size_t)BH * 4 * 4);
+  L.jr_hist = o; o += up((size_t)BH * (L.J1 + 1) * 4);
+  L.ncand = o; o += up((size_t)BH * 4);
+  L.pre_hist = o; o += up((size_t)BH * L.J1 * 4 * 4);
+  L.acc = o; o += up((size_t)BH * L.J1 * ACC * 4);
+  L.bcnt = o; o += up((size_t)BG * L.J1 * 4);
+  L.bcons = o; o += up((size_t)BG * L.J1 * 4);
+  L.zero_end = o;
+  L.winstats = o; o += up((size_t)BH * (D + 4) * 4);
+  L.vmaxp = o; o += up((size_t)BG * 4);
+  L.state = o; o += up((size_t)BH * 4 * 4);
+  L.plan_start = o; o += up((size_t)BG * L.J1 * 4);
+  L.plan_end = o; o += up((size_t)BG * L.J1 * 4);
+  L.plan_off = o; o += up(((size_t)BG * L.J1 + 1) * 4);
+  L.ubar = o; o += up((size_t)BG * s->n_max * G * 4);
+  L.s32 = o; o += up((size_t)BG * L.pcap * G * 4);
+  L.win = o; o += up((size_t)BG * kWindow * G * 4);
+  L.buckets = o; o += up((size_t)BG * L.J1 * L.pcap * 4);
+  L.dpart = o; o += up((size_t)dense_nsplit(s->n_max) * BH * (D + 2) * 4);
+  L.total = o;
+  return true;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = v > 0 ? v : 148;
+  }
+  return cached[dev];
+}
+
+csa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace csa
+
+using namespace csa;
+
+extern "C" {
+
+const char* csa_status_string(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported shape (d must be 64 or 128, G in {1,2,4,8}, B <= 128)";
+    case CSA_ERR_CUDA: return "CUDA error";
+    case CSA_ERR_NONFINITE: return "non-finite value in q, K or the statistics";
+    case CSA_ERR_TIMEOUT: return "device wait timed out";
+    case CSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+size_t csa_workspace_size(const csa_shape* shape, const csa_params* params) {
+  if (!shape_ok(shape) || !params_ok(params) || shape_supported(shape) != CSA_OK) return 0;
+  Layout L;
+  if (!make_layout(shape, params, L)) return 0;
+  return L.total;
+}
+
+size_t csa_dense_workspace_size(const csa_shape* shape) {
+  if (!shape_ok(shape) || shape_supported(shape) != CSA_OK) return 0;
+  return up((size_t)dense_nsplit(shape->n_max) * shape->B * shape->Hq * (shape->d + 2) * 4);
+}
+
+csa_status csa_workspace_layout(const csa_shape* shape, const csa_params* params, csa_workspace_map* out) {
+  if (!out || !shape_ok(shape) || !params_ok(params)) return CSA_ERR_INVALID_ARG;
+  csa_status su = shape_supported(shape);
+  if (su != CSA_OK) return su;
+  Layout L;
+  if (!make_layout(shape, params, L)) return CSA_ERR_INVALID_ARG;
+  out->ubar = L.ubar;
+  out->cmax = L.cmax;
+  out->s32 = L.s32;
+  out->jr_hist = L.jr_hist;
+  out->total = L.total;
+  out->J1 = L.J1;
+  out->reserved = 0;
+  return CSA_OK;
+}
+
+csa_status csa_quantize_keys(const csa_shape* shape, const void* K, const void* V, const int64_t* len,
+                             int64_t from_token, uint8_t* K4, float* bounds, float* vmax, void* stream) {
+  if (!shape_ok(shape) || !K || !V || !len || !K4 || !bounds || !vmax || from_token < 0)
+    return CSA_ERR_INVALID_ARG;
+  csa_status su = shape_supported(shape);
+  if (su != CSA_OK) return su;
+  SeqArgs seq;
+  std::memset(&seq, 0, sizeof(seq));
+  int64_t nblocks = 0;
+  const int64_t blk_from = from_token / kBlock;
+  for (int b = 0; b < shape->B; ++b) {
+    if (len[b] < 0 || len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
+    seq.n[b] = len[b];
+    const int64_t nb = (len[b] + kBlock - 1) / kBlock - blk_from;
+    if (nb > nblocks) nblocks = nb;
+  }
+  QuantArgs a;
+  a.K = K; a.V = V; a.K4 = K4; a.bounds = bounds; a.vmax = vmax; a.Hkv = shape->Hkv;
+  a.n_max = shape->n_max; a.nblk_max = (shape->n_max + kBlock - 1) / kBlock; a.blk_from = blk_from;
+  return cuda_status(launch_quant(a, seq, shape->B, shape->d, shape->dtype == CSA_BF16, nblocks,
+                                  (cudaStream_t)stream));
+}
+
+csa_status csa_dense_decode(const csa_shape* shape, const void* q, const void* K, const void* V,
+                            const int64_t* len, float* o, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!shape_ok(shape) || !q || !K || !V || !len || !o) return CSA_ERR_INVALID_ARG;
+  csa_status su = shape_supported(shape);
+  if (su != CSA_OK) return su;
+  const size_t need = csa_dense_workspace_size(shape);
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace % kAlign)) return CSA_ERR_WORKSPACE;
+  SeqArgs seq;
+  std::memset(&seq, 0, sizeof(seq));
+  int64_t nlive = 0;
+  for (int b = 0; b < shape->B; ++b) {
+    if (len[b] < 1 || len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
+    seq.n[b] = len[b];
+    if (len[b] > nlive) nlive = len[b];
+  }
+  DenseArgs a;
+  a.q = q; a.K = K; a.V = V; a.part = (float*)workspace; a.o = o; a.state = nullptr;
+  a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max;
+  a.nsplit = dense_nsplit(shape->n_max); a.rs = (float)(1.0 / std::sqrt((double)shape->d));
+  return cuda_status(launch_dense(a, seq, shape->d, shape->Hq / shape->Hkv, shape->dtype == CSA_BF16, nlive,
+                                  (cudaStream_t)stream));
+}
+
+csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
+                           const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
+                           const int64_t* len, const uint64_t* step_seed, float* o, float* beta,
+                           int32_t* level, int32_t* keys_read, csa_head_stats* stats, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!shape_ok(shape) || !params_ok(params) || !q || !K || !V || !K4 || !bounds || !vmax || !len ||
+      !step_seed || !o || !beta || !level || !keys_read)
+    return CSA_ERR_INVALID_ARG;
+  csa_status su = shape_supported(shape);
+  if (su != CSA_OK) return su;
+  Layout L;
+  if (!make_layout(shape, params, L)) return CSA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace % kAlign)) return CSA_ERR_WORKSPACE;
+  const int G = shape->Hq / shape->Hkv;
+  const bool bf16 = shape->dtype == CSA_BF16;
+  SeqArgs seq;
+  std::memset(&seq, 0, sizeof(seq));
+  int64_t nlive = 0;
+  for (int b = 0; b < shape->B; ++b) {
+    if (len[b] < 1 || len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
+    seq.n[b] = len[b];
+    seq.seed[b] = step_seed[b];
+    const int64_t P = len[b] > kWindow ? len[b] - kWindow : 0;
+    seq.J[b] = params->J_override >= 0 ? params->J_override : grid_J(P, params->r);
+    if (len[b] > nlive) nlive = len[b];
+  }
+  const int64_t plive = nlive > kWindow ? nlive - kWindow : 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  const float rs = (float)(1.0 / std::sqrt((double)shape->d));
+
+  if (cudaMemsetAsync(ws, 0, L.zero_end, st) != cudaSuccess) return CSA_ERR_CUDA;
+
+  ScanArgs sa;
+  sa.q = q; sa.K4 = K4; sa.bounds = bounds; sa.ubar = (float*)(ws + L.ubar);
+  sa.cmax = (unsigned*)(ws + L.cmax); sa.status = (unsigned*)(ws + L.status);
+  sa.Hq = shape->Hq; sa.Hkv = shape->Hkv; sa.n_max = shape->n_max; sa.nblk_max = L.nblk_max; sa.rs = rs;
+  cudaError_t e = launch_scan(sa, seq, shape->B, shape->d, G, bf16, nlive, st);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+
+  SparseArgs a;
+  a.q = q; a.K = K; a.V = V; a.vmax = vmax; a.ubar = (const float*)(ws + L.ubar);
+  a.s32 = (float*)(ws + L.s32); a.win = (float*)(ws + L.win); a.cmax = (unsigned*)(ws + L.cmax);
+  a.jr_hist = (unsigned*)(ws + L.jr_hist); a.ncand = (unsigned*)(ws + L.ncand);
+  a.pre_hist = (float*)(ws + L.pre_hist); a.acc = (float*)(ws + L.acc); a.winstats = (float*)(ws + L.winstats);
+  a.vmaxp = (float*)(ws + L.vmaxp); a.state = (int*)(ws + L.state); a.bcnt = (unsigned*)(ws + L.bcnt);
+  a.bcons = (unsigned*)(ws + L.bcons); a.buckets = (unsigned*)(ws + L.buckets);
+  a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);
+  a.plan_off = (unsigned*)(ws + L.plan_off); a.status = (unsigned*)(ws + L.status);
+  a.o = o; a.beta = beta; a.level = level; a.keys_read = keys_read; a.stats = stats;
+  a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max; a.nblk_max = L.nblk_max;
+  a.pcap = L.pcap; a.J1 = L.J1; a.r = params->r; a.eps = params->eps; a.delta = params->delta;
+  a.measure = params->measure; a.rs = rs;
+
+  if (plive > 0) {
+    if (launch_cstar(a, seq, shape->d, G, bf16, nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
+    if (launch_rescore(a, seq, shape->d, G, bf16, plive, st) != cudaSuccess) return CSA_ERR_CUDA;
+  }
+  if (launch_predict(a, seq, shape->d, G, bf16, st) != cudaSuccess) return CSA_ERR_CUDA;
+  const int nsm = sm_count();
+  for (int round = 0; round < 3; ++round)
+    if (launch_round(a, seq, shape->d, G, bf16, plive > 0 ? plive : 1, round, nsm, st) != cudaSuccess)
+      return CSA_ERR_CUDA;
+  // exact attention for heads with no certified level and sequences without a pool
+  DenseArgs da;
+  da.q = q; da.K = K; da.V = V; da.part = (float*)(ws + L.dpart); da.o = o; da.state = a.state;
+  da.B = shape->B; da.Hq = shape->Hq; da.Hkv = shape->Hkv; da.n_max = shape->n_max;
+  da.nsplit = dense_nsplit(shape->n_max); da.rs = rs;
+  if (launch_dense(da, seq, shape->d, G, bf16, nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
+  if (stats && plive > 0)
+    if (launch_near(a, seq, G, plive, st) != cudaSuccess) return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+csa_status csa_check(void* workspace, void* stream) {
+  if (!workspace) return CSA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return CSA_ERR_CUDA;
+  unsigned w = 0;
+  if (cudaMemcpy(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  if (w & 1u) return CSA_ERR_NONFINITE;
+  if (w & 2u) return CSA_ERR_WORKSPACE;
+  return CSA_OK;
+}
+
+}  // extern "C"

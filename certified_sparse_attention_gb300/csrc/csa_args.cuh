@@ -1,0 +1,98 @@
+// Argument blocks of the kernels and the launch functions of each
+// translation unit (one definition, shared by the host layer).
+#pragma once
+
+#include "csa_internal.cuh"
+
+namespace csa {
+
+struct ScanArgs {
+  const void* q;
+  const uint8_t* K4;
+  const float* bounds;
+  float* ubar;          // [B*Hkv][n_max][G]
+  unsigned* cmax;       // [B*Hq][4] ordered floats: c_lo, c_hi, cb, c32
+  unsigned* status;
+  int Hq, Hkv;
+  int64_t n_max, nblk_max;
+  float rs;             // float32(1/sqrt d)
+};
+
+struct SparseArgs {
+  const void* q;
+  const void* K;
+  const void* V;
+  const float* vmax;      // [B*Hkv][nblk_max]
+  const float* ubar;      // [B*Hkv][n_max][G]
+  float* s32;             // [B*Hkv][pcap][G]     candidate scores (-inf: not a candidate)
+  float* win;             // [B*Hkv][64][G]       window scores
+  unsigned* cmax;         // [B*Hq][4]            c_lo, c_hi, cb, c32 (ordered)
+  unsigned* jr_hist;      // [B*Hq][J1+1]         first level a key's K row is needed
+  unsigned* ncand;        // [B*Hq]
+  float* pre_hist;        // [B*Hq][J1][4]        d k, d D_B, d sampled (value free)
+  float* acc;             // [B*Hq][J1][ACC]      d S1[D], d N_B[D], d k, d S2, d D_B, d H_B, d sampled
+  float* winstats;        // [B*Hq][D+4]          N_R[D], D_R, H_R
+  float* vmaxp;           // [B*Hkv]              max vmax over pool blocks
+  int* state;             // [B*Hq][4]            lo, hi, stop, flags
+  unsigned* bcnt;         // [B*Hkv][J1]
+  unsigned* bcons;        // [B*Hkv][J1]
+  unsigned* buckets;      // [B*Hkv][J1][pcap]
+  unsigned* plan_start;   // [B*Hkv*J1]
+  unsigned* plan_end;     // [B*Hkv*J1]
+  unsigned* plan_off;     // [B*Hkv*J1 + 1]
+  unsigned* status;
+  float* o;
+  float* beta;
+  int* level;
+  int* keys_read;
+  csa_head_stats* stats;
+  int B, Hq, Hkv;
+  int64_t n_max, nblk_max, pcap;
+  int J1;                 // level stride: largest J + 1
+  int r;
+  float eps, delta;
+  int measure;
+  float rs;               // float32(1/sqrt d)
+};
+
+struct DenseArgs {
+  const void* q;
+  const void* K;
+  const void* V;
+  float* part;            // [nsplit][B*Hq][D+2]: m, l, acc[D]
+  float* o;               // [B*Hq][D]
+  const int* state;       // optional [B*Hq][4]: only heads with flag bit 0
+  int B, Hq, Hkv;
+  int64_t n_max;
+  int nsplit;
+  float rs;
+};
+
+struct QuantArgs {
+  const void* K;
+  const void* V;
+  uint8_t* K4;
+  float* bounds;
+  float* vmax;
+  int Hkv;
+  int64_t n_max, nblk_max;
+  int64_t blk_from;
+};
+
+cudaError_t launch_scan(const ScanArgs&, const SeqArgs&, int B, int d, int G, bool bf16, int64_t nmax_live,
+                        cudaStream_t);
+cudaError_t launch_cstar(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t nmax_live,
+                         cudaStream_t);
+cudaError_t launch_rescore(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t pmax_live,
+                           cudaStream_t);
+cudaError_t launch_predict(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, cudaStream_t);
+cudaError_t launch_round(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t pmax_live,
+                         int round, int nsm, cudaStream_t);
+cudaError_t launch_near(const SparseArgs&, const SeqArgs&, int G, int64_t pmax_live, cudaStream_t);
+cudaError_t launch_dense(const DenseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t nmax_live,
+                         cudaStream_t);
+cudaError_t launch_quant(const QuantArgs&, const SeqArgs&, int B, int d, bool bf16, int64_t nblocks,
+                         cudaStream_t);
+int dense_nsplit(int64_t n_max);
+
+}  // namespace csa

@@ -1,0 +1,189 @@
+// Dense decode attention (picx.dev "Problem Setup": o = sum_i w_i v_i / sum_i
+// w_i, w_i = exp(s_i - c*)), float32 throughout.  It is the same-build
+// comparator of the sparse step, and the exact fallback of the sparse step
+// for heads with no certified level (and for sequences with no pool).
+//
+// Split-K over the keys: a CTA takes 1024 keys of one (sequence, KV head)
+// for all G query heads; each warp scores eight K rows at a time (one row
+// load serves the G heads; lane-local products then an eight-row shuffle
+// reduction), keeps an online-softmax state per head and accumulates the
+// eight V rows.  A second kernel merges the splits.
+#include "csa_args.cuh"
+
+namespace csa {
+
+constexpr int kDenseChunk = 1024;
+
+template <int D, typename E>
+__device__ __forceinline__ void dload_row(const E* row, float* v) {
+  constexpr int CPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  if (CPL == 4) {
+    float4 f = Elem<E>::get4(row + lane * 4);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  } else {
+    float2 f = Elem<E>::get2(row + lane * 2);
+    v[0] = f.x; v[1] = f.y;
+  }
+}
+
+__device__ __forceinline__ bool group_wanted(const DenseArgs& a, int b, int g, int G) {
+  if (!a.state) return true;
+  for (int h = 0; h < G; ++h)
+    if (a.state[((int64_t)b * a.Hq + g * G + h) * 4 + 3] & 1) return true;
+  return false;
+}
+
+template <int D, int G, typename E>
+__global__ void __launch_bounds__(256) dense_split_kernel(const DenseArgs a, const __grid_constant__ SeqArgs seq) {
+  constexpr int CPL = D / 32;
+  __shared__ float s_m[8][G], s_l[8][G];
+  __shared__ float s_acc[8][G][D];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int64_t n = seq.n[b];
+  const int64_t start = (int64_t)blockIdx.x * kDenseChunk;
+  if (start >= n) return;
+  if (!group_wanted(a, b, g, G)) return;
+  const int64_t end = min(n, start + kDenseChunk);
+  float qv[G][CPL];
+  const E* qp = reinterpret_cast<const E*>(a.q) + ((int64_t)b * a.Hq + (int64_t)g * G) * D;
+#pragma unroll
+  for (int h = 0; h < G; ++h) dload_row<D, E>(qp + (int64_t)h * D, qv[h]);
+  float m[G], l[G], acc[G][CPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY; l[h] = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[h][c] = 0.f;
+  }
+  const E* Kb = reinterpret_cast<const E*>(a.K) + (int64_t)bg * a.n_max * D;
+  const E* Vb = reinterpret_cast<const E*>(a.V) + (int64_t)bg * a.n_max * D;
+  for (int64_t k0 = start + w * 8; k0 < end; k0 += 64) {
+    float kv[8][CPL], vv[8][CPL];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (k0 + r < end) {
+        dload_row<D, E>(Kb + (k0 + r) * D, kv[r]);
+        dload_row<D, E>(Vb + (k0 + r) * D, vv[r]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) { kv[r][c] = 0.f; vv[r][c] = 0.f; }
+      }
+    }
+    const bool valid = k0 + (lane & 7) < end;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float part[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        float p[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) p[c] = kv[r][c] * qv[h][c];
+        part[r] = local_tree<CPL>(p);
+      }
+      float s = reduce8_rows(part) * a.rs;
+      if (!valid) s = -INFINITY;
+      float m8 = s;
+      m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 1));
+      m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 2));
+      m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 4));
+      const float mn = fmaxf(m[h], m8);
+      const float sc = expf(m[h] - mn);
+      const float p = expf(s - mn);
+      float ps = p;
+      ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+      ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+      l[h] = l[h] * sc + ps;
+      m[h] = mn;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[h][c] *= sc;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float pr = __shfl_sync(0xffffffffu, p, r);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) acc[h][c] += pr * vv[r][c];
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    if (lane == 0) { s_m[w][h] = m[h]; s_l[w][h] = l[h]; }
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) s_acc[w][h][lane * CPL + c] = acc[h][c];
+  }
+  __syncthreads();
+  for (int i = tid; i < G * (D + 2); i += 256) {
+    const int h = i / (D + 2), c = i - h * (D + 2);
+    float M = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) M = fmaxf(M, s_m[x][h]);
+    float v = 0.f;
+    if (c == 0) v = M;
+    else {
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const float e = s_m[x][h] > -INFINITY ? expf(s_m[x][h] - M) : 0.f;
+        v += e * (c == 1 ? s_l[x][h] : s_acc[x][h][c - 2]);
+      }
+    }
+    a.part[((int64_t)blockIdx.x * a.B * a.Hq + (int64_t)b * a.Hq + g * G + h) * (D + 2) + c] = v;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) dense_combine_kernel(const DenseArgs a, const __grid_constant__ SeqArgs seq) {
+  const int bh = blockIdx.x;
+  const int b = bh / a.Hq;
+  if (a.state && !(a.state[(int64_t)bh * 4 + 3] & 1)) return;
+  const int64_t n = seq.n[b];
+  const int ns = (int)((n + kDenseChunk - 1) / kDenseChunk);
+  const int64_t stride = (int64_t)a.B * a.Hq * (D + 2);
+  const float* p = a.part + (int64_t)bh * (D + 2);
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, p[s * stride]);
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float num = 0.f, den = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float e = expf(p[s * stride] - M);
+      den += e * p[s * stride + 1];
+      num += e * p[s * stride + 2 + c];
+    }
+    a.o[(int64_t)bh * D + c] = num / den;
+  }
+}
+
+#define CSA_DENSE_SWITCH(FN, ...)                                                                \
+  switch (d * 100 + G * 10 + (bf16 ? 1 : 0)) {                                                   \
+    case 12811: FN<128, 1, __nv_bfloat16> __VA_ARGS__; break;                                    \
+    case 12821: FN<128, 2, __nv_bfloat16> __VA_ARGS__; break;                                    \
+    case 12841: FN<128, 4, __nv_bfloat16> __VA_ARGS__; break;                                    \
+    case 12881: FN<128, 8, __nv_bfloat16> __VA_ARGS__; break;                                    \
+    case 12810: FN<128, 1, float> __VA_ARGS__; break;                                            \
+    case 12820: FN<128, 2, float> __VA_ARGS__; break;                                            \
+    case 12840: FN<128, 4, float> __VA_ARGS__; break;                                            \
+    case 12880: FN<128, 8, float> __VA_ARGS__; break;                                            \
+    case 6411: FN<64, 1, __nv_bfloat16> __VA_ARGS__; break;                                      \
+    case 6421: FN<64, 2, __nv_bfloat16> __VA_ARGS__; break;                                      \
+    case 6441: FN<64, 4, __nv_bfloat16> __VA_ARGS__; break;                                      \
+    case 6481: FN<64, 8, __nv_bfloat16> __VA_ARGS__; break;                                      \
+    case 6410: FN<64, 1, float> __VA_ARGS__; break;                                              \
+    case 6420: FN<64, 2, float> __VA_ARGS__; break;                                              \
+    case 6440: FN<64, 4, float> __VA_ARGS__; break;                                              \
+    case 6480: FN<64, 8, float> __VA_ARGS__; break;                                              \
+    default: return cudaErrorInvalidValue;                                                       \
+  }
+
+int dense_nsplit(int64_t n_max) { return (int)((n_max + kDenseChunk - 1) / kDenseChunk); }
+
+cudaError_t launch_dense(const DenseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t nmax_live,
+                         cudaStream_t st) {
+  dim3 grid((unsigned)((nmax_live + kDenseChunk - 1) / kDenseChunk), (unsigned)(a.B * a.Hkv));
+  CSA_DENSE_SWITCH(dense_split_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  if (d == 128) dense_combine_kernel<128><<<a.B * a.Hq, 128, 0, st>>>(a, seq);
+  else dense_combine_kernel<64><<<a.B * a.Hq, 128, 0, st>>>(a, seq);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,289 @@
+// 4-bit key scan with deterministic score bounds, shared by a GQA group.
+//
+// picx.dev summary, "Algorithm Components" 4: a 4-bit per-block per-channel
+// quantisation gives deterministic upper bounds u_i >= s_i for every score;
+// readsearch.ai "Abstract": the scan is shared across the GQA group and reads
+// every key.  One CTA scans a tile of 256 keys (four 64-token blocks) of one
+// (sequence, KV head) for all G query heads:
+//   1. the packed codes (256 x d/2 bytes) and the four blocks' (m_c, Delta_c)
+//      are staged in shared memory with cp.async;
+//   2. per (block, head) the query is coded to int8 with a residual and a
+//      key-rounding slack (16 threads per (block, head), adjacent-pair float32
+//      trees over the channels);
+//   3. per key, int8 x u4 dot products (dp4a: low nibbles as bytes, high
+//      nibbles as 16 x byte) give the exact integer I, and
+//      ubar = fl(fl(alpha I) + b_hi), l = fl(fl(alpha I) + b_lo);
+//   4. ubar is stored key-major with the G heads interleaved, and the per-head
+//      maxima of l (c*_lo) and ubar are folded into global atomics.
+#include "csa_args.cuh"
+
+namespace csa {
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  int src = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+__device__ __forceinline__ int dp4a_us(unsigned a, unsigned b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Adjacent-pair tree over the CPT values a thread holds, then over 16 lanes.
+template <int CPT>
+__device__ __forceinline__ float tree16(const float* v) {
+  float s;
+  if (CPT == 8) {
+    s = fadd(fadd(fadd(v[0], v[1]), fadd(v[2], v[3])), fadd(fadd(v[4], v[5]), fadd(v[6], v[7])));
+  } else {
+    s = fadd(fadd(v[0], v[1]), fadd(v[2], v[3]));
+  }
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) s = fadd(s, __shfl_xor_sync(0xffffffffu, s, o));
+  return s;
+}
+
+template <int D, int G, typename E>
+__global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq) {
+  constexpr int CPT = D / 16;        // channels per prep thread
+  constexpr int ROWB = D / 2;        // bytes of codes per key
+  constexpr int CHR = ROWB / 16;     // 16-byte chunks per key
+  constexpr int WE = D / 8;          // even (and odd) code words per key
+  __shared__ __align__(16) uint8_t s_codes[kTile * ROWB];
+  __shared__ __align__(16) float s_bnd[4][2][D];
+  __shared__ __align__(16) float s_qt[G][D];
+  __shared__ __align__(16) unsigned s_atw[4][G][2 * WE];
+  __shared__ float s_q1[G];
+  __shared__ float s_alpha[4][G], s_bhi[4][G], s_blo[4][G];
+  __shared__ float s_red[8][G][2];
+
+  const int tid = threadIdx.x;
+  const int bg = blockIdx.y;
+  const int b = bg / a.Hkv;
+  const int g = bg - b * a.Hkv;
+  const int64_t n = seq.n[b];
+  const int64_t key0 = (int64_t)blockIdx.x * kTile;
+  if (key0 >= n) return;
+  const int64_t nblk_n = (n + kBlock - 1) / kBlock;
+
+  // 1. stage codes and block bounds
+  {
+    const uint8_t* src = a.K4 + ((int64_t)bg * a.nblk_max * kBlock + key0) * ROWB;
+    const int64_t rows_valid = nblk_n * kBlock - key0;
+#pragma unroll
+    for (int c = tid; c < kTile * CHR; c += 256) {
+      int row = c / CHR;
+      bool ok = row < rows_valid;
+      cp_async16(s_codes + c * 16, ok ? src + (int64_t)c * 16 : a.K4, ok);
+    }
+    cp_async_commit();
+    const int64_t blk0 = key0 / kBlock;
+    const float* bsrc = a.bounds + ((int64_t)bg * a.nblk_max + blk0) * 2 * D;
+    for (int c = tid; c < 4 * 2 * D / 4; c += 256) {
+      int blk = c / (2 * D / 4);
+      bool ok = blk0 + blk < nblk_n;
+      cp_async16(reinterpret_cast<float*>(s_bnd) + c * 4, ok ? bsrc + (int64_t)c * 4 : a.bounds, ok);
+    }
+    cp_async_commit();
+  }
+  // query (scaled by 1/sqrt d) for the group's G heads
+  {
+    const E* qp = reinterpret_cast<const E*>(a.q) + ((int64_t)b * a.Hq + (int64_t)g * G) * D;
+    bool bad = false;
+    for (int i = tid; i < G * D; i += 256) {
+      float v = Elem<E>::get(qp, i);
+      bad |= !isfinite(v);
+      s_qt[i / D][i % D] = fmul(v, a.rs);
+    }
+    if (bad) atomicOr(a.status, 1u);
+  }
+  __syncthreads();
+  {
+    const int w = tid >> 5, lane = tid & 31;
+    if (w < G) {
+      constexpr int CPL = D / 32;
+      float p[CPL];
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) p[k] = fabsf(s_qt[w][lane * CPL + k]);
+      float s = local_tree<CPL>(p);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) s = fadd(s, __shfl_xor_sync(0xffffffffu, s, o));
+      if (lane == 0) s_q1[w] = s;
+    }
+  }
+  cp_async_wait<1>();
+  __syncthreads();
+
+  // 2. per (block, head) query code
+  for (int u = tid >> 4; u < 4 * G; u += 16) {
+    const int blk = u / G, h = u - blk * G;
+    const int l16 = tid & 15;
+    const int c0 = l16 * CPT;
+    float av[CPT], mv[CPT];
+    float amax = 0.f, kabs = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+      float dl = s_bnd[blk][1][c0 + k];
+      mv[k] = s_bnd[blk][0][c0 + k];
+      av[k] = fmul(s_qt[h][c0 + k], dl);
+      amax = fmaxf(amax, fabsf(av[k]));
+      kabs = fmaxf(kabs, fadd(fabsf(mv[k]), fmul(16.0f, dl)));
+    }
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      kabs = fmaxf(kabs, __shfl_xor_sync(0xffffffffu, kabs, o));
+    }
+    float alpha = 0.f, inv = 0.f;
+    if (amax > 0.f) {
+      alpha = fdiv(amax, 127.0f);
+      inv = fdiv(127.0f, amax);
+    }
+    float tb[CPT], ta[CPT], tp[CPT], tn[CPT];
+    int at[CPT];
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+      float x = rintf(fmul(av[k], inv));
+      x = fminf(fmaxf(x, -127.0f), 127.0f);
+      at[k] = (int)x;
+      float r = fsub(av[k], fmul(alpha, x));
+      tb[k] = fmul(s_qt[h][c0 + k], mv[k]);
+      ta[k] = fabsf(av[k]);
+      tp[k] = fmaxf(r, 0.0f);
+      tn[k] = fmaxf(-r, 0.0f);
+    }
+    float Bq = tree16<CPT>(tb);
+    float A1 = tree16<CPT>(ta);
+    float Rp = tree16<CPT>(tp);
+    float Rn = tree16<CPT>(tn);
+    if (l16 == 0) {
+      float sk = fmul(A1, 0.5000152587890625f);
+      float hi = fadd(sk, fmul(15.0f, Rp));
+      float lo = fadd(sk, fmul(15.0f, Rn));
+      float mag = fadd(fadd(fmul(s_q1[h], kabs), hi), lo);
+      float marg = fmul(mag, 6.103515625e-05f);      // 2^-14
+      float bhi = fadd(fadd(Bq, hi), marg);
+      float blo = fsub(fsub(Bq, lo), marg);
+      s_alpha[blk][h] = alpha;
+      s_bhi[blk][h] = bhi;
+      s_blo[blk][h] = blo;
+      if (!isfinite(bhi) || !isfinite(blo) || !isfinite(alpha)) atomicOr(a.status, 1u);
+    }
+    // pack the code: word w covers channels 8w..8w+7; even word = channels
+    // 8w, 8w+2, 8w+4, 8w+6 (bytes 0..3), odd word = 8w+1, ..., 8w+7
+    if (CPT == 8) {
+      unsigned ev = (at[0] & 0xFF) | ((at[2] & 0xFF) << 8) | ((at[4] & 0xFF) << 16) | ((unsigned)(at[6] & 0xFF) << 24);
+      unsigned od = (at[1] & 0xFF) | ((at[3] & 0xFF) << 8) | ((at[5] & 0xFF) << 16) | ((unsigned)(at[7] & 0xFF) << 24);
+      s_atw[blk][h][l16] = ev;
+      s_atw[blk][h][WE + l16] = od;
+    } else {
+      unsigned short ev = (unsigned short)((at[0] & 0xFF) | ((at[2] & 0xFF) << 8));
+      unsigned short od = (unsigned short)((at[1] & 0xFF) | ((at[3] & 0xFF) << 8));
+      reinterpret_cast<unsigned short*>(&s_atw[blk][h][0])[l16] = ev;
+      reinterpret_cast<unsigned short*>(&s_atw[blk][h][WE])[l16] = od;
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // 3. bounds per key
+  const int64_t key = key0 + tid;
+  const bool live = key < n;
+  const int blk = tid >> 6;
+  float lmax[G], umax[G];
+  int ae[G], ao[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) { ae[h] = 0; ao[h] = 0; }
+  if (live) {
+    const uint4* row = reinterpret_cast<const uint4*>(s_codes + tid * ROWB);
+    const int rot = (CHR == 4) ? (tid >> 1) : (tid >> 2);
+#pragma unroll
+    for (int j = 0; j < CHR; ++j) {
+      const int jj = (j + rot) & (CHR - 1);
+      uint4 w = row[jj];
+      unsigned ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        uint4 e4 = *reinterpret_cast<const uint4*>(&s_atw[blk][h][4 * jj]);
+        uint4 o4 = *reinterpret_cast<const uint4*>(&s_atw[blk][h][WE + 4 * jj]);
+        unsigned es[4] = {e4.x, e4.y, e4.z, e4.w};
+        unsigned os[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ae[h] = dp4a_us(ws[e] & 0x0F0F0F0Fu, es[e], ae[h]);
+          ao[h] = dp4a_us(ws[e] & 0xF0F0F0F0u, os[e], ao[h]);
+        }
+      }
+    }
+  }
+  float ub[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    int I = ae[h] + (ao[h] >> 4);
+    float aI = fmul(s_alpha[blk][h], (float)I);
+    ub[h] = fadd(aI, s_bhi[blk][h]);
+    float lo = fadd(aI, s_blo[blk][h]);
+    umax[h] = live ? ub[h] : -INFINITY;
+    lmax[h] = live ? lo : -INFINITY;
+  }
+  if (live) {
+    float* dst = a.ubar + ((int64_t)bg * a.n_max + key) * G;
+    if (G == 4) {
+      *reinterpret_cast<float4*>(dst) = make_float4(ub[0], ub[1], ub[2], ub[3]);
+    } else if (G == 8) {
+      reinterpret_cast<float4*>(dst)[0] = make_float4(ub[0], ub[1], ub[2], ub[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(ub[4 % G], ub[5 % G], ub[6 % G], ub[7 % G]);
+    } else if (G == 2) {
+      *reinterpret_cast<float2*>(dst) = make_float2(ub[0], ub[1 % G]);
+    } else {
+      dst[0] = ub[0];
+    }
+  }
+  // 4. per-head maxima
+  const int w = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float x = lmax[h], y = umax[h];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+      y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, o));
+    }
+    if (lane == 0) { s_red[w][h][0] = x; s_red[w][h][1] = y; }
+  }
+  __syncthreads();
+  if (tid < G) {
+    float x = -INFINITY, y = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { x = fmaxf(x, s_red[i][tid][0]); y = fmaxf(y, s_red[i][tid][1]); }
+    unsigned* slot = a.cmax + ((int64_t)b * a.Hq + (int64_t)g * G + tid) * 4;
+    if (x > -INFINITY) atomic_max_f(slot + 0, x);
+    if (y > -INFINITY) atomic_max_f(slot + 1, y);
+  }
+}
+
+template <int D, int G, typename E>
+cudaError_t launch_scan_t(const ScanArgs& a, const SeqArgs& seq, int B, int64_t nmax_live, cudaStream_t st) {
+  dim3 grid((unsigned)((nmax_live + kTile - 1) / kTile), (unsigned)(B * a.Hkv));
+  scan_kernel<D, G, E><<<grid, 256, 0, st>>>(a, seq);
+  return cudaGetLastError();
+}
+
+#define CSA_SCAN_CASE(DD, GG)                                                          \
+  if (d == DD && G == GG)                                                              \
+    return bf16 ? launch_scan_t<DD, GG, __nv_bfloat16>(a, seq, B, nmax_live, st)       \
+                : launch_scan_t<DD, GG, float>(a, seq, B, nmax_live, st);
+
+cudaError_t launch_scan(const ScanArgs& a, const SeqArgs& seq, int B, int d, int G, bool bf16,
+                        int64_t nmax_live, cudaStream_t st) {
+  CSA_SCAN_CASE(128, 1) CSA_SCAN_CASE(128, 2) CSA_SCAN_CASE(128, 4) CSA_SCAN_CASE(128, 8)
+  CSA_SCAN_CASE(64, 1) CSA_SCAN_CASE(64, 2) CSA_SCAN_CASE(64, 4) CSA_SCAN_CASE(64, 8)
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace csa

@@ -1,0 +1,186 @@
+/*
+ * csa.h -- certified sparse decode attention on GB300 (sm_103a), C ABI.
+ *
+ * The operation is the decode-attention step of "Certified Sparse Attention
+ * via Perturbed Retrieval" (arXiv 2610.24991): picx.dev summary,
+ * "Methodology / Problem Setup" (scores s_i = q.k_i / sqrt(d), c* = max s_i,
+ * w_i = exp(s_i - c*), o = sum w_i v_i / sum w_i) and "Algorithm Components"
+ * 1-4 (window of the last 64 tokens read exactly; perturbations
+ * E_i = -ln u_i from a 53-bit hash; threshold sample
+ * S(tau) = {i in pool : s_i - c* + E_i >= log tau}; Horvitz-Thompson
+ * estimates on the grid tau_j = 2^(-j/r); Chernoff / Hilbert-space Bernstein
+ * certificate beta; stop at the first certified level; 4-bit scan with
+ * deterministic bounds shared across the GQA group), and the readsearch.ai
+ * abstract page ("fresh perturbations at every decoding step").
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device memory are device pointers owned by the
+ *    caller; the library allocates no device memory at all.  Scratch space
+ *    is the caller's `workspace` buffer (size from csa_workspace_size /
+ *    csa_dense_workspace_size).
+ *  - Host arrays (len, step_seed) are read before the call returns.
+ *  - Work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
+ *    stream); outputs are valid once the stream has synchronised.  The call
+ *    never synchronises the stream, so a decode step can be captured into a
+ *    CUDA graph (the host arrays are copied into kernel arguments).
+ *  - Argument errors return CSA_ERR_INVALID_ARG / CSA_ERR_UNSUPPORTED before
+ *    anything is enqueued.  Launch failures return CSA_ERR_CUDA.  Errors
+ *    found on the device (non-finite inputs, an exhausted buffer) are
+ *    recorded in a status word inside the workspace; csa_check reads it.
+ *  - Nothing throws across the ABI.
+ *
+ * Memory layouts (row-major, contiguous):
+ *   q      [B][Hq][d]                      element type `dtype`
+ *   K, V   [B][Hkv][n_max][d]              element type `dtype`
+ *   K4     [B][Hkv][nblk_max * 64][d/2]    uint8, two 4-bit codes per byte,
+ *                                          even channel in the low nibble
+ *   bounds [B][Hkv][nblk_max][2][d]        float: per block and channel the
+ *                                          minimum m_c, then the step Delta_c
+ *   vmax   [B][Hkv][nblk_max]              float: per-block bound on ||v_i||
+ *   o      [B][Hq][d] float;  beta, level, keys_read: [B][Hq]
+ * with nblk_max = ceil(n_max / 64).  Query head h uses KV head h / (Hq/Hkv).
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size or parameter          */
+  CSA_ERR_UNSUPPORTED = 2,   /* valid but not built: d, G or B out of range  */
+  CSA_ERR_CUDA = 3,          /* a CUDA call or launch failed                  */
+  CSA_ERR_NONFINITE = 4,     /* NaN/Inf met in q, K or the statistics         */
+  CSA_ERR_TIMEOUT = 5,       /* reserved: a bounded device wait gave up       */
+  CSA_ERR_WORKSPACE = 6      /* workspace missing or too small               */
+} csa_status;
+
+typedef enum { CSA_BF16 = 0, CSA_F32 = 1 } csa_dtype;
+
+/* Error measure that stops a head (picx.dev "Problem Setup"):
+ *  VALUE  ||o_hat - o|| <= eps * M,  M^2 = sum_i a_i ||v_i||^2  (default)
+ *  OUTPUT ||o_hat - o|| <= eps * ||o||
+ *  DENOM  |D_hat - D|   <= eps * D                                          */
+typedef enum {
+  CSA_MEASURE_VALUE = 0, CSA_MEASURE_OUTPUT = 1, CSA_MEASURE_DENOM = 2
+} csa_measure;
+
+typedef struct {
+  int B;          /* sequences, 1..128                                       */
+  int Hq;         /* query heads                                             */
+  int Hkv;        /* KV heads; G = Hq / Hkv in {1, 2, 4, 8}                  */
+  int d;          /* head dimension, 64 or 128                               */
+  int64_t n_max;  /* token capacity of K, V, K4 per (sequence, KV head)      */
+  csa_dtype dtype;/* element type of q, K, V                                 */
+} csa_shape;
+
+typedef struct {
+  float eps;      /* target error, > 0                                      */
+  float delta;    /* failure probability per (sequence, query head), (0,1)  */
+  int r;          /* grid resolution tau_j = 2^(-j/r), 1..4                  */
+  int measure;    /* csa_measure                                             */
+  int J_override; /* -1: last level J = ceil(r log2 |pool|); else J (<= 255) */
+} csa_params;
+
+/* Optional per-(sequence, query head) diagnostics. */
+typedef struct {
+  int32_t level;            /* stop level j*, J+1 after the exact fallback  */
+  int32_t keys_read;        /* 64 + |exact-max set U candidates jbar <= j*| */
+  int32_t values_read;      /* 64 + |S(tau_j*)|                             */
+  int32_t n_candidates;     /* pool keys with bound level jbar <= J         */
+  int32_t n_near_threshold; /* keys within 1e-5 nats of a threshold at j*   */
+  int32_t J;                /* last grid level of this sequence             */
+  int32_t rounds;           /* gather rounds the head needed (1..3)         */
+  int32_t reserved;
+} csa_head_stats;
+
+/* Bytes of workspace csa_decode_step needs for this shape and parameters.
+ * Returns 0 when the arguments are invalid. */
+size_t csa_workspace_size(const csa_shape* shape, const csa_params* params);
+
+/* 4-bit key quantiser and value-norm metadata (picx.dev "Algorithm
+ * Components" 4: 4-bit per-block per-channel codes as in KIVI).
+ * Rebuilds every 64-token block that holds a token at position
+ * >= from_token and < len[b]: codes, (m_c, Delta_c) and vmax.  In decode,
+ * from_token = the position of the token just appended (one block).
+ *   K, V   device, layout above;  len host [B], 0 <= len[b] <= n_max
+ *   K4, bounds, vmax: device outputs, layout above.
+ * Positions >= len[b] inside a rebuilt block get code 0. */
+csa_status csa_quantize_keys(const csa_shape* shape, const void* K,
+                             const void* V, const int64_t* len,
+                             int64_t from_token, uint8_t* K4, float* bounds,
+                             float* vmax, void* stream);
+
+/* One certified sparse decode-attention step for every (sequence, query
+ * head).  Inputs: q, K, V, K4, bounds, vmax (device, layout above; K4,
+ * bounds and vmax must describe the first len[b] tokens, see
+ * csa_quantize_keys), len host [B] (1 <= len[b] <= n_max), step_seed host
+ * [B] (fresh every step; the caller mixes in the layer).  Outputs (device):
+ *   o          [B][Hq][d]  o_hat at the stop level (exact o after fallback)
+ *   beta       [B][Hq]     certified bound on ||o_hat - o|| (0 after the
+ *                          exact fallback or when len <= 64)
+ *   level      [B][Hq]     stop level j*; J+1 after the exact fallback
+ *   keys_read  [B][Hq]     see csa_head_stats
+ *   stats      [B][Hq]     optional (NULL to skip)
+ * workspace: device buffer of at least csa_workspace_size bytes, 256-byte
+ * aligned; its contents on entry do not matter. */
+csa_status csa_decode_step(const csa_shape* shape, const csa_params* params,
+                           const void* q, const void* K, const void* V,
+                           const uint8_t* K4, const float* bounds,
+                           const float* vmax, const int64_t* len,
+                           const uint64_t* step_seed, float* o, float* beta,
+                           int32_t* level, int32_t* keys_read,
+                           csa_head_stats* stats, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace csa_dense_decode needs. */
+size_t csa_dense_workspace_size(const csa_shape* shape);
+
+/* Dense decode attention (the same-build comparator, and the exact formula
+ * of picx.dev "Problem Setup"): o = softmax(q K^T / sqrt d) V over the first
+ * len[b] tokens, float32 accumulation.  q, K, V device; len host [B];
+ * o device [B][Hq][d] float. */
+csa_status csa_dense_decode(const csa_shape* shape, const void* q,
+                            const void* K, const void* V, const int64_t* len,
+                            float* o, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* Where csa_decode_step keeps its intermediate arrays inside the workspace
+ * (byte offsets), for diagnostics and parity tests.  Valid after the step's
+ * stream has synchronised, until the workspace is reused.
+ *   ubar     float [B][Hkv][n_max][G]   4-bit upper bounds of every key
+ *   cmax     uint32 [B][Hq][4]          c*_lo, c*_hi, cb, c32 as ordered
+ *            integers (u >= 2^31: float bits u - 2^31; else bits ~u)
+ *   s32      float [B][Hkv][n_max-64][G] float32 score of each candidate
+ *            pool key for each head, -inf where it is not a candidate
+ *   jr_hist  uint32 [B][Hq][J+2]        first level at which the key's bf16
+ *            row is needed (exact-max set: level 0), J+1 = never
+ *   J1       largest J + 1 (row stride of jr_hist is J1 + 1) */
+typedef struct {
+  size_t ubar, cmax, s32, jr_hist, total;
+  int32_t J1, reserved;
+} csa_workspace_map;
+
+csa_status csa_workspace_layout(const csa_shape* shape,
+                                const csa_params* params,
+                                csa_workspace_map* out);
+
+/* Synchronises `stream`, then returns the device status word recorded in
+ * `workspace` by the last csa_decode_step that used it (CSA_OK, or
+ * CSA_ERR_NONFINITE / CSA_ERR_WORKSPACE), or CSA_ERR_CUDA if the stream
+ * reports an error. */
+csa_status csa_check(void* workspace, void* stream);
+
+/* Static English description of a status code. */
+const char* csa_status_string(csa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */

@@ -1,0 +1,98 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/csa.h declares; host-side argument checks (no GPU work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import certified_sparse_attention_gb300 as csa
+from tests.gpu_common import ensure_built
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "csa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ensure_built()
+
+
+def test_every_declared_symbol_exported(lib):
+    names = _declared()
+    assert "csa_decode_step" in names and "csa_quantize_keys" in names
+    for nm in names:
+        assert hasattr(lib, nm), nm
+    assert set(csa.EXPORTED) == set(names)
+
+
+def test_workspace_sizes(lib):
+    s = csa.make_shape(4, 32, 8, 128, 131072, "bf16")
+    p = csa.make_params(0.05, 0.05, 4)
+    ws = csa.csa_workspace_size(s, p)
+    m = csa.csa_workspace_layout(s, p)
+    assert ws == m.total and ws > 0
+    assert m.J1 == 69                   # J = ceil(4 log2 131008) = 68
+    assert m.ubar % 256 == 0 and m.s32 % 256 == 0
+    assert csa.csa_dense_workspace_size(s) > 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(d=96), dict(Hq=12, Hkv=8), dict(Hq=48, Hkv=3), dict(B=129)])
+def test_unsupported_shapes(lib, bad):
+    kw = dict(B=1, Hq=32, Hkv=8, d=128, n_max=4096, dtype="bf16")
+    kw.update(bad)
+    s = csa.make_shape(**kw)
+    assert csa.csa_workspace_size(s, csa.make_params()) == 0
+
+
+@pytest.mark.parametrize("pk", [dict(eps=0.0), dict(delta=1.0),
+                                dict(delta=0.0), dict(r=0), dict(r=5),
+                                dict(measure=3), dict(J_override=300)])
+def test_invalid_params(lib, pk):
+    s = csa.make_shape(1, 8, 2, 128, 4096, "bf16")
+    kw = dict(eps=0.05, delta=0.05, r=2)
+    kw.update(pk)
+    assert csa.csa_workspace_size(s, csa.make_params(**kw)) == 0
+
+
+def test_decode_rejects_bad_arguments_before_launch(lib):
+    s = csa.make_shape(1, 8, 2, 128, 4096, "bf16")
+    p = csa.make_params()
+    # null inputs, bad lengths, missing workspace: rejected on the host,
+    # nothing is launched (these calls run without a GPU)
+    st = lib.csa_decode_step(ctypes.byref(s), ctypes.byref(p), None, None,
+                             None, None, None, None,
+                             (ctypes.c_int64 * 1)(100),
+                             (ctypes.c_uint64 * 1)(1), None, None, None,
+                             None, None, None, 0, None)
+    assert st == 1
+    fake = 256
+    st = lib.csa_decode_step(ctypes.byref(s), ctypes.byref(p), fake, fake,
+                             fake, fake, fake, fake,
+                             (ctypes.c_int64 * 1)(5000),
+                             (ctypes.c_uint64 * 1)(1), fake, fake, fake,
+                             fake, None, fake, 1 << 30, None)
+    assert st == 1                       # len > n_max
+    st = lib.csa_decode_step(ctypes.byref(s), ctypes.byref(p), fake, fake,
+                             fake, fake, fake, fake,
+                             (ctypes.c_int64 * 1)(100),
+                             (ctypes.c_uint64 * 1)(1), fake, fake, fake,
+                             fake, None, fake, 16, None)
+    assert st == 6                       # workspace too small
+    assert csa.status_string(6).startswith("workspace")
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(csa.CsaLibraryMissing):
+        csa._lib_save = csa._lib
+        csa._lib = None
+        try:
+            csa.load_library(str(tmp_path / "nope.so"))
+        finally:
+            csa._lib = csa._lib_save

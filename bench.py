@@ -1,0 +1,490 @@
+#!/usr/bin/env python
+"""Benchmark of certified sparse decode attention on GB300.
+
+One step = the certified sparse decode-attention step of one layer for the
+whole batch: B = 4 sequences at n = 131072 tokens, 32 query heads / 8 KV
+heads, d = 128, bf16 KV cache, eps = 0.05, delta = 0.05, r = 4 (the 128K
+headline workload).  Timed steps rotate over several independently seeded
+layers resident in HBM, so the working set is far larger than L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  N > 1 runs under torch.distributed (one process per
+GPU); every rank decodes its own batch (weak scaling, no collective on the
+data path), the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import threading  # noqa: E402
+import time  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "certified sparse decode-attn µs/step & HBM GB/s (% roofline) at 128K ctx"
+WORKLOAD = "llama128k_b4"
+
+
+# --------------------------------------------------------------- host logic
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def rank_layers(rank: int, world: int, layers: int):
+    """Layer ids (generator seeds) decoded by a rank: disjoint per rank."""
+    return [rank * 1000 + i for i in range(layers)]
+
+
+def step_plan(rank: int, steps: int, layers: int):
+    """(layer slot, step index) of every timed step of a rank."""
+    return [(s % layers, s) for s in range(steps)]
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def algorithmic_bytes(stats, w, n):
+    """Bytes the method must move per step (per (sequence, KV head)):
+    scan |P| (d/2 + 8d/64 + 4/64) over the pool + the window's 64 scan rows,
+    2d bytes per bf16 K row and per V row actually needed (unions over the
+    GQA group, window included), and the per-level scratch (J+1)(2d+6)*4
+    per query head."""
+    d, G = w.d, w.G
+    P = n - 64
+    scan = n * (d / 2 + 8 * d / 64 + 4 / 64)
+    st = stats.reshape(w.B, w.Hkv, G, -1)
+    kr = st[:, :, 0, 7].astype(float)
+    vr = st[:, :, 0, 8].astype(float)
+    J = st[:, :, :, 5].astype(float)
+    rows = 2 * d * (kr + vr)
+    scratch = ((J + 1) * (2 * d + 6) * 4).sum(axis=2)
+    per = {
+        "scan": w.B * w.Hkv * scan,
+        "rows_k": float((2 * d * kr).sum()),
+        "rows_v": float((2 * d * vr).sum()),
+        "scratch": float(scratch.sum()),
+    }
+    per["total"] = per["scan"] + float(rows.sum()) + per["scratch"]
+    return per
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------ CPU baseline
+
+def time_oracle(w, K, V, q, seeds, groups):
+    import numpy as np
+    from oracle.step import Params, oracle_decode_group
+    p = Params(w.eps, w.delta, w.r)
+    total = 0.0
+    for (b, g) in groups:
+        Kn = K[b, g, :w.n].float().cpu().numpy()
+        Vn = V[b, g, :w.n].float().cpu().numpy()
+        qn = q[b, g * w.G:(g + 1) * w.G].float().cpu().numpy()
+        t1 = time.perf_counter()
+        oracle_decode_group(qn, Kn, Vn, w.n, int(seeds[b]), g, p,
+                            keep_detail=False)
+        total += time.perf_counter() - t1
+    return total / max(len(groups), 1)
+
+
+# ------------------------------------------------------------------ arms
+
+def setup_layers(w, layers, device, csa):
+    import torch
+    import synth
+    shape = csa.make_shape(w.B, w.Hq, w.Hkv, w.d, w.n, w.dtype)
+    data = []
+    for lid in layers:
+        K, V, meta = synth.kv_torch(w, layer=lid, device=device)
+        K4, bounds, vmax = csa.meta_buffers(shape, device)
+        csa.check(csa.csa_quantize_keys(shape, K, V, [w.n] * w.B, 0, K4,
+                                        bounds, vmax), "csa_quantize_keys")
+        qs = [synth.q_torch(w, meta, s, layer=lid, device=device)
+              for s in range(4)]
+        data.append({"K": K, "V": V, "K4": K4, "bounds": bounds,
+                     "vmax": vmax, "q": qs, "lid": lid})
+    torch.cuda.synchronize()
+    return shape, data
+
+
+def seeds_for(w, lid, s):
+    import synth
+    return [int(x) for x in synth.step_seeds(w, s, layer=lid)]
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    import synth
+    import certified_sparse_attention_gb300 as csa
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    csa.load_library()
+    w = synth.workload(WORKLOAD)
+    if args.n or args.batch:
+        # smaller captures for profilers; never used for the reported line
+        import dataclasses
+        w = dataclasses.replace(w, n=args.n or w.n, B=args.batch or w.B)
+    layers = rank_layers(rank, world, args.layers)
+    shape, data = setup_layers(w, layers, device, csa)
+    params = csa.make_params(w.eps, w.delta, w.r)
+    step = csa.DecodeStep(shape, params, device, with_stats=False)
+    step_diag = csa.DecodeStep(shape, params, device, with_stats=True)
+    dense = csa.DenseDecode(shape, device)
+    lens = [w.n] * w.B
+    stream = torch.cuda.current_stream(device)
+
+    nseed = max(args.steps, args.warmup, 64)
+    seed_tab = [[seeds_for(w, d["lid"], s) for s in range(nseed)]
+                for d in data]
+
+    def one(s, L):
+        d = data[L]
+        step(d["q"][s % 4], d["K"], d["V"], d["K4"], d["bounds"], d["vmax"],
+             lens, seed_tab[L][s % nseed], stream)
+
+    for s in range(args.warmup):
+        one(s, s % args.layers)
+        dense(data[s % args.layers]["q"][0], data[s % args.layers]["K"],
+              data[s % args.layers]["V"], lens, stream)
+    torch.cuda.synchronize()
+    csa.csa_profile_read()                      # reset launch counter
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    plan = step_plan(rank, args.steps, args.layers)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for (L, s) in plan:
+        one(s, L)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_sparse = e0.elapsed_time(e1) / args.steps
+    launches = csa.csa_profile_read()["launches"]
+    # same-build dense comparator over the same rotation
+    e0.record(stream)
+    for (L, s) in plan:
+        d = data[L]
+        dense(d["q"][s % 4], d["K"], d["V"], lens, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    ms_dense = e0.elapsed_time(e1) / args.steps
+    ms_sparse = max_over_ranks(ms_sparse, world, device)
+    ms_dense = max_over_ranks(ms_dense, world, device)
+
+    # live per-phase times (CUDA events at phase boundaries on the stream)
+    csa.csa_profile_enable(True)
+    nprof = min(args.steps, 32)
+    for (L, s) in plan[:nprof]:
+        one(s, L)
+    torch.cuda.synchronize()
+    prof = csa.csa_profile_read()
+    csa.csa_profile_enable(False)
+    phase_ms = {k: v / max(prof["steps"], 1) for k, v in prof["ms"].items()}
+
+    # algorithmic bytes: diagnostics of one step on every rotated layer
+    abs_ = []
+    for L in range(args.layers):
+        d = data[L]
+        step_diag(d["q"][L % 4], d["K"], d["V"], d["K4"], d["bounds"],
+                  d["vmax"], lens, seed_tab[L][L % nseed], stream)
+        torch.cuda.synchronize()
+        stats = step_diag.stats.cpu().numpy()
+        abs_.append(algorithmic_bytes(stats, w, w.n))
+    ab = {k: sum(x[k] for x in abs_) / len(abs_) for k in abs_[0]}
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    phase_bytes = {"scan": ab["scan"], "rescore": ab["rows_k"],
+                   "vgather": ab["rows_v"]}
+    phase_ms.setdefault("rescore", 0.0)
+    dom = max(phase_bytes, key=lambda k: phase_ms.get(k, 0.0))
+    dom_all = max(phase_ms, key=lambda k: phase_ms[k])
+    achieved = phase_bytes[dom] / (phase_ms[dom] * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as f:
+                tr = json.load(f)
+            traffic = tr.get(dom)
+        except (OSError, ValueError):
+            traffic = None
+    step_gbs = ab["total"] / (ms_sparse * 1e-3) / 1e9
+    dense_bytes = w.B * w.Hkv * w.n * 4 * w.d
+    dense_gbs = dense_bytes / (ms_dense * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers: H2D of the step's
+    # queries, re-quantisation of the last token's block, the step, D2H of
+    # the results
+    qh = torch.empty_like(data[0]["q"][0], device="cpu").pin_memory()
+    qh.copy_(data[0]["q"][0].cpu())
+    qd = torch.empty_like(data[0]["q"][0])
+    oh = torch.empty_like(step.o, device="cpu").pin_memory()
+    bh = torch.empty_like(step.beta, device="cpu").pin_memory()
+    lh = torch.empty_like(step.level, device="cpu").pin_memory()
+    kh = torch.empty_like(step.keys_read, device="cpu").pin_memory()
+    ne2e = max(1, min(args.steps, 64))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for (L, s) in plan[:ne2e]:
+        d = data[L]
+        qd.copy_(qh, non_blocking=True)
+        csa.check(csa.csa_quantize_keys(shape, d["K"], d["V"], lens,
+                                        w.n - 1, d["K4"], d["bounds"],
+                                        d["vmax"], stream))
+        step(qd, d["K"], d["V"], d["K4"], d["bounds"], d["vmax"], lens,
+             seed_tab[L][s % nseed], stream)
+        oh.copy_(step.o, non_blocking=True)
+        bh.copy_(step.beta, non_blocking=True)
+        lh.copy_(step.level, non_blocking=True)
+        kh.copy_(step.keys_read, non_blocking=True)
+        stream.synchronize()
+    ms_e2e = (time.perf_counter() - t0) * 1e3 / ne2e
+    ms_e2e = max_over_ranks(ms_e2e, world, device)
+    h2d = qh.numel() * qh.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in (oh, bh, lh, kh))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        groups = [(0, 0), (0, 1)]
+        sec = time_oracle(w, data[0]["K"], data[0]["V"], data[0]["q"][0],
+                          seeds_for(w, data[0]["lid"], 0), groups)
+        cpu = {"value": sec * w.B * w.Hkv * 1e6, "unit": "us/step",
+               "cores": 1, "kind": "oracle",
+               "sample": f"{len(groups)} of {w.B * w.Hkv} (sequence, KV "
+                         "head) groups of one layer (4 query heads each), "
+                         "float64 numpy oracle, extrapolated to the whole "
+                         "step"}
+
+    levels = stats[..., 0]
+    line = {
+        "metric": METRIC,
+        "value": round(ms_sparse * 1e3, 2),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_sparse, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded generator with Llama-3.1-8B-shaped "
+                "heads (keys = norm-4 shared direction + N(0,1) with 4 "
+                "outlier channels x8 and 32 needles per KV head; values "
+                "N(0,1) x lognormal(0,0.5); half the groups near-uniform); "
+                "stands in for the pages' real KV caches",
+        "config": {"workload": f"{WORKLOAD}: B={w.B} sequences x 1 layer "
+                               f"per step, n={w.n}, Hq={w.Hq}, Hkv={w.Hkv}, "
+                               f"d={w.d}, bf16, eps={w.eps}, "
+                               f"delta={w.delta}, r={w.r}",
+                   "layers_rotated": args.layers,
+                   "l2": f"inputs larger than L2: {args.layers} resident "
+                         f"layers (~{args.layers * 2.3:.0f} GB) rotated "
+                         "between steps",
+                   "batch_per_gpu": w.B},
+        "roofline": {"bound": "hbm", "kernel": dom,
+                     "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": traffic},
+        "step_roofline": {"algorithmic_bytes": round(ab["total"]),
+                          "achieved_gbs": round(step_gbs, 1),
+                          "frac": round(step_gbs / hbm_peak, 4)},
+        "phase_us": {k: round(v * 1e3, 1) for k, v in phase_ms.items()},
+        "dominant_phase": dom_all,
+        "dense_us_per_step": round(ms_dense * 1e3, 2),
+        "dense_gbs": round(dense_gbs, 1),
+        "sparse_over_dense_time": round(ms_sparse / ms_dense, 3),
+        "levels_hist": [int(x) for x in np.bincount(levels.ravel())],
+        "keys_read_mean": float(stats[..., 1].mean()),
+        "values_read_mean": float(stats[..., 2].mean()),
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(ms_e2e * 1e3, 2), "unit": "us/step",
+                "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, world, rank, local):
+    """The oracle, as it stands, on the host cores: each step is one
+    (sequence, KV head) group of the same workload, extrapolated to the
+    whole step."""
+    if rank != 0:
+        return
+    import numpy as np
+    import synth
+    from oracle.step import Params, oracle_decode_group
+    w = synth.workload(WORKLOAD, B=1)
+    wfull = synth.workload(WORKLOAD)
+    p = Params(w.eps, w.delta, w.r)
+    one = synth.workload(WORKLOAD, B=1, Hq=w.G, Hkv=1)
+    K, V, meta = synth.kv_numpy(one)
+    times = []
+    # each sample costs seconds of host time: at most 6 timed samples
+    nsteps = max(1, min(args.steps, 6))
+    args.steps = nsteps
+    args.warmup = min(args.warmup, 1)
+    for s in range(args.warmup + args.steps):
+        q = synth.q_numpy(one, meta, s)
+        seed = int(synth.step_seeds(one, s)[0])
+        t0 = time.perf_counter()
+        oracle_decode_group(q[0], K[0, 0], V[0, 0], one.n, seed, 0, p,
+                            keep_detail=False)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    us = statistics.mean(times) * wfull.B * wfull.Hkv * 1e6
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(us, 1), "unit": "us/step",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same generator and workload as the GPU arm)",
+        "config": {"workload": f"{WORKLOAD}: B={wfull.B}, n={wfull.n}, "
+                               f"Hq={wfull.Hq}, Hkv={wfull.Hkv}, d={wfull.d}"},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/step",
+                         "cores": 1, "kind": "oracle",
+                         "sample": "one (sequence, KV head) group (4 query "
+                                   "heads) per step, extrapolated x"
+                                   f"{wfull.B * wfull.Hkv} to the whole "
+                                   "step"},
+        "e2e": {"value": round(us, 1), "unit": "us/step",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n", type=int, default=0,
+                    help="override the context length (profiler captures)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch (profiler captures)")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -28,7 +28,15 @@ BLOCK = 64
 
 EXPORTED = ("csa_workspace_size", "csa_quantize_keys", "csa_decode_step",
             "csa_dense_workspace_size", "csa_dense_decode", "csa_check",
-            "csa_status_string", "csa_workspace_layout")
+            "csa_status_string", "csa_workspace_layout",
+            "csa_profile_enable", "csa_profile_read")
+STATS_FIELDS = 10
+STAT = {"level": 0, "keys_read": 1, "values_read": 2, "n_candidates": 3,
+        "n_near_threshold": 4, "J": 5, "rounds": 6, "group_keys_read": 7,
+        "group_values_read": 8}
+PHASES = ("clear", "scan", "exact_max", "candidates", "rescore", "predict",
+          "levels", "plan", "vgather", "certify", "fallback", "diagnostics",
+          "prehist")
 
 
 class CsaLibraryMissing(RuntimeError):
@@ -58,7 +66,10 @@ class csa_head_stats(ctypes.Structure):
                 ("values_read", ctypes.c_int32),
                 ("n_candidates", ctypes.c_int32),
                 ("n_near_threshold", ctypes.c_int32), ("J", ctypes.c_int32),
-                ("rounds", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("rounds", ctypes.c_int32),
+                ("group_keys_read", ctypes.c_int32),
+                ("group_values_read", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class csa_workspace_map(ctypes.Structure):
@@ -66,6 +77,11 @@ class csa_workspace_map(ctypes.Structure):
                 ("s32", ctypes.c_size_t), ("jr_hist", ctypes.c_size_t),
                 ("total", ctypes.c_size_t), ("J1", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class csa_phase_times(ctypes.Structure):
+    _fields_ = [("ms", ctypes.c_float * 13), ("steps", ctypes.c_int32),
+                ("launches", ctypes.c_int64)]
 
 
 _lib = None
@@ -103,6 +119,10 @@ def load_library(path: str = LIB_PATH):
     lib.csa_workspace_layout.argtypes = [P(csa_shape), P(csa_params),
                                          P(csa_workspace_map)]
     lib.csa_workspace_layout.restype = ctypes.c_int
+    lib.csa_profile_enable.argtypes = [ctypes.c_int]
+    lib.csa_profile_enable.restype = ctypes.c_int
+    lib.csa_profile_read.argtypes = [P(csa_phase_times)]
+    lib.csa_profile_read.restype = ctypes.c_int
     lib.csa_status_string.argtypes = [ctypes.c_int]
     lib.csa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -206,6 +226,19 @@ def csa_dense_decode(shape, q, K, V, lens, o, workspace, workspace_bytes,
         _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
+def csa_profile_enable(on: bool) -> int:
+    return load_library().csa_profile_enable(1 if on else 0)
+
+
+def csa_profile_read() -> dict:
+    """Accumulated ms per phase since the last read, steps, launches."""
+    t = csa_phase_times()
+    check(load_library().csa_profile_read(ctypes.byref(t)),
+          "csa_profile_read")
+    return {"ms": dict(zip(PHASES, list(t.ms))), "steps": int(t.steps),
+            "launches": int(t.launches)}
+
+
 def csa_check(workspace, stream=None) -> int:
     return load_library().csa_check(_ptr(workspace), _stream(stream))
 
@@ -250,7 +283,7 @@ class DecodeStep:
         self.level = torch.empty((B, Hq), dtype=torch.int32, device=device)
         self.keys_read = torch.empty((B, Hq), dtype=torch.int32,
                                      device=device)
-        self.stats = (torch.zeros((B, Hq, 8), dtype=torch.int32,
+        self.stats = (torch.zeros((B, Hq, STATS_FIELDS), dtype=torch.int32,
                                   device=device) if with_stats else None)
 
     def __call__(self, q, K, V, K4, bounds, vmax, lens, seeds, stream=None):

@@ -42,8 +42,10 @@ bool params_ok(const csa_params* p) {
 struct Layout {
   int J1;
   int64_t pcap, nblk_max;
-  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, zero_end;
-  size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, s32, win, buckets, dpart, total;
+  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, zero_end;
+  size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, s32, win, t32, clist, xlist, cmap,
+      buckets, dpart, total;
+  int64_t nchunk_cap;
 };
 
 bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
@@ -63,6 +65,9 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.acc = o; o += up((size_t)BH * L.J1 * ACC * 4);
   L.bcnt = o; o += up((size_t)BG * L.J1 * 4);
   L.bcons = o; o += up((size_t)BG * L.J1 * 4);
+  L.ccnt = o; o += up((size_t)BG * 4);
+  L.xcnt = o; o += up((size_t)BG * 4);
+  L.nfall = o; o += up(4);
   L.zero_end = o;
   L.winstats = o; o += up((size_t)BH * (D + 4) * 4);
   L.vmaxp = o; o += up((size_t)BG * 4);
@@ -73,7 +78,12 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.ubar = o; o += up((size_t)BG * s->n_max * G * 4);
   L.s32 = o; o += up((size_t)BG * L.pcap * G * 4);
   L.win = o; o += up((size_t)BG * kWindow * G * 4);
-  L.buckets = o; o += up((size_t)BG * L.J1 * L.pcap * 4);
+  L.t32 = o; o += up((size_t)BG * L.pcap * 4);
+  L.clist = o; o += up((size_t)BG * L.pcap * 8);
+  L.xlist = o; o += up((size_t)BG * s->n_max * 8);
+  L.nchunk_cap = (int64_t)BG * L.J1 + (int64_t)BG * L.pcap * 2 * G / 1024 + 16;
+  L.cmap = o; o += up((size_t)L.nchunk_cap * 4);
+  L.buckets = o; o += up((size_t)BG * L.J1 * L.pcap * 8);
   L.dpart = o; o += up((size_t)dense_nsplit(s->n_max) * BH * (D + 2) * 4);
   L.total = o;
   return true;
@@ -92,6 +102,45 @@ int sm_count() {
 }
 
 csa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+// ----------------------------------------------------------- phase timing
+constexpr int kProfSteps = 64;
+constexpr int kProfEv = 2 * CSA_NPHASE + 8;   // boundaries per step (rounds repeat phases)
+struct Profiler {
+  bool on = false;
+  bool made = false;
+  cudaEvent_t ev[kProfSteps][kProfEv];
+  int phase[kProfSteps][kProfEv];
+  int nev[kProfSteps];
+  int head = 0, count = 0, cur = -1;
+  long long launches = 0;
+};
+Profiler g_prof;
+
+void prof_step_begin(cudaStream_t st) {
+  if (!g_prof.on) return;
+  if (!g_prof.made) {
+    for (int i = 0; i < kProfSteps; ++i)
+      for (int j = 0; j < kProfEv; ++j) cudaEventCreate(&g_prof.ev[i][j]);
+    g_prof.made = true;
+  }
+  g_prof.cur = (g_prof.head + g_prof.count) % kProfSteps;
+  if (g_prof.count == kProfSteps) g_prof.head = (g_prof.head + 1) % kProfSteps;
+  else ++g_prof.count;
+  g_prof.nev[g_prof.cur] = 0;
+  cudaEventRecord(g_prof.ev[g_prof.cur][0], st);
+  g_prof.nev[g_prof.cur] = 1;
+}
+// mark the end of `phase` (the interval since the previous mark)
+void prof_mark(int phase, cudaStream_t st) {
+  if (!g_prof.on || g_prof.cur < 0) return;
+  int k = g_prof.nev[g_prof.cur];
+  if (k >= kProfEv) return;
+  g_prof.phase[g_prof.cur][k] = phase;
+  cudaEventRecord(g_prof.ev[g_prof.cur][k], st);
+  g_prof.nev[g_prof.cur] = k + 1;
+}
+void count_launches(int k) { g_prof.launches += k; }
 
 }  // namespace
 }  // namespace csa
@@ -160,6 +209,7 @@ csa_status csa_quantize_keys(const csa_shape* shape, const void* K, const void* 
   QuantArgs a;
   a.K = K; a.V = V; a.K4 = K4; a.bounds = bounds; a.vmax = vmax; a.Hkv = shape->Hkv;
   a.n_max = shape->n_max; a.nblk_max = (shape->n_max + kBlock - 1) / kBlock; a.blk_from = blk_from;
+  if (nblocks > 0) count_launches(1);
   return cuda_status(launch_quant(a, seq, shape->B, shape->d, shape->dtype == CSA_BF16, nblocks,
                                   (cudaStream_t)stream));
 }
@@ -181,9 +231,10 @@ csa_status csa_dense_decode(const csa_shape* shape, const void* q, const void* K
     if (len[b] > nlive) nlive = len[b];
   }
   DenseArgs a;
-  a.q = q; a.K = K; a.V = V; a.part = (float*)workspace; a.o = o; a.state = nullptr;
+  a.q = q; a.K = K; a.V = V; a.part = (float*)workspace; a.o = o; a.state = nullptr; a.nfall = nullptr;
   a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max;
   a.nsplit = dense_nsplit(shape->n_max); a.rs = (float)(1.0 / std::sqrt((double)shape->d));
+  count_launches(2);
   return cuda_status(launch_dense(a, seq, shape->d, shape->Hq / shape->Hkv, shape->dtype == CSA_BF16, nlive,
                                   (cudaStream_t)stream));
 }
@@ -219,7 +270,9 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   char* ws = (char*)workspace;
   const float rs = (float)(1.0 / std::sqrt((double)shape->d));
 
+  prof_step_begin(st);
   if (cudaMemsetAsync(ws, 0, L.zero_end, st) != cudaSuccess) return CSA_ERR_CUDA;
+  prof_mark(0, st);
 
   ScanArgs sa;
   sa.q = q; sa.K4 = K4; sa.bounds = bounds; sa.ubar = (float*)(ws + L.ubar);
@@ -227,6 +280,8 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   sa.Hq = shape->Hq; sa.Hkv = shape->Hkv; sa.n_max = shape->n_max; sa.nblk_max = L.nblk_max; sa.rs = rs;
   cudaError_t e = launch_scan(sa, seq, shape->B, shape->d, G, bf16, nlive, st);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
+  count_launches(1);
+  prof_mark(1, st);
 
   SparseArgs a;
   a.q = q; a.K = K; a.V = V; a.vmax = vmax; a.ubar = (const float*)(ws + L.ubar);
@@ -234,7 +289,11 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   a.jr_hist = (unsigned*)(ws + L.jr_hist); a.ncand = (unsigned*)(ws + L.ncand);
   a.pre_hist = (float*)(ws + L.pre_hist); a.acc = (float*)(ws + L.acc); a.winstats = (float*)(ws + L.winstats);
   a.vmaxp = (float*)(ws + L.vmaxp); a.state = (int*)(ws + L.state); a.bcnt = (unsigned*)(ws + L.bcnt);
-  a.bcons = (unsigned*)(ws + L.bcons); a.buckets = (unsigned*)(ws + L.buckets);
+  a.bcons = (unsigned*)(ws + L.bcons); a.buckets = (uint2*)(ws + L.buckets);
+  a.t32 = (float*)(ws + L.t32); a.clist = (uint2*)(ws + L.clist); a.ccnt = (unsigned*)(ws + L.ccnt);
+  a.nfall = (unsigned*)(ws + L.nfall);
+  a.xlist = (uint2*)(ws + L.xlist); a.xcnt = (unsigned*)(ws + L.xcnt);
+  a.chunk_map = (unsigned*)(ws + L.cmap); a.nchunk_cap = L.nchunk_cap;
   a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);
   a.plan_off = (unsigned*)(ws + L.plan_off); a.status = (unsigned*)(ws + L.status);
   a.o = o; a.beta = beta; a.level = level; a.keys_read = keys_read; a.stats = stats;
@@ -242,23 +301,66 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   a.pcap = L.pcap; a.J1 = L.J1; a.r = params->r; a.eps = params->eps; a.delta = params->delta;
   a.measure = params->measure; a.rs = rs;
 
+  const int nsm = sm_count();
   if (plive > 0) {
-    if (launch_cstar(a, seq, shape->d, G, bf16, nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
-    if (launch_rescore(a, seq, shape->d, G, bf16, plive, st) != cudaSuccess) return CSA_ERR_CUDA;
+    if (launch_cstar(a, seq, shape->d, G, bf16, nlive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
+    prof_mark(2, st);
+    if (launch_rescore(a, seq, shape->d, G, bf16, plive, nsm, st, g_prof.on ? prof_mark : nullptr) !=
+        cudaSuccess)
+      return CSA_ERR_CUDA;
+    prof_mark(12, st);
+    count_launches(5);
   }
   if (launch_predict(a, seq, shape->d, G, bf16, st) != cudaSuccess) return CSA_ERR_CUDA;
-  const int nsm = sm_count();
-  for (int round = 0; round < 3; ++round)
-    if (launch_round(a, seq, shape->d, G, bf16, plive > 0 ? plive : 1, round, nsm, st) != cudaSuccess)
+  count_launches(1);
+  prof_mark(5, st);
+  for (int round = 0; round < 3; ++round) {
+    if (launch_round(a, seq, shape->d, G, bf16, plive > 0 ? plive : 1, round, nsm, st,
+                     g_prof.on ? prof_mark : nullptr) != cudaSuccess)
       return CSA_ERR_CUDA;
+    count_launches(4);
+  }
   // exact attention for heads with no certified level and sequences without a pool
   DenseArgs da;
   da.q = q; da.K = K; da.V = V; da.part = (float*)(ws + L.dpart); da.o = o; da.state = a.state;
+  da.nfall = a.nfall;
   da.B = shape->B; da.Hq = shape->Hq; da.Hkv = shape->Hkv; da.n_max = shape->n_max;
   da.nsplit = dense_nsplit(shape->n_max); da.rs = rs;
   if (launch_dense(da, seq, shape->d, G, bf16, nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
-  if (stats && plive > 0)
+  count_launches(2);
+  prof_mark(10, st);
+  if (stats && plive > 0) {
     if (launch_near(a, seq, G, plive, st) != cudaSuccess) return CSA_ERR_CUDA;
+    count_launches(1);
+    prof_mark(11, st);
+  }
+  return CSA_OK;
+}
+
+csa_status csa_profile_enable(int on) {
+  g_prof.on = on != 0;
+  return CSA_OK;
+}
+
+csa_status csa_profile_read(csa_phase_times* out) {
+  if (!out) return CSA_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  for (int c = 0; c < g_prof.count; ++c) {
+    const int i = (g_prof.head + c) % kProfSteps;
+    if (g_prof.nev[i] < 2) continue;
+    if (cudaEventSynchronize(g_prof.ev[i][g_prof.nev[i] - 1]) != cudaSuccess) return CSA_ERR_CUDA;
+    for (int k = 1; k < g_prof.nev[i]; ++k) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, g_prof.ev[i][k - 1], g_prof.ev[i][k]) != cudaSuccess) return CSA_ERR_CUDA;
+      out->ms[g_prof.phase[i][k]] += ms;
+    }
+    out->steps += 1;
+  }
+  out->launches = g_prof.launches;
+  g_prof.head = 0;
+  g_prof.count = 0;
+  g_prof.cur = -1;
+  g_prof.launches = 0;
   return CSA_OK;
 }
 

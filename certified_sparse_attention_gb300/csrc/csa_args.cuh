@@ -34,9 +34,17 @@ struct SparseArgs {
   float* winstats;        // [B*Hq][D+4]          N_R[D], D_R, H_R
   float* vmaxp;           // [B*Hkv]              max vmax over pool blocks
   int* state;             // [B*Hq][4]            lo, hi, stop, flags
+  float* t32;             // [B*Hkv][pcap]        perturbation t_i = -log2 u_i
+  uint2* xlist;           // [B*Hkv][n_max]       exact-max set: key, head mask
+  unsigned* xcnt;         // [B*Hkv]
+  unsigned* chunk_map;    // [nchunk_cap]         gather work item -> bucket entry
+  int64_t nchunk_cap;
+  uint2* clist;           // [B*Hkv][pcap]        candidates to rescore: key, head mask
+  unsigned* ccnt;         // [B*Hkv]
+  unsigned* nfall;        // heads that need the exact fallback
   unsigned* bcnt;         // [B*Hkv][J1]
   unsigned* bcons;        // [B*Hkv][J1]
-  unsigned* buckets;      // [B*Hkv][J1][pcap]
+  uint2* buckets;         // [B*Hkv][J1][pcap]    key, event masks (add | trans<<8 | before<<16)
   unsigned* plan_start;   // [B*Hkv*J1]
   unsigned* plan_end;     // [B*Hkv*J1]
   unsigned* plan_off;     // [B*Hkv*J1 + 1]
@@ -62,6 +70,7 @@ struct DenseArgs {
   float* part;            // [nsplit][B*Hq][D+2]: m, l, acc[D]
   float* o;               // [B*Hq][D]
   const int* state;       // optional [B*Hq][4]: only heads with flag bit 0
+  const unsigned* nfall;  // optional: skip everything when it reads 0
   int B, Hq, Hkv;
   int64_t n_max;
   int nsplit;
@@ -82,12 +91,13 @@ struct QuantArgs {
 cudaError_t launch_scan(const ScanArgs&, const SeqArgs&, int B, int d, int G, bool bf16, int64_t nmax_live,
                         cudaStream_t);
 cudaError_t launch_cstar(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t nmax_live,
-                         cudaStream_t);
+                         int nsm, cudaStream_t);
 cudaError_t launch_rescore(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t pmax_live,
-                           cudaStream_t);
+                           int nsm, cudaStream_t, void (*mark)(int, cudaStream_t));
 cudaError_t launch_predict(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, cudaStream_t);
+typedef void (*PhaseMark)(int phase, cudaStream_t);
 cudaError_t launch_round(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t pmax_live,
-                         int round, int nsm, cudaStream_t);
+                         int round, int nsm, cudaStream_t, PhaseMark mark);
 cudaError_t launch_near(const SparseArgs&, const SeqArgs&, int G, int64_t pmax_live, cudaStream_t);
 cudaError_t launch_dense(const DenseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t nmax_live,
                          cudaStream_t);

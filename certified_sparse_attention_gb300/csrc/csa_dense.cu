@@ -35,16 +35,21 @@ __device__ __forceinline__ bool group_wanted(const DenseArgs& a, int b, int g, i
 }
 
 template <int D, int G, typename E>
-__global__ void __launch_bounds__(256) dense_split_kernel(const DenseArgs a, const __grid_constant__ SeqArgs seq) {
+__global__ void __launch_bounds__(256) dense_split_kernel(const DenseArgs a, const __grid_constant__ SeqArgs seq,
+                                                          int nsplit_live) {
   constexpr int CPL = D / 32;
   __shared__ float s_m[8][G], s_l[8][G];
   __shared__ float s_acc[8][G][D];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  if (a.nfall && *a.nfall == 0u) return;
+  const int nitems = nsplit_live * a.B * a.Hkv;
+  for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+  const int split = item % nsplit_live;
+  const int bg = item / nsplit_live, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
-  const int64_t start = (int64_t)blockIdx.x * kDenseChunk;
-  if (start >= n) return;
-  if (!group_wanted(a, b, g, G)) return;
+  const int64_t start = (int64_t)split * kDenseChunk;
+  if (start >= n) continue;
+  if (!group_wanted(a, b, g, G)) continue;
   const int64_t end = min(n, start + kDenseChunk);
   float qv[G][CPL];
   const E* qp = reinterpret_cast<const E*>(a.q) + ((int64_t)b * a.Hq + (int64_t)g * G) * D;
@@ -128,7 +133,9 @@ __global__ void __launch_bounds__(256) dense_split_kernel(const DenseArgs a, con
         v += e * (c == 1 ? s_l[x][h] : s_acc[x][h][c - 2]);
       }
     }
-    a.part[((int64_t)blockIdx.x * a.B * a.Hq + (int64_t)b * a.Hq + g * G + h) * (D + 2) + c] = v;
+    a.part[((int64_t)split * a.B * a.Hq + (int64_t)b * a.Hq + g * G + h) * (D + 2) + c] = v;
+  }
+  __syncthreads();
   }
 }
 
@@ -136,6 +143,7 @@ template <int D>
 __global__ void __launch_bounds__(128) dense_combine_kernel(const DenseArgs a, const __grid_constant__ SeqArgs seq) {
   const int bh = blockIdx.x;
   const int b = bh / a.Hq;
+  if (a.nfall && *a.nfall == 0u) return;
   if (a.state && !(a.state[(int64_t)bh * 4 + 3] & 1)) return;
   const int64_t n = seq.n[b];
   const int ns = (int)((n + kDenseChunk - 1) / kDenseChunk);
@@ -179,8 +187,12 @@ int dense_nsplit(int64_t n_max) { return (int)((n_max + kDenseChunk - 1) / kDens
 
 cudaError_t launch_dense(const DenseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t nmax_live,
                          cudaStream_t st) {
-  dim3 grid((unsigned)((nmax_live + kDenseChunk - 1) / kDenseChunk), (unsigned)(a.B * a.Hkv));
-  CSA_DENSE_SWITCH(dense_split_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  const int nsplit_live = (int)((nmax_live + kDenseChunk - 1) / kDenseChunk);
+  int items = nsplit_live * a.B * a.Hkv;
+  // comparator: one CTA per item; fallback (masked): a small persistent grid
+  const int cap = a.state ? 1024 : items;
+  dim3 grid((unsigned)(items < cap ? items : cap));
+  CSA_DENSE_SWITCH(dense_split_kernel, <<<grid, 256, 0, st>>>(a, seq, nsplit_live))
   if (d == 128) dense_combine_kernel<128><<<a.B * a.Hq, 128, 0, st>>>(a, seq);
   else dense_combine_kernel<64><<<a.B * a.Hq, 128, 0, st>>>(a, seq);
   return cudaGetLastError();

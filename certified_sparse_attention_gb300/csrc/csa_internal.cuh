@@ -164,6 +164,17 @@ __device__ __forceinline__ void exact_levels(float s, float c, float t, float ne
   hl = level_of(fmul(neg_r, y), J);
 }
 
+// ------------------------------------------------------- async staging
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  int src = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sa), "l"(gmem), "r"(src));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
 // ------------------------------------------------------ warp row products
 //
 // Eight rows at a time: lane l holds channels [l*CPL, (l+1)*CPL) of every

@@ -2,27 +2,34 @@
 //
 // picx.dev summary, "Algorithm Components" 1-4 and Theorem 4; readsearch.ai
 // "Abstract".  Kernels, in launch order, for every (sequence b, KV head g):
-//   cstar_kernel    exact maximum: float32 rescoring of the window and of the
-//                   pool keys with ubar >= c*_lo; c32 = max score, and the
-//                   certified lower bound cb = max fl(s32 - fl(mag * 2^-13))
-//   rescore_kernel  perturbations t_i, bound levels jbar_i, candidates
-//                   (jbar <= J); exact float32 scores of candidate K rows (one
-//                   row load serves the G heads); per-level counts and heavy
-//                   weights that need no values
-//   predict_kernel  window sums (D_R, N_R, H_R) and, from the value-free
-//                   per-level counts, a predicted stop level per head that
-//                   sizes the first gather round
-//   levels_kernel   (per round) exact inclusion / heavy levels; each key that
-//                   changes a head's sums at a level of the round is appended
-//                   once to the (b, g, level) bucket
-//   vplan_kernel    (per round) chunk list over the new bucket entries
+//   cset_kernel     the exact-max set: the window and the pool keys with
+//                   ubar >= c*_lo for some head, compacted into a list
+//   rows_kernel<0>  float32 rescoring of the listed K rows (one row load
+//                   serves the G heads): c32 = max score and the certified
+//                   lower bound cb = max fl(s32 - fl(mag * 2^-13))
+//   cand_kernel     perturbations t_i, bound levels jbar_i, candidates
+//                   (jbar <= J); keys of the exact-max set keep the scores
+//                   already computed, the others are compacted into a list
+//   rows_kernel<1>  float32 scores of the listed candidate K rows
+//   prehist_kernel  exact levels; per-level counts and heavy weights that
+//                   need no values (for the stop predictor)
+//   predict_kernel  window sums (D_R, N_R, H_R) and a predicted stop level
+//                   per head that sizes the first gather round
+//   levels_kernel   (per round) each key that changes a head's sums at a
+//                   level of the round is appended once to the (b, g, level)
+//                   bucket, with per-head event masks
+//   vplan_kernel    (per round) work items over the new bucket entries
 //   vgather_kernel  (per round) V rows of the bucketed keys; per-level
 //                   Horvitz-Thompson sums (light count, sum v, sum ||v||^2;
-//                   heavy sum w, sum w v, sum w ||v||^2) accumulated per head
+//                   heavy sum w, sum w v, sum w ||v||^2) per head
 //   certify_kernel  (per round) prefix over levels, Chernoff interval,
 //                   Bernstein bound on G, Pinelis bound zeta, beta, value
 //                   scale lower bound; first certified level -> outputs
-//   near_kernel     optional diagnostics: near-threshold keys at the stop
+//   near_kernel     optional diagnostics: near-threshold keys at the stop,
+//                   rows read per group
+// Row gathers (K rows, V rows) go through a per-warp ring of shared-memory
+// stages filled with cp.async, so the bytes in flight do not depend on the
+// registers a thread holds.
 #include "csa_args.cuh"
 
 namespace csa {
@@ -30,6 +37,8 @@ namespace csa {
 constexpr int kFlagFallback = 1;
 constexpr int kFlagDone = 2;
 constexpr int kChunk = 1024;   // bucket entries per gather work item
+constexpr int kRingS = 4;      // ring stages per warp
+constexpr int kRingW = 8;      // warps per CTA of the ring kernels
 
 // ----------------------------------------------------------- small helpers
 
@@ -61,39 +70,62 @@ __device__ __forceinline__ float cmax_get(const SparseArgs& a, int bh, int k) {
   return float_of_ord(a.cmax[(int64_t)bh * 4 + k]);
 }
 
-// Scores of eight rows (float32, adjacent-pair tree, times rs) for G heads.
-// rows[r] null -> zero row.  On return lane l holds in s[h] the score of row
-// (l & 7) and, when MAG, in m[h] the tree sum of |products| times rs.
-template <int D, int G, typename E, bool MAG>
-__device__ __forceinline__ void score8(const E* const rows[8], const float (&qv)[G][D / 32], float rs,
-                                       float (&s)[G], float (&m)[G]) {
-  constexpr int CPL = D / 32;
-  float kv[8][CPL];
-#pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    if (rows[r]) load_row<D, E>(rows[r], kv[r]);
-    else {
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) kv[r][c] = 0.f;
-    }
+// Warp-aggregated append of this lane's item to a global list (lanes with
+// want = false take no slot).  Returns the slot or -1.
+__device__ __forceinline__ int warp_append(unsigned* counter, bool want) {
+  const int lane = threadIdx.x & 31;
+  const unsigned bal = __ballot_sync(0xffffffffu, want);
+  unsigned base = 0;
+  if (lane == 0 && bal) base = atomicAdd(counter, (unsigned)__popc(bal));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  return want ? (int)(base + __popc(bal & ((1u << lane) - 1u))) : -1;
+}
+
+// Aggregated shared-memory histogram add: lane adds x to base[v] (v < 0:
+// nothing).  When the whole warp has the same v (the common case on flat
+// heads) one atomic carries the warp's total; otherwise each lane adds its
+// own (the values are then spread out and rarely collide).
+__device__ __forceinline__ void hist_add_i(int* base, int v, int x) {
+  const int v0 = __shfl_sync(0xffffffffu, v, 0);
+  if (__all_sync(0xffffffffu, v == v0)) {
+    const int tot = (int)__reduce_add_sync(0xffffffffu, (unsigned)x);
+    if ((threadIdx.x & 31) == 0 && v0 >= 0 && tot) atomicAdd(base + v0, tot);
+  } else if (v >= 0 && x) {
+    atomicAdd(base + v, x);
   }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float part[8], pm[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      float p[CPL], pa[CPL];
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        p[c] = fmul(kv[r][c], qv[h][c]);
-        pa[c] = fabsf(p[c]);
-      }
-      part[r] = local_tree<CPL>(p);
-      pm[r] = local_tree<CPL>(pa);
-    }
-    s[h] = fmul(reduce8_rows(part), rs);
-    if (MAG) m[h] = fmul(reduce8_rows(pm), rs);
+}
+__device__ __forceinline__ void hist_add_u(unsigned* base, int v, unsigned x) {
+  const int v0 = __shfl_sync(0xffffffffu, v, 0);
+  if (__all_sync(0xffffffffu, v == v0)) {
+    const unsigned tot = __reduce_add_sync(0xffffffffu, x);
+    if ((threadIdx.x & 31) == 0 && v0 >= 0 && tot) atomicAdd(base + v0, tot);
+  } else if (v >= 0 && x) {
+    atomicAdd(base + v, x);
   }
+}
+__device__ __forceinline__ void hist_add_f(float* base, int v, float x) {
+  const int v0 = __shfl_sync(0xffffffffu, v, 0);
+  if (__all_sync(0xffffffffu, v == v0)) {
+    float tot = x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if ((threadIdx.x & 31) == 0 && v0 >= 0) atomicAdd(base + v0, tot);
+  } else if (v >= 0) {
+    atomicAdd(base + v, x);
+  }
+}
+// Slot in a shared-memory counter per lane (v < 0: none), aggregated the
+// same way.
+__device__ __forceinline__ int slot_add(unsigned* base, int v) {
+  const int lane = threadIdx.x & 31;
+  const int v0 = __shfl_sync(0xffffffffu, v, 0);
+  if (__all_sync(0xffffffffu, v == v0)) {
+    if (v0 < 0) return -1;
+    unsigned b = 0;
+    if (lane == 0) b = atomicAdd(base + v0, 32u);
+    return (int)(__shfl_sync(0xffffffffu, b, 0) + lane);
+  }
+  return v >= 0 ? (int)atomicAdd(base + v, 1u) : -1;
 }
 
 // Chernoff interval for a Poisson-binomial count k (two-sided, budget
@@ -106,7 +138,6 @@ __device__ __forceinline__ float phi_y(float y) {
 __device__ void chernoff_gaps(float k, float Lz, float& below, float& above) {
   if (!(k > 0.f)) { below = 0.f; above = Lz; return; }
   float c0 = Lz / k;
-  // upper root, y > 0
   float lo = 0.f, hi = fmaxf(1.0f, logf(3.0f * c0 + 3.0f));
   for (int it = 0; it < 8 && phi_y(hi) < c0; ++it) hi *= 2.0f;
   for (int it = 0; it < 48; ++it) {
@@ -114,7 +145,6 @@ __device__ void chernoff_gaps(float k, float Lz, float& below, float& above) {
     if (phi_y(mid) <= c0) lo = mid; else hi = mid;
   }
   above = k * expm1f(hi);
-  // lower root, y < 0
   float a = -(c0 + 1.0f), b2 = 0.f;
   for (int it = 0; it < 48; ++it) {
     float mid = 0.5f * (a + b2);
@@ -123,45 +153,104 @@ __device__ void chernoff_gaps(float k, float Lz, float& below, float& above) {
   below = -k * expm1f(a);
 }
 
-// ----------------------------------------------------------------- c* step
+// Stage eight rows (row indices ent[0..nvalid).x) of a [rows][D] array into
+// dst with 16-byte cp.async copies; missing rows are zero-filled.
+template <int D, typename E>
+__device__ __forceinline__ void stage8(uint8_t* dst, const E* base, const uint2* ent, int nvalid) {
+  constexpr int RB = D * (int)sizeof(E);
+  constexpr int CH = RB / 16;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = lane; c < 8 * CH; c += 32) {
+    const int r = c / CH, part = c - r * CH;
+    const bool ok = r < nvalid;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(base) + (ok ? (int64_t)ent[r].x * RB + part * 16 : 0);
+    cp_async16(dst + r * RB + part * 16, src, ok);
+  }
+}
+
+// Same as stage8 with the 16-byte chunk c of row r stored at chunk
+// c ^ (r & 7): eight rows then read the same byte offset from eight
+// different bank groups (tensor-core fragment loads).
+template <int D, typename E>
+__device__ __forceinline__ void stage8_swz(uint8_t* dst, const E* base, const uint2* ent, int nvalid) {
+  constexpr int RB = D * (int)sizeof(E);
+  constexpr int CH = RB / 16;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = lane; c < 8 * CH; c += 32) {
+    const int r = c / CH, part = c - r * CH;
+    const bool ok = r < nvalid;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(base) + (ok ? (int64_t)ent[r].x * RB + part * 16 : 0);
+    cp_async16(dst + r * RB + ((part ^ (r & 7)) * 16), src, ok);
+  }
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const unsigned (&a)[4], unsigned b0, unsigned b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------- exact-max set
+
+template <int G>
+__global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int64_t n = seq.n[b];
+  if (n <= kWindow) return;
+  const int64_t P = n - kWindow;
+  const int64_t key = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if ((int64_t)blockIdx.x * 256 >= n) return;
+  const int bh0 = b * a.Hq + g * G;
+  unsigned qm = 0;
+  if (key < n) {
+    if (key >= P) qm = (1u << G) - 1u;
+    else {
+      const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        if (ub[h] >= cmax_get(a, bh0 + h, 0)) qm |= 1u << h;
+    }
+  }
+  const int slot = warp_append(a.xcnt + bg, qm != 0);
+  if (slot >= 0) a.xlist[(int64_t)bg * a.n_max + slot] = make_uint2((unsigned)key, qm);
+}
+
+// ------------------------------------------------------ ring row scoring
+//
+// MODE 0 (exact max): entries = exact-max set.  Scores and |product| sums
+//   of every head; the maxima of s32 and fl(s32 - fl(mag 2^-13)) over the
+//   heads in the entry's mask; raw scores stored (pool: s32, window: win).
+// MODE 1 (candidates): entries = candidates still to score; scores stored,
+//   -inf for the heads the key is not a candidate of.
 
 template <int D, int G, typename E>
-__global__ void __launch_bounds__(256) cstar_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+constexpr int rows_smem() {
+  return kRingW * kRingS * 8 * D * (int)sizeof(E) + kRingW * kRingS * 8 * 8 + kRingW * G * 2 * 4;
+}
+
+template <int D, int G, typename E, int MODE>
+__global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
   constexpr int CPL = D / 32;
-  __shared__ int s_list[kTile];
-  __shared__ unsigned s_qm[kTile];
-  __shared__ int s_cnt;
-  __shared__ float s_cb[8][G], s_c32[8][G];
+  constexpr int RB = D * (int)sizeof(E);
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint8_t* ring = dsm;
+  uint2* s_ent = reinterpret_cast<uint2*>(dsm + kRingW * kRingS * 8 * RB);
+  float* s_red = reinterpret_cast<float*>(dsm + kRingW * kRingS * 8 * RB + kRingW * kRingS * 8 * 8);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
   const int64_t P = n - kWindow;
-  const int64_t key0 = (int64_t)blockIdx.x * kTile;
-  if (key0 >= n) return;
-  if (tid == 0) s_cnt = 0;
-  __syncthreads();
+  const unsigned* cntp = MODE == 0 ? a.xcnt : a.ccnt;
+  const uint2* list = MODE == 0 ? a.xlist + (int64_t)bg * a.n_max : a.clist + (int64_t)bg * a.pcap;
+  const int cnt = (int)cntp[bg];
+  const int nbatch = (cnt + 7) / 8;
+  if ((int)blockIdx.x * kRingW >= nbatch) return;
   const int bh0 = b * a.Hq + g * G;
-  {
-    const int64_t key = key0 + tid;
-    unsigned qm = 0;
-    if (key < n) {
-      if (key >= P) qm = (1u << G) - 1u;
-      else {
-        const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          if (ub[h] >= cmax_get(a, bh0 + h, 0)) qm |= 1u << h;
-      }
-    }
-    if (qm) {
-      int p = atomicAdd(&s_cnt, 1);
-      s_list[p] = (int)(key - key0);
-      s_qm[p] = qm;
-    }
-  }
-  __syncthreads();
-  const int cnt = s_cnt;
   float qv[G][CPL];
   {
     const E* qp = reinterpret_cast<const E*>(a.q) + ((int64_t)b * a.Hq + (int64_t)g * G) * D;
@@ -172,145 +261,224 @@ __global__ void __launch_bounds__(256) cstar_kernel(const SparseArgs a, const __
 #pragma unroll
   for (int h = 0; h < G; ++h) { cbm[h] = -INFINITY; c3m[h] = -INFINITY; }
   const E* Kb = reinterpret_cast<const E*>(a.K) + (int64_t)bg * a.n_max * D;
-  for (int base = w * 8; base < cnt; base += 64) {
-    const E* rows[8];
+  uint8_t* my = ring + w * kRingS * 8 * RB;
+  uint2* me = s_ent + w * kRingS * 8;
+  const int wid = blockIdx.x * kRingW + w;
+  const int wstride = gridDim.x * kRingW;
+  // entries of ring cycle c, batch k = lane / 8, row lane % 8
+  auto load_ent = [&](int cyc) {
+    const int bt = wid + (4 * cyc + (lane >> 3)) * wstride;
+    const int row = bt * 8 + (lane & 7);
+    return (bt < nbatch && row < cnt) ? list[row] : make_uint2(0u, 0u);
+  };
+  auto nvalid = [&](int bt) { return bt < nbatch ? min(8, cnt - bt * 8) : 0; };
+  constexpr bool TC = (MODE == 1) && (sizeof(E) == 2);   // tensor-core scoring
+  {
+    const uint2 e0 = load_ent(0);
+    me[(lane >> 3) * 8 + (lane & 7)] = e0;
+    __syncwarp();
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      rows[r] = (base + r < cnt) ? Kb + (key0 + s_list[base + r]) * D : nullptr;
-    float s[G], m[G];
-    score8<D, G, E, true>(rows, qv, a.rs, s, m);
-    const int r = lane & 7;
-    if (lane < 8 && base + r < cnt) {
-      const int64_t key = key0 + s_list[base + r];
-      const unsigned qm = s_qm[base + r];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        if (qm & (1u << h)) {
-          cbm[h] = fmaxf(cbm[h], fsub(s[h], fmul(m[h], 1.220703125e-04f)));   // 2^-13
-          c3m[h] = fmaxf(c3m[h], s[h]);
-        }
-      }
-      if (key >= P) {
-        float* wp = a.win + ((int64_t)bg * kWindow + (key - P)) * G;
-#pragma unroll
-        for (int h = 0; h < G; ++h) wp[h] = s[h];
-      }
+    for (int k = 0; k < kRingS; ++k) {
+      if (TC) stage8_swz<D, E>(my + k * 8 * RB, Kb, me + k * 8, nvalid(wid + k * wstride));
+      else stage8<D, E>(my + k * 8 * RB, Kb, me + k * 8, nvalid(wid + k * wstride));
+      cp_async_commit();
     }
   }
+  // query fragments for the tensor-core path: M = heads (rows >= G zero),
+  // K = channels, two bf16 per register
+  constexpr int KS = D / 16;
+  unsigned qa[KS][2];
+  if (TC) {
+    const int gq = lane >> 2, tq = lane & 3;
+    const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                              ((int64_t)b * a.Hq + (int64_t)g * G + (gq < G ? gq : 0)) * D;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float x = warp_max(cbm[h]), y = warp_max(c3m[h]);
-    if (lane == 0) { s_cb[w][h] = x; s_c32[w][h] = y; }
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = gq < G ? *reinterpret_cast<const unsigned*>(qp + 16 * ks + 2 * tq) : 0u;
+      qa[ks][1] = gq < G ? *reinterpret_cast<const unsigned*>(qp + 16 * ks + 2 * tq + 8) : 0u;
+    }
   }
-  __syncthreads();
-  if (tid < G) {
-    float x = -INFINITY, y = -INFINITY;
-    for (int i = 0; i < 8; ++i) { x = fmaxf(x, s_cb[i][tid]); y = fmaxf(y, s_c32[i][tid]); }
-    if (x > -INFINITY) atomic_max_f(a.cmax + (int64_t)(bh0 + tid) * 4 + 2, x);
-    if (y > -INFINITY) atomic_max_f(a.cmax + (int64_t)(bh0 + tid) * 4 + 3, y);
+  uint2 pre = load_ent(1), pre2 = load_ent(2);
+  for (int it = 0;; ++it) {
+    const int bt = wid + it * wstride;
+    if (bt >= nbatch) break;
+    const int slot = it & (kRingS - 1);
+    cp_async_wait<kRingS - 1>();
+    __syncwarp();
+    const int nv = nvalid(bt);
+    if (TC) {
+      // scores of the stage's eight rows for all heads in one chain of
+      // m16n8k16 products; lane (g, t) gets head g, rows 2t and 2t+1
+      const int gq = lane >> 2, tq = lane & 3;
+      const uint8_t* st = my + slot * 8 * RB + gq * RB;      // row gq of the stage
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int c0 = 2 * ks, c1 = 2 * ks + 1;               // 16-byte chunks of channels 16ks..+15
+        const unsigned b0 = *reinterpret_cast<const unsigned*>(st + ((c0 ^ (gq & 7)) * 16) + 4 * tq);
+        const unsigned b1 = *reinterpret_cast<const unsigned*>(st + ((c1 ^ (gq & 7)) * 16) + 4 * tq);
+        const unsigned af[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+        mma_bf16_16816(acc, af, b0, b1);
+      }
+      if (gq < G) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int r = 2 * tq + u;
+          if (r < nv) {
+            const uint2 en = me[slot * 8 + r];
+            a.s32[((int64_t)bg * a.pcap + en.x) * G + gq] = ((en.y >> gq) & 1u) ? fmul(acc[u], a.rs) : -INFINITY;
+          }
+        }
+      }
+      __syncwarp();
+      if ((lane >> 3) == slot) me[slot * 8 + (lane & 7)] = pre;
+      __syncwarp();
+      stage8_swz<D, E>(my + slot * 8 * RB, Kb, me + slot * 8, nvalid(bt + kRingS * wstride));
+      cp_async_commit();
+      if (slot == kRingS - 1) { pre = pre2; pre2 = load_ent((it >> 2) + 3); }
+      continue;
+    }
+    float kv[8][CPL];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) load_row<D, E>(reinterpret_cast<const E*>(my + (slot * 8 + r) * RB), kv[r]);
+    float sc[G], mg[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float part[8], pm[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        float p[CPL], pa[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          p[c] = fmul(kv[r][c], qv[h][c]);
+          pa[c] = fabsf(p[c]);
+        }
+        part[r] = local_tree<CPL>(p);
+        if (MODE == 0) pm[r] = local_tree<CPL>(pa);
+      }
+      sc[h] = fmul(reduce8_rows(part), a.rs);
+      if (MODE == 0) mg[h] = fmul(reduce8_rows(pm), a.rs);
+    }
+    const int r = lane & 7;
+    if (lane < 8 && r < nv) {
+      const uint2 en = me[slot * 8 + r];
+      const int64_t key = en.x;
+      const unsigned cm = en.y;
+      if (MODE == 0) {
+        float* wp = key >= P ? a.win + ((int64_t)bg * kWindow + (key - P)) * G
+                             : a.s32 + ((int64_t)bg * a.pcap + key) * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          wp[h] = sc[h];
+          if ((cm >> h) & 1u) {
+            cbm[h] = fmaxf(cbm[h], fsub(sc[h], fmul(mg[h], 1.220703125e-04f)));   // 2^-13
+            c3m[h] = fmaxf(c3m[h], sc[h]);
+          }
+        }
+      } else {
+        float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h) sp[h] = ((cm >> h) & 1u) ? sc[h] : -INFINITY;
+      }
+    }
+    __syncwarp();
+    // refill this slot with the batch kRingS iterations ahead
+    if ((lane >> 3) == slot) me[slot * 8 + (lane & 7)] = pre;
+    __syncwarp();
+    stage8<D, E>(my + slot * 8 * RB, Kb, me + slot * 8, nvalid(bt + kRingS * wstride));
+    cp_async_commit();
+    if (slot == kRingS - 1) { pre = pre2; pre2 = load_ent((it >> 2) + 3); }
+  }
+  cp_async_wait<0>();
+  if (MODE == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float x = warp_max(cbm[h]), y = warp_max(c3m[h]);
+      if (lane == 0) { s_red[(w * G + h) * 2] = x; s_red[(w * G + h) * 2 + 1] = y; }
+    }
+    __syncthreads();
+    if (tid < G) {
+      float x = -INFINITY, y = -INFINITY;
+      for (int i = 0; i < kRingW; ++i) {
+        x = fmaxf(x, s_red[(i * G + tid) * 2]);
+        y = fmaxf(y, s_red[(i * G + tid) * 2 + 1]);
+      }
+      if (x > -INFINITY) atomic_max_f(a.cmax + (int64_t)(bh0 + tid) * 4 + 2, x);
+      if (y > -INFINITY) atomic_max_f(a.cmax + (int64_t)(bh0 + tid) * 4 + 3, y);
+    }
   }
 }
 
-// ------------------------------------------------- candidates + rescoring
+// ------------------------------------------------------------- candidates
 
-template <int D, int G, typename E>
-__global__ void __launch_bounds__(256) rescore_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
-  constexpr int CPL = D / 32;
-  __shared__ int s_list[kTile];
-  __shared__ unsigned s_cm[kTile];
-  __shared__ float s_t[kTile];
-  __shared__ int s_cnt;
+constexpr int kTilesPerCta = 16;   // key tiles per CTA of the per-key passes
+
+template <int G>
+__global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
   __shared__ unsigned s_jr[G][kMaxJ + 2];
   __shared__ unsigned s_nc[G];
-  __shared__ float s_pre[G][kMaxJ + 1][3];
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
   const int64_t P = n - kWindow;
-  const int64_t key0 = (int64_t)blockIdx.x * kTile;
-  if (key0 >= P) return;
+  const int64_t kbase = (int64_t)blockIdx.x * kTile * kTilesPerCta;
+  if (kbase >= P) return;
   const int J = seq.J[b];
   const float neg_r = -(float)a.r;
-  for (int i = tid; i < G * (kMaxJ + 2); i += 256) (&s_jr[0][0])[i] = 0u;
-  for (int i = tid; i < G * (J + 1) * 3; i += 256) {
-    int h = i / ((J + 1) * 3), rem = i - h * (J + 1) * 3;
-    s_pre[h][rem / 3][rem % 3] = 0.f;
-  }
+  for (int i = tid; i < G * (J + 2); i += 256) (&s_jr[0][0])[(i / (J + 2)) * (kMaxJ + 2) + i % (J + 2)] = 0u;
   if (tid < G) s_nc[tid] = 0u;
-  if (tid == 0) s_cnt = 0;
   __syncthreads();
   const int bh0 = b * a.Hq + g * G;
   const unsigned long long gk = group_key(seq.seed[b], g);
-  {
-    const int64_t key = key0 + tid;
-    unsigned cm = 0;
-    if (key < P) {
-      const float t = perturb_t(gk, key);
-      const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
+  for (int tile = 0; tile < kTilesPerCta; ++tile) {
+  const int64_t key0 = kbase + (int64_t)tile * kTile;
+  if (key0 >= P) break;
+  const int64_t key = key0 + tid;
+  const bool live = key < P;
+  unsigned cm = 0;
+  bool inset = false;
+  float t = 0.f;
+  float ub[G];
+  if (live) {
+    t = perturb_t(gk, key);
+    a.t32[(int64_t)bg * a.pcap + key] = t;
+    const float* up = a.ubar + ((int64_t)bg * a.n_max + key) * G;
+    if (G == 4) {
+      const float4 f = *reinterpret_cast<const float4*>(up);
+      ub[0] = f.x; ub[1 % G] = f.y; ub[2 % G] = f.z; ub[3 % G] = f.w;
+    } else {
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float u = ub[h];
-        const int jb = bound_level(u, cmax_get(a, bh0 + h, 2), t, neg_r, J);
-        const bool cand = jb <= J;
-        const bool inc = u >= cmax_get(a, bh0 + h, 0);
-        const int jr = inc ? 0 : (cand ? jb : J + 1);
-        atomicAdd(&s_jr[h][jr], 1u);
-        if (cand) { cm |= 1u << h; atomicAdd(&s_nc[h], 1u); }
-      }
-      if (cm) {
-        int p = atomicAdd(&s_cnt, 1);
-        s_list[p] = tid;
-        s_cm[p] = cm;
-        s_t[p] = t;
-      } else {
-        float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
-#pragma unroll
-        for (int h = 0; h < G; ++h) sp[h] = -INFINITY;
-      }
+      for (int h = 0; h < G; ++h) ub[h] = up[h];
     }
   }
-  __syncthreads();
-  const int cnt = s_cnt;
-  float qv[G][CPL];
-  {
-    const E* qp = reinterpret_cast<const E*>(a.q) + ((int64_t)b * a.Hq + (int64_t)g * G) * D;
 #pragma unroll
-    for (int h = 0; h < G; ++h) load_row<D, E>(qp + (int64_t)h * D, qv[h]);
-  }
-  float c32[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
-  const E* Kb = reinterpret_cast<const E*>(a.K) + (int64_t)bg * a.n_max * D;
-  for (int base = w * 8; base < cnt; base += 64) {
-    const E* rows[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-      rows[r] = (base + r < cnt) ? Kb + (key0 + s_list[base + r]) * D : nullptr;
-    float s[G], m[G];
-    score8<D, G, E, false>(rows, qv, a.rs, s, m);
-    const int r = lane & 7;
-    if (lane < 8 && base + r < cnt) {
-      const int64_t key = key0 + s_list[base + r];
-      const unsigned cm = s_cm[base + r];
-      const float t = s_t[base + r];
-      float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const bool c = cm & (1u << h);
-        sp[h] = c ? s[h] : -INFINITY;
-        if (c) {
-          int jl, hl;
-          exact_levels(s[h], c32[h], t, neg_r, J, jl, hl);
-          if (jl <= J) atomicAdd(&s_pre[h][jl][2], 1.0f);
-          if (jl < hl) {
-            atomicAdd(&s_pre[h][jl][0], 1.0f);
-            if (hl <= J) atomicAdd(&s_pre[h][hl][0], -1.0f);
-          }
-          if (hl <= J) atomicAdd(&s_pre[h][hl][1], expf(fsub(s[h], c32[h])));
-        }
-      }
+  for (int h = 0; h < G; ++h) {
+    int jr = -1;
+    if (live) {
+      const int jb = bound_level(ub[h], cmax_get(a, bh0 + h, 2), t, neg_r, J);
+      const bool cand = jb <= J;
+      const bool inc = ub[h] >= cmax_get(a, bh0 + h, 0);
+      inset |= inc;
+      jr = inc ? 0 : (cand ? jb : J + 1);
+      if (cand) cm |= 1u << h;
     }
+    hist_add_u(s_jr[h], jr, 1u);
+    const unsigned cb = __ballot_sync(0xffffffffu, (cm >> h) & 1u);
+    if (lane == 0 && cb) atomicAdd(&s_nc[h], (unsigned)__popc(cb));
+  }
+  float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
+  if (live && inset) {
+    // scored in the exact-max step: keep the candidate heads' scores
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      if (!((cm >> h) & 1u)) sp[h] = -INFINITY;
+  } else if (live && !cm) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) sp[h] = -INFINITY;
+  }
+  const int slot = warp_append(a.ccnt + bg, live && !inset && cm);
+  if (slot >= 0) a.clist[(int64_t)bg * a.pcap + slot] = make_uint2((unsigned)key, cm);
   }
   __syncthreads();
   for (int i = tid; i < G * (J + 2); i += 256) {
@@ -318,12 +486,74 @@ __global__ void __launch_bounds__(256) rescore_kernel(const SparseArgs a, const 
     unsigned v = s_jr[h][l];
     if (v) atomicAdd(a.jr_hist + (int64_t)(bh0 + h) * (a.J1 + 1) + l, v);
   }
-  for (int i = tid; i < G * (J + 1) * 3; i += 256) {
-    int h = i / ((J + 1) * 3), rem = i - h * (J + 1) * 3;
-    float v = s_pre[h][rem / 3][rem % 3];
-    if (v != 0.f) atomicAdd(a.pre_hist + ((int64_t)(bh0 + h) * a.J1 + rem / 3) * 4 + rem % 3, v);
-  }
   if (tid < G && s_nc[tid]) atomicAdd(a.ncand + bh0 + tid, s_nc[tid]);
+}
+
+// ------------------------------------------- value-free level histograms
+
+template <int G>
+__global__ void __launch_bounds__(256) prehist_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+  // counts as integers; heavy weights in 2^-24 fixed point (a prediction
+  // input only), all aggregated over equal levels within a warp
+  __shared__ int s_cnt[G][kMaxJ + 1][2];            // light count delta, sampled count
+  __shared__ float s_db[G][kMaxJ + 1];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int64_t n = seq.n[b];
+  if (n <= kWindow) return;
+  const int64_t P = n - kWindow;
+  const int64_t kbase = (int64_t)blockIdx.x * kTile * kTilesPerCta;
+  if (kbase >= P) return;
+  const int J = seq.J[b];
+  const float neg_r = -(float)a.r;
+  for (int i = tid; i < G * (J + 1); i += 256) {
+    const int h = i / (J + 1), l = i - h * (J + 1);
+    s_cnt[h][l][0] = 0; s_cnt[h][l][1] = 0; s_db[h][l] = 0.f;
+  }
+  __syncthreads();
+  const int bh0 = b * a.Hq + g * G;
+  float c32[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
+  for (int tile = 0; tile < kTilesPerCta; ++tile) {
+  const int64_t key0 = kbase + (int64_t)tile * kTile;
+  if (key0 >= P) break;
+  const int64_t key = key0 + tid;
+  float s[G];
+  float t = 0.f;
+  if (key < P) {
+    const float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
+    if (G == 4) {
+      const float4 f = *reinterpret_cast<const float4*>(sp);
+      s[0] = f.x; s[1 % G] = f.y; s[2 % G] = f.z; s[3 % G] = f.w;
+    } else {
+#pragma unroll
+      for (int h = 0; h < G; ++h) s[h] = sp[h];
+    }
+    t = a.t32[(int64_t)bg * a.pcap + key];
+  } else {
+#pragma unroll
+    for (int h = 0; h < G; ++h) s[h] = -INFINITY;
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    int jl = J + 1, hl = J + 1;
+    if (s[h] > -INFINITY) exact_levels(s[h], c32[h], t, neg_r, J, jl, hl);
+    int* cnt = &s_cnt[h][0][0];
+    hist_add_i(cnt + 1, jl <= J ? 2 * jl : -1, 1);                      // sampled at jl
+    hist_add_i(cnt, jl < hl ? 2 * jl : -1, 1);                          // light from jl
+    hist_add_i(cnt, (jl < hl && hl <= J) ? 2 * hl : -1, -1);            // light until hl
+    hist_add_f(s_db[h], hl <= J ? hl : -1, hl <= J ? __expf(s[h] - c32[h]) : 0.f);
+  }
+  }
+  __syncthreads();
+  for (int i = tid; i < G * (J + 1); i += 256) {
+    const int h = i / (J + 1), l = i - h * (J + 1);
+    float* dst = a.pre_hist + ((int64_t)(bh0 + h) * a.J1 + l) * 4;
+    if (s_cnt[h][l][0]) atomicAdd(dst + 0, (float)s_cnt[h][l][0]);
+    if (s_db[h][l] != 0.f) atomicAdd(dst + 1, s_db[h][l]);
+    if (s_cnt[h][l][1]) atomicAdd(dst + 2, (float)s_cnt[h][l][1]);
+  }
 }
 
 // -------------------------------------------- window sums + stop predictor
@@ -343,6 +573,7 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
     if (tid < G) {
       int* st = a.state + (int64_t)(bh0 + tid) * 4;
       st[0] = 0; st[1] = 0; st[2] = 0; st[3] = kFlagFallback | kFlagDone;
+      atomicAdd(a.nfall, 1u);
     }
     return;
   }
@@ -482,8 +713,7 @@ template <int G>
 __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
   __shared__ unsigned s_cnt[kMaxJ + 1];
   __shared__ unsigned s_base[kMaxJ + 1];
-  __shared__ int s_any;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
@@ -506,50 +736,80 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
   __syncthreads();
   const float neg_r = -(float)a.r;
   const int64_t key = key0 + tid;
-  int ev[2 * G], pos[2 * G];
-  int nev = 0;
+  int jl[G], hl[G];
+  bool some = false;
+#pragma unroll
+  for (int h = 0; h < G; ++h) { jl[h] = J + 1; hl[h] = J + 1; }
   if (key < P) {
     const float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
-    float s[G];
-    bool some = false;
+    float sv[G];
+    if (G == 4) {
+      const float4 f = *reinterpret_cast<const float4*>(sp);
+      sv[0] = f.x; sv[1 % G] = f.y; sv[2 % G] = f.z; sv[3 % G] = f.w;
+    } else {
 #pragma unroll
-    for (int h = 0; h < G; ++h) { s[h] = sp[h]; some |= s[h] > -INFINITY; }
-    if (some) {
-      const float t = perturb_t(group_key(seq.seed[b], g), key);
+      for (int h = 0; h < G; ++h) sv[h] = sp[h];
+    }
+    const float t = a.t32[(int64_t)bg * a.pcap + key];
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        if (!(s[h] > -INFINITY)) continue;
-        int jl, hl;
-        exact_levels(s[h], cmax_get(a, bh0 + h, 3), t, neg_r, J, jl, hl);
-        int c1 = (jl < hl && jl > lo[h] && jl <= hi[h]) ? jl : -1;
-        int c2 = (hl <= J && hl > lo[h] && hl <= hi[h]) ? hl : -1;
-        int cs[2] = {c1, c2};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          if (cs[e] < 0) continue;
-          bool dup = false;
-          for (int x = 0; x < nev; ++x) dup |= ev[x] == cs[e];
-          if (!dup) ev[nev++] = cs[e];
-        }
+    for (int h = 0; h < G; ++h) {
+      if (sv[h] > -INFINITY) {
+        exact_levels(sv[h], cmax_get(a, bh0 + h, 3), t, neg_r, J, jl[h], hl[h]);
+        some = true;
       }
     }
   }
-  for (int x = 0; x < nev; ++x) pos[x] = (int)atomicAdd(&s_cnt[ev[x]], 1u);
+  // event levels of this key in the round: a light entry at j (j < h) and
+  // the light-to-heavy transition at h, per head whose range holds them
+  int lv[2 * G], pos[2 * G];
+  unsigned mk[2 * G];
+  int nl = 0;
+  if (some) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const int c1 = (jl[h] < hl[h] && jl[h] > lo[h] && jl[h] <= hi[h]) ? jl[h] : -1;
+      const int c2 = (hl[h] <= J && hl[h] > lo[h] && hl[h] <= hi[h]) ? hl[h] : -1;
+      if (c1 >= 0) { bool dup = false; for (int x = 0; x < nl; ++x) dup |= lv[x] == c1; if (!dup) lv[nl++] = c1; }
+      if (c2 >= 0) { bool dup = false; for (int x = 0; x < nl; ++x) dup |= lv[x] == c2; if (!dup) lv[nl++] = c2; }
+    }
+  }
+  for (int x = 0; x < nl; ++x) {
+    const int l = lv[x];
+    unsigned m = 0;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      if (!(l > lo[h] && l <= hi[h])) continue;
+      if (jl[h] == l && jl[h] < hl[h]) m |= 1u << h;
+      if (hl[h] == l) {
+        m |= 1u << (8 + h);
+        if (jl[h] < hl[h]) m |= 1u << (16 + h);
+      }
+    }
+    mk[x] = m;
+  }
+  // shared-memory slots, aggregated over the warp's lanes with equal level
+  const int maxl = (int)__reduce_max_sync(0xffffffffu, (unsigned)nl);
+  for (int x = 0; x < maxl; ++x) {
+    const int l = x < nl ? lv[x] : -1;
+    const int p = slot_add(s_cnt, l);
+    if (l >= 0) pos[x] = p;
+  }
   __syncthreads();
   for (int i = tid; i <= J; i += 256)
     if (s_cnt[i]) s_base[i] = atomicAdd(a.bcnt + (int64_t)bg * a.J1 + i, s_cnt[i]);
   __syncthreads();
-  for (int x = 0; x < nev; ++x) {
-    const int l = ev[x];
+  for (int x = 0; x < nl; ++x) {
+    const int l = lv[x];
     const unsigned p = s_base[l] + (unsigned)pos[x];
     if (p < (unsigned)a.pcap)
-      a.buckets[((int64_t)bg * a.J1 + l) * a.pcap + p] = (unsigned)key;
+      a.buckets[((int64_t)bg * a.J1 + l) * a.pcap + p] = make_uint2((unsigned)key, mk[x]);
     else
       atomicOr(a.status, 2u);
   }
 }
 
-// One CTA: chunk list over the bucket entries appended since the last plan.
+// One CTA: work items (chunks of kChunk entries) over the bucket entries
+// appended since the last plan, and the chunk -> entry map.
 __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nent) {
   __shared__ unsigned s_part[1024];
   const int tid = threadIdx.x;
@@ -574,45 +834,68 @@ __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nen
   }
   unsigned run = s_part[tid] - sum;
   for (int i = i0; i < i1; ++i) {
+    const unsigned nch = (a.plan_end[i] - a.plan_start[i] + kChunk - 1) / kChunk;
     a.plan_off[i] = run;
-    run += (a.plan_end[i] - a.plan_start[i] + kChunk - 1) / kChunk;
+    for (unsigned k = 0; k < nch; ++k)
+      if (run + k < (unsigned)a.nchunk_cap) a.chunk_map[run + k] = (unsigned)i;
+    run += nch;
   }
-  if (tid == 1023) a.plan_off[nent] = s_part[1023];
+  if (tid == 1023) {
+    unsigned tot = s_part[1023];
+    a.plan_off[nent] = tot < (unsigned)a.nchunk_cap ? tot : (unsigned)a.nchunk_cap;
+  }
 }
 
 // ------------------------------------------------------------- V gather
+
+template <int D, int G, typename E>
+constexpr int vgather_smem() {
+  return kRingW * kRingS * 8 * D * (int)sizeof(E) + kRingW * kRingS * 8 * 16 + G * (2 * D + 8) * 4 +
+         kRingW * (kChunk / kRingW) * 8 + kRingW * kRingS * 8 * G * 4;
+}
 
 template <int D, int G, typename E>
 __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
                                                       int nent) {
   constexpr int CPL = D / 32;
   constexpr int ACC = 2 * D + 8;
-  __shared__ float s_acc[G][ACC];
+  constexpr int RB = D * (int)sizeof(E);
+  constexpr int EPW = kChunk / kRingW;          // events per warp per work item
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint8_t* ring = dsm;
+  float* s_sc = reinterpret_cast<float*>(dsm + kRingW * kRingS * 8 * RB);            // [W][S][8][4]
+  float (*s_acc)[ACC] = reinterpret_cast<float (*)[ACC]>(dsm + kRingW * kRingS * 8 * RB + kRingW * kRingS * 8 * 16);
+  uint2* s_ev = reinterpret_cast<uint2*>(dsm + kRingW * kRingS * 8 * RB + kRingW * kRingS * 8 * 16 + G * ACC * 4);
+  float* s_ww = reinterpret_cast<float*>(dsm + kRingW * kRingS * 8 * RB + kRingW * kRingS * 8 * 16 + G * ACC * 4 +
+                                         kRingW * EPW * 8);                       // [W][S][8][G]
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const unsigned total = a.plan_off[nent];
-  const float neg_r = -(float)a.r;
+  uint8_t* my = ring + w * kRingS * 8 * RB;
+  float* msc = s_sc + w * kRingS * 8 * 4;
+  uint2* mev = s_ev + w * EPW;
+  float* mww = s_ww + w * kRingS * 8 * G;
   for (unsigned c = blockIdx.x; c < total; c += gridDim.x) {
-    // find the (b, g, level) entry of chunk c
-    int lo_e = 0, hi_e = nent - 1;
-    while (lo_e < hi_e) {
-      int mid = (lo_e + hi_e + 1) >> 1;
-      if (a.plan_off[mid] <= c) lo_e = mid; else hi_e = mid - 1;
-    }
-    const int e = lo_e;
+    const int e = (int)a.chunk_map[c];
     const int bg = e / a.J1, l = e - bg * a.J1;
     const int b = bg / a.Hkv, g = bg - b * a.Hkv;
     const int bh0 = b * a.Hq + g * G;
-    const int J = seq.J[b];
     const unsigned ev0 = a.plan_start[e] + (c - a.plan_off[e]) * kChunk;
     const unsigned ev1 = min(a.plan_end[e], ev0 + kChunk);
-    unsigned hm = 0;
+    // this warp's batches of eight events: w, w + 8, w + 16, ... of the
+    // work item (balanced over the warps), loaded in one sweep
+    const int nev = (int)(ev1 - ev0);
+    const int nball = (nev + 7) / 8;
+    const int nmy = nball > w ? (nball - w + kRingW - 1) / kRingW : 0;   // batches of this warp
+    const uint2* bk = a.buckets + (int64_t)e * a.pcap + ev0;
+#pragma unroll
+    for (int i = lane; i < EPW; i += 32) {
+      const int k = i >> 3, r = i & 7;
+      const int idx = (w + k * kRingW) * 8 + r;
+      mev[i] = (k < nmy && idx < nev) ? bk[idx] : make_uint2(0u, 0u);
+    }
     float c32[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const int* st = a.state + (int64_t)(bh0 + h) * 4;
-      if (!(st[3] & kFlagDone) && l > st[0] && l <= st[1]) hm |= 1u << h;
-      c32[h] = cmax_get(a, bh0 + h, 3);
-    }
+    for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
     __syncthreads();
     for (int i = tid; i < G * ACC; i += 256) (&s_acc[0][0])[i] = 0.f;
     __syncthreads();
@@ -623,100 +906,335 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
 #pragma unroll
       for (int x = 0; x < CPL; ++x) { S1[h][x] = 0.f; NB[h][x] = 0.f; }
     }
-    const unsigned* bk = a.buckets + (int64_t)e * a.pcap;
+    unsigned hm = 0;
     const E* Vb = reinterpret_cast<const E*>(a.V) + (int64_t)bg * a.n_max * D;
     const float* sb = a.s32 + (int64_t)bg * a.pcap * G;
-    const unsigned long long gk = group_key(seq.seed[b], g);
-    for (unsigned base = ev0 + w * 32; base < ev1 && hm; base += 256) {
-      // lane-parallel per-event bookkeeping
-      const unsigned my = base + lane;
-      unsigned key = 0, msk = 0;
-      float wl[G];
+    const int nbatch = nmy;
+    // events in the warp's k-th batch
+    auto bcount = [&](int k) { return k < nmy ? min(8, nev - (w + k * kRingW) * 8) : 0; };
+    auto issue = [&](int slot, int bt) {
+      const int nv = bcount(bt);
+      stage8<D, E>(my + slot * 8 * RB, Vb, mev + bt * 8, nv);
+      // the G scores of each event (16-byte rows of s32 when G = 4)
+      if (lane < 8) {
+        const bool ok = lane < nv;
+        const float* src = ok ? sb + (int64_t)mev[bt * 8 + lane].x * G : sb;
+        if (G == 4) cp_async16(msc + (slot * 8 + lane) * 4, src, ok);
+      }
+      cp_async_commit();
+    };
 #pragma unroll
-      for (int h = 0; h < G; ++h) wl[h] = 0.f;
-      if (my < ev1) {
-        key = bk[my];
-        const float t = perturb_t(gk, key);
-        const float* sp = sb + (int64_t)key * G;
+    for (int sl = 0; sl < kRingS; ++sl) issue(sl, sl);
+    for (int bt = 0; bt < nbatch; ++bt) {
+      const int slot = bt & (kRingS - 1);
+      cp_async_wait<kRingS - 1>();
+      __syncwarp();
+      const int nv = bcount(bt);
+      // transition weights, one lane per event
+      if (lane < nv) {
+        const uint2 ev = mev[bt * 8 + lane];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          if (!(hm & (1u << h))) continue;
-          const float s = sp[h];
-          if (!(s > -INFINITY)) continue;
-          int jl, hl;
-          exact_levels(s, c32[h], t, neg_r, J, jl, hl);
-          const bool add = (jl == l) && (jl < hl);
-          const bool trn = (hl == l);
-          const bool bef = jl < hl;
-          if (add) { msk |= 1u << h; kc[h] += 1.f; }
+          float ww = 0.f;
+          if (ev.y & (1u << (8 + h))) {
+            const float sh = G == 4 ? msc[(slot * 8 + lane) * 4 + h] : sb[(int64_t)ev.x * G + h];
+            ww = expf(fsub(sh, c32[h]));
+          }
+          mww[(slot * 8 + lane) * G + h] = ww;
+        }
+      }
+      __syncwarp();
+      for (int r = 0; r < nv; ++r) {
+        const uint2 ev = mev[bt * 8 + r];
+        const unsigned m = ev.y;
+        hm |= m;
+        float v[CPL];
+        load_row<D, E>(reinterpret_cast<const E*>(my + (slot * 8 + r) * RB), v);
+        float sq = 0.f;
+#pragma unroll
+        for (int x = 0; x < CPL; ++x) sq += v[x] * v[x];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const bool add = m & (1u << h), trn = m & (1u << (8 + h)), bef = m & (1u << (16 + h));
+          if (add) {
+#pragma unroll
+            for (int x = 0; x < CPL; ++x) S1[h][x] += v[x];
+            s2[h] += sq;
+            kc[h] += 1.f;
+            ns[h] += 1.f;
+          }
           if (trn) {
-            msk |= 1u << (8 + h);
-            if (bef) { msk |= 1u << (16 + h); kc[h] -= 1.f; }
-            wl[h] = expf(fsub(s, c32[h]));
-            db[h] += wl[h];
-          }
-          if (jl == l) ns[h] += 1.f;
-        }
-      }
-      const int cntw = (int)min(32u, ev1 - base);
-      for (int j0 = 0; j0 < cntw; j0 += 4) {
-        float v[4][CPL];
-        unsigned mk[4];
-        float wv[4][G];
+            const float ww = mww[(slot * 8 + r) * G + h];
+            if (bef) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = j0 + u;
-          const unsigned kk = __shfl_sync(0xffffffffu, key, j & 31);
-          mk[u] = __shfl_sync(0xffffffffu, msk, j & 31);
-#pragma unroll
-          for (int h = 0; h < G; ++h) wv[u][h] = __shfl_sync(0xffffffffu, wl[h], j & 31);
-          if (j < cntw && mk[u]) load_row<D, E>(Vb + (int64_t)kk * D, v[u]);
-          else {
-            mk[u] = 0;
-#pragma unroll
-            for (int x = 0; x < CPL; ++x) v[u][x] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (!mk[u]) continue;
-          float sq = 0.f;
-#pragma unroll
-          for (int x = 0; x < CPL; ++x) sq += v[u][x] * v[u][x];
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            if (mk[u] & (1u << h)) {
-#pragma unroll
-              for (int x = 0; x < CPL; ++x) S1[h][x] += v[u][x];
-              s2[h] += sq;
+              for (int x = 0; x < CPL; ++x) S1[h][x] -= v[x];
+              s2[h] -= sq;
+              kc[h] -= 1.f;
+            } else {
+              ns[h] += 1.f;
             }
-            if (mk[u] & (1u << (8 + h))) {
-              if (mk[u] & (1u << (16 + h))) {
 #pragma unroll
-                for (int x = 0; x < CPL; ++x) S1[h][x] -= v[u][x];
-                s2[h] -= sq;
-              }
-              const float ww = wv[u][h];
-#pragma unroll
-              for (int x = 0; x < CPL; ++x) NB[h][x] += ww * v[u][x];
-              hb[h] += ww * sq;
-            }
+            for (int x = 0; x < CPL; ++x) NB[h][x] += ww * v[x];
+            hb[h] += ww * sq;
+            db[h] += ww;
           }
         }
       }
+      __syncwarp();
+      issue(slot, bt + kRingS);
     }
-    // fold the warp's sums into the CTA, then into the per-level sums
+    cp_async_wait<0>();
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      if (!(hm & (1u << h))) continue;
+      if (!(hm & (0x101u << h))) continue;
 #pragma unroll
       for (int x = 0; x < CPL; ++x) {
         atomicAdd(&s_acc[h][lane * CPL + x], S1[h][x]);
         atomicAdd(&s_acc[h][D + lane * CPL + x], NB[h][x]);
       }
+      const float s2_ = warp_sum(s2[h]), hb_ = warp_sum(hb[h]);
+      if (lane == 0) {
+        // counts and weights are the same in every lane
+        atomicAdd(&s_acc[h][2 * D + 0], kc[h]);
+        atomicAdd(&s_acc[h][2 * D + 1], s2_);
+        atomicAdd(&s_acc[h][2 * D + 2], db[h]);
+        atomicAdd(&s_acc[h][2 * D + 3], hb_);
+        atomicAdd(&s_acc[h][2 * D + 4], ns[h]);
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < G * ACC; i += 256) {
+      const int h = i / ACC, x = i - h * ACC;
+      if (x >= 2 * D + 5) continue;
+      const float v = s_acc[h][x];
+      if (v != 0.f) atomicAdd(a.acc + ((int64_t)(bh0 + h) * a.J1 + l) * ACC + x, v);
+    }
+  }
+}
+
+// Tensor-core V gather (bf16 caches).  Per batch of 16 events of one
+// level, with Vb the 16 x d block of their value rows:
+//   C += A_hi Vb + A_lo Vb,  C rows 0..G-1 = per-head light sums
+//   (coefficient +1 on a light entry, -1 when a light key turns heavy),
+//   rows G..2G-1 = per-head heavy sums (coefficient w, split as
+//   bf16(w) + bf16(w - bf16(w)) so the product stays float32-accurate).
+constexpr int kVgW = 4;                        // warps per CTA
+constexpr int kVgS = 4;                        // ring stages per warp
+constexpr int kVgB = 16;                       // events per batch (mma k)
+constexpr int kVgEPW = kChunk / kVgW;          // events per warp per item
+
+template <int D, int G>
+constexpr int vgather_tc_smem() {
+  return kVgW * kVgS * kVgB * D * 2 +                    // value rows
+         kVgW * kVgS * kVgB * 16 +                       // staged scores (G = 4)
+         kVgW * kVgEPW * 8 +                             // events
+         kVgW * kVgB * G * 4 * 2 +                       // per-event coefficients, weights
+         G * (2 * D + 8) * 4;                            // CTA sums
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(unsigned (&r)[4], const void* p) {
+  unsigned sa = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(sa));
+}
+__device__ __forceinline__ unsigned pack_bf16(float lo, float hi) {
+  const unsigned a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const unsigned b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return a | (b << 16);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(128) vgather_tc_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+                                                         int nent) {
+  constexpr int RB = D * 2;
+  constexpr int NT = D / 8;                     // n-tiles of 8 channels
+  constexpr int ACC = 2 * D + 8;
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint8_t* ring = dsm;
+  float* s_sc = reinterpret_cast<float*>(dsm + kVgW * kVgS * kVgB * RB);
+  uint2* s_ev = reinterpret_cast<uint2*>(dsm + kVgW * kVgS * kVgB * RB + kVgW * kVgS * kVgB * 16);
+  float* s_cf = reinterpret_cast<float*>(dsm + kVgW * kVgS * kVgB * RB + kVgW * kVgS * kVgB * 16 +
+                                         kVgW * kVgEPW * 8);
+  float (*s_acc)[ACC] = reinterpret_cast<float (*)[ACC]>(dsm + kVgW * kVgS * kVgB * RB + kVgW * kVgS * kVgB * 16 +
+                                                          kVgW * kVgEPW * 8 + kVgW * kVgB * G * 4 * 2);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int gq = lane >> 2, tq = lane & 3;
+  const unsigned total = a.plan_off[nent];
+  uint8_t* my = ring + w * kVgS * kVgB * RB;
+  float* msc = s_sc + w * kVgS * kVgB * 4;
+  uint2* mev = s_ev + w * kVgEPW;
+  float* mcf = s_cf + w * kVgB * G * 2;          // [16 events][G] coefficient, then [16][G] weight
+  for (unsigned c = blockIdx.x; c < total; c += gridDim.x) {
+    const int e = (int)a.chunk_map[c];
+    const int bg = e / a.J1, l = e - bg * a.J1;
+    const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+    const int bh0 = b * a.Hq + g * G;
+    const unsigned ev0 = a.plan_start[e] + (c - a.plan_off[e]) * kChunk;
+    const unsigned ev1 = min(a.plan_end[e], ev0 + kChunk);
+    const int nev = (int)(ev1 - ev0);
+    const int nball = (nev + kVgB - 1) / kVgB;
+    const int nmy = nball > w ? (nball - w + kVgW - 1) / kVgW : 0;
+    const uint2* bk = a.buckets + (int64_t)e * a.pcap + ev0;
+    for (int i = lane; i < kVgEPW; i += 32) {
+      const int k = i / kVgB, r = i % kVgB;
+      const int idx = (w + k * kVgW) * kVgB + r;
+      mev[i] = (k < nmy && idx < nev) ? bk[idx] : make_uint2(0u, 0u);
+    }
+    float c32[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
+    __syncthreads();
+    for (int i = tid; i < G * ACC; i += 128) (&s_acc[0][0])[i] = 0.f;
+    __syncthreads();
+    float C[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) { C[j][0] = C[j][1] = C[j][2] = C[j][3] = 0.f; }
+    float s2[G], hb[G], kc[G], db[G], ns[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) s2[h] = hb[h] = kc[h] = db[h] = ns[h] = 0.f;
+    unsigned hm = 0;
+    const __nv_bfloat16* Vb = reinterpret_cast<const __nv_bfloat16*>(a.V) + (int64_t)bg * a.n_max * D;
+    const float* sb = a.s32 + (int64_t)bg * a.pcap * G;
+    auto bcount = [&](int k) { return k < nmy ? min(kVgB, nev - (w + k * kVgW) * kVgB) : 0; };
+    auto issue = [&](int slot, int k) {
+      const int nv = bcount(k);
+      uint8_t* dst = my + slot * kVgB * RB;
+      constexpr int CH = RB / 16;
+#pragma unroll
+      for (int cc = lane; cc < kVgB * CH; cc += 32) {
+        const int r = cc / CH, part = cc - r * CH;
+        const bool ok = r < nv;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(Vb) + (ok ? (int64_t)mev[k * kVgB + r].x * RB + part * 16 : 0);
+        cp_async16(dst + r * RB + ((part ^ (r & 7)) * 16), src, ok);
+      }
+      if (G == 4 && lane < kVgB) {
+        const bool ok = lane < nv;
+        const float* src = ok ? sb + (int64_t)mev[k * kVgB + lane].x * 4 : sb;
+        cp_async16(msc + (slot * kVgB + lane) * 4, src, ok);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int sl = 0; sl < kVgS; ++sl) issue(sl, sl);
+    for (int k = 0; k < nmy; ++k) {
+      const int slot = k & (kVgS - 1);
+      cp_async_wait<kVgS - 1>();
+      __syncwarp();
+      const int nv = bcount(k);
+      const uint8_t* stg = my + slot * kVgB * RB;
+      // squared norms of the 16 value rows (lane partials, reduce-scatter)
+      float part[kVgB];
+#pragma unroll
+      for (int r = 0; r < kVgB; ++r) {
+        constexpr int CPL = D / 32;
+        const int byte = lane * CPL * 2;                         // this lane's channels
+        const uint8_t* row = stg + r * RB + (((byte >> 4) ^ (r & 7)) << 4) + (byte & 15);
+        float v0, v1, v2 = 0.f, v3 = 0.f;
+        if (CPL == 4) {
+          const uint2 u = *reinterpret_cast<const uint2*>(row);
+          v0 = __uint_as_float(u.x << 16); v1 = __uint_as_float(u.x & 0xFFFF0000u);
+          v2 = __uint_as_float(u.y << 16); v3 = __uint_as_float(u.y & 0xFFFF0000u);
+        } else {
+          const unsigned u = *reinterpret_cast<const unsigned*>(row);
+          v0 = __uint_as_float(u << 16); v1 = __uint_as_float(u & 0xFFFF0000u);
+        }
+        part[r] = v0 * v0 + v1 * v1 + v2 * v2 + v3 * v3;
+      }
+#pragma unroll
+      for (int st = 0, cnt = kVgB / 2; st < 4; ++st, cnt >>= 1) {
+        const int o = 1 << st;
+        const bool hi = lane & o;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i < cnt) {
+            const float send = hi ? part[2 * i] : part[2 * i + 1];
+            const float keep = hi ? part[2 * i + 1] : part[2 * i];
+            part[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+      }
+      const float nrm2 = part[0] + __shfl_xor_sync(0xffffffffu, part[0], 16);   // event lane & 15
+      // one lane per event: masks, weights, scalar sums, coefficients
+      if (lane < kVgB) {
+        const bool ok = lane < nv;
+        const uint2 ev = ok ? mev[k * kVgB + lane] : make_uint2(0u, 0u);
+        const unsigned m = ev.y;
+        hm |= m;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const bool add = m & (1u << h), trn = m & (1u << (8 + h)), bef = m & (1u << (16 + h));
+          float wt = 0.f;
+          if (trn) {
+            const float sh = G == 4 ? msc[(slot * kVgB + lane) * 4 + h] : sb[(int64_t)ev.x * G + h];
+            wt = expf(fsub(sh, c32[h]));
+          }
+          const float cf = add ? 1.f : ((trn && bef) ? -1.f : 0.f);
+          mcf[lane * G + h] = cf;
+          mcf[kVgB * G + lane * G + h] = wt;
+          kc[h] += cf;
+          s2[h] += cf * nrm2;
+          db[h] += wt;
+          hb[h] += wt * nrm2;
+          ns[h] += (add || (trn && !bef)) ? 1.f : 0.f;
+        }
+      }
+      __syncwarp();
+      // A fragments: rows g and g + 8, events 2t, 2t+1 and 2t+8, 2t+9
+      auto coef = [&](int row, int ev, bool lo) -> float {
+        if (row < G) return lo ? 0.f : mcf[ev * G + row];
+        if (row < 2 * G) {
+          const float wt = mcf[kVgB * G + ev * G + (row - G)];
+          const float hi = __bfloat162float(__float2bfloat16_rn(wt));
+          return lo ? wt - hi : hi;
+        }
+        return 0.f;
+      };
+      unsigned ah[4], al[4];
+      {
+        const int r0 = gq, r1 = gq + 8, e0 = 2 * tq, e1 = 2 * tq + 8;
+        ah[0] = pack_bf16(coef(r0, e0, false), coef(r0, e0 + 1, false));
+        ah[1] = pack_bf16(coef(r1, e0, false), coef(r1, e0 + 1, false));
+        ah[2] = pack_bf16(coef(r0, e1, false), coef(r0, e1 + 1, false));
+        ah[3] = pack_bf16(coef(r1, e1, false), coef(r1, e1 + 1, false));
+        al[0] = pack_bf16(coef(r0, e0, true), coef(r0, e0 + 1, true));
+        al[1] = pack_bf16(coef(r1, e0, true), coef(r1, e0 + 1, true));
+        al[2] = pack_bf16(coef(r0, e1, true), coef(r0, e1 + 1, true));
+        al[3] = pack_bf16(coef(r1, e1, true), coef(r1, e1 + 1, true));
+      }
+      // B fragments: value rows transposed, two n-tiles per ldmatrix.x4
+      const int mi = lane >> 3, rr = lane & 7;                  // matrix, row within it
+#pragma unroll
+      for (int jp = 0; jp < NT / 2; ++jp) {
+        const int ev = (mi & 1) * 8 + rr;                         // event (matrix row)
+        const int chunk = 2 * jp + (mi >> 1);                     // 16-byte channel chunk
+        unsigned bfr[4];
+        ldsm_x4_trans(bfr, stg + ev * RB + ((chunk ^ (ev & 7)) << 4));
+        mma_bf16_16816(C[2 * jp], ah, bfr[0], bfr[1]);
+        mma_bf16_16816(C[2 * jp], al, bfr[0], bfr[1]);
+        mma_bf16_16816(C[2 * jp + 1], ah, bfr[2], bfr[3]);
+        mma_bf16_16816(C[2 * jp + 1], al, bfr[2], bfr[3]);
+      }
+      __syncwarp();
+      issue(slot, k + kVgS);
+    }
+    cp_async_wait<0>();
+    // C rows -> per-head light sums (rows < G) and heavy sums (G..2G-1)
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = gq + (u >> 1) * 8;
+        const int ch = 8 * j + 2 * tq + (u & 1);
+        if (row < G) atomicAdd(&s_acc[row][ch], C[j][u]);
+        else if (row < 2 * G) atomicAdd(&s_acc[row - G][D + ch], C[j][u]);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
       const float k_ = warp_sum(kc[h]), s2_ = warp_sum(s2[h]), db_ = warp_sum(db[h]);
       const float hb_ = warp_sum(hb[h]), ns_ = warp_sum(ns[h]);
-      if (lane == 0) {
+      if (lane == 0 && (k_ != 0.f || ns_ != 0.f || db_ != 0.f)) {
         atomicAdd(&s_acc[h][2 * D + 0], k_);
         atomicAdd(&s_acc[h][2 * D + 1], s2_);
         atomicAdd(&s_acc[h][2 * D + 2], db_);
@@ -725,9 +1243,9 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
       }
     }
     __syncthreads();
-    for (int i = tid; i < G * ACC; i += 256) {
+    for (int i = tid; i < G * ACC; i += 128) {
       const int h = i / ACC, x = i - h * ACC;
-      if (!(hm & (1u << h)) || x >= 2 * D + 5) continue;
+      if (x >= 2 * D + 5) continue;
       const float v = s_acc[h][x];
       if (v != 0.f) atomicAdd(a.acc + ((int64_t)(bh0 + h) * a.J1 + l) * ACC + x, v);
     }
@@ -744,6 +1262,7 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
   constexpr int LB = 32;                   // levels per shared-memory batch
   __shared__ float s_pre[LB][ACC];
   __shared__ float s_run[ACC];
+  __shared__ float s_vec[LB][4];           // ||c||^2, ||o_hat - c||^2, c.S1, ||o_hat||^2
   __shared__ float s_beta[LB], s_dh[LB];
   __shared__ int s_cert[LB];
   __shared__ float s_win[D + 4];
@@ -761,7 +1280,7 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       const int64_t n = seq.n[b];
       a.beta[bh] = 0.f; a.level[bh] = 0; a.keys_read[bh] = (int)n;
       if (a.stats) {
-        csa_head_stats hs = {0, (int)n, (int)n, 0, 0, 0, 1, 0};
+        csa_head_stats hs = {0, (int)n, (int)n, 0, 0, 0, 1, (int)n, (int)n, 0};
         a.stats[bh] = hs;
       }
     }
@@ -771,7 +1290,6 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
   const int J = seq.J[b];
   const int lo = st[0], hi = st[1];
   for (int i = tid; i < D + 4; i += 256) s_win[i] = a.winstats[(int64_t)bh * (D + 4) + i];
-  for (int x = tid; x < ACC; x += 256) s_run[x] = 0.f;
   __syncthreads();
   const float DR = s_win[D], HR = s_win[D + 1];
   const float Vp = a.vmaxp[bg];
@@ -779,7 +1297,6 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
   const float L = logf(1.0f / de), Lz = logf(2.0f / de);
   const float* accb = a.acc + (int64_t)bh * a.J1 * ACC;
   int found = -1;
-  // prefix up to lo (levels already known not to certify)
   for (int x = tid; x < ACC; x += 256) {
     float run = 0.f;
     for (int l = 0; l <= lo; ++l) run += accb[(int64_t)l * ACC + x];
@@ -797,11 +1314,12 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       s_run[x] = run;
     }
     __syncthreads();
+    // vector parts, one warp per level
     for (int i = w; i < nl; i += 8) {
       const int j = l0 + i;
       const float tau = exp2f(-(float)j / (float)a.r);
       const float* p = s_pre[i];
-      const float k = p[2 * D], S2 = p[2 * D + 1], DB = p[2 * D + 2], HB = p[2 * D + 3];
+      const float k = p[2 * D], DB = p[2 * D + 2];
       const float DRB = DR + DB;
       const float Dh = DRB + tau * k;
       float cc = 0.f, oc = 0.f, cs1 = 0.f, oo = 0.f;
@@ -817,37 +1335,47 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
         oo += oh * oh;
       }
       cc = warp_sum(cc); oc = warp_sum(oc); cs1 = warp_sum(cs1); oo = warp_sum(oo);
-      if (lane == 0) {
-        float below, above;
-        chernoff_gaps(k, Lz, below, above);
-        const float dD = tau * fmaxf(below, above);
-        const float cn = sqrtf(cc);
-        const float Rc = Vp + cn;
-        const float Gh = tau * fmaxf(S2 - 2.f * cs1 + k * cc, 0.f);
-        const float aa = sqrtf(2.f * tau * Rc * Rc * L);
-        const float sq = sqrtf(aa * aa + 4.f * (Gh + (2.f / 3.f) * tau * Rc * Rc * L));
-        const float Ghi = 0.25f * (aa + sq) * (aa + sq);
-        const float zeta = sqrtf(2.f * tau * Ghi * Lz) + (2.f / 3.f) * tau * Rc * Lz;
-        const bool pos = Dh > dD;
-        const float beta = pos ? (zeta + sqrtf(oc) * dD) / (Dh - dD) : INFINITY;
-        bool cert;
-        if (a.measure == CSA_MEASURE_VALUE) {
-          const float Hh = tau * S2;
-          const float ap = sqrtf(2.f * tau * Vp * Vp * L);
-          const float br = Hh - (2.f / 3.f) * tau * Vp * Vp * L;
-          const float t2 = br > 0.f ? 0.5f * (-ap + sqrtf(ap * ap + 4.f * br)) : 0.f;
-          const float Dhi = DRB + tau * (k + above);
-          const float Mlo = sqrtf((HR + HB + t2 * t2) / Dhi);
-          cert = pos && beta <= a.eps * Mlo;
-        } else if (a.measure == CSA_MEASURE_OUTPUT) {
-          cert = pos && beta * (1.f + a.eps) <= a.eps * sqrtf(oo);
-        } else {
-          cert = pos && dD <= a.eps * (Dh - dD);
-        }
-        s_cert[i] = cert;
-        s_beta[i] = beta;
-        s_dh[i] = Dh;
+      if (lane == 0) { s_vec[i][0] = cc; s_vec[i][1] = oc; s_vec[i][2] = cs1; s_vec[i][3] = oo; }
+    }
+    __syncthreads();
+    // scalar parts, one thread per level
+    if (tid < nl) {
+      const int i = tid, j = l0 + i;
+      const float tau = exp2f(-(float)j / (float)a.r);
+      const float* p = s_pre[i];
+      const float k = p[2 * D], S2 = p[2 * D + 1], DB = p[2 * D + 2], HB = p[2 * D + 3];
+      const float DRB = DR + DB;
+      const float Dh = DRB + tau * k;
+      const float cc = s_vec[i][0], oc = s_vec[i][1], cs1 = s_vec[i][2], oo = s_vec[i][3];
+      float below, above;
+      chernoff_gaps(k, Lz, below, above);
+      const float dD = tau * fmaxf(below, above);
+      const float cn = sqrtf(cc);
+      const float Rc = Vp + cn;
+      const float Gh = tau * fmaxf(S2 - 2.f * cs1 + k * cc, 0.f);
+      const float aa = sqrtf(2.f * tau * Rc * Rc * L);
+      const float sq = sqrtf(aa * aa + 4.f * (Gh + (2.f / 3.f) * tau * Rc * Rc * L));
+      const float Ghi = 0.25f * (aa + sq) * (aa + sq);
+      const float zeta = sqrtf(2.f * tau * Ghi * Lz) + (2.f / 3.f) * tau * Rc * Lz;
+      const bool pos = Dh > dD;
+      const float beta = pos ? (zeta + sqrtf(oc) * dD) / (Dh - dD) : INFINITY;
+      bool cert;
+      if (a.measure == CSA_MEASURE_VALUE) {
+        const float Hh = tau * S2;
+        const float ap = sqrtf(2.f * tau * Vp * Vp * L);
+        const float br = Hh - (2.f / 3.f) * tau * Vp * Vp * L;
+        const float t2 = br > 0.f ? 0.5f * (-ap + sqrtf(ap * ap + 4.f * br)) : 0.f;
+        const float Dhi = DRB + tau * (k + above);
+        const float Mlo = sqrtf((HR + HB + t2 * t2) / Dhi);
+        cert = pos && beta <= a.eps * Mlo;
+      } else if (a.measure == CSA_MEASURE_OUTPUT) {
+        cert = pos && beta * (1.f + a.eps) <= a.eps * sqrtf(oo);
+      } else {
+        cert = pos && dD <= a.eps * (Dh - dD);
       }
+      s_cert[i] = cert;
+      s_beta[i] = beta;
+      s_dh[i] = Dh;
     }
     __syncthreads();
     for (int i = 0; i < nl; ++i)
@@ -869,7 +1397,8 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
         st[2] = found;
         st[3] = flags | kFlagDone;
         if (a.stats) {
-          csa_head_stats hs = {found, kWindow + (int)kr, vr, (int)a.ncand[bh], 0, J, round + 1, 0};
+          csa_head_stats hs = {found, kWindow + (int)kr, vr, (int)a.ncand[bh], 0, J, round + 1,
+                               kWindow, kWindow, 0};
           a.stats[bh] = hs;
         }
       }
@@ -884,13 +1413,13 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       a.keys_read[bh] = (int)n;
       st[2] = J + 1;
       st[3] = flags | kFlagDone | kFlagFallback;
+      atomicAdd(a.nfall, 1u);
       if (a.stats) {
-        csa_head_stats hs = {J + 1, (int)n, (int)n, (int)a.ncand[bh], 0, J, round + 1, 0};
+        csa_head_stats hs = {J + 1, (int)n, (int)n, (int)a.ncand[bh], 0, J, round + 1, kWindow, kWindow, 0};
         a.stats[bh] = hs;
       }
     } else {
       int nh = (round == 0) ? hi + 2 * a.r : J;
-      if (round >= 1) nh = J;
       st[0] = hi;
       st[1] = nh > J ? J : nh;
     }
@@ -906,21 +1435,44 @@ __global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __g
   if (n <= kWindow || !a.stats) return;
   const int64_t P = n - kWindow;
   const int64_t key = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  if (key >= P) return;
+  const int lane = threadIdx.x & 31;
   const int bh0 = b * a.Hq + g * G;
-  const float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
-  const float t = perturb_t(group_key(seq.seed[b], g), key);
+  const int J = seq.J[b];
+  const float neg_r = -(float)a.r;
+  bool needK = false, needV = false;
+  if (key < P) {
+    const float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
+    const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
+    const float t = a.t32[(int64_t)bg * a.pcap + key];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const int js = a.state[(int64_t)(bh0 + h) * 4 + 2];
-    if (js < 0 || js > seq.J[b]) continue;
-    const float s = sp[h];
-    if (!(s > -INFINITY)) continue;
-    const float dl = fsub(s, cmax_get(a, bh0 + h, 3));
-    const float thr = -((float)js / (float)a.r) * 0.69314718f;
-    const float x = dl + t * 0.69314718f;
-    if (fabsf(x - thr) < 1e-5f || fabsf(dl - thr) < 1e-5f)
-      atomicAdd(&a.stats[bh0 + h].n_near_threshold, 1);
+    for (int h = 0; h < G; ++h) {
+      const int js = a.state[(int64_t)(bh0 + h) * 4 + 2];
+      if (js > J) { needK = needV = true; continue; }   // exact fallback
+      if (js < 0) continue;
+      const float u = ub[h];
+      const int jb = bound_level(u, cmax_get(a, bh0 + h, 2), t, neg_r, J);
+      if (u >= cmax_get(a, bh0 + h, 0) || jb <= js) needK = true;
+      const float s = sp[h];
+      if (!(s > -INFINITY)) continue;
+      int jl, hl;
+      exact_levels(s, cmax_get(a, bh0 + h, 3), t, neg_r, J, jl, hl);
+      if (jl <= js) needV = true;
+      // keys within 1e-5 nats of the light or heavy threshold at the stop
+      const float dl = fsub(s, cmax_get(a, bh0 + h, 3));
+      const float thr = -((float)js / (float)a.r) * 0.69314718f;
+      const float x = dl + t * 0.69314718f;
+      if (fabsf(x - thr) < 1e-5f || fabsf(dl - thr) < 1e-5f)
+        atomicAdd(&a.stats[bh0 + h].n_near_threshold, 1);
+    }
+  }
+  const int ck = __popc(__ballot_sync(0xffffffffu, needK));
+  const int cv = __popc(__ballot_sync(0xffffffffu, needV));
+  if (lane == 0 && (ck || cv)) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      if (ck) atomicAdd(&a.stats[bh0 + h].group_keys_read, ck);
+      if (cv) atomicAdd(&a.stats[bh0 + h].group_values_read, cv);
+    }
   }
 }
 
@@ -947,16 +1499,78 @@ __global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __g
     default: return cudaErrorInvalidValue;                                                       \
   }
 
+#define CSA_G_SWITCH(FN, ...)                                                                    \
+  switch (G) {                                                                                   \
+    case 1: FN<1> __VA_ARGS__; break;                                                            \
+    case 2: FN<2> __VA_ARGS__; break;                                                            \
+    case 4: FN<4> __VA_ARGS__; break;                                                            \
+    case 8: FN<8> __VA_ARGS__; break;                                                            \
+    default: return cudaErrorInvalidValue;                                                       \
+  }
+
+template <int D, int G, typename E, int MODE>
+void launch_rows_t(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
+  constexpr int smem = rows_smem<D, G, E>();
+  static bool set = false;
+  if (!set) {
+    cudaFuncSetAttribute(rows_kernel<D, G, E, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    set = true;
+  }
+  rows_kernel<D, G, E, MODE><<<grid, 256, smem, st>>>(a, seq);
+}
+template <int D, int G, typename E>
+void launch_rows0(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
+  launch_rows_t<D, G, E, 0>(grid, st, a, seq);
+}
+template <int D, int G, typename E>
+void launch_rows1(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
+  launch_rows_t<D, G, E, 1>(grid, st, a, seq);
+}
+template <int D, int G, typename E>
+void launch_vgather_t(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int nent) {
+  if (sizeof(E) == 2) {
+    constexpr int smem = vgather_tc_smem<D, G>();
+    static bool set = false;
+    if (!set) {
+      cudaFuncSetAttribute(vgather_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      set = true;
+    }
+    vgather_tc_kernel<D, G><<<dim3(grid.x * 2), 128, smem, st>>>(a, seq, nent);
+    return;
+  }
+  constexpr int smem = vgather_smem<D, G, E>();
+  static bool set = false;
+  if (!set) {
+    cudaFuncSetAttribute(vgather_kernel<D, G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    set = true;
+  }
+  vgather_kernel<D, G, E><<<grid, 256, smem, st>>>(a, seq, nent);
+}
+
+static dim3 rows_grid(const SparseArgs& a, int64_t items, int nsm) {
+  int per = (4 * nsm + a.B * a.Hkv - 1) / (a.B * a.Hkv);
+  int cap = (int)((items + 8 * kRingW - 1) / (8 * kRingW));
+  per = per < 1 ? 1 : (per > cap ? cap : per);
+  if (per < 1) per = 1;
+  return dim3((unsigned)per, (unsigned)(a.B * a.Hkv));
+}
+
 cudaError_t launch_cstar(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t nmax_live,
-                         cudaStream_t st) {
-  dim3 grid((unsigned)((nmax_live + kTile - 1) / kTile), (unsigned)(a.B * a.Hkv));
-  CSA_DG_SWITCH(cstar_kernel, <<<grid, 256, 0, st>>>(a, seq))
+                         int nsm, cudaStream_t st) {
+  dim3 grid((unsigned)((nmax_live + 255) / 256), (unsigned)(a.B * a.Hkv));
+  CSA_G_SWITCH(cset_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  CSA_DG_SWITCH(launch_rows0, (rows_grid(a, nmax_live, nsm), st, a, seq))
   return cudaGetLastError();
 }
 cudaError_t launch_rescore(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16,
-                           int64_t pmax_live, cudaStream_t st) {
-  dim3 grid((unsigned)((pmax_live + kTile - 1) / kTile), (unsigned)(a.B * a.Hkv));
-  CSA_DG_SWITCH(rescore_kernel, <<<grid, 256, 0, st>>>(a, seq))
+                           int64_t pmax_live, int nsm, cudaStream_t st, void (*mark)(int, cudaStream_t)) {
+  const int64_t span = (int64_t)kTile * kTilesPerCta;
+  dim3 grid((unsigned)((pmax_live + span - 1) / span), (unsigned)(a.B * a.Hkv));
+  CSA_G_SWITCH(cand_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  if (mark) mark(3, st);
+  CSA_DG_SWITCH(launch_rows1, (rows_grid(a, pmax_live, nsm), st, a, seq))
+  if (mark) mark(4, st);
+  CSA_G_SWITCH(prehist_kernel, <<<grid, 256, 0, st>>>(a, seq))
   return cudaGetLastError();
 }
 cudaError_t launch_predict(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, cudaStream_t st) {
@@ -965,33 +1579,24 @@ cudaError_t launch_predict(const SparseArgs& a, const SeqArgs& seq, int d, int G
   return cudaGetLastError();
 }
 cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t pmax_live,
-                         int round, int nsm, cudaStream_t st) {
+                         int round, int nsm, cudaStream_t st, PhaseMark mark) {
   dim3 grid((unsigned)((pmax_live + kTile - 1) / kTile), (unsigned)(a.B * a.Hkv));
-  switch (G) {
-    case 1: levels_kernel<1><<<grid, 256, 0, st>>>(a, seq); break;
-    case 2: levels_kernel<2><<<grid, 256, 0, st>>>(a, seq); break;
-    case 4: levels_kernel<4><<<grid, 256, 0, st>>>(a, seq); break;
-    case 8: levels_kernel<8><<<grid, 256, 0, st>>>(a, seq); break;
-    default: return cudaErrorInvalidValue;
-  }
+  CSA_G_SWITCH(levels_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  if (mark) mark(6, st);
   const int nent = a.B * a.Hkv * a.J1;
   vplan_kernel<<<1, 1024, 0, st>>>(a, nent);
-  dim3 vg((unsigned)(nsm * 4));
-  CSA_DG_SWITCH(vgather_kernel, <<<vg, 256, 0, st>>>(a, seq, nent))
+  if (mark) mark(7, st);
+  CSA_DG_SWITCH(launch_vgather_t, (dim3((unsigned)(nsm * 2)), st, a, seq, nent))
+  if (mark) mark(8, st);
   dim3 cg((unsigned)(a.B * a.Hq));
   if (d == 128) certify_kernel<128><<<cg, 256, 0, st>>>(a, seq, round);
   else certify_kernel<64><<<cg, 256, 0, st>>>(a, seq, round);
+  if (mark) mark(9, st);
   return cudaGetLastError();
 }
 cudaError_t launch_near(const SparseArgs& a, const SeqArgs& seq, int G, int64_t pmax_live, cudaStream_t st) {
   dim3 grid((unsigned)((pmax_live + 255) / 256), (unsigned)(a.B * a.Hkv));
-  switch (G) {
-    case 1: near_kernel<1><<<grid, 256, 0, st>>>(a, seq); break;
-    case 2: near_kernel<2><<<grid, 256, 0, st>>>(a, seq); break;
-    case 4: near_kernel<4><<<grid, 256, 0, st>>>(a, seq); break;
-    case 8: near_kernel<8><<<grid, 256, 0, st>>>(a, seq); break;
-    default: return cudaErrorInvalidValue;
-  }
+  CSA_G_SWITCH(near_kernel, <<<grid, 256, 0, st>>>(a, seq))
   return cudaGetLastError();
 }
 

@@ -96,6 +96,10 @@ typedef struct {
   int32_t n_near_threshold; /* keys within 1e-5 nats of a threshold at j*   */
   int32_t J;                /* last grid level of this sequence             */
   int32_t rounds;           /* gather rounds the head needed (1..3)         */
+  int32_t group_keys_read;  /* 64 + |union over the head's GQA group of the */
+                            /* pool rows counted in keys_read| (one bf16 K  */
+                            /* row load serves the whole group)             */
+  int32_t group_values_read;/* the same union for values_read              */
   int32_t reserved;
 } csa_head_stats;
 
@@ -169,6 +173,26 @@ typedef struct {
 csa_status csa_workspace_layout(const csa_shape* shape,
                                 const csa_params* params,
                                 csa_workspace_map* out);
+
+/* Phase timing (tracing).  When enabled, csa_decode_step records a CUDA
+ * event at every phase boundary on its stream; csa_profile_read waits for
+ * the recorded events and returns the accumulated milliseconds per phase
+ * since the previous read (then resets).  Up to 64 steps are buffered;
+ * older ones are dropped.  `launches` counts the library's kernel launches
+ * (profiling on or off) since the previous read.  Not thread-safe.
+ * Phases: 0 workspace clear, 1 scan, 2 exact max, 3 candidates,
+ * 4 rescoring of candidate K rows, 5 predictor + window, 6 level buckets,
+ * 7 gather plan, 8 V gather, 9 certificate, 10 exact fallback,
+ * 11 diagnostics, 12 value-free level histograms. */
+#define CSA_NPHASE 13
+typedef struct {
+  float ms[CSA_NPHASE];
+  int32_t steps;
+  int64_t launches;
+} csa_phase_times;
+
+csa_status csa_profile_enable(int on);
+csa_status csa_profile_read(csa_phase_times* out);
 
 /* Synchronises `stream`, then returns the device status word recorded in
  * `workspace` by the last csa_decode_step that used it (CSA_OK, or

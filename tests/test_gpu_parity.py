@@ -115,6 +115,7 @@ def _compare_group(run, w, K, V, q, b, g, res, p, report):
     J = res.J
     Vd = V[b, g, :n].astype(np.float64)
     t = perturb_t(run.seeds[b], g, np.arange(P))
+    needK, needV = set(), set()
     for h in range(w.G):
         hq = g * w.G + h
         det = res.detail[h]
@@ -175,6 +176,18 @@ def _compare_group(run, w, K, V, q, b, g, res, p, report):
         assert err <= TOL * np.linalg.norm(o_ref) + 1e-6, (b, g, h, err)
         report["heads"] += 1
         report["levels"].append(gl)
+        # rows the head needs, for the group unions
+        if gl <= J:
+            needK.update(np.union1d(det["cset"],
+                                    np.nonzero(det["jbar"] <= gl)[0]).tolist())
+            needV.update(np.nonzero(jr <= gl)[0].tolist())
+        else:
+            needK.update(range(P))
+            needV.update(range(P))
+    for h in range(w.G):
+        hq = g * w.G + h
+        assert stats[b, hq, 7] == 64 + len(needK)
+        assert stats[b, hq, 8] == 64 + len(needV)
 
 
 def _run_and_compare(w, K, V, q, lens, seeds, n_alloc, **pover):

@@ -29,7 +29,10 @@ BLOCK = 64
 EXPORTED = ("csa_workspace_size", "csa_quantize_keys", "csa_decode_step",
             "csa_dense_workspace_size", "csa_dense_decode", "csa_check",
             "csa_status_string", "csa_workspace_layout",
-            "csa_profile_enable", "csa_profile_read")
+            "csa_profile_enable", "csa_profile_read",
+            "csa_dense_decode_static")
+# size of the fixed scratch array behind csa_dense_decode_static
+DENSE_STATIC_SCRATCH_BYTES = 16 << 20
 STATS_FIELDS = 10
 STAT = {"level": 0, "keys_read": 1, "values_read": 2, "n_candidates": 3,
         "n_near_threshold": 4, "J": 5, "rounds": 6, "group_keys_read": 7,
@@ -114,6 +117,9 @@ def load_library(path: str = LIB_PATH):
     lib.csa_dense_decode.argtypes = [P(csa_shape), vp, vp, vp,
                                      P(ctypes.c_int64), vp, vp, sz, vp]
     lib.csa_dense_decode.restype = ctypes.c_int
+    lib.csa_dense_decode_static.argtypes = [P(csa_shape), vp, vp, vp,
+                                            P(ctypes.c_int64), vp, vp]
+    lib.csa_dense_decode_static.restype = ctypes.c_int
     lib.csa_check.argtypes = [vp, vp]
     lib.csa_check.restype = ctypes.c_int
     lib.csa_workspace_layout.argtypes = [P(csa_shape), P(csa_params),
@@ -224,6 +230,12 @@ def csa_dense_decode(shape, q, K, V, lens, o, workspace, workspace_bytes,
     return load_library().csa_dense_decode(
         ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V), _i64(lens), _ptr(o),
         _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def csa_dense_decode_static(shape, q, K, V, lens, o, stream=None) -> int:
+    return load_library().csa_dense_decode_static(
+        ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V), _i64(lens), _ptr(o),
+        _stream(stream))
 
 
 def csa_profile_enable(on: bool) -> int:

@@ -143,6 +143,9 @@ void prof_mark(int phase, cudaStream_t st) {
 void count_launches(int k) { g_prof.launches += k; }
 
 }  // namespace
+
+void add_launches(int k) { count_launches(k); }
+
 }  // namespace csa
 
 using namespace csa;

@@ -104,5 +104,6 @@ cudaError_t launch_dense(const DenseArgs&, const SeqArgs&, int d, int G, bool bf
 cudaError_t launch_quant(const QuantArgs&, const SeqArgs&, int B, int d, bool bf16, int64_t nblocks,
                          cudaStream_t);
 int dense_nsplit(int64_t n_max);
+void add_launches(int k);   // adds to the launch count csa_profile_read reports
 
 }  // namespace csa

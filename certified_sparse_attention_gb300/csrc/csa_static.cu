@@ -1,0 +1,89 @@
+// Dense decode attention with its split-K partials in a fixed, file-scope
+// device array instead of a caller-supplied workspace: the library's one
+// entry point that needs no device allocation by anyone.  It exists for
+// callers that cannot allocate device memory at the point of the call: a
+// plain C host program that links only this library and owns no device
+// allocator, or a callback that runs while another component holds all of
+// the device memory and its allocator's lock.  The kernels are the same two
+// launches csa_dense_decode makes; only where the partials live differs.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "csa_args.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)CSA_DENSE_STATIC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+// Split-K partials, [nsplit][B*Hq][d+2] floats.  Every slot the combine
+// kernel reads is written by the split kernel of the same call first, so the
+// contents on entry do not matter and nothing has to start at zero.  One
+// array per device, shared by every call on that device: two calls whose
+// kernels overlap in time (different streams, or host threads) race on it.
+static __device__ __align__(256) unsigned char g_dense_scratch[kStaticScratchBytes];
+
+std::mutex g_addr_mu;
+void* g_addr[kMaxDevices] = {};
+
+// Device address of g_dense_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+csa_status scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return CSA_ERR_CUDA;
+  if (dev >= kMaxDevices) return CSA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_addr_mu);
+  if (!g_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dense_scratch) != cudaSuccess || !p) return CSA_ERR_CUDA;
+    g_addr[dev] = p;
+  }
+  *out = g_addr[dev];
+  return CSA_OK;
+}
+
+}  // namespace
+}  // namespace csa
+
+using namespace csa;
+
+extern "C" {
+
+csa_status csa_dense_decode_static(const csa_shape* shape, const void* q, const void* K, const void* V,
+                                   const int64_t* len, float* o, void* stream) {
+  if (!shape || !q || !K || !V || !len || !o) return CSA_ERR_INVALID_ARG;
+  const size_t need = csa_dense_workspace_size(shape);
+  if (need == 0) {
+    // invalid or unsupported shape: report which, as csa_dense_decode does
+    const bool valid = shape->B >= 1 && shape->Hq >= 1 && shape->Hkv >= 1 && shape->Hq % shape->Hkv == 0 &&
+                       shape->n_max >= 1 && shape->n_max <= (int64_t)1 << 31 &&
+                       (shape->dtype == CSA_BF16 || shape->dtype == CSA_F32);
+    return valid ? CSA_ERR_UNSUPPORTED : CSA_ERR_INVALID_ARG;
+  }
+  if (need > kStaticScratchBytes) return CSA_ERR_WORKSPACE;
+  SeqArgs seq;
+  std::memset(&seq, 0, sizeof(seq));
+  int64_t nlive = 0;
+  for (int b = 0; b < shape->B; ++b) {
+    if (len[b] < 1 || len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
+    seq.n[b] = len[b];
+    if (len[b] > nlive) nlive = len[b];
+  }
+  void* scratch = nullptr;
+  const csa_status sa = scratch_address(&scratch);
+  if (sa != CSA_OK) return sa;
+  DenseArgs a;
+  a.q = q; a.K = K; a.V = V; a.part = (float*)scratch; a.o = o; a.state = nullptr; a.nfall = nullptr;
+  a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max;
+  a.nsplit = dense_nsplit(shape->n_max); a.rs = (float)(1.0 / std::sqrt((double)shape->d));
+  add_launches(2);
+  return launch_dense(a, seq, shape->d, shape->Hq / shape->Hkv, shape->dtype == CSA_BF16, nlive,
+                      (cudaStream_t)stream) == cudaSuccess
+             ? CSA_OK
+             : CSA_ERR_CUDA;
+}
+
+}  // extern "C"

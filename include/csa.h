@@ -17,7 +17,8 @@
  *  - Pointers named as device memory are device pointers owned by the
  *    caller; the library allocates no device memory at all.  Scratch space
  *    is the caller's `workspace` buffer (size from csa_workspace_size /
- *    csa_dense_workspace_size).
+ *    csa_dense_workspace_size), except for csa_dense_decode_static, which
+ *    uses a fixed array compiled into the library.
  *  - Host arrays (len, step_seed) are read before the call returns.
  *  - Work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
  *    stream); outputs are valid once the stream has synchronised.  The call
@@ -153,6 +154,35 @@ csa_status csa_dense_decode(const csa_shape* shape, const void* q,
                             const void* K, const void* V, const int64_t* len,
                             float* o, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/* Dense decode attention with no workspace argument and no allocation by
+ * anyone.  The paper has no counterpart to this entry point: it is a
+ * deployment variant of csa_dense_decode for callers that cannot allocate
+ * device memory where they call it -- a plain C host program that links only
+ * this library and owns no device allocator, or a callback that runs while
+ * another component holds the device memory and its allocator.
+ *
+ * Same operation, arguments, layouts and results as csa_dense_decode (the
+ * same two kernels run); the split-K partials live in a file-scope device
+ * array of CSA_DENSE_STATIC_SCRATCH_BYTES (16 MiB) per device instead.
+ *  - The shape needs csa_dense_workspace_size(shape) bytes of scratch; a
+ *    shape that needs more than CSA_DENSE_STATIC_SCRATCH_BYTES returns
+ *    CSA_ERR_WORKSPACE before anything is enqueued (16 MiB holds, e.g.,
+ *    B = 4, Hq = 32, d = 128 up to n_max = 258,048).
+ *  - The array's contents on entry do not matter: every partial the combine
+ *    step reads is written earlier in the same call.
+ *  - All calls on one device share the array.  Calls whose work overlaps in
+ *    time (different streams, or several host threads) race on it and give
+ *    wrong results; serialise them (one stream, or events between streams).
+ *  - The first call on each device looks up the array's device address with
+ *    that device current (cudaGetSymbolAddress; the address is cached per
+ *    device).  Make that first call before any stream capture starts.  A
+ *    failed lookup returns CSA_ERR_CUDA.
+ * Other errors as csa_dense_decode. */
+#define CSA_DENSE_STATIC_SCRATCH_BYTES (16u << 20)
+csa_status csa_dense_decode_static(const csa_shape* shape, const void* q,
+                                   const void* K, const void* V,
+                                   const int64_t* len, float* o, void* stream);
 
 /* Where csa_decode_step keeps its intermediate arrays inside the workspace
  * (byte offsets), for diagnostics and parity tests.  Valid after the step's

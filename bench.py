@@ -183,13 +183,12 @@ def setup_layers(w, layers, device, csa):
     data = []
     for lid in layers:
         K, V, meta = synth.kv_torch(w, layer=lid, device=device)
-        K4, bounds, vmax = csa.meta_buffers(shape, device)
-        csa.check(csa.csa_quantize_keys(shape, K, V, [w.n] * w.B, 0, K4,
-                                        bounds, vmax), "csa_quantize_keys")
+        mt = csa.meta_buffers(shape, device)
+        csa.check(csa.csa_quantize_keys(shape, K, V, [w.n] * w.B, 0, *mt),
+                  "csa_quantize_keys")
         qs = [synth.q_torch(w, meta, s, layer=lid, device=device)
               for s in range(4)]
-        data.append({"K": K, "V": V, "K4": K4, "bounds": bounds,
-                     "vmax": vmax, "q": qs, "lid": lid})
+        data.append({"K": K, "V": V, "meta": mt, "q": qs, "lid": lid})
     torch.cuda.synchronize()
     return shape, data
 
@@ -227,8 +226,8 @@ def run_ours(args, world, rank, local):
 
     def one(s, L):
         d = data[L]
-        step(d["q"][s % 4], d["K"], d["V"], d["K4"], d["bounds"], d["vmax"],
-             lens, seed_tab[L][s % nseed], stream)
+        step(d["q"][s % 4], d["K"], d["V"], d["meta"], lens,
+             seed_tab[L][s % nseed], stream)
 
     for s in range(args.warmup):
         one(s, s % args.layers)
@@ -279,8 +278,8 @@ def run_ours(args, world, rank, local):
     abs_ = []
     for L in range(args.layers):
         d = data[L]
-        step_diag(d["q"][L % 4], d["K"], d["V"], d["K4"], d["bounds"],
-                  d["vmax"], lens, seed_tab[L][L % nseed], stream)
+        step_diag(d["q"][L % 4], d["K"], d["V"], d["meta"], lens,
+                  seed_tab[L][L % nseed], stream)
         torch.cuda.synchronize()
         stats = step_diag.stats.cpu().numpy()
         abs_.append(algorithmic_bytes(stats, w, w.n))
@@ -329,10 +328,9 @@ def run_ours(args, world, rank, local):
         d = data[L]
         qd.copy_(qh, non_blocking=True)
         csa.check(csa.csa_quantize_keys(shape, d["K"], d["V"], lens,
-                                        w.n - 1, d["K4"], d["bounds"],
-                                        d["vmax"], stream))
-        step(qd, d["K"], d["V"], d["K4"], d["bounds"], d["vmax"], lens,
-             seed_tab[L][s % nseed], stream)
+                                        w.n - 1, *d["meta"], stream))
+        step(qd, d["K"], d["V"], d["meta"], lens, seed_tab[L][s % nseed],
+             stream)
         oh.copy_(step.o, non_blocking=True)
         bh.copy_(step.beta, non_blocking=True)
         lh.copy_(step.level, non_blocking=True)

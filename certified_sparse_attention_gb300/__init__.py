@@ -15,7 +15,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Optional, Sequence
+from typing import NamedTuple, Optional, Sequence
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libcsa.so")
@@ -78,7 +78,8 @@ class csa_head_stats(ctypes.Structure):
 class csa_workspace_map(ctypes.Structure):
     _fields_ = [("ubar", ctypes.c_size_t), ("cmax", ctypes.c_size_t),
                 ("s32", ctypes.c_size_t), ("jr_hist", ctypes.c_size_t),
-                ("total", ctypes.c_size_t), ("J1", ctypes.c_int32),
+                ("bcnt", ctypes.c_size_t), ("total", ctypes.c_size_t),
+                ("J1", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
 
 
@@ -107,10 +108,10 @@ def load_library(path: str = LIB_PATH):
     lib.csa_dense_workspace_size.argtypes = [P(csa_shape)]
     lib.csa_dense_workspace_size.restype = sz
     lib.csa_quantize_keys.argtypes = [P(csa_shape), vp, vp, P(ctypes.c_int64),
-                                      ctypes.c_int64, vp, vp, vp, vp]
+                                      ctypes.c_int64, vp, vp, vp, vp, vp]
     lib.csa_quantize_keys.restype = ctypes.c_int
     lib.csa_decode_step.argtypes = [P(csa_shape), P(csa_params), vp, vp, vp,
-                                    vp, vp, vp, P(ctypes.c_int64),
+                                    vp, vp, vp, vp, P(ctypes.c_int64),
                                     P(ctypes.c_uint64), vp, vp, vp, vp, vp,
                                     vp, sz, vp]
     lib.csa_decode_step.restype = ctypes.c_int
@@ -209,18 +210,19 @@ def decode_ordered(u):
 
 
 def csa_quantize_keys(shape, K, V, lens, from_token, K4, bounds, vmax,
-                      stream=None) -> int:
+                      vnorm2, stream=None) -> int:
     return load_library().csa_quantize_keys(
         ctypes.byref(shape), _ptr(K), _ptr(V), _i64(lens), int(from_token),
-        _ptr(K4), _ptr(bounds), _ptr(vmax), _stream(stream))
+        _ptr(K4), _ptr(bounds), _ptr(vmax), _ptr(vnorm2), _stream(stream))
 
 
-def csa_decode_step(shape, params, q, K, V, K4, bounds, vmax, lens, seeds,
-                    o, beta, level, keys_read, stats, workspace,
+def csa_decode_step(shape, params, q, K, V, K4, bounds, vmax, vnorm2, lens,
+                    seeds, o, beta, level, keys_read, stats, workspace,
                     workspace_bytes, stream=None) -> int:
     return load_library().csa_decode_step(
         ctypes.byref(shape), ctypes.byref(params), _ptr(q), _ptr(K), _ptr(V),
-        _ptr(K4), _ptr(bounds), _ptr(vmax), _i64(lens), _u64(seeds), _ptr(o),
+        _ptr(K4), _ptr(bounds), _ptr(vmax), _ptr(vnorm2), _i64(lens),
+        _u64(seeds), _ptr(o),
         _ptr(beta), _ptr(level), _ptr(keys_read), _ptr(stats),
         _ptr(workspace), int(workspace_bytes), _stream(stream))
 
@@ -262,8 +264,16 @@ def check(status: int, where: str = "csa") -> None:
 
 # ---------------------------------------------------- tensor conveniences
 
-def meta_buffers(shape: csa_shape, device):
-    """Allocate K4, bounds, vmax (torch, device) for a shape."""
+class KVMeta(NamedTuple):
+    """Device metadata csa_quantize_keys writes and csa_decode_step reads."""
+    K4: object
+    bounds: object
+    vmax: object
+    vnorm2: object
+
+
+def meta_buffers(shape: csa_shape, device) -> KVMeta:
+    """Allocate K4, bounds, vmax, vnorm2 (torch, device) for a shape."""
     import torch
     nblk = (shape.n_max + BLOCK - 1) // BLOCK
     K4 = torch.zeros((shape.B, shape.Hkv, nblk * BLOCK, shape.d // 2),
@@ -272,7 +282,9 @@ def meta_buffers(shape: csa_shape, device):
                          dtype=torch.float32, device=device)
     vmax = torch.zeros((shape.B, shape.Hkv, nblk), dtype=torch.float32,
                        device=device)
-    return K4, bounds, vmax
+    vnorm2 = torch.zeros((shape.B, shape.Hkv, shape.n_max),
+                         dtype=torch.float32, device=device)
+    return KVMeta(K4, bounds, vmax, vnorm2)
 
 
 class DecodeStep:
@@ -298,9 +310,10 @@ class DecodeStep:
         self.stats = (torch.zeros((B, Hq, STATS_FIELDS), dtype=torch.int32,
                                   device=device) if with_stats else None)
 
-    def __call__(self, q, K, V, K4, bounds, vmax, lens, seeds, stream=None):
-        st = csa_decode_step(self.shape, self.params, q, K, V, K4, bounds,
-                             vmax, lens, seeds, self.o, self.beta,
+    def __call__(self, q, K, V, meta: KVMeta, lens, seeds, stream=None):
+        st = csa_decode_step(self.shape, self.params, q, K, V, meta.K4,
+                             meta.bounds, meta.vmax, meta.vnorm2, lens, seeds,
+                             self.o, self.beta,
                              self.level, self.keys_read, self.stats, self.ws,
                              self.ws_bytes, stream)
         check(st, "csa_decode_step")

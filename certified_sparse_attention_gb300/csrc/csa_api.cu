@@ -187,6 +187,7 @@ csa_status csa_workspace_layout(const csa_shape* shape, const csa_params* params
   out->cmax = L.cmax;
   out->s32 = L.s32;
   out->jr_hist = L.jr_hist;
+  out->bcnt = L.bcnt;
   out->total = L.total;
   out->J1 = L.J1;
   out->reserved = 0;
@@ -194,8 +195,9 @@ csa_status csa_workspace_layout(const csa_shape* shape, const csa_params* params
 }
 
 csa_status csa_quantize_keys(const csa_shape* shape, const void* K, const void* V, const int64_t* len,
-                             int64_t from_token, uint8_t* K4, float* bounds, float* vmax, void* stream) {
-  if (!shape_ok(shape) || !K || !V || !len || !K4 || !bounds || !vmax || from_token < 0)
+                             int64_t from_token, uint8_t* K4, float* bounds, float* vmax, float* vnorm2,
+                             void* stream) {
+  if (!shape_ok(shape) || !K || !V || !len || !K4 || !bounds || !vmax || !vnorm2 || from_token < 0)
     return CSA_ERR_INVALID_ARG;
   csa_status su = shape_supported(shape);
   if (su != CSA_OK) return su;
@@ -210,7 +212,7 @@ csa_status csa_quantize_keys(const csa_shape* shape, const void* K, const void* 
     if (nb > nblocks) nblocks = nb;
   }
   QuantArgs a;
-  a.K = K; a.V = V; a.K4 = K4; a.bounds = bounds; a.vmax = vmax; a.Hkv = shape->Hkv;
+  a.K = K; a.V = V; a.K4 = K4; a.bounds = bounds; a.vmax = vmax; a.vnorm2 = vnorm2; a.Hkv = shape->Hkv;
   a.n_max = shape->n_max; a.nblk_max = (shape->n_max + kBlock - 1) / kBlock; a.blk_from = blk_from;
   if (nblocks > 0) count_launches(1);
   return cuda_status(launch_quant(a, seq, shape->B, shape->d, shape->dtype == CSA_BF16, nblocks,
@@ -244,10 +246,11 @@ csa_status csa_dense_decode(const csa_shape* shape, const void* q, const void* K
 
 csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
                            const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
+                           const float* vnorm2,
                            const int64_t* len, const uint64_t* step_seed, float* o, float* beta,
                            int32_t* level, int32_t* keys_read, csa_head_stats* stats, void* workspace,
                            size_t workspace_bytes, void* stream) {
-  if (!shape_ok(shape) || !params_ok(params) || !q || !K || !V || !K4 || !bounds || !vmax || !len ||
+  if (!shape_ok(shape) || !params_ok(params) || !q || !K || !V || !K4 || !bounds || !vmax || !vnorm2 || !len ||
       !step_seed || !o || !beta || !level || !keys_read)
     return CSA_ERR_INVALID_ARG;
   csa_status su = shape_supported(shape);
@@ -287,7 +290,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   prof_mark(1, st);
 
   SparseArgs a;
-  a.q = q; a.K = K; a.V = V; a.vmax = vmax; a.ubar = (const float*)(ws + L.ubar);
+  a.q = q; a.K = K; a.V = V; a.vmax = vmax; a.vnorm2 = vnorm2; a.ubar = (const float*)(ws + L.ubar);
   a.s32 = (float*)(ws + L.s32); a.win = (float*)(ws + L.win); a.cmax = (unsigned*)(ws + L.cmax);
   a.jr_hist = (unsigned*)(ws + L.jr_hist); a.ncand = (unsigned*)(ws + L.ncand);
   a.pre_hist = (float*)(ws + L.pre_hist); a.acc = (float*)(ws + L.acc); a.winstats = (float*)(ws + L.winstats);

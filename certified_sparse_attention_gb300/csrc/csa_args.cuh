@@ -23,6 +23,7 @@ struct SparseArgs {
   const void* K;
   const void* V;
   const float* vmax;      // [B*Hkv][nblk_max]
+  const float* vnorm2;    // [B*Hkv][n_max]        ||v_i||^2 per token
   const float* ubar;      // [B*Hkv][n_max][G]
   float* s32;             // [B*Hkv][pcap][G]     candidate scores (-inf: not a candidate)
   float* win;             // [B*Hkv][64][G]       window scores
@@ -83,6 +84,7 @@ struct QuantArgs {
   uint8_t* K4;
   float* bounds;
   float* vmax;
+  float* vnorm2;
   int Hkv;
   int64_t n_max, nblk_max;
   int64_t blk_from;

@@ -7,7 +7,8 @@
 //   code = clamp(rint(fl(fl(k - m_c) / Delta_c)), 0, 15)   (ties to even),
 // two codes per byte with the even channel in the low nibble.  vmax of the
 // block = max over its tokens of sqrt(sequential float32 sum of v_c^2),
-// times (1 + 2^-16), an upper bound on every ||v_i|| of the block.
+// times (1 + 2^-16), an upper bound on every ||v_i|| of the block; the sums
+// themselves are kept per token (vnorm2) for the value gather.
 // One CTA per (sequence, KV head, block); thread c owns channel c.
 #include "csa_args.cuh"
 
@@ -50,9 +51,8 @@ __global__ void __launch_bounds__(D) quant_kernel(const QuantArgs a, const __gri
   }
   // value norms: thread t < rows walks its row sequentially
   if (c < kBlock) {
-    float nrm = 0.0f;
+    float nrm = 0.0f, ss = 0.0f;
     if (c < rows) {
-      float ss = 0.0f;
       for (int x = 0; x < D; ++x) {
         const float v = Elem<E>::get(Vb, (int64_t)c * D + x);
         ss = fadd(ss, fmul(v, v));
@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(D) quant_kernel(const QuantArgs a, const __gri
       nrm = __fsqrt_rn(ss);
     }
     s_vm[c] = nrm;
+    if (t0 + c < a.n_max) a.vnorm2[(int64_t)bg * a.n_max + t0 + c] = ss;
   }
   __syncthreads();
   if (c == 0) {

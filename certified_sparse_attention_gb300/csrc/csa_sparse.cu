@@ -646,8 +646,12 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
     const float de = a.delta / (4.0f * (float)(J + 1));
     const float L = logf(1.0f / de), Lz = logf(2.0f / de);
     const float Rc = Vp + cn;
+    // pred: first level the value-free certificate passes; spred: first
+    // level it passes with the error target halved.  Round 1 gathers up to
+    // spred, at most (r + 1) / 2 levels beyond pred.
+    const int margin = (a.r + 1) / 2;
     float runk = 0.f, rundb = 0.f;
-    int pred = J;
+    int pred = -1, spred = -1;
     for (int l0 = 0; l0 <= J; l0 += 32) {
       const int j = l0 + lane;
       float dk = 0.f, ddb = 0.f;
@@ -665,7 +669,7 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
       k += runk; db += rundb;
       runk = __shfl_sync(0xffffffffu, k, 31);
       rundb = __shfl_sync(0xffffffffu, db, 31);
-      bool pass = false;
+      bool pass = false, spass = false;
       if (j <= J) {
         const float tau = exp2f(-(float)j / (float)a.r);
         float below, above;
@@ -674,6 +678,7 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
         const float Dh = DR + db + tau * k;
         if (a.measure == CSA_MEASURE_DENOM) {
           pass = Dh > dD && dD <= a.eps * (Dh - dD);
+          spass = Dh > dD && dD <= 0.5f * a.eps * (Dh - dD);
         } else {
           const float Gh = tau * k * fmaxf(nu - cn2, 0.f);
           const float aa = sqrtf(2.f * tau * Rc * Rc * L);
@@ -690,16 +695,24 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
             const float Mlo = sqrtf((HR + db * nu + t2 * t2) / (DR + db + tau * (k + above)));
             scale = Mlo;
             pass = Dh > dD && beta <= a.eps * scale;
+            spass = Dh > dD && beta <= 0.5f * a.eps * scale;
           } else {
             pass = Dh > dD && beta * (1.f + a.eps) <= a.eps * cn;
+            spass = Dh > dD && beta * (1.f + 0.5f * a.eps) <= 0.5f * a.eps * cn;
           }
         }
       }
-      unsigned bal = __ballot_sync(0xffffffffu, pass);
-      if (bal) { pred = l0 + __ffs(bal) - 1; break; }
+      const unsigned bal = __ballot_sync(0xffffffffu, pass);
+      const unsigned sbal = __ballot_sync(0xffffffffu, spass);
+      if (pred < 0 && bal) pred = l0 + __ffs(bal) - 1;
+      if (spred < 0 && sbal) spred = l0 + __ffs(sbal) - 1;
+      if (spred >= 0 || (pred >= 0 && l0 + 31 >= pred + margin)) break;
     }
     if (lane == 0) {
-      int hi = pred + (a.r + 1) / 2;
+      if (pred < 0) pred = J;
+      int hi = pred + margin;
+      if (spred >= 0 && spred < hi) hi = spred;
+      if (hi < pred) hi = pred;
       if (hi > J) hi = J;
       int* st = a.state + (int64_t)bh * 4;
       st[0] = -1; st[1] = hi; st[2] = -1; st[3] = 0;
@@ -808,8 +821,12 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
   }
 }
 
-// One CTA: work items (chunks of kChunk entries) over the bucket entries
-// appended since the last plan, and the chunk -> entry map.
+// One CTA: the bucket entries appended since the last plan, as per-bucket
+// ranges [plan_start, plan_end) and their exclusive prefix plan_off over
+// the buckets.  EV: the prefix counts entries (the tensor-core gather cuts
+// it into per-warp ranges); otherwise it counts work items of kChunk
+// entries and chunk_map maps each item to its bucket.
+template <bool EV>
 __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nent) {
   __shared__ unsigned s_part[1024];
   const int tid = threadIdx.x;
@@ -822,7 +839,7 @@ __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nen
     a.plan_start[i] = st;
     a.plan_end[i] = en;
     a.bcons[i] = en;
-    sum += (en - st + kChunk - 1) / kChunk;
+    sum += EV ? en - st : (en - st + kChunk - 1) / kChunk;
   }
   s_part[tid] = sum;
   __syncthreads();
@@ -834,15 +851,19 @@ __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nen
   }
   unsigned run = s_part[tid] - sum;
   for (int i = i0; i < i1; ++i) {
-    const unsigned nch = (a.plan_end[i] - a.plan_start[i] + kChunk - 1) / kChunk;
     a.plan_off[i] = run;
-    for (unsigned k = 0; k < nch; ++k)
-      if (run + k < (unsigned)a.nchunk_cap) a.chunk_map[run + k] = (unsigned)i;
-    run += nch;
+    if (EV) {
+      run += a.plan_end[i] - a.plan_start[i];
+    } else {
+      const unsigned nch = (a.plan_end[i] - a.plan_start[i] + kChunk - 1) / kChunk;
+      for (unsigned k = 0; k < nch; ++k)
+        if (run + k < (unsigned)a.nchunk_cap) a.chunk_map[run + k] = (unsigned)i;
+      run += nch;
+    }
   }
   if (tid == 1023) {
     unsigned tot = s_part[1023];
-    a.plan_off[nent] = tot < (unsigned)a.nchunk_cap ? tot : (unsigned)a.nchunk_cap;
+    a.plan_off[nent] = (EV || tot < (unsigned)a.nchunk_cap) ? tot : (unsigned)a.nchunk_cap;
   }
 }
 
@@ -1012,24 +1033,46 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
   }
 }
 
-// Tensor-core V gather (bf16 caches).  Per batch of 16 events of one
-// level, with Vb the 16 x d block of their value rows:
-//   C += A_hi Vb + A_lo Vb,  C rows 0..G-1 = per-head light sums
-//   (coefficient +1 on a light entry, -1 when a light key turns heavy),
-//   rows G..2G-1 = per-head heavy sums (coefficient w, split as
-//   bf16(w) + bf16(w - bf16(w)) so the product stays float32-accurate).
-constexpr int kVgW = 4;                        // warps per CTA
-constexpr int kVgS = 4;                        // ring stages per warp
-constexpr int kVgB = 16;                       // events per batch (mma k)
-constexpr int kVgEPW = kChunk / kVgW;          // events per warp per item
+// Tensor-core V gather (bf16 caches).  The round's new bucket entries,
+// concatenated bucket after bucket, are cut into one contiguous range per
+// warp.  A warp walks its range in batches of 16 entries of one bucket
+// (one level of one group), staging the 16 value rows, the candidates'
+// scores and their ||v||^2 in a per-warp ring filled with cp.async, and
+// accumulates
+//   C += A Vx,   Vx = [value rows | 1, hi(||v||^2), lo(||v||^2), 0...]
+// where A has 4G rows per event column: rows 0..G-1 the light coefficient
+// (+1 on a light entry, -1 when a light key turns heavy), rows G..2G-1 and
+// 2G..3G-1 the heavy weight w = exp(s - c32) split as bf16(w) and
+// bf16(w - bf16(w)) so the product stays float32-accurate, rows 3G..4G-1
+// the sampled-key flag.  One batch is (D/8 + 1) mma per 16 rows of A.  The
+// accumulators go to the per-level sums with vector reductions whenever the
+// bucket changes and at the end of the range.
+constexpr int kVsW = 4;                         // warps per CTA
+constexpr int kVsS = 3;                         // row stages per warp
+constexpr int kVsE = 2 * kVsS;                  // entry / descriptor slots per warp
+constexpr int kVsB = 16;                        // entries per batch (mma k)
 
 template <int D, int G>
-constexpr int vgather_tc_smem() {
-  return kVgW * kVgS * kVgB * D * 2 +                    // value rows
-         kVgW * kVgS * kVgB * 16 +                       // staged scores (G = 4)
-         kVgW * kVgEPW * 8 +                             // events
-         kVgW * kVgB * G * 4 * 2 +                       // per-event coefficients, weights
-         G * (2 * D + 8) * 4;                            // CTA sums
+struct VsLayout {
+  static constexpr int RB = 2 * D;                               // bf16 value row
+  static constexpr int MT = (4 * G + 15) / 16;                   // m-tiles of A
+  static constexpr int SCB = 4 * G;                              // scores per entry
+  static constexpr int rows = 0;
+  static constexpr int sc = rows + kVsS * kVsB * RB;
+  static constexpr int vn = sc + kVsS * kVsB * SCB;
+  static constexpr int ent = vn + kVsS * kVsB * 4;
+  static constexpr int desc = ent + kVsE * kVsB * 8;             // [e, entry offset, count, bg, c32 x 8]
+  static constexpr int at = desc + kVsE * 64;                    // A^T: [16 entries][16 MT] bf16
+  static constexpr int bx = at + kVsB * MT * 32;                 // [16 entries][8] bf16
+  static constexpr int per_warp = bx + kVsB * 16;
+  static constexpr int smem = kVsW * per_warp;
+};
+
+template <int BYTES>
+__device__ __forceinline__ void cp_async_small(void* smem, const void* gmem, bool valid) {
+  unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  int src = valid ? BYTES : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;\n" ::"r"(sa), "l"(gmem), "n"(BYTES), "r"(src));
 }
 
 __device__ __forceinline__ void ldsm_x4_trans(unsigned (&r)[4], const void* p) {
@@ -1038,218 +1081,282 @@ __device__ __forceinline__ void ldsm_x4_trans(unsigned (&r)[4], const void* p) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(sa));
 }
+__device__ __forceinline__ void ldsm_x2_trans(unsigned (&r)[2], const void* p) {
+  unsigned sa = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(sa));
+}
 __device__ __forceinline__ unsigned pack_bf16(float lo, float hi) {
-  const unsigned a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const unsigned b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return a | (b << 16);
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);   // lo in the low half
+  return *reinterpret_cast<const unsigned*>(&v);
+}
+__device__ __forceinline__ void red_add2(float* p, float x, float y) {
+  if (x != 0.f || y != 0.f) atomicAdd(reinterpret_cast<float2*>(p), make_float2(x, y));
+}
+
+// Batch generator over a warp's range [pos, end) of the concatenated new
+// bucket entries (warp-uniform state).
+struct VsGen {
+  int e, bg;          // current bucket and its (sequence, KV head)
+  unsigned pos, end;  // next entry, end of range (concatenated numbering)
+  unsigned off0, off1;  // concatenated offsets of bucket e and e + 1
+  unsigned start;     // bucket-local index of the bucket's first new entry
+};
+
+// Smallest bucket e' >= e0 whose new entries hold concatenated position x
+// (plan_off non-decreasing, plan_off[nent] > x), with its offsets.
+__device__ __forceinline__ void vs_seek(const SparseArgs& a, int nent, int e0, unsigned x, VsGen& g) {
+  const int lane = threadIdx.x & 31;
+  for (int base = e0;; base += 32) {
+    const int e = base + lane;
+    const bool in = e < nent;
+    const unsigned o1 = in ? a.plan_off[e + 1] : 0xffffffffu;
+    const unsigned bal = __ballot_sync(0xffffffffu, o1 > x);
+    if (bal) {
+      const int f = __ffs(bal) - 1;
+      const unsigned o0 = in ? a.plan_off[e] : 0u;
+      const unsigned st = in ? a.plan_start[e] : 0u;
+      g.e = base + f;
+      g.bg = g.e / a.J1;
+      g.off0 = __shfl_sync(0xffffffffu, o0, f);
+      g.off1 = __shfl_sync(0xffffffffu, o1, f);
+      g.start = __shfl_sync(0xffffffffu, st, f);
+      return;
+    }
+  }
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(128) vgather_tc_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
-                                                         int nent) {
-  constexpr int RB = D * 2;
-  constexpr int NT = D / 8;                     // n-tiles of 8 channels
+__global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int nent) {
+  using Lt = VsLayout<D, G>;
+  constexpr int RB = Lt::RB, MT = Lt::MT, NT = D / 8, CH = RB / 16;
   constexpr int ACC = 2 * D + 8;
   extern __shared__ __align__(16) uint8_t dsm[];
-  uint8_t* ring = dsm;
-  float* s_sc = reinterpret_cast<float*>(dsm + kVgW * kVgS * kVgB * RB);
-  uint2* s_ev = reinterpret_cast<uint2*>(dsm + kVgW * kVgS * kVgB * RB + kVgW * kVgS * kVgB * 16);
-  float* s_cf = reinterpret_cast<float*>(dsm + kVgW * kVgS * kVgB * RB + kVgW * kVgS * kVgB * 16 +
-                                         kVgW * kVgEPW * 8);
-  float (*s_acc)[ACC] = reinterpret_cast<float (*)[ACC]>(dsm + kVgW * kVgS * kVgB * RB + kVgW * kVgS * kVgB * 16 +
-                                                          kVgW * kVgEPW * 8 + kVgW * kVgB * G * 4 * 2);
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int gq = lane >> 2, tq = lane & 3;
-  const unsigned total = a.plan_off[nent];
-  uint8_t* my = ring + w * kVgS * kVgB * RB;
-  float* msc = s_sc + w * kVgS * kVgB * 4;
-  uint2* mev = s_ev + w * kVgEPW;
-  float* mcf = s_cf + w * kVgB * G * 2;          // [16 events][G] coefficient, then [16][G] weight
-  for (unsigned c = blockIdx.x; c < total; c += gridDim.x) {
-    const int e = (int)a.chunk_map[c];
-    const int bg = e / a.J1, l = e - bg * a.J1;
-    const int b = bg / a.Hkv, g = bg - b * a.Hkv;
-    const int bh0 = b * a.Hq + g * G;
-    const unsigned ev0 = a.plan_start[e] + (c - a.plan_off[e]) * kChunk;
-    const unsigned ev1 = min(a.plan_end[e], ev0 + kChunk);
-    const int nev = (int)(ev1 - ev0);
-    const int nball = (nev + kVgB - 1) / kVgB;
-    const int nmy = nball > w ? (nball - w + kVgW - 1) / kVgW : 0;
-    const uint2* bk = a.buckets + (int64_t)e * a.pcap + ev0;
-    for (int i = lane; i < kVgEPW; i += 32) {
-      const int k = i / kVgB, r = i % kVgB;
-      const int idx = (w + k * kVgW) * kVgB + r;
-      mev[i] = (k < nmy && idx < nev) ? bk[idx] : make_uint2(0u, 0u);
+  uint8_t* base = dsm + w * Lt::per_warp;
+  uint8_t* s_rows = base + Lt::rows;
+  uint8_t* s_sc = base + Lt::sc;
+  float* s_vn = reinterpret_cast<float*>(base + Lt::vn);
+  uint2* s_ent = reinterpret_cast<uint2*>(base + Lt::ent);
+  int* s_desc = reinterpret_cast<int*>(base + Lt::desc);
+  uint8_t* s_at = base + Lt::at;
+  uint8_t* s_bx = base + Lt::bx;
+
+  const unsigned E = a.plan_off[nent];
+  const unsigned nw = gridDim.x * kVsW, gw = blockIdx.x * kVsW + w;
+  VsGen gen;
+  gen.pos = (unsigned)(((unsigned long long)E * gw) / nw);
+  gen.end = (unsigned)(((unsigned long long)E * (gw + 1)) / nw);
+  if (gen.pos >= gen.end) return;
+  {
+    // largest bucket with plan_off <= pos: 32-ary search
+    int lo = 0, hi = nent;
+    while (hi - lo > 1) {
+      const int p = lo + 1 + (int)(((int64_t)(hi - lo - 1) * lane) / 32);
+      const unsigned bal = __ballot_sync(0xffffffffu, a.plan_off[p] <= gen.pos);
+      const int cnt = __popc(bal);
+      const int plo = __shfl_sync(0xffffffffu, p, cnt > 0 ? cnt - 1 : 0);
+      const int phi = __shfl_sync(0xffffffffu, p, cnt < 32 ? cnt : 31);
+      if (cnt == 0) hi = plo;
+      else { lo = plo; if (cnt < 32) hi = phi; }
     }
-    float c32[G];
+    vs_seek(a, nent, lo, gen.pos, gen);
+  }
+
+  // next batch descriptor into slot ds; entries and c32 by cp.async
+  auto gen_next = [&](int ds) {
+    int* dp = s_desc + ds * 16;
+    int cnt = 0, e = -1, bg = 0;
+    unsigned eoff = 0;
+    if (gen.pos < gen.end) {
+      if (gen.pos >= gen.off1) vs_seek(a, nent, gen.e + 1, gen.pos, gen);
+      e = gen.e;
+      bg = gen.bg;
+      cnt = (int)min(min(gen.off1, gen.end) - gen.pos, (unsigned)kVsB);
+      eoff = gen.start + (gen.pos - gen.off0);
+      gen.pos += cnt;
+    }
+    if (lane == 0) { dp[0] = e; dp[1] = (int)eoff; dp[2] = cnt; dp[3] = bg; }
+    if (cnt > 0) {
+      const uint2* src = a.buckets + (int64_t)e * a.pcap + eoff;
+      if (lane < cnt) cp_async_small<8>(s_ent + ds * kVsB + lane, src + lane, true);
+      // query heads of group bg: bh = b * Hq + g * G = bg * G (Hq = G * Hkv)
+      if (lane < G) cp_async_small<4>(dp + 4 + lane, a.cmax + ((int64_t)bg * G + lane) * 4 + 3, true);
+    }
+  };
+  // rows, scores and ||v||^2 of batch in descriptor slot ds into stage ss
+  auto issue_rows = [&](int ds, int ss) {
+    const int* dp = s_desc + ds * 16;
+    const int cnt = dp[2];
+    if (cnt <= 0) return;
+    const int bg = dp[3];
+    // lanes 2r and 2r + 1 copy row r (halves of its 16-byte chunks)
+    const int r = lane >> 1, half = lane & 1;
+    const bool ok = r < cnt;
+    const unsigned key = ok ? s_ent[ds * kVsB + r].x : 0u;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(a.V) + ((int64_t)bg * a.n_max + key) * RB +
+                         half * (RB / 2);
+    uint8_t* dst = s_rows + (ss * kVsB + r) * RB;
 #pragma unroll
-    for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
-    __syncthreads();
-    for (int i = tid; i < G * ACC; i += 128) (&s_acc[0][0])[i] = 0.f;
-    __syncthreads();
-    float C[NT][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) { C[j][0] = C[j][1] = C[j][2] = C[j][3] = 0.f; }
-    float s2[G], hb[G], kc[G], db[G], ns[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) s2[h] = hb[h] = kc[h] = db[h] = ns[h] = 0.f;
-    unsigned hm = 0;
-    const __nv_bfloat16* Vb = reinterpret_cast<const __nv_bfloat16*>(a.V) + (int64_t)bg * a.n_max * D;
-    const float* sb = a.s32 + (int64_t)bg * a.pcap * G;
-    auto bcount = [&](int k) { return k < nmy ? min(kVgB, nev - (w + k * kVgW) * kVgB) : 0; };
-    auto issue = [&](int slot, int k) {
-      const int nv = bcount(k);
-      uint8_t* dst = my + slot * kVgB * RB;
-      constexpr int CH = RB / 16;
-#pragma unroll
-      for (int cc = lane; cc < kVgB * CH; cc += 32) {
-        const int r = cc / CH, part = cc - r * CH;
-        const bool ok = r < nv;
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(Vb) + (ok ? (int64_t)mev[k * kVgB + r].x * RB + part * 16 : 0);
-        cp_async16(dst + r * RB + ((part ^ (r & 7)) * 16), src, ok);
+    for (int i = 0; i < CH / 2; ++i) {
+      const int part = half * (CH / 2) + i;
+      cp_async16(dst + ((part ^ (r & 7)) << 4), src + i * 16, ok);
+    }
+    if (half == 0) {
+      const float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
+      uint8_t* sd = s_sc + (ss * kVsB + r) * Lt::SCB;
+      if (G == 8) {
+        cp_async16(sd, sp, ok);
+        cp_async16(sd + 16, sp + 4, ok);
+      } else if (G == 4) {
+        cp_async16(sd, sp, ok);
+      } else if (G == 2) {
+        cp_async_small<8>(sd, sp, ok);
+      } else {
+        cp_async_small<4>(sd, sp, ok);
       }
-      if (G == 4 && lane < kVgB) {
-        const bool ok = lane < nv;
-        const float* src = ok ? sb + (int64_t)mev[k * kVgB + lane].x * 4 : sb;
-        cp_async16(msc + (slot * kVgB + lane) * 4, src, ok);
-      }
-      cp_async_commit();
-    };
+    } else {
+      cp_async_small<4>(s_vn + ss * kVsB + r, a.vnorm2 + (int64_t)bg * a.n_max + key, ok);
+    }
+  };
+
+  float C[MT][NT + 1][4];
 #pragma unroll
-    for (int sl = 0; sl < kVgS; ++sl) issue(sl, sl);
-    for (int k = 0; k < nmy; ++k) {
-      const int slot = k & (kVgS - 1);
-      cp_async_wait<kVgS - 1>();
-      __syncwarp();
-      const int nv = bcount(k);
-      const uint8_t* stg = my + slot * kVgB * RB;
-      // squared norms of the 16 value rows (lane partials, reduce-scatter)
-      float part[kVgB];
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int r = 0; r < kVgB; ++r) {
-        constexpr int CPL = D / 32;
-        const int byte = lane * CPL * 2;                         // this lane's channels
-        const uint8_t* row = stg + r * RB + (((byte >> 4) ^ (r & 7)) << 4) + (byte & 15);
-        float v0, v1, v2 = 0.f, v3 = 0.f;
-        if (CPL == 4) {
-          const uint2 u = *reinterpret_cast<const uint2*>(row);
-          v0 = __uint_as_float(u.x << 16); v1 = __uint_as_float(u.x & 0xFFFF0000u);
-          v2 = __uint_as_float(u.y << 16); v3 = __uint_as_float(u.y & 0xFFFF0000u);
-        } else {
-          const unsigned u = *reinterpret_cast<const unsigned*>(row);
-          v0 = __uint_as_float(u << 16); v1 = __uint_as_float(u & 0xFFFF0000u);
+    for (int j = 0; j <= NT; ++j) C[mt][j][0] = C[mt][j][1] = C[mt][j][2] = C[mt][j][3] = 0.f;
+  int cur = -1, cur_bg = 0;
+
+  auto flush = [&]() {
+    const int l = cur - cur_bg * a.J1;
+    float* accl = a.acc + ((int64_t)cur_bg * G * a.J1 + l) * ACC;
+    const int64_t hstride = (int64_t)a.J1 * ACC;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int row = 16 * mt + gq + 8 * hf;
+        if (row >= 4 * G) continue;
+        const int type = row / G, h = row - type * G;
+        float* ah = accl + h * hstride;
+        if (type < 3) {
+          const int off = type == 0 ? 0 : D;
+#pragma unroll
+          for (int j = 0; j < NT; ++j) red_add2(ah + off + 8 * j + 2 * tq, C[mt][j][2 * hf], C[mt][j][2 * hf + 1]);
         }
-        part[r] = v0 * v0 + v1 * v1 + v2 * v2 + v3 * v3;
-      }
-#pragma unroll
-      for (int st = 0, cnt = kVgB / 2; st < 4; ++st, cnt >>= 1) {
-        const int o = 1 << st;
-        const bool hi = lane & o;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (i < cnt) {
-            const float send = hi ? part[2 * i] : part[2 * i + 1];
-            const float keep = hi ? part[2 * i + 1] : part[2 * i];
-            part[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-          }
-        }
-      }
-      const float nrm2 = part[0] + __shfl_xor_sync(0xffffffffu, part[0], 16);   // event lane & 15
-      // one lane per event: masks, weights, scalar sums, coefficients
-      if (lane < kVgB) {
-        const bool ok = lane < nv;
-        const uint2 ev = ok ? mev[k * kVgB + lane] : make_uint2(0u, 0u);
-        const unsigned m = ev.y;
-        hm |= m;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const bool add = m & (1u << h), trn = m & (1u << (8 + h)), bef = m & (1u << (16 + h));
-          float wt = 0.f;
-          if (trn) {
-            const float sh = G == 4 ? msc[(slot * kVgB + lane) * 4 + h] : sb[(int64_t)ev.x * G + h];
-            wt = expf(fsub(sh, c32[h]));
-          }
-          const float cf = add ? 1.f : ((trn && bef) ? -1.f : 0.f);
-          mcf[lane * G + h] = cf;
-          mcf[kVgB * G + lane * G + h] = wt;
-          kc[h] += cf;
-          s2[h] += cf * nrm2;
-          db[h] += wt;
-          hb[h] += wt * nrm2;
-          ns[h] += (add || (trn && !bef)) ? 1.f : 0.f;
+        // scalar tile: channel 0 = count / weight / sampled, 1 + 2 = ||v||^2 terms
+        const float c0 = C[mt][NT][2 * hf], c1 = C[mt][NT][2 * hf + 1];
+        if (tq == 0) {
+          const int s0 = type == 0 ? 2 * D : (type < 3 ? 2 * D + 2 : 2 * D + 4);
+          if (c0 != 0.f) atomicAdd(ah + s0, c0);
+          if (type < 3 && c1 != 0.f) atomicAdd(ah + s0 + 1, c1);
+        } else if (tq == 1 && type < 3) {
+          if (c0 != 0.f) atomicAdd(ah + (type == 0 ? 2 * D + 1 : 2 * D + 3), c0);
         }
       }
-      __syncwarp();
-      // A fragments: rows g and g + 8, events 2t, 2t+1 and 2t+8, 2t+9
-      auto coef = [&](int row, int ev, bool lo) -> float {
-        if (row < G) return lo ? 0.f : mcf[ev * G + row];
-        if (row < 2 * G) {
-          const float wt = mcf[kVgB * G + ev * G + (row - G)];
-          const float hi = __bfloat162float(__float2bfloat16_rn(wt));
-          return lo ? wt - hi : hi;
-        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int j = 0; j <= NT; ++j) C[mt][j][0] = C[mt][j][1] = C[mt][j][2] = C[mt][j][3] = 0.f;
+  };
+
+  // prologue: descriptors and entries of the first kVsE batches, then rows
+  // of the first kVsS
+  for (int i = 0; i < kVsE; ++i) gen_next(i);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncwarp();
+  for (int i = 0; i < kVsS; ++i) {
+    issue_rows(i, i);
+    cp_async_commit();
+  }
+  for (int i = 0;; ++i) {
+    const int ds = i % kVsE, ss = i % kVsS;
+    cp_async_wait<kVsS - 1>();
+    __syncwarp();
+    const int* dp = s_desc + ds * 16;
+    const int e = dp[0], cnt = dp[2];
+    if (cnt <= 0) break;
+    if (e != cur) {
+      if (cur >= 0) flush();
+      cur = e;
+      cur_bg = dp[3];
+    }
+    if (lane < kVsB) {
+      const uint2 ev = lane < cnt ? s_ent[ds * kVsB + lane] : make_uint2(0u, 0u);
+      const unsigned m = ev.y;
+      const float* sc = reinterpret_cast<const float*>(s_sc + (ss * kVsB + lane) * Lt::SCB);
+      const float vn = s_vn[ss * kVsB + lane];
+      float cf[G], wh[G], wl[G], ns[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const bool add = m & (1u << h), trn = m & (1u << (8 + h)), bef = m & (1u << (16 + h));
+        float wt = 0.f;
+        if (trn) wt = __expf(fsub(sc[h], float_of_ord((unsigned)dp[4 + h])));
+        cf[h] = add ? 1.f : ((trn && bef) ? -1.f : 0.f);
+        wh[h] = __bfloat162float(__float2bfloat16_rn(wt));
+        wl[h] = wt - wh[h];
+        ns[h] = (add || (trn && !bef)) ? 1.f : 0.f;
+      }
+      auto coef = [&](int row) -> float {
+        if (row < G) return cf[row];
+        if (row < 2 * G) return wh[row - G];
+        if (row < 3 * G) return wl[row - 2 * G];
+        if (row < 4 * G) return ns[row - 3 * G];
         return 0.f;
       };
-      unsigned ah[4], al[4];
-      {
-        const int r0 = gq, r1 = gq + 8, e0 = 2 * tq, e1 = 2 * tq + 8;
-        ah[0] = pack_bf16(coef(r0, e0, false), coef(r0, e0 + 1, false));
-        ah[1] = pack_bf16(coef(r1, e0, false), coef(r1, e0 + 1, false));
-        ah[2] = pack_bf16(coef(r0, e1, false), coef(r0, e1 + 1, false));
-        ah[3] = pack_bf16(coef(r1, e1, false), coef(r1, e1 + 1, false));
-        al[0] = pack_bf16(coef(r0, e0, true), coef(r0, e0 + 1, true));
-        al[1] = pack_bf16(coef(r1, e0, true), coef(r1, e0 + 1, true));
-        al[2] = pack_bf16(coef(r0, e1, true), coef(r0, e1 + 1, true));
-        al[3] = pack_bf16(coef(r1, e1, true), coef(r1, e1 + 1, true));
+      uint4* arow = reinterpret_cast<uint4*>(s_at + lane * MT * 32);
+#pragma unroll
+      for (int q = 0; q < 2 * MT; ++q) {
+        uint4 u;
+        u.x = pack_bf16(coef(8 * q + 0), coef(8 * q + 1));
+        u.y = pack_bf16(coef(8 * q + 2), coef(8 * q + 3));
+        u.z = pack_bf16(coef(8 * q + 4), coef(8 * q + 5));
+        u.w = pack_bf16(coef(8 * q + 6), coef(8 * q + 7));
+        arow[q] = u;
       }
-      // B fragments: value rows transposed, two n-tiles per ldmatrix.x4
-      const int mi = lane >> 3, rr = lane & 7;                  // matrix, row within it
+      const float vh = __bfloat162float(__float2bfloat16_rn(vn));
+      *reinterpret_cast<uint4*>(s_bx + lane * 16) = make_uint4(pack_bf16(1.f, vh), pack_bf16(vn - vh, 0.f), 0u, 0u);
+    }
+    __syncwarp();
+    // A fragments (A^T stored entry-major): matrices (rows m 0-7 | 8-15) x (k 0-7 | 8-15)
+    unsigned af[MT][4];
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int k = (mi >> 1) * 8 + rr, mh = mi & 1;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) ldsm_x4_trans(af[mt], s_at + k * MT * 32 + mt * 32 + mh * 16);
+    }
+    unsigned bxf[2];
+    ldsm_x2_trans(bxf, s_bx + (lane & 15) * 16);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(C[mt][NT], af[mt], bxf[0], bxf[1]);
+    const uint8_t* stg = s_rows + ss * kVsB * RB;
+    {
+      const int mi = lane >> 3, rr = lane & 7;
+      const int ev = (mi & 1) * 8 + rr;
 #pragma unroll
       for (int jp = 0; jp < NT / 2; ++jp) {
-        const int ev = (mi & 1) * 8 + rr;                         // event (matrix row)
-        const int chunk = 2 * jp + (mi >> 1);                     // 16-byte channel chunk
+        const int chunk = 2 * jp + (mi >> 1);
         unsigned bfr[4];
         ldsm_x4_trans(bfr, stg + ev * RB + ((chunk ^ (ev & 7)) << 4));
-        mma_bf16_16816(C[2 * jp], ah, bfr[0], bfr[1]);
-        mma_bf16_16816(C[2 * jp], al, bfr[0], bfr[1]);
-        mma_bf16_16816(C[2 * jp + 1], ah, bfr[2], bfr[3]);
-        mma_bf16_16816(C[2 * jp + 1], al, bfr[2], bfr[3]);
-      }
-      __syncwarp();
-      issue(slot, k + kVgS);
-    }
-    cp_async_wait<0>();
-    // C rows -> per-head light sums (rows < G) and heavy sums (G..2G-1)
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int row = gq + (u >> 1) * 8;
-        const int ch = 8 * j + 2 * tq + (u & 1);
-        if (row < G) atomicAdd(&s_acc[row][ch], C[j][u]);
-        else if (row < 2 * G) atomicAdd(&s_acc[row - G][D + ch], C[j][u]);
+        for (int mt = 0; mt < MT; ++mt) {
+          mma_bf16_16816(C[mt][2 * jp], af[mt], bfr[0], bfr[1]);
+          mma_bf16_16816(C[mt][2 * jp + 1], af[mt], bfr[2], bfr[3]);
+        }
       }
     }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float k_ = warp_sum(kc[h]), s2_ = warp_sum(s2[h]), db_ = warp_sum(db[h]);
-      const float hb_ = warp_sum(hb[h]), ns_ = warp_sum(ns[h]);
-      if (lane == 0 && (k_ != 0.f || ns_ != 0.f || db_ != 0.f)) {
-        atomicAdd(&s_acc[h][2 * D + 0], k_);
-        atomicAdd(&s_acc[h][2 * D + 1], s2_);
-        atomicAdd(&s_acc[h][2 * D + 2], db_);
-        atomicAdd(&s_acc[h][2 * D + 3], hb_);
-        atomicAdd(&s_acc[h][2 * D + 4], ns_);
-      }
-    }
-    __syncthreads();
-    for (int i = tid; i < G * ACC; i += 128) {
-      const int h = i / ACC, x = i - h * ACC;
-      if (x >= 2 * D + 5) continue;
-      const float v = s_acc[h][x];
-      if (v != 0.f) atomicAdd(a.acc + ((int64_t)(bh0 + h) * a.J1 + l) * ACC + x, v);
-    }
+    __syncwarp();
+    issue_rows((i + kVsS) % kVsE, ss);
+    gen_next(ds);
+    cp_async_commit();
   }
+  cp_async_wait<0>();
+  if (cur >= 0) flush();
 }
 
 // ------------------------------------------------------------ certificate
@@ -1527,24 +1634,32 @@ void launch_rows1(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs
   launch_rows_t<D, G, E, 1>(grid, st, a, seq);
 }
 template <int D, int G, typename E>
-void launch_vgather_t(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int nent) {
-  if (sizeof(E) == 2) {
-    constexpr int smem = vgather_tc_smem<D, G>();
+void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int nent,
+                      PhaseMark mark) {
+  if constexpr (sizeof(E) == 2) {
+    constexpr int smem = VsLayout<D, G>::smem;
+    static int per_sm = 0;
+    if (!per_sm) {
+      cudaFuncSetAttribute(vsum_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vsum_kernel<D, G>, kVsW * 32, smem) !=
+              cudaSuccess ||
+          per_sm < 1)
+        per_sm = 1;
+    }
+    vplan_kernel<true><<<1, 1024, 0, st>>>(a, nent);
+    if (mark) mark(7, st);
+    vsum_kernel<D, G><<<dim3((unsigned)(nsm * per_sm)), kVsW * 32, smem, st>>>(a, nent);
+  } else {
+    constexpr int smem = vgather_smem<D, G, E>();
     static bool set = false;
     if (!set) {
-      cudaFuncSetAttribute(vgather_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(vgather_kernel<D, G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       set = true;
     }
-    vgather_tc_kernel<D, G><<<dim3(grid.x * 2), 128, smem, st>>>(a, seq, nent);
-    return;
+    vplan_kernel<false><<<1, 1024, 0, st>>>(a, nent);
+    if (mark) mark(7, st);
+    vgather_kernel<D, G, E><<<dim3((unsigned)(nsm * 2)), 256, smem, st>>>(a, seq, nent);
   }
-  constexpr int smem = vgather_smem<D, G, E>();
-  static bool set = false;
-  if (!set) {
-    cudaFuncSetAttribute(vgather_kernel<D, G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    set = true;
-  }
-  vgather_kernel<D, G, E><<<grid, 256, smem, st>>>(a, seq, nent);
 }
 
 static dim3 rows_grid(const SparseArgs& a, int64_t items, int nsm) {
@@ -1584,9 +1699,7 @@ cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
   CSA_G_SWITCH(levels_kernel, <<<grid, 256, 0, st>>>(a, seq))
   if (mark) mark(6, st);
   const int nent = a.B * a.Hkv * a.J1;
-  vplan_kernel<<<1, 1024, 0, st>>>(a, nent);
-  if (mark) mark(7, st);
-  CSA_DG_SWITCH(launch_vgather_t, (dim3((unsigned)(nsm * 2)), st, a, seq, nent))
+  CSA_DG_SWITCH(launch_vgather_t, (nsm, st, a, seq, nent, mark))
   if (mark) mark(8, st);
   dim3 cg((unsigned)(a.B * a.Hq));
   if (d == 128) certify_kernel<128><<<cg, 256, 0, st>>>(a, seq, round);

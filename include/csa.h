@@ -38,6 +38,8 @@
  *   bounds [B][Hkv][nblk_max][2][d]        float: per block and channel the
  *                                          minimum m_c, then the step Delta_c
  *   vmax   [B][Hkv][nblk_max]              float: per-block bound on ||v_i||
+ *   vnorm2 [B][Hkv][n_max]                 float: ||v_i||^2 of each token, the
+ *                                          sequential float32 sum of v_c^2
  *   o      [B][Hq][d] float;  beta, level, keys_read: [B][Hq]
  * with nblk_max = ceil(n_max / 64).  Query head h uses KV head h / (Hq/Hkv).
  */
@@ -111,19 +113,20 @@ size_t csa_workspace_size(const csa_shape* shape, const csa_params* params);
 /* 4-bit key quantiser and value-norm metadata (picx.dev "Algorithm
  * Components" 4: 4-bit per-block per-channel codes as in KIVI).
  * Rebuilds every 64-token block that holds a token at position
- * >= from_token and < len[b]: codes, (m_c, Delta_c) and vmax.  In decode,
- * from_token = the position of the token just appended (one block).
+ * >= from_token and < len[b]: codes, (m_c, Delta_c), vmax and the
+ * blocks' vnorm2 entries.  In decode, from_token = the position of the
+ * token just appended (one block).
  *   K, V   device, layout above;  len host [B], 0 <= len[b] <= n_max
- *   K4, bounds, vmax: device outputs, layout above.
- * Positions >= len[b] inside a rebuilt block get code 0. */
+ *   K4, bounds, vmax, vnorm2: device outputs, layout above.
+ * Positions >= len[b] inside a rebuilt block get code 0 and vnorm2 0. */
 csa_status csa_quantize_keys(const csa_shape* shape, const void* K,
                              const void* V, const int64_t* len,
                              int64_t from_token, uint8_t* K4, float* bounds,
-                             float* vmax, void* stream);
+                             float* vmax, float* vnorm2, void* stream);
 
 /* One certified sparse decode-attention step for every (sequence, query
- * head).  Inputs: q, K, V, K4, bounds, vmax (device, layout above; K4,
- * bounds and vmax must describe the first len[b] tokens, see
+ * head).  Inputs: q, K, V, K4, bounds, vmax, vnorm2 (device, layout above;
+ * K4, bounds, vmax and vnorm2 must describe the first len[b] tokens, see
  * csa_quantize_keys), len host [B] (1 <= len[b] <= n_max), step_seed host
  * [B] (fresh every step; the caller mixes in the layer).  Outputs (device):
  *   o          [B][Hq][d]  o_hat at the stop level (exact o after fallback)
@@ -137,7 +140,8 @@ csa_status csa_quantize_keys(const csa_shape* shape, const void* K,
 csa_status csa_decode_step(const csa_shape* shape, const csa_params* params,
                            const void* q, const void* K, const void* V,
                            const uint8_t* K4, const float* bounds,
-                           const float* vmax, const int64_t* len,
+                           const float* vmax, const float* vnorm2,
+                           const int64_t* len,
                            const uint64_t* step_seed, float* o, float* beta,
                            int32_t* level, int32_t* keys_read,
                            csa_head_stats* stats, void* workspace,
@@ -194,9 +198,12 @@ csa_status csa_dense_decode_static(const csa_shape* shape, const void* q,
  *            pool key for each head, -inf where it is not a candidate
  *   jr_hist  uint32 [B][Hq][J+2]        first level at which the key's bf16
  *            row is needed (exact-max set: level 0), J+1 = never
+ *   bcnt     uint32 [B][Hkv][J1]        entries appended to each level bucket
+ *            (one per key and level at which the key changes a head's sums;
+ *            each entry is one value-row load of the gather)
  *   J1       largest J + 1 (row stride of jr_hist is J1 + 1) */
 typedef struct {
-  size_t ubar, cmax, s32, jr_hist, total;
+  size_t ubar, cmax, s32, jr_hist, bcnt, total;
   int32_t J1, reserved;
 } csa_workspace_map;
 

@@ -30,7 +30,7 @@ Parity status per function (the pins live in ``tests/test_oracle_*.py``):
 """
 from .fp32 import tree_sum_f32, log2_m53_f32
 from .hashing import mix64, group_key, key_hashes, perturb_t
-from .quantize import quantize_keys, vmax_blocks
+from .quantize import quantize_keys, value_sq_norms_f32, vmax_blocks
 from .bounds import query_prep, key_bounds, QM_DEFAULT
 from .certificate import chernoff_interval, certificate_levels
 from .step import (Params, grid_J, oracle_decode_group, dense_attention,
@@ -39,7 +39,7 @@ from .step import (Params, grid_J, oracle_decode_group, dense_attention,
 
 __all__ = [
     "tree_sum_f32", "log2_m53_f32", "mix64", "group_key", "key_hashes",
-    "perturb_t", "quantize_keys", "vmax_blocks", "query_prep", "key_bounds",
+    "perturb_t", "quantize_keys", "value_sq_norms_f32", "vmax_blocks", "query_prep", "key_bounds",
     "QM_DEFAULT", "chernoff_interval", "certificate_levels", "Params",
     "grid_J", "oracle_decode_group", "dense_attention", "GroupResult",
     "exact_levels", "level_sums", "score_f32", "cstar_lower_f32",

@@ -57,13 +57,22 @@ def quantize_keys(K: np.ndarray, n: int, T: int = T_BLOCK):
     return codes, packed, mins, deltas
 
 
-def vmax_blocks(V: np.ndarray, n: int, T: int = T_BLOCK) -> np.ndarray:
-    """Per-block upper bound on ||v_i|| (float32 [nblk])."""
+def value_sq_norms_f32(V: np.ndarray, n: int) -> np.ndarray:
+    """||v_i||^2 of the first n value rows as the sequential float32 sum of
+    v_c^2 over the channels c = 0, 1, ... (float32 [n]).  The value norms
+    enter the Hilbert-space Bernstein bound and the value scale M of the
+    certificate (picx.dev "Algorithm Components" 3)."""
     V = np.asarray(V[:n], dtype=np.float32)
     d = V.shape[1]
     ss = np.zeros(V.shape[0], np.float32)
     for c in range(d):
         ss = ss + V[:, c] * V[:, c]
+    return ss
+
+
+def vmax_blocks(V: np.ndarray, n: int, T: int = T_BLOCK) -> np.ndarray:
+    """Per-block upper bound on ||v_i|| (float32 [nblk])."""
+    ss = value_sq_norms_f32(V, n)
     nrm = np.sqrt(ss).astype(np.float32)
     nblk = (n + T - 1) // T
     out = np.zeros(nblk, np.float32)

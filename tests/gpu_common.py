@@ -50,14 +50,13 @@ class GpuRun:
         self.K = to_dev(Kp, w.dtype, device)
         self.V = to_dev(Vp, w.dtype, device)
         self.q = to_dev(q, w.dtype, device)
-        self.K4, self.bounds, self.vmax = csa.meta_buffers(self.shape, device)
+        self.meta = csa.meta_buffers(self.shape, device)
         csa.check(csa.csa_quantize_keys(self.shape, self.K, self.V, self.lens,
-                                        0, self.K4, self.bounds, self.vmax),
+                                        0, *self.meta),
                   "csa_quantize_keys")
         self.step = csa.DecodeStep(self.shape, self.params, device,
                                    with_stats=True)
-        self.step(self.q, self.K, self.V, self.K4, self.bounds, self.vmax,
-                  self.lens, self.seeds)
+        self.step(self.q, self.K, self.V, self.meta, self.lens, self.seeds)
         torch.cuda.synchronize()
         csa.check(csa.csa_check(self.step.ws), "csa_check")
         self.map = csa.csa_workspace_layout(self.shape, self.params)

@@ -67,20 +67,20 @@ def test_decode_rejects_bad_arguments_before_launch(lib):
     # null inputs, bad lengths, missing workspace: rejected on the host,
     # nothing is launched (these calls run without a GPU)
     st = lib.csa_decode_step(ctypes.byref(s), ctypes.byref(p), None, None,
-                             None, None, None, None,
+                             None, None, None, None, None,
                              (ctypes.c_int64 * 1)(100),
                              (ctypes.c_uint64 * 1)(1), None, None, None,
                              None, None, None, 0, None)
     assert st == 1
     fake = 256
     st = lib.csa_decode_step(ctypes.byref(s), ctypes.byref(p), fake, fake,
-                             fake, fake, fake, fake,
+                             fake, fake, fake, fake, fake,
                              (ctypes.c_int64 * 1)(5000),
                              (ctypes.c_uint64 * 1)(1), fake, fake, fake,
                              fake, None, fake, 1 << 30, None)
     assert st == 1                       # len > n_max
     st = lib.csa_decode_step(ctypes.byref(s), ctypes.byref(p), fake, fake,
-                             fake, fake, fake, fake,
+                             fake, fake, fake, fake, fake,
                              (ctypes.c_int64 * 1)(100),
                              (ctypes.c_uint64 * 1)(1), fake, fake, fake,
                              fake, None, fake, 16, None)

@@ -16,7 +16,7 @@ import pytest
 import synth
 from oracle.certificate import certificate_levels
 from oracle.hashing import perturb_t
-from oracle.quantize import quantize_keys, vmax_blocks
+from oracle.quantize import quantize_keys, value_sq_norms_f32, vmax_blocks
 from oracle.step import (Params, bound_levels_f32, dense_attention,
                          level_sums, oracle_decode_group)
 from tests.gpu_common import GpuRun, ensure_built, gpu_levels, to_dev
@@ -58,9 +58,9 @@ def test_quantizer_bit_exact(name, n, over):
     Vp = np.zeros_like(Kp)
     Kp[:, :, :n], Vp[:, :, :n] = K, V
     Kt, Vt = to_dev(Kp, w.dtype, "cuda"), to_dev(Vp, w.dtype, "cuda")
-    K4, bounds, vmax = csa.meta_buffers(shape, "cuda")
+    K4, bounds, vmax, vnorm2 = csa.meta_buffers(shape, "cuda")
     csa.check(csa.csa_quantize_keys(shape, Kt, Vt, [n] * w.B, 0, K4, bounds,
-                                    vmax))
+                                    vmax, vnorm2))
     torch.cuda.synchronize()
     for g in range(w.Hkv):
         codes, packed, mins, deltas = quantize_keys(K[0, g], n)
@@ -70,6 +70,9 @@ def test_quantizer_bit_exact(name, n, over):
         assert np.array_equal(bounds[0, g, :nb, 0].cpu().numpy(), mins)
         assert np.array_equal(bounds[0, g, :nb, 1].cpu().numpy(), deltas)
         assert np.array_equal(vmax[0, g, :nb].cpu().numpy(), vm)
+        vn = vnorm2[0, g].cpu().numpy()
+        assert np.array_equal(vn[:n], value_sq_norms_f32(V[0, g], n))
+        assert not vn[n:nb * 64].any()
 
 
 def test_quantizer_append_one_block():
@@ -83,15 +86,16 @@ def test_quantizer_append_one_block():
     Vp = np.zeros_like(Kp)
     Kp[:, :, :1000], Vp[:, :, :1000] = K, V
     Kt, Vt = to_dev(Kp, "bf16", "cuda"), to_dev(Vp, "bf16", "cuda")
-    K4, bounds, vmax = csa.meta_buffers(shape, "cuda")
-    csa.check(csa.csa_quantize_keys(shape, Kt, Vt, [1000], 0, K4, bounds, vmax))
+    K4, bounds, vmax, vnorm2 = csa.meta_buffers(shape, "cuda")
+    csa.check(csa.csa_quantize_keys(shape, Kt, Vt, [1000], 0, K4, bounds, vmax,
+                                    vnorm2))
     rng = np.random.default_rng(5)
     newk = synth.bf16_round_np(rng.standard_normal(128).astype(np.float32) * 3)
     newv = synth.bf16_round_np(rng.standard_normal(128).astype(np.float32))
     Kt[0, 0, 1000] = torch.from_numpy(newk).to(Kt)
     Vt[0, 0, 1000] = torch.from_numpy(newv).to(Vt)
     csa.check(csa.csa_quantize_keys(shape, Kt, Vt, [1001], 1000, K4, bounds,
-                                    vmax))
+                                    vmax, vnorm2))
     torch.cuda.synchronize()
     Kn = np.concatenate([K[0, 0], newk[None]], 0)
     Vn = np.concatenate([V[0, 0], newv[None]], 0)
@@ -101,6 +105,8 @@ def test_quantizer_append_one_block():
     assert np.array_equal(bounds[0, 0, :len(mins), 1].cpu().numpy(), deltas)
     assert np.array_equal(vmax[0, 0, :len(mins)].cpu().numpy(),
                           vmax_blocks(Vn, 1001))
+    assert np.array_equal(vnorm2[0, 0, :1001].cpu().numpy(),
+                          value_sq_norms_f32(Vn, 1001))
 
 
 # ------------------------------------------------------------- decode step

@@ -13,7 +13,7 @@ import pytest
 
 import synth
 from oracle.bounds import key_bounds, query_prep
-from oracle.quantize import quantize_keys, vmax_blocks
+from oracle.quantize import quantize_keys, value_sq_norms_f32, vmax_blocks
 from oracle.step import grid_J, score_f32, cstar_lower_f32
 
 
@@ -71,6 +71,24 @@ def test_vmax_is_upper_bound():
     for b in range(5):
         assert vm[b] >= nrm[b * 64:(b + 1) * 64].max()
         assert vm[b] <= nrm[b * 64:(b + 1) * 64].max() * (1 + 1e-4)
+
+
+def test_value_sq_norms_exact_cases_and_error():
+    # small integers: every partial sum is exact in float32
+    V = np.array([[3, 4, 0, 0], [1, 1, 1, 1], [0, 0, 0, 12]], np.float32)
+    assert value_sq_norms_f32(V, 3).tolist() == [25.0, 4.0, 144.0]
+    assert value_sq_norms_f32(V, 2).shape == (2,)
+    # against float64 within the sequential-sum error bound d * 2^-24
+    rng = np.random.default_rng(7)
+    W = (rng.standard_normal((200, 128)) * 5).astype(np.float32)
+    ss = value_sq_norms_f32(W, 200).astype(np.float64)
+    ref = (W.astype(np.float64) ** 2).sum(axis=1)
+    assert np.all(np.abs(ss - ref) <= 128 * 2.0 ** -24 * ref)
+    # the block bound is built from the same sums
+    vm = vmax_blocks(W, 200)
+    for b in range(4):
+        top = np.sqrt(ss[b * 64:(b + 1) * 64].astype(np.float32)).max()
+        assert vm[b] == np.float32(top) * np.float32(1 + 2.0 ** -16)
 
 
 def test_integer_dot_brute_force():

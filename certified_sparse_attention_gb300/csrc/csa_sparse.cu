@@ -493,10 +493,11 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
 
 template <int G>
 __global__ void __launch_bounds__(256) prehist_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
-  // counts as integers; heavy weights in 2^-24 fixed point (a prediction
-  // input only), all aggregated over equal levels within a warp
+  // counts as integers; heavy weights in 2^-18 fixed point (a prediction
+  // input only; at most 2^12 keys of weight <= 1 per CTA), all aggregated
+  // over equal levels within a warp
   __shared__ int s_cnt[G][kMaxJ + 1][2];            // light count delta, sampled count
-  __shared__ float s_db[G][kMaxJ + 1];
+  __shared__ unsigned s_db[G][kMaxJ + 1];
   const int tid = threadIdx.x, lane = tid & 31;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(256) prehist_kernel(const SparseArgs a, const 
   const float neg_r = -(float)a.r;
   for (int i = tid; i < G * (J + 1); i += 256) {
     const int h = i / (J + 1), l = i - h * (J + 1);
-    s_cnt[h][l][0] = 0; s_cnt[h][l][1] = 0; s_db[h][l] = 0.f;
+    s_cnt[h][l][0] = 0; s_cnt[h][l][1] = 0; s_db[h][l] = 0u;
   }
   __syncthreads();
   const int bh0 = b * a.Hq + g * G;
@@ -543,7 +544,7 @@ __global__ void __launch_bounds__(256) prehist_kernel(const SparseArgs a, const 
     hist_add_i(cnt + 1, jl <= J ? 2 * jl : -1, 1);                      // sampled at jl
     hist_add_i(cnt, jl < hl ? 2 * jl : -1, 1);                          // light from jl
     hist_add_i(cnt, (jl < hl && hl <= J) ? 2 * hl : -1, -1);            // light until hl
-    hist_add_f(s_db[h], hl <= J ? hl : -1, hl <= J ? __expf(s[h] - c32[h]) : 0.f);
+    hist_add_u(s_db[h], hl <= J ? hl : -1, hl <= J ? __float2uint_rn(__expf(s[h] - c32[h]) * 262144.f) : 0u);
   }
   }
   __syncthreads();
@@ -551,7 +552,7 @@ __global__ void __launch_bounds__(256) prehist_kernel(const SparseArgs a, const 
     const int h = i / (J + 1), l = i - h * (J + 1);
     float* dst = a.pre_hist + ((int64_t)(bh0 + h) * a.J1 + l) * 4;
     if (s_cnt[h][l][0]) atomicAdd(dst + 0, (float)s_cnt[h][l][0]);
-    if (s_db[h][l] != 0.f) atomicAdd(dst + 1, s_db[h][l]);
+    if (s_db[h][l]) atomicAdd(dst + 1, (float)s_db[h][l] * 3.814697265625e-06f);   // 2^-18
     if (s_cnt[h][l][1]) atomicAdd(dst + 2, (float)s_cnt[h][l][1]);
   }
 }

@@ -42,7 +42,7 @@ bool params_ok(const csa_params* p) {
 struct Layout {
   int J1;
   int64_t pcap, nblk_max;
-  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, zero_end;
+  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, zero_end;
   size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, s32, win, t32, clist, xlist, cmap,
       buckets, dpart, total;
   int64_t nchunk_cap;
@@ -68,6 +68,7 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.ccnt = o; o += up((size_t)BG * 4);
   L.xcnt = o; o += up((size_t)BG * 4);
   L.nfall = o; o += up(4);
+  L.rq = o; o += up(((size_t)BG * 6 + 6) * 4);
   L.zero_end = o;
   L.winstats = o; o += up((size_t)BH * (D + 4) * 4);
   L.vmaxp = o; o += up((size_t)BG * 4);
@@ -298,6 +299,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   a.bcons = (unsigned*)(ws + L.bcons); a.buckets = (uint2*)(ws + L.buckets);
   a.t32 = (float*)(ws + L.t32); a.clist = (uint2*)(ws + L.clist); a.ccnt = (unsigned*)(ws + L.ccnt);
   a.nfall = (unsigned*)(ws + L.nfall);
+  a.rq = (unsigned*)(ws + L.rq);
   a.xlist = (uint2*)(ws + L.xlist); a.xcnt = (unsigned*)(ws + L.xcnt);
   a.chunk_map = (unsigned*)(ws + L.cmap); a.nchunk_cap = L.nchunk_cap;
   a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);

@@ -43,6 +43,8 @@ struct SparseArgs {
   uint2* clist;           // [B*Hkv][pcap]        candidates to rescore: key, head mask
   unsigned* ccnt;         // [B*Hkv]
   unsigned* nfall;        // heads that need the exact fallback
+  unsigned* rq;           // round queues: [3][B*Hkv] groups per round, [3][B*Hkv] flags,
+                          // [3] group counts, [3] work-item counters
   unsigned* bcnt;         // [B*Hkv][J1]
   unsigned* bcons;        // [B*Hkv][J1]
   uint2* buckets;         // [B*Hkv][J1][pcap]    key, event masks (add | trans<<8 | before<<16)

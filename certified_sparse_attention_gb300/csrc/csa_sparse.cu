@@ -70,6 +70,16 @@ __device__ __forceinline__ float cmax_get(const SparseArgs& a, int bh, int k) {
   return float_of_ord(a.cmax[(int64_t)bh * 4 + k]);
 }
 
+// Round queues: the (sequence, KV head) groups that take part in gather
+// round r, each listed once (rq layout in SparseArgs).
+__device__ __forceinline__ void rq_push(const SparseArgs& a, int r, int bg) {
+  const int BG = a.B * a.Hkv;
+  if (atomicOr(a.rq + 3 * BG + r * BG + bg, 1u) == 0u) {
+    const unsigned i = atomicAdd(a.rq + 6 * BG + r, 1u);
+    a.rq[r * BG + i] = (unsigned)bg;
+  }
+}
+
 // Warp-aggregated append of this lane's item to a global list (lanes with
 // want = false take no slot).  Returns the slot or -1.
 __device__ __forceinline__ int warp_append(unsigned* counter, bool want) {
@@ -719,106 +729,117 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
       st[0] = -1; st[1] = hi; st[2] = -1; st[3] = 0;
     }
   }
+  if (tid == 0) rq_push(a, 0, bg);
 }
 
 // --------------------------------------------------------- level buckets
 
+constexpr int kLevItem = 2048;   // keys per work item of the level pass
+
+// One work item: keys [k0, k0 + kLevItem) of group bg.
 template <int G>
-__global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
-  __shared__ unsigned s_cnt[kMaxJ + 1];
-  __shared__ unsigned s_base[kMaxJ + 1];
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+__device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& seq, int bg, int64_t k0) {
+  const int lane = threadIdx.x & 31;
+  const int b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
   const int64_t P = n - kWindow;
-  const int64_t key0 = (int64_t)blockIdx.x * kTile;
-  if (key0 >= P) return;
+  if (k0 >= P) return;
+  const int64_t kend = min(P, k0 + kLevItem);
   const int J = seq.J[b];
   const int bh0 = b * a.Hq + g * G;
   int lo[G], hi[G];
-  bool any = false;
+  int wlo = J + 1, whi = -1;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     const int* st = a.state + (int64_t)(bh0 + h) * 4;
     lo[h] = st[0];
     hi[h] = (st[3] & kFlagDone) ? st[0] : st[1];
-    any |= hi[h] > lo[h];
+    if (hi[h] > lo[h]) { wlo = min(wlo, lo[h] + 1); whi = max(whi, hi[h]); }
   }
-  if (!any) return;
-  for (int i = tid; i <= J; i += 256) s_cnt[i] = 0u;
-  __syncthreads();
+  if (whi < 0) return;
+  float c32[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
   const float neg_r = -(float)a.r;
-  const int64_t key = key0 + tid;
-  int jl[G], hl[G];
-  bool some = false;
+  unsigned* bcnt = a.bcnt + (int64_t)bg * a.J1;
+  uint2* bk = a.buckets + (int64_t)bg * a.J1 * a.pcap;
+  const float* sb = a.s32 + (int64_t)bg * a.pcap * G;
+  const float* tb = a.t32 + (int64_t)bg * a.pcap;
+  for (int64_t key0 = k0; key0 < kend; key0 += 256) {
+    const int64_t key = key0 + threadIdx.x;
+    int jl[G], hl[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) { jl[h] = J + 1; hl[h] = J + 1; }
-  if (key < P) {
-    const float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
-    float sv[G];
-    if (G == 4) {
-      const float4 f = *reinterpret_cast<const float4*>(sp);
-      sv[0] = f.x; sv[1 % G] = f.y; sv[2 % G] = f.z; sv[3 % G] = f.w;
-    } else {
+    for (int h = 0; h < G; ++h) { jl[h] = J + 1; hl[h] = J + 1; }
+    if (key < kend) {
+      float sv[G];
+      if (G == 4) {
+        const float4 f = *reinterpret_cast<const float4*>(sb + key * G);
+        sv[0] = f.x; sv[1 % G] = f.y; sv[2 % G] = f.z; sv[3 % G] = f.w;
+      } else {
 #pragma unroll
-      for (int h = 0; h < G; ++h) sv[h] = sp[h];
+        for (int h = 0; h < G; ++h) sv[h] = sb[key * G + h];
+      }
+      const float t = tb[key];
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        if (sv[h] > -INFINITY) exact_levels(sv[h], c32[h], t, neg_r, J, jl[h], hl[h]);
     }
-    const float t = a.t32[(int64_t)bg * a.pcap + key];
+    // events of the key in the round (a light entry at jl < hl, the
+    // light-to-heavy transition at hl), as a mask over 32-level windows
+    for (int base = wlo; base <= whi; base += 32) {
+      unsigned evm = 0;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      if (sv[h] > -INFINITY) {
-        exact_levels(sv[h], cmax_get(a, bh0 + h, 3), t, neg_r, J, jl[h], hl[h]);
-        some = true;
+      for (int h = 0; h < G; ++h) {
+        const int e1 = jl[h] - base, e2 = hl[h] - base;
+        if (jl[h] < hl[h] && jl[h] > lo[h] && jl[h] <= hi[h] && e1 >= 0 && e1 < 32) evm |= 1u << e1;
+        if (hl[h] <= J && hl[h] > lo[h] && hl[h] <= hi[h] && e2 >= 0 && e2 < 32) evm |= 1u << e2;
+      }
+      while (__any_sync(0xffffffffu, evm != 0u)) {
+        int l = -1;
+        if (evm) {
+          l = base + __ffs(evm) - 1;
+          evm &= evm - 1u;
+        }
+        unsigned m = 0;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          if (!(l > lo[h] && l <= hi[h])) continue;
+          if (jl[h] == l && jl[h] < hl[h]) m |= 1u << h;
+          if (hl[h] == l) {
+            m |= 1u << (8 + h);
+            if (jl[h] < hl[h]) m |= 1u << (16 + h);
+          }
+        }
+        // lanes with the same level take consecutive slots of its bucket
+        const unsigned grp = __match_any_sync(0xffffffffu, l);
+        const int leader = __ffs(grp) - 1;
+        unsigned p0 = 0;
+        if (lane == leader && l >= 0) p0 = atomicAdd(bcnt + l, (unsigned)__popc(grp));
+        p0 = __shfl_sync(0xffffffffu, p0, leader);
+        if (l >= 0) {
+          const unsigned p = p0 + (unsigned)__popc(grp & ((1u << lane) - 1u));
+          if (p < (unsigned)a.pcap) bk[(int64_t)l * a.pcap + p] = make_uint2((unsigned)key, m);
+          else atomicOr(a.status, 2u);
+        }
       }
     }
   }
-  // event levels of this key in the round: a light entry at j (j < h) and
-  // the light-to-heavy transition at h, per head whose range holds them
-  int lv[2 * G], pos[2 * G];
-  unsigned mk[2 * G];
-  int nl = 0;
-  if (some) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const int c1 = (jl[h] < hl[h] && jl[h] > lo[h] && jl[h] <= hi[h]) ? jl[h] : -1;
-      const int c2 = (hl[h] <= J && hl[h] > lo[h] && hl[h] <= hi[h]) ? hl[h] : -1;
-      if (c1 >= 0) { bool dup = false; for (int x = 0; x < nl; ++x) dup |= lv[x] == c1; if (!dup) lv[nl++] = c1; }
-      if (c2 >= 0) { bool dup = false; for (int x = 0; x < nl; ++x) dup |= lv[x] == c2; if (!dup) lv[nl++] = c2; }
-    }
-  }
-  for (int x = 0; x < nl; ++x) {
-    const int l = lv[x];
-    unsigned m = 0;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      if (!(l > lo[h] && l <= hi[h])) continue;
-      if (jl[h] == l && jl[h] < hl[h]) m |= 1u << h;
-      if (hl[h] == l) {
-        m |= 1u << (8 + h);
-        if (jl[h] < hl[h]) m |= 1u << (16 + h);
-      }
-    }
-    mk[x] = m;
-  }
-  // shared-memory slots, aggregated over the warp's lanes with equal level
-  const int maxl = (int)__reduce_max_sync(0xffffffffu, (unsigned)nl);
-  for (int x = 0; x < maxl; ++x) {
-    const int l = x < nl ? lv[x] : -1;
-    const int p = slot_add(s_cnt, l);
-    if (l >= 0) pos[x] = p;
-  }
-  __syncthreads();
-  for (int i = tid; i <= J; i += 256)
-    if (s_cnt[i]) s_base[i] = atomicAdd(a.bcnt + (int64_t)bg * a.J1 + i, s_cnt[i]);
-  __syncthreads();
-  for (int x = 0; x < nl; ++x) {
-    const int l = lv[x];
-    const unsigned p = s_base[l] + (unsigned)pos[x];
-    if (p < (unsigned)a.pcap)
-      a.buckets[((int64_t)bg * a.J1 + l) * a.pcap + p] = make_uint2((unsigned)key, mk[x]);
-    else
-      atomicOr(a.status, 2u);
+}
+
+template <int G>
+__global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+                                                     int round, unsigned tpg) {
+  __shared__ unsigned s_item;
+  const int BG = a.B * a.Hkv;
+  const unsigned total = a.rq[6 * BG + round] * tpg;
+  for (;;) {
+    if (threadIdx.x == 0) s_item = atomicAdd(a.rq + 6 * BG + 3 + round, 1u);
+    __syncthreads();
+    const unsigned item = s_item;
+    __syncthreads();
+    if (item >= total) break;
+    levels_item<G>(a, seq, (int)a.rq[round * BG + item / tpg], (int64_t)(item % tpg) * kLevItem);
   }
 }
 
@@ -1530,6 +1551,7 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       int nh = (round == 0) ? hi + 2 * a.r : J;
       st[0] = hi;
       st[1] = nh > J ? J : nh;
+      if (round < 2) rq_push(a, round + 1, bg);
     }
   }
 }
@@ -1696,8 +1718,15 @@ cudaError_t launch_predict(const SparseArgs& a, const SeqArgs& seq, int d, int G
 }
 cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t pmax_live,
                          int round, int nsm, cudaStream_t st, PhaseMark mark) {
-  dim3 grid((unsigned)((pmax_live + kTile - 1) / kTile), (unsigned)(a.B * a.Hkv));
-  CSA_G_SWITCH(levels_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  // eight 256-thread CTAs per SM pull work items (kLevItem keys of a group
+  // listed for this round) from the round's queue
+  const unsigned tpg = (unsigned)((pmax_live + kLevItem - 1) / kLevItem);
+  int64_t nct = 8 * (int64_t)nsm;
+  const int64_t items = (int64_t)tpg * a.B * a.Hkv;
+  if (nct > items) nct = items;
+  if (nct < 1) nct = 1;
+  dim3 grid((unsigned)nct);
+  CSA_G_SWITCH(levels_kernel, <<<grid, 256, 0, st>>>(a, seq, round, tpg))
   if (mark) mark(6, st);
   const int nent = a.B * a.Hkv * a.J1;
   CSA_DG_SWITCH(launch_vgather_t, (nsm, st, a, seq, nent, mark))

@@ -139,28 +139,37 @@ __device__ __forceinline__ int slot_add(unsigned* base, int v) {
 }
 
 // Chernoff interval for a Poisson-binomial count k (two-sided, budget
-// delta_e / 2 per side): mu = k e^y with e^y - 1 - y = Lz / k.  Returns
-// k - mu_lo and mu_hi - k (both >= 0), bracket ends taken outward.
+// delta_e / 2 per side): mu = k e^y with phi(y) = e^y - 1 - y = Lz / k.
+// Returns k - mu_lo and mu_hi - k (both >= 0).  phi is convex, so Newton's
+// iteration started outside a root (where phi > Lz / k) stays outside and
+// converges to it monotonically: the iterates are outward ends of the
+// root's bracket, as the certificate needs.
 __device__ __forceinline__ float phi_y(float y) {
   if (fabsf(y) < 0.05f) return y * y * (0.5f + y * (1.0f / 6.0f + y * (1.0f / 24.0f + y * (1.0f / 120.0f))));
   return expm1f(y) - y;
 }
 __device__ void chernoff_gaps(float k, float Lz, float& below, float& above) {
   if (!(k > 0.f)) { below = 0.f; above = Lz; return; }
-  float c0 = Lz / k;
-  float lo = 0.f, hi = fmaxf(1.0f, logf(3.0f * c0 + 3.0f));
+  const float c0 = Lz / k;
+  // upper root: start where phi >= c0, step down the tangent
+  float hi = fmaxf(1.0f, logf(3.0f * c0 + 3.0f));
   for (int it = 0; it < 8 && phi_y(hi) < c0; ++it) hi *= 2.0f;
-  for (int it = 0; it < 48; ++it) {
-    float mid = 0.5f * (lo + hi);
-    if (phi_y(mid) <= c0) lo = mid; else hi = mid;
+  for (int it = 0; it < 12; ++it) {
+    const float f = phi_y(hi) - c0;
+    const float nx = hi - f / expm1f(hi);
+    if (!(nx < hi) || phi_y(nx) < c0) break;   // converged (or rounding crossed the root)
+    hi = nx;
   }
   above = k * expm1f(hi);
-  float a = -(c0 + 1.0f), b2 = 0.f;
-  for (int it = 0; it < 48; ++it) {
-    float mid = 0.5f * (a + b2);
-    if (phi_y(mid) > c0) a = mid; else b2 = mid;
+  // lower root: start at -(c0 + 1) (phi > c0 there), step up the tangent
+  float lo = -(c0 + 1.0f);
+  for (int it = 0; it < 12; ++it) {
+    const float f = phi_y(lo) - c0;
+    const float nx = lo - f / expm1f(lo);
+    if (!(nx > lo) || nx >= 0.f || phi_y(nx) < c0) break;
+    lo = nx;
   }
-  below = -k * expm1f(a);
+  below = -k * expm1f(lo);
 }
 
 // Stage eight rows (row indices ent[0..nvalid).x) of a [rows][D] array into
@@ -604,6 +613,7 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
 #pragma unroll
     for (int c = 0; c < CPL; ++c) nr[h][c] = 0.f;
   }
+#pragma unroll
   for (int row = w; row < kWindow; row += 8) {
     float v[CPL];
     load_row<D, E>(Vb + (int64_t)row * D, v);
@@ -631,6 +641,7 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
   {
     const int64_t nbp = (P + kBlock - 1) / kBlock;
     float m = 0.f;
+#pragma unroll 8
     for (int64_t i = tid; i < nbp; i += 256) m = fmaxf(m, a.vmax[(int64_t)bg * a.nblk_max + i]);
     m = warp_max(m);
     if (lane == 0) s_vm[w] = m;
@@ -1069,8 +1080,14 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
 // the sampled-key flag.  One batch is (D/8 + 1) mma per 16 rows of A.  The
 // accumulators go to the per-level sums with vector reductions whenever the
 // bucket changes and at the end of the range.
-constexpr int kVsW = 4;                         // warps per CTA
-constexpr int kVsS = 3;                         // row stages per warp
+#ifndef CSA_VS_WARPS
+#define CSA_VS_WARPS 4
+#endif
+#ifndef CSA_VS_STAGES
+#define CSA_VS_STAGES 3
+#endif
+constexpr int kVsW = CSA_VS_WARPS;              // warps per CTA
+constexpr int kVsS = CSA_VS_STAGES;             // row stages per warp (>= 2)
 constexpr int kVsE = 2 * kVsS;                  // entry / descriptor slots per warp
 constexpr int kVsB = 16;                        // entries per batch (mma k)
 
@@ -1084,9 +1101,10 @@ struct VsLayout {
   static constexpr int vn = sc + kVsS * kVsB * SCB;
   static constexpr int ent = vn + kVsS * kVsB * 4;
   static constexpr int desc = ent + kVsE * kVsB * 8;             // [e, entry offset, count, bg, c32 x 8]
-  static constexpr int at = desc + kVsE * 64;                    // A^T: [16 entries][16 MT] bf16
-  static constexpr int bx = at + kVsB * MT * 32;                 // [16 entries][8] bf16
-  static constexpr int per_warp = bx + kVsB * 16;
+  static constexpr int atb = kVsB * MT * 32;                     // A^T: [16 entries][16 MT] bf16
+  static constexpr int at = desc + kVsE * 64;                    // two A^T buffers
+  static constexpr int bx = at + 2 * atb;                        // two [16 entries][8] bf16
+  static constexpr int per_warp = bx + 2 * kVsB * 16;
   static constexpr int smem = kVsW * per_warp;
 };
 
@@ -1295,65 +1313,79 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
     issue_rows(i, i);
     cp_async_commit();
   }
+  // coefficient tile of the batch in descriptor slot b_ds / stage b_ss into
+  // tile buffer buf: lane k (mod 16) is entry k, lanes 0-15 take heads
+  // [0, G/2) and lanes 16-31 heads [G/2, G); branch-free, so it shares a
+  // basic block with the previous batch's products
+  auto prep = [&](int b_ds, int b_ss, int buf) {
+    constexpr int HH = G >= 2 ? G / 2 : 1;
+    const int* dq = s_desc + b_ds * 16;
+    const int k = lane & 15, hf = lane >> 4;
+    const int h0 = G >= 2 ? hf * HH : 0;
+    const bool ok = k < dq[2];
+    const unsigned m = ok ? s_ent[b_ds * kVsB + k].y : 0u;
+    const float* sc = reinterpret_cast<const float*>(s_sc + (b_ss * kVsB + k) * Lt::SCB);
+    float cf[HH], wh[HH], wl[HH], ns[HH];
+#pragma unroll
+    for (int t = 0; t < HH; ++t) {
+      const int h = h0 + t;
+      const bool add = m & (1u << h), trn = m & (1u << (8 + h)), bef = m & (1u << (16 + h));
+      const float x = fsub(sc[h], float_of_ord((unsigned)dq[4 + h]));
+      const float wt = trn ? __expf(x) : 0.f;
+      cf[t] = add ? 1.f : ((trn && bef) ? -1.f : 0.f);
+      wh[t] = __bfloat162float(__float2bfloat16_rn(wt));
+      wl[t] = wt - wh[t];
+      ns[t] = (add || (trn && !bef)) ? 1.f : 0.f;
+    }
+    uint8_t* arow = s_at + buf * Lt::atb + k * MT * 32;
+    if constexpr (HH >= 2) {
+#pragma unroll
+      for (int t = 0; t < HH; t += 2) {
+        const int e0 = h0 + t;
+        *reinterpret_cast<unsigned*>(arow + 2 * (0 * G + e0)) = pack_bf16(cf[t], cf[t + 1]);
+        *reinterpret_cast<unsigned*>(arow + 2 * (1 * G + e0)) = pack_bf16(wh[t], wh[t + 1]);
+        *reinterpret_cast<unsigned*>(arow + 2 * (2 * G + e0)) = pack_bf16(wl[t], wl[t + 1]);
+        *reinterpret_cast<unsigned*>(arow + 2 * (3 * G + e0)) = pack_bf16(ns[t], ns[t + 1]);
+      }
+    } else {
+      *reinterpret_cast<__nv_bfloat16*>(arow + 2 * (0 * G + h0)) = __float2bfloat16_rn(cf[0]);
+      *reinterpret_cast<__nv_bfloat16*>(arow + 2 * (1 * G + h0)) = __float2bfloat16_rn(wh[0]);
+      *reinterpret_cast<__nv_bfloat16*>(arow + 2 * (2 * G + h0)) = __float2bfloat16_rn(wl[0]);
+      *reinterpret_cast<__nv_bfloat16*>(arow + 2 * (3 * G + h0)) = __float2bfloat16_rn(ns[0]);
+    }
+    const float vn = s_vn[b_ss * kVsB + k];
+    const float vh = __bfloat162float(__float2bfloat16_rn(vn));
+    *reinterpret_cast<uint4*>(s_bx + buf * kVsB * 16 + k * 16) =
+        make_uint4(pack_bf16(1.f, vh), pack_bf16(vn - vh, 0.f), 0u, 0u);
+  };
+  // rows of A past 4G stay zero in both buffers
+  for (int i = lane; i < 2 * Lt::atb / 16; i += 32) reinterpret_cast<uint4*>(s_at)[i] = make_uint4(0u, 0u, 0u, 0u);
+  cp_async_wait<kVsS - 1>();
+  __syncwarp();
+  prep(0, 0, 0);
   for (int i = 0;; ++i) {
-    const int ds = i % kVsE, ss = i % kVsS;
-    cp_async_wait<kVsS - 1>();
-    __syncwarp();
+    const int ds = i % kVsE, ss = i % kVsS, buf = i & 1;
     const int* dp = s_desc + ds * 16;
     const int e = dp[0], cnt = dp[2];
     if (cnt <= 0) break;
+    cp_async_wait<kVsS - 2>();     // rows of batch i + 1 (for its tile)
+    __syncwarp();
     if (e != cur) {
       if (cur >= 0) flush();
       cur = e;
       cur_bg = dp[3];
     }
-    if (lane < kVsB) {
-      const uint2 ev = lane < cnt ? s_ent[ds * kVsB + lane] : make_uint2(0u, 0u);
-      const unsigned m = ev.y;
-      const float* sc = reinterpret_cast<const float*>(s_sc + (ss * kVsB + lane) * Lt::SCB);
-      const float vn = s_vn[ss * kVsB + lane];
-      float cf[G], wh[G], wl[G], ns[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const bool add = m & (1u << h), trn = m & (1u << (8 + h)), bef = m & (1u << (16 + h));
-        float wt = 0.f;
-        if (trn) wt = __expf(fsub(sc[h], float_of_ord((unsigned)dp[4 + h])));
-        cf[h] = add ? 1.f : ((trn && bef) ? -1.f : 0.f);
-        wh[h] = __bfloat162float(__float2bfloat16_rn(wt));
-        wl[h] = wt - wh[h];
-        ns[h] = (add || (trn && !bef)) ? 1.f : 0.f;
-      }
-      auto coef = [&](int row) -> float {
-        if (row < G) return cf[row];
-        if (row < 2 * G) return wh[row - G];
-        if (row < 3 * G) return wl[row - 2 * G];
-        if (row < 4 * G) return ns[row - 3 * G];
-        return 0.f;
-      };
-      uint4* arow = reinterpret_cast<uint4*>(s_at + lane * MT * 32);
-#pragma unroll
-      for (int q = 0; q < 2 * MT; ++q) {
-        uint4 u;
-        u.x = pack_bf16(coef(8 * q + 0), coef(8 * q + 1));
-        u.y = pack_bf16(coef(8 * q + 2), coef(8 * q + 3));
-        u.z = pack_bf16(coef(8 * q + 4), coef(8 * q + 5));
-        u.w = pack_bf16(coef(8 * q + 6), coef(8 * q + 7));
-        arow[q] = u;
-      }
-      const float vh = __bfloat162float(__float2bfloat16_rn(vn));
-      *reinterpret_cast<uint4*>(s_bx + lane * 16) = make_uint4(pack_bf16(1.f, vh), pack_bf16(vn - vh, 0.f), 0u, 0u);
-    }
-    __syncwarp();
+    prep((i + 1) % kVsE, (i + 1) % kVsS, buf ^ 1);
     // A fragments (A^T stored entry-major): matrices (rows m 0-7 | 8-15) x (k 0-7 | 8-15)
     unsigned af[MT][4];
     {
       const int mi = lane >> 3, rr = lane & 7;
       const int k = (mi >> 1) * 8 + rr, mh = mi & 1;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) ldsm_x4_trans(af[mt], s_at + k * MT * 32 + mt * 32 + mh * 16);
+      for (int mt = 0; mt < MT; ++mt) ldsm_x4_trans(af[mt], s_at + buf * Lt::atb + k * MT * 32 + mt * 32 + mh * 16);
     }
     unsigned bxf[2];
-    ldsm_x2_trans(bxf, s_bx + (lane & 15) * 16);
+    ldsm_x2_trans(bxf, s_bx + buf * kVsB * 16 + (lane & 15) * 16);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(C[mt][NT], af[mt], bxf[0], bxf[1]);
     const uint8_t* stg = s_rows + ss * kVsB * RB;
@@ -1426,9 +1458,19 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
   const float L = logf(1.0f / de), Lz = logf(2.0f / de);
   const float* accb = a.acc + (int64_t)bh * a.J1 * ACC;
   int found = -1;
+  // prefix over the levels of earlier rounds; eight independent loads at a
+  // time so the L2 latency is paid once per eight levels
   for (int x = tid; x < ACC; x += 256) {
     float run = 0.f;
-    for (int l = 0; l <= lo; ++l) run += accb[(int64_t)l * ACC + x];
+    int l = 0;
+    for (; l + 8 <= lo + 1; l += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = accb[(int64_t)(l + u) * ACC + x];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) run += v[u];
+    }
+    for (; l <= lo; ++l) run += accb[(int64_t)l * ACC + x];
     s_run[x] = run;
   }
   __syncthreads();
@@ -1436,7 +1478,15 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
     const int nl = min(LB, hi - l0 + 1);
     for (int x = tid; x < ACC; x += 256) {
       float run = s_run[x];
-      for (int i = 0; i < nl; ++i) {
+      int i = 0;
+      for (; i + 8 <= nl; i += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = accb[(int64_t)(l0 + i + u) * ACC + x];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) { run += v[u]; s_pre[i + u][x] = run; }
+      }
+      for (; i < nl; ++i) {
         run += accb[(int64_t)(l0 + i) * ACC + x];
         s_pre[i][x] = run;
       }
@@ -1515,10 +1565,14 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       const float Dh = s_dh[i];
       for (int c = tid; c < D; c += 256)
         a.o[(int64_t)bh * D + c] = (s_win[c] + s_pre[i][D + c] + tau * s_pre[i][c]) / Dh;
-      if (tid == 0) {
+      // rows read up to the stop level: warp 0 sums the bound-level histogram
+      unsigned kr = 0;
+      if (w == 0) {
         const unsigned* jr = a.jr_hist + (int64_t)bh * (a.J1 + 1);
-        unsigned kr = 0;
-        for (int l = 0; l <= found; ++l) kr += jr[l];
+        for (int l = lane; l <= found; l += 32) kr += jr[l];
+        kr = __reduce_add_sync(0xffffffffu, kr);
+      }
+      if (tid == 0) {
         const int vr = kWindow + (int)s_pre[i][2 * D + 4];
         a.beta[bh] = s_beta[i];
         a.level[bh] = found;

@@ -73,6 +73,12 @@ def barrier(world: int):
         dist.barrier()
 
 
+def workload_name(w) -> str:
+    return (f"{WORKLOAD}: B={w.B} sequences x 1 layer per step, n={w.n}, "
+            f"Hq={w.Hq}, Hkv={w.Hkv}, d={w.d}, bf16, eps={w.eps}, "
+            f"delta={w.delta}, r={w.r}")
+
+
 def algorithmic_bytes(stats, w, n):
     """Bytes the method must move per step (per (sequence, KV head)):
     scan |P| (d/2 + 8d/64 + 4/64) over the pool + the window's 64 scan rows,
@@ -371,10 +377,7 @@ def run_ours(args, world, rank, local):
                 "outlier channels x8 and 32 needles per KV head; values "
                 "N(0,1) x lognormal(0,0.5); half the groups near-uniform); "
                 "stands in for the pages' real KV caches",
-        "config": {"workload": f"{WORKLOAD}: B={w.B} sequences x 1 layer "
-                               f"per step, n={w.n}, Hq={w.Hq}, Hkv={w.Hkv}, "
-                               f"d={w.d}, bf16, eps={w.eps}, "
-                               f"delta={w.delta}, r={w.r}",
+        "config": {"workload": workload_name(w),
                    "layers_rotated": args.layers,
                    "l2": f"inputs larger than L2: {args.layers} resident "
                          f"layers (~{args.layers * 2.3:.0f} GB) rotated "
@@ -421,10 +424,11 @@ def run_reference(args, world, rank, local):
     one = synth.workload(WORKLOAD, B=1, Hq=w.G, Hkv=1)
     K, V, meta = synth.kv_numpy(one)
     times = []
-    # each sample costs seconds of host time: at most 6 timed samples
+    # each sample costs seconds of host time: at most 3 warm-up and 6 timed
+    # samples (the line reports the counts actually run)
     nsteps = max(1, min(args.steps, 6))
     args.steps = nsteps
-    args.warmup = min(args.warmup, 1)
+    args.warmup = min(args.warmup, 3)
     for s in range(args.warmup + args.steps):
         q = synth.q_numpy(one, meta, s)
         seed = int(synth.step_seeds(one, s)[0])
@@ -441,8 +445,7 @@ def run_reference(args, world, rank, local):
         "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same generator and workload as the GPU arm)",
-        "config": {"workload": f"{WORKLOAD}: B={wfull.B}, n={wfull.n}, "
-                               f"Hq={wfull.Hq}, Hkv={wfull.Hkv}, d={wfull.d}"},
+        "config": {"workload": workload_name(wfull)},
         "cpu_baseline": {"value": round(us, 1), "unit": "us/step",
                          "cores": 1, "kind": "oracle",
                          "sample": "one (sequence, KV head) group (4 query "

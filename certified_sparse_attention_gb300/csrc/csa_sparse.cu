@@ -436,6 +436,10 @@ template <int G>
 __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
   __shared__ unsigned s_jr[G][kMaxJ + 2];
   __shared__ unsigned s_nc[G];
+  // the CTA's candidates, staged here and written out with one global slot
+  // reservation (a per-warp reservation on the group's counter serialises)
+  __shared__ uint2 s_list[kTile * kTilesPerCta];
+  __shared__ unsigned s_n, s_gbase;
   const int tid = threadIdx.x, lane = tid & 31;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
@@ -447,6 +451,7 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   const float neg_r = -(float)a.r;
   for (int i = tid; i < G * (J + 2); i += 256) (&s_jr[0][0])[(i / (J + 2)) * (kMaxJ + 2) + i % (J + 2)] = 0u;
   if (tid < G) s_nc[tid] = 0u;
+  if (tid == 0) s_n = 0u;
   __syncthreads();
   const int bh0 = b * a.Hq + g * G;
   const unsigned long long gk = group_key(seq.seed[b], g);
@@ -496,10 +501,13 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
 #pragma unroll
     for (int h = 0; h < G; ++h) sp[h] = -INFINITY;
   }
-  const int slot = warp_append(a.ccnt + bg, live && !inset && cm);
-  if (slot >= 0) a.clist[(int64_t)bg * a.pcap + slot] = make_uint2((unsigned)key, cm);
+  const int slot = warp_append(&s_n, live && !inset && cm);
+  if (slot >= 0) s_list[slot] = make_uint2((unsigned)key, cm);
   }
   __syncthreads();
+  if (tid == 0) s_gbase = s_n ? atomicAdd(a.ccnt + bg, s_n) : 0u;
+  __syncthreads();
+  for (unsigned i = tid; i < s_n; i += 256) a.clist[(int64_t)bg * a.pcap + s_gbase + i] = s_list[i];
   for (int i = tid; i < G * (J + 2); i += 256) {
     int h = i / (J + 2), l = i - h * (J + 2);
     unsigned v = s_jr[h][l];

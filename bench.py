@@ -258,6 +258,9 @@ def run_ours(args, world, rank, local):
     barrier(world)
     ms_sparse = e0.elapsed_time(e1) / args.steps
     launches = csa.csa_profile_read()["launches"]
+    # the device status word of the last timed step (non-finite inputs, an
+    # exhausted buffer): a failing run prints no number
+    csa.check(csa.csa_check(step.ws, stream), "csa_check (timed steps)")
     # same-build dense comparator over the same rotation
     e0.record(stream)
     for (L, s) in plan:

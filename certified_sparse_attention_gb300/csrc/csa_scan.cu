@@ -62,8 +62,17 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
   if (key0 >= n) return;
   const int64_t nblk_n = (n + kBlock - 1) / kBlock;
 
-  // 1. stage codes and block bounds
+  // 1. stage the block bounds (first group: the query prep needs them) and
+  // the codes (second group: the dot products need them)
   {
+    const int64_t blk0 = key0 / kBlock;
+    const float* bsrc = a.bounds + ((int64_t)bg * a.nblk_max + blk0) * 2 * D;
+    for (int c = tid; c < 4 * 2 * D / 4; c += 256) {
+      int blk = c / (2 * D / 4);
+      bool ok = blk0 + blk < nblk_n;
+      cp_async16(reinterpret_cast<float*>(s_bnd) + c * 4, ok ? bsrc + (int64_t)c * 4 : a.bounds, ok);
+    }
+    cp_async_commit();
     const uint8_t* src = a.K4 + ((int64_t)bg * a.nblk_max * kBlock + key0) * ROWB;
     const int64_t rows_valid = nblk_n * kBlock - key0;
 #pragma unroll
@@ -71,14 +80,6 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
       int row = c / CHR;
       bool ok = row < rows_valid;
       cp_async16(s_codes + c * 16, ok ? src + (int64_t)c * 16 : a.K4, ok);
-    }
-    cp_async_commit();
-    const int64_t blk0 = key0 / kBlock;
-    const float* bsrc = a.bounds + ((int64_t)bg * a.nblk_max + blk0) * 2 * D;
-    for (int c = tid; c < 4 * 2 * D / 4; c += 256) {
-      int blk = c / (2 * D / 4);
-      bool ok = blk0 + blk < nblk_n;
-      cp_async16(reinterpret_cast<float*>(s_bnd) + c * 4, ok ? bsrc + (int64_t)c * 4 : a.bounds, ok);
     }
     cp_async_commit();
   }
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
       if (lane == 0) s_q1[w] = s;
     }
   }
-  cp_async_wait<1>();
+  cp_async_wait<1>();            // the bounds group has landed
   __syncthreads();
 
   // 2. per (block, head) query code
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
       reinterpret_cast<unsigned short*>(&s_atw[blk][h][WE])[l16] = od;
     }
   }
-  cp_async_wait<0>();
+  cp_async_wait<0>();            // the codes too
   __syncthreads();
 
   // 3. bounds per key

@@ -8,8 +8,13 @@ import os
 import numpy as np
 
 import synth
+from oracle.certificate import certificate_levels
+from oracle.hashing import perturb_t
+from oracle.step import Params, dense_attention, level_sums, oracle_decode_group
 
 F = np.float32
+TOL = 2e-3      # o and beta, relative
+NEAR = 1e-5     # nats: memberships this close to a threshold may differ
 
 
 def ensure_built():
@@ -61,6 +66,30 @@ class GpuRun:
         csa.check(csa.csa_check(self.step.ws), "csa_check")
         self.map = csa.csa_workspace_layout(self.shape, self.params)
 
+    def rerun(self, q, lens, seeds):
+        """The same caches, a new step: fresh queries, lengths and seeds."""
+        import torch
+        self.lens = [int(x) for x in lens]
+        self.seeds = [int(x) for x in seeds]
+        self.q = to_dev(q, self.w.dtype, self.q.device)
+        self.step(self.q, self.K, self.V, self.meta, self.lens, self.seeds)
+        torch.cuda.synchronize()
+        self.csa.check(self.csa.csa_check(self.step.ws), "csa_check")
+
+    def append(self, b, pos, k_row, v_row):
+        """Write token `pos` of sequence b (all KV heads; [Hkv, d] rows) and
+        re-quantise its block, as a decode step does after appending."""
+        import torch
+        dt = self.K.dtype
+        self.K[b, :, pos] = torch.from_numpy(np.ascontiguousarray(k_row)).to(self.K.device).to(dt)
+        self.V[b, :, pos] = torch.from_numpy(np.ascontiguousarray(v_row)).to(self.V.device).to(dt)
+        lens = list(self.lens)
+        lens[b] = max(lens[b], pos + 1)
+        self.csa.check(self.csa.csa_quantize_keys(self.shape, self.K, self.V,
+                                                  lens, pos, *self.meta),
+                       "csa_quantize_keys")
+        self.lens = lens
+
     def ws_view(self, off, count, dtype):
         import torch
         nbytes = count * 4
@@ -105,3 +134,106 @@ def gpu_levels(s32, c32, t, r, J):
         out = np.where(v <= F(J), np.maximum(np.ceil(v), 0), J + 1)
         return np.where(np.isnan(v), J + 1, out).astype(np.int64)
     return lvl(F(-r) * x), lvl(F(-r) * y)
+
+
+# ------------------------------------------- comparison with the oracle
+
+def compare_group(run, w, K, V, q, b, g, res, p, report):
+    ub = run.ubar()
+    cm = run.cmax()
+    s32 = run.s32()
+    o_g, beta_g, lvl_g, kr_g, stats = run.outputs()
+    n = run.lens[b]
+    P = n - 64
+    J = res.J
+    Vd = V[b, g, :n].astype(np.float64)
+    t = perturb_t(run.seeds[b], g, np.arange(P))
+    needK, needV = set(), set()
+    for h in range(w.G):
+        hq = g * w.G + h
+        det = res.detail[h]
+        # bit-exact bounds, maxima and candidates
+        assert np.array_equal(ub[b, g, :n, h], det["ubar"]), (b, g, h)
+        assert cm[b, hq, 0] == det["c_lo"] and cm[b, hq, 1] == det["c_hi"]
+        assert cm[b, hq, 2] == det["cb"]
+        cand_g = np.isfinite(s32[b, g, :P, h])
+        assert np.array_equal(cand_g, det["cand"]), (b, g, h)
+        assert stats[b, hq, 3] == res.n_candidates[h]
+        # memberships: device float32 vs oracle float64
+        c32 = cm[b, hq, 3]
+        jg, hg = gpu_levels(s32[b, g, :P, h], c32, t, p.r, J)
+        # levels beyond the grid are all "never" (J + 1)
+        jo = np.minimum(det["jl_c"], J + 1)
+        ho = np.minimum(det["hl_c"], J + 1)
+        jg = np.where(cand_g, jg, J + 1)
+        hg = np.where(cand_g, hg, J + 1)
+        sp = det["s"][:P] - det["c_star"]
+        xs = sp + t.astype(np.float64) * math.log(2.0)
+        for gl, ol, val in ((jg, jo, xs), (hg, ho, sp)):
+            bad = np.nonzero(gl != ol)[0]
+            jm = np.minimum(gl[bad], ol[bad])
+            thr = -(jm / p.r) * math.log(2.0)
+            assert np.all(np.abs(val[bad] - thr) < NEAR), (b, g, h, bad)
+            report["flips"] += len(bad)
+        # oracle re-evaluated with the device's memberships
+        jr = np.where(jg != jo, jg, jo)
+        hr = np.where(hg != ho, hg, ho)
+        sums = level_sums(jr, hr, det["w"][:P], Vd[:P], det["D_R"],
+                          det["N_R"], J + 1)
+        cert = certificate_levels(det["tau"], sums["k"], sums["S1"],
+                                  sums["Gs"], sums["S2"], sums["D_B"],
+                                  sums["N_B"], sums["H_B"], det["D_R"],
+                                  det["N_R"], det["H_R"], det["Vmax"],
+                                  det["delta_e"], p.eps, p.measure)
+        ok = np.nonzero(cert["certified"])[0]
+        ref_lvl = int(ok[0]) if len(ok) else J + 1
+        gl = int(lvl_g[b, hq])
+        if gl != ref_lvl:
+            jm = min(gl, ref_lvl)
+            assert jm <= J
+            tgt = p.eps * cert["scale_lo"][jm]
+            assert abs(cert["beta"][jm] - tgt) <= 2e-3 * tgt, (gl, ref_lvl)
+            report["level_flips"] += 1
+        if gl <= J:
+            o_ref = cert["o_hat"][gl]
+            b_ref = cert["beta"][gl]
+            assert abs(beta_g[b, hq] - b_ref) <= TOL * b_ref
+            kr = 64 + len(np.union1d(det["cset"],
+                                     np.nonzero(det["jbar"] <= gl)[0]))
+            assert kr_g[b, hq] == kr
+            assert stats[b, hq, 2] == 64 + int((jr <= gl).sum())
+        else:
+            o_ref, _ = dense_attention(q[b, hq], K[b, g, :n], V[b, g, :n])
+            assert beta_g[b, hq] == 0 and kr_g[b, hq] == n
+        err = np.linalg.norm(o_g[b, hq] - o_ref)
+        assert err <= TOL * np.linalg.norm(o_ref) + 1e-6, (b, g, h, err)
+        report["heads"] += 1
+        report["levels"].append(gl)
+        # rows the head needs, for the group unions
+        if gl <= J:
+            needK.update(np.union1d(det["cset"],
+                                    np.nonzero(det["jbar"] <= gl)[0]).tolist())
+            needV.update(np.nonzero(jr <= gl)[0].tolist())
+        else:
+            needK.update(range(P))
+            needV.update(range(P))
+    for h in range(w.G):
+        hq = g * w.G + h
+        assert stats[b, hq, 7] == 64 + len(needK)
+        assert stats[b, hq, 8] == 64 + len(needV)
+
+
+def run_and_compare(w, K, V, q, lens, seeds, n_alloc, **pover):
+    run = GpuRun(w, K, V, q, lens, seeds, n_alloc, **pover)
+    p = Params(run.params.eps, run.params.delta, run.params.r,
+               measure=run.params.measure, J_override=run.params.J_override)
+    report = {"flips": 0, "level_flips": 0, "heads": 0, "levels": []}
+    for b in range(w.B):
+        n = run.lens[b]
+        if n <= 64:
+            continue
+        for g in range(w.Hkv):
+            res = oracle_decode_group(q[b, g * w.G:(g + 1) * w.G], K[b, g],
+                                      V[b, g], n, run.seeds[b], g, p)
+            compare_group(run, w, K, V, q, b, g, res, p, report)
+    return run, report

@@ -1,0 +1,185 @@
+"""Certificate coverage and the larger workloads, on the GPU.
+
+* Coverage (picx.dev "Certificate Validity"; Theorem 4): with probability at
+  least 1 - delta per (sequence, query head, step), the returned beta bounds
+  the true error ||o_hat - o||, and the stop rule then gives
+  ||o_hat - o|| <= eps * M (value scale).  Measured against float64 exact
+  attention over many fresh steps at 16K and at the 128K batch-4 shape.
+* Decode with appends at the 32K batch shape, eps = 0.02: each step appends
+  a token and re-quantises its block; sampled groups are compared with the
+  oracle exactly as in the parity tests.
+* The stress regimes (flat, heavy-tailed, adversarial) at 256K against the
+  oracle, and at 1M tokens against exact attention.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+from oracle.step import Params, oracle_decode_group
+from tests.gpu_common import GpuRun, compare_group, ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_built()
+
+
+def _exact(q, K, V, lens, G):
+    """float64 exact attention o and value scale M = sqrt(sum_i a_i ||v_i||^2)
+    per (sequence, query head), from device tensors."""
+    import torch
+    B, Hq, d = q.shape
+    o = torch.empty((B, Hq, d), dtype=torch.float64, device=q.device)
+    M = torch.empty((B, Hq), dtype=torch.float64, device=q.device)
+    for b in range(B):
+        n = int(lens[b])
+        for g in range(Hq // G):
+            Kd = K[b, g, :n].double()
+            Vd = V[b, g, :n].double()
+            qd = q[b, g * G:(g + 1) * G].double()
+            s = qd @ Kd.T / math.sqrt(d)
+            a = torch.softmax(s, dim=1)
+            o[b, g * G:(g + 1) * G] = a @ Vd
+            M[b, g * G:(g + 1) * G] = torch.sqrt(a @ (Vd * Vd).sum(dim=1))
+    return o, M
+
+
+class _Tally:
+    def __init__(self):
+        self.n = 0
+        self.beta_viol = 0
+        self.eps_viol = 0
+        self.fallback = 0
+        self.ratios = []
+
+    def add(self, o_hat, beta, level, o, M, eps, J):
+        import torch
+        err = torch.linalg.norm(o_hat.double() - o, dim=-1)
+        lv = level.long()
+        fb = lv > J
+        self.n += err.numel()
+        self.fallback += int(fb.sum())
+        # exact fallback: beta = 0 and o_hat is float32 exact attention
+        tol = 1e-4 * torch.linalg.norm(o, dim=-1)
+        self.beta_viol += int(((err > beta.double() + 1e-7) & ~fb).sum())
+        self.beta_viol += int(((err > tol) & fb).sum())
+        self.eps_viol += int((err > eps * M).sum())
+        self.ratios.extend((err / (eps * M)).flatten().tolist())
+
+    def check(self, delta):
+        # each head-step fails with probability at most delta: allow delta*N
+        assert self.beta_viol <= delta * self.n, (self.beta_viol, self.n)
+        assert self.eps_viol <= delta * self.n, (self.eps_viol, self.n)
+        r = np.asarray(self.ratios)
+        return {"head_steps": self.n, "beta_violations": self.beta_viol,
+                "eps_violations": self.eps_viol, "fallbacks": self.fallback,
+                "err_over_epsM_p50": float(np.percentile(r, 50)),
+                "err_over_epsM_p90": float(np.percentile(r, 90)),
+                "err_over_epsM_max": float(r.max())}
+
+
+def _coverage(w, steps, layer=0):
+    import torch
+    import certified_sparse_attention_gb300 as csa
+    dev = torch.device("cuda:0")
+    K, V, meta = synth.kv_torch(w, layer=layer, device=dev)
+    shape = csa.make_shape(w.B, w.Hq, w.Hkv, w.d, w.n, w.dtype)
+    mt = csa.meta_buffers(shape, dev)
+    lens = [w.n] * w.B
+    csa.check(csa.csa_quantize_keys(shape, K, V, lens, 0, *mt))
+    step = csa.DecodeStep(shape, csa.make_params(w.eps, w.delta, w.r), dev)
+    J = int(np.ceil(w.r * np.log2(w.n - 64)))
+    tally = _Tally()
+    for s in range(steps):
+        q = synth.q_torch(w, meta, s, layer=layer, device=dev)
+        seeds = [int(x) for x in synth.step_seeds(w, s, layer=layer)]
+        o_hat, beta, level, _ = step(q, K, V, mt, lens, seeds)
+        torch.cuda.synchronize()
+        csa.check(csa.csa_check(step.ws), "csa_check")
+        o, M = _exact(q, K, V, lens, w.G)
+        assert torch.isfinite(o_hat).all() and torch.isfinite(beta).all()
+        assert (beta >= 0).all() and (level >= 0).all() and (level <= J + 1).all()
+        tally.add(o_hat, beta, level, o, M, w.eps, J)
+    return tally.check(w.delta)
+
+
+def test_coverage_llama16k():
+    w = synth.workload("llama16k")
+    summary = _coverage(w, steps=24)
+    print("coverage llama16k", summary)
+
+
+def test_coverage_llama128k_b4():
+    w = synth.workload("llama128k_b4")
+    summary = _coverage(w, steps=3)
+    print("coverage llama128k_b4", summary)
+
+
+def test_decode_with_appends_32k():
+    # the 32K batch shape, eps = 0.02: three steps, each appending a token
+    w = synth.workload("llama32k_b8", B=2, eps=0.02)
+    steps = 3
+    n0 = w.n - steps + 1
+    K, V, meta = synth.kv_numpy(w)              # rows >= n0 are appended later
+    q0 = synth.q_numpy(w, meta, 0)
+    lens = [n0] * w.B
+    run = GpuRun(w, K, V, q0, lens, synth.step_seeds(w, 0), w.n)
+    p = Params(w.eps, w.delta, w.r)
+    report = {"flips": 0, "level_flips": 0, "heads": 0, "levels": []}
+    for s in range(steps):
+        if s > 0:
+            for b in range(w.B):
+                pos = n0 + s - 1
+                run.append(b, pos, K[b, :, pos], V[b, :, pos])
+            q = synth.q_numpy(w, meta, s)
+            run.rerun(q, run.lens, synth.step_seeds(w, s))
+        else:
+            q = q0
+        for (b, g) in ((0, s % w.Hkv), (1, (s + 3) % w.Hkv)):
+            n = run.lens[b]
+            res = oracle_decode_group(q[b, g * w.G:(g + 1) * w.G], K[b, g],
+                                      V[b, g], n, run.seeds[b], g, p)
+            compare_group(run, w, K, V, q, b, g, res, p, report)
+    assert report["heads"] == 2 * steps * w.G
+    assert run.lens == [w.n] * w.B
+    print("appends 32k: levels", report["levels"], "flips", report["flips"])
+
+
+@pytest.mark.parametrize("regime", ["flat", "heavy", "adversarial"])
+def test_stress_256k_against_oracle(regime):
+    # batch 1, GQA 4, d 128, r 2 at 256K tokens; two KV heads keep the
+    # oracle's host time bounded; group 0 compared with the oracle, every
+    # head against exact attention
+    import torch
+    w = synth.stress(262144, 0.05, regime)
+    w = synth.workload("llama16k", n=w.n, eps=w.eps, regime=regime,
+                       Hq=8, Hkv=2)
+    K, V, meta = synth.kv_numpy(w)
+    q = synth.q_numpy(w, meta, 0)
+    run = GpuRun(w, K, V, q, [w.n], synth.step_seeds(w, 0), w.n)
+    p = Params(w.eps, w.delta, w.r)
+    report = {"flips": 0, "level_flips": 0, "heads": 0, "levels": []}
+    res = oracle_decode_group(q[0, 0:w.G], K[0, 0], V[0, 0], w.n,
+                              run.seeds[0], 0, p)
+    compare_group(run, w, K, V, q, 0, 0, res, p, report)
+    J = int(np.ceil(w.r * np.log2(w.n - 64)))
+    o, M = _exact(run.q, run.K, run.V, [w.n], w.G)
+    tally = _Tally()
+    tally.add(run.step.o, run.step.beta, run.step.level, o, M, w.eps, J)
+    print("stress", regime, report["levels"], tally.check(w.delta))
+
+
+def test_stress_1m_flat_and_adversarial():
+    # one million tokens (8 KV heads): exact attention as the reference
+    w0 = synth.stress(1048576, 0.05, "flat")
+    for regime in ("flat", "adversarial"):
+        w = synth.workload("llama16k", n=w0.n, eps=0.05, regime=regime)
+        summary = _coverage(w, steps=1)
+        print("stress 1M", regime, summary)

@@ -215,27 +215,46 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const unsigned (&a
 
 // ------------------------------------------------------- exact-max set
 
+constexpr int kCsetTiles = 16;   // 256-key tiles per CTA of the exact-max set pass
+
 template <int G>
 __global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+  // a CTA covers kCsetTiles tiles of 256 keys; its members are staged in
+  // shared memory and take one slot range of the group's list (a per-warp
+  // reservation on the group's counter serialises)
+  __shared__ uint2 s_list[256 * kCsetTiles];
+  __shared__ unsigned s_n, s_gbase;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
   const int64_t P = n - kWindow;
-  const int64_t key = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  if ((int64_t)blockIdx.x * 256 >= n) return;
+  const int64_t k0 = (int64_t)blockIdx.x * 256 * kCsetTiles;
+  if (k0 >= n) return;
   const int bh0 = b * a.Hq + g * G;
-  unsigned qm = 0;
-  if (key < n) {
-    if (key >= P) qm = (1u << G) - 1u;
-    else {
-      const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
+  float clo[G];
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        if (ub[h] >= cmax_get(a, bh0 + h, 0)) qm |= 1u << h;
+  for (int h = 0; h < G; ++h) clo[h] = cmax_get(a, bh0 + h, 0);
+  if (threadIdx.x == 0) s_n = 0u;
+  __syncthreads();
+  for (int t = 0; t < kCsetTiles; ++t) {
+    const int64_t key = k0 + (int64_t)t * 256 + threadIdx.x;
+    unsigned qm = 0;
+    if (key < n) {
+      if (key >= P) qm = (1u << G) - 1u;
+      else {
+        const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          if (ub[h] >= clo[h]) qm |= 1u << h;
+      }
     }
+    const int slot = warp_append(&s_n, qm != 0);
+    if (slot >= 0) s_list[slot] = make_uint2((unsigned)key, qm);
   }
-  const int slot = warp_append(a.xcnt + bg, qm != 0);
-  if (slot >= 0) a.xlist[(int64_t)bg * a.n_max + slot] = make_uint2((unsigned)key, qm);
+  __syncthreads();
+  if (threadIdx.x == 0) s_gbase = s_n ? atomicAdd(a.xcnt + bg, s_n) : 0u;
+  __syncthreads();
+  for (unsigned i = threadIdx.x; i < s_n; i += 256) a.xlist[(int64_t)bg * a.n_max + s_gbase + i] = s_list[i];
 }
 
 // ------------------------------------------------------ ring row scoring
@@ -1757,7 +1776,8 @@ static dim3 rows_grid(const SparseArgs& a, int64_t items, int nsm) {
 
 cudaError_t launch_cstar(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t nmax_live,
                          int nsm, cudaStream_t st) {
-  dim3 grid((unsigned)((nmax_live + 255) / 256), (unsigned)(a.B * a.Hkv));
+  const int64_t span = 256 * kCsetTiles;
+  dim3 grid((unsigned)((nmax_live + span - 1) / span), (unsigned)(a.B * a.Hkv));
   CSA_G_SWITCH(cset_kernel, <<<grid, 256, 0, st>>>(a, seq))
   CSA_DG_SWITCH(launch_rows0, (rows_grid(a, nmax_live, nsm), st, a, seq))
   return cudaGetLastError();

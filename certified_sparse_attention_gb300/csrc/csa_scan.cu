@@ -77,9 +77,12 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
     const int64_t rows_valid = nblk_n * kBlock - key0;
 #pragma unroll
     for (int c = tid; c < kTile * CHR; c += 256) {
-      int row = c / CHR;
+      const int row = c / CHR, part = c - row * CHR;
       bool ok = row < rows_valid;
-      cp_async16(s_codes + c * 16, ok ? src + (int64_t)c * 16 : a.K4, ok);
+      // chunk `part` of a row at chunk part ^ (row % CHR): the fragment
+      // loads of eight rows then spread over the banks
+      cp_async16(s_codes + row * ROWB + ((part ^ (row & (CHR - 1))) << 4),
+                 ok ? src + (int64_t)c * 16 : a.K4, ok);
     }
     cp_async_commit();
   }
@@ -183,70 +186,83 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
   cp_async_wait<0>();            // the codes too
   __syncthreads();
 
-  // 3. bounds per key
-  const int64_t key = key0 + tid;
-  const bool live = key < n;
-  const int blk = tid >> 6;
-  float lmax[G], umax[G];
-  int ae[G], ao[G];
+  // 3. bounds per key.  The exact integer dot products I = sum_c qcode_c *
+  // code_c come from u8 x s8 m16n8k32 tensor-core products: a warp takes its
+  // 32 keys (one 64-key block) as two 16-key tiles (M), the heads are N
+  // (padded to 8), and k-step s covers code words 4s..4s+3: thread t's four
+  // k positions 4t..4t+3 are the even channels of word 4s+t (low nibbles)
+  // and 16+4t..16+4t+3 its odd channels (high nibbles), matching the even
+  // and odd query-code words.  Integer sums are exact in any order.
+  const int w = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int blk = w >> 1;
+  constexpr int KS = D / 32;
+  unsigned bq[KS][2];
 #pragma unroll
-  for (int h = 0; h < G; ++h) { ae[h] = 0; ao[h] = 0; }
-  if (live) {
-    const uint4* row = reinterpret_cast<const uint4*>(s_codes + tid * ROWB);
-    const int rot = (CHR == 4) ? (tid >> 1) : (tid >> 2);
+  for (int ks = 0; ks < KS; ++ks) {
+    bq[ks][0] = gq < G ? s_atw[blk][gq < G ? gq : 0][4 * ks + tq] : 0u;
+    bq[ks][1] = gq < G ? s_atw[blk][gq < G ? gq : 0][WE + 4 * ks + tq] : 0u;
+  }
+  float lmax[2] = {-INFINITY, -INFINITY}, umax[2] = {-INFINITY, -INFINITY};   // heads 2tq, 2tq+1
 #pragma unroll
-    for (int j = 0; j < CHR; ++j) {
-      const int jj = (j + rot) & (CHR - 1);
-      uint4 w = row[jj];
-      unsigned ws[4] = {w.x, w.y, w.z, w.w};
+  for (int mt = 0; mt < 2; ++mt) {
+    const int r0 = 32 * w + 16 * mt + gq, r1 = r0 + 8;
+    int acc[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        uint4 e4 = *reinterpret_cast<const uint4*>(&s_atw[blk][h][4 * jj]);
-        uint4 o4 = *reinterpret_cast<const uint4*>(&s_atw[blk][h][WE + 4 * jj]);
-        unsigned es[4] = {e4.x, e4.y, e4.z, e4.w};
-        unsigned os[4] = {o4.x, o4.y, o4.z, o4.w};
+    for (int ks = 0; ks < KS; ++ks) {
+      // word 4ks+tq of rows r0, r1: chunk ks, word tq (swizzled chunks)
+      const unsigned w0 = *reinterpret_cast<const unsigned*>(s_codes + r0 * ROWB + ((ks ^ (r0 & (CHR - 1))) << 4) + 4 * tq);
+      const unsigned w1 = *reinterpret_cast<const unsigned*>(s_codes + r1 * ROWB + ((ks ^ (r1 & (CHR - 1))) << 4) + 4 * tq);
+      const unsigned af0 = w0 & 0x0F0F0F0Fu, af1 = w1 & 0x0F0F0F0Fu;
+      const unsigned af2 = (w0 >> 4) & 0x0F0F0F0Fu, af3 = (w1 >> 4) & 0x0F0F0F0Fu;
+      asm volatile(
+          "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+          "{%0,%1,%2,%3};\n"
+          : "+r"(acc[0]), "+r"(acc[1]), "+r"(acc[2]), "+r"(acc[3])
+          : "r"(af0), "r"(af1), "r"(af2), "r"(af3), "r"(bq[ks][0]), "r"(bq[ks][1]));
+    }
+    // acc[0], acc[1]: key r0, heads 2tq, 2tq+1; acc[2], acc[3]: key r1
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          ae[h] = dp4a_us(ws[e] & 0x0F0F0F0Fu, es[e], ae[h]);
-          ao[h] = dp4a_us(ws[e] & 0xF0F0F0F0u, os[e], ao[h]);
+    for (int half = 0; half < 2; ++half) {
+      const int r = half ? r1 : r0;
+      const int64_t key = key0 + r;
+      const bool live = key < n;
+      float ubv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int h = 2 * tq + u;
+        ubv[u] = 0.f;
+        if (h < G) {
+          const float aI = fmul(s_alpha[blk][h], (float)acc[2 * half + u]);
+          const float ub = fadd(aI, s_bhi[blk][h]);
+          const float lo = fadd(aI, s_blo[blk][h]);
+          ubv[u] = ub;
+          if (live) { umax[u] = fmaxf(umax[u], ub); lmax[u] = fmaxf(lmax[u], lo); }
         }
+      }
+      if (live && 2 * tq < G) {
+        float* dst = a.ubar + ((int64_t)bg * a.n_max + key) * G + 2 * tq;
+        if (G >= 2) *reinterpret_cast<float2*>(dst) = make_float2(ubv[0], ubv[1]);
+        else dst[0] = ubv[0];
       }
     }
   }
-  float ub[G];
+  // 4. per-head maxima: over the eight key rows of the thread's column
+  // group, then over the warps
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    int I = ae[h] + (ao[h] >> 4);
-    float aI = fmul(s_alpha[blk][h], (float)I);
-    ub[h] = fadd(aI, s_bhi[blk][h]);
-    float lo = fadd(aI, s_blo[blk][h]);
-    umax[h] = live ? ub[h] : -INFINITY;
-    lmax[h] = live ? lo : -INFINITY;
-  }
-  if (live) {
-    float* dst = a.ubar + ((int64_t)bg * a.n_max + key) * G;
-    if (G == 4) {
-      *reinterpret_cast<float4*>(dst) = make_float4(ub[0], ub[1], ub[2], ub[3]);
-    } else if (G == 8) {
-      reinterpret_cast<float4*>(dst)[0] = make_float4(ub[0], ub[1], ub[2], ub[3]);
-      reinterpret_cast<float4*>(dst)[1] = make_float4(ub[4 % G], ub[5 % G], ub[6 % G], ub[7 % G]);
-    } else if (G == 2) {
-      *reinterpret_cast<float2*>(dst) = make_float2(ub[0], ub[1 % G]);
-    } else {
-      dst[0] = ub[0];
+  for (int u = 0; u < 2; ++u) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      lmax[u] = fmaxf(lmax[u], __shfl_xor_sync(0xffffffffu, lmax[u], o));
+      umax[u] = fmaxf(umax[u], __shfl_xor_sync(0xffffffffu, umax[u], o));
     }
   }
-  // 4. per-head maxima
-  const int w = tid >> 5, lane = tid & 31;
+  if (gq == 0) {
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float x = lmax[h], y = umax[h];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-      y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, o));
+    for (int u = 0; u < 2; ++u) {
+      const int h = 2 * tq + u;
+      if (h < G) { s_red[w][h][0] = lmax[u]; s_red[w][h][1] = umax[u]; }
     }
-    if (lane == 0) { s_red[w][h][0] = x; s_red[w][h][1] = y; }
   }
   __syncthreads();
   if (tid < G) {

@@ -108,6 +108,23 @@ cudaError_t launch_dense(const DenseArgs&, const SeqArgs&, int d, int G, bool bf
 cudaError_t launch_quant(const QuantArgs&, const SeqArgs&, int B, int d, bool bf16, int64_t nblocks,
                          cudaStream_t);
 int dense_nsplit(int64_t n_max);
+
+// Launch with programmatic stream serialisation (see pdl_entry).
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kern, args...);
+}
 void add_launches(int k);   // adds to the launch count csa_profile_read reports
 
 }  // namespace csa

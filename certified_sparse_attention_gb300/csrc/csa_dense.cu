@@ -37,6 +37,7 @@ __device__ __forceinline__ bool group_wanted(const DenseArgs& a, int b, int g, i
 template <int D, int G, typename E>
 __global__ void __launch_bounds__(256) dense_split_kernel(const DenseArgs a, const __grid_constant__ SeqArgs seq,
                                                           int nsplit_live) {
+  pdl_entry();
   constexpr int CPL = D / 32;
   __shared__ float s_m[8][G], s_l[8][G];
   __shared__ float s_acc[8][G][D];
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(256) dense_split_kernel(const DenseArgs a, con
 
 template <int D>
 __global__ void __launch_bounds__(128) dense_combine_kernel(const DenseArgs a, const __grid_constant__ SeqArgs seq) {
+  pdl_entry();
   const int bh = blockIdx.x;
   const int b = bh / a.Hq;
   if (a.nfall && *a.nfall == 0u) return;
@@ -164,22 +166,22 @@ __global__ void __launch_bounds__(128) dense_combine_kernel(const DenseArgs a, c
 
 #define CSA_DENSE_SWITCH(FN, ...)                                                                \
   switch (d * 100 + G * 10 + (bf16 ? 1 : 0)) {                                                   \
-    case 12811: FN<128, 1, __nv_bfloat16> __VA_ARGS__; break;                                    \
-    case 12821: FN<128, 2, __nv_bfloat16> __VA_ARGS__; break;                                    \
-    case 12841: FN<128, 4, __nv_bfloat16> __VA_ARGS__; break;                                    \
-    case 12881: FN<128, 8, __nv_bfloat16> __VA_ARGS__; break;                                    \
-    case 12810: FN<128, 1, float> __VA_ARGS__; break;                                            \
-    case 12820: FN<128, 2, float> __VA_ARGS__; break;                                            \
-    case 12840: FN<128, 4, float> __VA_ARGS__; break;                                            \
-    case 12880: FN<128, 8, float> __VA_ARGS__; break;                                            \
-    case 6411: FN<64, 1, __nv_bfloat16> __VA_ARGS__; break;                                      \
-    case 6421: FN<64, 2, __nv_bfloat16> __VA_ARGS__; break;                                      \
-    case 6441: FN<64, 4, __nv_bfloat16> __VA_ARGS__; break;                                      \
-    case 6481: FN<64, 8, __nv_bfloat16> __VA_ARGS__; break;                                      \
-    case 6410: FN<64, 1, float> __VA_ARGS__; break;                                              \
-    case 6420: FN<64, 2, float> __VA_ARGS__; break;                                              \
-    case 6440: FN<64, 4, float> __VA_ARGS__; break;                                              \
-    case 6480: FN<64, 8, float> __VA_ARGS__; break;                                              \
+    case 12811: launch_pdl(FN<128, 1, __nv_bfloat16>, __VA_ARGS__); break;                                    \
+    case 12821: launch_pdl(FN<128, 2, __nv_bfloat16>, __VA_ARGS__); break;                                    \
+    case 12841: launch_pdl(FN<128, 4, __nv_bfloat16>, __VA_ARGS__); break;                                    \
+    case 12881: launch_pdl(FN<128, 8, __nv_bfloat16>, __VA_ARGS__); break;                                    \
+    case 12810: launch_pdl(FN<128, 1, float>, __VA_ARGS__); break;                                            \
+    case 12820: launch_pdl(FN<128, 2, float>, __VA_ARGS__); break;                                            \
+    case 12840: launch_pdl(FN<128, 4, float>, __VA_ARGS__); break;                                            \
+    case 12880: launch_pdl(FN<128, 8, float>, __VA_ARGS__); break;                                            \
+    case 6411: launch_pdl(FN<64, 1, __nv_bfloat16>, __VA_ARGS__); break;                                      \
+    case 6421: launch_pdl(FN<64, 2, __nv_bfloat16>, __VA_ARGS__); break;                                      \
+    case 6441: launch_pdl(FN<64, 4, __nv_bfloat16>, __VA_ARGS__); break;                                      \
+    case 6481: launch_pdl(FN<64, 8, __nv_bfloat16>, __VA_ARGS__); break;                                      \
+    case 6410: launch_pdl(FN<64, 1, float>, __VA_ARGS__); break;                                              \
+    case 6420: launch_pdl(FN<64, 2, float>, __VA_ARGS__); break;                                              \
+    case 6440: launch_pdl(FN<64, 4, float>, __VA_ARGS__); break;                                              \
+    case 6480: launch_pdl(FN<64, 8, float>, __VA_ARGS__); break;                                              \
     default: return cudaErrorInvalidValue;                                                       \
   }
 
@@ -192,9 +194,9 @@ cudaError_t launch_dense(const DenseArgs& a, const SeqArgs& seq, int d, int G, b
   // comparator: one CTA per item; fallback (masked): a small persistent grid
   const int cap = a.state ? 1024 : items;
   dim3 grid((unsigned)(items < cap ? items : cap));
-  CSA_DENSE_SWITCH(dense_split_kernel, <<<grid, 256, 0, st>>>(a, seq, nsplit_live))
-  if (d == 128) dense_combine_kernel<128><<<a.B * a.Hq, 128, 0, st>>>(a, seq);
-  else dense_combine_kernel<64><<<a.B * a.Hq, 128, 0, st>>>(a, seq);
+  CSA_DENSE_SWITCH(dense_split_kernel, grid, dim3(256), 0, st, a, seq, nsplit_live)
+  if (d == 128) launch_pdl(dense_combine_kernel<128>, dim3(a.B * a.Hq), dim3(128), 0, st, a, seq);
+  else launch_pdl(dense_combine_kernel<64>, dim3(a.B * a.Hq), dim3(128), 0, st, a, seq);
   return cudaGetLastError();
 }
 

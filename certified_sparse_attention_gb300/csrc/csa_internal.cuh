@@ -164,6 +164,18 @@ __device__ __forceinline__ void exact_levels(float s, float c, float t, float ne
   hl = level_of(fmul(neg_r, y), J);
 }
 
+// ------------------------------------------ programmatic dependent launch
+//
+// Every kernel of the library is launched with programmatic stream
+// serialisation (launch_pdl): the next kernel on the stream may be
+// scheduled while this one's last CTAs run.  Each kernel therefore starts
+// by waiting for its predecessor grid (its results are then visible), and
+// then lets its own dependent launch.
+__device__ __forceinline__ void pdl_entry() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ------------------------------------------------------- async staging
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {

@@ -16,6 +16,7 @@ namespace csa {
 
 template <int D, typename E>
 __global__ void __launch_bounds__(D) quant_kernel(const QuantArgs a, const __grid_constant__ SeqArgs seq) {
+  pdl_entry();
   __shared__ float s_vm[kBlock];
   const int c = threadIdx.x;
   const int bg = blockIdx.y, b = bg / a.Hkv;
@@ -75,11 +76,11 @@ cudaError_t launch_quant(const QuantArgs& a, const SeqArgs& seq, int B, int d, b
   if (nblocks <= 0) return cudaSuccess;
   dim3 grid((unsigned)nblocks, (unsigned)(B * a.Hkv));
   if (d == 128) {
-    if (bf16) quant_kernel<128, __nv_bfloat16><<<grid, 128, 0, st>>>(a, seq);
-    else quant_kernel<128, float><<<grid, 128, 0, st>>>(a, seq);
+    if (bf16) launch_pdl(quant_kernel<128, __nv_bfloat16>, grid, dim3(128), 0, st, a, seq);
+    else launch_pdl(quant_kernel<128, float>, grid, dim3(128), 0, st, a, seq);
   } else {
-    if (bf16) quant_kernel<64, __nv_bfloat16><<<grid, 64, 0, st>>>(a, seq);
-    else quant_kernel<64, float><<<grid, 64, 0, st>>>(a, seq);
+    if (bf16) launch_pdl(quant_kernel<64, __nv_bfloat16>, grid, dim3(64), 0, st, a, seq);
+    else launch_pdl(quant_kernel<64, float>, grid, dim3(64), 0, st, a, seq);
   }
   return cudaGetLastError();
 }

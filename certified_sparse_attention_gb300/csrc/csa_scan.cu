@@ -41,6 +41,7 @@ __device__ __forceinline__ float tree16(const float* v) {
 
 template <int D, int G, typename E>
 __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq) {
+  pdl_entry();
   constexpr int CPT = D / 16;        // channels per prep thread
   constexpr int ROWB = D / 2;        // bytes of codes per key
   constexpr int CHR = ROWB / 16;     // 16-byte chunks per key
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
 template <int D, int G, typename E>
 cudaError_t launch_scan_t(const ScanArgs& a, const SeqArgs& seq, int B, int64_t nmax_live, cudaStream_t st) {
   dim3 grid((unsigned)((nmax_live + kTile - 1) / kTile), (unsigned)(B * a.Hkv));
-  scan_kernel<D, G, E><<<grid, 256, 0, st>>>(a, seq);
+  launch_pdl(scan_kernel<D, G, E>, grid, dim3(256), 0, st, a, seq);
   return cudaGetLastError();
 }
 

@@ -219,6 +219,7 @@ constexpr int kCsetTiles = 16;   // 256-key tiles per CTA of the exact-max set p
 
 template <int G>
 __global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+  pdl_entry();
   // a CTA covers kCsetTiles tiles of 256 keys; its members are staged in
   // shared memory and take one slot range of the group's list (a per-warp
   // reservation on the group's counter serialises)
@@ -272,6 +273,7 @@ constexpr int rows_smem() {
 
 template <int D, int G, typename E, int MODE>
 __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+  pdl_entry();
   constexpr int CPL = D / 32;
   constexpr int RB = D * (int)sizeof(E);
   extern __shared__ __align__(16) uint8_t dsm[];
@@ -453,6 +455,7 @@ constexpr int kTilesPerCta = 16;   // key tiles per CTA of the per-key passes
 
 template <int G>
 __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+  pdl_entry();
   __shared__ unsigned s_jr[G][kMaxJ + 2];
   __shared__ unsigned s_nc[G];
   // the CTA's candidates, staged here and written out with one global slot
@@ -539,6 +542,7 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
 
 template <int G>
 __global__ void __launch_bounds__(256) prehist_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+  pdl_entry();
   // counts as integers; heavy weights in 2^-18 fixed point (a prediction
   // input only; at most 2^12 keys of weight <= 1 per CTA), all aggregated
   // over equal levels within a warp
@@ -607,6 +611,7 @@ __global__ void __launch_bounds__(256) prehist_kernel(const SparseArgs a, const 
 
 template <int D, int G, typename E>
 __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+  pdl_entry();
   constexpr int CPL = D / 32;
   __shared__ float s_nr[G][D];
   __shared__ float s_dr[G], s_hr[G];
@@ -868,6 +873,7 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
 template <int G>
 __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
                                                      int round, unsigned tpg) {
+  pdl_entry();
   __shared__ unsigned s_item;
   const int BG = a.B * a.Hkv;
   const unsigned total = a.rq[6 * BG + round] * tpg;
@@ -888,6 +894,7 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
 // entries and chunk_map maps each item to its bucket.
 template <bool EV>
 __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nent) {
+  pdl_entry();
   __shared__ unsigned s_part[1024];
   const int tid = threadIdx.x;
   const int per = (nent + 1023) / 1024;
@@ -938,6 +945,7 @@ constexpr int vgather_smem() {
 template <int D, int G, typename E>
 __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
                                                       int nent) {
+  pdl_entry();
   constexpr int CPL = D / 32;
   constexpr int ACC = 2 * D + 8;
   constexpr int RB = D * (int)sizeof(E);
@@ -1196,6 +1204,7 @@ __device__ __forceinline__ void vs_seek(const SparseArgs& a, int nent, int e0, u
 
 template <int D, int G>
 __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int nent) {
+  pdl_entry();
   using Lt = VsLayout<D, G>;
   constexpr int RB = Lt::RB, MT = Lt::MT, NT = D / 8, CH = RB / 16;
   constexpr int ACC = 2 * D + 8;
@@ -1445,6 +1454,7 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
 template <int D>
 __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
                                                       int round) {
+  pdl_entry();
   constexpr int ACC = 2 * D + 8;
   constexpr int CPL = D / 32;
   constexpr int LB = 32;                   // levels per shared-memory batch
@@ -1641,6 +1651,7 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
 
 template <int G>
 __global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+  pdl_entry();
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow || !a.stats) return;
@@ -1710,12 +1721,33 @@ __global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __g
     default: return cudaErrorInvalidValue;                                                       \
   }
 
+#define CSA_DG_LAUNCH(FN, ...)                                                                   \
+  switch (d * 100 + G * 10 + (bf16 ? 1 : 0)) {                                                   \
+    case 12811: launch_pdl(FN<128, 1, __nv_bfloat16>, __VA_ARGS__); break;                                    \
+    case 12821: launch_pdl(FN<128, 2, __nv_bfloat16>, __VA_ARGS__); break;                                    \
+    case 12841: launch_pdl(FN<128, 4, __nv_bfloat16>, __VA_ARGS__); break;                                    \
+    case 12881: launch_pdl(FN<128, 8, __nv_bfloat16>, __VA_ARGS__); break;                                    \
+    case 12810: launch_pdl(FN<128, 1, float>, __VA_ARGS__); break;                                            \
+    case 12820: launch_pdl(FN<128, 2, float>, __VA_ARGS__); break;                                            \
+    case 12840: launch_pdl(FN<128, 4, float>, __VA_ARGS__); break;                                            \
+    case 12880: launch_pdl(FN<128, 8, float>, __VA_ARGS__); break;                                            \
+    case 6411: launch_pdl(FN<64, 1, __nv_bfloat16>, __VA_ARGS__); break;                                      \
+    case 6421: launch_pdl(FN<64, 2, __nv_bfloat16>, __VA_ARGS__); break;                                      \
+    case 6441: launch_pdl(FN<64, 4, __nv_bfloat16>, __VA_ARGS__); break;                                      \
+    case 6481: launch_pdl(FN<64, 8, __nv_bfloat16>, __VA_ARGS__); break;                                      \
+    case 6410: launch_pdl(FN<64, 1, float>, __VA_ARGS__); break;                                              \
+    case 6420: launch_pdl(FN<64, 2, float>, __VA_ARGS__); break;                                              \
+    case 6440: launch_pdl(FN<64, 4, float>, __VA_ARGS__); break;                                              \
+    case 6480: launch_pdl(FN<64, 8, float>, __VA_ARGS__); break;                                              \
+    default: return cudaErrorInvalidValue;                                                       \
+  }
+
 #define CSA_G_SWITCH(FN, ...)                                                                    \
   switch (G) {                                                                                   \
-    case 1: FN<1> __VA_ARGS__; break;                                                            \
-    case 2: FN<2> __VA_ARGS__; break;                                                            \
-    case 4: FN<4> __VA_ARGS__; break;                                                            \
-    case 8: FN<8> __VA_ARGS__; break;                                                            \
+    case 1: launch_pdl(FN<1>, __VA_ARGS__); break;                                               \
+    case 2: launch_pdl(FN<2>, __VA_ARGS__); break;                                               \
+    case 4: launch_pdl(FN<4>, __VA_ARGS__); break;                                               \
+    case 8: launch_pdl(FN<8>, __VA_ARGS__); break;                                               \
     default: return cudaErrorInvalidValue;                                                       \
   }
 
@@ -1727,7 +1759,7 @@ void launch_rows_t(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArg
     cudaFuncSetAttribute(rows_kernel<D, G, E, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     set = true;
   }
-  rows_kernel<D, G, E, MODE><<<grid, 256, smem, st>>>(a, seq);
+  launch_pdl(rows_kernel<D, G, E, MODE>, grid, dim3(256), smem, st, a, seq);
 }
 template <int D, int G, typename E>
 void launch_rows0(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
@@ -1750,9 +1782,9 @@ void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqAr
           per_sm < 1)
         per_sm = 1;
     }
-    vplan_kernel<true><<<1, 1024, 0, st>>>(a, nent);
+    launch_pdl(vplan_kernel<true>, dim3(1), dim3(1024), 0, st, a, nent);
     if (mark) mark(7, st);
-    vsum_kernel<D, G><<<dim3((unsigned)(nsm * per_sm)), kVsW * 32, smem, st>>>(a, nent);
+    launch_pdl(vsum_kernel<D, G>, dim3((unsigned)(nsm * per_sm)), dim3(kVsW * 32), smem, st, a, nent);
   } else {
     constexpr int smem = vgather_smem<D, G, E>();
     static bool set = false;
@@ -1760,9 +1792,9 @@ void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqAr
       cudaFuncSetAttribute(vgather_kernel<D, G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       set = true;
     }
-    vplan_kernel<false><<<1, 1024, 0, st>>>(a, nent);
+    launch_pdl(vplan_kernel<false>, dim3(1), dim3(1024), 0, st, a, nent);
     if (mark) mark(7, st);
-    vgather_kernel<D, G, E><<<dim3((unsigned)(nsm * 2)), 256, smem, st>>>(a, seq, nent);
+    launch_pdl(vgather_kernel<D, G, E>, dim3((unsigned)(nsm * 2)), dim3(256), smem, st, a, seq, nent);
   }
 }
 
@@ -1778,7 +1810,7 @@ cudaError_t launch_cstar(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
                          int nsm, cudaStream_t st) {
   const int64_t span = 256 * kCsetTiles;
   dim3 grid((unsigned)((nmax_live + span - 1) / span), (unsigned)(a.B * a.Hkv));
-  CSA_G_SWITCH(cset_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  CSA_G_SWITCH(cset_kernel, grid, dim3(256), 0, st, a, seq)
   CSA_DG_SWITCH(launch_rows0, (rows_grid(a, nmax_live, nsm), st, a, seq))
   return cudaGetLastError();
 }
@@ -1786,16 +1818,16 @@ cudaError_t launch_rescore(const SparseArgs& a, const SeqArgs& seq, int d, int G
                            int64_t pmax_live, int nsm, cudaStream_t st, void (*mark)(int, cudaStream_t)) {
   const int64_t span = (int64_t)kTile * kTilesPerCta;
   dim3 grid((unsigned)((pmax_live + span - 1) / span), (unsigned)(a.B * a.Hkv));
-  CSA_G_SWITCH(cand_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  CSA_G_SWITCH(cand_kernel, grid, dim3(256), 0, st, a, seq)
   if (mark) mark(3, st);
   CSA_DG_SWITCH(launch_rows1, (rows_grid(a, pmax_live, nsm), st, a, seq))
   if (mark) mark(4, st);
-  CSA_G_SWITCH(prehist_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  CSA_G_SWITCH(prehist_kernel, grid, dim3(256), 0, st, a, seq)
   return cudaGetLastError();
 }
 cudaError_t launch_predict(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, cudaStream_t st) {
   dim3 grid((unsigned)(a.B * a.Hkv));
-  CSA_DG_SWITCH(predict_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  CSA_DG_LAUNCH(predict_kernel, grid, dim3(256), 0, st, a, seq)
   return cudaGetLastError();
 }
 cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t pmax_live,
@@ -1808,20 +1840,20 @@ cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
   if (nct > items) nct = items;
   if (nct < 1) nct = 1;
   dim3 grid((unsigned)nct);
-  CSA_G_SWITCH(levels_kernel, <<<grid, 256, 0, st>>>(a, seq, round, tpg))
+  CSA_G_SWITCH(levels_kernel, grid, dim3(256), 0, st, a, seq, round, tpg)
   if (mark) mark(6, st);
   const int nent = a.B * a.Hkv * a.J1;
   CSA_DG_SWITCH(launch_vgather_t, (nsm, st, a, seq, nent, mark))
   if (mark) mark(8, st);
   dim3 cg((unsigned)(a.B * a.Hq));
-  if (d == 128) certify_kernel<128><<<cg, 256, 0, st>>>(a, seq, round);
-  else certify_kernel<64><<<cg, 256, 0, st>>>(a, seq, round);
+  if (d == 128) launch_pdl(certify_kernel<128>, cg, dim3(256), 0, st, a, seq, round);
+  else launch_pdl(certify_kernel<64>, cg, dim3(256), 0, st, a, seq, round);
   if (mark) mark(9, st);
   return cudaGetLastError();
 }
 cudaError_t launch_near(const SparseArgs& a, const SeqArgs& seq, int G, int64_t pmax_live, cudaStream_t st) {
   dim3 grid((unsigned)((pmax_live + 255) / 256), (unsigned)(a.B * a.Hkv));
-  CSA_G_SWITCH(near_kernel, <<<grid, 256, 0, st>>>(a, seq))
+  CSA_G_SWITCH(near_kernel, grid, dim3(256), 0, st, a, seq)
   return cudaGetLastError();
 }
 

@@ -188,7 +188,7 @@ csa_status csa_workspace_layout(const csa_shape* shape, const csa_params* params
   out->cmax = L.cmax;
   out->s32 = L.s32;
   out->jr_hist = L.jr_hist;
-  out->bcnt = L.bcnt;
+  out->bcnt = L.bcons;   // cumulative over the step's rounds
   out->total = L.total;
   out->J1 = L.J1;
   out->reserved = 0;

@@ -45,8 +45,8 @@ struct SparseArgs {
   unsigned* nfall;        // heads that need the exact fallback
   unsigned* rq;           // round queues: [3][B*Hkv] groups per round, [3][B*Hkv] flags,
                           // [3] group counts, [3] work-item counters
-  unsigned* bcnt;         // [B*Hkv][J1]
-  unsigned* bcons;        // [B*Hkv][J1]
+  unsigned* bcnt;         // [B*Hkv][J1]           entries of the current round
+  unsigned* bcons;        // [B*Hkv][J1]           entries over the step (diagnostics)
   uint2* buckets;         // [B*Hkv][J1][pcap]    key, event masks (add | trans<<8 | before<<16)
   unsigned* plan_start;   // [B*Hkv*J1]
   unsigned* plan_end;     // [B*Hkv*J1]

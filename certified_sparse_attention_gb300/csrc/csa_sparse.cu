@@ -700,12 +700,11 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
     const float de = a.delta / (4.0f * (float)(J + 1));
     const float L = logf(1.0f / de), Lz = logf(2.0f / de);
     const float Rc = Vp + cn;
-    // pred: first level the value-free certificate passes; spred: first
-    // level it passes with the error target halved.  Round 1 gathers up to
-    // spred, at most (r + 1) / 2 levels beyond pred.
-    const int margin = (a.r + 1) / 2;
+    // pred: first level the value-free certificate passes; round 1 gathers
+    // up to it (a margin beyond it cost more in gathered values than the
+    // second rounds it saved)
     float runk = 0.f, rundb = 0.f;
-    int pred = -1, spred = -1;
+    int pred = -1;
     for (int l0 = 0; l0 <= J; l0 += 32) {
       const int j = l0 + lane;
       float dk = 0.f, ddb = 0.f;
@@ -723,7 +722,7 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
       k += runk; db += rundb;
       runk = __shfl_sync(0xffffffffu, k, 31);
       rundb = __shfl_sync(0xffffffffu, db, 31);
-      bool pass = false, spass = false;
+      bool pass = false;
       if (j <= J) {
         const float tau = exp2f(-(float)j / (float)a.r);
         float below, above;
@@ -732,7 +731,6 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
         const float Dh = DR + db + tau * k;
         if (a.measure == CSA_MEASURE_DENOM) {
           pass = Dh > dD && dD <= a.eps * (Dh - dD);
-          spass = Dh > dD && dD <= 0.5f * a.eps * (Dh - dD);
         } else {
           const float Gh = tau * k * fmaxf(nu - cn2, 0.f);
           const float aa = sqrtf(2.f * tau * Rc * Rc * L);
@@ -749,25 +747,16 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
             const float Mlo = sqrtf((HR + db * nu + t2 * t2) / (DR + db + tau * (k + above)));
             scale = Mlo;
             pass = Dh > dD && beta <= a.eps * scale;
-            spass = Dh > dD && beta <= 0.5f * a.eps * scale;
           } else {
             pass = Dh > dD && beta * (1.f + a.eps) <= a.eps * cn;
-            spass = Dh > dD && beta * (1.f + 0.5f * a.eps) <= 0.5f * a.eps * cn;
           }
         }
       }
       const unsigned bal = __ballot_sync(0xffffffffu, pass);
-      const unsigned sbal = __ballot_sync(0xffffffffu, spass);
-      if (pred < 0 && bal) pred = l0 + __ffs(bal) - 1;
-      if (spred < 0 && sbal) spred = l0 + __ffs(sbal) - 1;
-      if (spred >= 0 || (pred >= 0 && l0 + 31 >= pred + margin)) break;
+      if (bal) { pred = l0 + __ffs(bal) - 1; break; }
     }
     if (lane == 0) {
-      if (pred < 0) pred = J;
-      int hi = pred + margin;
-      if (spred >= 0 && spred < hi) hi = spred;
-      if (hi < pred) hi = pred;
-      if (hi > J) hi = J;
+      const int hi = pred < 0 ? J : pred;
       int* st = a.state + (int64_t)bh * 4;
       st[0] = -1; st[1] = hi; st[2] = -1; st[3] = 0;
     }
@@ -887,9 +876,9 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
   }
 }
 
-// One CTA: the bucket entries appended since the last plan, as per-bucket
-// ranges [plan_start, plan_end) and their exclusive prefix plan_off over
-// the buckets.  EV: the prefix counts entries (the tensor-core gather cuts
+// One CTA: the bucket entries appended in this round, as per-bucket ranges
+// [plan_start, plan_end) and their exclusive prefix plan_off over the
+// buckets.  EV: the prefix counts entries (the tensor-core gather cuts
 // it into per-warp ranges); otherwise it counts work items of kChunk
 // entries and chunk_map maps each item to its bucket.
 template <bool EV>
@@ -901,11 +890,16 @@ __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nen
   const int i0 = tid * per, i1 = min(nent, i0 + per);
   unsigned sum = 0;
   for (int i = i0; i < i1; ++i) {
-    unsigned st = a.bcons[i], en = a.bcnt[i];
+    // this round's entries; the counters restart at 0 for the next round
+    // (a bucket holds at most one entry per key in a round), the step's
+    // cumulative count is kept in bcons (diagnostics)
+    const unsigned st = 0;
+    unsigned en = a.bcnt[i];
     if (en > (unsigned)a.pcap) en = (unsigned)a.pcap;
     a.plan_start[i] = st;
     a.plan_end[i] = en;
-    a.bcons[i] = en;
+    a.bcons[i] += en;
+    a.bcnt[i] = 0u;
     sum += EV ? en - st : (en - st + kChunk - 1) / kChunk;
   }
   s_part[tid] = sum;

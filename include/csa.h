@@ -199,8 +199,9 @@ csa_status csa_dense_decode_static(const csa_shape* shape, const void* q,
  *   jr_hist  uint32 [B][Hq][J+2]        first level at which the key's bf16
  *            row is needed (exact-max set: level 0), J+1 = never
  *   bcnt     uint32 [B][Hkv][J1]        entries appended to each level bucket
- *            (one per key and level at which the key changes a head's sums;
- *            each entry is one value-row load of the gather)
+ *            over the step's gather rounds (one per key, level and round at
+ *            which the key changes a head's sums; each entry is one
+ *            value-row load of the gather)
  *   J1       largest J + 1 (row stride of jr_hist is J1 + 1) */
 typedef struct {
   size_t ubar, cmax, s32, jr_hist, bcnt, total;

@@ -616,6 +616,7 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
   __shared__ float s_nr[G][D];
   __shared__ float s_dr[G], s_hr[G];
   __shared__ float s_vm[8];
+  __shared__ float s_wp[8][G][D + 2];     // per-warp window partials
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int bg = blockIdx.x, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
@@ -665,9 +666,9 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
 #pragma unroll
   for (int h = 0; h < G; ++h) {
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) atomicAdd(&s_nr[h][lane * CPL + c], nr[h][c]);
-    float hs = warp_sum(hr[h]);
-    if (lane == 0) { atomicAdd(&s_dr[h], dr[h]); atomicAdd(&s_hr[h], hs); }
+    for (int c = 0; c < CPL; ++c) s_wp[w][h][lane * CPL + c] = nr[h][c];
+    const float hs = warp_sum(hr[h]);       // lanes hold channel partials
+    if (lane == 0) { s_wp[w][h][D] = dr[h]; s_wp[w][h][D + 1] = hs; }   // dr: same in every lane
   }
   // largest value-norm bound over the pool blocks
   {
@@ -677,6 +678,17 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
     for (int64_t i = tid; i < nbp; i += 256) m = fmaxf(m, a.vmax[(int64_t)bg * a.nblk_max + i]);
     m = warp_max(m);
     if (lane == 0) s_vm[w] = m;
+  }
+  __syncthreads();
+  // window sums: the eight warps' partials in a fixed order
+  for (int i = tid; i < G * (D + 2); i += 256) {
+    const int h = i / (D + 2), c = i - h * (D + 2);
+    float v = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) v += s_wp[ww][h][c];
+    if (c < D) s_nr[h][c] = v;
+    else if (c == D) s_dr[h] = v;
+    else s_hr[h] = v;
   }
   __syncthreads();
   float Vp = 0.f;
@@ -902,15 +914,29 @@ __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nen
     a.bcnt[i] = 0u;
     sum += EV ? en - st : (en - st + kChunk - 1) / kChunk;
   }
-  s_part[tid] = sum;
-  __syncthreads();
-  for (int o = 1; o < 1024; o <<= 1) {
-    unsigned x = tid >= o ? s_part[tid - o] : 0u;
-    __syncthreads();
-    s_part[tid] += x;
-    __syncthreads();
+  // exclusive prefix of the per-thread sums: a shuffle scan within each
+  // warp, then one over the 32 warp totals
+  const int lane = tid & 31, wp = tid >> 5;
+  unsigned inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned x = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += x;
   }
-  unsigned run = s_part[tid] - sum;
+  if (lane == 31) s_part[wp] = inc;
+  __syncthreads();
+  if (wp == 0) {
+    unsigned t = s_part[lane], ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned x = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += x;
+    }
+    s_part[32 + lane] = ti - t;          // exclusive warp offsets
+    if (lane == 31) s_part[64] = ti;     // total
+  }
+  __syncthreads();
+  unsigned run = s_part[32 + wp] + inc - sum;
   for (int i = i0; i < i1; ++i) {
     a.plan_off[i] = run;
     if (EV) {
@@ -923,7 +949,7 @@ __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nen
     }
   }
   if (tid == 1023) {
-    unsigned tot = s_part[1023];
+    unsigned tot = s_part[64];
     a.plan_off[nent] = (EV || tot < (unsigned)a.nchunk_cap) ? tot : (unsigned)a.nchunk_cap;
   }
 }

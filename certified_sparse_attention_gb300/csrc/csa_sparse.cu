@@ -829,6 +829,31 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
       for (int h = 0; h < G; ++h)
         if (sv[h] > -INFINITY) exact_levels(sv[h], c32[h], t, neg_r, J, jl[h], hl[h]);
     }
+    if (wlo == whi) {
+      // a one-level round (the common case for flat groups): at most one
+      // event per key, slots by a ballot and one atomic per warp
+      const int l = wlo;
+      unsigned m = 0;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if (!(l > lo[h] && l <= hi[h])) continue;
+        if (jl[h] == l && jl[h] < hl[h]) m |= 1u << h;
+        if (hl[h] == l) {
+          m |= 1u << (8 + h);
+          if (jl[h] < hl[h]) m |= 1u << (16 + h);
+        }
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, m != 0u);
+      unsigned p0 = 0;
+      if (lane == 0 && bal) p0 = atomicAdd(bcnt + l, (unsigned)__popc(bal));
+      p0 = __shfl_sync(0xffffffffu, p0, 0);
+      if (m) {
+        const unsigned p = p0 + (unsigned)__popc(bal & ((1u << lane) - 1u));
+        if (p < (unsigned)a.pcap) bk[(int64_t)l * a.pcap + p] = make_uint2((unsigned)key, m);
+        else atomicOr(a.status, 2u);
+      }
+      continue;
+    }
     // events of the key in the round (a light entry at jl < hl, the
     // light-to-heavy transition at hl), as a mask over 32-level windows
     for (int base = wlo; base <= whi; base += 32) {

@@ -44,7 +44,7 @@ struct Layout {
   int64_t pcap, nblk_max;
   size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, zero_end;
   size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, s32, win, t32, clist, xlist, cmap,
-      buckets, dpart, total;
+      buckets, dpart, pref, total;
   int64_t nchunk_cap;
 };
 
@@ -86,6 +86,7 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.cmap = o; o += up((size_t)L.nchunk_cap * 4);
   L.buckets = o; o += up((size_t)BG * L.J1 * L.pcap * 8);
   L.dpart = o; o += up((size_t)dense_nsplit(s->n_max) * BH * (D + 2) * 4);
+  L.pref = o; o += up((size_t)BH * ACC * 4);
   L.total = o;
   return true;
 }
@@ -300,6 +301,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   a.t32 = (float*)(ws + L.t32); a.clist = (uint2*)(ws + L.clist); a.ccnt = (unsigned*)(ws + L.ccnt);
   a.nfall = (unsigned*)(ws + L.nfall);
   a.rq = (unsigned*)(ws + L.rq);
+  a.pref = (float*)(ws + L.pref);
   a.xlist = (uint2*)(ws + L.xlist); a.xcnt = (unsigned*)(ws + L.xcnt);
   a.chunk_map = (unsigned*)(ws + L.cmap); a.nchunk_cap = L.nchunk_cap;
   a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);

@@ -36,6 +36,7 @@ struct SparseArgs {
   float* vmaxp;           // [B*Hkv]              max vmax over pool blocks
   int* state;             // [B*Hq][4]            lo, hi, stop, flags
   float* t32;             // [B*Hkv][pcap]        perturbation t_i = -log2 u_i
+  float* pref;            // [B*Hq][ACC]          a continuing head's sums through its last range
   uint2* xlist;           // [B*Hkv][n_max]       exact-max set: key, head mask
   unsigned* xcnt;         // [B*Hkv]
   unsigned* chunk_map;    // [nchunk_cap]         gather work item -> bucket entry

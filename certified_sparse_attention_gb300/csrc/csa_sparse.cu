@@ -1540,21 +1540,8 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
   const float L = logf(1.0f / de), Lz = logf(2.0f / de);
   const float* accb = a.acc + (int64_t)bh * a.J1 * ACC;
   int found = -1;
-  // prefix over the levels of earlier rounds; eight independent loads at a
-  // time so the L2 latency is paid once per eight levels
-  for (int x = tid; x < ACC; x += 256) {
-    float run = 0.f;
-    int l = 0;
-    for (; l + 8 <= lo + 1; l += 8) {
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = accb[(int64_t)(l + u) * ACC + x];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) run += v[u];
-    }
-    for (; l <= lo; ++l) run += accb[(int64_t)l * ACC + x];
-    s_run[x] = run;
-  }
+  // sums over the levels of earlier rounds: kept by the previous round
+  for (int x = tid; x < ACC; x += 256) s_run[x] = lo >= 0 ? a.pref[(int64_t)bh * ACC + x] : 0.f;
   __syncthreads();
   for (int l0 = lo + 1; l0 <= hi && found < 0; l0 += LB) {
     const int nl = min(LB, hi - l0 + 1);
@@ -1669,6 +1656,10 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       }
     }
     __syncthreads();
+  }
+  if (found < 0 && hi < J) {
+    // the head continues: keep its sums through this range for the next round
+    for (int x = tid; x < ACC; x += 256) a.pref[(int64_t)bh * ACC + x] = s_run[x];
   }
   if (found < 0 && tid == 0) {
     if (hi >= J) {

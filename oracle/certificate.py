@@ -39,15 +39,31 @@ replaced by a lower confidence bound so the claim is relative to the truth:
     output (||o_hat - o|| <= eps ||o||): beta (1 + eps) <= eps ||o_hat||;
     denom  (|D_hat - D| <= eps D):       dD <= eps (D_hat - dD);
 and always D_hat > dD.
+
+Uncertified comparison mode (picx.dev "Theoretical Contributions": certified
+runs read 1.8-3.5x more keys than uncertified CLT rules): MEASURE_CLT stops
+at the first level where a normal-approximation error estimate meets the
+target,
+    beta_clt = z sqrt(tau G_hat) / D_hat,   z = Phi^-1(1 - delta/2),
+    (tau G_hat estimates Var Z_c = sum_A tau w_i (1 - w_i/tau) ||v_i - c||^2)
+    stop iff D_hat > 0 and beta_clt <= eps M_hat,
+    M_hat = sqrt((H_R + H_B + tau S2) / D_hat)  (plug-in value scale).
+It carries no guarantee; it is the baseline the certificate is compared with.
 Test infrastructure only.
 """
 from __future__ import annotations
 
 import math
+from statistics import NormalDist
 
 import numpy as np
 
-MEASURE_VALUE, MEASURE_OUTPUT, MEASURE_DENOM = 0, 1, 2
+MEASURE_VALUE, MEASURE_OUTPUT, MEASURE_DENOM, MEASURE_CLT = 0, 1, 2, 3
+
+
+def clt_quantile(delta: float) -> float:
+    """z = Phi^-1(1 - delta/2), the two-sided normal quantile."""
+    return NormalDist().inv_cdf(1.0 - delta / 2.0)
 
 
 def chernoff_interval(k: np.ndarray, Lz: float, iters: int = 200):
@@ -86,7 +102,7 @@ def chernoff_interval(k: np.ndarray, Lz: float, iters: int = 200):
 
 
 def certificate_levels(tau, k, S1, Gsum, S2, D_B, N_B, H_B, D_R, N_R, H_R,
-                       Vmax, delta_e, eps, measure=MEASURE_VALUE):
+                       Vmax, delta_e, eps, measure=MEASURE_VALUE, delta=None):
     """Certificate quantities at every level (all float64).
 
     Per-level inputs (leading axis = level): tau, k (light sampled count),
@@ -94,7 +110,8 @@ def certificate_levels(tau, k, S1, Gsum, S2, D_B, N_B, H_B, D_R, N_R, H_R,
     light sampled, with c_j the level's centre), S2 (sum of ||v||^2 over light
     sampled), D_B, N_B [.., d], H_B (heavy sums).  Window sums D_R, N_R [d],
     H_R.  Returns a dict of per-level arrays: D_hat, o_hat, dD, c, beta,
-    scale_lo, certified.
+    scale_lo, certified.  delta (the per-step failure probability) is used
+    only by MEASURE_CLT, whose quantile takes no union bound over levels.
     """
     L = math.log(1.0 / delta_e)
     Lz = math.log(2.0 / delta_e)
@@ -139,6 +156,13 @@ def certificate_levels(tau, k, S1, Gsum, S2, D_B, N_B, H_B, D_R, N_R, H_R,
         extra = {}
         scale = D_hat - dD
         cert = pos & (dD <= eps * (D_hat - dD))
+    elif measure == MEASURE_CLT:
+        z = clt_quantile(delta)
+        beta = z * np.sqrt(tau * np.maximum(G_hat, 0.0)) / D_hat
+        M_hat = np.sqrt((H_R + H_B + tau * S2) / D_hat)
+        extra = {"M_hat": M_hat}
+        scale = M_hat
+        cert = (D_hat > 0) & (beta <= eps * M_hat)
     else:
         raise ValueError("unknown measure")
     return {"D_hat": D_hat, "o_hat": o_hat, "dD": dD, "c": c, "beta": beta,

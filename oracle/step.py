@@ -256,7 +256,8 @@ def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
         k, S1, S2, Gs = sums["k"], sums["S1"], sums["S2"], sums["Gs"]
         D_B, N_B, H_B = sums["D_B"], sums["N_B"], sums["H_B"]
         cert = certificate_levels(tau, k, S1, Gs, S2, D_B, N_B, H_B, D_R, N_R,
-                                  H_R, Vmax, delta_e, p.eps, p.measure)
+                                  H_R, Vmax, delta_e, p.eps, p.measure,
+                                  delta=p.delta)
         ok = np.nonzero(cert["certified"])[0]
         if len(ok):
             js = int(ok[0])

@@ -184,7 +184,8 @@ def compare_group(run, w, K, V, q, b, g, res, p, report):
                                   sums["Gs"], sums["S2"], sums["D_B"],
                                   sums["N_B"], sums["H_B"], det["D_R"],
                                   det["N_R"], det["H_R"], det["Vmax"],
-                                  det["delta_e"], p.eps, p.measure)
+                                  det["delta_e"], p.eps, p.measure,
+                                  delta=p.delta)
         ok = np.nonzero(cert["certified"])[0]
         ref_lvl = int(ok[0]) if len(ok) else J + 1
         gl = int(lvl_g[b, hq])

@@ -14,7 +14,8 @@ import numpy as np
 import pytest
 
 import synth
-from oracle.certificate import (MEASURE_DENOM, MEASURE_OUTPUT, MEASURE_VALUE,
+from oracle.certificate import (MEASURE_CLT, MEASURE_DENOM, MEASURE_OUTPUT,
+                                MEASURE_VALUE, clt_quantile,
                                 certificate_levels, chernoff_interval)
 from oracle.step import Params, dense_attention, oracle_decode_group
 
@@ -262,3 +263,59 @@ def test_bernstein_near_tight_regime(delta_e):
     assert miss_g / n_mc <= delta_e + se
     assert miss_b / n_mc <= 4 * delta_e + se
     assert bad_inter == 0
+
+
+@pytest.mark.parametrize("delta", [0.05, 0.2])
+def test_clt_estimate_coverage_monte_carlo(delta):
+    # The uncertified comparison rule: beta_clt = z sqrt(tau G_hat) / D_hat
+    # with z the two-sided normal quantile.  With small inclusion
+    # probabilities Var Z_c = tau G_A and, for scalar values centred on c,
+    # o_hat - o ~ -Z_c / D, so P(|o_hat - o| <= beta_clt) ~ 1 - delta.  A
+    # dropped square root, tau or quantile moves the coverage far off.
+    m, tau, n_mc, d = 2000, 0.25, 40000, 1
+    rng = np.random.default_rng(31)
+    w = rng.uniform(0.005, 0.03, m) * tau
+    v = rng.normal(0, 1, (m, d))
+    c = np.zeros(d)
+    X = (rng.random((n_mc, m)) < (w / tau)[None, :]).astype(np.float64)
+    vn2 = (v * v).sum(axis=1)
+    gc = ((v - c) ** 2).sum(axis=1)
+    D_R = 5.0
+    N_R = c * D_R
+    J1 = 7                                # levels of the certified rule
+    res = certificate_levels(
+        np.full(n_mc, tau), X.sum(1), X @ v, X @ gc, X @ vn2,
+        np.zeros(n_mc), np.zeros((n_mc, d)), np.zeros(n_mc), D_R, N_R,
+        0.0, float(np.sqrt(vn2.max())), delta / (4.0 * J1), 0.05,
+        MEASURE_CLT, delta=delta)
+    D = D_R + w.sum()
+    o = (N_R + w @ v) / D
+    err = np.linalg.norm(res["o_hat"] - o[None, :], axis=1)
+    cover = (err <= res["beta"]).mean()
+    assert abs(cover - (1.0 - delta)) <= 0.02, cover
+    assert abs(clt_quantile(0.05) - 1.959964) < 1e-5
+    # the certified bound at the same level is wider
+    cert = certificate_levels(
+        np.full(n_mc, tau), X.sum(1), X @ v, X @ gc, X @ vn2,
+        np.zeros(n_mc), np.zeros((n_mc, d)), np.zeros(n_mc), D_R, N_R,
+        0.0, float(np.sqrt(vn2.max())), delta / (4.0 * J1), 0.05,
+        MEASURE_VALUE)
+    assert np.median(res["beta"]) < np.median(cert["beta"])
+
+
+def test_clt_rule_stops_no_later_than_certificate():
+    # on the same draws the uncertified rule stops at or before the
+    # certified stop level (its bound is narrower at every level)
+    w = synth.workload("llama16k", n=3000, Hq=8, Hkv=2)
+    K, V, meta = synth.kv_numpy(w)
+    q = synth.q_numpy(w, meta, 0)
+    seed = int(synth.step_seeds(w, 0)[0])
+    for g in range(w.Hkv):
+        qs = q[0, g * w.G:(g + 1) * w.G]
+        a = oracle_decode_group(qs, K[0, g], V[0, g], w.n, seed, g,
+                                Params(w.eps, w.delta, w.r), keep_detail=False)
+        b = oracle_decode_group(qs, K[0, g], V[0, g], w.n, seed, g,
+                                Params(w.eps, w.delta, w.r, measure=MEASURE_CLT),
+                                keep_detail=False)
+        assert np.all(b.level <= a.level)
+        assert np.all(b.values_read <= a.values_read)

@@ -151,6 +151,57 @@ class Coverage:
                 "reference": "float64 exact attention on the device"}
 
 
+def clt_comparison(args, csa, w, shape, data, lens, seed_tab, nseed, plan,
+                   stream, device, reads_cert):
+    """The same steps under the uncertified CLT stop rule (picx.dev
+    "Theoretical Contributions" compares the certificate with it): keys and
+    values read, time per step, and its error against exact attention."""
+    import torch
+    params = csa.make_params(w.eps, w.delta, w.r, csa.CSA_MEASURE_CLT)
+    step = csa.DecodeStep(shape, params, device, with_stats=False)
+    diag = csa.DecodeStep(shape, params, device, with_stats=True)
+    cov = Coverage(w)
+    kr, vr = [], []
+    for L in range(args.layers):
+        d = data[L]
+        diag(d["q"][L % 4], d["K"], d["V"], d["meta"], lens,
+             seed_tab[L][L % nseed], stream)
+        torch.cuda.synchronize()
+        csa.check(csa.csa_check(diag.ws, stream), "csa_check (CLT)")
+        st = diag.stats.cpu().numpy()
+        kr.append(st[..., 1].mean())
+        vr.append(st[..., 2].mean())
+        cov.add(d["q"][L % 4], d["K"], d["V"], lens, diag)
+    for (L, s) in plan[:3]:
+        d = data[L]
+        step(d["q"][s % 4], d["K"], d["V"], d["meta"], lens,
+             seed_tab[L][s % nseed], stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for (L, s) in plan:
+        d = data[L]
+        step(d["q"][s % 4], d["K"], d["V"], d["meta"], lens,
+             seed_tab[L][s % nseed], stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    csa.check(csa.csa_check(step.ws, stream), "csa_check (CLT timed)")
+    k_clt, v_clt = float(sum(kr) / len(kr)), float(sum(vr) / len(vr))
+    cs = cov.summary()
+    return {"us_per_step": round(e0.elapsed_time(e1) / len(plan) * 1e3, 2),
+            "keys_read_mean": round(k_clt, 1),
+            "values_read_mean": round(v_clt, 1),
+            "certified_over_clt_keys": round(
+                float(sum(x[0] for x in reads_cert)) / len(reads_cert) / k_clt,
+                3),
+            "certified_over_clt_values": round(
+                float(sum(x[1] for x in reads_cert)) / len(reads_cert) / v_clt,
+                3),
+            "eps_violations": cs["eps_violations"],
+            "head_steps": cs["head_steps"],
+            "err_over_epsM": cs["err_over_epsM"]}
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,"
@@ -364,6 +415,7 @@ def run_ours(args, world, rank, local):
     # algorithmic bytes: diagnostics of one step on every rotated layer;
     # the same steps against float64 exact attention (certificate coverage)
     abs_ = []
+    reads = []
     cov = Coverage(w)
     for L in range(args.layers):
         d = data[L]
@@ -373,8 +425,11 @@ def run_ours(args, world, rank, local):
         csa.check(csa.csa_check(step_diag.ws, stream), "csa_check")
         stats = step_diag.stats.cpu().numpy()
         abs_.append(algorithmic_bytes(stats, w, w.n))
+        reads.append((stats[..., 1].mean(), stats[..., 2].mean()))
         cov.add(d["q"][L % 4], d["K"], d["V"], lens, step_diag)
     ab = {k: sum(x[k] for x in abs_) / len(abs_) for k in abs_[0]}
+    clt = clt_comparison(args, csa, w, shape, data, lens, seed_tab, nseed,
+                         plan, stream, device, reads)
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -489,6 +544,7 @@ def run_ours(args, world, rank, local):
         "sparse_over_dense_time": round(ms_sparse / ms_dense, 3),
         "levels_hist": [int(x) for x in np.bincount(levels.ravel())],
         "certificate": cov.summary(),
+        "clt_comparison": clt,
         "keys_read_mean": float(stats[..., 1].mean()),
         "values_read_mean": float(stats[..., 2].mean()),
         "clocks": clocks.summary(),

@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(HERE, "_lib", "libcsa.so")
 
 CSA_OK = 0
 CSA_BF16, CSA_F32 = 0, 1
-CSA_MEASURE_VALUE, CSA_MEASURE_OUTPUT, CSA_MEASURE_DENOM = 0, 1, 2
+CSA_MEASURE_VALUE, CSA_MEASURE_OUTPUT, CSA_MEASURE_DENOM, CSA_MEASURE_CLT = \
+    0, 1, 2, 3
 WINDOW = 64
 BLOCK = 64
 

@@ -36,7 +36,18 @@ csa_status shape_supported(const csa_shape* s) {
 }
 bool params_ok(const csa_params* p) {
   return p && p->eps > 0.f && std::isfinite(p->eps) && p->delta > 0.f && p->delta < 1.f && p->r >= 1 &&
-         p->r <= 4 && p->measure >= 0 && p->measure <= 2 && p->J_override >= -1 && p->J_override <= kMaxJ;
+         p->r <= 4 && p->measure >= 0 && p->measure <= 3 && p->J_override >= -1 && p->J_override <= kMaxJ;
+}
+
+// z with P(|N(0,1)| > z) = delta, i.e. erfc(z / sqrt 2) = delta: bisection
+// on the decreasing function erfc (double precision, 200 halvings).
+float normal_quantile_two_sided(double delta) {
+  double lo = 0.0, hi = 40.0;
+  for (int i = 0; i < 200; ++i) {
+    const double mid = 0.5 * (lo + hi);
+    if (std::erfc(mid / std::sqrt(2.0)) > delta) lo = mid; else hi = mid;
+  }
+  return (float)(0.5 * (lo + hi));
 }
 
 struct Layout {
@@ -310,6 +321,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max; a.nblk_max = L.nblk_max;
   a.pcap = L.pcap; a.J1 = L.J1; a.r = params->r; a.eps = params->eps; a.delta = params->delta;
   a.measure = params->measure; a.rs = rs;
+  a.zclt = normal_quantile_two_sided((double)params->delta);
 
   const int nsm = sm_count();
   if (plive > 0) {

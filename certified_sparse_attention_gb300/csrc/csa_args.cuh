@@ -64,6 +64,7 @@ struct SparseArgs {
   int r;
   float eps, delta;
   int measure;
+  float zclt;             // two-sided normal quantile at delta (CLT rule)
   float rs;               // float32(1/sqrt d)
 };
 

@@ -743,6 +743,10 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
         const float Dh = DR + db + tau * k;
         if (a.measure == CSA_MEASURE_DENOM) {
           pass = Dh > dD && dD <= a.eps * (Dh - dD);
+        } else if (a.measure == CSA_MEASURE_CLT) {
+          const float Gh = tau * k * fmaxf(nu - cn2, 0.f);
+          const float Mh = sqrtf((HR + db * nu + tau * k * nu) / Dh);
+          pass = Dh > 0.f && a.zclt * sqrtf(tau * Gh) <= a.eps * Mh * Dh;
         } else {
           const float Gh = tau * k * fmaxf(nu - cn2, 0.f);
           const float aa = sqrtf(2.f * tau * Rc * Rc * L);
@@ -1606,9 +1610,13 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       const float Ghi = 0.25f * (aa + sq) * (aa + sq);
       const float zeta = sqrtf(2.f * tau * Ghi * Lz) + (2.f / 3.f) * tau * Rc * Lz;
       const bool pos = Dh > dD;
-      const float beta = pos ? (zeta + sqrtf(oc) * dD) / (Dh - dD) : INFINITY;
+      float beta = pos ? (zeta + sqrtf(oc) * dD) / (Dh - dD) : INFINITY;
       bool cert;
-      if (a.measure == CSA_MEASURE_VALUE) {
+      if (a.measure == CSA_MEASURE_CLT) {
+        beta = a.zclt * sqrtf(tau * Gh) / Dh;
+        const float Mh = sqrtf((HR + HB + tau * S2) / Dh);
+        cert = Dh > 0.f && beta <= a.eps * Mh;
+      } else if (a.measure == CSA_MEASURE_VALUE) {
         const float Hh = tau * S2;
         const float ap = sqrtf(2.f * tau * Vp * Vp * L);
         const float br = Hh - (2.f / 3.f) * tau * Vp * Vp * L;

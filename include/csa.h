@@ -68,9 +68,16 @@ typedef enum { CSA_BF16 = 0, CSA_F32 = 1 } csa_dtype;
 /* Error measure that stops a head (picx.dev "Problem Setup"):
  *  VALUE  ||o_hat - o|| <= eps * M,  M^2 = sum_i a_i ||v_i||^2  (default)
  *  OUTPUT ||o_hat - o|| <= eps * ||o||
- *  DENOM  |D_hat - D|   <= eps * D                                          */
+ *  DENOM  |D_hat - D|   <= eps * D
+ *  CLT    UNCERTIFIED comparison rule (picx.dev "Theoretical Contributions",
+ *         which compares the certificate with CLT-style stop rules): stops at
+ *         the first level with z sqrt(tau G_hat) / D_hat <= eps M_hat, z the
+ *         two-sided normal quantile at delta, M_hat the plug-in value scale;
+ *         the returned beta is that normal-approximation estimate, not a
+ *         bound.                                                             */
 typedef enum {
-  CSA_MEASURE_VALUE = 0, CSA_MEASURE_OUTPUT = 1, CSA_MEASURE_DENOM = 2
+  CSA_MEASURE_VALUE = 0, CSA_MEASURE_OUTPUT = 1, CSA_MEASURE_DENOM = 2,
+  CSA_MEASURE_CLT = 3
 } csa_measure;
 
 typedef struct {

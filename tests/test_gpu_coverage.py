@@ -183,3 +183,43 @@ def test_stress_1m_flat_and_adversarial():
         w = synth.workload("llama16k", n=w0.n, eps=0.05, regime=regime)
         summary = _coverage(w, steps=1)
         print("stress 1M", regime, summary)
+
+
+def test_clt_rule_stops_no_later_llama16k():
+    # the uncertified CLT comparison rule on the same steps: its estimate is
+    # below the certified bound at every level and its value scale above the
+    # certified lower bound, so no head stops later than under the
+    # certificate; its error against exact attention is reported, not bounded
+    import torch
+    import certified_sparse_attention_gb300 as csa
+    w = synth.workload("llama16k")
+    dev = torch.device("cuda:0")
+    K, V, meta = synth.kv_torch(w, device=dev)
+    shape = csa.make_shape(w.B, w.Hq, w.Hkv, w.d, w.n, w.dtype)
+    mt = csa.meta_buffers(shape, dev)
+    lens = [w.n] * w.B
+    csa.check(csa.csa_quantize_keys(shape, K, V, lens, 0, *mt))
+    cert = csa.DecodeStep(shape, csa.make_params(w.eps, w.delta, w.r), dev,
+                          with_stats=True)
+    clt = csa.DecodeStep(shape, csa.make_params(w.eps, w.delta, w.r,
+                                                csa.CSA_MEASURE_CLT), dev,
+                         with_stats=True)
+    J = int(np.ceil(w.r * np.log2(w.n - 64)))
+    tally = _Tally()
+    kc, kl = 0, 0
+    for s in range(4):
+        q = synth.q_torch(w, meta, s, device=dev)
+        seeds = [int(x) for x in synth.step_seeds(w, s)]
+        cert(q, K, V, mt, lens, seeds)
+        o_hat, beta, level, _ = clt(q, K, V, mt, lens, seeds)
+        torch.cuda.synchronize()
+        csa.check(csa.csa_check(cert.ws), "csa_check")
+        csa.check(csa.csa_check(clt.ws), "csa_check")
+        assert torch.all(clt.level <= cert.level)
+        assert torch.all(clt.stats[..., 1] <= cert.stats[..., 1])
+        kc += int(cert.stats[..., 1].sum())
+        kl += int(clt.stats[..., 1].sum())
+        o, M = _exact(q, K, V, lens, w.G)
+        tally.add(o_hat, beta, level, o, M, w.eps, J)
+    print("CLT rule llama16k: keys certified/CLT", kc / kl,
+          "eps violations", tally.eps_viol, "of", tally.n)

@@ -144,7 +144,7 @@ def test_decode_group_sizes(G, d):
     run_and_compare(w, K, V, q, [900], seeds, 900)
 
 
-@pytest.mark.parametrize("measure", [1, 2])
+@pytest.mark.parametrize("measure", [1, 2, 3])
 def test_decode_other_measures(measure):
     w, K, V, q = _case("llama16k", 1100, Hq=8, Hkv=2)
     seeds = synth.step_seeds(w, 6)

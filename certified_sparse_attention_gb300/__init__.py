@@ -40,7 +40,7 @@ STAT = {"level": 0, "keys_read": 1, "values_read": 2, "n_candidates": 3,
         "group_values_read": 8}
 PHASES = ("clear", "scan", "exact_max", "candidates", "rescore", "predict",
           "levels", "plan", "vgather", "certify", "fallback", "diagnostics",
-          "prehist")
+          "reserved")
 
 
 class CsaLibraryMissing(RuntimeError):

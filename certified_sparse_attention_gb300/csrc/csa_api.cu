@@ -53,8 +53,8 @@ float normal_quantile_two_sided(double delta) {
 struct Layout {
   int J1;
   int64_t pcap, nblk_max;
-  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, zero_end;
-  size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, s32, win, t32, clist, xlist, cmap,
+  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, front, zero_end;
+  size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, hw, s32, win, t32, clist, xlist, cmap,
       buckets, dpart, pref, total;
   int64_t nchunk_cap;
 };
@@ -80,6 +80,7 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.xcnt = o; o += up((size_t)BG * 4);
   L.nfall = o; o += up(4);
   L.rq = o; o += up(((size_t)BG * 6 + 6) * 4);
+  L.front = o; o += up((size_t)4 * BG * 4);
   L.zero_end = o;
   L.winstats = o; o += up((size_t)BH * (D + 4) * 4);
   L.vmaxp = o; o += up((size_t)BG * 4);
@@ -88,6 +89,7 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.plan_end = o; o += up((size_t)BG * L.J1 * 4);
   L.plan_off = o; o += up(((size_t)BG * L.J1 + 1) * 4);
   L.ubar = o; o += up((size_t)BG * s->n_max * G * 4);
+  L.hw = o; o += up((size_t)BG * L.nblk_max * G * 4);
   L.s32 = o; o += up((size_t)BG * L.pcap * G * 4);
   L.win = o; o += up((size_t)BG * kWindow * G * 4);
   L.t32 = o; o += up((size_t)BG * L.pcap * 4);
@@ -295,6 +297,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
 
   ScanArgs sa;
   sa.q = q; sa.K4 = K4; sa.bounds = bounds; sa.ubar = (float*)(ws + L.ubar);
+  sa.hw = (float*)(ws + L.hw);
   sa.cmax = (unsigned*)(ws + L.cmax); sa.status = (unsigned*)(ws + L.status);
   sa.Hq = shape->Hq; sa.Hkv = shape->Hkv; sa.n_max = shape->n_max; sa.nblk_max = L.nblk_max; sa.rs = rs;
   cudaError_t e = launch_scan(sa, seq, shape->B, shape->d, G, bf16, nlive, st);
@@ -313,6 +316,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   a.nfall = (unsigned*)(ws + L.nfall);
   a.rq = (unsigned*)(ws + L.rq);
   a.pref = (float*)(ws + L.pref);
+  a.hw = (const float*)(ws + L.hw); a.front = (int*)(ws + L.front);
   a.xlist = (uint2*)(ws + L.xlist); a.xcnt = (unsigned*)(ws + L.xcnt);
   a.chunk_map = (unsigned*)(ws + L.cmap); a.nchunk_cap = L.nchunk_cap;
   a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);
@@ -327,11 +331,9 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   if (plive > 0) {
     if (launch_cstar(a, seq, shape->d, G, bf16, nlive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
     prof_mark(2, st);
-    if (launch_rescore(a, seq, shape->d, G, bf16, plive, nsm, st, g_prof.on ? prof_mark : nullptr) !=
-        cudaSuccess)
-      return CSA_ERR_CUDA;
-    prof_mark(12, st);
-    count_launches(5);
+    if (launch_candidates(a, seq, G, plive, st) != cudaSuccess) return CSA_ERR_CUDA;
+    prof_mark(3, st);
+    count_launches(3);
   }
   if (launch_predict(a, seq, shape->d, G, bf16, st) != cudaSuccess) return CSA_ERR_CUDA;
   count_launches(1);
@@ -340,7 +342,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
     if (launch_round(a, seq, shape->d, G, bf16, plive > 0 ? plive : 1, round, nsm, st,
                      g_prof.on ? prof_mark : nullptr) != cudaSuccess)
       return CSA_ERR_CUDA;
-    count_launches(4);
+    count_launches(5);
   }
   // exact attention for heads with no certified level and sequences without a pool
   DenseArgs da;

@@ -11,6 +11,7 @@ struct ScanArgs {
   const uint8_t* K4;
   const float* bounds;
   float* ubar;          // [B*Hkv][n_max][G]
+  float* hw;            // [B*Hkv][nblk_max][G] half width (ubar - l) / 2 per block
   unsigned* cmax;       // [B*Hq][4] ordered floats: c_lo, c_hi, cb, c32
   unsigned* status;
   int Hq, Hkv;
@@ -25,12 +26,13 @@ struct SparseArgs {
   const float* vmax;      // [B*Hkv][nblk_max]
   const float* vnorm2;    // [B*Hkv][n_max]        ||v_i||^2 per token
   const float* ubar;      // [B*Hkv][n_max][G]
-  float* s32;             // [B*Hkv][pcap][G]     candidate scores (-inf: not a candidate)
+  const float* hw;        // [B*Hkv][nblk_max][G] half width of the score bound per block
+  float* s32;             // [B*Hkv][pcap][G]     scores (-inf: not a candidate, or not rescored)
   float* win;             // [B*Hkv][64][G]       window scores
   unsigned* cmax;         // [B*Hq][4]            c_lo, c_hi, cb, c32 (ordered)
   unsigned* jr_hist;      // [B*Hq][J1+1]         first level a key's K row is needed
   unsigned* ncand;        // [B*Hq]
-  float* pre_hist;        // [B*Hq][J1][4]        d k, d D_B, d sampled (value free)
+  float* pre_hist;        // [B*Hq][J1][4]        d k, d D_B, d sampled (value free, estimated)
   float* acc;             // [B*Hq][J1][ACC]      d S1[D], d N_B[D], d k, d S2, d D_B, d H_B, d sampled
   float* winstats;        // [B*Hq][D+4]          N_R[D], D_R, H_R
   float* vmaxp;           // [B*Hkv]              max vmax over pool blocks
@@ -41,7 +43,8 @@ struct SparseArgs {
   unsigned* xcnt;         // [B*Hkv]
   unsigned* chunk_map;    // [nchunk_cap]         gather work item -> bucket entry
   int64_t nchunk_cap;
-  uint2* clist;           // [B*Hkv][pcap]        candidates to rescore: key, head mask
+  uint2* clist;           // [B*Hkv][pcap]        candidates: key, head mask | min bound level << 8
+  int* front;             // [4][B*Hkv]           rescored through bound level (+1) before round r
   unsigned* ccnt;         // [B*Hkv]
   unsigned* nfall;        // heads that need the exact fallback
   unsigned* rq;           // round queues: [3][B*Hkv] groups per round, [3][B*Hkv] flags,
@@ -98,8 +101,7 @@ cudaError_t launch_scan(const ScanArgs&, const SeqArgs&, int B, int d, int G, bo
                         cudaStream_t);
 cudaError_t launch_cstar(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t nmax_live,
                          int nsm, cudaStream_t);
-cudaError_t launch_rescore(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t pmax_live,
-                           int nsm, cudaStream_t, void (*mark)(int, cudaStream_t));
+cudaError_t launch_candidates(const SparseArgs&, const SeqArgs&, int G, int64_t pmax_live, cudaStream_t);
 cudaError_t launch_predict(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, cudaStream_t);
 typedef void (*PhaseMark)(int phase, cudaStream_t);
 cudaError_t launch_round(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t pmax_live,

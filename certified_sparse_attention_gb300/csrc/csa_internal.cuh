@@ -17,6 +17,7 @@ namespace csa {
 constexpr int kBlock = 64;     // quantisation block (tokens)
 constexpr int kWindow = 64;    // window read exactly (last tokens)
 constexpr int kTile = 256;     // keys per scan / candidate tile
+constexpr int kCandSeg = 4096; // pool keys per candidate-list segment (one candidate CTA)
 constexpr int kMaxB = 128;     // sequences per call
 constexpr int kMaxJ = 255;     // last grid level supported
 

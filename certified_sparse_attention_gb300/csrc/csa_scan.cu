@@ -168,6 +168,10 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
       s_alpha[blk][h] = alpha;
       s_bhi[blk][h] = bhi;
       s_blo[blk][h] = blo;
+      // half width of the block's score interval: the candidate pass takes
+      // ubar minus it as a score estimate for the stop prediction
+      const int64_t gblk = key0 / kBlock + blk;
+      if (gblk < nblk_n) a.hw[((int64_t)bg * a.nblk_max + gblk) * G + h] = fmul(0.5f, fsub(bhi, blo));
       if (!isfinite(bhi) || !isfinite(blo) || !isfinite(alpha)) atomicOr(a.status, 1u);
     }
     // pack the code: word w covers channels 8w..8w+7; even word = channels

@@ -9,12 +9,15 @@
 //                   lower bound cb = max fl(s32 - fl(mag * 2^-13))
 //   cand_kernel     perturbations t_i, bound levels jbar_i, candidates
 //                   (jbar <= J); keys of the exact-max set keep the scores
-//                   already computed, the others are compacted into a list
-//   rows_kernel<1>  float32 scores of the listed candidate K rows
-//   prehist_kernel  exact levels; per-level counts and heavy weights that
-//                   need no values (for the stop predictor)
+//                   already computed, the others are compacted into a list;
+//                   per-level counts and heavy weights of estimated levels
+//                   (no values, no K rows: for the stop predictor)
 //   predict_kernel  window sums (D_R, N_R, H_R) and a predicted stop level
 //                   per head that sizes the first gather round
+//   rows_kernel<1>  (per round) float32 scores of the listed candidates
+//                   whose smallest bound level lies in the range that the
+//                   round's levels newly need (jbar_i <= j implies
+//                   jl_i >= jbar_i, so a key outside it has no event there)
 //   levels_kernel   (per round) each key that changes a head's sums at a
 //                   level of the round is appended once to the (b, g, level)
 //                   bucket, with per-head event masks
@@ -263,36 +266,66 @@ __global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __g
 // MODE 0 (exact max): entries = exact-max set.  Scores and |product| sums
 //   of every head; the maxima of s32 and fl(s32 - fl(mag 2^-13)) over the
 //   heads in the entry's mask; raw scores stored (pool: s32, window: win).
-// MODE 1 (candidates): entries = candidates still to score; scores stored,
+// MODE 1 (candidates, per round): entries = candidates whose smallest bound
+//   level lies in (lold, lnew], the range this round newly needs (lnew = the
+//   largest range end of the group's heads still running); scores stored,
 //   -inf for the heads the key is not a candidate of.
+//
+// Each warp takes a contiguous share of the list (in key order within the
+// candidate pass's CTA chunks, so consecutive rows are mostly adjacent in
+// HBM), reads it 128 entries ahead, compacts the wanted entries into a
+// small queue and stages them eight rows per ring slot.
+
+constexpr int kQueue = 64;       // per-warp queue of wanted entries (power of 2)
 
 template <int D, int G, typename E>
-constexpr int rows_smem() {
-  return kRingW * kRingS * 8 * D * (int)sizeof(E) + kRingW * kRingS * 8 * 8 + kRingW * G * 2 * 4;
+__host__ __device__ constexpr int rows_smem() {
+  return kRingW * kRingS * 8 * D * (int)sizeof(E) + kRingW * kRingS * 8 * 8 + kRingW * kQueue * 8 +
+         kRingW * G * 2 * 4;
 }
 
 template <int D, int G, typename E, int MODE>
-__global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+__global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+                                                   int round) {
   pdl_entry();
   constexpr int CPL = D / 32;
   constexpr int RB = D * (int)sizeof(E);
   extern __shared__ __align__(16) uint8_t dsm[];
   uint8_t* ring = dsm;
   uint2* s_ent = reinterpret_cast<uint2*>(dsm + kRingW * kRingS * 8 * RB);
-  float* s_red = reinterpret_cast<float*>(dsm + kRingW * kRingS * 8 * RB + kRingW * kRingS * 8 * 8);
+  uint2* s_q = s_ent + kRingW * kRingS * 8;
+  float* s_red = reinterpret_cast<float*>(s_q + kRingW * kQueue);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
   const int64_t P = n - kWindow;
-  const unsigned* cntp = MODE == 0 ? a.xcnt : a.ccnt;
-  const uint2* list = MODE == 0 ? a.xlist + (int64_t)bg * a.n_max : a.clist + (int64_t)bg * a.pcap;
-  const int cnt = (int)cntp[bg];
-  const int nbatch = (cnt + 7) / 8;
-  if ((int)blockIdx.x * kRingW >= nbatch) return;
   const int bh0 = b * a.Hq + g * G;
+  const uint2* list;
+  int cnt, lold = -1, lnew = -1;
+  if (MODE == 0) {
+    list = a.xlist + (int64_t)bg * a.n_max;
+    cnt = (int)a.xcnt[bg];
+  } else {
+    list = a.clist + (int64_t)bg * a.pcap;
+    cnt = (int)a.ccnt[bg];
+    const int BG = a.B * a.Hkv;
+    lold = a.front[round * BG + bg] - 1;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const int* st = a.state + (int64_t)(bh0 + h) * 4;
+      if (!(st[3] & kFlagDone)) lnew = max(lnew, st[1]);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.front[(round + 1) * BG + bg] = max(lold, lnew) + 1;
+    if (lnew <= lold) return;
+  }
+  // the warp's share [cur, end) of the list
+  const int nw = gridDim.x * kRingW;
+  const int wid = blockIdx.x * kRingW + w;
+  int cur = (int)((int64_t)cnt * wid / nw);
+  const int end = (int)((int64_t)cnt * (wid + 1) / nw);
   float qv[G][CPL];
-  {
+  if (MODE == 0 || sizeof(E) != 2) {
     const E* qp = reinterpret_cast<const E*>(a.q) + ((int64_t)b * a.Hq + (int64_t)g * G) * D;
 #pragma unroll
     for (int h = 0; h < G; ++h) load_row<D, E>(qp + (int64_t)h * D, qv[h]);
@@ -303,26 +336,57 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
   const E* Kb = reinterpret_cast<const E*>(a.K) + (int64_t)bg * a.n_max * D;
   uint8_t* my = ring + w * kRingS * 8 * RB;
   uint2* me = s_ent + w * kRingS * 8;
-  const int wid = blockIdx.x * kRingW + w;
-  const int wstride = gridDim.x * kRingW;
-  // entries of ring cycle c, batch k = lane / 8, row lane % 8
-  auto load_ent = [&](int cyc) {
-    const int bt = wid + (4 * cyc + (lane >> 3)) * wstride;
-    const int row = bt * 8 + (lane & 7);
-    return (bt < nbatch && row < cnt) ? list[row] : make_uint2(0u, 0u);
-  };
-  auto nvalid = [&](int bt) { return bt < nbatch ? min(8, cnt - bt * 8) : 0; };
-  constexpr bool TC = (MODE == 1) && (sizeof(E) == 2);   // tensor-core scoring
-  {
-    const uint2 e0 = load_ent(0);
-    me[(lane >> 3) * 8 + (lane & 7)] = e0;
-    __syncwarp();
+  uint2* myq = s_q + w * kQueue;
+  // entries are read 128 at a time (four per lane), one window ahead
+  uint2 cw[4], nx[4];
+  auto load_win = [&](int base, uint2 (&dst)[4]) {
 #pragma unroll
-    for (int k = 0; k < kRingS; ++k) {
-      if (TC) stage8_swz<D, E>(my + k * 8 * RB, Kb, me + k * 8, nvalid(wid + k * wstride));
-      else stage8<D, E>(my + k * 8 * RB, Kb, me + k * 8, nvalid(wid + k * wstride));
-      cp_async_commit();
+    for (int k = 0; k < 4; ++k) {
+      const int i = base + 32 * k + lane;
+      dst[k] = i < end ? list[i] : make_uint2(~0u, 0u);
     }
+  };
+  load_win(cur, cw);
+  load_win(cur + 128, nx);
+  int ck = 0;                 // next 32-entry chunk of the current window
+  int qh = 0, qt = 0;         // queue head and tail (warp-uniform)
+  // fill ring slot k with up to eight wanted entries; 0 only when the
+  // warp's share is exhausted
+  auto produce = [&](int k) {
+    while (qt - qh < 8 && cur < end) {
+      const uint2 e = ck == 0 ? cw[0] : (ck == 1 ? cw[1] : (ck == 2 ? cw[2] : cw[3]));
+      bool keep = e.x != ~0u;
+      if (MODE == 1 && keep) {
+        const int jm = (int)((e.y >> 8) & 0xFFu);
+        keep = jm > lold && jm <= lnew;
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) myq[(qt + __popc(bal & ((1u << lane) - 1u))) & (kQueue - 1)] = e;
+      qt += __popc(bal);
+      cur += 32;
+      if (++ck == 4) {
+        ck = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cw[q] = nx[q];
+        load_win(cur + 128, nx);
+      }
+    }
+    __syncwarp();
+    const int take = min(8, qt - qh);
+    if (lane < take) me[k * 8 + lane] = myq[(qh + lane) & (kQueue - 1)];
+    qh += take;
+    __syncwarp();
+    return take;
+  };
+  constexpr bool TC = (MODE == 1) && (sizeof(E) == 2);   // tensor-core scoring
+  unsigned nvpack = 0;        // rows staged per slot, 8 bits each
+#pragma unroll
+  for (int k = 0; k < kRingS; ++k) {
+    const int nv = produce(k);
+    nvpack |= (unsigned)nv << (8 * k);
+    if (TC) stage8_swz<D, E>(my + k * 8 * RB, Kb, me + k * 8, nv);
+    else stage8<D, E>(my + k * 8 * RB, Kb, me + k * 8, nv);
+    cp_async_commit();
   }
   // query fragments for the tensor-core path: M = heads (rows >= G zero),
   // K = channels, two bf16 per register
@@ -338,14 +402,13 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
       qa[ks][1] = gq < G ? *reinterpret_cast<const unsigned*>(qp + 16 * ks + 2 * tq + 8) : 0u;
     }
   }
-  uint2 pre = load_ent(1), pre2 = load_ent(2);
   for (int it = 0;; ++it) {
-    const int bt = wid + it * wstride;
-    if (bt >= nbatch) break;
     const int slot = it & (kRingS - 1);
+    const int nv = (int)((nvpack >> (8 * slot)) & 0xFFu);
+    // slots are filled in order, so the first empty one ends the share
+    if (nv == 0) break;
     cp_async_wait<kRingS - 1>();
     __syncwarp();
-    const int nv = nvalid(bt);
     if (TC) {
       // scores of the stage's eight rows for all heads in one chain of
       // m16n8k16 products; lane (g, t) gets head g, rows 2t and 2t+1
@@ -370,64 +433,58 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
           }
         }
       }
-      __syncwarp();
-      if ((lane >> 3) == slot) me[slot * 8 + (lane & 7)] = pre;
-      __syncwarp();
-      stage8_swz<D, E>(my + slot * 8 * RB, Kb, me + slot * 8, nvalid(bt + kRingS * wstride));
-      cp_async_commit();
-      if (slot == kRingS - 1) { pre = pre2; pre2 = load_ent((it >> 2) + 3); }
-      continue;
-    }
-    float kv[8][CPL];
+    } else {
+      float kv[8][CPL];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) load_row<D, E>(reinterpret_cast<const E*>(my + (slot * 8 + r) * RB), kv[r]);
-    float sc[G], mg[G];
+      for (int r = 0; r < 8; ++r) load_row<D, E>(reinterpret_cast<const E*>(my + (slot * 8 + r) * RB), kv[r]);
+      float sc[G], mg[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float part[8], pm[8];
+      for (int h = 0; h < G; ++h) {
+        float part[8], pm[8];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        float p[CPL], pa[CPL];
+        for (int r = 0; r < 8; ++r) {
+          float p[CPL], pa[CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          p[c] = fmul(kv[r][c], qv[h][c]);
-          pa[c] = fabsf(p[c]);
-        }
-        part[r] = local_tree<CPL>(p);
-        if (MODE == 0) pm[r] = local_tree<CPL>(pa);
-      }
-      sc[h] = fmul(reduce8_rows(part), a.rs);
-      if (MODE == 0) mg[h] = fmul(reduce8_rows(pm), a.rs);
-    }
-    const int r = lane & 7;
-    if (lane < 8 && r < nv) {
-      const uint2 en = me[slot * 8 + r];
-      const int64_t key = en.x;
-      const unsigned cm = en.y;
-      if (MODE == 0) {
-        float* wp = key >= P ? a.win + ((int64_t)bg * kWindow + (key - P)) * G
-                             : a.s32 + ((int64_t)bg * a.pcap + key) * G;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          wp[h] = sc[h];
-          if ((cm >> h) & 1u) {
-            cbm[h] = fmaxf(cbm[h], fsub(sc[h], fmul(mg[h], 1.220703125e-04f)));   // 2^-13
-            c3m[h] = fmaxf(c3m[h], sc[h]);
+          for (int c = 0; c < CPL; ++c) {
+            p[c] = fmul(kv[r][c], qv[h][c]);
+            pa[c] = fabsf(p[c]);
           }
+          part[r] = local_tree<CPL>(p);
+          if (MODE == 0) pm[r] = local_tree<CPL>(pa);
         }
-      } else {
-        float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
+        sc[h] = fmul(reduce8_rows(part), a.rs);
+        if (MODE == 0) mg[h] = fmul(reduce8_rows(pm), a.rs);
+      }
+      const int r = lane & 7;
+      if (lane < 8 && r < nv) {
+        const uint2 en = me[slot * 8 + r];
+        const int64_t key = en.x;
+        const unsigned cm = en.y;
+        if (MODE == 0) {
+          float* wp = key >= P ? a.win + ((int64_t)bg * kWindow + (key - P)) * G
+                               : a.s32 + ((int64_t)bg * a.pcap + key) * G;
 #pragma unroll
-        for (int h = 0; h < G; ++h) sp[h] = ((cm >> h) & 1u) ? sc[h] : -INFINITY;
+          for (int h = 0; h < G; ++h) {
+            wp[h] = sc[h];
+            if ((cm >> h) & 1u) {
+              cbm[h] = fmaxf(cbm[h], fsub(sc[h], fmul(mg[h], 1.220703125e-04f)));   // 2^-13
+              c3m[h] = fmaxf(c3m[h], sc[h]);
+            }
+          }
+        } else {
+          float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
+#pragma unroll
+          for (int h = 0; h < G; ++h) sp[h] = ((cm >> h) & 1u) ? sc[h] : -INFINITY;
+        }
       }
     }
     __syncwarp();
-    // refill this slot with the batch kRingS iterations ahead
-    if ((lane >> 3) == slot) me[slot * 8 + (lane & 7)] = pre;
-    __syncwarp();
-    stage8<D, E>(my + slot * 8 * RB, Kb, me + slot * 8, nvalid(bt + kRingS * wstride));
+    // refill this slot: the next rows of the share, kRingS batches ahead
+    const int nn = produce(slot);
+    nvpack = (nvpack & ~(0xFFu << (8 * slot))) | ((unsigned)nn << (8 * slot));
+    if (TC) stage8_swz<D, E>(my + slot * 8 * RB, Kb, me + slot * 8, nn);
+    else stage8<D, E>(my + slot * 8 * RB, Kb, me + slot * 8, nn);
     cp_async_commit();
-    if (slot == kRingS - 1) { pre = pre2; pre2 = load_ent((it >> 2) + 3); }
   }
   cp_async_wait<0>();
   if (MODE == 0) {
@@ -451,16 +508,38 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
 
 // ------------------------------------------------------------- candidates
 
-constexpr int kTilesPerCta = 16;   // key tiles per CTA of the per-key passes
+constexpr int kTilesPerCta = kCandSeg / kTile;   // key tiles per CTA of the per-key passes
 
+// Dynamic shared memory of the candidate pass: the staged list, then per
+// head the bound-level histogram and the estimated-level histograms.
+constexpr int cand_smem(int G, int J1) {
+  return kTile * kTilesPerCta * 8 + G * (J1 + 1) * 4 + G * J1 * 2 * 4 + G * J1 * 4;
+}
+
+// One pass over the pool keys of a group (after the exact maximum):
+//  * t_i, the bound level jbar_i per head, the candidate list (jbar <= J;
+//    the entry carries the head mask and the smallest jbar over the heads,
+//    so that a round rescores only the range it newly needs), the
+//    histogram of the first level at which a key's K row is needed;
+//  * scores reset to -inf for keys outside the exact-max set: a candidate's
+//    score is written when it is rescored, and until then it has no event;
+//  * value-free level histograms from an estimated score (exact for the
+//    exact-max set, ubar minus the block's half width otherwise; the other
+//    keys subsampled one tile in four): counts of light entries and exits,
+//    sampled entries and fixed-point heavy weights per level.  They only
+//    size the first gather round.
 template <int G>
 __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
   pdl_entry();
-  __shared__ unsigned s_jr[G][kMaxJ + 2];
-  __shared__ unsigned s_nc[G];
+  extern __shared__ __align__(16) uint8_t dsm[];
+  const int J1 = a.J1, JS = a.J1 + 1;
   // the CTA's candidates, staged here and written out with one global slot
   // reservation (a per-warp reservation on the group's counter serialises)
-  __shared__ uint2 s_list[kTile * kTilesPerCta];
+  uint2* s_list = reinterpret_cast<uint2*>(dsm);
+  unsigned* s_jr = reinterpret_cast<unsigned*>(dsm + kTile * kTilesPerCta * 8);   // [G][JS]
+  int* s_cnt = reinterpret_cast<int*>(s_jr + G * JS);                              // [G][J1][2]
+  unsigned* s_db = reinterpret_cast<unsigned*>(s_cnt + G * J1 * 2);                // [G][J1]
+  __shared__ unsigned s_nc[G];
   __shared__ unsigned s_n, s_gbase;
   const int tid = threadIdx.x, lane = tid & 31;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
@@ -471,60 +550,106 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   if (kbase >= P) return;
   const int J = seq.J[b];
   const float neg_r = -(float)a.r;
-  for (int i = tid; i < G * (J + 2); i += 256) (&s_jr[0][0])[(i / (J + 2)) * (kMaxJ + 2) + i % (J + 2)] = 0u;
+  for (int i = tid; i < G * JS; i += 256) s_jr[i] = 0u;
+  for (int i = tid; i < G * J1 * 2; i += 256) s_cnt[i] = 0;
+  for (int i = tid; i < G * J1; i += 256) s_db[i] = 0u;
   if (tid < G) s_nc[tid] = 0u;
   if (tid == 0) s_n = 0u;
   __syncthreads();
   const int bh0 = b * a.Hq + g * G;
+  float c_lo[G], c_b[G], c32[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    c_lo[h] = cmax_get(a, bh0 + h, 0);
+    c_b[h] = cmax_get(a, bh0 + h, 2);
+    c32[h] = cmax_get(a, bh0 + h, 3);
+  }
   const unsigned long long gk = group_key(seq.seed[b], g);
+  // ubar and the block half widths of a key, loaded one tile ahead
+  auto load_key = [&](int64_t k, float (&u)[G], float (&h)[G]) {
+    if (k >= P) return;
+    const float* up = a.ubar + ((int64_t)bg * a.n_max + k) * G;
+    const float* hp = a.hw + ((int64_t)bg * a.nblk_max + k / kBlock) * G;
+    if (G == 4) {
+      const float4 f = *reinterpret_cast<const float4*>(up);
+      u[0] = f.x; u[1 % G] = f.y; u[2 % G] = f.z; u[3 % G] = f.w;
+      const float4 e = *reinterpret_cast<const float4*>(hp);
+      h[0] = e.x; h[1 % G] = e.y; h[2 % G] = e.z; h[3 % G] = e.w;
+    } else {
+#pragma unroll
+      for (int x = 0; x < G; ++x) { u[x] = up[x]; h[x] = hp[x]; }
+    }
+  };
+  float ub[G], hw[G], nub[G], nhw[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) { ub[h] = hw[h] = nub[h] = nhw[h] = 0.f; }
+  load_key(kbase + tid, ub, hw);
   for (int tile = 0; tile < kTilesPerCta; ++tile) {
   const int64_t key0 = kbase + (int64_t)tile * kTile;
   if (key0 >= P) break;
   const int64_t key = key0 + tid;
   const bool live = key < P;
+  if (tile + 1 < kTilesPerCta) load_key(key + kTile, nub, nhw);
   unsigned cm = 0;
   bool inset = false;
   float t = 0.f;
-  float ub[G];
   if (live) {
     t = perturb_t(gk, key);
     a.t32[(int64_t)bg * a.pcap + key] = t;
-    const float* up = a.ubar + ((int64_t)bg * a.n_max + key) * G;
-    if (G == 4) {
-      const float4 f = *reinterpret_cast<const float4*>(up);
-      ub[0] = f.x; ub[1 % G] = f.y; ub[2 % G] = f.z; ub[3 % G] = f.w;
-    } else {
-#pragma unroll
-      for (int h = 0; h < G; ++h) ub[h] = up[h];
-    }
   }
+  int jmin = 255;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     int jr = -1;
     if (live) {
-      const int jb = bound_level(ub[h], cmax_get(a, bh0 + h, 2), t, neg_r, J);
+      const int jb = bound_level(ub[h], c_b[h], t, neg_r, J);
       const bool cand = jb <= J;
-      const bool inc = ub[h] >= cmax_get(a, bh0 + h, 0);
+      const bool inc = ub[h] >= c_lo[h];
       inset |= inc;
       jr = inc ? 0 : (cand ? jb : J + 1);
-      if (cand) cm |= 1u << h;
+      if (cand) { cm |= 1u << h; jmin = min(jmin, jb); }
     }
-    hist_add_u(s_jr[h], jr, 1u);
+    hist_add_u(s_jr + h * JS, jr, 1u);
     const unsigned cb = __ballot_sync(0xffffffffu, (cm >> h) & 1u);
     if (lane == 0 && cb) atomicAdd(&s_nc[h], (unsigned)__popc(cb));
   }
   float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
+  // estimated levels (a key that is no candidate of a head has no level
+  // up to J for it): the keys of the exact-max set (which carry the heavy
+  // weight) on every tile with weight 1, the others on one tile in four
+  // with weight 4
+  const bool samp = (tile & 3) == 0;
+  if (samp || __any_sync(0xffffffffu, live && inset)) {
+    const int mult = (live && inset) ? 1 : (live && samp ? 4 : 0);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      int jl = J + 1, hl = J + 1;
+      float est = 0.f;
+      if (mult && ((cm >> h) & 1u)) {
+        est = inset ? sp[h] : fsub(ub[h], hw[h]);
+        exact_levels(est, c32[h], t, neg_r, J, jl, hl);
+      }
+      int* cnt = s_cnt + h * J1 * 2;
+      hist_add_i(cnt + 1, jl <= J ? 2 * jl : -1, mult);                  // sampled at jl
+      hist_add_i(cnt, jl < hl ? 2 * jl : -1, mult);                      // light from jl
+      hist_add_i(cnt, (jl < hl && hl <= J) ? 2 * hl : -1, -mult);        // light until hl
+      hist_add_u(s_db + h * J1, hl <= J ? hl : -1,
+                 hl <= J ? (unsigned)mult * __float2uint_rn(__expf(fminf(est - c32[h], 0.f)) * 262144.f) : 0u);
+    }
+  }
   if (live && inset) {
     // scored in the exact-max step: keep the candidate heads' scores
 #pragma unroll
     for (int h = 0; h < G; ++h)
       if (!((cm >> h) & 1u)) sp[h] = -INFINITY;
-  } else if (live && !cm) {
+  } else if (live) {
 #pragma unroll
     for (int h = 0; h < G; ++h) sp[h] = -INFINITY;
   }
   const int slot = warp_append(&s_n, live && !inset && cm);
-  if (slot >= 0) s_list[slot] = make_uint2((unsigned)key, cm);
+  if (slot >= 0) s_list[slot] = make_uint2((unsigned)key, cm | ((unsigned)jmin << 8));
+#pragma unroll
+  for (int h = 0; h < G; ++h) { ub[h] = nub[h]; hw[h] = nhw[h]; }
   }
   __syncthreads();
   if (tid == 0) s_gbase = s_n ? atomicAdd(a.ccnt + bg, s_n) : 0u;
@@ -532,78 +657,18 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   for (unsigned i = tid; i < s_n; i += 256) a.clist[(int64_t)bg * a.pcap + s_gbase + i] = s_list[i];
   for (int i = tid; i < G * (J + 2); i += 256) {
     int h = i / (J + 2), l = i - h * (J + 2);
-    unsigned v = s_jr[h][l];
+    unsigned v = s_jr[h * JS + l];
     if (v) atomicAdd(a.jr_hist + (int64_t)(bh0 + h) * (a.J1 + 1) + l, v);
   }
   if (tid < G && s_nc[tid]) atomicAdd(a.ncand + bh0 + tid, s_nc[tid]);
-}
-
-// ------------------------------------------- value-free level histograms
-
-template <int G>
-__global__ void __launch_bounds__(256) prehist_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
-  pdl_entry();
-  // counts as integers; heavy weights in 2^-18 fixed point (a prediction
-  // input only; at most 2^12 keys of weight <= 1 per CTA), all aggregated
-  // over equal levels within a warp
-  __shared__ int s_cnt[G][kMaxJ + 1][2];            // light count delta, sampled count
-  __shared__ unsigned s_db[G][kMaxJ + 1];
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
-  const int64_t n = seq.n[b];
-  if (n <= kWindow) return;
-  const int64_t P = n - kWindow;
-  const int64_t kbase = (int64_t)blockIdx.x * kTile * kTilesPerCta;
-  if (kbase >= P) return;
-  const int J = seq.J[b];
-  const float neg_r = -(float)a.r;
-  for (int i = tid; i < G * (J + 1); i += 256) {
-    const int h = i / (J + 1), l = i - h * (J + 1);
-    s_cnt[h][l][0] = 0; s_cnt[h][l][1] = 0; s_db[h][l] = 0u;
-  }
-  __syncthreads();
-  const int bh0 = b * a.Hq + g * G;
-  float c32[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
-  for (int tile = 0; tile < kTilesPerCta; ++tile) {
-  const int64_t key0 = kbase + (int64_t)tile * kTile;
-  if (key0 >= P) break;
-  const int64_t key = key0 + tid;
-  float s[G];
-  float t = 0.f;
-  if (key < P) {
-    const float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
-    if (G == 4) {
-      const float4 f = *reinterpret_cast<const float4*>(sp);
-      s[0] = f.x; s[1 % G] = f.y; s[2 % G] = f.z; s[3 % G] = f.w;
-    } else {
-#pragma unroll
-      for (int h = 0; h < G; ++h) s[h] = sp[h];
-    }
-    t = a.t32[(int64_t)bg * a.pcap + key];
-  } else {
-#pragma unroll
-    for (int h = 0; h < G; ++h) s[h] = -INFINITY;
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    int jl = J + 1, hl = J + 1;
-    if (s[h] > -INFINITY) exact_levels(s[h], c32[h], t, neg_r, J, jl, hl);
-    int* cnt = &s_cnt[h][0][0];
-    hist_add_i(cnt + 1, jl <= J ? 2 * jl : -1, 1);                      // sampled at jl
-    hist_add_i(cnt, jl < hl ? 2 * jl : -1, 1);                          // light from jl
-    hist_add_i(cnt, (jl < hl && hl <= J) ? 2 * hl : -1, -1);            // light until hl
-    hist_add_u(s_db[h], hl <= J ? hl : -1, hl <= J ? __float2uint_rn(__expf(s[h] - c32[h]) * 262144.f) : 0u);
-  }
-  }
-  __syncthreads();
   for (int i = tid; i < G * (J + 1); i += 256) {
     const int h = i / (J + 1), l = i - h * (J + 1);
     float* dst = a.pre_hist + ((int64_t)(bh0 + h) * a.J1 + l) * 4;
-    if (s_cnt[h][l][0]) atomicAdd(dst + 0, (float)s_cnt[h][l][0]);
-    if (s_db[h][l]) atomicAdd(dst + 1, (float)s_db[h][l] * 3.814697265625e-06f);   // 2^-18
-    if (s_cnt[h][l][1]) atomicAdd(dst + 2, (float)s_cnt[h][l][1]);
+    const int c0 = s_cnt[(h * J1 + l) * 2], c1 = s_cnt[(h * J1 + l) * 2 + 1];
+    const unsigned db = s_db[h * J1 + l];
+    if (c0) atomicAdd(dst + 0, (float)c0);
+    if (db) atomicAdd(dst + 1, (float)db * 3.814697265625e-06f);   // 2^-18
+    if (c1) atomicAdd(dst + 2, (float)c1);
   }
 }
 
@@ -814,25 +879,34 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
   uint2* bk = a.buckets + (int64_t)bg * a.J1 * a.pcap;
   const float* sb = a.s32 + (int64_t)bg * a.pcap * G;
   const float* tb = a.t32 + (int64_t)bg * a.pcap;
+  // scores and t of a key, loaded one 256-key step ahead
+  auto load_key = [&](int64_t k, float (&sv)[G], float& t) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) sv[h] = -INFINITY;
+    t = 0.f;
+    if (k >= kend) return;
+    if (G == 4) {
+      const float4 f = *reinterpret_cast<const float4*>(sb + k * G);
+      sv[0] = f.x; sv[1 % G] = f.y; sv[2 % G] = f.z; sv[3 % G] = f.w;
+    } else {
+#pragma unroll
+      for (int h = 0; h < G; ++h) sv[h] = sb[k * G + h];
+    }
+    t = tb[k];
+  };
+  float cs[G], ns[G], ct, nt;
+  load_key(k0 + threadIdx.x, cs, ct);
   for (int64_t key0 = k0; key0 < kend; key0 += 256) {
     const int64_t key = key0 + threadIdx.x;
+    load_key(key + 256, ns, nt);
     int jl[G], hl[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) { jl[h] = J + 1; hl[h] = J + 1; }
-    if (key < kend) {
-      float sv[G];
-      if (G == 4) {
-        const float4 f = *reinterpret_cast<const float4*>(sb + key * G);
-        sv[0] = f.x; sv[1 % G] = f.y; sv[2 % G] = f.z; sv[3 % G] = f.w;
-      } else {
-#pragma unroll
-        for (int h = 0; h < G; ++h) sv[h] = sb[key * G + h];
-      }
-      const float t = tb[key];
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-        if (sv[h] > -INFINITY) exact_levels(sv[h], c32[h], t, neg_r, J, jl[h], hl[h]);
+    for (int h = 0; h < G; ++h) {
+      jl[h] = J + 1; hl[h] = J + 1;
+      if (cs[h] > -INFINITY) exact_levels(cs[h], c32[h], ct, neg_r, J, jl[h], hl[h]);
+      cs[h] = ns[h];
     }
+    ct = nt;
     if (wlo == whi) {
       // a one-level round (the common case for flat groups): at most one
       // event per key, slots by a ballot and one atomic per warp
@@ -1796,22 +1870,32 @@ __global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __g
   }
 
 template <int D, int G, typename E, int MODE>
-void launch_rows_t(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
-  constexpr int smem = rows_smem<D, G, E>();
-  static bool set = false;
-  if (!set) {
+void launch_rows_t(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int round) {
+  const int smem = rows_smem<D, G, E>();
+  static int set = 0;
+  if (smem > set) {
     cudaFuncSetAttribute(rows_kernel<D, G, E, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    set = true;
+    set = smem;
   }
-  launch_pdl(rows_kernel<D, G, E, MODE>, grid, dim3(256), smem, st, a, seq);
+  launch_pdl(rows_kernel<D, G, E, MODE>, grid, dim3(256), smem, st, a, seq, round);
 }
 template <int D, int G, typename E>
 void launch_rows0(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
-  launch_rows_t<D, G, E, 0>(grid, st, a, seq);
+  launch_rows_t<D, G, E, 0>(grid, st, a, seq, 0);
 }
 template <int D, int G, typename E>
-void launch_rows1(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
-  launch_rows_t<D, G, E, 1>(grid, st, a, seq);
+void launch_rows1(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int round) {
+  launch_rows_t<D, G, E, 1>(grid, st, a, seq, round);
+}
+template <int G>
+void launch_cand_t(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
+  const int smem = cand_smem(G, a.J1);
+  static int set = 0;
+  if (smem > set) {
+    cudaFuncSetAttribute(cand_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    set = smem;
+  }
+  launch_pdl(cand_kernel<G>, grid, dim3(256), smem, st, a, seq);
 }
 template <int D, int G, typename E>
 void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int nent,
@@ -1858,15 +1942,17 @@ cudaError_t launch_cstar(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
   CSA_DG_SWITCH(launch_rows0, (rows_grid(a, nmax_live, nsm), st, a, seq))
   return cudaGetLastError();
 }
-cudaError_t launch_rescore(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16,
-                           int64_t pmax_live, int nsm, cudaStream_t st, void (*mark)(int, cudaStream_t)) {
+cudaError_t launch_candidates(const SparseArgs& a, const SeqArgs& seq, int G, int64_t pmax_live,
+                              cudaStream_t st) {
   const int64_t span = (int64_t)kTile * kTilesPerCta;
   dim3 grid((unsigned)((pmax_live + span - 1) / span), (unsigned)(a.B * a.Hkv));
-  CSA_G_SWITCH(cand_kernel, grid, dim3(256), 0, st, a, seq)
-  if (mark) mark(3, st);
-  CSA_DG_SWITCH(launch_rows1, (rows_grid(a, pmax_live, nsm), st, a, seq))
-  if (mark) mark(4, st);
-  CSA_G_SWITCH(prehist_kernel, grid, dim3(256), 0, st, a, seq)
+  switch (G) {
+    case 1: launch_cand_t<1>(grid, st, a, seq); break;
+    case 2: launch_cand_t<2>(grid, st, a, seq); break;
+    case 4: launch_cand_t<4>(grid, st, a, seq); break;
+    case 8: launch_cand_t<8>(grid, st, a, seq); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 cudaError_t launch_predict(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, cudaStream_t st) {
@@ -1884,6 +1970,8 @@ cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
   if (nct > items) nct = items;
   if (nct < 1) nct = 1;
   dim3 grid((unsigned)nct);
+  CSA_DG_SWITCH(launch_rows1, (rows_grid(a, pmax_live, nsm), st, a, seq, round))
+  if (mark) mark(4, st);
   CSA_G_SWITCH(levels_kernel, grid, dim3(256), 0, st, a, seq, round, tpg)
   if (mark) mark(6, st);
   const int nent = a.B * a.Hkv * a.J1;

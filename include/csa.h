@@ -225,10 +225,10 @@ csa_status csa_workspace_layout(const csa_shape* shape,
  * since the previous read (then resets).  Up to 64 steps are buffered;
  * older ones are dropped.  `launches` counts the library's kernel launches
  * (profiling on or off) since the previous read.  Not thread-safe.
- * Phases: 0 workspace clear, 1 scan, 2 exact max, 3 candidates,
- * 4 rescoring of candidate K rows, 5 predictor + window, 6 level buckets,
- * 7 gather plan, 8 V gather, 9 certificate, 10 exact fallback,
- * 11 diagnostics, 12 value-free level histograms. */
+ * Phases: 0 workspace clear, 1 scan, 2 exact max, 3 candidates (with the
+ * value-free level histograms), 4 rescoring of candidate K rows (per
+ * round), 5 predictor + window, 6 level buckets, 7 gather plan, 8 V gather,
+ * 9 certificate, 10 exact fallback, 11 diagnostics, 12 reserved (0). */
 #define CSA_NPHASE 13
 typedef struct {
   float ms[CSA_NPHASE];

@@ -156,17 +156,27 @@ def compare_group(run, w, K, V, q, b, g, res, p, report):
         assert np.array_equal(ub[b, g, :n, h], det["ubar"]), (b, g, h)
         assert cm[b, hq, 0] == det["c_lo"] and cm[b, hq, 1] == det["c_hi"]
         assert cm[b, hq, 2] == det["cb"]
-        cand_g = np.isfinite(s32[b, g, :P, h])
-        assert np.array_equal(cand_g, det["cand"]), (b, g, h)
+        # candidates are rescored by bound-level range, round by round:
+        # every candidate with jbar up to the stop level has its score, no
+        # key outside the candidates has one, and a candidate left unscored
+        # has its exact level beyond the stop (jl >= jbar)
+        cand = det["cand"]
+        lv = min(int(lvl_g[b, hq]), J)
+        scored = np.isfinite(s32[b, g, :P, h])
+        assert not np.any(scored & ~cand), (b, g, h)
+        assert np.all(scored[cand & (det["jbar"] <= lv)]), (b, g, h)
+        pend = cand & ~scored
+        assert np.all(det["jl_c"][pend] > lv), (b, g, h)
         assert stats[b, hq, 3] == res.n_candidates[h]
         # memberships: device float32 vs oracle float64
         c32 = cm[b, hq, 3]
         jg, hg = gpu_levels(s32[b, g, :P, h], c32, t, p.r, J)
-        # levels beyond the grid are all "never" (J + 1)
-        jo = np.minimum(det["jl_c"], J + 1)
-        ho = np.minimum(det["hl_c"], J + 1)
-        jg = np.where(cand_g, jg, J + 1)
-        hg = np.where(cand_g, hg, J + 1)
+        # levels beyond the grid are all "never" (J + 1); so are the levels
+        # of candidates not rescored (they lie beyond the stop level)
+        jo = np.where(pend, J + 1, np.minimum(det["jl_c"], J + 1))
+        ho = np.where(pend, J + 1, np.minimum(det["hl_c"], J + 1))
+        jg = np.where(scored, jg, J + 1)
+        hg = np.where(scored, hg, J + 1)
         sp = det["s"][:P] - det["c_star"]
         xs = sp + t.astype(np.float64) * math.log(2.0)
         for gl, ol, val in ((jg, jo, xs), (hg, ho, sp)):

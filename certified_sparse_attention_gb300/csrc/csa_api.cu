@@ -331,7 +331,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   if (plive > 0) {
     if (launch_cstar(a, seq, shape->d, G, bf16, nlive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
     prof_mark(2, st);
-    if (launch_candidates(a, seq, G, plive, st) != cudaSuccess) return CSA_ERR_CUDA;
+    if (launch_candidates(a, seq, G, plive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
     prof_mark(3, st);
     count_launches(3);
   }

@@ -32,7 +32,7 @@ struct SparseArgs {
   unsigned* cmax;         // [B*Hq][4]            c_lo, c_hi, cb, c32 (ordered)
   unsigned* jr_hist;      // [B*Hq][J1+1]         first level a key's K row is needed
   unsigned* ncand;        // [B*Hq]
-  float* pre_hist;        // [B*Hq][J1][4]        d k, d D_B, d sampled (value free, estimated)
+  float* pre_hist;        // [B*Hq][J1][4]        d k, d D_B (value free, estimated); 2 unused
   float* acc;             // [B*Hq][J1][ACC]      d S1[D], d N_B[D], d k, d S2, d D_B, d H_B, d sampled
   float* winstats;        // [B*Hq][D+4]          N_R[D], D_R, H_R
   float* vmaxp;           // [B*Hkv]              max vmax over pool blocks
@@ -101,7 +101,7 @@ cudaError_t launch_scan(const ScanArgs&, const SeqArgs&, int B, int d, int G, bo
                         cudaStream_t);
 cudaError_t launch_cstar(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t nmax_live,
                          int nsm, cudaStream_t);
-cudaError_t launch_candidates(const SparseArgs&, const SeqArgs&, int G, int64_t pmax_live, cudaStream_t);
+cudaError_t launch_candidates(const SparseArgs&, const SeqArgs&, int G, int64_t pmax_live, int nsm, cudaStream_t);
 cudaError_t launch_predict(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, cudaStream_t);
 typedef void (*PhaseMark)(int phase, cudaStream_t);
 cudaError_t launch_round(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t pmax_live,

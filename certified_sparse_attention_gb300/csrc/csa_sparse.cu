@@ -218,47 +218,74 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const unsigned (&a
 
 // ------------------------------------------------------- exact-max set
 
-constexpr int kCsetTiles = 16;   // 256-key tiles per CTA of the exact-max set pass
+constexpr int kCsetTiles = 16;   // 256-key tiles staged between list flushes
 
+// A CTA covers `span` keys (a multiple of 256) of one group; grids are
+// sized to the resident CTA count so the pass runs in one wave.
 template <int G>
-__global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+__global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+                                                   int span) {
   pdl_entry();
-  // a CTA covers kCsetTiles tiles of 256 keys; its members are staged in
-  // shared memory and take one slot range of the group's list (a per-warp
-  // reservation on the group's counter serialises)
+  // members are staged in shared memory and take one slot range of the
+  // group's list per 16 tiles (a per-warp reservation on the group's
+  // counter serialises)
   __shared__ uint2 s_list[256 * kCsetTiles];
   __shared__ unsigned s_n, s_gbase;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
   const int64_t P = n - kWindow;
-  const int64_t k0 = (int64_t)blockIdx.x * 256 * kCsetTiles;
+  const int64_t k0 = (int64_t)blockIdx.x * span;
   if (k0 >= n) return;
+  const int64_t kstop = min(n, k0 + span);
   const int bh0 = b * a.Hq + g * G;
   float clo[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) clo[h] = cmax_get(a, bh0 + h, 0);
   if (threadIdx.x == 0) s_n = 0u;
   __syncthreads();
-  for (int t = 0; t < kCsetTiles; ++t) {
-    const int64_t key = k0 + (int64_t)t * 256 + threadIdx.x;
+  auto load = [&](int64_t key, float (&u)[G]) {
+    if (key >= P) return;
+    const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
+    if (G == 4) {
+      const float4 f = *reinterpret_cast<const float4*>(ub);
+      u[0] = f.x; u[1 % G] = f.y; u[2 % G] = f.z; u[3 % G] = f.w;
+    } else {
+#pragma unroll
+      for (int h = 0; h < G; ++h) u[h] = ub[h];
+    }
+  };
+  float cu[G], nu[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) { cu[h] = nu[h] = -INFINITY; }
+  load(k0 + threadIdx.x, cu);
+  int t = 0;
+  for (int64_t kt = k0; kt < kstop; kt += 256, ++t) {
+    const int64_t key = kt + threadIdx.x;
+    if (kt + 256 < kstop) load(key + 256, nu);
     unsigned qm = 0;
-    if (key < n) {
+    if (key < kstop) {
       if (key >= P) qm = (1u << G) - 1u;
       else {
-        const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
 #pragma unroll
         for (int h = 0; h < G; ++h)
-          if (ub[h] >= clo[h]) qm |= 1u << h;
+          if (cu[h] >= clo[h]) qm |= 1u << h;
       }
     }
+#pragma unroll
+    for (int h = 0; h < G; ++h) cu[h] = nu[h];
     const int slot = warp_append(&s_n, qm != 0);
     if (slot >= 0) s_list[slot] = make_uint2((unsigned)key, qm);
+    if ((t + 1) % kCsetTiles == 0 || kt + 256 >= kstop) {
+      __syncthreads();
+      if (threadIdx.x == 0) s_gbase = s_n ? atomicAdd(a.xcnt + bg, s_n) : 0u;
+      __syncthreads();
+      for (unsigned i = threadIdx.x; i < s_n; i += 256) a.xlist[(int64_t)bg * a.n_max + s_gbase + i] = s_list[i];
+      __syncthreads();
+      if (threadIdx.x == 0) s_n = 0u;
+      __syncthreads();
+    }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) s_gbase = s_n ? atomicAdd(a.xcnt + bg, s_n) : 0u;
-  __syncthreads();
-  for (unsigned i = threadIdx.x; i < s_n; i += 256) a.xlist[(int64_t)bg * a.n_max + s_gbase + i] = s_list[i];
 }
 
 // ------------------------------------------------------ ring row scoring
@@ -513,7 +540,18 @@ constexpr int kTilesPerCta = kCandSeg / kTile;   // key tiles per CTA of the per
 // Dynamic shared memory of the candidate pass: the staged list, then per
 // head the bound-level histogram and the estimated-level histograms.
 constexpr int cand_smem(int G, int J1) {
-  return kTile * kTilesPerCta * 8 + G * (J1 + 1) * 4 + G * J1 * 2 * 4 + G * J1 * 4;
+  return kTile * kTilesPerCta * 8 + G * J1 * 8 + G * (J1 + 1) * 4 + G * J1 * 4;
+}
+
+// Aggregated shared-memory add of a packed (count << 40) + weight pair.
+__device__ __forceinline__ void hist_add_cw(unsigned long long* base, int v, unsigned cnt, unsigned wgt) {
+  const int v0 = __shfl_sync(0xffffffffu, v, 0);
+  if (__all_sync(0xffffffffu, v == v0)) {
+    const unsigned c = __reduce_add_sync(0xffffffffu, cnt), w = __reduce_add_sync(0xffffffffu, wgt);
+    if ((threadIdx.x & 31) == 0 && v0 >= 0 && (c | w)) atomicAdd(base + v0, ((unsigned long long)c << 40) + w);
+  } else if (v >= 0 && (cnt | wgt)) {
+    atomicAdd(base + v, ((unsigned long long)cnt << 40) + wgt);
+  }
 }
 
 // One pass over the pool keys of a group (after the exact maximum):
@@ -525,20 +563,23 @@ constexpr int cand_smem(int G, int J1) {
 //    score is written when it is rescored, and until then it has no event;
 //  * value-free level histograms from an estimated score (exact for the
 //    exact-max set, ubar minus the block's half width otherwise; the other
-//    keys subsampled one tile in four): counts of light entries and exits,
-//    sampled entries and fixed-point heavy weights per level.  They only
-//    size the first gather round.
+//    keys subsampled one tile in four): counts of light entries and exits
+//    and fixed-point heavy weights per level.  They only size the first
+//    gather round.
 template <int G>
-__global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+__global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+                                                   int span) {
   pdl_entry();
   extern __shared__ __align__(16) uint8_t dsm[];
   const int J1 = a.J1, JS = a.J1 + 1;
   // the CTA's candidates, staged here and written out with one global slot
   // reservation (a per-warp reservation on the group's counter serialises)
   uint2* s_list = reinterpret_cast<uint2*>(dsm);
-  unsigned* s_jr = reinterpret_cast<unsigned*>(dsm + kTile * kTilesPerCta * 8);   // [G][JS]
-  int* s_cnt = reinterpret_cast<int*>(s_jr + G * JS);                              // [G][J1][2]
-  unsigned* s_db = reinterpret_cast<unsigned*>(s_cnt + G * J1 * 2);                // [G][J1]
+  // estimated levels: light exits and heavy weights at hl, packed
+  // (exits << 40) + weight in 2^-18 fixed point; light entries at jl
+  unsigned long long* s_hv = reinterpret_cast<unsigned long long*>(dsm + kTile * kTilesPerCta * 8);  // [G][J1]
+  unsigned* s_jr = reinterpret_cast<unsigned*>(s_hv + G * J1);                     // [G][JS]
+  int* s_cnt = reinterpret_cast<int*>(s_jr + G * JS);                              // [G][J1]
   __shared__ unsigned s_nc[G];
   __shared__ unsigned s_n, s_gbase;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -546,13 +587,13 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
   const int64_t P = n - kWindow;
-  const int64_t kbase = (int64_t)blockIdx.x * kTile * kTilesPerCta;
+  const int64_t kbase = (int64_t)blockIdx.x * span;
   if (kbase >= P) return;
+  const int64_t kstop = min(P, kbase + span);
   const int J = seq.J[b];
   const float neg_r = -(float)a.r;
   for (int i = tid; i < G * JS; i += 256) s_jr[i] = 0u;
-  for (int i = tid; i < G * J1 * 2; i += 256) s_cnt[i] = 0;
-  for (int i = tid; i < G * J1; i += 256) s_db[i] = 0u;
+  for (int i = tid; i < G * J1; i += 256) { s_cnt[i] = 0; s_hv[i] = 0ull; }
   if (tid < G) s_nc[tid] = 0u;
   if (tid == 0) s_n = 0u;
   __syncthreads();
@@ -565,6 +606,7 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
     c32[h] = cmax_get(a, bh0 + h, 3);
   }
   const unsigned long long gk = group_key(seq.seed[b], g);
+  const bool inset_all = (int64_t)a.xcnt[bg] * 32 <= P;
   // ubar and the block half widths of a key, loaded one tile ahead
   auto load_key = [&](int64_t k, float (&u)[G], float (&h)[G]) {
     if (k >= P) return;
@@ -584,12 +626,11 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
 #pragma unroll
   for (int h = 0; h < G; ++h) { ub[h] = hw[h] = nub[h] = nhw[h] = 0.f; }
   load_key(kbase + tid, ub, hw);
-  for (int tile = 0; tile < kTilesPerCta; ++tile) {
-  const int64_t key0 = kbase + (int64_t)tile * kTile;
-  if (key0 >= P) break;
+  int tile = 0;
+  for (int64_t key0 = kbase; key0 < kstop; key0 += kTile, ++tile) {
   const int64_t key = key0 + tid;
-  const bool live = key < P;
-  if (tile + 1 < kTilesPerCta) load_key(key + kTile, nub, nhw);
+  const bool live = key < kstop;
+  if (key0 + kTile < kstop) load_key(key + kTile, nub, nhw);
   unsigned cm = 0;
   bool inset = false;
   float t = 0.f;
@@ -615,12 +656,12 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   }
   float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
   // estimated levels (a key that is no candidate of a head has no level
-  // up to J for it): the keys of the exact-max set (which carry the heavy
-  // weight) on every tile with weight 1, the others on one tile in four
-  // with weight 4
+  // up to J for it): one tile in four with weight 4; when the exact-max
+  // set is small (it then holds the few keys that carry the heavy weight)
+  // its keys on every tile with weight 1
   const bool samp = (tile & 3) == 0;
-  if (samp || __any_sync(0xffffffffu, live && inset)) {
-    const int mult = (live && inset) ? 1 : (live && samp ? 4 : 0);
+  if (samp || (inset_all && __any_sync(0xffffffffu, live && inset))) {
+    const unsigned mult = (live && inset && inset_all) ? 1u : (live && samp ? 4u : 0u);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       int jl = J + 1, hl = J + 1;
@@ -629,12 +670,9 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
         est = inset ? sp[h] : fsub(ub[h], hw[h]);
         exact_levels(est, c32[h], t, neg_r, J, jl, hl);
       }
-      int* cnt = s_cnt + h * J1 * 2;
-      hist_add_i(cnt + 1, jl <= J ? 2 * jl : -1, mult);                  // sampled at jl
-      hist_add_i(cnt, jl < hl ? 2 * jl : -1, mult);                      // light from jl
-      hist_add_i(cnt, (jl < hl && hl <= J) ? 2 * hl : -1, -mult);        // light until hl
-      hist_add_u(s_db + h * J1, hl <= J ? hl : -1,
-                 hl <= J ? (unsigned)mult * __float2uint_rn(__expf(fminf(est - c32[h], 0.f)) * 262144.f) : 0u);
+      hist_add_i(s_cnt + h * J1, jl < hl ? jl : -1, (int)mult);                     // light from jl
+      hist_add_cw(s_hv + h * J1, hl <= J ? hl : -1, jl < hl ? mult : 0u,             // light until hl,
+                  mult * __float2uint_rn(__expf(fminf(est - c32[h], 0.f)) * 262144.f));   // heavy from hl
     }
   }
   if (live && inset) {
@@ -650,11 +688,17 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   if (slot >= 0) s_list[slot] = make_uint2((unsigned)key, cm | ((unsigned)jmin << 8));
 #pragma unroll
   for (int h = 0; h < G; ++h) { ub[h] = nub[h]; hw[h] = nhw[h]; }
+  if ((tile + 1) % kTilesPerCta == 0 || key0 + kTile >= kstop) {
+    __syncthreads();
+    if (tid == 0) s_gbase = s_n ? atomicAdd(a.ccnt + bg, s_n) : 0u;
+    __syncthreads();
+    for (unsigned i = tid; i < s_n; i += 256) a.clist[(int64_t)bg * a.pcap + s_gbase + i] = s_list[i];
+    __syncthreads();
+    if (tid == 0) s_n = 0u;
+    __syncthreads();
+  }
   }
   __syncthreads();
-  if (tid == 0) s_gbase = s_n ? atomicAdd(a.ccnt + bg, s_n) : 0u;
-  __syncthreads();
-  for (unsigned i = tid; i < s_n; i += 256) a.clist[(int64_t)bg * a.pcap + s_gbase + i] = s_list[i];
   for (int i = tid; i < G * (J + 2); i += 256) {
     int h = i / (J + 2), l = i - h * (J + 2);
     unsigned v = s_jr[h * JS + l];
@@ -664,11 +708,11 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   for (int i = tid; i < G * (J + 1); i += 256) {
     const int h = i / (J + 1), l = i - h * (J + 1);
     float* dst = a.pre_hist + ((int64_t)(bh0 + h) * a.J1 + l) * 4;
-    const int c0 = s_cnt[(h * J1 + l) * 2], c1 = s_cnt[(h * J1 + l) * 2 + 1];
-    const unsigned db = s_db[h * J1 + l];
-    if (c0) atomicAdd(dst + 0, (float)c0);
+    const unsigned long long hv = s_hv[h * J1 + l];
+    const int dk = s_cnt[h * J1 + l] - (int)(hv >> 40);
+    const unsigned long long db = hv & ((1ull << 40) - 1ull);
+    if (dk) atomicAdd(dst + 0, (float)dk);
     if (db) atomicAdd(dst + 1, (float)db * 3.814697265625e-06f);   // 2^-18
-    if (c1) atomicAdd(dst + 2, (float)c1);
   }
 }
 
@@ -1869,33 +1913,53 @@ __global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __g
     default: return cudaErrorInvalidValue;                                                       \
   }
 
+// CTAs per (b, g) group: `target` CTAs shared out over the groups (at
+// least 1, at most `cap`)
+static int per_group(const SparseArgs& a, int64_t target, int64_t cap) {
+  int64_t per = (target + a.B * a.Hkv - 1) / (a.B * a.Hkv);
+  if (per > cap) per = cap;
+  return per < 1 ? 1 : (int)per;
+}
+
 template <int D, int G, typename E, int MODE>
-void launch_rows_t(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int round) {
-  const int smem = rows_smem<D, G, E>();
-  static int set = 0;
-  if (smem > set) {
+void launch_rows_t(int64_t items, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int round) {
+  constexpr int smem = rows_smem<D, G, E>();
+  static bool set = false;
+  if (!set) {
     cudaFuncSetAttribute(rows_kernel<D, G, E, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    set = smem;
+    set = true;
   }
-  launch_pdl(rows_kernel<D, G, E, MODE>, grid, dim3(256), smem, st, a, seq, round);
+  // four CTAs per SM over all groups: more, shorter shares than one wave
+  // holds balance the uneven density of wanted entries better
+  const int per = per_group(a, 4 * (int64_t)nsm, (items + 8 * kRingW - 1) / (8 * kRingW));
+  launch_pdl(rows_kernel<D, G, E, MODE>, dim3((unsigned)per, (unsigned)(a.B * a.Hkv)), dim3(256), smem, st, a,
+             seq, round);
 }
 template <int D, int G, typename E>
-void launch_rows0(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
-  launch_rows_t<D, G, E, 0>(grid, st, a, seq, 0);
+void launch_rows0(int64_t items, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
+  launch_rows_t<D, G, E, 0>(items, nsm, st, a, seq, 0);
 }
 template <int D, int G, typename E>
-void launch_rows1(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int round) {
-  launch_rows_t<D, G, E, 1>(grid, st, a, seq, round);
+void launch_rows1(int64_t items, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int round) {
+  launch_rows_t<D, G, E, 1>(items, nsm, st, a, seq, round);
 }
 template <int G>
-void launch_cand_t(dim3 grid, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
+void launch_cand_t(int64_t pmax, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
   const int smem = cand_smem(G, a.J1);
   static int set = 0;
   if (smem > set) {
     cudaFuncSetAttribute(cand_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     set = smem;
   }
-  launch_pdl(cand_kernel<G>, grid, dim3(256), smem, st, a, seq);
+  const int64_t span = (int64_t)kTile * kTilesPerCta;
+  dim3 grid((unsigned)((pmax + span - 1) / span), (unsigned)(a.B * a.Hkv));
+  launch_pdl(cand_kernel<G>, grid, dim3(256), smem, st, a, seq, (int)span);
+}
+template <int G>
+void launch_cset_t(int64_t nmax, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
+  const int64_t span = 256 * kCsetTiles;
+  dim3 grid((unsigned)((nmax + span - 1) / span), (unsigned)(a.B * a.Hkv));
+  launch_pdl(cset_kernel<G>, grid, dim3(256), 0, st, a, seq, (int)span);
 }
 template <int D, int G, typename E>
 void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int nent,
@@ -1926,31 +1990,25 @@ void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqAr
   }
 }
 
-static dim3 rows_grid(const SparseArgs& a, int64_t items, int nsm) {
-  int per = (4 * nsm + a.B * a.Hkv - 1) / (a.B * a.Hkv);
-  int cap = (int)((items + 8 * kRingW - 1) / (8 * kRingW));
-  per = per < 1 ? 1 : (per > cap ? cap : per);
-  if (per < 1) per = 1;
-  return dim3((unsigned)per, (unsigned)(a.B * a.Hkv));
-}
-
 cudaError_t launch_cstar(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t nmax_live,
                          int nsm, cudaStream_t st) {
-  const int64_t span = 256 * kCsetTiles;
-  dim3 grid((unsigned)((nmax_live + span - 1) / span), (unsigned)(a.B * a.Hkv));
-  CSA_G_SWITCH(cset_kernel, grid, dim3(256), 0, st, a, seq)
-  CSA_DG_SWITCH(launch_rows0, (rows_grid(a, nmax_live, nsm), st, a, seq))
+  switch (G) {
+    case 1: launch_cset_t<1>(nmax_live, nsm, st, a, seq); break;
+    case 2: launch_cset_t<2>(nmax_live, nsm, st, a, seq); break;
+    case 4: launch_cset_t<4>(nmax_live, nsm, st, a, seq); break;
+    case 8: launch_cset_t<8>(nmax_live, nsm, st, a, seq); break;
+    default: return cudaErrorInvalidValue;
+  }
+  CSA_DG_SWITCH(launch_rows0, (nmax_live, nsm, st, a, seq))
   return cudaGetLastError();
 }
-cudaError_t launch_candidates(const SparseArgs& a, const SeqArgs& seq, int G, int64_t pmax_live,
+cudaError_t launch_candidates(const SparseArgs& a, const SeqArgs& seq, int G, int64_t pmax_live, int nsm,
                               cudaStream_t st) {
-  const int64_t span = (int64_t)kTile * kTilesPerCta;
-  dim3 grid((unsigned)((pmax_live + span - 1) / span), (unsigned)(a.B * a.Hkv));
   switch (G) {
-    case 1: launch_cand_t<1>(grid, st, a, seq); break;
-    case 2: launch_cand_t<2>(grid, st, a, seq); break;
-    case 4: launch_cand_t<4>(grid, st, a, seq); break;
-    case 8: launch_cand_t<8>(grid, st, a, seq); break;
+    case 1: launch_cand_t<1>(pmax_live, nsm, st, a, seq); break;
+    case 2: launch_cand_t<2>(pmax_live, nsm, st, a, seq); break;
+    case 4: launch_cand_t<4>(pmax_live, nsm, st, a, seq); break;
+    case 8: launch_cand_t<8>(pmax_live, nsm, st, a, seq); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -1970,7 +2028,7 @@ cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
   if (nct > items) nct = items;
   if (nct < 1) nct = 1;
   dim3 grid((unsigned)nct);
-  CSA_DG_SWITCH(launch_rows1, (rows_grid(a, pmax_live, nsm), st, a, seq, round))
+  CSA_DG_SWITCH(launch_rows1, (pmax_live, nsm, st, a, seq, round))
   if (mark) mark(4, st);
   CSA_G_SWITCH(levels_kernel, grid, dim3(256), 0, st, a, seq, round, tpg)
   if (mark) mark(6, st);

@@ -53,8 +53,8 @@ float normal_quantile_two_sided(double delta) {
 struct Layout {
   int J1;
   int64_t pcap, nblk_max;
-  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, front, zero_end;
-  size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, hw, s32, win, t32, clist, xlist, cmap,
+  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, front, rcnt, zero_end;
+  size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, hw, s32, win, t32, clist, rlist, xlist, cmap,
       buckets, dpart, pref, total;
   int64_t nchunk_cap;
 };
@@ -81,6 +81,7 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.nfall = o; o += up(4);
   L.rq = o; o += up(((size_t)BG * 6 + 6) * 4);
   L.front = o; o += up((size_t)4 * BG * 4);
+  L.rcnt = o; o += up((size_t)3 * BG * 4);
   L.zero_end = o;
   L.winstats = o; o += up((size_t)BH * (D + 4) * 4);
   L.vmaxp = o; o += up((size_t)BG * 4);
@@ -94,6 +95,7 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.win = o; o += up((size_t)BG * kWindow * G * 4);
   L.t32 = o; o += up((size_t)BG * L.pcap * 4);
   L.clist = o; o += up((size_t)BG * L.pcap * 8);
+  L.rlist = o; o += up((size_t)BG * L.pcap * 8);
   L.xlist = o; o += up((size_t)BG * s->n_max * 8);
   L.nchunk_cap = (int64_t)BG * L.J1 + (int64_t)BG * L.pcap * 2 * G / 1024 + 16;
   L.cmap = o; o += up((size_t)L.nchunk_cap * 4);
@@ -317,6 +319,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
   a.rq = (unsigned*)(ws + L.rq);
   a.pref = (float*)(ws + L.pref);
   a.hw = (const float*)(ws + L.hw); a.front = (int*)(ws + L.front);
+  a.rlist = (uint2*)(ws + L.rlist); a.rcnt = (unsigned*)(ws + L.rcnt);
   a.xlist = (uint2*)(ws + L.xlist); a.xcnt = (unsigned*)(ws + L.xcnt);
   a.chunk_map = (unsigned*)(ws + L.cmap); a.nchunk_cap = L.nchunk_cap;
   a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);
@@ -342,7 +345,7 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
     if (launch_round(a, seq, shape->d, G, bf16, plive > 0 ? plive : 1, round, nsm, st,
                      g_prof.on ? prof_mark : nullptr) != cudaSuccess)
       return CSA_ERR_CUDA;
-    count_launches(5);
+    count_launches(round > 0 ? 6 : 5);
   }
   // exact attention for heads with no certified level and sequences without a pool
   DenseArgs da;

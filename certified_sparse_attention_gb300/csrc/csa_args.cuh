@@ -44,6 +44,8 @@ struct SparseArgs {
   unsigned* chunk_map;    // [nchunk_cap]         gather work item -> bucket entry
   int64_t nchunk_cap;
   uint2* clist;           // [B*Hkv][pcap]        candidates: key, head mask | min bound level << 8
+  uint2* rlist;           // [B*Hkv][pcap]        a later round's candidates to rescore
+  unsigned* rcnt;         // [3][B*Hkv]
   int* front;             // [4][B*Hkv]           rescored through bound level (+1) before round r
   unsigned* ccnt;         // [B*Hkv]
   unsigned* nfall;        // heads that need the exact fallback

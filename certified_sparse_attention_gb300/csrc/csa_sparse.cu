@@ -14,6 +14,8 @@
 //                   (no values, no K rows: for the stop predictor)
 //   predict_kernel  window sums (D_R, N_R, H_R) and a predicted stop level
 //                   per head that sizes the first gather round
+//   rsel_kernel     (rounds after the first) the candidates a round newly
+//                   needs, compacted
 //   rows_kernel<1>  (per round) float32 scores of the listed candidates
 //                   whose smallest bound level lies in the range that the
 //                   round's levels newly need (jbar_i <= j implies
@@ -333,6 +335,12 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
   if (MODE == 0) {
     list = a.xlist + (int64_t)bg * a.n_max;
     cnt = (int)a.xcnt[bg];
+  } else if (round > 0) {
+    // later rounds: the wanted entries, compacted by rsel_kernel
+    list = a.rlist + (int64_t)bg * a.pcap;
+    cnt = (int)a.rcnt[round * (a.B * a.Hkv) + bg];
+    lnew = 255;
+    if (cnt == 0) return;
   } else {
     list = a.clist + (int64_t)bg * a.pcap;
     cnt = (int)a.ccnt[bg];
@@ -531,6 +539,56 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
       if (y > -INFINITY) atomic_max_f(a.cmax + (int64_t)(bh0 + tid) * 4 + 3, y);
     }
   }
+}
+
+// Rounds after the first: the candidates of the groups still running whose
+// smallest bound level lies in the range the round newly needs, compacted
+// (one list reservation per CTA) so that the rescoring pass reads only
+// those.  Also advances the group's rescored-through level.
+constexpr int kRsel = 4096;      // list entries per CTA
+
+template <int G>
+__global__ void __launch_bounds__(256) rsel_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+                                                   int round) {
+  pdl_entry();
+  __shared__ uint2 s_list[kRsel];
+  __shared__ unsigned s_n, s_gbase;
+  const int tid = threadIdx.x;
+  const int BG = a.B * a.Hkv;
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  if (seq.n[b] <= kWindow) return;
+  const int bh0 = b * a.Hq + g * G;
+  const int lold = a.front[round * BG + bg] - 1;
+  int lnew = -1;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const int* st = a.state + (int64_t)(bh0 + h) * 4;
+    if (!(st[3] & kFlagDone)) lnew = max(lnew, st[1]);
+  }
+  if (blockIdx.x == 0 && tid == 0) a.front[(round + 1) * BG + bg] = max(lold, lnew) + 1;
+  const int cnt = (int)a.ccnt[bg];
+  const int e0 = blockIdx.x * kRsel;
+  if (lnew <= lold || e0 >= cnt) return;
+  if (tid == 0) s_n = 0u;
+  __syncthreads();
+  const uint2* cl = a.clist + (int64_t)bg * a.pcap;
+#pragma unroll 4
+  for (int k = 0; k < kRsel / 256; ++k) {
+    const int i = e0 + k * 256 + tid;
+    uint2 e = make_uint2(0u, 0u);
+    bool keep = false;
+    if (i < cnt) {
+      e = cl[i];
+      const int jm = (int)((e.y >> 8) & 0xFFu);
+      keep = jm > lold && jm <= lnew;
+    }
+    const int slot = warp_append(&s_n, keep);
+    if (slot >= 0) s_list[slot] = e;
+  }
+  __syncthreads();
+  if (tid == 0) s_gbase = s_n ? atomicAdd(a.rcnt + round * BG + bg, s_n) : 0u;
+  __syncthreads();
+  for (unsigned i = tid; i < s_n; i += 256) a.rlist[(int64_t)bg * a.pcap + s_gbase + i] = s_list[i];
 }
 
 // ------------------------------------------------------------- candidates
@@ -822,8 +880,8 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
     const float L = logf(1.0f / de), Lz = logf(2.0f / de);
     const float Rc = Vp + cn;
     // pred: first level the value-free certificate passes; round 1 gathers
-    // up to it (a margin beyond it cost more in gathered values than the
-    // second rounds it saved)
+    // one level past it (the estimate tends to pass a level early; wider
+    // margins cost more in gathered values than the rounds they saved)
     float runk = 0.f, rundb = 0.f;
     int pred = -1;
     for (int l0 = 0; l0 <= J; l0 += 32) {
@@ -881,7 +939,7 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
       if (bal) { pred = l0 + __ffs(bal) - 1; break; }
     }
     if (lane == 0) {
-      const int hi = pred < 0 ? J : pred;
+      const int hi = pred < 0 ? J : min(J, pred + 1);
       int* st = a.state + (int64_t)bh * 4;
       st[0] = -1; st[1] = hi; st[2] = -1; st[3] = 0;
     }
@@ -891,18 +949,20 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
 
 // --------------------------------------------------------- level buckets
 
-constexpr int kLevItem = 2048;   // keys per work item of the level pass
+constexpr int kLevItem = 2048;   // keys per work item of the level pass (first round)
+constexpr int kLevItemLate = 512; // later rounds: few groups, more and shorter items
 
-// One work item: keys [k0, k0 + kLevItem) of group bg.
+// One work item: keys [k0, k0 + isz) of group bg.
 template <int G>
-__device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& seq, int bg, int64_t k0) {
+__device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& seq, int bg, int64_t k0,
+                                            int isz) {
   const int lane = threadIdx.x & 31;
   const int b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
   const int64_t P = n - kWindow;
   if (k0 >= P) return;
-  const int64_t kend = min(P, k0 + kLevItem);
+  const int64_t kend = min(P, k0 + isz);
   const int J = seq.J[b];
   const int bh0 = b * a.Hq + g * G;
   int lo[G], hi[G];
@@ -1020,7 +1080,7 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
 
 template <int G>
 __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
-                                                     int round, unsigned tpg) {
+                                                     int round, unsigned tpg, int isz) {
   pdl_entry();
   __shared__ unsigned s_item;
   const int BG = a.B * a.Hkv;
@@ -1031,7 +1091,7 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
     const unsigned item = s_item;
     __syncthreads();
     if (item >= total) break;
-    levels_item<G>(a, seq, (int)a.rq[round * BG + item / tpg], (int64_t)(item % tpg) * kLevItem);
+    levels_item<G>(a, seq, (int)a.rq[round * BG + item / tpg], (int64_t)(item % tpg) * isz, isz);
   }
 }
 
@@ -2020,17 +2080,22 @@ cudaError_t launch_predict(const SparseArgs& a, const SeqArgs& seq, int d, int G
 }
 cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t pmax_live,
                          int round, int nsm, cudaStream_t st, PhaseMark mark) {
-  // eight 256-thread CTAs per SM pull work items (kLevItem keys of a group
+  // eight 256-thread CTAs per SM pull work items (isz keys of a group
   // listed for this round) from the round's queue
-  const unsigned tpg = (unsigned)((pmax_live + kLevItem - 1) / kLevItem);
+  const int isz = round == 0 ? kLevItem : kLevItemLate;
+  const unsigned tpg = (unsigned)((pmax_live + isz - 1) / isz);
   int64_t nct = 8 * (int64_t)nsm;
   const int64_t items = (int64_t)tpg * a.B * a.Hkv;
   if (nct > items) nct = items;
   if (nct < 1) nct = 1;
   dim3 grid((unsigned)nct);
+  if (round > 0) {
+    dim3 rg((unsigned)((pmax_live + kRsel - 1) / kRsel), (unsigned)(a.B * a.Hkv));
+    CSA_G_SWITCH(rsel_kernel, rg, dim3(256), 0, st, a, seq, round)
+  }
   CSA_DG_SWITCH(launch_rows1, (pmax_live, nsm, st, a, seq, round))
   if (mark) mark(4, st);
-  CSA_G_SWITCH(levels_kernel, grid, dim3(256), 0, st, a, seq, round, tpg)
+  CSA_G_SWITCH(levels_kernel, grid, dim3(256), 0, st, a, seq, round, tpg, isz)
   if (mark) mark(6, st);
   const int nent = a.B * a.Hkv * a.J1;
   CSA_DG_SWITCH(launch_vgather_t, (nsm, st, a, seq, nent, mark))

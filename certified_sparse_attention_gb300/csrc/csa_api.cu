@@ -1,7 +1,9 @@
 // Host side of the C ABI declared in include/csa.h: argument checks, the
 // workspace layout, the exact grid size J = ceil(r log2 |pool|), and the
 // launch sequence of one decode step.  No device memory is allocated here.
+#include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <cstring>
 
 #include "csa_args.cuh"
@@ -36,7 +38,8 @@ csa_status shape_supported(const csa_shape* s) {
 }
 bool params_ok(const csa_params* p) {
   return p && p->eps > 0.f && std::isfinite(p->eps) && p->delta > 0.f && p->delta < 1.f && p->r >= 1 &&
-         p->r <= 4 && p->measure >= 0 && p->measure <= 3 && p->J_override >= -1 && p->J_override <= kMaxJ;
+         p->r <= 4 && p->measure >= 0 && p->measure <= 3 && p->J_override >= -1 && p->J_override <= kMaxJ &&
+         p->sub_batches >= 0 && p->sub_batches <= kMaxSub;
 }
 
 // z with P(|N(0,1)| > z) = delta, i.e. erfc(z / sqrt 2) = delta: bisection
@@ -159,6 +162,166 @@ void prof_mark(int phase, cudaStream_t st) {
 }
 void count_launches(int k) { g_prof.launches += k; }
 
+// ------------------------------------------------------------ sub-batches
+//
+// A batch of B >= 2 sequences runs by default as two sub-batches of
+// consecutive sequences on two library-owned streams: the step is a chain
+// of ~20 dependent launches, several of them latency-bound, and two
+// independent chains fill the GPU better than one.  Each sub-batch has its
+// own workspace region (stride `stride`); they share sub-batch 0's status
+// word.
+
+struct SubPlan {
+  int nsub, Bc;
+  size_t stride, total;
+};
+
+bool sub_plan(const csa_shape* s, const csa_params* p, SubPlan& sp) {
+  Layout whole;
+  if (!make_layout(s, p, whole)) return false;
+  sp.nsub = p->sub_batches == 0 ? (s->B >= 2 ? 2 : 1) : std::min(p->sub_batches, s->B);
+  if (sp.nsub <= 1) {
+    sp.nsub = 1; sp.Bc = s->B; sp.stride = whole.total; sp.total = whole.total;
+    return true;
+  }
+  sp.Bc = (s->B + sp.nsub - 1) / sp.nsub;
+  sp.nsub = (s->B + sp.Bc - 1) / sp.Bc;   // sub-batches that hold a sequence
+  csa_shape sc = *s;
+  sc.B = sp.Bc;
+  Layout part;
+  if (!make_layout(&sc, p, part)) return false;
+  sp.stride = up(part.total);
+  // room for the unsplit layout too (phase timing runs unsplit)
+  sp.total = std::max(sp.stride * sp.nsub, whole.total);
+  return true;
+}
+
+struct SubStreams {
+  cudaStream_t st[kMaxSub];
+  cudaEvent_t fork, join[kMaxSub];
+};
+struct SubState {
+  std::mutex mu;
+  SubStreams* per_dev[64] = {nullptr};
+};
+SubState g_sub;
+
+// the calling thread's device's streams and events, made on first use
+// (callers hold g_sub.mu)
+SubStreams* sub_streams() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!g_sub.per_dev[dev]) {
+    SubStreams* ss = new SubStreams;
+    bool ok = cudaEventCreateWithFlags(&ss->fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; c < kMaxSub && ok; ++c) {
+      ok = cudaStreamCreateWithFlags(&ss->st[c], cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&ss->join[c], cudaEventDisableTiming) == cudaSuccess;
+    }
+    if (!ok) return nullptr;
+    g_sub.per_dev[dev] = ss;
+  }
+  return g_sub.per_dev[dev];
+}
+
+// One (sub-)batch on one stream.  `status` is the device status word (shared
+// by the sub-batches of a split call); `clear` zeroes the per-step counters
+// (a split call clears sub-batch 0's, which hold the status word, before it
+// forks).
+csa_status decode_batch(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
+                        const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
+                        const float* vnorm2, const int64_t* len, const uint64_t* step_seed, float* o,
+                        float* beta, int32_t* level, int32_t* keys_read, csa_head_stats* stats, char* ws,
+                        unsigned* status, bool clear, cudaStream_t st) {
+  Layout L;
+  if (!make_layout(shape, params, L)) return CSA_ERR_INVALID_ARG;
+  const int G = shape->Hq / shape->Hkv;
+  const bool bf16 = shape->dtype == CSA_BF16;
+  SeqArgs seq;
+  std::memset(&seq, 0, sizeof(seq));
+  int64_t nlive = 0;
+  for (int b = 0; b < shape->B; ++b) {
+    if (len[b] < 1 || len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
+    seq.n[b] = len[b];
+    seq.seed[b] = step_seed[b];
+    const int64_t P = len[b] > kWindow ? len[b] - kWindow : 0;
+    seq.J[b] = params->J_override >= 0 ? params->J_override : grid_J(P, params->r);
+    if (len[b] > nlive) nlive = len[b];
+  }
+  const int64_t plive = nlive > kWindow ? nlive - kWindow : 0;
+  const float rs = (float)(1.0 / std::sqrt((double)shape->d));
+
+  prof_step_begin(st);
+  if (clear && cudaMemsetAsync(ws, 0, L.zero_end, st) != cudaSuccess) return CSA_ERR_CUDA;
+  prof_mark(0, st);
+
+  ScanArgs sa;
+  sa.q = q; sa.K4 = K4; sa.bounds = bounds; sa.ubar = (float*)(ws + L.ubar);
+  sa.hw = (float*)(ws + L.hw);
+  sa.cmax = (unsigned*)(ws + L.cmax); sa.status = status;
+  sa.Hq = shape->Hq; sa.Hkv = shape->Hkv; sa.n_max = shape->n_max; sa.nblk_max = L.nblk_max; sa.rs = rs;
+  cudaError_t e = launch_scan(sa, seq, shape->B, shape->d, G, bf16, nlive, st);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+  count_launches(1);
+  prof_mark(1, st);
+
+  SparseArgs a;
+  a.q = q; a.K = K; a.V = V; a.vmax = vmax; a.vnorm2 = vnorm2; a.ubar = (const float*)(ws + L.ubar);
+  a.s32 = (float*)(ws + L.s32); a.win = (float*)(ws + L.win); a.cmax = (unsigned*)(ws + L.cmax);
+  a.jr_hist = (unsigned*)(ws + L.jr_hist); a.ncand = (unsigned*)(ws + L.ncand);
+  a.pre_hist = (float*)(ws + L.pre_hist); a.acc = (float*)(ws + L.acc); a.winstats = (float*)(ws + L.winstats);
+  a.vmaxp = (float*)(ws + L.vmaxp); a.state = (int*)(ws + L.state); a.bcnt = (unsigned*)(ws + L.bcnt);
+  a.bcons = (unsigned*)(ws + L.bcons); a.buckets = (uint2*)(ws + L.buckets);
+  a.t32 = (float*)(ws + L.t32); a.clist = (uint2*)(ws + L.clist); a.ccnt = (unsigned*)(ws + L.ccnt);
+  a.nfall = (unsigned*)(ws + L.nfall);
+  a.rq = (unsigned*)(ws + L.rq);
+  a.pref = (float*)(ws + L.pref);
+  a.hw = (const float*)(ws + L.hw); a.front = (int*)(ws + L.front);
+  a.rlist = (uint2*)(ws + L.rlist); a.rcnt = (unsigned*)(ws + L.rcnt);
+  a.xlist = (uint2*)(ws + L.xlist); a.xcnt = (unsigned*)(ws + L.xcnt);
+  a.chunk_map = (unsigned*)(ws + L.cmap); a.nchunk_cap = L.nchunk_cap;
+  a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);
+  a.plan_off = (unsigned*)(ws + L.plan_off); a.status = status;
+  a.o = o; a.beta = beta; a.level = level; a.keys_read = keys_read; a.stats = stats;
+  a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max; a.nblk_max = L.nblk_max;
+  a.pcap = L.pcap; a.J1 = L.J1; a.r = params->r; a.eps = params->eps; a.delta = params->delta;
+  a.measure = params->measure; a.rs = rs;
+  a.zclt = normal_quantile_two_sided((double)params->delta);
+
+  const int nsm = sm_count();
+  if (plive > 0) {
+    if (launch_cstar(a, seq, shape->d, G, bf16, nlive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
+    prof_mark(2, st);
+    if (launch_candidates(a, seq, G, plive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
+    prof_mark(3, st);
+    count_launches(3);
+  }
+  if (launch_predict(a, seq, shape->d, G, bf16, st) != cudaSuccess) return CSA_ERR_CUDA;
+  count_launches(1);
+  prof_mark(5, st);
+  for (int round = 0; round < 3; ++round) {
+    if (launch_round(a, seq, shape->d, G, bf16, plive > 0 ? plive : 1, round, nsm, st,
+                     g_prof.on ? prof_mark : nullptr) != cudaSuccess)
+      return CSA_ERR_CUDA;
+    count_launches(round > 0 ? 6 : 5);
+  }
+  // exact attention for heads with no certified level and sequences without a pool
+  DenseArgs da;
+  da.q = q; da.K = K; da.V = V; da.part = (float*)(ws + L.dpart); da.o = o; da.state = a.state;
+  da.nfall = a.nfall;
+  da.B = shape->B; da.Hq = shape->Hq; da.Hkv = shape->Hkv; da.n_max = shape->n_max;
+  da.nsplit = dense_nsplit(shape->n_max); da.rs = rs;
+  if (launch_dense(da, seq, shape->d, G, bf16, nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
+  count_launches(2);
+  prof_mark(10, st);
+  if (stats && plive > 0) {
+    if (launch_near(a, seq, G, plive, st) != cudaSuccess) return CSA_ERR_CUDA;
+    count_launches(1);
+    prof_mark(11, st);
+  }
+  return CSA_OK;
+}
+
 }  // namespace
 
 void add_launches(int k) { count_launches(k); }
@@ -184,9 +347,9 @@ const char* csa_status_string(csa_status s) {
 
 size_t csa_workspace_size(const csa_shape* shape, const csa_params* params) {
   if (!shape_ok(shape) || !params_ok(params) || shape_supported(shape) != CSA_OK) return 0;
-  Layout L;
-  if (!make_layout(shape, params, L)) return 0;
-  return L.total;
+  SubPlan sp;
+  if (!sub_plan(shape, params, sp)) return 0;
+  return sp.total;
 }
 
 size_t csa_dense_workspace_size(const csa_shape* shape) {
@@ -198,16 +361,22 @@ csa_status csa_workspace_layout(const csa_shape* shape, const csa_params* params
   if (!out || !shape_ok(shape) || !params_ok(params)) return CSA_ERR_INVALID_ARG;
   csa_status su = shape_supported(shape);
   if (su != CSA_OK) return su;
+  SubPlan sp;
+  if (!sub_plan(shape, params, sp)) return CSA_ERR_INVALID_ARG;
+  csa_shape s0 = *shape;
+  s0.B = sp.Bc;
   Layout L;
-  if (!make_layout(shape, params, L)) return CSA_ERR_INVALID_ARG;
+  if (!make_layout(&s0, params, L)) return CSA_ERR_INVALID_ARG;
   out->ubar = L.ubar;
   out->cmax = L.cmax;
   out->s32 = L.s32;
   out->jr_hist = L.jr_hist;
   out->bcnt = L.bcons;   // cumulative over the step's rounds
-  out->total = L.total;
+  out->total = sp.total;
   out->J1 = L.J1;
-  out->reserved = 0;
+  out->sub_batches = sp.nsub;
+  out->sub_stride = sp.stride;
+  out->sub_B = sp.Bc;
   return CSA_OK;
 }
 
@@ -272,94 +441,52 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
     return CSA_ERR_INVALID_ARG;
   csa_status su = shape_supported(shape);
   if (su != CSA_OK) return su;
-  Layout L;
-  if (!make_layout(shape, params, L)) return CSA_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace % kAlign)) return CSA_ERR_WORKSPACE;
-  const int G = shape->Hq / shape->Hkv;
-  const bool bf16 = shape->dtype == CSA_BF16;
-  SeqArgs seq;
-  std::memset(&seq, 0, sizeof(seq));
-  int64_t nlive = 0;
-  for (int b = 0; b < shape->B; ++b) {
+  SubPlan sp;
+  if (!sub_plan(shape, params, sp)) return CSA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < sp.total || ((uintptr_t)workspace % kAlign)) return CSA_ERR_WORKSPACE;
+  for (int b = 0; b < shape->B; ++b)
     if (len[b] < 1 || len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
-    seq.n[b] = len[b];
-    seq.seed[b] = step_seed[b];
-    const int64_t P = len[b] > kWindow ? len[b] - kWindow : 0;
-    seq.J[b] = params->J_override >= 0 ? params->J_override : grid_J(P, params->r);
-    if (len[b] > nlive) nlive = len[b];
-  }
-  const int64_t plive = nlive > kWindow ? nlive - kWindow : 0;
   cudaStream_t st = (cudaStream_t)stream;
   char* ws = (char*)workspace;
-  const float rs = (float)(1.0 / std::sqrt((double)shape->d));
-
-  prof_step_begin(st);
-  if (cudaMemsetAsync(ws, 0, L.zero_end, st) != cudaSuccess) return CSA_ERR_CUDA;
-  prof_mark(0, st);
-
-  ScanArgs sa;
-  sa.q = q; sa.K4 = K4; sa.bounds = bounds; sa.ubar = (float*)(ws + L.ubar);
-  sa.hw = (float*)(ws + L.hw);
-  sa.cmax = (unsigned*)(ws + L.cmax); sa.status = (unsigned*)(ws + L.status);
-  sa.Hq = shape->Hq; sa.Hkv = shape->Hkv; sa.n_max = shape->n_max; sa.nblk_max = L.nblk_max; sa.rs = rs;
-  cudaError_t e = launch_scan(sa, seq, shape->B, shape->d, G, bf16, nlive, st);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
-  count_launches(1);
-  prof_mark(1, st);
-
-  SparseArgs a;
-  a.q = q; a.K = K; a.V = V; a.vmax = vmax; a.vnorm2 = vnorm2; a.ubar = (const float*)(ws + L.ubar);
-  a.s32 = (float*)(ws + L.s32); a.win = (float*)(ws + L.win); a.cmax = (unsigned*)(ws + L.cmax);
-  a.jr_hist = (unsigned*)(ws + L.jr_hist); a.ncand = (unsigned*)(ws + L.ncand);
-  a.pre_hist = (float*)(ws + L.pre_hist); a.acc = (float*)(ws + L.acc); a.winstats = (float*)(ws + L.winstats);
-  a.vmaxp = (float*)(ws + L.vmaxp); a.state = (int*)(ws + L.state); a.bcnt = (unsigned*)(ws + L.bcnt);
-  a.bcons = (unsigned*)(ws + L.bcons); a.buckets = (uint2*)(ws + L.buckets);
-  a.t32 = (float*)(ws + L.t32); a.clist = (uint2*)(ws + L.clist); a.ccnt = (unsigned*)(ws + L.ccnt);
-  a.nfall = (unsigned*)(ws + L.nfall);
-  a.rq = (unsigned*)(ws + L.rq);
-  a.pref = (float*)(ws + L.pref);
-  a.hw = (const float*)(ws + L.hw); a.front = (int*)(ws + L.front);
-  a.rlist = (uint2*)(ws + L.rlist); a.rcnt = (unsigned*)(ws + L.rcnt);
-  a.xlist = (uint2*)(ws + L.xlist); a.xcnt = (unsigned*)(ws + L.xcnt);
-  a.chunk_map = (unsigned*)(ws + L.cmap); a.nchunk_cap = L.nchunk_cap;
-  a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);
-  a.plan_off = (unsigned*)(ws + L.plan_off); a.status = (unsigned*)(ws + L.status);
-  a.o = o; a.beta = beta; a.level = level; a.keys_read = keys_read; a.stats = stats;
-  a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max; a.nblk_max = L.nblk_max;
-  a.pcap = L.pcap; a.J1 = L.J1; a.r = params->r; a.eps = params->eps; a.delta = params->delta;
-  a.measure = params->measure; a.rs = rs;
-  a.zclt = normal_quantile_two_sided((double)params->delta);
-
-  const int nsm = sm_count();
-  if (plive > 0) {
-    if (launch_cstar(a, seq, shape->d, G, bf16, nlive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
-    prof_mark(2, st);
-    if (launch_candidates(a, seq, G, plive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
-    prof_mark(3, st);
-    count_launches(3);
+  unsigned* status = (unsigned*)ws;   // offset 0 of (sub-batch 0's) layout
+  if (sp.nsub == 1 || g_prof.on) {
+    // one stream (phase timing runs unsplit so its events bracket whole phases)
+    return decode_batch(shape, params, q, K, V, K4, bounds, vmax, vnorm2, len, step_seed, o, beta, level,
+                        keys_read, stats, ws, status, true, st);
   }
-  if (launch_predict(a, seq, shape->d, G, bf16, st) != cudaSuccess) return CSA_ERR_CUDA;
-  count_launches(1);
-  prof_mark(5, st);
-  for (int round = 0; round < 3; ++round) {
-    if (launch_round(a, seq, shape->d, G, bf16, plive > 0 ? plive : 1, round, nsm, st,
-                     g_prof.on ? prof_mark : nullptr) != cudaSuccess)
-      return CSA_ERR_CUDA;
-    count_launches(round > 0 ? 6 : 5);
+  // sub-batches of consecutive sequences on the library's streams: fork
+  // after clearing sub-batch 0's counters (they hold the status word), join
+  // back onto the caller's stream
+  std::lock_guard<std::mutex> lock(g_sub.mu);
+  SubStreams* ss = sub_streams();
+  if (!ss) return CSA_ERR_CUDA;
+  {
+    csa_shape s0 = *shape;
+    s0.B = sp.Bc;
+    Layout L0;
+    if (!make_layout(&s0, params, L0)) return CSA_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(ws, 0, L0.zero_end, st) != cudaSuccess) return CSA_ERR_CUDA;
   }
-  // exact attention for heads with no certified level and sequences without a pool
-  DenseArgs da;
-  da.q = q; da.K = K; da.V = V; da.part = (float*)(ws + L.dpart); da.o = o; da.state = a.state;
-  da.nfall = a.nfall;
-  da.B = shape->B; da.Hq = shape->Hq; da.Hkv = shape->Hkv; da.n_max = shape->n_max;
-  da.nsplit = dense_nsplit(shape->n_max); da.rs = rs;
-  if (launch_dense(da, seq, shape->d, G, bf16, nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
-  count_launches(2);
-  prof_mark(10, st);
-  if (stats && plive > 0) {
-    if (launch_near(a, seq, G, plive, st) != cudaSuccess) return CSA_ERR_CUDA;
-    count_launches(1);
-    prof_mark(11, st);
+  if (cudaEventRecord(ss->fork, st) != cudaSuccess) return CSA_ERR_CUDA;
+  const size_t esz = shape->dtype == CSA_BF16 ? 2 : 4;
+  const int64_t nblk = (shape->n_max + kBlock - 1) / kBlock;
+  const int64_t Hq = shape->Hq, Hkv = shape->Hkv, D = shape->d, N = shape->n_max;
+  for (int c = 0; c < sp.nsub; ++c) {
+    const int64_t b0 = (int64_t)c * sp.Bc;
+    if (b0 >= shape->B) break;
+    csa_shape sc = *shape;
+    sc.B = (int)std::min<int64_t>(sp.Bc, shape->B - b0);
+    cudaStream_t cs = ss->st[c];
+    if (cudaStreamWaitEvent(cs, ss->fork, 0) != cudaSuccess) return CSA_ERR_CUDA;
+    csa_status r = decode_batch(
+        &sc, params, (const char*)q + b0 * Hq * D * esz, (const char*)K + b0 * Hkv * N * D * esz,
+        (const char*)V + b0 * Hkv * N * D * esz, K4 + b0 * Hkv * nblk * kBlock * (D / 2),
+        bounds + b0 * Hkv * nblk * 2 * D, vmax + b0 * Hkv * nblk, vnorm2 + b0 * Hkv * N, len + b0,
+        step_seed + b0, o + b0 * Hq * D, beta + b0 * Hq, level + b0 * Hq, keys_read + b0 * Hq,
+        stats ? stats + b0 * Hq : nullptr, ws + c * sp.stride, status, c > 0, cs);
+    if (r != CSA_OK) return r;
+    if (cudaEventRecord(ss->join[c], cs) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaStreamWaitEvent(st, ss->join[c], 0) != cudaSuccess) return CSA_ERR_CUDA;
   }
   return CSA_OK;
 }

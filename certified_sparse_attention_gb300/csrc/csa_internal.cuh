@@ -20,6 +20,7 @@ constexpr int kTile = 256;     // keys per scan / candidate tile
 constexpr int kCandSeg = 4096; // pool keys per candidate-list segment (one candidate CTA)
 constexpr int kMaxB = 128;     // sequences per call
 constexpr int kMaxJ = 255;     // last grid level supported
+constexpr int kMaxSub = 4;     // sub-batches of one decode call
 
 // Per-call sequence data passed by value (graph-capturable).
 struct SeqArgs {

@@ -95,6 +95,11 @@ typedef struct {
   int r;          /* grid resolution tau_j = 2^(-j/r), 1..4                  */
   int measure;    /* csa_measure                                             */
   int J_override; /* -1: last level J = ceil(r log2 |pool|); else J (<= 255) */
+  int sub_batches;/* scheduling only, results do not depend on it: 0 = two
+                   * when B >= 2, else one; 1..4 = that many sub-batches of
+                   * consecutive sequences, each an independent chain of
+                   * launches on a library-owned stream, forked from and
+                   * joined back onto the caller's stream                   */
 } csa_params;
 
 /* Optional per-(sequence, query head) diagnostics. */
@@ -209,10 +214,18 @@ csa_status csa_dense_decode_static(const csa_shape* shape, const void* q,
  *            over the step's gather rounds (one per key, level and round at
  *            which the key changes a head's sums; each entry is one
  *            value-row load of the gather)
- *   J1       largest J + 1 (row stride of jr_hist is J1 + 1) */
+ *   J1       largest J + 1 (row stride of jr_hist is J1 + 1)
+ * With sub-batches the arrays above are those of sub-batch 0 (its first
+ * sub_B sequences); sub-batch c's are sub_stride * c bytes further.
+ *   total        workspace bytes (csa_workspace_size)
+ *   sub_batches  sub-batches the step runs as
+ *   sub_stride   bytes between sub-batch regions
+ *   sub_B        sequences per sub-batch (the last may hold fewer) */
 typedef struct {
   size_t ubar, cmax, s32, jr_hist, bcnt, total;
-  int32_t J1, reserved;
+  int32_t J1, sub_batches;
+  size_t sub_stride;
+  int32_t sub_B, reserved;
 } csa_workspace_map;
 
 csa_status csa_workspace_layout(const csa_shape* shape,

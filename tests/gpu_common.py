@@ -36,7 +36,7 @@ class GpuRun:
 
     def __init__(self, w: synth.Workload, K, V, q, lens, seeds, n_alloc,
                  device="cuda:0", eps=None, delta=None, r=None,
-                 measure=0, J_override=-1):
+                 measure=0, J_override=-1, sub_batches=0):
         import torch
         import certified_sparse_attention_gb300 as csa
         self.csa = csa
@@ -47,7 +47,7 @@ class GpuRun:
         self.params = csa.make_params(w.eps if eps is None else eps,
                                       w.delta if delta is None else delta,
                                       w.r if r is None else r, measure,
-                                      J_override)
+                                      J_override, sub_batches)
         Kp = np.zeros((w.B, w.Hkv, n_alloc, w.d), np.float32)
         Vp = np.zeros_like(Kp)
         Kp[:, :, :K.shape[2]] = K
@@ -90,30 +90,39 @@ class GpuRun:
                        "csa_quantize_keys")
         self.lens = lens
 
-    def ws_view(self, off, count, dtype):
+    def ws_view(self, off, per_seq, dtype):
+        """A per-sequence array of the workspace ([B][per_seq] 4-byte
+        words), gathered over the step's sub-batch regions."""
         import torch
-        nbytes = count * 4
-        t = self.step.ws[off:off + nbytes]
-        return t.view(dtype).cpu().numpy()
+        m = self.map
+        parts = []
+        for c in range(m.sub_batches):
+            nb = min(m.sub_B, self.w.B - c * m.sub_B)
+            if nb <= 0:
+                break
+            o = c * m.sub_stride + off
+            t = self.step.ws[o:o + nb * per_seq * 4]
+            parts.append(t.view(dtype).cpu().numpy())
+        return np.concatenate(parts)
 
     def ubar(self):
         import torch
         w = self.w
         n = self.shape.n_max
-        a = self.ws_view(self.map.ubar, w.B * w.Hkv * n * w.G, torch.float32)
+        a = self.ws_view(self.map.ubar, w.Hkv * n * w.G, torch.float32)
         return a.reshape(w.B, w.Hkv, n, w.G)
 
     def cmax(self):
         import torch
         w = self.w
-        a = self.ws_view(self.map.cmax, w.B * w.Hq * 4, torch.int32)
+        a = self.ws_view(self.map.cmax, w.Hq * 4, torch.int32)
         return self.csa.decode_ordered(a.view(np.uint32)).reshape(w.B, w.Hq, 4)
 
     def s32(self):
         import torch
         w = self.w
         pcap = max(self.shape.n_max - 64, 1)
-        a = self.ws_view(self.map.s32, w.B * w.Hkv * pcap * w.G, torch.float32)
+        a = self.ws_view(self.map.s32, w.Hkv * pcap * w.G, torch.float32)
         return a.reshape(w.B, w.Hkv, pcap, w.G)
 
     def outputs(self):

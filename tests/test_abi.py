@@ -40,6 +40,20 @@ def test_workspace_sizes(lib):
     assert m.J1 == 69                   # J = ceil(4 log2 131008) = 68
     assert m.ubar % 256 == 0 and m.s32 % 256 == 0
     assert csa.csa_dense_workspace_size(s) > 0
+    # two sub-batches of two sequences by default; the regions do not
+    # overlap and the unsplit layout fits too
+    assert m.sub_batches == 2 and m.sub_B == 2 and m.sub_stride % 256 == 0
+    one = csa.make_params(0.05, 0.05, 4, sub_batches=1)
+    m1 = csa.csa_workspace_layout(s, one)
+    assert m1.sub_batches == 1 and m1.sub_B == 4
+    assert m.total >= max(2 * m.sub_stride, m1.total)
+    assert m.sub_stride < m1.total
+    # one sequence: nothing to split; an uneven split rounds up
+    s1 = csa.make_shape(1, 32, 8, 128, 4096, "bf16")
+    assert csa.csa_workspace_layout(s1, p).sub_batches == 1
+    s3 = csa.make_shape(3, 32, 8, 128, 4096, "bf16")
+    m3 = csa.csa_workspace_layout(s3, csa.make_params(sub_batches=3))
+    assert m3.sub_batches == 3 and m3.sub_B == 1
 
 
 @pytest.mark.parametrize("bad", [
@@ -53,7 +67,8 @@ def test_unsupported_shapes(lib, bad):
 
 @pytest.mark.parametrize("pk", [dict(eps=0.0), dict(delta=1.0),
                                 dict(delta=0.0), dict(r=0), dict(r=5),
-                                dict(measure=4), dict(J_override=300)])
+                                dict(measure=4), dict(J_override=300),
+                                dict(sub_batches=5), dict(sub_batches=-1)])
 def test_invalid_params(lib, pk):
     s = csa.make_shape(1, 8, 2, 128, 4096, "bf16")
     kw = dict(eps=0.05, delta=0.05, r=2)

@@ -137,6 +137,19 @@ def test_decode_batch_mixed_lengths():
         assert beta_g[2, hq] == 0 and lvl_g[2, hq] == 0 and kr_g[2, hq] == 50
 
 
+@pytest.mark.parametrize("sub,runs", [(1, 1), (3, 2), (4, 4)])
+def test_decode_sub_batches(sub, runs):
+    # the batch unsplit, asked for 3 sub-batches (two of two sequences) and
+    # as 4 sub-batches on the library's streams: every group against the
+    # oracle
+    w, K, V, q = _case("llama16k", 1500, B=4, Hq=8, Hkv=2)
+    lens = [1500, 1333, 901, 1500]
+    seeds = synth.step_seeds(w, 8)
+    run, rep = run_and_compare(w, K, V, q, lens, seeds, 1500, sub_batches=sub)
+    assert run.map.sub_batches == runs
+    assert rep["heads"] == 32
+
+
 @pytest.mark.parametrize("G,d", [(1, 128), (2, 64), (8, 128)])
 def test_decode_group_sizes(G, d):
     w, K, V, q = _case("llama16k", 900, Hq=2 * G, Hkv=2, d=d)

@@ -96,52 +96,6 @@ __device__ __forceinline__ int warp_append(unsigned* counter, bool want) {
   return want ? (int)(base + __popc(bal & ((1u << lane) - 1u))) : -1;
 }
 
-// Aggregated shared-memory histogram add: lane adds x to base[v] (v < 0:
-// nothing).  When the whole warp has the same v (the common case on flat
-// heads) one atomic carries the warp's total; otherwise each lane adds its
-// own (the values are then spread out and rarely collide).
-__device__ __forceinline__ void hist_add_i(int* base, int v, int x) {
-  const int v0 = __shfl_sync(0xffffffffu, v, 0);
-  if (__all_sync(0xffffffffu, v == v0)) {
-    const int tot = (int)__reduce_add_sync(0xffffffffu, (unsigned)x);
-    if ((threadIdx.x & 31) == 0 && v0 >= 0 && tot) atomicAdd(base + v0, tot);
-  } else if (v >= 0 && x) {
-    atomicAdd(base + v, x);
-  }
-}
-__device__ __forceinline__ void hist_add_u(unsigned* base, int v, unsigned x) {
-  const int v0 = __shfl_sync(0xffffffffu, v, 0);
-  if (__all_sync(0xffffffffu, v == v0)) {
-    const unsigned tot = __reduce_add_sync(0xffffffffu, x);
-    if ((threadIdx.x & 31) == 0 && v0 >= 0 && tot) atomicAdd(base + v0, tot);
-  } else if (v >= 0 && x) {
-    atomicAdd(base + v, x);
-  }
-}
-__device__ __forceinline__ void hist_add_f(float* base, int v, float x) {
-  const int v0 = __shfl_sync(0xffffffffu, v, 0);
-  if (__all_sync(0xffffffffu, v == v0)) {
-    float tot = x;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    if ((threadIdx.x & 31) == 0 && v0 >= 0) atomicAdd(base + v0, tot);
-  } else if (v >= 0) {
-    atomicAdd(base + v, x);
-  }
-}
-// Slot in a shared-memory counter per lane (v < 0: none), aggregated the
-// same way.
-__device__ __forceinline__ int slot_add(unsigned* base, int v) {
-  const int lane = threadIdx.x & 31;
-  const int v0 = __shfl_sync(0xffffffffu, v, 0);
-  if (__all_sync(0xffffffffu, v == v0)) {
-    if (v0 < 0) return -1;
-    unsigned b = 0;
-    if (lane == 0) b = atomicAdd(base + v0, 32u);
-    return (int)(__shfl_sync(0xffffffffu, b, 0) + lane);
-  }
-  return v >= 0 ? (int)atomicAdd(base + v, 1u) : -1;
-}
 
 // Chernoff interval for a Poisson-binomial count k (two-sided, budget
 // delta_e / 2 per side): mu = k e^y with phi(y) = e^y - 1 - y = Lz / k.
@@ -601,16 +555,6 @@ constexpr int cand_smem(int G, int J1) {
   return kTile * kTilesPerCta * 8 + G * J1 * 8 + G * (J1 + 1) * 4 + G * J1 * 4;
 }
 
-// Aggregated shared-memory add of a packed (count << 40) + weight pair.
-__device__ __forceinline__ void hist_add_cw(unsigned long long* base, int v, unsigned cnt, unsigned wgt) {
-  const int v0 = __shfl_sync(0xffffffffu, v, 0);
-  if (__all_sync(0xffffffffu, v == v0)) {
-    const unsigned c = __reduce_add_sync(0xffffffffu, cnt), w = __reduce_add_sync(0xffffffffu, wgt);
-    if ((threadIdx.x & 31) == 0 && v0 >= 0 && (c | w)) atomicAdd(base + v0, ((unsigned long long)c << 40) + w);
-  } else if (v >= 0 && (cnt | wgt)) {
-    atomicAdd(base + v, ((unsigned long long)cnt << 40) + wgt);
-  }
-}
 
 // One pass over the pool keys of a group (after the exact maximum):
 //  * t_i, the bound level jbar_i per head, the candidate list (jbar <= J;
@@ -708,7 +652,7 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
       jr = inc ? 0 : (cand ? jb : J + 1);
       if (cand) { cm |= 1u << h; jmin = min(jmin, jb); }
     }
-    hist_add_u(s_jr + h * JS, jr, 1u);
+    if (jr >= 0) atomicAdd(&s_jr[h * JS + jr], 1u);
     const unsigned cb = __ballot_sync(0xffffffffu, (cm >> h) & 1u);
     if (lane == 0 && cb) atomicAdd(&s_nc[h], (unsigned)__popc(cb));
   }
@@ -728,9 +672,12 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
         est = inset ? sp[h] : fsub(ub[h], hw[h]);
         exact_levels(est, c32[h], t, neg_r, J, jl, hl);
       }
-      hist_add_i(s_cnt + h * J1, jl < hl ? jl : -1, (int)mult);                     // light from jl
-      hist_add_cw(s_hv + h * J1, hl <= J ? hl : -1, jl < hl ? mult : 0u,             // light until hl,
-                  mult * __float2uint_rn(__expf(fminf(est - c32[h], 0.f)) * 262144.f));   // heavy from hl
+      // plain per-lane shared atomics (aggregating over equal levels first
+      // cost more than the conflicts it saved)
+      if (jl < hl) atomicAdd(&s_cnt[h * J1 + jl], (int)mult);                        // light from jl
+      if (hl <= J)                                                                   // light until hl,
+        atomicAdd(&s_hv[h * J1 + hl], ((unsigned long long)(jl < hl ? mult : 0u) << 40) +   // heavy from hl
+                                          mult * __float2uint_rn(__expf(fminf(est - c32[h], 0.f)) * 262144.f));
     }
   }
   if (live && inset) {

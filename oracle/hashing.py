@@ -13,6 +13,9 @@ k-th output of a generator seeded with s is mix64(s + k * gamma).
   log2 units t_i     = -log2 u_i = 53 - log2((h_i >> 11) + 1)  (float32)
 so E_i = t_i * ln 2 >= 0 is finite.  The draw depends on (sequence, KV head,
 position, step seed) only, so it is shared by the G query heads of a group.
+Optional per-query-head draws (the alternative the sharing question leaves
+open): query head h of group g uses stream PER_HEAD_STREAM + g G + h in
+place of g, so every head has its own independent draw.
 Test infrastructure only.
 """
 from __future__ import annotations
@@ -34,6 +37,14 @@ def mix64(z):
         z = (z ^ (z >> np.uint64(27))) * _C2
         z = z ^ (z >> np.uint64(31))
     return z
+
+
+PER_HEAD_STREAM = 1 << 20    # stream ids of per-query-head draws start here
+
+
+def head_stream(g: int, G: int, h: int) -> int:
+    """Stream id of query head h of KV group g (per-query-head draws)."""
+    return PER_HEAD_STREAM + g * G + h
 
 
 def group_key(step_seed: int, g: int) -> np.uint64:

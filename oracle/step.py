@@ -49,7 +49,7 @@ import numpy as np
 from .bounds import QM_DEFAULT, key_bounds, query_prep, inv_sqrt_d_f32
 from .certificate import MEASURE_VALUE, certificate_levels
 from .fp32 import tree_sum_f32
-from .hashing import perturb_t
+from .hashing import head_stream, perturb_t
 from .quantize import T_BLOCK, quantize_keys, vmax_blocks
 
 F = np.float32
@@ -68,6 +68,7 @@ class Params:
     measure: int = MEASURE_VALUE
     J_override: int = -1
     QM: int = QM_DEFAULT
+    per_head: bool = False      # one perturbation draw per query head
 
 
 def grid_J(pool: int, r: int) -> int:
@@ -221,11 +222,14 @@ def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
     delta_e = p.delta / (4.0 * (J + 1))
     nblk_pool = (pool + T_BLOCK - 1) // T_BLOCK
     Vmax = float(vmax[:nblk_pool].max())
-    t = perturb_t(step_seed, g, np.arange(pool))           # float32 [pool]
+    t_shared = None if p.per_head else perturb_t(step_seed, g, np.arange(pool))
     win = np.arange(pool, n)
     levels = np.arange(J + 1)
     tau = 2.0 ** (-levels / p.r)
     for h in range(Gh):
+        # the perturbation: shared by the group, or the head's own draw
+        t = (perturb_t(step_seed, head_stream(g, Gh, h), np.arange(pool))
+             if p.per_head else t_shared)                  # float32 [pool]
         # step 2: bounds
         at, alpha, b_hi, b_lo = query_prep(q[h], mins, deltas, p.QM)
         ubar, low, _ = key_bounds(codes, at, alpha, b_hi, b_lo, n)

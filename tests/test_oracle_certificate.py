@@ -128,7 +128,7 @@ def _coverage(name, n, measure, eps, steps, delta):
     for st in range(steps):
         q = synth.q_numpy(w, meta, st, K=K)
         p = Params(eps, delta, 2, measure=measure)
-        res = oracle_decode_group(q[0], K[0, 0], V[0, 0], n, 1000 + st, 0, p,
+        res = oracle_decode_group(q[0, :1], K[0, 0], V[0, 0], n, 1000 + st, 0, p,
                                   keep_detail=False)
         o, s = dense_attention(q[0, 0], K[0, 0, :n], V[0, 0, :n])
         a = np.exp(s - s.max())
@@ -319,3 +319,29 @@ def test_clt_rule_stops_no_later_than_certificate():
                                 keep_detail=False)
         assert np.all(b.level <= a.level)
         assert np.all(b.values_read <= a.values_read)
+
+
+def test_certificate_coverage_per_head_draws():
+    # one perturbation draw per query head (instead of one per KV group):
+    # each head's certificate is the same construction on its own sample,
+    # so Theorem 4 holds per head; 4 heads x 60 fresh steps at 1024 tokens
+    w = synth.workload("llama16k", B=1, n=1024, Hq=4, Hkv=1)
+    K, V, meta = synth.kv_numpy(w)
+    Vd = V[0, 0].astype(np.float64)
+    viol, heads, differ = 0, 0, 0
+    for st in range(60):
+        q = synth.q_numpy(w, meta, st, K=K)
+        p = Params(w.eps, w.delta, w.r, per_head=True)
+        res = oracle_decode_group(q[0], K[0, 0], V[0, 0], w.n, 500 + st, 0, p)
+        ts = [d["t"] for d in res.detail]
+        differ += int(not np.array_equal(ts[0], ts[1]))
+        for h in range(w.G):
+            o, s_ = dense_attention(q[0, h], K[0, 0], V[0, 0])
+            a = np.exp(s_ - s_.max())
+            a /= a.sum()
+            M = math.sqrt(a @ (Vd * Vd).sum(axis=1))
+            heads += 1
+            if res.level[h] <= res.J and np.linalg.norm(res.o[h] - o) > w.eps * M:
+                viol += 1
+    assert differ == 60
+    assert viol <= w.delta * heads + 3.1 * math.sqrt(w.delta * heads)

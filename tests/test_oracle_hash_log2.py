@@ -9,7 +9,8 @@ import pytest
 from scipy import stats
 
 from oracle.fp32 import log2_m53_f32
-from oracle.hashing import GAMMA, group_key, key_hashes, mix64, perturb_t
+from oracle.hashing import (GAMMA, PER_HEAD_STREAM, group_key, head_stream,
+                            key_hashes, mix64, perturb_t)
 
 
 def test_splitmix64_published_outputs():
@@ -90,3 +91,20 @@ def test_u_in_unit_interval(seed):
     h = key_hashes(seed, 0, np.arange(1000))
     m = (h >> np.uint64(11)) + np.uint64(1)
     assert m.min() >= 1 and m.max() <= 2 ** 53
+
+
+def test_per_head_streams():
+    # per-query-head draws: stream ids never meet the KV-group ids, each
+    # head's draw is Exp(1) in nats and the heads' draws are uncorrelated
+    # with each other and with the group's shared draw
+    G, n = 4, 200000
+    ids = [head_stream(g, G, h) for g in range(64) for h in range(G)]
+    assert len(set(ids)) == len(ids) and min(ids) >= PER_HEAD_STREAM
+    draws = [perturb_t(77, head_stream(3, G, h), np.arange(n)).astype(np.float64)
+             for h in range(G)]
+    shared = perturb_t(77, 3, np.arange(n)).astype(np.float64)
+    for h in range(G):
+        assert stats.kstest(draws[h] * np.log(2.0), "expon").pvalue > 1e-3
+        assert abs(np.corrcoef(draws[h], shared)[0, 1]) < 5.0 / np.sqrt(n)
+        for h2 in range(h + 1, G):
+            assert abs(np.corrcoef(draws[h], draws[h2])[0, 1]) < 5.0 / np.sqrt(n)

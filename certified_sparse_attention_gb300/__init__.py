@@ -62,7 +62,8 @@ class csa_shape(ctypes.Structure):
 class csa_params(ctypes.Structure):
     _fields_ = [("eps", ctypes.c_float), ("delta", ctypes.c_float),
                 ("r", ctypes.c_int), ("measure", ctypes.c_int),
-                ("J_override", ctypes.c_int), ("sub_batches", ctypes.c_int)]
+                ("J_override", ctypes.c_int), ("sub_batches", ctypes.c_int),
+                ("perturb", ctypes.c_int)]
 
 
 class csa_head_stats(ctypes.Structure):
@@ -178,9 +179,9 @@ def make_shape(B, Hq, Hkv, d, n_max, dtype) -> csa_shape:
 
 
 def make_params(eps=0.05, delta=0.05, r=2, measure=CSA_MEASURE_VALUE,
-                J_override=-1, sub_batches=0) -> csa_params:
+                J_override=-1, sub_batches=0, perturb=0) -> csa_params:
     return csa_params(float(eps), float(delta), int(r), int(measure),
-                      int(J_override), int(sub_batches))
+                      int(J_override), int(sub_batches), int(perturb))
 
 
 def csa_workspace_size(shape: csa_shape, params: csa_params) -> int:

@@ -39,7 +39,7 @@ csa_status shape_supported(const csa_shape* s) {
 bool params_ok(const csa_params* p) {
   return p && p->eps > 0.f && std::isfinite(p->eps) && p->delta > 0.f && p->delta < 1.f && p->r >= 1 &&
          p->r <= 4 && p->measure >= 0 && p->measure <= 3 && p->J_override >= -1 && p->J_override <= kMaxJ &&
-         p->sub_batches >= 0 && p->sub_batches <= kMaxSub;
+         p->sub_batches >= 0 && p->sub_batches <= kMaxSub && (p->perturb == 0 || p->perturb == 1);
 }
 
 // z with P(|N(0,1)| > z) = delta, i.e. erfc(z / sqrt 2) = delta: bisection
@@ -96,7 +96,7 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.hw = o; o += up((size_t)BG * L.nblk_max * G * 4);
   L.s32 = o; o += up((size_t)BG * L.pcap * G * 4);
   L.win = o; o += up((size_t)BG * kWindow * G * 4);
-  L.t32 = o; o += up((size_t)BG * L.pcap * 4);
+  L.t32 = o; o += up((size_t)BG * L.pcap * (p->perturb ? G : 1) * 4);
   L.clist = o; o += up((size_t)BG * L.pcap * 8);
   L.rlist = o; o += up((size_t)BG * L.pcap * 8);
   L.xlist = o; o += up((size_t)BG * s->n_max * 8);
@@ -285,7 +285,7 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
   a.o = o; a.beta = beta; a.level = level; a.keys_read = keys_read; a.stats = stats;
   a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max; a.nblk_max = L.nblk_max;
   a.pcap = L.pcap; a.J1 = L.J1; a.r = params->r; a.eps = params->eps; a.delta = params->delta;
-  a.measure = params->measure; a.rs = rs;
+  a.measure = params->measure; a.rs = rs; a.per_head = params->perturb;
   a.zclt = normal_quantile_two_sided((double)params->delta);
 
   const int nsm = sm_count();

@@ -37,7 +37,7 @@ struct SparseArgs {
   float* winstats;        // [B*Hq][D+4]          N_R[D], D_R, H_R
   float* vmaxp;           // [B*Hkv]              max vmax over pool blocks
   int* state;             // [B*Hq][4]            lo, hi, stop, flags
-  float* t32;             // [B*Hkv][pcap]        perturbation t_i = -log2 u_i
+  float* t32;             // [B*Hkv][pcap]([G])   perturbation t_i = -log2 u_i (per head if per_head)
   float* pref;            // [B*Hq][ACC]          a continuing head's sums through its last range
   uint2* xlist;           // [B*Hkv][n_max]       exact-max set: key, head mask
   unsigned* xcnt;         // [B*Hkv]
@@ -69,6 +69,7 @@ struct SparseArgs {
   int r;
   float eps, delta;
   int measure;
+  int per_head;           // one perturbation draw per query head
   float zclt;             // two-sided normal quantile at delta (CLT rule)
   float rs;               // float32(1/sqrt d)
 };

@@ -21,6 +21,7 @@ constexpr int kCandSeg = 4096; // pool keys per candidate-list segment (one cand
 constexpr int kMaxB = 128;     // sequences per call
 constexpr int kMaxJ = 255;     // last grid level supported
 constexpr int kMaxSub = 4;     // sub-batches of one decode call
+constexpr int kHeadStream = 1 << 20;   // stream ids of per-query-head draws start here
 
 // Per-call sequence data passed by value (graph-capturable).
 struct SeqArgs {

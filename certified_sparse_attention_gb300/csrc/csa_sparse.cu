@@ -607,7 +607,10 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
     c_b[h] = cmax_get(a, bh0 + h, 2);
     c32[h] = cmax_get(a, bh0 + h, 3);
   }
-  const unsigned long long gk = group_key(seq.seed[b], g);
+  // perturbation keys: the group's, or one per query head
+  unsigned long long gk[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) gk[h] = group_key(seq.seed[b], a.per_head ? kHeadStream + g * G + h : g);
   const bool inset_all = (int64_t)a.xcnt[bg] * 32 <= P;
   // ubar and the block half widths of a key, loaded one tile ahead
   auto load_key = [&](int64_t k, float (&u)[G], float (&h)[G]) {
@@ -635,17 +638,32 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   if (key0 + kTile < kstop) load_key(key + kTile, nub, nhw);
   unsigned cm = 0;
   bool inset = false;
-  float t = 0.f;
+  float t[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) t[h] = 0.f;
   if (live) {
-    t = perturb_t(gk, key);
-    a.t32[(int64_t)bg * a.pcap + key] = t;
+    if (a.per_head) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) t[h] = perturb_t(gk[h], key);
+      float* tp = a.t32 + ((int64_t)bg * a.pcap + key) * G;
+      if (G == 4) *reinterpret_cast<float4*>(tp) = make_float4(t[0], t[1 % G], t[2 % G], t[3 % G]);
+      else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) tp[h] = t[h];
+      }
+    } else {
+      const float t0 = perturb_t(gk[0], key);
+#pragma unroll
+      for (int h = 0; h < G; ++h) t[h] = t0;
+      a.t32[(int64_t)bg * a.pcap + key] = t0;
+    }
   }
   int jmin = 255;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     int jr = -1;
     if (live) {
-      const int jb = bound_level(ub[h], c_b[h], t, neg_r, J);
+      const int jb = bound_level(ub[h], c_b[h], t[h], neg_r, J);
       const bool cand = jb <= J;
       const bool inc = ub[h] >= c_lo[h];
       inset |= inc;
@@ -670,7 +688,7 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
       float est = 0.f;
       if (mult && ((cm >> h) & 1u)) {
         est = inset ? sp[h] : fsub(ub[h], hw[h]);
-        exact_levels(est, c32[h], t, neg_r, J, jl, hl);
+        exact_levels(est, c32[h], t[h], neg_r, J, jl, hl);
       }
       // plain per-lane shared atomics (aggregating over equal levels first
       // cost more than the conflicts it saved)
@@ -900,7 +918,7 @@ constexpr int kLevItem = 2048;   // keys per work item of the level pass (first 
 constexpr int kLevItemLate = 512; // later rounds: few groups, more and shorter items
 
 // One work item: keys [k0, k0 + isz) of group bg.
-template <int G>
+template <int G, bool PH>
 __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& seq, int bg, int64_t k0,
                                             int isz) {
   const int lane = threadIdx.x & 31;
@@ -929,12 +947,11 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
   unsigned* bcnt = a.bcnt + (int64_t)bg * a.J1;
   uint2* bk = a.buckets + (int64_t)bg * a.J1 * a.pcap;
   const float* sb = a.s32 + (int64_t)bg * a.pcap * G;
-  const float* tb = a.t32 + (int64_t)bg * a.pcap;
+  const float* tb = a.t32 + (int64_t)bg * a.pcap * (PH ? G : 1);
   // scores and t of a key, loaded one 256-key step ahead
-  auto load_key = [&](int64_t k, float (&sv)[G], float& t) {
+  auto load_key = [&](int64_t k, float (&sv)[G], float (&t)[G]) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) sv[h] = -INFINITY;
-    t = 0.f;
+    for (int h = 0; h < G; ++h) { sv[h] = -INFINITY; t[h] = 0.f; }
     if (k >= kend) return;
     if (G == 4) {
       const float4 f = *reinterpret_cast<const float4*>(sb + k * G);
@@ -943,9 +960,16 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
 #pragma unroll
       for (int h = 0; h < G; ++h) sv[h] = sb[k * G + h];
     }
-    t = tb[k];
+    if (PH) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) t[h] = tb[k * G + h];
+    } else {
+      const float t0 = tb[k];
+#pragma unroll
+      for (int h = 0; h < G; ++h) t[h] = t0;
+    }
   };
-  float cs[G], ns[G], ct, nt;
+  float cs[G], ns[G], ct[G], nt[G];
   load_key(k0 + threadIdx.x, cs, ct);
   for (int64_t key0 = k0; key0 < kend; key0 += 256) {
     const int64_t key = key0 + threadIdx.x;
@@ -954,10 +978,10 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       jl[h] = J + 1; hl[h] = J + 1;
-      if (cs[h] > -INFINITY) exact_levels(cs[h], c32[h], ct, neg_r, J, jl[h], hl[h]);
+      if (cs[h] > -INFINITY) exact_levels(cs[h], c32[h], ct[h], neg_r, J, jl[h], hl[h]);
       cs[h] = ns[h];
+      ct[h] = nt[h];
     }
-    ct = nt;
     if (wlo == whi) {
       // a one-level round (the common case for flat groups): at most one
       // event per key, slots by a ballot and one atomic per warp
@@ -1025,7 +1049,7 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
   }
 }
 
-template <int G>
+template <int G, bool PH>
 __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
                                                      int round, unsigned tpg, int isz) {
   pdl_entry();
@@ -1038,7 +1062,7 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
     const unsigned item = s_item;
     __syncthreads();
     if (item >= total) break;
-    levels_item<G>(a, seq, (int)a.rq[round * BG + item / tpg], (int64_t)(item % tpg) * isz, isz);
+    levels_item<G, PH>(a, seq, (int)a.rq[round * BG + item / tpg], (int64_t)(item % tpg) * isz, isz);
   }
 }
 
@@ -1834,9 +1858,9 @@ __global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __g
   if (key < P) {
     const float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
     const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
-    const float t = a.t32[(int64_t)bg * a.pcap + key];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
+      const float t = a.per_head ? a.t32[((int64_t)bg * a.pcap + key) * G + h] : a.t32[(int64_t)bg * a.pcap + key];
       const int js = a.state[(int64_t)(bh0 + h) * 4 + 2];
       if (js > J) { needK = needV = true; continue; }   // exact fallback
       if (js < 0) continue;
@@ -2042,7 +2066,17 @@ cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
   }
   CSA_DG_SWITCH(launch_rows1, (pmax_live, nsm, st, a, seq, round))
   if (mark) mark(4, st);
-  CSA_G_SWITCH(levels_kernel, grid, dim3(256), 0, st, a, seq, round, tpg, isz)
+  switch (G * 2 + (a.per_head ? 1 : 0)) {
+    case 2: launch_pdl(levels_kernel<1, false>, grid, dim3(256), 0, st, a, seq, round, tpg, isz); break;
+    case 3: launch_pdl(levels_kernel<1, true>, grid, dim3(256), 0, st, a, seq, round, tpg, isz); break;
+    case 4: launch_pdl(levels_kernel<2, false>, grid, dim3(256), 0, st, a, seq, round, tpg, isz); break;
+    case 5: launch_pdl(levels_kernel<2, true>, grid, dim3(256), 0, st, a, seq, round, tpg, isz); break;
+    case 8: launch_pdl(levels_kernel<4, false>, grid, dim3(256), 0, st, a, seq, round, tpg, isz); break;
+    case 9: launch_pdl(levels_kernel<4, true>, grid, dim3(256), 0, st, a, seq, round, tpg, isz); break;
+    case 16: launch_pdl(levels_kernel<8, false>, grid, dim3(256), 0, st, a, seq, round, tpg, isz); break;
+    case 17: launch_pdl(levels_kernel<8, true>, grid, dim3(256), 0, st, a, seq, round, tpg, isz); break;
+    default: return cudaErrorInvalidValue;
+  }
   if (mark) mark(6, st);
   const int nent = a.B * a.Hkv * a.J1;
   CSA_DG_SWITCH(launch_vgather_t, (nsm, st, a, seq, nent, mark))

@@ -100,6 +100,9 @@ typedef struct {
                    * consecutive sequences, each an independent chain of
                    * launches on a library-owned stream, forked from and
                    * joined back onto the caller's stream                   */
+  int perturb;    /* 0: one perturbation draw per (sequence, KV head, key),
+                   * shared by the group's query heads (default); 1: one draw
+                   * per query head (stream 2^20 + g G + h of the keying)   */
 } csa_params;
 
 /* Optional per-(sequence, query head) diagnostics. */

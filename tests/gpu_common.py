@@ -9,7 +9,7 @@ import numpy as np
 
 import synth
 from oracle.certificate import certificate_levels
-from oracle.hashing import perturb_t
+from oracle.hashing import head_stream, perturb_t
 from oracle.step import Params, dense_attention, level_sums, oracle_decode_group
 
 F = np.float32
@@ -36,7 +36,7 @@ class GpuRun:
 
     def __init__(self, w: synth.Workload, K, V, q, lens, seeds, n_alloc,
                  device="cuda:0", eps=None, delta=None, r=None,
-                 measure=0, J_override=-1, sub_batches=0):
+                 measure=0, J_override=-1, sub_batches=0, perturb=0):
         import torch
         import certified_sparse_attention_gb300 as csa
         self.csa = csa
@@ -47,7 +47,7 @@ class GpuRun:
         self.params = csa.make_params(w.eps if eps is None else eps,
                                       w.delta if delta is None else delta,
                                       w.r if r is None else r, measure,
-                                      J_override, sub_batches)
+                                      J_override, sub_batches, perturb)
         Kp = np.zeros((w.B, w.Hkv, n_alloc, w.d), np.float32)
         Vp = np.zeros_like(Kp)
         Kp[:, :, :K.shape[2]] = K
@@ -156,7 +156,6 @@ def compare_group(run, w, K, V, q, b, g, res, p, report):
     P = n - 64
     J = res.J
     Vd = V[b, g, :n].astype(np.float64)
-    t = perturb_t(run.seeds[b], g, np.arange(P))
     needK, needV = set(), set()
     for h in range(w.G):
         hq = g * w.G + h
@@ -179,6 +178,11 @@ def compare_group(run, w, K, V, q, b, g, res, p, report):
         assert stats[b, hq, 3] == res.n_candidates[h]
         # memberships: device float32 vs oracle float64
         c32 = cm[b, hq, 3]
+        # the head's perturbation, recomputed from the published hash (the
+        # oracle's own draw for this head: shared or per head)
+        t = perturb_t(run.seeds[b],
+                      head_stream(g, w.G, h) if p.per_head else g, np.arange(P))
+        assert np.array_equal(t, det["t"])
         jg, hg = gpu_levels(s32[b, g, :P, h], c32, t, p.r, J)
         # levels beyond the grid are all "never" (J + 1); so are the levels
         # of candidates not rescored (they lie beyond the stop level)
@@ -246,7 +250,8 @@ def compare_group(run, w, K, V, q, b, g, res, p, report):
 def run_and_compare(w, K, V, q, lens, seeds, n_alloc, **pover):
     run = GpuRun(w, K, V, q, lens, seeds, n_alloc, **pover)
     p = Params(run.params.eps, run.params.delta, run.params.r,
-               measure=run.params.measure, J_override=run.params.J_override)
+               measure=run.params.measure, J_override=run.params.J_override,
+               per_head=bool(run.params.perturb))
     report = {"flips": 0, "level_flips": 0, "heads": 0, "levels": []}
     for b in range(w.B):
         n = run.lens[b]

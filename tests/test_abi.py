@@ -68,7 +68,8 @@ def test_unsupported_shapes(lib, bad):
 @pytest.mark.parametrize("pk", [dict(eps=0.0), dict(delta=1.0),
                                 dict(delta=0.0), dict(r=0), dict(r=5),
                                 dict(measure=4), dict(J_override=300),
-                                dict(sub_batches=5), dict(sub_batches=-1)])
+                                dict(sub_batches=5), dict(sub_batches=-1),
+                                dict(perturb=2)])
 def test_invalid_params(lib, pk):
     s = csa.make_shape(1, 8, 2, 128, 4096, "bf16")
     kw = dict(eps=0.05, delta=0.05, r=2)

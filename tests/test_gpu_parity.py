@@ -150,6 +150,17 @@ def test_decode_sub_batches(sub, runs):
     assert rep["heads"] == 32
 
 
+@pytest.mark.parametrize("G,n", [(4, 1100), (8, 900), (2, 1500)])
+def test_decode_per_head_perturbations(G, n):
+    # one perturbation draw per query head: candidates, memberships, o and
+    # beta against the oracle with the same per-head draws, across
+    # sub-batches
+    w, K, V, q = _case("llama16k", n, B=2, Hq=2 * G, Hkv=2)
+    seeds = synth.step_seeds(w, 9)
+    run, rep = run_and_compare(w, K, V, q, [n, n - 77], seeds, n, perturb=1)
+    assert rep["heads"] == 4 * G
+
+
 @pytest.mark.parametrize("G,d", [(1, 128), (2, 64), (8, 128)])
 def test_decode_group_sizes(G, d):
     w, K, V, q = _case("llama16k", 900, Hq=2 * G, Hkv=2, d=d)

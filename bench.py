@@ -158,11 +158,12 @@ class Coverage:
 
 
 def run_mode(args, csa, w, shape, data, lens, seed_tab, nseed, plan, stream,
-             device, measure):
-    """The same steps under another stop measure: keys and values read per
-    head, time per step, and the error against exact attention."""
+             device, measure, perturb=0):
+    """The same steps under another stop measure (or with per-query-head
+    perturbation draws): keys and values read per head, time per step, and
+    the error against exact attention."""
     import torch
-    params = csa.make_params(w.eps, w.delta, w.r, measure)
+    params = csa.make_params(w.eps, w.delta, w.r, measure, perturb=perturb)
     step = csa.DecodeStep(shape, params, device, with_stats=False)
     diag = csa.DecodeStep(shape, params, device, with_stats=True)
     cov = Coverage(w)
@@ -450,9 +451,10 @@ def run_ours(args, world, rank, local):
                          plan, stream, device, reads)
     # the other error measures of the pages' problem setup as benchmark modes
     modes = {name: run_mode(args, csa, w, shape, data, lens, seed_tab, nseed,
-                            plan, stream, device, m)
-             for name, m in (("output", csa.CSA_MEASURE_OUTPUT),
-                             ("denom", csa.CSA_MEASURE_DENOM))}
+                            plan, stream, device, m, pt)
+             for name, m, pt in (("output", csa.CSA_MEASURE_OUTPUT, 0),
+                                 ("denom", csa.CSA_MEASURE_DENOM, 0),
+                                 ("value_per_head_draws", csa.CSA_MEASURE_VALUE, 1))}
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:

@@ -147,22 +147,29 @@ __device__ __forceinline__ void stage8(uint8_t* dst, const E* base, const uint2*
   }
 }
 
-// Same as stage8 with the 16-byte chunk c of row r stored at chunk
-// c ^ (r & 7): eight rows then read the same byte offset from eight
-// different bank groups (tensor-core fragment loads).
-template <int D, typename E>
-__device__ __forceinline__ void stage8_swz(uint8_t* dst, const E* base, const uint2* ent, int nvalid) {
+// NB rows with the 16-byte chunk c of row r stored at chunk c ^ (r & 7)
+// (tensor-core fragment loads of eight rows then hit eight bank groups).
+template <int D, typename E, int NB>
+__device__ __forceinline__ void stage_swz(uint8_t* dst, const E* base, const uint2* ent, int nvalid) {
   constexpr int RB = D * (int)sizeof(E);
   constexpr int CH = RB / 16;
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int c = lane; c < 8 * CH; c += 32) {
+  for (int c = lane; c < NB * CH; c += 32) {
     const int r = c / CH, part = c - r * CH;
     const bool ok = r < nvalid;
     const uint8_t* src = reinterpret_cast<const uint8_t*>(base) + (ok ? (int64_t)ent[r].x * RB + part * 16 : 0);
     cp_async16(dst + r * RB + ((part ^ (r & 7)) * 16), src, ok);
   }
 }
+
+__device__ __forceinline__ void ldsm_x4(unsigned (&r)[4], const void* p) {
+  unsigned sa = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(sa));
+}
+
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const unsigned (&a)[4], unsigned b0, unsigned b1) {
   asm volatile(
@@ -323,6 +330,12 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
 #pragma unroll
   for (int h = 0; h < G; ++h) { cbm[h] = -INFINITY; c3m[h] = -INFINITY; }
   const E* Kb = reinterpret_cast<const E*>(a.K) + (int64_t)bg * a.n_max * D;
+  constexpr bool TC = (MODE == 1) && (sizeof(E) == 2);   // tensor-core scoring
+  // rows per ring slot and slots per warp (the same shared memory either
+  // way): the tensor-core path scores 16 rows per product chain
+  constexpr int NB = TC ? 16 : 8;
+  constexpr int NS = TC ? 2 : kRingS;
+  static_assert(NB * NS == 8 * kRingS, "ring size");
   uint8_t* my = ring + w * kRingS * 8 * RB;
   uint2* me = s_ent + w * kRingS * 8;
   uint2* myq = s_q + w * kQueue;
@@ -339,10 +352,10 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
   load_win(cur + 128, nx);
   int ck = 0;                 // next 32-entry chunk of the current window
   int qh = 0, qt = 0;         // queue head and tail (warp-uniform)
-  // fill ring slot k with up to eight wanted entries; 0 only when the
-  // warp's share is exhausted
+  // fill ring slot k with up to NB wanted entries; 0 only when the warp's
+  // share is exhausted
   auto produce = [&](int k) {
-    while (qt - qh < 8 && cur < end) {
+    while (qt - qh < NB && cur < end) {
       const uint2 e = ck == 0 ? cw[0] : (ck == 1 ? cw[1] : (ck == 2 ? cw[2] : cw[3]));
       bool keep = e.x != ~0u;
       if (MODE == 1 && keep) {
@@ -361,24 +374,26 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
       }
     }
     __syncwarp();
-    const int take = min(8, qt - qh);
-    if (lane < take) me[k * 8 + lane] = myq[(qh + lane) & (kQueue - 1)];
+    const int take = min(NB, qt - qh);
+    if (lane < take) me[k * NB + lane] = myq[(qh + lane) & (kQueue - 1)];
     qh += take;
     __syncwarp();
     return take;
   };
-  constexpr bool TC = (MODE == 1) && (sizeof(E) == 2);   // tensor-core scoring
+  auto stage = [&](int k, int nv) {
+    if (TC) stage_swz<D, E, NB>(my + k * NB * RB, Kb, me + k * NB, nv);
+    else stage8<D, E>(my + k * NB * RB, Kb, me + k * NB, nv);
+    cp_async_commit();
+  };
   unsigned nvpack = 0;        // rows staged per slot, 8 bits each
 #pragma unroll
-  for (int k = 0; k < kRingS; ++k) {
+  for (int k = 0; k < NS; ++k) {
     const int nv = produce(k);
     nvpack |= (unsigned)nv << (8 * k);
-    if (TC) stage8_swz<D, E>(my + k * 8 * RB, Kb, me + k * 8, nv);
-    else stage8<D, E>(my + k * 8 * RB, Kb, me + k * 8, nv);
-    cp_async_commit();
+    stage(k, nv);
   }
-  // query fragments for the tensor-core path: M = heads (rows >= G zero),
-  // K = channels, two bf16 per register
+  // query fragments for the tensor-core path: the B operand (K = channels,
+  // N = heads padded to 8), two bf16 per register
   constexpr int KS = D / 16;
   unsigned qa[KS][2];
   if (TC) {
@@ -392,33 +407,42 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
     }
   }
   for (int it = 0;; ++it) {
-    const int slot = it & (kRingS - 1);
+    const int slot = it % NS;
     const int nv = (int)((nvpack >> (8 * slot)) & 0xFFu);
     // slots are filled in order, so the first empty one ends the share
     if (nv == 0) break;
-    cp_async_wait<kRingS - 1>();
+    cp_async_wait<NS - 1>();
     __syncwarp();
     if (TC) {
-      // scores of the stage's eight rows for all heads in one chain of
-      // m16n8k16 products; lane (g, t) gets head g, rows 2t and 2t+1
+      // scores of the stage's 16 rows for all heads in one chain of
+      // m16n8k16 products: A = rows x channels (ldmatrix from the swizzled
+      // stage), B = the query heads; lane (g, t) gets rows g and g + 8,
+      // heads 2t and 2t + 1 (rows past nv hold zeros and are not stored)
       const int gq = lane >> 2, tq = lane & 3;
-      const uint8_t* st = my + slot * 8 * RB + gq * RB;      // row gq of the stage
+      const int lr = (lane & 7) + ((lane >> 3) & 1) * 8;     // row this lane addresses
+      const uint8_t* st = my + slot * NB * RB + lr * RB;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        const int c0 = 2 * ks, c1 = 2 * ks + 1;               // 16-byte chunks of channels 16ks..+15
-        const unsigned b0 = *reinterpret_cast<const unsigned*>(st + ((c0 ^ (gq & 7)) * 16) + 4 * tq);
-        const unsigned b1 = *reinterpret_cast<const unsigned*>(st + ((c1 ^ (gq & 7)) * 16) + 4 * tq);
-        const unsigned af[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-        mma_bf16_16816(acc, af, b0, b1);
+        const int c = 2 * ks + (lane >> 4);                    // 16-byte chunk of channels
+        unsigned af[4];
+        ldsm_x4(af, st + ((c ^ (lr & 7)) * 16));
+        mma_bf16_16816(acc, af, qa[ks][0], qa[ks][1]);
       }
-      if (gq < G) {
+      if (2 * tq < G) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int r = 2 * tq + u;
+        for (int half = 0; half < 2; ++half) {
+          const int r = gq + 8 * half;
           if (r < nv) {
-            const uint2 en = me[slot * 8 + r];
-            a.s32[((int64_t)bg * a.pcap + en.x) * G + gq] = ((en.y >> gq) & 1u) ? fmul(acc[u], a.rs) : -INFINITY;
+            const uint2 en = me[slot * NB + r];
+            float* dst = a.s32 + ((int64_t)bg * a.pcap + en.x) * G + 2 * tq;
+            const float x0 = ((en.y >> (2 * tq)) & 1u) ? fmul(acc[2 * half], a.rs) : -INFINITY;
+            if (G >= 2) {
+              const float x1 = ((en.y >> (2 * tq + 1)) & 1u) ? fmul(acc[2 * half + 1], a.rs) : -INFINITY;
+              *reinterpret_cast<float2*>(dst) = make_float2(x0, x1);
+            } else {
+              dst[0] = x0;
+            }
           }
         }
       }
@@ -471,9 +495,7 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
     // refill this slot: the next rows of the share, kRingS batches ahead
     const int nn = produce(slot);
     nvpack = (nvpack & ~(0xFFu << (8 * slot))) | ((unsigned)nn << (8 * slot));
-    if (TC) stage8_swz<D, E>(my + slot * 8 * RB, Kb, me + slot * 8, nn);
-    else stage8<D, E>(my + slot * 8 * RB, Kb, me + slot * 8, nn);
-    cp_async_commit();
+    stage(slot, nn);
   }
   cp_async_wait<0>();
   if (MODE == 0) {

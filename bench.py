@@ -367,7 +367,9 @@ def run_ours(args, world, rank, local):
         w = dataclasses.replace(w, n=args.n or w.n, B=args.batch or w.B)
     layers = rank_layers(rank, world, args.layers)
     shape, data = setup_layers(w, layers, device, csa)
-    params = csa.make_params(w.eps, w.delta, w.r)
+    # --sub-batches: profiler captures of the unsplit chain (a scheduling
+    # choice only; the reported line uses the default)
+    params = csa.make_params(w.eps, w.delta, w.r, sub_batches=args.sub_batches)
     step = csa.DecodeStep(shape, params, device, with_stats=False)
     step_diag = csa.DecodeStep(shape, params, device, with_stats=True)
     dense = csa.DenseDecode(shape, device)
@@ -447,14 +449,17 @@ def run_ours(args, world, rank, local):
         reads.append((stats[..., 1].mean(), stats[..., 2].mean()))
         cov.add(d["q"][L % 4], d["K"], d["V"], lens, step_diag)
     ab = {k: sum(x[k] for x in abs_) / len(abs_) for k in abs_[0]}
-    clt = clt_comparison(args, csa, w, shape, data, lens, seed_tab, nseed,
-                         plan, stream, device, reads)
-    # the other error measures of the pages' problem setup as benchmark modes
-    modes = {name: run_mode(args, csa, w, shape, data, lens, seed_tab, nseed,
-                            plan, stream, device, m, pt)
-             for name, m, pt in (("output", csa.CSA_MEASURE_OUTPUT, 0),
-                                 ("denom", csa.CSA_MEASURE_DENOM, 0),
-                                 ("value_per_head_draws", csa.CSA_MEASURE_VALUE, 1))}
+    clt, modes = None, None
+    if not args.no_modes:
+        clt = clt_comparison(args, csa, w, shape, data, lens, seed_tab, nseed,
+                             plan, stream, device, reads)
+        # the other error measures of the pages' problem setup as modes
+        modes = {name: run_mode(args, csa, w, shape, data, lens, seed_tab,
+                                nseed, plan, stream, device, m, pt)
+                 for name, m, pt in (("output", csa.CSA_MEASURE_OUTPUT, 0),
+                                     ("denom", csa.CSA_MEASURE_DENOM, 0),
+                                     ("value_per_head_draws",
+                                      csa.CSA_MEASURE_VALUE, 1))}
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -646,6 +651,10 @@ def main(argv=None):
                     help="override the context length (profiler captures)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch (profiler captures)")
+    ap.add_argument("--no-modes", action="store_true",
+                    help="skip the CLT / other-measure comparisons (profiler captures)")
+    ap.add_argument("--sub-batches", type=int, default=0,
+                    help="sub-batches of the decode call (0: the library default)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world, rank, local = dist_env()

@@ -221,6 +221,71 @@ def clt_comparison(args, csa, w, shape, data, lens, seed_tab, nseed, plan,
             "err_over_epsM": r["err_over_epsM"]}
 
 
+def decode_loop(args, csa, w, device, stream):
+    """Whole-model decode: every token appends one row per layer and runs
+    that layer's step, over `args.decode_layers` layers of the workload's
+    shape (picx.dev "Theoretical Contributions": fresh perturbations at
+    every decoding step).  Per layer and token: re-quantise the appended
+    token's block (csa_quantize_keys from that position), then the decode
+    step with the grown length and a fresh seed.  The K, V rows of the
+    appended tokens are generated with the cache; the loop extends the
+    length over them.  Launched stream-ordered (lengths and seeds are host
+    arguments, new every token)."""
+    import torch
+    import synth
+    L, T = args.decode_layers, 8
+    n0 = w.n - T
+    shape = csa.make_shape(w.B, w.Hq, w.Hkv, w.d, w.n, w.dtype)
+    params = csa.make_params(w.eps, w.delta, w.r)
+    step = csa.DecodeStep(shape, params, device)
+    layers = []
+    for lid in range(L):
+        K, V, meta = synth.kv_torch(w, layer=100 + lid, device=device)
+        mt = csa.meta_buffers(shape, device)
+        csa.check(csa.csa_quantize_keys(shape, K, V, [n0] * w.B, 0, *mt),
+                  "csa_quantize_keys")
+        qs = [synth.q_torch(w, meta, t, layer=100 + lid, device=device)
+              for t in range(T)]
+        layers.append((K, V, mt, qs, lid))
+    torch.cuda.synchronize()
+    seeds = [[seeds_for(w, 100 + lid, t) for t in range(T)] for lid in range(L)]
+
+    def token(t, quant_only=False):
+        pos = n0 + t
+        lens = [pos + 1] * w.B
+        for (K, V, mt, qs, lid) in layers:
+            csa.check(csa.csa_quantize_keys(shape, K, V, lens, pos, *mt, stream=stream),
+                      "csa_quantize_keys")
+            if not quant_only:
+                step(qs[t], K, V, mt, lens, seeds[lid][t], stream)
+
+    token(0)                                   # warm-up (token 0)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(1, T):
+        token(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    csa.check(csa.csa_check(step.ws, stream), "csa_check (decode loop)")
+    us_tok = e0.elapsed_time(e1) / (T - 1) * 1e3
+    e0.record(stream)
+    for t in range(1, T):
+        token(t, quant_only=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us_q = e0.elapsed_time(e1) / (T - 1) * 1e3
+    del layers
+    torch.cuda.empty_cache()
+    return {"layers": L, "tokens_timed": T - 1, "context": f"{n0 + 1}..{w.n}",
+            "us_per_token": round(us_tok, 1),
+            "us_per_layer": round(us_tok / L, 1),
+            "append_quantize_us_per_token": round(us_q, 1),
+            "note": "each layer: quantise the appended token's block, then "
+                    "the certified step with a fresh seed"}
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,"
@@ -449,7 +514,9 @@ def run_ours(args, world, rank, local):
         reads.append((stats[..., 1].mean(), stats[..., 2].mean()))
         cov.add(d["q"][L % 4], d["K"], d["V"], lens, step_diag)
     ab = {k: sum(x[k] for x in abs_) / len(abs_) for k in abs_[0]}
-    clt, modes = None, None
+    clt, modes, loop = None, None, None
+    if not args.no_modes and args.decode_layers > 0:
+        loop = decode_loop(args, csa, w, device, stream)
     if not args.no_modes:
         clt = clt_comparison(args, csa, w, shape, data, lens, seed_tab, nseed,
                              plan, stream, device, reads)
@@ -576,6 +643,7 @@ def run_ours(args, world, rank, local):
         "certificate": cov.summary(),
         "clt_comparison": clt,
         "measures": modes,
+        "decode_loop": loop,
         "keys_read_mean": float(stats[..., 1].mean()),
         "values_read_mean": float(stats[..., 2].mean()),
         "clocks": clocks.summary(),
@@ -651,6 +719,8 @@ def main(argv=None):
                     help="override the context length (profiler captures)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch (profiler captures)")
+    ap.add_argument("--decode-layers", type=int, default=32,
+                    help="layers of the whole-model decode loop (0: skip it)")
     ap.add_argument("--no-modes", action="store_true",
                     help="skip the CLT / other-measure comparisons (profiler captures)")
     ap.add_argument("--sub-batches", type=int, default=0,

@@ -867,8 +867,9 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
     const float L = logf(1.0f / de), Lz = logf(2.0f / de);
     const float Rc = Vp + cn;
     // pred: first level the value-free certificate passes; round 1 gathers
-    // one level past it (the estimate tends to pass a level early; wider
-    // margins cost more in gathered values than the rounds they saved)
+    // max(1, r - 1) levels past it (the estimate tends to pass a few levels
+    // early on peaked heads; margins of 1, 2, 3 and 4 levels at r = 4 gave
+    // 763, 722, 716 and 719 us per 128K x 4 step)
     float runk = 0.f, rundb = 0.f;
     int pred = -1;
     for (int l0 = 0; l0 <= J; l0 += 32) {
@@ -928,7 +929,8 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
     if (lane == 0) {
       // (a prediction of level 0, the flat heads', is not widened: it was
       // exact on every flat head measured, and level 1 would add ~20% rows)
-      const int hi = pred < 0 ? J : (pred == 0 ? 0 : min(J, pred + 1));
+      const int margin = a.r > 2 ? a.r - 1 : 1;
+      const int hi = pred < 0 ? J : (pred == 0 ? 0 : min(J, pred + margin));
       int* st = a.state + (int64_t)bh * 4;
       st[0] = -1; st[1] = hi; st[2] = -1; st[3] = 0;
     }

@@ -7,12 +7,38 @@
 // for all G query heads; each warp scores eight K rows at a time (one row
 // load serves the G heads; lane-local products then an eight-row shuffle
 // reduction), keeps an online-softmax state per head and accumulates the
-// eight V rows.  A second kernel merges the splits.
+// eight V rows.  The K and V rows come through a per-warp ring of
+// shared-memory stages filled with cp.async, kDenseStages batches ahead.
+// A second kernel merges the splits.
 #include "csa_args.cuh"
 
 namespace csa {
 
 constexpr int kDenseChunk = 1024;
+
+// ring stages per warp: 8 K rows and 8 V rows each
+template <typename E>
+__host__ __device__ constexpr int dense_stages() { return sizeof(E) == 2 ? 4 : 2; }
+template <int D, typename E>
+__host__ __device__ constexpr int dense_smem() { return 8 * dense_stages<E>() * 2 * 8 * D * (int)sizeof(E); }
+
+// stage the 8 consecutive rows [k0, k0 + 8) of K and V (rows >= end are
+// zero-filled) with 16-byte cp.async copies
+template <int D, typename E>
+__device__ __forceinline__ void dense_stage(uint8_t* dk, uint8_t* dv, const E* Kb, const E* Vb, int64_t k0,
+                                            int64_t end) {
+  constexpr int RB = D * (int)sizeof(E);
+  constexpr int CH = RB / 16;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = lane; c < 8 * CH; c += 32) {
+    const int r = c / CH, part = c - r * CH;
+    const bool ok = k0 + r < end;
+    const int64_t off = ok ? (k0 + r) * RB + part * 16 : 0;
+    cp_async16(dk + r * RB + part * 16, reinterpret_cast<const uint8_t*>(Kb) + off, ok);
+    cp_async16(dv + r * RB + part * 16, reinterpret_cast<const uint8_t*>(Vb) + off, ok);
+  }
+}
 
 template <int D, typename E>
 __device__ __forceinline__ void dload_row(const E* row, float* v) {
@@ -39,9 +65,14 @@ __global__ void __launch_bounds__(256) dense_split_kernel(const DenseArgs a, con
                                                           int nsplit_live) {
   pdl_entry();
   constexpr int CPL = D / 32;
+  constexpr int S = dense_stages<E>();
+  constexpr int RB = D * (int)sizeof(E);
   __shared__ float s_m[8][G], s_l[8][G];
   __shared__ float s_acc[8][G][D];
+  extern __shared__ __align__(16) uint8_t dsm[];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  uint8_t* ringk = dsm + w * S * 2 * 8 * RB;          // [S][8 rows] of K, then of V
+  uint8_t* ringv = ringk + S * 8 * RB;
   if (a.nfall && *a.nfall == 0u) return;
   const int nitems = nsplit_live * a.B * a.Hkv;
   for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
@@ -65,18 +96,30 @@ __global__ void __launch_bounds__(256) dense_split_kernel(const DenseArgs a, con
   }
   const E* Kb = reinterpret_cast<const E*>(a.K) + (int64_t)bg * a.n_max * D;
   const E* Vb = reinterpret_cast<const E*>(a.V) + (int64_t)bg * a.n_max * D;
-  for (int64_t k0 = start + w * 8; k0 < end; k0 += 64) {
+  // this warp's batches: rows [start + 8w + 64i, + 8) for i < nb
+  const int64_t first = start + w * 8;
+  const int nb = first < end ? (int)((end - first + 63) / 64) : 0;
+#pragma unroll
+  for (int i = 0; i < S; ++i) {
+    if (i < nb) dense_stage<D, E>(ringk + i * 8 * RB, ringv + i * 8 * RB, Kb, Vb, first + 64 * i, end);
+    cp_async_commit();
+  }
+  for (int i = 0; i < nb; ++i) {
+    const int64_t k0 = first + 64 * i;
+    const int slot = i % S;
+    cp_async_wait<S - 1>();
+    __syncwarp();
     float kv[8][CPL], vv[8][CPL];
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      if (k0 + r < end) {
-        dload_row<D, E>(Kb + (k0 + r) * D, kv[r]);
-        dload_row<D, E>(Vb + (k0 + r) * D, vv[r]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) { kv[r][c] = 0.f; vv[r][c] = 0.f; }
-      }
+      dload_row<D, E>(reinterpret_cast<const E*>(ringk + (slot * 8 + r) * RB), kv[r]);
+      dload_row<D, E>(reinterpret_cast<const E*>(ringv + (slot * 8 + r) * RB), vv[r]);
     }
+    __syncwarp();
+    // refill the slot with the batch S ahead
+    if (i + S < nb)
+      dense_stage<D, E>(ringk + slot * 8 * RB, ringv + slot * 8 * RB, Kb, Vb, first + 64 * (i + S), end);
+    cp_async_commit();
     const bool valid = k0 + (lane & 7) < end;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -187,6 +230,22 @@ __global__ void __launch_bounds__(128) dense_combine_kernel(const DenseArgs a, c
 
 int dense_nsplit(int64_t n_max) { return (int)((n_max + kDenseChunk - 1) / kDenseChunk); }
 
+// opt in to the ring's dynamic shared memory once per instantiation
+template <int D, typename E>
+void set_dense_smem(int G) {
+  static bool done[9] = {false};
+  if (G < 1 || G > 8 || done[G]) return;
+  const int smem = dense_smem<D, E>();
+  switch (G) {
+    case 1: cudaFuncSetAttribute(dense_split_kernel<D, 1, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
+    case 2: cudaFuncSetAttribute(dense_split_kernel<D, 2, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
+    case 4: cudaFuncSetAttribute(dense_split_kernel<D, 4, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
+    case 8: cudaFuncSetAttribute(dense_split_kernel<D, 8, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
+    default: break;
+  }
+  done[G] = true;
+}
+
 cudaError_t launch_dense(const DenseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t nmax_live,
                          cudaStream_t st) {
   const int nsplit_live = (int)((nmax_live + kDenseChunk - 1) / kDenseChunk);
@@ -194,7 +253,16 @@ cudaError_t launch_dense(const DenseArgs& a, const SeqArgs& seq, int d, int G, b
   // comparator: one CTA per item; fallback (masked): a small persistent grid
   const int cap = a.state ? 1024 : items;
   dim3 grid((unsigned)(items < cap ? items : cap));
-  CSA_DENSE_SWITCH(dense_split_kernel, grid, dim3(256), 0, st, a, seq, nsplit_live)
+  if (d == 128) {
+    if (bf16) set_dense_smem<128, __nv_bfloat16>(G);
+    else set_dense_smem<128, float>(G);
+  } else {
+    if (bf16) set_dense_smem<64, __nv_bfloat16>(G);
+    else set_dense_smem<64, float>(G);
+  }
+  const int smem = d == 128 ? (bf16 ? dense_smem<128, __nv_bfloat16>() : dense_smem<128, float>())
+                            : (bf16 ? dense_smem<64, __nv_bfloat16>() : dense_smem<64, float>());
+  CSA_DENSE_SWITCH(dense_split_kernel, grid, dim3(256), smem, st, a, seq, nsplit_live)
   if (d == 128) launch_pdl(dense_combine_kernel<128>, dim3(a.B * a.Hq), dim3(128), 0, st, a, seq);
   else launch_pdl(dense_combine_kernel<64>, dim3(a.B * a.Hq), dim3(128), 0, st, a, seq);
   return cudaGetLastError();

@@ -146,12 +146,19 @@ csa_status csa_quantize_keys(const csa_shape* shape, const void* K,
  * [B] (fresh every step; the caller mixes in the layer).  Outputs (device):
  *   o          [B][Hq][d]  o_hat at the stop level (exact o after fallback)
  *   beta       [B][Hq]     certified bound on ||o_hat - o|| (0 after the
- *                          exact fallback or when len <= 64)
+ *                          exact fallback or when len <= 64; under
+ *                          CSA_MEASURE_CLT the uncertified estimate)
  *   level      [B][Hq]     stop level j*; J+1 after the exact fallback
  *   keys_read  [B][Hq]     see csa_head_stats
  *   stats      [B][Hq]     optional (NULL to skip)
  * workspace: device buffer of at least csa_workspace_size bytes, 256-byte
- * aligned; its contents on entry do not matter. */
+ * aligned; its contents on entry do not matter.
+ * With sub-batches (csa_params.sub_batches) the call forks onto the
+ * library's streams of the current device and joins back onto `stream`
+ * before returning control of the outputs; enqueueing is serialised by a
+ * host lock, so concurrent callers are safe but queue behind one another.
+ * Everything is asynchronous on `stream` and capturable into a CUDA graph
+ * (the fork and join are event waits). */
 csa_status csa_decode_step(const csa_shape* shape, const csa_params* params,
                            const void* q, const void* K, const void* V,
                            const uint8_t* K4, const float* bounds,

@@ -218,3 +218,37 @@ def test_decode_llama16k_full_size():
     assert rep["heads"] == 32
     print("near-threshold flips", rep["flips"], "level flips",
           rep["level_flips"], "levels", rep["levels"])
+
+
+def test_decode_step_in_cuda_graph():
+    # the step (two sub-batches: fork and join by events) captured into a
+    # CUDA graph and replayed gives what the eager call gives
+    import torch
+    import certified_sparse_attention_gb300 as csa
+    w, K, V, q = _case("llama16k", 2000, B=2, Hq=8, Hkv=2)
+    dev = torch.device("cuda:0")
+    shape = csa.make_shape(w.B, w.Hq, w.Hkv, w.d, w.n, w.dtype)
+    Kt = torch.from_numpy(K).to(dev).to(torch.bfloat16)
+    Vt = torch.from_numpy(V).to(dev).to(torch.bfloat16)
+    qt = torch.from_numpy(q).to(dev).to(torch.bfloat16)
+    mt = csa.meta_buffers(shape, dev)
+    csa.check(csa.csa_quantize_keys(shape, Kt, Vt, [w.n] * w.B, 0, *mt))
+    seeds = [int(x) for x in synth.step_seeds(w, 11)]
+    step = csa.DecodeStep(shape, csa.make_params(w.eps, w.delta, w.r), dev)
+    side = torch.cuda.Stream(dev)
+    with torch.cuda.stream(side):
+        step(qt, Kt, Vt, mt, [w.n] * w.B, seeds)        # eager (warms up)
+    torch.cuda.synchronize()
+    o_ref = step.o.clone()
+    lv_ref = step.level.clone()
+    step.o.zero_()
+    step.level.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step(qt, Kt, Vt, mt, [w.n] * w.B, seeds)
+    graph.replay()
+    torch.cuda.synchronize()
+    csa.check(csa.csa_check(step.ws), "csa_check")
+    assert torch.equal(step.level, lv_ref)
+    err = torch.linalg.norm(step.o - o_ref, dim=-1)
+    assert torch.all(err <= 1e-4 * torch.linalg.norm(o_ref, dim=-1) + 1e-6)

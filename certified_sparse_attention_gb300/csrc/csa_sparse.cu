@@ -587,7 +587,7 @@ constexpr int cand_smem(int G, int J1) {
 //    score is written when it is rescored, and until then it has no event;
 //  * value-free level histograms from an estimated score (exact for the
 //    exact-max set, ubar minus the block's half width otherwise; the other
-//    keys subsampled one tile in four): counts of light entries and exits
+//    keys subsampled one tile in eight): counts of light entries and exits
 //    and fixed-point heavy weights per level.  They only size the first
 //    gather round.
 template <int G>
@@ -698,12 +698,13 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   }
   float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
   // estimated levels (a key that is no candidate of a head has no level
-  // up to J for it): one tile in four with weight 4; when the exact-max
+  // up to J for it): one tile in eight with weight 8; when the exact-max
   // set is small (it then holds the few keys that carry the heavy weight)
-  // its keys on every tile with weight 1
-  const bool samp = (tile & 3) == 0;
+  // its keys on every tile with weight 1.  (One tile in 4, 8, 16: 717,
+  // 709, 715 us per 128K x 4 step; sparser samples blur the prediction.)
+  const bool samp = (tile & 7) == 0;
   if (samp || (inset_all && __any_sync(0xffffffffu, live && inset))) {
-    const unsigned mult = (live && inset && inset_all) ? 1u : (live && samp ? 4u : 0u);
+    const unsigned mult = (live && inset && inset_all) ? 1u : (live && samp ? 8u : 0u);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       int jl = J + 1, hl = J + 1;

@@ -31,7 +31,7 @@ def to_dev(x, dtype, device):
     return t.to(torch.bfloat16 if dtype == "bf16" else torch.float32)
 
 
-class GpuRun:
+class DeviceRun:
     """One decode step of a workload on the GPU, with workspace views."""
 
     def __init__(self, w: synth.Workload, K, V, q, lens, seeds, n_alloc,
@@ -248,7 +248,7 @@ def compare_group(run, w, K, V, q, b, g, res, p, report):
 
 
 def run_and_compare(w, K, V, q, lens, seeds, n_alloc, **pover):
-    run = GpuRun(w, K, V, q, lens, seeds, n_alloc, **pover)
+    run = DeviceRun(w, K, V, q, lens, seeds, n_alloc, **pover)
     p = Params(run.params.eps, run.params.delta, run.params.r,
                measure=run.params.measure, J_override=run.params.J_override,
                per_head=bool(run.params.perturb))

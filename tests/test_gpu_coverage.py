@@ -18,7 +18,7 @@ import pytest
 
 import synth
 from oracle.step import Params, oracle_decode_group
-from tests.gpu_common import GpuRun, compare_group, ensure_built
+from tests.gpu_common import DeviceRun, compare_group, ensure_built
 
 pytestmark = pytest.mark.gpu
 
@@ -130,7 +130,7 @@ def test_decode_with_appends_32k():
     K, V, meta = synth.kv_numpy(w)              # rows >= n0 are appended later
     q0 = synth.q_numpy(w, meta, 0)
     lens = [n0] * w.B
-    run = GpuRun(w, K, V, q0, lens, synth.step_seeds(w, 0), w.n)
+    run = DeviceRun(w, K, V, q0, lens, synth.step_seeds(w, 0), w.n)
     p = Params(w.eps, w.delta, w.r)
     report = {"flips": 0, "level_flips": 0, "heads": 0, "levels": []}
     for s in range(steps):
@@ -163,7 +163,7 @@ def test_stress_256k_against_oracle(regime):
                        Hq=8, Hkv=2)
     K, V, meta = synth.kv_numpy(w)
     q = synth.q_numpy(w, meta, 0)
-    run = GpuRun(w, K, V, q, [w.n], synth.step_seeds(w, 0), w.n)
+    run = DeviceRun(w, K, V, q, [w.n], synth.step_seeds(w, 0), w.n)
     p = Params(w.eps, w.delta, w.r)
     report = {"flips": 0, "level_flips": 0, "heads": 0, "levels": []}
     res = oracle_decode_group(q[0, 0:w.G], K[0, 0], V[0, 0], w.n,

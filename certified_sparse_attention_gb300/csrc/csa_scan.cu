@@ -19,12 +19,6 @@
 
 namespace csa {
 
-__device__ __forceinline__ int dp4a_us(unsigned a, unsigned b, int c) {
-  int d;
-  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
 // Adjacent-pair tree over the CPT values a thread holds, then over 16 lanes.
 template <int CPT>
 __device__ __forceinline__ float tree16(const float* v) {

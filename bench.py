@@ -145,7 +145,9 @@ class Coverage:
         import numpy as np
         r = np.asarray(self.ratio)
         return {"head_steps": self.n, "beta_violations": self.beta_viol,
-                "eps_violations": self.eps_viol, "fallbacks": self.fallback,
+                "eps_violations": self.eps_viol,
+                "eps_violations_output_norm": int(np.sum(np.asarray(self.ratio_o) > 1.0)),
+                "fallbacks": self.fallback,
                 "delta": self.w.delta,
                 "err_over_epsM": {"p50": round(float(np.percentile(r, 50)), 4),
                                   "p90": round(float(np.percentile(r, 90)), 4),
@@ -199,6 +201,7 @@ def run_mode(args, csa, w, shape, data, lens, seed_tab, nseed, plan, stream,
             "head_steps": cs["head_steps"],
             "beta_violations": cs["beta_violations"],
             "eps_violations_value_scale": cs["eps_violations"],
+            "eps_violations_output_norm": cs["eps_violations_output_norm"],
             "err_over_epsM": cs["err_over_epsM"],
             "err_over_eps_norm_o": cs["err_over_eps_norm_o"]}
 

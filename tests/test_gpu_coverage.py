@@ -59,9 +59,12 @@ class _Tally:
         self.fallback = 0
         self.ratios = []
 
-    def add(self, o_hat, beta, level, o, M, eps, J):
+    def add(self, o_hat, beta, level, o, M, eps, J, output_norm=False):
         import torch
         err = torch.linalg.norm(o_hat.double() - o, dim=-1)
+        if output_norm:
+            # the output measure: ||o_hat - o|| <= eps ||o||
+            M = torch.linalg.norm(o, dim=-1)
         lv = level.long()
         fb = lv > J
         self.n += err.numel()
@@ -85,7 +88,7 @@ class _Tally:
                 "err_over_epsM_max": float(r.max())}
 
 
-def _coverage(w, steps, layer=0):
+def _coverage(w, steps, layer=0, measure=0):
     import torch
     import certified_sparse_attention_gb300 as csa
     dev = torch.device("cuda:0")
@@ -94,7 +97,7 @@ def _coverage(w, steps, layer=0):
     mt = csa.meta_buffers(shape, dev)
     lens = [w.n] * w.B
     csa.check(csa.csa_quantize_keys(shape, K, V, lens, 0, *mt))
-    step = csa.DecodeStep(shape, csa.make_params(w.eps, w.delta, w.r), dev)
+    step = csa.DecodeStep(shape, csa.make_params(w.eps, w.delta, w.r, measure), dev)
     J = int(np.ceil(w.r * np.log2(w.n - 64)))
     tally = _Tally()
     for s in range(steps):
@@ -106,7 +109,8 @@ def _coverage(w, steps, layer=0):
         o, M = _exact(q, K, V, lens, w.G)
         assert torch.isfinite(o_hat).all() and torch.isfinite(beta).all()
         assert (beta >= 0).all() and (level >= 0).all() and (level <= J + 1).all()
-        tally.add(o_hat, beta, level, o, M, w.eps, J)
+        tally.add(o_hat, beta, level, o, M, w.eps, J,
+                  output_norm=(measure == csa.CSA_MEASURE_OUTPUT))
     return tally.check(w.delta)
 
 
@@ -114,6 +118,14 @@ def test_coverage_llama16k():
     w = synth.workload("llama16k")
     summary = _coverage(w, steps=24)
     print("coverage llama16k", summary)
+
+
+def test_coverage_llama16k_output_measure():
+    # the output-norm measure (||o_hat - o|| <= eps ||o||) over 8 steps
+    import certified_sparse_attention_gb300 as csa
+    w = synth.workload("llama16k")
+    summary = _coverage(w, steps=8, measure=csa.CSA_MEASURE_OUTPUT)
+    print("coverage llama16k output measure", summary)
 
 
 def test_coverage_llama128k_b4():

@@ -252,3 +252,27 @@ def test_decode_step_in_cuda_graph():
     assert torch.equal(step.level, lv_ref)
     err = torch.linalg.norm(step.o - o_ref, dim=-1)
     assert torch.all(err <= 1e-4 * torch.linalg.norm(o_ref, dim=-1) + 1e-6)
+
+
+def test_decode_largest_batch_ragged():
+    # the largest batch the boundary takes (128 sequences), ragged lengths
+    # from 1 to 400 tokens (many without a pool): every group against the
+    # oracle, as two sub-batches of 64
+    w, K, V, q = _case("llama16k", 400, B=128, Hq=4, Hkv=2)
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(1, 401, size=w.B)]
+    lens[0], lens[1] = 1, 400
+    seeds = synth.step_seeds(w, 12)
+    run, rep = run_and_compare(w, K, V, q, lens, seeds, 400)
+    assert run.map.sub_batches == 2
+    assert rep["heads"] == w.Hq * sum(1 for n in lens if n > 64)
+    # sequences without a pool: exact attention, beta 0, level 0
+    o_g, beta_g, lvl_g, kr_g, _ = run.outputs()
+    for b, n in enumerate(lens):
+        if n > 64:
+            continue
+        for hq in range(w.Hq):
+            g = hq // w.G
+            o_ref, _ = dense_attention(q[b, hq], K[b, g, :n], V[b, g, :n])
+            assert np.linalg.norm(o_g[b, hq] - o_ref) <= 1e-5 * np.linalg.norm(o_ref) + 1e-6
+            assert beta_g[b, hq] == 0 and lvl_g[b, hq] == 0 and kr_g[b, hq] == n

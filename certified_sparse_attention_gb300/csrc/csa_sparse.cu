@@ -23,13 +23,16 @@
 //   levels_kernel   (per round) each key that changes a head's sums at a
 //                   level of the round is appended once to the (b, g, level)
 //                   bucket, with per-head event masks
-//   vplan_kernel    (per round) work items over the new bucket entries
-//   vgather_kernel  (per round) V rows of the bucketed keys; per-level
+//   vplan_kernel    (per round) ranges of the new bucket entries
+//   vsum_kernel     (per round, bf16) V rows of the bucketed keys in
+//                   batches of 16 entries of one level; per-level
 //                   Horvitz-Thompson sums (light count, sum v, sum ||v||^2;
-//                   heavy sum w, sum w v, sum w ||v||^2) per head
+//                   heavy sum w, sum w v, sum w ||v||^2) per head as
+//                   tensor-core products (vgather_kernel: the float32 path)
 //   certify_kernel  (per round) prefix over levels, Chernoff interval,
 //                   Bernstein bound on G, Pinelis bound zeta, beta, value
-//                   scale lower bound; first certified level -> outputs
+//                   scale lower bound; first certified level -> outputs;
+//                   a head with none in its range goes to the next round
 //   near_kernel     optional diagnostics: near-threshold keys at the stop,
 //                   rows read per group
 // Row gathers (K rows, V rows) go through a per-warp ring of shared-memory

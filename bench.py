@@ -705,6 +705,56 @@ def run_reference(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def context_sweep(args):
+    """Step time against context length: the certified sparse step and the
+    same-build dense decode at 128K to 1M tokens (batch 1, and batch 4 up
+    to 256K), two independently seeded layers rotated.  One JSON line per
+    point; not part of the benchmark line."""
+    import torch
+    import synth
+    import certified_sparse_attention_gb300 as csa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    csa.load_library()
+    for n in (131072, 262144, 524288, 1048576):
+        for B in (1, 4):
+            if B == 4 and n > 262144:
+                continue
+            w = synth.workload(WORKLOAD, n=n, B=B)
+            shape, data = setup_layers(w, [0, 1], dev, csa)
+            step = csa.DecodeStep(shape, csa.make_params(w.eps, w.delta, w.r), dev)
+            dense = csa.DenseDecode(shape, dev)
+            lens = [n] * B
+            st = torch.cuda.current_stream(dev)
+
+            def run_sparse(i):
+                d = data[i % 2]
+                step(d["q"][i % 4], d["K"], d["V"], d["meta"], lens,
+                     seeds_for(w, d["lid"], i), st)
+
+            def run_dense(i):
+                d = data[i % 2]
+                dense(d["q"][i % 4], d["K"], d["V"], lens, st)
+
+            res = {}
+            for name, fn in (("sparse_us", run_sparse), ("dense_us", run_dense)):
+                for i in range(4):
+                    fn(i)
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                for i in range(20):
+                    fn(i)
+                e1.record(st)
+                torch.cuda.synchronize()
+                res[name] = round(e0.elapsed_time(e1) / 20 * 1e3, 1)
+            csa.check(csa.csa_check(step.ws), "csa_check (context sweep)")
+            print(json.dumps({"context_sweep": {"n": n, "B": B, **res}}), flush=True)
+            del data, step, dense
+            torch.cuda.empty_cache()
+
+
 def synth_workload(name):
     import synth
     return synth.workload(name)
@@ -722,6 +772,8 @@ def main(argv=None):
                     help="override the context length (profiler captures)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch (profiler captures)")
+    ap.add_argument("--context-sweep", action="store_true",
+                    help="print step times from 128K to 1M tokens and exit")
     ap.add_argument("--decode-layers", type=int, default=32,
                     help="layers of the whole-model decode loop (0: skip it)")
     ap.add_argument("--no-modes", action="store_true",
@@ -733,6 +785,10 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank, local)
+        return
+    if args.context_sweep:
+        if rank == 0:
+            context_sweep(args)
         return
     if world > 1:
         import torch.distributed as dist

@@ -21,9 +21,14 @@ import synth  # noqa: E402
 from oracle.step import Params, oracle_decode_group  # noqa: E402
 
 CASES = [
-    # name, workload, overrides, n, step, seed
+    # name, workload, overrides, n, step, seed[, oracle parameter overrides]
     ("tiny_n300", "tiny", {}, 300, 2, 77),
     ("llama_g2_n700", "llama16k", {"Hq": 8, "Hkv": 2}, 700, 0, 12345),
+    # the uncertified CLT comparison rule and per-query-head draws
+    ("llama_g2_n700_clt", "llama16k", {"Hq": 8, "Hkv": 2}, 700, 0, 12345,
+     {"measure": 3}),
+    ("llama_g2_n700_perhead", "llama16k", {"Hq": 8, "Hkv": 2}, 700, 0, 12345,
+     {"per_head": True}),
 ]
 
 
@@ -31,7 +36,7 @@ def _digest(a):
     return hashlib.sha256(np.ascontiguousarray(a).tobytes()).hexdigest()[:16]
 
 
-def run_case(wname, over, n, step, seed):
+def run_case(wname, over, n, step, seed, pover=None):
     w = synth.workload(wname, B=1, n=n, **over)
     K, V, meta = synth.kv_numpy(w)
     q = synth.q_numpy(w, meta, step, K=K)
@@ -39,7 +44,7 @@ def run_case(wname, over, n, step, seed):
     for g in range(w.Hkv):
         res = oracle_decode_group(q[0, g * w.G:(g + 1) * w.G], K[0, g],
                                   V[0, g], n, seed, g,
-                                  Params(w.eps, w.delta, w.r))
+                                  Params(w.eps, w.delta, w.r, **(pover or {})))
         for h, det in enumerate(res.detail):
             out.append({
                 "g": g, "h": h, "J": res.J,
@@ -57,10 +62,12 @@ def run_case(wname, over, n, step, seed):
 
 
 def main():
-    for name, wname, over, n, step, seed in CASES:
+    for case in CASES:
+        name, wname, over, n, step, seed = case[:6]
+        pover = case[6] if len(case) > 6 else {}
         data = {"case": name, "workload": wname, "overrides": over, "n": n,
-                "step": step, "seed": seed,
-                "heads": run_case(wname, over, n, step, seed)}
+                "step": step, "seed": seed, "params": pover,
+                "heads": run_case(wname, over, n, step, seed, pover)}
         with open(os.path.join(HERE, name + ".json"), "w") as f:
             json.dump(data, f, indent=1)
         print("wrote", name)

@@ -17,10 +17,11 @@ HERE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_oracle_matches_fixture(case):
-    name, wname, over, n, step, seed = case
+    name, wname, over, n, step, seed = case[:6]
+    pover = case[6] if len(case) > 6 else {}
     with open(os.path.join(HERE, name + ".json")) as f:
         ref = json.load(f)
-    got = run_case(wname, over, n, step, seed)
+    got = run_case(wname, over, n, step, seed, pover)
     assert len(got) == len(ref["heads"])
     for a, b in zip(got, ref["heads"]):
         for key in ("J", "level", "keys_read", "values_read", "n_candidates",

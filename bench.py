@@ -652,7 +652,7 @@ def run_ours(args, world, rank, local):
         "keys_read_mean": float(stats[..., 1].mean()),
         "values_read_mean": float(stats[..., 2].mean()),
         "clocks": clocks.summary(),
-        "e2e": {"value": round(ms_e2e * 1e3, 2), "unit": "us/step",
+        "e2e": {"value": round(ms_e2e * 1e3 / world, 2), "unit": "us/step",
                 "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(launches),

@@ -74,7 +74,7 @@ def barrier(world: int):
 
 
 def workload_name(w) -> str:
-    return (f"{WORKLOAD}: B={w.B} sequences x 1 layer per step, n={w.n}, "
+    return (f"{w.name}: B={w.B} sequences x 1 layer per step, n={w.n}, "
             f"Hq={w.Hq}, Hkv={w.Hkv}, d={w.d}, bf16, eps={w.eps}, "
             f"delta={w.delta}, r={w.r}")
 
@@ -374,7 +374,7 @@ def _oracle_task(job):
     return t1 - t0, t2 - t1
 
 
-def oracle_step_times(pool, cores, w, step):
+def oracle_step_times(pool, cores, w, step, name=None):
     """Host time of the oracle for one step (all B x Hkv groups), from a
     bounded sample: `cores` groups (half peaked, half near-uniform), one
     per process, in parallel.  Returns (sparse, dense) seconds per whole
@@ -382,7 +382,7 @@ def oracle_step_times(pool, cores, w, step):
     group x groups / cores), and the sparse core seconds per whole step."""
     groups = w.B * w.Hkv
     ns = min(cores, groups)
-    jobs = [(WORKLOAD, 1000 + 97 * step + i, step, i % 2) for i in range(ns)]
+    jobs = [(name or WORKLOAD, 1000 + 97 * step + i, step, i % 2) for i in range(ns)]
     res = pool.map(_oracle_task, jobs, chunksize=1)
     sp = sum(r[0] for r in res) / ns * groups
     de = sum(r[1] for r in res) / ns * groups
@@ -491,6 +491,20 @@ def run_ours(args, world, rank, local):
     ms_sparse = max_over_ranks(ms_sparse, world, device)
     ms_dense = max_over_ranks(ms_dense, world, device)
 
+    # per-step times (events around each step on the caller's stream, after
+    # the join), for the median and 90th percentile
+    ndist = min(len(plan), 100)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ndist)]
+    for i, (L, s) in enumerate(plan[:ndist]):
+        evs[2 * i].record(stream)
+        one(s, L)
+        evs[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(ndist))
+    step_dist = {"steps": ndist,
+                 "median_us": round(per_step[ndist // 2] * 1e3, 1),
+                 "p90_us": round(per_step[min(ndist - 1, (9 * ndist) // 10)] * 1e3, 1)}
+
     # live per-phase times (CUDA events at phase boundaries on the stream)
     csa.csa_profile_enable(True)
     nprof = min(args.steps, 32)
@@ -592,6 +606,9 @@ def run_ours(args, world, rank, local):
         pool, cores = cpu_pool()
         try:
             sp, de, sp_core, de_core = oracle_step_times(pool, cores, w, 0)
+            w16 = synth.workload("llama16k")
+            sp16, de16, sp16_core, _ = oracle_step_times(pool, cores, w16, 0,
+                                                         name="llama16k")
         finally:
             pool.close()
             pool.join()
@@ -604,7 +621,11 @@ def run_ours(args, world, rank, local):
                          f"parallel on {cores} host cores; value = mean core "
                          "time per group x groups per step / cores",
                "single_core_us": round(sp_core * 1e6, 1),
-               "dense_oracle_us": round(de * 1e6, 1)}
+               "dense_oracle_us": round(de * 1e6, 1),
+               "llama16k": {"workload": workload_name(w16),
+                            "value": round(sp16 * 1e6, 1),
+                            "single_core_us": round(sp16_core * 1e6, 1),
+                            "dense_oracle_us": round(de16 * 1e6, 1)}}
 
     levels = stats[..., 0]
     line = {
@@ -641,6 +662,7 @@ def run_ours(args, world, rank, local):
                           "frac": round(step_gbs / hbm_peak, 4)},
         "phase_us": {k: round(v * 1e3, 1) for k, v in phase_ms.items()},
         "dominant_phase": dom_all,
+        "step_us_distribution": step_dist,
         "dense_us_per_step": round(ms_dense * 1e3, 2),
         "dense_gbs": round(dense_gbs, 1),
         "sparse_over_dense_time": round(ms_sparse / ms_dense, 3),
@@ -709,52 +731,54 @@ def run_reference(args, world, rank, local):
 
 def context_sweep(args):
     """Step time against context length: the certified sparse step and the
-    same-build dense decode at 128K to 1M tokens (batch 1, and batch 4 up
-    to 256K), two independently seeded layers rotated.  One JSON line per
-    point; not part of the benchmark line."""
+    same-build dense decode for the 16K single-layer shape, then 128K to 1M
+    tokens (batch 1, and batch 4 up to 256K), two independently seeded
+    layers rotated.  One JSON line per point; not part of the benchmark
+    line."""
     import torch
     import synth
     import certified_sparse_attention_gb300 as csa
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     csa.load_library()
-    for n in (131072, 262144, 524288, 1048576):
-        for B in (1, 4):
-            if B == 4 and n > 262144:
-                continue
-            w = synth.workload(WORKLOAD, n=n, B=B)
-            shape, data = setup_layers(w, [0, 1], dev, csa)
-            step = csa.DecodeStep(shape, csa.make_params(w.eps, w.delta, w.r), dev)
-            dense = csa.DenseDecode(shape, dev)
-            lens = [n] * B
-            st = torch.cuda.current_stream(dev)
+    points = [("llama16k", 16384, 1)]
+    points += [(WORKLOAD, n, B) for n in (131072, 262144, 524288, 1048576)
+               for B in (1, 4) if not (B == 4 and n > 262144)]
+    for name, n, B in points:
+        w = synth.workload(name, n=n, B=B)
+        shape, data = setup_layers(w, [0, 1], dev, csa)
+        step = csa.DecodeStep(shape, csa.make_params(w.eps, w.delta, w.r), dev)
+        dense = csa.DenseDecode(shape, dev)
+        lens = [n] * B
+        st = torch.cuda.current_stream(dev)
 
-            def run_sparse(i):
-                d = data[i % 2]
-                step(d["q"][i % 4], d["K"], d["V"], d["meta"], lens,
-                     seeds_for(w, d["lid"], i), st)
+        def run_sparse(i):
+            d = data[i % 2]
+            step(d["q"][i % 4], d["K"], d["V"], d["meta"], lens,
+                 seeds_for(w, d["lid"], i), st)
 
-            def run_dense(i):
-                d = data[i % 2]
-                dense(d["q"][i % 4], d["K"], d["V"], lens, st)
+        def run_dense(i):
+            d = data[i % 2]
+            dense(d["q"][i % 4], d["K"], d["V"], lens, st)
 
-            res = {}
-            for name, fn in (("sparse_us", run_sparse), ("dense_us", run_dense)):
-                for i in range(4):
-                    fn(i)
-                torch.cuda.synchronize()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(st)
-                for i in range(20):
-                    fn(i)
-                e1.record(st)
-                torch.cuda.synchronize()
-                res[name] = round(e0.elapsed_time(e1) / 20 * 1e3, 1)
-            csa.check(csa.csa_check(step.ws), "csa_check (context sweep)")
-            print(json.dumps({"context_sweep": {"n": n, "B": B, **res}}), flush=True)
-            del data, step, dense
-            torch.cuda.empty_cache()
+        res = {}
+        for key, fn in (("sparse_us", run_sparse), ("dense_us", run_dense)):
+            for i in range(4):
+                fn(i)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for i in range(20):
+                fn(i)
+            e1.record(st)
+            torch.cuda.synchronize()
+            res[key] = round(e0.elapsed_time(e1) / 20 * 1e3, 1)
+        csa.check(csa.csa_check(step.ws), "csa_check (context sweep)")
+        print(json.dumps({"context_sweep": {"workload": name, "n": n, "B": B,
+                                            "r": w.r, **res}}), flush=True)
+        del data, step, dense
+        torch.cuda.empty_cache()
 
 
 def synth_workload(name):

@@ -73,6 +73,9 @@ def barrier(world: int):
         dist.barrier()
 
 
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e nominal bandwidth (the measured copy peak is the roofline)
+
+
 def workload_name(w) -> str:
     return (f"{w.name}: B={w.B} sequences x 1 layer per step, n={w.n}, "
             f"Hq={w.Hq}, Hkv={w.Hkv}, d={w.d}, bf16, eps={w.eps}, "
@@ -656,10 +659,12 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": dom,
                      "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "peak_source": peak_src, "traffic": traffic},
+                     "peak_source": peak_src, "traffic": traffic,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
         "step_roofline": {"algorithmic_bytes": round(ab["total"]),
                           "achieved_gbs": round(step_gbs, 1),
-                          "frac": round(step_gbs / hbm_peak, 4)},
+                          "frac": round(step_gbs / hbm_peak, 4),
+                          "frac_of_nominal": round(step_gbs / NOMINAL_HBM_GBS, 4)},
         "phase_us": {k: round(v * 1e3, 1) for k, v in phase_ms.items()},
         "dominant_phase": dom_all,
         "step_us_distribution": step_dist,

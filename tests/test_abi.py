@@ -112,3 +112,28 @@ def test_missing_library_fails_loudly(tmp_path):
             csa.load_library(str(tmp_path / "nope.so"))
         finally:
             csa._lib = csa._lib_save
+
+
+def test_plain_c_caller_builds(lib, tmp_path):
+    # the boundary needs no PyTorch: a plain C program (CUDA runtime for
+    # device memory only) compiles and links against libcsa.so; it runs a
+    # quantise + decode step on a GPU
+    import shutil
+    import subprocess
+    cc = shutil.which("cc") or shutil.which("gcc")
+    cuda = "/usr/local/cuda"
+    if not cc or not os.path.exists(os.path.join(cuda, "include", "cuda_runtime_api.h")):
+        pytest.skip("no C compiler or CUDA headers")
+    libdir = os.path.dirname(csa.LIB_PATH)
+    cudalib = next((os.path.join(cuda, p) for p in ("lib64", "lib", "targets/sbsa-linux/lib")
+                    if os.path.exists(os.path.join(cuda, p, "libcudart.so"))), None)
+    if cudalib is None:
+        pytest.skip("no libcudart.so")
+    out = tmp_path / "decode_example"
+    cmd = [cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+           "-I", os.path.join(cuda, "include"),
+           os.path.join(ROOT, "tests", "c", "decode_example.c"),
+           "-L", libdir, "-lcsa", "-L", cudalib, "-lcudart", "-lm", "-o", str(out)]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert out.exists()

@@ -561,13 +561,14 @@ def run_ours(args, world, rank, local):
     dom = max(phase_bytes, key=lambda k: phase_ms.get(k, 0.0))
     dom_all = max(phase_ms, key=lambda k: phase_ms[k])
     achieved = phase_bytes[dom] / (phase_ms[dom] * 1e-3) / 1e9
-    traffic = None
+    traffic, scan_issue = None, None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         try:
             with open(tpath) as f:
                 tr = json.load(f)
             traffic = tr.get(dom)
+            scan_issue = tr.get("scan_issue_active_pct")
         except (OSError, ValueError):
             traffic = None
     step_gbs = ab["total"] / (ms_sparse * 1e-3) / 1e9
@@ -660,7 +661,9 @@ def run_ours(args, world, rank, local):
                      "achieved": round(achieved, 1), "peak": hbm_peak,
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "peak_source": peak_src, "traffic": traffic,
-                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     # the scan's secondary bound: ncu issue-slot use
+                     "scan_issue_active_pct": scan_issue},
         "step_roofline": {"algorithmic_bytes": round(ab["total"]),
                           "achieved_gbs": round(step_gbs, 1),
                           "frac": round(step_gbs / hbm_peak, 4),

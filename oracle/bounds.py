@@ -49,10 +49,14 @@ def inv_sqrt_d_f32(d: int) -> np.float32:
 
 
 def query_prep(q: np.ndarray, mins: np.ndarray, deltas: np.ndarray,
-               QM: int = QM_DEFAULT):
+               QM: int = QM_DEFAULT, levels: int = 15):
     """Per-block query code for one query head.
 
-    q float32 [d]; mins, deltas float32 [nblk, d].
+    q float32 [d]; mins, deltas float32 [nblk, d]; `levels` the largest key
+    code (15 for the 4-bit keys; 255 for the 8-bit refinement codes, whose
+    bound is the same construction with 15 -> 255 and 16 -> 256, best with
+    a finer query code, QM = 2047: with QM = 127 the query residual term
+    levels * sum |r_c| outweighs the 8-bit keys' rounding slack).
     Returns (at int32 [nblk, d], alpha f32 [nblk], b_hi f32 [nblk],
     b_lo f32 [nblk]).
     """
@@ -72,10 +76,10 @@ def query_prep(q: np.ndarray, mins: np.ndarray, deltas: np.ndarray,
     Rp = tree_sum_f32(np.maximum(r, F(0.0)))
     Rn = tree_sum_f32(np.maximum(-r, F(0.0)))
     sk = A1 * _RHO
-    hi = sk + F(15.0) * Rp
-    lo = sk + F(15.0) * Rn
+    hi = sk + F(levels) * Rp
+    lo = sk + F(levels) * Rn
     Q1 = tree_sum_f32(np.abs(qt))
-    Kabs = (np.abs(mins) + F(16.0) * deltas).max(axis=1)
+    Kabs = (np.abs(mins) + F(levels + 1) * deltas).max(axis=1)
     mag = ((Q1 * Kabs) + hi) + lo
     marg = mag * _MARG
     b_hi = (Bq + hi) + marg

@@ -28,13 +28,9 @@ T_BLOCK = 64
 _VMAX_UP = F(1.0 + 2.0 ** -16)
 
 
-def quantize_keys(K: np.ndarray, n: int, T: int = T_BLOCK):
-    """Quantise the first n rows of K (float32 [>=n, d]).
-
-    Returns (codes uint8 [nblk*T, d] unpacked, packed uint8 [nblk*T, d/2],
-    mins float32 [nblk, d], deltas float32 [nblk, d]).
-    Rows at positions >= n get code 0.
-    """
+def _quantize(K: np.ndarray, n: int, T: int, levels: int):
+    """Per-block per-channel quantiser with codes 0..levels (the rule in the
+    module docstring, with `levels` in place of 15)."""
     K = np.asarray(K, dtype=np.float32)
     d = K.shape[1]
     nblk = (n + T - 1) // T
@@ -46,15 +42,35 @@ def quantize_keys(K: np.ndarray, n: int, T: int = T_BLOCK):
         rows = K[a:b]
         m = rows.min(axis=0)
         M = rows.max(axis=0)
-        dl = (M - m) / F(15.0)
+        dl = (M - m) / F(levels)
         dl = np.where(dl == F(0.0), F(1.0), dl).astype(np.float32)
         x = (rows - m[None, :]) / dl[None, :]
-        c = np.clip(np.rint(x), 0, 15)
+        c = np.clip(np.rint(x), 0, levels)
         codes[a:b] = c.astype(np.uint8)
         mins[blk] = m
         deltas[blk] = dl
+    return codes, mins, deltas
+
+
+def quantize_keys(K: np.ndarray, n: int, T: int = T_BLOCK):
+    """Quantise the first n rows of K (float32 [>=n, d]) to 4 bits.
+
+    Returns (codes uint8 [nblk*T, d] unpacked, packed uint8 [nblk*T, d/2],
+    mins float32 [nblk, d], deltas float32 [nblk, d]).
+    Rows at positions >= n get code 0.
+    """
+    codes, mins, deltas = _quantize(K, n, T, 15)
     packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
     return codes, packed, mins, deltas
+
+
+def quantize_keys8(K: np.ndarray, n: int, T: int = T_BLOCK):
+    """8-bit codes of the same blocks (picx.dev "Algorithm Components" 4:
+    "8-bit refinement" before the exact 16-bit reads; the pages give no
+    detail, so the 4-bit rule with 255 levels: Delta8_c = fl((M_c -
+    m_c) / 255), code = clamp(rint(fl(fl(k - m_c) / Delta8_c)), 0, 255)).
+    Returns (codes uint8 [nblk*T, d], mins, deltas8)."""
+    return _quantize(K, n, T, 255)
 
 
 def value_sq_norms_f32(V: np.ndarray, n: int) -> np.ndarray:

@@ -208,3 +208,87 @@ def test_bound_tight_for_aligned_query_residual():
     tol = 0.5 * np.abs(qt).sum() * (1 + 3e-3)
     assert ub[2] - s[2] <= tol
     assert s[3] - lo[3] <= tol
+
+
+# ----------------------------------------------------- 8-bit refinement codes
+
+QM8 = 2047
+
+def test_quantizer8_error_bound_and_codes():
+    # the 8-bit codes of the same blocks: 0..255 and |k - m - code Delta8|
+    # <= Delta8 (1/2 + 2^-16), Delta8 = (max - min) / 255
+    from oracle.quantize import quantize_keys8
+    rng = np.random.default_rng(3)
+    n, d = 1000, 64
+    K = (rng.normal(size=(n, d)) * rng.lognormal(0, 1, d)).astype(np.float32)
+    codes, mins, deltas = quantize_keys8(K, n)
+    assert codes.max() <= 255
+    blk = np.arange(n) // 64
+    err = np.abs(K.astype(np.float64) - mins[blk] - codes[:n] * deltas[blk].astype(np.float64))
+    assert np.all(err <= deltas[blk] * (0.5 + 2.0 ** -16))
+    nf = n // 64
+    Kb = K[:nf * 64].reshape(nf, 64, d)
+    span = Kb.max(axis=1) - Kb.min(axis=1)
+    assert np.allclose(deltas[:nf], span / 255.0, rtol=1e-6)
+
+
+@pytest.mark.parametrize("regime", ["llama", "outliers"])
+def test_bounds8_hold_and_are_tighter(regime):
+    # the same bound construction on 8-bit codes (15 -> 255) holds for every
+    # key and is an order of magnitude narrower than the 4-bit one
+    from oracle.quantize import quantize_keys8
+    rng = np.random.default_rng(4)
+    n, d = 1500, 128
+    K = rng.normal(size=(n, d)).astype(np.float32)
+    if regime == "outliers":
+        K[:, :4] *= 8.0
+    q = (rng.normal(size=d) * 3.0).astype(np.float32)
+    s = _exact_scores(q, K)
+    c4, _, m4, d4 = quantize_keys(K, n)
+    at4, al4, bh4, bl4 = query_prep(q, m4, d4)
+    u4, l4, _ = key_bounds(c4, at4, al4, bh4, bl4, n)
+    c8, m8, d8 = quantize_keys8(K, n)
+    # 12-bit query codes (QM 2047): with int8 ones the query residual term,
+    # 255 x sum |r_c|, would dominate the 8-bit keys' rounding slack
+    at8, al8, bh8, bl8 = query_prep(q, m8, d8, QM=QM8, levels=255)
+    u8, l8, I8 = key_bounds(c8, at8, al8, bh8, bl8, n)
+    assert np.abs(I8).max() < 2 ** 24          # exact in float32
+    assert np.all(u8.astype(np.float64) >= s) and np.all(l8.astype(np.float64) <= s)
+    # brute-force integer dot products
+    blk = np.arange(n) // 64
+    for i in (0, 77, n - 1):
+        assert I8[i] == int(np.dot(c8[i].astype(np.int64), at8[blk[i]].astype(np.int64)))
+    w4 = float(np.mean(u4 - l4))
+    w8 = float(np.mean(u8 - l8))
+    assert w8 < w4 / 12.0, (w4, w8)
+
+
+def test_refined_bound_level_stays_below_the_exact_level():
+    # refinement: the bound level from min(ubar4, ubar8) is at least the
+    # 4-bit bound level and never above the exact level, so a key it drops
+    # cannot enter the sample at that level; on a peaked head it drops most
+    # of the keys the 4-bit bound keeps at the stop level
+    from oracle.quantize import quantize_keys8
+    from oracle.step import Params, bound_levels_f32, oracle_decode_group
+    w = synth.workload("llama16k", B=1, n=3000, Hq=4, Hkv=1)
+    K, V, meta = synth.kv_numpy(w)
+    q = synth.q_numpy(w, meta, 0)
+    seed = int(synth.step_seeds(w, 0)[0])
+    res = oracle_decode_group(q[0], K[0, 0], V[0, 0], w.n, seed, 0,
+                              Params(w.eps, w.delta, w.r))
+    P = w.n - 64
+    c8, m8, d8 = quantize_keys8(K[0, 0, :w.n], w.n)
+    kept4 = kept8 = 0
+    for h in range(w.G):
+        det = res.detail[h]
+        at8, al8, bh8, bl8 = query_prep(q[0, h], m8, d8, QM=QM8, levels=255)
+        u8, _, _ = key_bounds(c8, at8, al8, bh8, bl8, w.n)
+        u = np.minimum(det["ubar"][:P], u8[:P])
+        jb8 = np.minimum(bound_levels_f32(u, det["cb"], det["t"], w.r), res.J + 1)
+        jl = np.minimum(det["jl"], res.J + 1)
+        assert np.all(jb8 >= np.minimum(det["jbar"], res.J + 1))
+        assert np.all(jb8 <= jl)
+        L = min(int(res.level[h]), res.J)
+        kept4 += int((det["jbar"] <= L).sum())
+        kept8 += int((jb8 <= L).sum())
+    assert kept8 < kept4

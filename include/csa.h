@@ -226,7 +226,9 @@ csa_status csa_dense_decode_static(const csa_shape* shape, const void* q,
  *            value-row load of the gather)
  *   J1       largest J + 1 (row stride of jr_hist is J1 + 1)
  * With sub-batches the arrays above are those of sub-batch 0 (its first
- * sub_B sequences); sub-batch c's are sub_stride * c bytes further.
+ * sub_B sequences); sub-batch c's are sub_stride * c bytes further.  (While
+ * phase timing is enabled the step runs unsplit: its arrays are then where
+ * the map for sub_batches = 1 puts them.)
  *   total        workspace bytes (csa_workspace_size)
  *   sub_batches  sub-batches the step runs as
  *   sub_stride   bytes between sub-batch regions

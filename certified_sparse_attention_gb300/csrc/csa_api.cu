@@ -212,13 +212,27 @@ SubStreams* sub_streams() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   if (!g_sub.per_dev[dev]) {
-    SubStreams* ss = new SubStreams;
+    SubStreams* ss = new SubStreams{};
     bool ok = cudaEventCreateWithFlags(&ss->fork, cudaEventDisableTiming) == cudaSuccess;
+    int made = 0;
     for (int c = 0; c < kMaxSub && ok; ++c) {
-      ok = cudaStreamCreateWithFlags(&ss->st[c], cudaStreamNonBlocking) == cudaSuccess &&
-           cudaEventCreateWithFlags(&ss->join[c], cudaEventDisableTiming) == cudaSuccess;
+      ok = cudaStreamCreateWithFlags(&ss->st[c], cudaStreamNonBlocking) == cudaSuccess;
+      if (ok && cudaEventCreateWithFlags(&ss->join[c], cudaEventDisableTiming) != cudaSuccess) {
+        cudaStreamDestroy(ss->st[c]);
+        ok = false;
+      }
+      if (ok) ++made;
     }
-    if (!ok) return nullptr;
+    if (!ok) {
+      // release what was made; a later call tries again
+      for (int c = 0; c < made; ++c) {
+        cudaStreamDestroy(ss->st[c]);
+        cudaEventDestroy(ss->join[c]);
+      }
+      if (ss->fork) cudaEventDestroy(ss->fork);
+      delete ss;
+      return nullptr;
+    }
     g_sub.per_dev[dev] = ss;
   }
   return g_sub.per_dev[dev];

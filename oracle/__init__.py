@@ -23,7 +23,8 @@ multiply-add), with the operation order written out in ``bounds.py`` and
 Parity status per function (the pins live in ``tests/test_oracle_*.py``):
   * hashing / log2, quantiser, bounds, inclusion law, nestedness,
     unbiasedness, exact special cases, Chernoff / Bernstein events,
-    coverage: pinned (closed forms, brute force, Monte Carlo).
+    coverage, the Theorem 2 error bound and sample size: pinned (closed
+    forms, brute force, Monte Carlo).
   * which level stops and the exact o / beta values there: parity unpinned by
     the pages (they print no worked example); pinned only through the
     statistical and algebraic checks above.

@@ -36,6 +36,17 @@ below, in this order, separately for each query head h of the group (the
 10. keys_read = 64 + |exact-max set of the pool U {candidates with
     jbar_i <= j*}|;  values_read = 64 + |S(tau_j*)|.
 
+Optional 8-bit refinement ("Algorithm Components" 4: an 8-bit stage before
+the exact 16-bit reads; ``Params.refine8``): each candidate with
+jbar_i <= j* also gets the bound ubar8_i from 8-bit codes of the same blocks
+(``quantize_keys8``, query codes with QM8 levels), and the refined level
+jref_i = max(0, ceil(...)) of step 6 with min(ubar_i, ubar8_i) in place of
+ubar_i.  jbar_i <= jref_i <= j_i, so the sample, the estimates, the stop
+level and the outputs are unchanged; only keys_read shrinks, to 64 + |exact-
+max set U {candidates with jref_i <= j*}|, and the step also reads the 8-bit
+rows of the candidates with jbar_i <= j* outside the exact-max set
+(``rows8``).
+
 Test infrastructure only.
 """
 from __future__ import annotations
@@ -50,7 +61,7 @@ from .bounds import QM_DEFAULT, key_bounds, query_prep, inv_sqrt_d_f32
 from .certificate import MEASURE_VALUE, certificate_levels
 from .fp32 import tree_sum_f32
 from .hashing import head_stream, perturb_t
-from .quantize import T_BLOCK, quantize_keys, vmax_blocks
+from .quantize import T_BLOCK, quantize_keys, quantize_keys8, vmax_blocks
 
 F = np.float32
 WINDOW = 64
@@ -69,6 +80,8 @@ class Params:
     J_override: int = -1
     QM: int = QM_DEFAULT
     per_head: bool = False      # one perturbation draw per query head
+    refine8: bool = False       # 8-bit refinement before the bf16 reads
+    QM8: int = 2047             # query code range of the 8-bit bounds
 
 
 def grid_J(pool: int, r: int) -> int:
@@ -176,17 +189,20 @@ class GroupResult:
     n_near: np.ndarray         # [G] int (near-threshold keys at the stop)
     J: int
     detail: list               # per-head dict (levels, bounds, sets ...)
+    rows8: Optional[np.ndarray] = None   # [G] int: 8-bit rows read (refine8)
 
 
 def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
                         step_seed: int, g: int, p: Params,
                         quant: Optional[tuple] = None,
-                        keep_detail: bool = True) -> GroupResult:
+                        keep_detail: bool = True,
+                        quant8: Optional[tuple] = None) -> GroupResult:
     """Decode step for query heads q [G, d] of one KV group.
 
     K, V float32 [>= n, d] (exact values of the cache).  ``quant`` may pass a
     precomputed (codes, packed, mins, deltas, vmax) from the oracle's own
-    quantiser; otherwise it is computed here.
+    quantiser; otherwise it is computed here.  With ``p.refine8``, ``quant8``
+    may pass the (codes8, mins, deltas8) of ``quantize_keys8`` likewise.
     """
     q = np.asarray(q, np.float32)
     Gh, d = q.shape
@@ -206,6 +222,7 @@ def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
     out_vr = np.zeros(Gh, np.int64)
     out_nc = np.zeros(Gh, np.int64)
     out_near = np.zeros(Gh, np.int64)
+    out_r8 = np.zeros(Gh, np.int64) if p.refine8 else None
     details = []
     Kd = K.astype(np.float64)
     Vd = V.astype(np.float64)
@@ -218,7 +235,10 @@ def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
             out_vr[h] = n
             details.append({})
         return GroupResult(out_o, out_beta, out_lvl, out_kr, out_vr, out_nc,
-                           out_near, J, details)
+                           out_near, J, details, out_r8)
+    if p.refine8:
+        codes8, mins8, deltas8 = (quant8 if quant8 is not None
+                                  else quantize_keys8(K, n))
     delta_e = p.delta / (4.0 * (J + 1))
     nblk_pool = (pool + T_BLOCK - 1) // T_BLOCK
     Vmax = float(vmax[:nblk_pool].max())
@@ -242,6 +262,16 @@ def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
         cb = cstar_lower_f32(q[h], K[rows])
         # step 6: candidates
         jbar = bound_levels_f32(ubar[:pool], cb, t, p.r)
+        # optional 8-bit refinement: the level from the tighter of the two
+        # upper bounds (never below jbar, never above the exact level)
+        if p.refine8:
+            at8, al8, bh8, bl8 = query_prep(q[h], mins8, deltas8, p.QM8,
+                                            levels=255)
+            ubar8, _, _ = key_bounds(codes8, at8, al8, bh8, bl8, n)
+            jref = bound_levels_f32(np.minimum(ubar[:pool], ubar8[:pool]), cb,
+                                    t, p.r)
+        else:
+            ubar8, jref = None, jbar
         cand = jbar <= J
         # step 7: exact levels (all pool keys computed for the invariant
         # checks; only candidates enter the estimate)
@@ -268,7 +298,9 @@ def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
             out_o[h] = cert["o_hat"][js]
             out_beta[h] = cert["beta"][js]
             out_lvl[h] = js
-            rset = np.union1d(cset, np.nonzero(jbar <= js)[0])
+            rset = np.union1d(cset, np.nonzero(jref <= js)[0])
+            if p.refine8:
+                out_r8[h] = len(np.setdiff1d(np.nonzero(jbar <= js)[0], cset))
             out_kr[h] = WINDOW + len(rset)
             out_vr[h] = WINDOW + int((jl_c <= js).sum())
             xs = (sp - c_star) + t.astype(np.float64) * math.log(2.0)
@@ -284,6 +316,8 @@ def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
             out_lvl[h] = js
             out_kr[h] = n
             out_vr[h] = n
+            if p.refine8:
+                out_r8[h] = len(np.setdiff1d(np.nonzero(cand)[0], cset))
         out_nc[h] = int(cand.sum())
         if keep_detail:
             details.append({
@@ -294,8 +328,9 @@ def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
                 "hl_c": hl_c, "k": k, "D_B": D_B, "S2": S2,
                 "D_R": D_R, "N_R": N_R, "H_R": H_R, "Vmax": Vmax,
                 "delta_e": delta_e, "t": t, "alpha": alpha, "b_hi": b_hi,
-                "b_lo": b_lo, "at": at, "stop": js})
+                "b_lo": b_lo, "at": at, "stop": js, "ubar8": ubar8,
+                "jref": jref})
         else:
             details.append({"stop": js})
     return GroupResult(out_o, out_beta, out_lvl, out_kr, out_vr, out_nc,
-                       out_near, J, details)
+                       out_near, J, details, out_r8)

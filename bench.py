@@ -230,8 +230,8 @@ def clt_comparison(args, csa, w, shape, data, lens, seed_tab, nseed, plan,
 def decode_loop(args, csa, w, device, stream):
     """Whole-model decode: every token appends one row per layer and runs
     that layer's step, over `args.decode_layers` layers of the workload's
-    shape (picx.dev "Theoretical Contributions": fresh perturbations at
-    every decoding step).  Per layer and token: re-quantise the appended
+    shape (readsearch.ai "Abstract": new perturbation draws for each
+    decode step).  Per layer and token: re-quantise the appended
     token's block (csa_quantize_keys from that position), then the decode
     step with the grown length and a fresh seed.  The K, V rows of the
     appended tokens are generated with the cache; the loop extends the

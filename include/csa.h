@@ -6,12 +6,12 @@
  * "Methodology / Problem Setup" (scores s_i = q.k_i / sqrt(d), c* = max s_i,
  * w_i = exp(s_i - c*), o = sum w_i v_i / sum w_i) and "Algorithm Components"
  * 1-4 (window of the last 64 tokens read exactly; perturbations
- * E_i = -ln u_i from a 53-bit hash; threshold sample
+ * E_i = -ln u_i, u_i built from 53 hashed bits; threshold sample
  * S(tau) = {i in pool : s_i - c* + E_i >= log tau}; Horvitz-Thompson
  * estimates on the grid tau_j = 2^(-j/r); Chernoff / Hilbert-space Bernstein
- * certificate beta; stop at the first certified level; 4-bit scan with
+ * certificate beta; each head ends at its lowest certified level; 4-bit scan with
  * deterministic bounds shared across the GQA group), and the readsearch.ai
- * abstract page ("fresh perturbations at every decoding step").
+ * abstract page (the perturbations are drawn anew for each decode step).
  *
  * Conventions for every entry point:
  *  - Pointers named as device memory are device pointers owned by the

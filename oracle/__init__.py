@@ -5,8 +5,8 @@ This package is a plain, slow, independent restatement of the decode step of
 Sources, cited by page and section in every function:
   * picx.dev summary -- "Methodology / Problem Setup", "Algorithm Components"
     1-4, "Theoretical Contributions" (Theorems 1-4);
-  * readsearch.ai abstract page -- "Abstract" (GQA-shared scan, fresh
-    perturbations at every decoding step).
+  * readsearch.ai abstract page -- "Abstract" (one scan serves a GQA group;
+    the perturbations are drawn anew for each decode step).
 
 It shares no code with the CUDA library under
 ``certified_sparse_attention_gb300/``: no headers, kernels, helpers, constants

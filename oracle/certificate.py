@@ -32,7 +32,7 @@ Output bound (picx.dev, "Algorithm Components" 3):
     beta = (zeta + ||o_hat - c|| dD) / (D_hat - dD),  +inf if D_hat <= dD.
 It follows from o - o_hat = [(o_hat - c)(D_hat - D) - Z_c] / D.
 
-Certified (stopping rule, "stop at first certified level"), with the scale
+Certified (the stopping rule: a head ends at its lowest certified level), with the scale
 replaced by a lower confidence bound so the claim is relative to the truth:
     value  (||o_hat - o|| <= eps M):   beta <= eps * M_lo,
            M_lo = sqrt((H_R + H_B + H_lo) / D_hi), D_hi = D_RB + tau mu_hi;

@@ -1,8 +1,9 @@
 """Counter-hash perturbations E_i = -ln u_i.
 
-picx.dev summary, "Algorithm Components" 1: every pool key gets
-E_i = -ln u_i from a 53-bit uniform hash; readsearch.ai "Abstract": fresh
-perturbations at every decoding step, and one scan shared by a GQA group.
+picx.dev summary, "Algorithm Components" 1: each pool key's perturbation is
+E_i = -ln u_i with u_i a uniform number made from 53 hashed bits;
+readsearch.ai "Abstract": the draws are new at each decode step, and a GQA
+group shares one scan.
 
 The hash is SplitMix64 (Steele, Lea & Flood, "Fast splittable pseudorandom
 number generators", OOPSLA 2014; constants of Vigna's splitmix64.c): the

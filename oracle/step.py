@@ -12,11 +12,11 @@ below, in this order, separately for each query head h of the group (the
  2. 4-bit bounds ubar_i >= s_i >= l_i for every key (``bounds.py``);
     c*_lo = max_i l_i.
  3. Exact maximum: c* = max of s_i over R and the pool keys with
-    ubar_i >= c*_lo ("exact maximum computation").
+    ubar_i >= c*_lo (the exact-maximum step of "Algorithm Components" 4).
  4. Perturbations t_i = -log2 u_i (``hashing.py``).
  5. Grid tau_j = 2^(-j/r), j = 0..J with J = ceil(r log2 |P|) (tau_J <= 1/|P|),
     budget delta_e = delta / (4 (J+1)) per confidence event.
- 6. Candidates ("bucketed by earliest possible inclusion level"): the bound
+ 6. Candidates, grouped by the lowest level that could include them: the bound
     level jbar_i = max(0, ceil(-r xbar_i)) with
         xbar_i = fl(fl(fl(ubar_i - cb) * log2e) + t_i)   (float32),
         jbar_i = max(0, ceil(fl(fl(-r * xbar_i) - 2^-10))),

@@ -1,4 +1,4 @@
-"""Pins for Theorem 2 ("Sample size independent of context").
+"""Pins for Theorem 2 (the sample size it needs does not grow with n).
 
 picx.dev summary, "Theoretical Contributions", Theorem 2: with the
 threshold set to tau = D/m, the estimate is within

@@ -1,8 +1,9 @@
 """Pins for perturbed threshold sampling and the Horvitz-Thompson estimates.
 
-picx.dev summary, "Theoretical Foundation": s_i - c* + E_i >= log tau holds
-with probability min(1, w_i / tau) (Poisson PPS sampling), lowering tau adds
-keys (nested samples), and the Horvitz-Thompson estimates are unbiased
+picx.dev summary, "Theoretical Foundation": key i passes the perturbed
+threshold s_i - c* + E_i >= log tau with probability min(1, w_i / tau)
+(threshold PPS sampling), a lower tau only adds keys (the samples nest),
+and the Horvitz-Thompson estimates are unbiased
 (Theorem 1: E D_hat = D, E N_hat = N, Var D_hat <= tau D_A).  These tests run
 the oracle's own level and sum routines over many step seeds.
 """

@@ -29,6 +29,9 @@ CASES = [
      {"measure": 3}),
     ("llama_g2_n700_perhead", "llama16k", {"Hq": 8, "Hkv": 2}, 700, 0, 12345,
      {"per_head": True}),
+    # the 8-bit refinement option (changes keys_read only)
+    ("llama_g2_n700_refine8", "llama16k", {"Hq": 8, "Hkv": 2}, 700, 0, 12345,
+     {"refine8": True}),
 ]
 
 
@@ -46,6 +49,9 @@ def run_case(wname, over, n, step, seed, pover=None):
                                   V[0, g], n, seed, g,
                                   Params(w.eps, w.delta, w.r, **(pover or {})))
         for h, det in enumerate(res.detail):
+            extra = ({"rows8": int(res.rows8[h]),
+                      "jref_sha": _digest(det["jref"].astype(np.int64))}
+                     if res.rows8 is not None else {})
             out.append({
                 "g": g, "h": h, "J": res.J,
                 "o": [float(x) for x in res.o[h]],
@@ -57,6 +63,7 @@ def run_case(wname, over, n, step, seed, pover=None):
                 "cb": float(det["cb"]),
                 "jbar_sha": _digest(det["jbar"].astype(np.int64)),
                 "ubar_sha": _digest(det["ubar"].astype(np.float32)),
+                **extra,
             })
     return out
 

@@ -27,5 +27,7 @@ def test_oracle_matches_fixture(case):
         for key in ("J", "level", "keys_read", "values_read", "n_candidates",
                     "c_lo", "c_hi", "cb", "jbar_sha", "ubar_sha"):
             assert a[key] == b[key], key
+        for key in ("rows8", "jref_sha"):
+            assert a.get(key) == b.get(key), key
         assert np.allclose(a["o"], b["o"], rtol=1e-12, atol=1e-12)
         assert a["beta"] == pytest.approx(b["beta"], rel=1e-12, abs=1e-12)

@@ -137,3 +137,47 @@ def test_plain_c_caller_builds(lib, tmp_path):
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     assert out.exists()
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    # the ctypes mirrors of the header's structs have the C compiler's size
+    # and field offsets (a plain C program built against include/csa.h
+    # prints them; a field the binding lacks would change the size or an
+    # offset), and the phase names match CSA_NPHASE
+    import shutil
+    import subprocess
+    cc = shutil.which("cc") or shutil.which("gcc")
+    if not cc:
+        pytest.skip("no C compiler")
+    structs = (csa.csa_shape, csa.csa_params, csa.csa_head_stats,
+               csa.csa_workspace_map, csa.csa_phase_times)
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "csa.h"',
+             "int main(void) {"]
+    for st in structs:
+        nm = st.__name__
+        lines.append(f'  printf("{nm} sizeof %zu\\n", sizeof({nm}));')
+        for f, _ in st._fields_:
+            lines.append(f'  printf("{nm} {f} %zu\\n", offsetof({nm}, {f}));')
+    lines += ['  printf("CSA_NPHASE value %d\\n", CSA_NPHASE);', "  return 0;",
+              "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I",
+                        os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    got = {}
+    for ln in subprocess.run([str(exe)], capture_output=True, text=True,
+                             check=True).stdout.split("\n"):
+        if ln:
+            a, b, c = ln.split()
+            got[(a, b)] = int(c)
+    for st in structs:
+        nm = st.__name__
+        assert got[(nm, "sizeof")] == ctypes.sizeof(st), nm
+        for f, _ in st._fields_:
+            assert got[(nm, f)] == getattr(st, f).offset, (nm, f)
+    assert len(csa.PHASES) == got[("CSA_NPHASE", "value")]
+    assert ctypes.sizeof(csa.csa_phase_times._fields_[0][1]) == \
+        4 * len(csa.PHASES)

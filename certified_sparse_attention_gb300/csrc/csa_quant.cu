@@ -1,7 +1,7 @@
 // 4-bit per-block, per-channel key quantiser and per-block value-norm bound.
 //
-// picx.dev summary, "Algorithm Components" 4: 4-bit per-block per-channel
-// quantisation of the keys (as in KIVI).  Per 64-token block (aligned to
+// picx.dev summary, "Algorithm Components" 4: keys quantised to 4 bits per
+// block and channel, the KIVI scheme.  Per 64-token block (aligned to
 // position 0, the tokens present only) and channel c:
 //   m_c = min, Delta_c = fl((max - min) / 15) (0 -> 1),
 //   code = clamp(rint(fl(fl(k - m_c) / Delta_c)), 0, 15)   (ties to even),

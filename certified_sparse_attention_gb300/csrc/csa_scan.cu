@@ -1,9 +1,9 @@
 // 4-bit key scan with deterministic score bounds, shared by a GQA group.
 //
-// picx.dev summary, "Algorithm Components" 4: a 4-bit per-block per-channel
-// quantisation gives deterministic upper bounds u_i >= s_i for every score;
-// readsearch.ai "Abstract": the scan is shared across the GQA group and reads
-// every key.  One CTA scans a tile of 256 keys (four 64-token blocks) of one
+// picx.dev summary, "Algorithm Components" 4: the keys' 4-bit codes (per
+// block and channel) bound every score from above, deterministically
+// (u_i >= s_i); readsearch.ai "Abstract": one scan over every key serves
+// the whole GQA group.  One CTA scans a tile of 256 keys (four 64-token blocks) of one
 // (sequence, KV head) for all G query heads:
 //   1. the packed codes (256 x d/2 bytes) and the four blocks' (m_c, Delta_c)
 //      are staged in shared memory with cp.async;

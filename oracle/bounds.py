@@ -27,7 +27,10 @@ Why it bounds s_i: k_ic = m_c + code_ic Delta_c + e_ic with
 |e_ic| <= Delta_c (1/2 + 2^-16), and sum_c a_c code_c = alpha I_i +
 sum_c r_c code_c with 0 <= code <= 15; every float32 rounding above is at most
 2^-24 relative to a quantity bounded by Q1 * Kabs, far inside marg.
-QM = 127 (int8 codes, as for the pages' u8 x s8 dot products).
+QM = 127 (int8 codes, as for the pages' u8 x s8 dot products).  Option:
+two-digit codes, QM = QM_TWO_DIGIT = 127 * 257 (at = 256 hi + lo, two s8
+digits), with both residual terms replaced by the closed form
+fl(fl(15 d) * fl(alpha * (1/2 + 2^-6))) (see ``query_prep``).
 Test infrastructure only.
 """
 from __future__ import annotations
@@ -40,6 +43,9 @@ from .fp32 import tree_sum_f32
 
 F = np.float32
 QM_DEFAULT = 127
+# two signed 8-bit digits per query code: at = 256 hi + lo, |hi|, |lo| <= 127
+QM_TWO_DIGIT = 127 * 257
+_RES_HALF = F(0.5 + 2.0 ** -6)
 _RHO = F(0.5 + 2.0 ** -16)
 _MARG = F(2.0 ** -14)
 
@@ -49,7 +55,8 @@ def inv_sqrt_d_f32(d: int) -> np.float32:
 
 
 def query_prep(q: np.ndarray, mins: np.ndarray, deltas: np.ndarray,
-               QM: int = QM_DEFAULT, levels: int = 15):
+               QM: int = QM_DEFAULT, levels: int = 15,
+               closed_residual: bool = False):
     """Per-block query code for one query head.
 
     q float32 [d]; mins, deltas float32 [nblk, d]; `levels` the largest key
@@ -57,9 +64,16 @@ def query_prep(q: np.ndarray, mins: np.ndarray, deltas: np.ndarray,
     bound is the same construction with 15 -> 255 and 16 -> 256, best with
     a finer query code, QM = 2047: with QM = 127 the query residual term
     levels * sum |r_c| outweighs the 8-bit keys' rounding slack).
+    With ``closed_residual`` the two residual trees give way to a closed
+    form, meant for fine query codes (QM_TWO_DIGIT): a_c - alpha at_c is
+    within 1/2 + 2^-6 of alpha per channel (rint's half step, plus the
+    float32 roundings of inv, a_c inv and alpha, each at most QM 2^-23
+    relative to alpha), so both residual terms are replaced by
+    fl(fl(levels d) * fl(alpha * (1/2 + 2^-6))).
     Returns (at int32 [nblk, d], alpha f32 [nblk], b_hi f32 [nblk],
     b_lo f32 [nblk]).
     """
+    assert not closed_residual or QM <= QM_TWO_DIGIT
     q = np.asarray(q, dtype=np.float32)
     d = q.shape[0]
     qt = q * inv_sqrt_d_f32(d)
@@ -70,14 +84,19 @@ def query_prep(q: np.ndarray, mins: np.ndarray, deltas: np.ndarray,
     alpha = np.where(pos, safe / F(QM), F(0.0)).astype(np.float32)
     inv = np.where(pos, F(QM) / safe, F(0.0)).astype(np.float32)
     at = np.clip(np.rint(a * inv[:, None]), -QM, QM).astype(np.float32)
-    r = a - alpha[:, None] * at
     Bq = tree_sum_f32(qt[None, :] * mins)
     A1 = tree_sum_f32(np.abs(a))
-    Rp = tree_sum_f32(np.maximum(r, F(0.0)))
-    Rn = tree_sum_f32(np.maximum(-r, F(0.0)))
     sk = A1 * _RHO
-    hi = sk + F(levels) * Rp
-    lo = sk + F(levels) * Rn
+    if closed_residual:
+        res = F(levels * d) * (alpha * _RES_HALF)
+        hi = sk + res
+        lo = sk + res
+    else:
+        r = a - alpha[:, None] * at
+        Rp = tree_sum_f32(np.maximum(r, F(0.0)))
+        Rn = tree_sum_f32(np.maximum(-r, F(0.0)))
+        hi = sk + F(levels) * Rp
+        lo = sk + F(levels) * Rn
     Q1 = tree_sum_f32(np.abs(qt))
     Kabs = (np.abs(mins) + F(levels + 1) * deltas).max(axis=1)
     mag = ((Q1 * Kabs) + hi) + lo
@@ -96,7 +115,9 @@ def key_bounds(codes: np.ndarray, at: np.ndarray, alpha: np.ndarray,
     blk = np.arange(n) // T
     I = np.einsum("nd,nd->n", codes[:n].astype(np.int64),
                   at[blk].astype(np.int64))
-    aI = alpha[blk] * I.astype(np.float32)     # |I| < 2^24: exact in float32
+    # |I| < 2^24 with int8 query codes, so I converts exactly; with
+    # two-digit codes it may round (to nearest even), which the margin covers
+    aI = alpha[blk] * I.astype(np.float32)
     ubar = aI + b_hi[blk]
     low = aI + b_lo[blk]
     return ubar.astype(np.float32), low.astype(np.float32), I

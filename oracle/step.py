@@ -9,8 +9,9 @@ below, in this order, separately for each query head h of the group (the
 
  1. Window R = the last 64 positions, read exactly; pool P = the rest.
     With |P| = 0 the step is dense attention (beta = 0, level 0).
- 2. 4-bit bounds ubar_i >= s_i >= l_i for every key (``bounds.py``);
-    c*_lo = max_i l_i.
+ 2. 4-bit bounds ubar_i >= s_i >= l_i for every key (``bounds.py``; int8
+    query codes, or two-digit codes with ``Params.two_digit``: the bounds
+    change, the results below do not); c*_lo = max_i l_i.
  3. Exact maximum: c* = max of s_i over R and the pool keys with
     ubar_i >= c*_lo (the exact-maximum step of "Algorithm Components" 4).
  4. Perturbations t_i = -log2 u_i (``hashing.py``).
@@ -57,7 +58,8 @@ from typing import Optional
 
 import numpy as np
 
-from .bounds import QM_DEFAULT, key_bounds, query_prep, inv_sqrt_d_f32
+from .bounds import (QM_DEFAULT, QM_TWO_DIGIT, key_bounds, query_prep,
+                     inv_sqrt_d_f32)
 from .certificate import MEASURE_VALUE, certificate_levels
 from .fp32 import tree_sum_f32
 from .hashing import head_stream, perturb_t
@@ -80,6 +82,8 @@ class Params:
     J_override: int = -1
     QM: int = QM_DEFAULT
     per_head: bool = False      # one perturbation draw per query head
+    two_digit: bool = False     # query codes of two s8 digits (QM_TWO_DIGIT)
+                                # with the closed-form residual term
     refine8: bool = False       # 8-bit refinement before the bf16 reads
     QM8: int = 2047             # query code range of the 8-bit bounds
 
@@ -251,7 +255,12 @@ def oracle_decode_group(q: np.ndarray, K: np.ndarray, V: np.ndarray, n: int,
         t = (perturb_t(step_seed, head_stream(g, Gh, h), np.arange(pool))
              if p.per_head else t_shared)                  # float32 [pool]
         # step 2: bounds
-        at, alpha, b_hi, b_lo = query_prep(q[h], mins, deltas, p.QM)
+        if p.two_digit:
+            at, alpha, b_hi, b_lo = query_prep(q[h], mins, deltas,
+                                               QM_TWO_DIGIT,
+                                               closed_residual=True)
+        else:
+            at, alpha, b_hi, b_lo = query_prep(q[h], mins, deltas, p.QM)
         ubar, low, _ = key_bounds(codes, at, alpha, b_hi, b_lo, n)
         c_lo = F(low.max())
         # step 3: exact maximum over R and {ubar >= c*_lo}

@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import certified_sparse_attention_gb300 as csa
@@ -181,3 +182,40 @@ def test_binding_structs_match_the_header(tmp_path):
     assert len(csa.PHASES) == got[("CSA_NPHASE", "value")]
     assert ctypes.sizeof(csa.csa_phase_times._fields_[0][1]) == \
         4 * len(csa.PHASES)
+
+
+def test_workspace_layout_properties(lib):
+    # over many shapes and parameters: the documented arrays lie inside
+    # their sub-batch region, 256-byte aligned and disjoint; the regions
+    # fit in the reported size; the sub-batches cover the batch; J1 is the
+    # grid of the longest sequence
+    from oracle.step import grid_J
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        G = int(rng.choice([1, 2, 4, 8]))
+        Hkv = int(rng.integers(1, 9))
+        d = int(rng.choice([64, 128]))
+        B = int(rng.choice([1, 2, 3, 4, 7, 32, 128]))
+        n = int(rng.choice([1, 63, 64, 65, 100, 1000, 4096, 131072, 1 << 20]))
+        r = int(rng.integers(1, 5))
+        p = csa.make_params(0.05, 0.05, r, int(rng.integers(0, 4)), -1,
+                            int(rng.integers(0, 5)), int(rng.integers(0, 2)))
+        s = csa.make_shape(B, G * Hkv, Hkv, d, n, "bf16")
+        m = csa.csa_workspace_layout(s, p)
+        assert csa.csa_workspace_size(s, p) == m.total > 0
+        assert 1 <= m.sub_batches <= 4 and m.sub_B >= 1
+        assert m.sub_B * m.sub_batches >= B > (m.sub_batches - 1) * m.sub_B
+        region = m.sub_stride if m.sub_batches > 1 else m.total
+        assert m.sub_batches * m.sub_stride <= m.total or m.sub_batches == 1
+        assert m.J1 == grid_J(max(n - 64, 0), r) + 1
+        Bs, Hq = m.sub_B, G * Hkv
+        pcap = max(n - 64, 1)
+        arrays = [(m.ubar, Bs * Hkv * n * G * 4), (m.cmax, Bs * Hq * 16),
+                  (m.s32, Bs * Hkv * pcap * G * 4),
+                  (m.jr_hist, Bs * Hq * (m.J1 + 1) * 4),
+                  (m.bcnt, Bs * Hkv * m.J1 * 4)]
+        for off, size in arrays:
+            assert off % 256 == 0 and off + size <= region, (off, size, region)
+        arrays.sort()
+        for (o1, s1), (o2, _) in zip(arrays, arrays[1:]):
+            assert o1 + s1 <= o2

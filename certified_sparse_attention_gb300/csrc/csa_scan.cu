@@ -3,16 +3,17 @@
 // picx.dev summary, "Algorithm Components" 4: the keys' 4-bit codes (per
 // block and channel) bound every score from above, deterministically
 // (u_i >= s_i); readsearch.ai "Abstract": one scan over every key serves
-// the whole GQA group.  One CTA scans a tile of 256 keys (four 64-token blocks) of one
-// (sequence, KV head) for all G query heads:
+// the whole GQA group.  One CTA scans a tile of 256 keys (four 64-token
+// blocks) of one (sequence, KV head) for all G query heads:
 //   1. the packed codes (256 x d/2 bytes) and the four blocks' (m_c, Delta_c)
 //      are staged in shared memory with cp.async;
 //   2. per (block, head) the query is coded to int8 with a residual and a
 //      key-rounding slack (16 threads per (block, head), adjacent-pair float32
 //      trees over the channels);
-//   3. per key, int8 x u4 dot products (dp4a: low nibbles as bytes, high
-//      nibbles as 16 x byte) give the exact integer I, and
-//      ubar = fl(fl(alpha I) + b_hi), l = fl(fl(alpha I) + b_lo);
+//   3. per key, the exact integer dot product I of the 4-bit codes with the
+//      int8 query code comes from u8 x s8 tensor-core products (mma.sync
+//      m16n8k32: 16 keys x heads x 32 channels, low and high nibbles as
+//      bytes), and ubar = fl(fl(alpha I) + b_hi), l = fl(fl(alpha I) + b_lo);
 //   4. ubar is stored key-major with the G heads interleaved, and the per-head
 //      maxima of l (c*_lo) and ubar are folded into global atomics.
 #include "csa_args.cuh"

@@ -66,12 +66,19 @@ def test_residual_within_closed_form():
         deltas = rng.lognormal(-2, 1.5, (4, d)).astype(F)
         mins = rng.standard_normal((4, d)).astype(F)
         _residual_ok(q, mins, deltas)
-    # ties: values whose scaled code lands on a half step, and the largest
-    # |a_c| itself (the clamp)
+    # exact ties: with amax = QM / 1024, inv = 1024 and alpha = 2^-10
+    # exactly, so a_c = (k + 1/2) / 1024 scales to a half step and rint
+    # leaves a residual of exactly alpha / 2; the first channel is amax
+    # itself (the clamp)
     d = 64
     deltas = np.ones((1, d), F)
-    q = (np.arange(d, dtype=F) - 31.5) * F(8.0)
-    _residual_ok(q, np.zeros((1, d), F), deltas)
+    a = (np.arange(d, dtype=np.float64) * 97.0 - 3000.0 + 0.5) / 1024.0
+    a[0] = QM_TWO_DIGIT / 1024.0
+    q = (a * 8.0).astype(F)               # qt = q / sqrt(64) = a exactly
+    at, alpha = _residual_ok(q, np.zeros((1, d), F), deltas)
+    assert alpha[0] == F(2.0 ** -10) and at[0, 0] == QM_TWO_DIGIT
+    r = a[1:] - float(alpha[0]) * at[0, 1:]
+    assert np.all(np.abs(r) == 2.0 ** -11)
     q = np.zeros(d, F)
     q[0] = 1.0
     q[1] = -1.0

@@ -290,6 +290,44 @@ def meta_buffers(shape: csa_shape, device) -> KVMeta:
     return KVMeta(K4, bounds, vmax, vnorm2)
 
 
+def _require(t, name: str, nbytes: int) -> None:
+    """Refuse a tensor the kernels would read from host memory or past its
+    end: it must be a contiguous CUDA tensor of at least ``nbytes``."""
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name}: a CUDA tensor is required")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: the tensor must be contiguous")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name}: {have} bytes, the shape needs {nbytes}")
+
+
+def _check_batch(shape: csa_shape, lens, seeds=None) -> None:
+    if len(lens) != shape.B:
+        raise ValueError(f"lens: {len(lens)} entries for B = {shape.B}")
+    if seeds is not None and len(seeds) != shape.B:
+        raise ValueError(f"seeds: {len(seeds)} entries for B = {shape.B}")
+
+
+def check_step_inputs(shape: csa_shape, q, K, V, meta=None, lens=(),
+                      seeds=None) -> None:
+    """Host-side checks of the tensors and host arrays a decode step (or,
+    without ``meta``, a dense decode) reads: the layouts of include/csa.h,
+    on the device, contiguous and large enough.  Raises ValueError."""
+    B, Hq, Hkv, d, n = shape.B, shape.Hq, shape.Hkv, shape.d, shape.n_max
+    esz = 4 if shape.dtype == CSA_F32 else 2
+    nblk = (n + BLOCK - 1) // BLOCK
+    _check_batch(shape, lens, seeds)
+    _require(q, "q", B * Hq * d * esz)
+    _require(K, "K", B * Hkv * n * d * esz)
+    _require(V, "V", B * Hkv * n * d * esz)
+    if meta is not None:
+        _require(meta.K4, "K4", B * Hkv * nblk * BLOCK * (d // 2))
+        _require(meta.bounds, "bounds", B * Hkv * nblk * 2 * d * 4)
+        _require(meta.vmax, "vmax", B * Hkv * nblk * 4)
+        _require(meta.vnorm2, "vnorm2", B * Hkv * n * 4)
+
+
 class DecodeStep:
     """Owns the workspace and output buffers of csa_decode_step for one
     shape and parameter set; ``__call__`` runs one step on the current
@@ -314,6 +352,7 @@ class DecodeStep:
                                   device=device) if with_stats else None)
 
     def __call__(self, q, K, V, meta: KVMeta, lens, seeds, stream=None):
+        check_step_inputs(self.shape, q, K, V, meta, lens, seeds)
         st = csa_decode_step(self.shape, self.params, q, K, V, meta.K4,
                              meta.bounds, meta.vmax, meta.vnorm2, lens, seeds,
                              self.o, self.beta,
@@ -336,6 +375,7 @@ class DenseDecode:
                              dtype=torch.float32, device=device)
 
     def __call__(self, q, K, V, lens, stream=None):
+        check_step_inputs(self.shape, q, K, V, None, lens)
         check(csa_dense_decode(self.shape, q, K, V, lens, self.o, self.ws,
                                self.ws_bytes, stream), "csa_dense_decode")
         return self.o

@@ -219,3 +219,60 @@ def test_workspace_layout_properties(lib):
         arrays.sort()
         for (o1, s1), (o2, _) in zip(arrays, arrays[1:]):
             assert o1 + s1 <= o2
+
+
+class _FakeDev:
+    """Stands in for a CUDA tensor in host-only checks."""
+
+    def __init__(self, nbytes, esz=2, contiguous=True, cuda=True):
+        self.n, self.esz = nbytes // esz, esz
+        self.contig, self.is_cuda = contiguous, cuda
+
+    def numel(self):
+        return self.n
+
+    def element_size(self):
+        return self.esz
+
+    def is_contiguous(self):
+        return self.contig
+
+
+def test_step_inputs_checked_before_the_call():
+    # the tensor wrappers refuse what the kernels would read past its end or
+    # from host memory, and host arrays of the wrong length, before calling
+    # the library
+    B, Hq, Hkv, d, n = 2, 8, 2, 128, 1000
+    s = csa.make_shape(B, Hq, Hkv, d, n, "bf16")
+    nblk = (n + 63) // 64
+    ok = dict(q=_FakeDev(B * Hq * d * 2), K=_FakeDev(B * Hkv * n * d * 2),
+              V=_FakeDev(B * Hkv * n * d * 2))
+    meta = csa.KVMeta(_FakeDev(B * Hkv * nblk * 64 * d // 2, 1),
+                      _FakeDev(B * Hkv * nblk * 2 * d * 4, 4),
+                      _FakeDev(B * Hkv * nblk * 4, 4),
+                      _FakeDev(B * Hkv * n * 4, 4))
+    csa.check_step_inputs(s, ok["q"], ok["K"], ok["V"], meta, [n, n], [1, 2])
+    csa.check_step_inputs(s, ok["q"], ok["K"], ok["V"], None, [n, n])
+    bad = [
+        dict(lens=[n]),                                   # one length short
+        dict(seeds=[1, 2, 3]),
+        dict(K=_FakeDev(B * Hkv * n * d * 2 - 2)),        # one element short
+        dict(q=_FakeDev(B * Hq * d * 2, contiguous=False)),
+        dict(V=_FakeDev(B * Hkv * n * d * 2, cuda=False)),
+        dict(meta=meta._replace(vnorm2=_FakeDev(B * Hkv * n * 2, 4))),
+    ]
+    for over in bad:
+        args = dict(q=ok["q"], K=ok["K"], V=ok["V"], meta=meta, lens=[n, n],
+                    seeds=[1, 2])
+        args.update(over)
+        with pytest.raises(ValueError):
+            csa.check_step_inputs(s, **args)
+    # an f32 shape needs four bytes per element: bf16-sized tensors fail
+    s32 = csa.make_shape(B, Hq, Hkv, d, n, "f32")
+    with pytest.raises(ValueError):
+        csa.check_step_inputs(s32, ok["q"], ok["K"], ok["V"], None, [n, n])
+    # a host tensor is refused
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):
+        csa.check_step_inputs(s, torch.zeros(B, Hq, d, dtype=torch.bfloat16),
+                              ok["K"], ok["V"], None, [n, n])

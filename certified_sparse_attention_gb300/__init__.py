@@ -214,6 +214,7 @@ def decode_ordered(u):
 
 def csa_quantize_keys(shape, K, V, lens, from_token, K4, bounds, vmax,
                       vnorm2, stream=None) -> int:
+    _check_batch(shape, lens)
     return load_library().csa_quantize_keys(
         ctypes.byref(shape), _ptr(K), _ptr(V), _i64(lens), int(from_token),
         _ptr(K4), _ptr(bounds), _ptr(vmax), _ptr(vnorm2), _stream(stream))
@@ -222,6 +223,7 @@ def csa_quantize_keys(shape, K, V, lens, from_token, K4, bounds, vmax,
 def csa_decode_step(shape, params, q, K, V, K4, bounds, vmax, vnorm2, lens,
                     seeds, o, beta, level, keys_read, stats, workspace,
                     workspace_bytes, stream=None) -> int:
+    _check_batch(shape, lens, seeds)
     return load_library().csa_decode_step(
         ctypes.byref(shape), ctypes.byref(params), _ptr(q), _ptr(K), _ptr(V),
         _ptr(K4), _ptr(bounds), _ptr(vmax), _ptr(vnorm2), _i64(lens),
@@ -232,12 +234,14 @@ def csa_decode_step(shape, params, q, K, V, K4, bounds, vmax, vnorm2, lens,
 
 def csa_dense_decode(shape, q, K, V, lens, o, workspace, workspace_bytes,
                      stream=None) -> int:
+    _check_batch(shape, lens)
     return load_library().csa_dense_decode(
         ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V), _i64(lens), _ptr(o),
         _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def csa_dense_decode_static(shape, q, K, V, lens, o, stream=None) -> int:
+    _check_batch(shape, lens)
     return load_library().csa_dense_decode_static(
         ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V), _i64(lens), _ptr(o),
         _stream(stream))

@@ -276,3 +276,19 @@ def test_step_inputs_checked_before_the_call():
     with pytest.raises(ValueError):
         csa.check_step_inputs(s, torch.zeros(B, Hq, d, dtype=torch.bfloat16),
                               ok["K"], ok["V"], None, [n, n])
+
+
+def test_host_arrays_checked_in_the_low_level_wrappers(lib):
+    # lens / seeds with other than B entries would make the library read
+    # past a host array: the wrappers refuse them before the call
+    s = csa.make_shape(2, 8, 2, 128, 4096, "bf16")
+    p = csa.make_params()
+    with pytest.raises(ValueError):
+        csa.csa_quantize_keys(s, 1, 1, [100], 0, 1, 1, 1, 1, stream=0)
+    with pytest.raises(ValueError):
+        csa.csa_decode_step(s, p, 1, 1, 1, 1, 1, 1, 1, [100, 100], [1],
+                            1, 1, 1, 1, None, 1, 1 << 20, stream=0)
+    with pytest.raises(ValueError):
+        csa.csa_dense_decode(s, 1, 1, 1, [1, 2, 3], 1, 1, 1 << 20, stream=0)
+    with pytest.raises(ValueError):
+        csa.csa_dense_decode_static(s, 1, 1, 1, [1], 1, stream=0)

@@ -9,8 +9,8 @@
  * E_i = -ln u_i, u_i built from 53 hashed bits; threshold sample
  * S(tau) = {i in pool : s_i - c* + E_i >= log tau}; Horvitz-Thompson
  * estimates on the grid tau_j = 2^(-j/r); Chernoff / Hilbert-space Bernstein
- * certificate beta; each head ends at its lowest certified level; 4-bit scan with
- * deterministic bounds shared across the GQA group), and the readsearch.ai
+ * certificate beta; each head ends at its lowest certified level; one
+ * 4-bit scan per GQA group bounding every score), and the readsearch.ai
  * abstract page (the perturbations are drawn anew for each decode step).
  *
  * Conventions for every entry point:

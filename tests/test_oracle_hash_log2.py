@@ -1,7 +1,7 @@
 """Pins for the oracle's perturbation source (hash, uniform, own log2).
 
-picx.dev summary, "Algorithm Components" 1: E_i = -ln u_i from a 53-bit
-uniform hash.  The hash is SplitMix64; its published output vectors pin the
+picx.dev summary, "Algorithm Components" 1: E_i = -ln u_i, with u_i a
+uniform number built from 53 hashed bits.  The hash is SplitMix64; its published output vectors pin the
 implementation, and distribution tests pin u ~ U(0,1], E ~ Exp(1).
 """
 import numpy as np

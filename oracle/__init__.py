@@ -27,7 +27,9 @@ Parity status per function (the pins live in ``tests/test_oracle_*.py``):
     forms, brute force, Monte Carlo).
   * which level stops and the exact o / beta values there: parity unpinned by
     the pages (they print no worked example); pinned only through the
-    statistical and algebraic checks above.
+    statistical and algebraic checks above and metamorphic relations
+    between runs (monotone in eps and delta, homogeneous in the values,
+    invariant to a common score shift).
 """
 from .fp32 import tree_sum_f32, log2_m53_f32
 from .hashing import mix64, group_key, key_hashes, perturb_t

@@ -11,7 +11,9 @@ properties the method must have; picx.dev summary, "Problem Setup" and
   value scale, the output norm and the value bound all scale with v);
 * adding the same amount to every score (keys shifted along a direction the
   query sees as a constant) changes the 4-bit bounds and the candidates but
-  not the weights w_i = exp(s_i - c*), hence not the result.
+  not the weights w_i = exp(s_i - c*), hence not the result;
+* with the group's shared draw, permuting a group's query heads permutes
+  their results.
 """
 import numpy as np
 import pytest
@@ -98,3 +100,19 @@ def test_common_score_shift_changes_no_result():
         assert np.allclose(b.o, a.o, rtol=1e-9, atol=1e-12)
         assert np.allclose(b.beta, a.beta, rtol=1e-9, atol=1e-12)
         assert np.array_equal(a.values_read, b.values_read)
+
+
+def test_permuting_query_heads_permutes_results():
+    # with the group's shared draw, a head's result depends on its own query
+    # only: reversing the heads of a group reverses the outputs exactly
+    w, K, V, q, seed = _group()
+    G = w.G
+    for g in range(w.Hkv):
+        a = _run(w, K, V, q, seed, g)
+        qr = q.copy()
+        qr[0, g * G:(g + 1) * G] = q[0, g * G:(g + 1) * G][::-1]
+        b = _run(w, K, V, qr, seed, g)
+        assert np.array_equal(a.o[::-1], b.o)
+        assert np.array_equal(a.beta[::-1], b.beta)
+        assert np.array_equal(a.level[::-1], b.level)
+        assert np.array_equal(a.keys_read[::-1], b.keys_read)

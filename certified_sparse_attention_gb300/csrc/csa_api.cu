@@ -3,6 +3,7 @@
 // launch sequence of one decode step.  No device memory is allocated here.
 #include <algorithm>
 #include <cmath>
+#include <cuda.h>
 #include <mutex>
 #include <cstring>
 
@@ -25,9 +26,13 @@ int grid_J(int64_t P, int r) {
   return j;
 }
 
+// Head counts are capped so that no workspace size can overflow size_t
+// (the largest region, B Hkv (J+1) |pool| 8 bytes, stays below 2^60 with
+// B <= 128, Hkv <= 1024, J + 1 <= 256 and n_max <= 2^31).
 bool shape_ok(const csa_shape* s) {
-  return s && s->B >= 1 && s->Hq >= 1 && s->Hkv >= 1 && s->Hq % s->Hkv == 0 && s->n_max >= 1 &&
-         s->n_max <= (int64_t)1 << 31 && (s->dtype == CSA_BF16 || s->dtype == CSA_F32);
+  return s && s->B >= 1 && s->Hq >= 1 && s->Hkv >= 1 && s->Hq <= kMaxHeads && s->Hkv <= kMaxHeads &&
+         s->Hq % s->Hkv == 0 && s->n_max >= 1 && s->n_max <= (int64_t)1 << 31 &&
+         (s->dtype == CSA_BF16 || s->dtype == CSA_F32);
 }
 csa_status shape_supported(const csa_shape* s) {
   const int G = s->Hq / s->Hkv;
@@ -199,6 +204,7 @@ bool sub_plan(const csa_shape* s, const csa_params* p, SubPlan& sp) {
 struct SubStreams {
   cudaStream_t st[kMaxSub];
   cudaEvent_t fork, join[kMaxSub];
+  unsigned long long ctx;   // context the streams belong to
 };
 struct SubState {
   std::mutex mu;
@@ -211,8 +217,16 @@ SubState g_sub;
 SubStreams* sub_streams() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  // the streams are keyed on the current context: after a device reset
+  // they belong to a context that no longer exists, and are made again (the
+  // old handles are dead).  (A caller of the step has device memory, so a
+  // context is current; if none is, 0 stands for "made before any".)
+  unsigned long long ctx = 0;
+  if (!current_context_id(&ctx)) ctx = 0;
+  if (g_sub.per_dev[dev] && g_sub.per_dev[dev]->ctx != ctx) g_sub.per_dev[dev] = nullptr;
   if (!g_sub.per_dev[dev]) {
     SubStreams* ss = new SubStreams{};
+    ss->ctx = ctx;
     bool ok = cudaEventCreateWithFlags(&ss->fork, cudaEventDisableTiming) == cudaSuccess;
     int made = 0;
     for (int c = 0; c < kMaxSub && ok; ++c) {
@@ -339,6 +353,29 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
 }  // namespace
 
 void add_launches(int k) { count_launches(k); }
+
+bool current_context_id(unsigned long long* id) {
+  typedef CUresult (*GetCurrent)(CUcontext*);
+  typedef CUresult (*GetId)(CUcontext, unsigned long long*);
+  static std::once_flag once;
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = (GetCurrent)f;
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = (GetId)f;
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 }  // namespace csa
 

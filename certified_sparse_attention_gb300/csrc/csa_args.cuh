@@ -134,4 +134,12 @@ inline void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 void add_launches(int k);   // adds to the launch count csa_profile_read reports
 
+// Unique id of the calling thread's current CUDA context (the driver's
+// cuCtxGetId, reached through the runtime's driver entry points, so that the
+// library does not link libcuda).  Returns false when no context is current.
+// Per-device state tied to a context (a device address of a file-scope
+// array, library streams) is keyed on this id: after a device reset the
+// runtime creates a new primary context, with a new id.
+bool current_context_id(unsigned long long* id);
+
 }  // namespace csa

@@ -232,20 +232,20 @@ __global__ void __launch_bounds__(128) dense_combine_kernel(const DenseArgs a, c
 
 int dense_nsplit(int64_t n_max) { return (int)((n_max + kDenseChunk - 1) / kDenseChunk); }
 
-// opt in to the ring's dynamic shared memory once per instantiation
+// opt in to the ring's dynamic shared memory.  Done on every launch: the
+// attribute belongs to the function in the current context, so a flag kept
+// per process would be wrong on a second device or after a device reset,
+// and the call is cheap.
 template <int D, typename E>
-void set_dense_smem(int G) {
-  static bool done[9] = {false};
-  if (G < 1 || G > 8 || done[G]) return;
+cudaError_t set_dense_smem(int G) {
   const int smem = dense_smem<D, E>();
   switch (G) {
-    case 1: cudaFuncSetAttribute(dense_split_kernel<D, 1, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
-    case 2: cudaFuncSetAttribute(dense_split_kernel<D, 2, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
-    case 4: cudaFuncSetAttribute(dense_split_kernel<D, 4, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
-    case 8: cudaFuncSetAttribute(dense_split_kernel<D, 8, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); break;
-    default: break;
+    case 1: return cudaFuncSetAttribute(dense_split_kernel<D, 1, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    case 2: return cudaFuncSetAttribute(dense_split_kernel<D, 2, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    case 4: return cudaFuncSetAttribute(dense_split_kernel<D, 4, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    case 8: return cudaFuncSetAttribute(dense_split_kernel<D, 8, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    default: return cudaErrorInvalidValue;
   }
-  done[G] = true;
 }
 
 cudaError_t launch_dense(const DenseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t nmax_live,
@@ -255,13 +255,9 @@ cudaError_t launch_dense(const DenseArgs& a, const SeqArgs& seq, int d, int G, b
   // comparator: one CTA per item; fallback (masked): a small persistent grid
   const int cap = a.state ? 1024 : items;
   dim3 grid((unsigned)(items < cap ? items : cap));
-  if (d == 128) {
-    if (bf16) set_dense_smem<128, __nv_bfloat16>(G);
-    else set_dense_smem<128, float>(G);
-  } else {
-    if (bf16) set_dense_smem<64, __nv_bfloat16>(G);
-    else set_dense_smem<64, float>(G);
-  }
+  const cudaError_t ea = d == 128 ? (bf16 ? set_dense_smem<128, __nv_bfloat16>(G) : set_dense_smem<128, float>(G))
+                                  : (bf16 ? set_dense_smem<64, __nv_bfloat16>(G) : set_dense_smem<64, float>(G));
+  if (ea != cudaSuccess) return ea;
   const int smem = d == 128 ? (bf16 ? dense_smem<128, __nv_bfloat16>() : dense_smem<128, float>())
                             : (bf16 ? dense_smem<64, __nv_bfloat16>() : dense_smem<64, float>());
   CSA_DENSE_SWITCH(dense_split_kernel, grid, dim3(256), smem, st, a, seq, nsplit_live)

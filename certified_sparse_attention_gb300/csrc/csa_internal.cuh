@@ -19,6 +19,7 @@ constexpr int kWindow = 64;    // window read exactly (last tokens)
 constexpr int kTile = 256;     // keys per scan / candidate tile
 constexpr int kCandSeg = 4096; // pool keys per candidate-list segment (one candidate CTA)
 constexpr int kMaxB = 128;     // sequences per call
+constexpr int kMaxHeads = 1024; // query heads and KV heads per call
 constexpr int kMaxJ = 255;     // last grid level supported
 constexpr int kMaxSub = 4;     // sub-batches of one decode call
 constexpr int kHeadStream = 1 << 20;   // stream ids of per-query-head draws start here

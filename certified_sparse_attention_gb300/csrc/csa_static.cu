@@ -27,21 +27,41 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_dense_scratch[kStaticScratchBytes];
 
 std::mutex g_addr_mu;
-void* g_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  void* ptr;
+  unsigned long long ctx;   // context the address belongs to
+};
+ScratchAddr g_addr[kMaxDevices] = {};
 
-// Device address of g_dense_scratch on the current device, looked up once
-// per device (with that device current) and cached.
-csa_status scratch_address(void** out) {
+// Device address of g_dense_scratch in the current device's context.  The
+// host-side name g_dense_scratch is only a stand-in for the array (a kernel
+// given it would fault, or where the GPU can reach host memory, quietly use
+// the wrong memory); the device address comes from cudaGetSymbolAddress,
+// made with the device current.  A call made outside a stream capture looks
+// it up every time (cheap once the module is loaded; the first lookup on a
+// device loads the module) and caches it with the context's id; a call
+// inside a capture takes the cached address of its device and context, and
+// fails if there is none.  So a device reset, which ends the context and
+// the module holding the array, can never leave a stale address in use.
+csa_status scratch_address(cudaStream_t st, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return CSA_ERR_CUDA;
   if (dev >= kMaxDevices) return CSA_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return CSA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_addr_mu);
-  if (!g_addr[dev]) {
+  unsigned long long ctx = 0;
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
+    // also makes the device's primary context current if it was not
     if (cudaGetSymbolAddress(&p, g_dense_scratch) != cudaSuccess || !p) return CSA_ERR_CUDA;
-    g_addr[dev] = p;
+    if (!current_context_id(&ctx)) return CSA_ERR_CUDA;
+    g_addr[dev].ptr = p;
+    g_addr[dev].ctx = ctx;
+  } else if (!current_context_id(&ctx) || !g_addr[dev].ptr || g_addr[dev].ctx != ctx) {
+    return CSA_ERR_CUDA;   // no lookup made outside a capture in this context
   }
-  *out = g_addr[dev];
+  *out = g_addr[dev].ptr;
   return CSA_OK;
 }
 
@@ -58,7 +78,8 @@ csa_status csa_dense_decode_static(const csa_shape* shape, const void* q, const 
   const size_t need = csa_dense_workspace_size(shape);
   if (need == 0) {
     // invalid or unsupported shape: report which, as csa_dense_decode does
-    const bool valid = shape->B >= 1 && shape->Hq >= 1 && shape->Hkv >= 1 && shape->Hq % shape->Hkv == 0 &&
+    const bool valid = shape->B >= 1 && shape->Hq >= 1 && shape->Hkv >= 1 && shape->Hq <= kMaxHeads &&
+                       shape->Hkv <= kMaxHeads && shape->Hq % shape->Hkv == 0 &&
                        shape->n_max >= 1 && shape->n_max <= (int64_t)1 << 31 &&
                        (shape->dtype == CSA_BF16 || shape->dtype == CSA_F32);
     return valid ? CSA_ERR_UNSUPPORTED : CSA_ERR_INVALID_ARG;
@@ -73,7 +94,7 @@ csa_status csa_dense_decode_static(const csa_shape* shape, const void* q, const 
     if (len[b] > nlive) nlive = len[b];
   }
   void* scratch = nullptr;
-  const csa_status sa = scratch_address(&scratch);
+  const csa_status sa = scratch_address((cudaStream_t)stream, &scratch);
   if (sa != CSA_OK) return sa;
   DenseArgs a;
   a.q = q; a.K = K; a.V = V; a.part = (float*)scratch; a.o = o; a.state = nullptr; a.nfall = nullptr;

@@ -82,8 +82,8 @@ typedef enum {
 
 typedef struct {
   int B;          /* sequences, 1..128                                       */
-  int Hq;         /* query heads                                             */
-  int Hkv;        /* KV heads; G = Hq / Hkv in {1, 2, 4, 8}                  */
+  int Hq;         /* query heads, 1..1024                                    */
+  int Hkv;        /* KV heads, 1..1024; G = Hq / Hkv in {1, 2, 4, 8}         */
   int d;          /* head dimension, 64 or 128                               */
   int64_t n_max;  /* token capacity of K, V, K4 per (sequence, KV head)      */
   csa_dtype dtype;/* element type of q, K, V                                 */
@@ -200,10 +200,14 @@ csa_status csa_dense_decode(const csa_shape* shape, const void* q,
  *  - All calls on one device share the array.  Calls whose work overlaps in
  *    time (different streams, or several host threads) race on it and give
  *    wrong results; serialise them (one stream, or events between streams).
- *  - The first call on each device looks up the array's device address with
- *    that device current (cudaGetSymbolAddress; the address is cached per
- *    device).  Make that first call before any stream capture starts.  A
- *    failed lookup returns CSA_ERR_CUDA.
+ *  - The array's device address is looked up (cudaGetSymbolAddress, with
+ *    the device current) on every call made outside a stream capture, and
+ *    cached with the device's current CUDA context; the first call on a
+ *    device also loads the library's device code there.  A call made while
+ *    `stream` is being captured uses that cached address instead, so make
+ *    at least one call outside a capture first (again after a device reset,
+ *    which ends the context and the array with it); without one the call
+ *    returns CSA_ERR_CUDA.  A failed lookup returns CSA_ERR_CUDA.
  * Other errors as csa_dense_decode. */
 #define CSA_DENSE_STATIC_SCRATCH_BYTES (16u << 20)
 csa_status csa_dense_decode_static(const csa_shape* shape, const void* q,

@@ -89,3 +89,106 @@ def test_matches_workspace_entry_point_on_consecutive_calls(lib):
                 exact = w @ Vf[b, h // G, :n] / w.sum()
                 np.testing.assert_allclose(oh[b, h], exact, rtol=0,
                                            atol=2e-5 * (1 + np.abs(exact).max()))
+
+
+# A device reset ends the CUDA context, and with it the module that holds the
+# scratch array; the array's device address in the next context may differ.
+# The entry point caches the address per context, so a call after a reset
+# must look it up again rather than write through the old address.  The
+# check runs in a child process that holds device memory through the CUDA
+# runtime alone (a reset would leave this process's torch allocations dead).
+_RESET_CHILD = r'''
+import ctypes, math, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+import certified_sparse_attention_gb300 as csa
+csa.load_library()
+path = next(l.split()[-1] for l in open("/proc/self/maps")
+            if "libcudart.so" in l)
+rt = ctypes.CDLL(path)
+rt.cudaMalloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t]
+rt.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                          ctypes.c_int]
+rt.cudaFree.argtypes = [ctypes.c_void_p]
+
+def ok(e, what):
+    if e != 0:
+        raise SystemExit(f"{what}: cuda error {e}")
+
+def bf16_bits(x):
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+def upload(a):
+    p = ctypes.c_void_p()
+    ok(rt.cudaMalloc(ctypes.byref(p), a.nbytes), "cudaMalloc")
+    ok(rt.cudaMemcpy(p, a.ctypes.data, a.nbytes, 1), "H2D")
+    return p.value
+
+def download(p, shape):
+    a = np.empty(shape, np.float32)
+    ok(rt.cudaMemcpy(a.ctypes.data, p, a.nbytes, 2), "D2H")
+    return a
+
+B, Hq, Hkv, d, n = 2, 8, 2, 128, 3000
+lens = [3000, 1777]
+rng = np.random.default_rng(5)
+qb = bf16_bits(rng.normal(0, 1, (B, Hq, d)))
+Kb = bf16_bits(rng.normal(0, 1, (B, Hkv, n, d)) + 0.5)
+Vb = bf16_bits(rng.normal(0, 1, (B, Hkv, n, d)))
+shape = csa.make_shape(B, Hq, Hkv, d, n, "bf16")
+
+def run_static():
+    q, K, V = upload(qb), upload(Kb), upload(Vb)
+    o = upload(np.full((B, Hq, d), np.nan, np.float32))
+    csa.check(csa.csa_dense_decode_static(shape, q, K, V, lens, o, stream=0),
+              "static")
+    ok(rt.cudaDeviceSynchronize(), "sync")
+    out = download(o, (B, Hq, d))
+    for p in (q, K, V, o):
+        ok(rt.cudaFree(p), "cudaFree")
+    return out
+
+def run_workspace():
+    q, K, V = upload(qb), upload(Kb), upload(Vb)
+    o = upload(np.zeros((B, Hq, d), np.float32))
+    nb = csa.csa_dense_workspace_size(shape)
+    ws = upload(np.zeros(nb, np.uint8))
+    csa.check(csa.csa_dense_decode(shape, q, K, V, lens, o, ws, nb, stream=0),
+              "workspace")
+    ok(rt.cudaDeviceSynchronize(), "sync")
+    out = download(o, (B, Hq, d))
+    for p in (q, K, V, o, ws):
+        ok(rt.cudaFree(p), "cudaFree")
+    return out
+
+before = run_static()
+ref = run_workspace()
+assert np.array_equal(before, ref)
+ok(rt.cudaDeviceReset(), "cudaDeviceReset")
+after1 = run_static()
+after2 = run_static()
+assert np.array_equal(after1, ref) and np.array_equal(after2, ref)
+f = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+q64, K64, V64 = f(qb), f(Kb), f(Vb)
+G = Hq // Hkv
+for b in range(B):
+    for h in range(Hq):
+        s = K64[b, h // G, :lens[b]] @ q64[b, h] / math.sqrt(d)
+        w = np.exp(s - s.max())
+        exact = w @ V64[b, h // G, :lens[b]] / w.sum()
+        assert np.allclose(after1[b, h], exact, rtol=0, atol=2e-5 * (1 + np.abs(exact).max()))
+print("reset ok")
+'''
+
+
+@pytest.mark.gpu
+def test_lookup_again_after_device_reset(lib):
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _RESET_CHILD, root],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "reset ok" in r.stdout

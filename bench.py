@@ -186,14 +186,14 @@ def run_mode(args, csa, w, shape, data, lens, seed_tab, nseed, plan, stream,
     for (L, s) in plan[:3]:
         d = data[L]
         step(d["q"][s % 4], d["K"], d["V"], d["meta"], lens,
-             seed_tab[L][s % nseed], stream)
+             seed_tab[L][s % nseed], stream, meta8=d.get("meta8"))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for (L, s) in plan:
         d = data[L]
         step(d["q"][s % 4], d["K"], d["V"], d["meta"], lens,
-             seed_tab[L][s % nseed], stream)
+             seed_tab[L][s % nseed], stream, meta8=d.get("meta8"))
     e1.record(stream)
     torch.cuda.synchronize()
     csa.check(csa.csa_check(step.ws, stream), "csa_check (measure %d, timed)" % measure)
@@ -231,12 +231,15 @@ def decode_loop(args, csa, w, device, stream):
     """Whole-model decode: every token appends one row per layer and runs
     that layer's step, over `args.decode_layers` layers of the workload's
     shape (readsearch.ai "Abstract": new perturbation draws for each
-    decode step).  Per layer and token: re-quantise the appended
-    token's block (csa_quantize_keys from that position), then the decode
-    step with the grown length and a fresh seed.  The K, V rows of the
-    appended tokens are generated with the cache; the loop extends the
-    length over them.  Launched stream-ordered (lengths and seeds are host
-    arguments, new every token)."""
+    decode step).  The lengths, the token index and every layer's seeds
+    live in device memory, so the whole token (all layers) is captured once
+    into a CUDA graph and replayed: per layer the graph picks the token's
+    query and seeds, and runs csa_decode_step_device, whose first kernel
+    re-quantises the appended token's block.  The K, V rows of the appended
+    tokens are generated with the cache; the loop extends the length over
+    them.  Also timed: the same token launched stream-ordered through
+    csa_decode_step (host lengths and seeds, csa_quantize_keys on the
+    appended block first)."""
     import torch
     import synth
     L, T = args.decode_layers, 8
@@ -245,51 +248,85 @@ def decode_loop(args, csa, w, device, stream):
     params = csa.make_params(w.eps, w.delta, w.r)
     step = csa.DecodeStep(shape, params, device)
     layers = []
+    q_all, seed_all = [], []
     for lid in range(L):
         K, V, meta = synth.kv_torch(w, layer=100 + lid, device=device)
         mt = csa.meta_buffers(shape, device)
         csa.check(csa.csa_quantize_keys(shape, K, V, [n0] * w.B, 0, *mt),
                   "csa_quantize_keys")
-        qs = [synth.q_torch(w, meta, t, layer=100 + lid, device=device)
-              for t in range(T)]
-        layers.append((K, V, mt, qs, lid))
+        q_all.append(torch.stack([synth.q_torch(w, meta, t, layer=100 + lid,
+                                                device=device)
+                                  for t in range(T)]))
+        seed_all.append(torch.tensor(
+            [[s - (1 << 64) if s >= (1 << 63) else s
+              for s in seeds_for(w, 100 + lid, t)] for t in range(T)],
+            dtype=torch.int64, device=device))
+        layers.append((K, V, mt, lid))
+    q_all = torch.stack(q_all, 1)            # [T, L, B, Hq, d]
+    seed_all = torch.stack(seed_all, 1)      # [T, L, B]
     torch.cuda.synchronize()
-    seeds = [[seeds_for(w, 100 + lid, t) for t in range(T)] for lid in range(L)]
+    t_dev = torch.zeros(1, dtype=torch.int64, device=device)
+    lens_dev = torch.zeros(w.B, dtype=torch.int64, device=device)
+    q_cur = torch.empty_like(q_all[0, 0])
+    seed_cur = torch.empty(w.B, dtype=torch.int64, device=device)
 
-    def token(t, quant_only=False):
+    def token_device():
+        lens_dev.copy_((t_dev + (n0 + 1)).expand(w.B))
+        qt = q_all.index_select(0, t_dev)[0]         # [L, B, Hq, d]
+        st = seed_all.index_select(0, t_dev)[0]      # [L, B]
+        for li, (K, V, mt, lid) in enumerate(layers):
+            q_cur.copy_(qt[li])
+            seed_cur.copy_(st[li])
+            step.device_step(q_cur, K, V, mt, lens_dev, seed_cur, True)
+        t_dev.add_(1)
+
+    def token_host(t):
         pos = n0 + t
         lens = [pos + 1] * w.B
-        for (K, V, mt, qs, lid) in layers:
-            csa.check(csa.csa_quantize_keys(shape, K, V, lens, pos, *mt, stream=stream),
+        for li, (K, V, mt, lid) in enumerate(layers):
+            csa.check(csa.csa_quantize_keys(shape, K, V, lens, pos, *mt,
+                                            stream=stream),
                       "csa_quantize_keys")
-            if not quant_only:
-                step(qs[t], K, V, mt, lens, seeds[lid][t], stream)
+            step(q_all[t, li], K, V, mt, lens,
+                 seeds_for(w, 100 + lid, t), stream)
 
-    token(0)                                   # warm-up (token 0)
+    with torch.cuda.stream(stream):
+        token_device()                       # warm-up, eager (token 0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        token_device()
+    t_dev.fill_(1)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for t in range(1, T):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    csa.check(csa.csa_check(step.ws, stream), "csa_check (decode loop)")
+    us_graph = e0.elapsed_time(e1) / (T - 1) * 1e3
     e0.record(stream)
     for t in range(1, T):
-        token(t)
+        token_host(t)
     e1.record(stream)
     torch.cuda.synchronize()
     csa.check(csa.csa_check(step.ws, stream), "csa_check (decode loop)")
-    us_tok = e0.elapsed_time(e1) / (T - 1) * 1e3
-    e0.record(stream)
-    for t in range(1, T):
-        token(t, quant_only=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    us_q = e0.elapsed_time(e1) / (T - 1) * 1e3
-    del layers
+    us_host = e0.elapsed_time(e1) / (T - 1) * 1e3
+    del layers, graph
     torch.cuda.empty_cache()
     return {"layers": L, "tokens_timed": T - 1, "context": f"{n0 + 1}..{w.n}",
-            "us_per_token": round(us_tok, 1),
-            "us_per_layer": round(us_tok / L, 1),
-            "append_quantize_us_per_token": round(us_q, 1),
-            "note": "each layer: quantise the appended token's block, then "
-                    "the certified step with a fresh seed"}
+            "us_per_token": round(us_graph, 1),
+            "us_per_layer": round(us_graph / L, 1),
+            "stream_ordered_us_per_token": round(us_host, 1),
+            "stream_ordered_us_per_layer": round(us_host / L, 1),
+            "note": "one CUDA graph per token over all layers: device "
+                    "lengths and seeds, the appended block re-quantised "
+                    "inside each step's first kernel; stream_ordered: host "
+                    "lengths, csa_quantize_keys then csa_decode_step per "
+                    "layer"}
 
 
 class ClockSampler:
@@ -401,7 +438,7 @@ def cpu_pool():
 
 # ------------------------------------------------------------------ arms
 
-def setup_layers(w, layers, device, csa):
+def setup_layers(w, layers, device, csa, refine8=0):
     import torch
     import synth
     shape = csa.make_shape(w.B, w.Hq, w.Hkv, w.d, w.n, w.dtype)
@@ -414,6 +451,11 @@ def setup_layers(w, layers, device, csa):
         qs = [synth.q_torch(w, meta, s, layer=lid, device=device)
               for s in range(4)]
         data.append({"K": K, "V": V, "meta": mt, "q": qs, "lid": lid})
+        if refine8:
+            m8 = csa.meta8_buffers(shape, device)
+            csa.check(csa.csa_quantize_keys8(shape, K, [w.n] * w.B, 0, *m8),
+                      "csa_quantize_keys8")
+            data[-1]["meta8"] = m8
     torch.cuda.synchronize()
     return shape, data
 
@@ -437,10 +479,11 @@ def run_ours(args, world, rank, local):
         import dataclasses
         w = dataclasses.replace(w, n=args.n or w.n, B=args.batch or w.B)
     layers = rank_layers(rank, world, args.layers)
-    shape, data = setup_layers(w, layers, device, csa)
+    shape, data = setup_layers(w, layers, device, csa, args.refine8)
     # --sub-batches: profiler captures of the unsplit chain (a scheduling
     # choice only; the reported line uses the default)
-    params = csa.make_params(w.eps, w.delta, w.r, sub_batches=args.sub_batches)
+    params = csa.make_params(w.eps, w.delta, w.r, sub_batches=args.sub_batches,
+                             qcode=args.qcode, refine8=args.refine8)
     step = csa.DecodeStep(shape, params, device, with_stats=False)
     step_diag = csa.DecodeStep(shape, params, device, with_stats=True)
     dense = csa.DenseDecode(shape, device)
@@ -454,7 +497,7 @@ def run_ours(args, world, rank, local):
     def one(s, L):
         d = data[L]
         step(d["q"][s % 4], d["K"], d["V"], d["meta"], lens,
-             seed_tab[L][s % nseed], stream)
+             seed_tab[L][s % nseed], stream, meta8=d.get("meta8"))
 
     for s in range(args.warmup):
         one(s, s % args.layers)
@@ -526,7 +569,7 @@ def run_ours(args, world, rank, local):
     for L in range(args.layers):
         d = data[L]
         step_diag(d["q"][L % 4], d["K"], d["V"], d["meta"], lens,
-                  seed_tab[L][L % nseed], stream)
+                  seed_tab[L][L % nseed], stream, meta8=d.get("meta8"))
         torch.cuda.synchronize()
         csa.check(csa.csa_check(step_diag.ws, stream), "csa_check")
         stats = step_diag.stats.cpu().numpy()
@@ -594,7 +637,7 @@ def run_ours(args, world, rank, local):
         csa.check(csa.csa_quantize_keys(shape, d["K"], d["V"], lens,
                                         w.n - 1, *d["meta"], stream))
         step(qd, d["K"], d["V"], d["meta"], lens, seed_tab[L][s % nseed],
-             stream)
+             stream, meta8=d.get("meta8"))
         oh.copy_(step.o, non_blocking=True)
         bh.copy_(step.beta, non_blocking=True)
         lh.copy_(step.level, non_blocking=True)
@@ -763,7 +806,7 @@ def context_sweep(args):
         def run_sparse(i):
             d = data[i % 2]
             step(d["q"][i % 4], d["K"], d["V"], d["meta"], lens,
-                 seeds_for(w, d["lid"], i), st)
+                 seeds_for(w, d["lid"], i), st, meta8=d.get("meta8"))
 
         def run_dense(i):
             d = data[i % 2]
@@ -812,6 +855,11 @@ def main(argv=None):
                     help="layers of the whole-model decode loop (0: skip it)")
     ap.add_argument("--no-modes", action="store_true",
                     help="skip the CLT / other-measure comparisons (profiler captures)")
+    ap.add_argument("--refine8", type=int, default=0,
+                    help="8-bit refinement tier: 0 off, 1 every group, 2 "
+                         "groups whose first range reaches level r")
+    ap.add_argument("--qcode", type=int, default=0,
+                    help="query code of the 4-bit bounds: 0 int8, 1 two digits")
     ap.add_argument("--sub-batches", type=int, default=0,
                     help="sub-batches of the decode call (0: the library default)")
     args = ap.parse_args(argv)

@@ -31,16 +31,17 @@ EXPORTED = ("csa_workspace_size", "csa_quantize_keys", "csa_decode_step",
             "csa_dense_workspace_size", "csa_dense_decode", "csa_check",
             "csa_status_string", "csa_workspace_layout",
             "csa_profile_enable", "csa_profile_read",
-            "csa_dense_decode_static")
+            "csa_dense_decode_static", "csa_decode_step_device",
+            "csa_quantize_keys8", "csa_decode_step_refined")
 # size of the fixed scratch array behind csa_dense_decode_static
 DENSE_STATIC_SCRATCH_BYTES = 16 << 20
 STATS_FIELDS = 10
 STAT = {"level": 0, "keys_read": 1, "values_read": 2, "n_candidates": 3,
         "n_near_threshold": 4, "J": 5, "rounds": 6, "group_keys_read": 7,
-        "group_values_read": 8}
+        "group_values_read": 8, "rows8": 9}
 PHASES = ("clear", "scan", "exact_max", "candidates", "rescore", "predict",
           "levels", "plan", "vgather", "certify", "fallback", "diagnostics",
-          "reserved")
+          "refine8")
 
 
 class CsaLibraryMissing(RuntimeError):
@@ -63,7 +64,8 @@ class csa_params(ctypes.Structure):
     _fields_ = [("eps", ctypes.c_float), ("delta", ctypes.c_float),
                 ("r", ctypes.c_int), ("measure", ctypes.c_int),
                 ("J_override", ctypes.c_int), ("sub_batches", ctypes.c_int),
-                ("perturb", ctypes.c_int)]
+                ("perturb", ctypes.c_int), ("qcode", ctypes.c_int),
+                ("refine8", ctypes.c_int)]
 
 
 class csa_head_stats(ctypes.Structure):
@@ -74,7 +76,7 @@ class csa_head_stats(ctypes.Structure):
                 ("rounds", ctypes.c_int32),
                 ("group_keys_read", ctypes.c_int32),
                 ("group_values_read", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("rows8", ctypes.c_int32)]
 
 
 class csa_workspace_map(ctypes.Structure):
@@ -118,6 +120,20 @@ def load_library(path: str = LIB_PATH):
                                     P(ctypes.c_uint64), vp, vp, vp, vp, vp,
                                     vp, sz, vp]
     lib.csa_decode_step.restype = ctypes.c_int
+    lib.csa_decode_step_device.argtypes = [P(csa_shape), P(csa_params), vp,
+                                           vp, vp, vp, vp, vp, vp, vp, vp,
+                                           ctypes.c_int, vp, vp, vp, vp, vp,
+                                           vp, sz, vp]
+    lib.csa_decode_step_device.restype = ctypes.c_int
+    lib.csa_quantize_keys8.argtypes = [P(csa_shape), vp, P(ctypes.c_int64),
+                                       ctypes.c_int64, vp, vp, vp]
+    lib.csa_quantize_keys8.restype = ctypes.c_int
+    lib.csa_decode_step_refined.argtypes = [P(csa_shape), P(csa_params), vp,
+                                            vp, vp, vp, vp, vp, vp, vp, vp,
+                                            P(ctypes.c_int64),
+                                            P(ctypes.c_uint64), vp, vp, vp,
+                                            vp, vp, vp, sz, vp]
+    lib.csa_decode_step_refined.restype = ctypes.c_int
     lib.csa_dense_decode.argtypes = [P(csa_shape), vp, vp, vp,
                                      P(ctypes.c_int64), vp, vp, sz, vp]
     lib.csa_dense_decode.restype = ctypes.c_int
@@ -179,9 +195,11 @@ def make_shape(B, Hq, Hkv, d, n_max, dtype) -> csa_shape:
 
 
 def make_params(eps=0.05, delta=0.05, r=2, measure=CSA_MEASURE_VALUE,
-                J_override=-1, sub_batches=0, perturb=0) -> csa_params:
+                J_override=-1, sub_batches=0, perturb=0,
+                qcode=0, refine8=0) -> csa_params:
     return csa_params(float(eps), float(delta), int(r), int(measure),
-                      int(J_override), int(sub_batches), int(perturb))
+                      int(J_override), int(sub_batches), int(perturb),
+                      int(qcode), int(refine8))
 
 
 def csa_workspace_size(shape: csa_shape, params: csa_params) -> int:
@@ -230,6 +248,51 @@ def csa_decode_step(shape, params, q, K, V, K4, bounds, vmax, vnorm2, lens,
         _u64(seeds), _ptr(o),
         _ptr(beta), _ptr(level), _ptr(keys_read), _ptr(stats),
         _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def csa_quantize_keys8(shape, K, lens, from_token, K8, delta8,
+                       stream=None) -> int:
+    _check_batch(shape, lens)
+    return load_library().csa_quantize_keys8(
+        ctypes.byref(shape), _ptr(K), _i64(lens), int(from_token), _ptr(K8),
+        _ptr(delta8), _stream(stream))
+
+
+def meta8_buffers(shape: csa_shape, device):
+    """(K8, delta8) device tensors for csa_quantize_keys8 (the 8-bit tier)."""
+    import torch
+    nblk = (shape.n_max + BLOCK - 1) // BLOCK
+    K8 = torch.zeros((shape.B, shape.Hkv, nblk * BLOCK, shape.d),
+                     dtype=torch.uint8, device=device)
+    d8 = torch.zeros((shape.B, shape.Hkv, nblk, shape.d), dtype=torch.float32,
+                     device=device)
+    return K8, d8
+
+
+def csa_decode_step_refined(shape, params, q, K, V, K4, bounds, vmax, vnorm2,
+                            K8, delta8, lens, seeds, o, beta, level,
+                            keys_read, stats, workspace, workspace_bytes,
+                            stream=None) -> int:
+    _check_batch(shape, lens, seeds)
+    return load_library().csa_decode_step_refined(
+        ctypes.byref(shape), ctypes.byref(params), _ptr(q), _ptr(K), _ptr(V),
+        _ptr(K4), _ptr(bounds), _ptr(vmax), _ptr(vnorm2), _ptr(K8),
+        _ptr(delta8), _i64(lens), _u64(seeds), _ptr(o), _ptr(beta),
+        _ptr(level), _ptr(keys_read), _ptr(stats), _ptr(workspace),
+        int(workspace_bytes), _stream(stream))
+
+
+def csa_decode_step_device(shape, params, q, K, V, K4, bounds, vmax, vnorm2,
+                           lens_dev, seeds_dev, requantize_last, o, beta,
+                           level, keys_read, stats, workspace,
+                           workspace_bytes, stream=None) -> int:
+    """lens_dev: device int64 [B]; seeds_dev: device uint64 (or int64) [B]."""
+    return load_library().csa_decode_step_device(
+        ctypes.byref(shape), ctypes.byref(params), _ptr(q), _ptr(K), _ptr(V),
+        _ptr(K4), _ptr(bounds), _ptr(vmax), _ptr(vnorm2), _ptr(lens_dev),
+        _ptr(seeds_dev), int(requantize_last), _ptr(o), _ptr(beta),
+        _ptr(level), _ptr(keys_read), _ptr(stats), _ptr(workspace),
+        int(workspace_bytes), _stream(stream))
 
 
 def csa_dense_decode(shape, q, K, V, lens, o, workspace, workspace_bytes,
@@ -355,14 +418,50 @@ class DecodeStep:
         self.stats = (torch.zeros((B, Hq, STATS_FIELDS), dtype=torch.int32,
                                   device=device) if with_stats else None)
 
-    def __call__(self, q, K, V, meta: KVMeta, lens, seeds, stream=None):
+    def __call__(self, q, K, V, meta: KVMeta, lens, seeds, stream=None,
+                 meta8=None):
+        """meta8: (K8, delta8) of the 8-bit tier, required when the
+        parameters ask for it (csa_decode_step_refined)."""
         check_step_inputs(self.shape, q, K, V, meta, lens, seeds)
-        st = csa_decode_step(self.shape, self.params, q, K, V, meta.K4,
-                             meta.bounds, meta.vmax, meta.vnorm2, lens, seeds,
-                             self.o, self.beta,
-                             self.level, self.keys_read, self.stats, self.ws,
-                             self.ws_bytes, stream)
-        check(st, "csa_decode_step")
+        if self.params.refine8:
+            if meta8 is None:
+                raise ValueError("refine8: the 8-bit codes (meta8) are needed")
+            nblk = (self.shape.n_max + BLOCK - 1) // BLOCK
+            n8 = self.shape.B * self.shape.Hkv * nblk
+            _require(meta8[0], "K8", n8 * BLOCK * self.shape.d)
+            _require(meta8[1], "delta8", n8 * self.shape.d * 4)
+            st = csa_decode_step_refined(
+                self.shape, self.params, q, K, V, meta.K4, meta.bounds,
+                meta.vmax, meta.vnorm2, meta8[0], meta8[1], lens, seeds,
+                self.o, self.beta, self.level, self.keys_read, self.stats,
+                self.ws, self.ws_bytes, stream)
+            check(st, "csa_decode_step_refined")
+        else:
+            st = csa_decode_step(self.shape, self.params, q, K, V, meta.K4,
+                                 meta.bounds, meta.vmax, meta.vnorm2, lens,
+                                 seeds, self.o, self.beta, self.level,
+                                 self.keys_read, self.stats, self.ws,
+                                 self.ws_bytes, stream)
+            check(st, "csa_decode_step")
+        return self.o, self.beta, self.level, self.keys_read
+
+    def device_step(self, q, K, V, meta: KVMeta, lens_dev, seeds_dev,
+                    requantize_last: bool = True, stream=None):
+        """The step with lengths and seeds read from device tensors (int64
+        [B] each), optionally re-quantising the block of the token just
+        appended; capturable into a CUDA graph that is replayed with new
+        lengths and seeds written into the same tensors."""
+        check_step_inputs(self.shape, q, K, V, meta, [1] * self.shape.B)
+        for t, name in ((lens_dev, "lens_dev"), (seeds_dev, "seeds_dev")):
+            _require(t, name, 8 * self.shape.B)
+        st = csa_decode_step_device(self.shape, self.params, q, K, V,
+                                    meta.K4, meta.bounds, meta.vmax,
+                                    meta.vnorm2, lens_dev, seeds_dev,
+                                    1 if requantize_last else 0, self.o,
+                                    self.beta, self.level, self.keys_read,
+                                    self.stats, self.ws, self.ws_bytes,
+                                    stream)
+        check(st, "csa_decode_step_device")
         return self.o, self.beta, self.level, self.keys_read
 
 

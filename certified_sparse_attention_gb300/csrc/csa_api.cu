@@ -44,7 +44,8 @@ csa_status shape_supported(const csa_shape* s) {
 bool params_ok(const csa_params* p) {
   return p && p->eps > 0.f && std::isfinite(p->eps) && p->delta > 0.f && p->delta < 1.f && p->r >= 1 &&
          p->r <= 4 && p->measure >= 0 && p->measure <= 3 && p->J_override >= -1 && p->J_override <= kMaxJ &&
-         p->sub_batches >= 0 && p->sub_batches <= kMaxSub && (p->perturb == 0 || p->perturb == 1);
+         p->sub_batches >= 0 && p->sub_batches <= kMaxSub && (p->perturb == 0 || p->perturb == 1) &&
+         (p->qcode == 0 || p->qcode == 1) && p->refine8 >= 0 && p->refine8 <= 2;
 }
 
 // z with P(|N(0,1)| > z) = delta, i.e. erfc(z / sqrt 2) = delta: bisection
@@ -61,8 +62,9 @@ float normal_quantile_two_sided(double delta) {
 struct Layout {
   int J1;
   int64_t pcap, nblk_max;
-  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, front, rcnt, zero_end;
-  size_t winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, hw, s32, win, t32, clist, rlist, xlist, cmap,
+  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, front, rcnt, jrd, ninset,
+      zero_end;
+  size_t jkey, jref, seqd, winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, hw, s32, win, t32, clist, rlist, xlist, cmap,
       buckets, dpart, pref, total;
   int64_t nchunk_cap;
 };
@@ -90,7 +92,12 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.rq = o; o += up(((size_t)BG * 6 + 6) * 4);
   L.front = o; o += up((size_t)4 * BG * 4);
   L.rcnt = o; o += up((size_t)3 * BG * 4);
+  L.jrd = o; o += up(p->refine8 ? (size_t)BH * (L.J1 + 1) * 4 : 0);
+  L.ninset = o; o += up(p->refine8 ? (size_t)BH * 4 : 0);
   L.zero_end = o;
+  L.seqd = o; o += up(sizeof(SeqArgs));
+  L.jkey = o; o += up(p->refine8 ? (size_t)BG * L.pcap * 2 : 0);
+  L.jref = o; o += up(p->refine8 ? (size_t)BG * L.pcap * G * 2 : 0);
   L.winstats = o; o += up((size_t)BH * (D + 4) * 4);
   L.vmaxp = o; o += up((size_t)BG * 4);
   L.state = o; o += up((size_t)BH * 4 * 4);
@@ -252,13 +259,29 @@ SubStreams* sub_streams() {
   return g_sub.per_dev[dev];
 }
 
+// Where a step's per-sequence lengths and seeds come from: host arrays
+// (copied into the launch arguments) or device arrays (read by a first
+// kernel into the workspace; grids are then sized from the capacity n_max).
+struct SeqSource {
+  const int64_t* len;
+  const uint64_t* seed;
+  bool dev;
+  bool requant;            // device lengths: re-quantise the block of token len - 1
+  uint8_t* K4w;
+  float* boundsw;
+  float* vmaxw;
+  float* vnorm2w;
+  const uint8_t* K8;       // 8-bit codes and steps (refinement tier), or null
+  const float* delta8;
+};
+
 // One (sub-)batch on one stream.  `status` is the device status word (shared
 // by the sub-batches of a split call); `clear` zeroes the per-step counters
 // (a split call clears sub-batch 0's, which hold the status word, before it
 // forks).
 csa_status decode_batch(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
                         const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
-                        const float* vnorm2, const int64_t* len, const uint64_t* step_seed, float* o,
+                        const float* vnorm2, const SeqSource& src, float* o,
                         float* beta, int32_t* level, int32_t* keys_read, csa_head_stats* stats, char* ws,
                         unsigned* status, bool clear, cudaStream_t st) {
   Layout L;
@@ -268,32 +291,49 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
   SeqArgs seq;
   std::memset(&seq, 0, sizeof(seq));
   int64_t nlive = 0;
-  for (int b = 0; b < shape->B; ++b) {
-    if (len[b] < 1 || len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
-    seq.n[b] = len[b];
-    seq.seed[b] = step_seed[b];
-    const int64_t P = len[b] > kWindow ? len[b] - kWindow : 0;
-    seq.J[b] = params->J_override >= 0 ? params->J_override : grid_J(P, params->r);
-    if (len[b] > nlive) nlive = len[b];
+  const SeqArgs* seqd = nullptr;
+  if (!src.dev) {
+    for (int b = 0; b < shape->B; ++b) {
+      const int64_t n = src.len[b];
+      if (n < 1 || n > shape->n_max) return CSA_ERR_INVALID_ARG;
+      seq.n[b] = n;
+      seq.seed[b] = src.seed[b];
+      const int64_t P = n > kWindow ? n - kWindow : 0;
+      seq.J[b] = params->J_override >= 0 ? params->J_override : grid_J(P, params->r);
+      if (n > nlive) nlive = n;
+    }
+  } else {
+    nlive = shape->n_max;
+    seqd = (const SeqArgs*)(ws + L.seqd);
   }
   const int64_t plive = nlive > kWindow ? nlive - kWindow : 0;
   const float rs = (float)(1.0 / std::sqrt((double)shape->d));
 
   prof_step_begin(st);
   if (clear && cudaMemsetAsync(ws, 0, L.zero_end, st) != cudaSuccess) return CSA_ERR_CUDA;
+  if (src.dev) {
+    if (launch_seq_prep(src.len, src.seed, shape->B, shape->n_max, params->r, params->J_override,
+                        (SeqArgs*)(ws + L.seqd), status, st) != cudaSuccess)
+      return CSA_ERR_CUDA;
+    count_launches(1);
+  }
   prof_mark(0, st);
 
-  ScanArgs sa;
+  ScanArgs sa = {};
   sa.q = q; sa.K4 = K4; sa.bounds = bounds; sa.ubar = (float*)(ws + L.ubar);
   sa.hw = (float*)(ws + L.hw);
   sa.cmax = (unsigned*)(ws + L.cmax); sa.status = status;
   sa.Hq = shape->Hq; sa.Hkv = shape->Hkv; sa.n_max = shape->n_max; sa.nblk_max = L.nblk_max; sa.rs = rs;
+  sa.two_digit = params->qcode == 1;
+  sa.seqd = seqd;
+  sa.requant = src.dev && src.requant;
+  sa.K = K; sa.V = V; sa.K4w = src.K4w; sa.boundsw = src.boundsw; sa.vmaxw = src.vmaxw; sa.vnorm2w = src.vnorm2w;
   cudaError_t e = launch_scan(sa, seq, shape->B, shape->d, G, bf16, nlive, st);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   count_launches(1);
   prof_mark(1, st);
 
-  SparseArgs a;
+  SparseArgs a = {};
   a.q = q; a.K = K; a.V = V; a.vmax = vmax; a.vnorm2 = vnorm2; a.ubar = (const float*)(ws + L.ubar);
   a.s32 = (float*)(ws + L.s32); a.win = (float*)(ws + L.win); a.cmax = (unsigned*)(ws + L.cmax);
   a.jr_hist = (unsigned*)(ws + L.jr_hist); a.ncand = (unsigned*)(ws + L.ncand);
@@ -315,6 +355,13 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
   a.pcap = L.pcap; a.J1 = L.J1; a.r = params->r; a.eps = params->eps; a.delta = params->delta;
   a.measure = params->measure; a.rs = rs; a.per_head = params->perturb;
   a.zclt = normal_quantile_two_sided((double)params->delta);
+  a.seqd = seqd;
+  a.refine8 = params->refine8;
+  if (params->refine8) {
+    a.K8 = src.K8; a.delta8 = src.delta8; a.bounds = bounds;
+    a.jkey = (uint16_t*)(ws + L.jkey); a.jrd = (int*)(ws + L.jrd); a.ninset = (unsigned*)(ws + L.ninset);
+    a.jref = (uint16_t*)(ws + L.jref);
+  }
 
   const int nsm = sm_count();
   if (plive > 0) {
@@ -334,9 +381,11 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
     count_launches(round > 0 ? 6 : 5);
   }
   // exact attention for heads with no certified level and sequences without a pool
-  DenseArgs da;
+  DenseArgs da = {};
   da.q = q; da.K = K; da.V = V; da.part = (float*)(ws + L.dpart); da.o = o; da.state = a.state;
   da.nfall = a.nfall;
+  da.status = status;
+  da.seqd = seqd;
   da.B = shape->B; da.Hq = shape->Hq; da.Hkv = shape->Hkv; da.n_max = shape->n_max;
   da.nsplit = dense_nsplit(shape->n_max); da.rs = rs;
   if (launch_dense(da, seq, shape->d, G, bf16, nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
@@ -353,6 +402,31 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
 }  // namespace
 
 void add_launches(int k) { count_launches(k); }
+
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                       uint32_t box_inner, uint32_t box_rows) {
+  typedef CUresult (*Encode)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                             CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static std::once_flag once;
+  static Encode encode = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = (Encode)f;
+  });
+  if (!encode || !base || ((uintptr_t)base & 15u) || (pitch_bytes & 15u)) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool current_context_id(unsigned long long* id) {
   typedef CUresult (*GetCurrent)(CUcontext*);
@@ -403,9 +477,10 @@ size_t csa_workspace_size(const csa_shape* shape, const csa_params* params) {
   return sp.total;
 }
 
+// dense workspace: the status word (256 bytes), then the split-K partials
 size_t csa_dense_workspace_size(const csa_shape* shape) {
   if (!shape_ok(shape) || shape_supported(shape) != CSA_OK) return 0;
-  return up((size_t)dense_nsplit(shape->n_max) * shape->B * shape->Hq * (shape->d + 2) * 4);
+  return kAlign + up((size_t)dense_nsplit(shape->n_max) * shape->B * shape->Hq * (shape->d + 2) * 4);
 }
 
 csa_status csa_workspace_layout(const csa_shape* shape, const csa_params* params, csa_workspace_map* out) {
@@ -448,12 +523,35 @@ csa_status csa_quantize_keys(const csa_shape* shape, const void* K, const void* 
     const int64_t nb = (len[b] + kBlock - 1) / kBlock - blk_from;
     if (nb > nblocks) nblocks = nb;
   }
-  QuantArgs a;
+  QuantArgs a = {};
   a.K = K; a.V = V; a.K4 = K4; a.bounds = bounds; a.vmax = vmax; a.vnorm2 = vnorm2; a.Hkv = shape->Hkv;
   a.n_max = shape->n_max; a.nblk_max = (shape->n_max + kBlock - 1) / kBlock; a.blk_from = blk_from;
   if (nblocks > 0) count_launches(1);
   return cuda_status(launch_quant(a, seq, shape->B, shape->d, shape->dtype == CSA_BF16, nblocks,
                                   (cudaStream_t)stream));
+}
+
+csa_status csa_quantize_keys8(const csa_shape* shape, const void* K, const int64_t* len, int64_t from_token,
+                              uint8_t* K8, float* delta8, void* stream) {
+  if (!shape_ok(shape) || !K || !len || !K8 || !delta8 || from_token < 0) return CSA_ERR_INVALID_ARG;
+  csa_status su = shape_supported(shape);
+  if (su != CSA_OK) return su;
+  SeqArgs seq;
+  std::memset(&seq, 0, sizeof(seq));
+  int64_t nblocks = 0;
+  const int64_t blk_from = from_token / kBlock;
+  for (int b = 0; b < shape->B; ++b) {
+    if (len[b] < 0 || len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
+    seq.n[b] = len[b];
+    const int64_t nb = (len[b] + kBlock - 1) / kBlock - blk_from;
+    if (nb > nblocks) nblocks = nb;
+  }
+  QuantArgs a = {};
+  a.K = K; a.K8 = K8; a.delta8 = delta8; a.Hkv = shape->Hkv;
+  a.n_max = shape->n_max; a.nblk_max = (shape->n_max + kBlock - 1) / kBlock; a.blk_from = blk_from;
+  if (nblocks > 0) count_launches(1);
+  return cuda_status(launch_quant8(a, seq, shape->B, shape->d, shape->dtype == CSA_BF16, nblocks,
+                                   (cudaStream_t)stream));
 }
 
 csa_status csa_dense_decode(const csa_shape* shape, const void* q, const void* K, const void* V,
@@ -472,8 +570,10 @@ csa_status csa_dense_decode(const csa_shape* shape, const void* q, const void* K
     seq.n[b] = len[b];
     if (len[b] > nlive) nlive = len[b];
   }
-  DenseArgs a;
-  a.q = q; a.K = K; a.V = V; a.part = (float*)workspace; a.o = o; a.state = nullptr; a.nfall = nullptr;
+  if (cudaMemsetAsync(workspace, 0, sizeof(unsigned), (cudaStream_t)stream) != cudaSuccess) return CSA_ERR_CUDA;
+  DenseArgs a = {};
+  a.q = q; a.K = K; a.V = V; a.part = (float*)((char*)workspace + kAlign); a.o = o; a.state = nullptr;
+  a.nfall = nullptr; a.status = (unsigned*)workspace;
   a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max;
   a.nsplit = dense_nsplit(shape->n_max); a.rs = (float)(1.0 / std::sqrt((double)shape->d));
   count_launches(2);
@@ -481,29 +581,38 @@ csa_status csa_dense_decode(const csa_shape* shape, const void* q, const void* K
                                   (cudaStream_t)stream));
 }
 
-csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
-                           const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
-                           const float* vnorm2,
-                           const int64_t* len, const uint64_t* step_seed, float* o, float* beta,
-                           int32_t* level, int32_t* keys_read, csa_head_stats* stats, void* workspace,
-                           size_t workspace_bytes, void* stream) {
-  if (!shape_ok(shape) || !params_ok(params) || !q || !K || !V || !K4 || !bounds || !vmax || !vnorm2 || !len ||
-      !step_seed || !o || !beta || !level || !keys_read)
+}  // extern "C"
+
+namespace csa {
+namespace {
+
+// The step for host or device lengths: checks, then one chain or the
+// sub-batch fork.
+csa_status decode_step_impl(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
+                            const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
+                            const float* vnorm2, const SeqSource& src, float* o, float* beta, int32_t* level,
+                            int32_t* keys_read, csa_head_stats* stats, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!shape_ok(shape) || !params_ok(params) || !q || !K || !V || !K4 || !bounds || !vmax || !vnorm2 ||
+      !src.len || !src.seed || !o || !beta || !level || !keys_read)
     return CSA_ERR_INVALID_ARG;
+  if (params->refine8 && (!src.K8 || !src.delta8)) return CSA_ERR_INVALID_ARG;
   csa_status su = shape_supported(shape);
   if (su != CSA_OK) return su;
+  if (params->refine8 && shape->dtype != CSA_BF16) return CSA_ERR_UNSUPPORTED;
   SubPlan sp;
   if (!sub_plan(shape, params, sp)) return CSA_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < sp.total || ((uintptr_t)workspace % kAlign)) return CSA_ERR_WORKSPACE;
-  for (int b = 0; b < shape->B; ++b)
-    if (len[b] < 1 || len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
+  if (!src.dev)
+    for (int b = 0; b < shape->B; ++b)
+      if (src.len[b] < 1 || src.len[b] > shape->n_max) return CSA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   char* ws = (char*)workspace;
   unsigned* status = (unsigned*)ws;   // offset 0 of (sub-batch 0's) layout
   if (sp.nsub == 1 || g_prof.on) {
     // one stream (phase timing runs unsplit so its events bracket whole phases)
-    return decode_batch(shape, params, q, K, V, K4, bounds, vmax, vnorm2, len, step_seed, o, beta, level,
-                        keys_read, stats, ws, status, true, st);
+    return decode_batch(shape, params, q, K, V, K4, bounds, vmax, vnorm2, src, o, beta, level, keys_read, stats,
+                        ws, status, true, st);
   }
   // sub-batches of consecutive sequences on the library's streams: fork
   // after clearing sub-batch 0's counters (they hold the status word), join
@@ -529,17 +638,69 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, con
     sc.B = (int)std::min<int64_t>(sp.Bc, shape->B - b0);
     cudaStream_t cs = ss->st[c];
     if (cudaStreamWaitEvent(cs, ss->fork, 0) != cudaSuccess) return CSA_ERR_CUDA;
+    SeqSource sc_src = src;
+    sc_src.len = src.len + b0;
+    sc_src.seed = src.seed + b0;
+    if (src.requant) {
+      sc_src.K4w = src.K4w + b0 * Hkv * nblk * kBlock * (D / 2);
+      sc_src.boundsw = src.boundsw + b0 * Hkv * nblk * 2 * D;
+      sc_src.vmaxw = src.vmaxw + b0 * Hkv * nblk;
+      sc_src.vnorm2w = src.vnorm2w + b0 * Hkv * N;
+    }
+    if (src.K8) {
+      sc_src.K8 = src.K8 + b0 * Hkv * nblk * kBlock * D;
+      sc_src.delta8 = src.delta8 + b0 * Hkv * nblk * D;
+    }
     csa_status r = decode_batch(
         &sc, params, (const char*)q + b0 * Hq * D * esz, (const char*)K + b0 * Hkv * N * D * esz,
         (const char*)V + b0 * Hkv * N * D * esz, K4 + b0 * Hkv * nblk * kBlock * (D / 2),
-        bounds + b0 * Hkv * nblk * 2 * D, vmax + b0 * Hkv * nblk, vnorm2 + b0 * Hkv * N, len + b0,
-        step_seed + b0, o + b0 * Hq * D, beta + b0 * Hq, level + b0 * Hq, keys_read + b0 * Hq,
+        bounds + b0 * Hkv * nblk * 2 * D, vmax + b0 * Hkv * nblk, vnorm2 + b0 * Hkv * N, sc_src,
+        o + b0 * Hq * D, beta + b0 * Hq, level + b0 * Hq, keys_read + b0 * Hq,
         stats ? stats + b0 * Hq : nullptr, ws + c * sp.stride, status, c > 0, cs);
     if (r != CSA_OK) return r;
     if (cudaEventRecord(ss->join[c], cs) != cudaSuccess) return CSA_ERR_CUDA;
     if (cudaStreamWaitEvent(st, ss->join[c], 0) != cudaSuccess) return CSA_ERR_CUDA;
   }
   return CSA_OK;
+}
+
+}  // namespace
+}  // namespace csa
+
+extern "C" {
+
+csa_status csa_decode_step(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
+                           const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
+                           const float* vnorm2, const int64_t* len, const uint64_t* step_seed, float* o,
+                           float* beta, int32_t* level, int32_t* keys_read, csa_head_stats* stats, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  SeqSource src = {len, step_seed, false, false, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  return decode_step_impl(shape, params, q, K, V, K4, bounds, vmax, vnorm2, src, o, beta, level, keys_read, stats,
+                          workspace, workspace_bytes, stream);
+}
+
+csa_status csa_decode_step_refined(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
+                                   const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
+                                   const float* vnorm2, const uint8_t* K8, const float* delta8, const int64_t* len,
+                                   const uint64_t* step_seed, float* o, float* beta, int32_t* level,
+                                   int32_t* keys_read, csa_head_stats* stats, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!K8 || !delta8) return CSA_ERR_INVALID_ARG;
+  SeqSource src = {len, step_seed, false, false, nullptr, nullptr, nullptr, nullptr, K8, delta8};
+  return decode_step_impl(shape, params, q, K, V, K4, bounds, vmax, vnorm2, src, o, beta, level, keys_read, stats,
+                          workspace, workspace_bytes, stream);
+}
+
+csa_status csa_decode_step_device(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
+                                  const void* V, uint8_t* K4, float* bounds, float* vmax, float* vnorm2,
+                                  const int64_t* len, const uint64_t* step_seed, int requantize_last, float* o,
+                                  float* beta, int32_t* level, int32_t* keys_read, csa_head_stats* stats,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (requantize_last != 0 && requantize_last != 1) return CSA_ERR_INVALID_ARG;
+  if (params && params->refine8) return CSA_ERR_INVALID_ARG;   // (the refinement takes host lengths)
+  SeqSource src = {len, step_seed, true, requantize_last == 1, K4, bounds, vmax, vnorm2, nullptr, nullptr};
+  return decode_step_impl(shape, params, q, K, V, K4, bounds, vmax, vnorm2, src, o, beta, level, keys_read, stats,
+                          workspace, workspace_bytes, stream);
 }
 
 csa_status csa_profile_enable(int on) {
@@ -577,6 +738,8 @@ csa_status csa_check(void* workspace, void* stream) {
   if (cudaMemcpy(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
   if (w & 1u) return CSA_ERR_NONFINITE;
   if (w & 2u) return CSA_ERR_WORKSPACE;
+  if (w & 4u) return CSA_ERR_TIMEOUT;
+  if (w & 8u) return CSA_ERR_INVALID_ARG;
   return CSA_OK;
 }
 

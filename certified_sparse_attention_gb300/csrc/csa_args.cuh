@@ -2,11 +2,15 @@
 // translation unit (one definition, shared by the host layer).
 #pragma once
 
+#include <cuda.h>
+
 #include "csa_internal.cuh"
 
 namespace csa {
 
 struct ScanArgs {
+  const SeqArgs* seqd;    // per-sequence data in device memory (device-length
+                          // steps), else null: the launch argument holds it
   const void* q;
   const uint8_t* K4;
   const float* bounds;
@@ -17,9 +21,22 @@ struct ScanArgs {
   int Hq, Hkv;
   int64_t n_max, nblk_max;
   float rs;             // float32(1/sqrt d)
+  bool two_digit;       // query codes of two s8 digits (QM = 127 * 257)
+  // fused re-quantisation (device-length steps): the CTA whose tile holds
+  // the block of token n - 1 rebuilds that block's codes, bounds, vmax and
+  // vnorm2 from K and V before it scans it
+  int requant;
+  const void* K;
+  const void* V;
+  uint8_t* K4w;
+  float* boundsw;
+  float* vmaxw;
+  float* vnorm2w;
 };
 
 struct SparseArgs {
+  const SeqArgs* seqd;    // per-sequence data in device memory (device-length
+                          // steps), else null: the launch argument holds it
   const void* q;
   const void* K;
   const void* V;
@@ -38,6 +55,17 @@ struct SparseArgs {
   float* vmaxp;           // [B*Hkv]              max vmax over pool blocks
   int* state;             // [B*Hq][4]            lo, hi, stop, flags
   float* t32;             // [B*Hkv][pcap]([G])   perturbation t_i = -log2 u_i (per head if per_head)
+  // 8-bit refinement tier (refine8 != 0)
+  const uint8_t* K8;      // [B*Hkv][nblk_max*64][D] 8-bit codes
+  const float* delta8;    // [B*Hkv][nblk_max][D]
+  const float* bounds;    // [B*Hkv][nblk_max][2][D] (the minima m_c)
+  uint16_t* jkey;         // [B*Hkv][pcap] per pool key: smallest bound level over the heads that
+                          // can still need its row (bits 0-8; 0x1FF none), refined (bit 9),
+                          // in the exact-max set (bit 10)
+  int* jrd;               // [B*Hq][J1+1] keys_read histogram moves of the refinement
+  uint16_t* jref;         // [B*Hkv][pcap][G] refined level of a refined key per head (diagnostics)
+  unsigned* ninset;       // [B*Hq] pool keys in the head's exact-max set
+  int refine8;            // 0 off, 1 every group, 2 groups whose first range reaches level r
   float* pref;            // [B*Hq][ACC]          a continuing head's sums through its last range
   uint2* xlist;           // [B*Hkv][n_max]       exact-max set: key, head mask
   unsigned* xcnt;         // [B*Hkv]
@@ -75,6 +103,8 @@ struct SparseArgs {
 };
 
 struct DenseArgs {
+  const SeqArgs* seqd;    // per-sequence data in device memory (device-length
+                          // steps), else null: the launch argument holds it
   const void* q;
   const void* K;
   const void* V;
@@ -82,6 +112,7 @@ struct DenseArgs {
   float* o;               // [B*Hq][D]
   const int* state;       // optional [B*Hq][4]: only heads with flag bit 0
   const unsigned* nfall;  // optional: skip everything when it reads 0
+  unsigned* status;       // optional: status word (bit 4: a bounded wait gave up)
   int B, Hq, Hkv;
   int64_t n_max;
   int nsplit;
@@ -89,12 +120,16 @@ struct DenseArgs {
 };
 
 struct QuantArgs {
+  const SeqArgs* seqd;    // per-sequence data in device memory (device-length
+                          // steps), else null: the launch argument holds it
   const void* K;
   const void* V;
   uint8_t* K4;
   float* bounds;
   float* vmax;
   float* vnorm2;
+  uint8_t* K8;          // 8-bit codes [B*Hkv][nblk_max*64][D] (quant8_kernel)
+  float* delta8;        // [B*Hkv][nblk_max][D]
   int Hkv;
   int64_t n_max, nblk_max;
   int64_t blk_from;
@@ -114,7 +149,11 @@ cudaError_t launch_dense(const DenseArgs&, const SeqArgs&, int d, int G, bool bf
                          cudaStream_t);
 cudaError_t launch_quant(const QuantArgs&, const SeqArgs&, int B, int d, bool bf16, int64_t nblocks,
                          cudaStream_t);
+cudaError_t launch_quant8(const QuantArgs&, const SeqArgs&, int B, int d, bool bf16, int64_t nblocks,
+                          cudaStream_t);
 int dense_nsplit(int64_t n_max);
+cudaError_t launch_seq_prep(const int64_t* len, const uint64_t* seed, int B, int64_t n_max, int r, int J_override,
+                            SeqArgs* out, unsigned* status, cudaStream_t);
 
 // Launch with programmatic stream serialisation (see pdl_entry).
 template <typename... KArgs, typename... Args>
@@ -141,5 +180,13 @@ void add_launches(int k);   // adds to the launch count csa_profile_read reports
 // array, library streams) is keyed on this id: after a device reset the
 // runtime creates a new primary context, with a new id.
 bool current_context_id(unsigned long long* id);
+
+// A 2-D tensor map over a row-major array of `rows` rows of `inner` 16-bit
+// elements (row pitch `pitch_bytes`), box = box_inner x box_rows elements,
+// 128-byte swizzle, zero fill out of bounds (cuTensorMapEncodeTiled, reached
+// through the runtime's driver entry points).  False if the driver refuses
+// (base or pitch not 16-byte aligned, sizes out of range).
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                       uint32_t box_inner, uint32_t box_rows);
 
 }  // namespace csa

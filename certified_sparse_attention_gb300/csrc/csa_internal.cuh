@@ -191,6 +191,173 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
+// --------------------------------------------- bulk tensor copies (TMA)
+//
+// Tiles move from global to shared memory with cp.async.bulk.tensor (the
+// tensor memory accelerator), completing on an mbarrier with a transaction
+// byte count.  Every wait on an mbarrier is bounded in time: after
+// kWaitNs nanoseconds it gives up and returns false, the caller records
+// CSA_ERR_TIMEOUT in the status word and leaves.
+
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+// make initialised barriers visible to the async proxy (the copies)
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+// wait for the phase of parity `parity` to complete; false after kWaitNs
+__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity) {
+  unsigned long long t0 = 0;
+  for (unsigned it = 0;; ++it) {
+    unsigned done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (it == 0) t0 = global_ns();
+    else if ((it & 63u) == 0u && global_ns() - t0 > kWaitNs) return false;
+  }
+}
+// 2-D tiled load of box (x, y) of `map` into shared memory at dst
+__device__ __forceinline__ void tma_load_2d(unsigned dst, const void* map, int x, int y, unsigned bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];\n" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// barrier over the first `count` threads of the CTA (named barrier `id`)
+__device__ __forceinline__ void bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
+// ------------------------------------------------------ block quantiser
+//
+// 4-bit per-block, per-channel key codes and the block's value-norm data
+// (picx.dev "Algorithm Components" 4, the KIVI scheme).  For the 64-token
+// block `blk` of group bg (aligned to position 0; tokens present: those
+// below n) and channel c:
+//   m_c = min, Delta_c = fl((max - min) / 15) (0 -> 1),
+//   code = clamp(rint(fl(fl(k - m_c) / Delta_c)), 0, 15)   (ties to even),
+// two codes per byte with the even channel in the low nibble (positions of
+// the block at or past n get code 0 and vnorm2 0).  vnorm2 of a token is
+// the sequential float32 sum of v_c^2; vmax of the block = max over its
+// tokens of sqrt(vnorm2), times (1 + 2^-16): an upper bound on every
+// ||v_i|| of the block.  Thread c < D owns channel c; every thread of the
+// CTA calls it (it holds a barrier).
+template <int D, typename E>
+__device__ __forceinline__ void quantize_block(const void* K, const void* V, uint8_t* K4, float* bounds,
+                                               float* vmax, float* vnorm2, int64_t n_max, int64_t nblk_max,
+                                               int bg, int64_t blk, int64_t n, float* s_vm) {
+  const int c = threadIdx.x;
+  const int64_t t0 = blk * kBlock;
+  const int rows = (int)min((int64_t)kBlock, n - t0);
+  const E* Kb = reinterpret_cast<const E*>(K) + ((int64_t)bg * n_max + t0) * D;
+  const E* Vb = reinterpret_cast<const E*>(V) + ((int64_t)bg * n_max + t0) * D;
+  if (c < D) {
+    float mn = INFINITY, mx = -INFINITY;
+    for (int t = 0; t < rows; ++t) {
+      const float k = Elem<E>::get(Kb, (int64_t)t * D + c);
+      mn = fminf(mn, k);
+      mx = fmaxf(mx, k);
+    }
+    float dl = fdiv(fsub(mx, mn), 15.0f);
+    if (dl == 0.0f) dl = 1.0f;
+    float* bp = bounds + ((int64_t)bg * nblk_max + blk) * 2 * D;
+    bp[c] = mn;
+    bp[D + c] = dl;
+    uint8_t* kp = K4 + ((int64_t)bg * nblk_max * kBlock + t0) * (D / 2);
+    for (int t = 0; t < kBlock; ++t) {
+      int code = 0;
+      if (t < rows) {
+        const float k = Elem<E>::get(Kb, (int64_t)t * D + c);
+        float x = rintf(fdiv(fsub(k, mn), dl));
+        x = fminf(fmaxf(x, 0.0f), 15.0f);
+        code = (int)x;
+      }
+      const int hi = __shfl_down_sync(0xffffffffu, code, 1);
+      if ((c & 1) == 0) kp[(int64_t)t * (D / 2) + c / 2] = (uint8_t)(code | (hi << 4));
+    }
+  }
+  // value norms: thread t < rows walks its row sequentially
+  if (c < kBlock) {
+    float nrm = 0.0f, ss = 0.0f;
+    if (c < rows) {
+      for (int x = 0; x < D; ++x) {
+        const float v = Elem<E>::get(Vb, (int64_t)c * D + x);
+        ss = fadd(ss, fmul(v, v));
+      }
+      nrm = __fsqrt_rn(ss);
+    }
+    s_vm[c] = nrm;
+    if (t0 + c < n_max) vnorm2[(int64_t)bg * n_max + t0 + c] = ss;
+  }
+  __syncthreads();
+  if (c == 0) {
+    float m = 0.0f;
+    for (int t = 0; t < rows; ++t) m = fmaxf(m, s_vm[t]);
+    vmax[(int64_t)bg * nblk_max + blk] = fmul(m, 1.0000152587890625f);
+  }
+}
+
+// 8-bit codes of the same blocks for the refinement tier (picx.dev
+// "Algorithm Components" 4: an 8-bit stage between the 4-bit candidates and
+// the exact 16-bit reads): per block and channel the same minimum m_c,
+// Delta8_c = fl((max - min) / 255) (0 -> 1),
+// code = clamp(rint(fl(fl(k - m_c) / Delta8_c)), 0, 255); one byte per code,
+// positions at or past n get code 0.  Thread c < D owns channel c.
+template <int D, typename E>
+__device__ __forceinline__ void quantize_block8(const void* K, uint8_t* K8, float* delta8, int64_t n_max,
+                                                int64_t nblk_max, int bg, int64_t blk, int64_t n) {
+  const int c = threadIdx.x;
+  if (c >= D) return;
+  const int64_t t0 = blk * kBlock;
+  const int rows = (int)min((int64_t)kBlock, n - t0);
+  const E* Kb = reinterpret_cast<const E*>(K) + ((int64_t)bg * n_max + t0) * D;
+  float mn = INFINITY, mx = -INFINITY;
+  for (int t = 0; t < rows; ++t) {
+    const float k = Elem<E>::get(Kb, (int64_t)t * D + c);
+    mn = fminf(mn, k);
+    mx = fmaxf(mx, k);
+  }
+  float dl = fdiv(fsub(mx, mn), 255.0f);
+  if (dl == 0.0f) dl = 1.0f;
+  delta8[((int64_t)bg * nblk_max + blk) * D + c] = dl;
+  uint8_t* kp = K8 + ((int64_t)bg * nblk_max * kBlock + t0) * D;
+  for (int t = 0; t < kBlock; ++t) {
+    int code = 0;
+    if (t < rows) {
+      const float k = Elem<E>::get(Kb, (int64_t)t * D + c);
+      float x = rintf(fdiv(fsub(k, mn), dl));
+      x = fminf(fmaxf(x, 0.0f), 255.0f);
+      code = (int)x;
+    }
+    kp[(int64_t)t * D + c] = (uint8_t)code;
+  }
+}
+
 // ------------------------------------------------------ warp row products
 //
 // Eight rows at a time: lane l holds channels [l*CPL, (l+1)*CPL) of every

@@ -34,9 +34,16 @@ __device__ __forceinline__ float tree16(const float* v) {
   return s;
 }
 
-template <int D, int G, typename E>
-__global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq) {
+// TWO: query codes of two s8 digits, at = 256 hi + lo with |at| <= 127 * 257,
+// and the closed-form residual term fl(fl(15 d) * fl(alpha * (1/2 + 2^-6)))
+// in place of the two residual trees (|a_c - alpha at_c| <= alpha (1/2 +
+// 2^-6) for codes this fine); I = 256 I_hi + I_lo from two products.
+template <int D, int G, typename E, bool TWO, bool REQ>
+__global__ void __launch_bounds__(256, 6) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq_arg) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
+  constexpr int ND = TWO ? 2 : 1;    // query-code digits
+  constexpr float QMF = TWO ? 32639.0f : 127.0f;
   constexpr int CPT = D / 16;        // channels per prep thread
   constexpr int ROWB = D / 2;        // bytes of codes per key
   constexpr int CHR = ROWB / 16;     // 16-byte chunks per key
@@ -44,7 +51,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
   __shared__ __align__(16) uint8_t s_codes[kTile * ROWB];
   __shared__ __align__(16) float s_bnd[4][2][D];
   __shared__ __align__(16) float s_qt[G][D];
-  __shared__ __align__(16) unsigned s_atw[4][G][2 * WE];
+  __shared__ __align__(16) unsigned s_atw[ND][4][G][2 * WE];   // [digit]: lo, hi
   __shared__ float s_q1[G];
   __shared__ float s_alpha[4][G], s_bhi[4][G], s_blo[4][G];
   __shared__ float s_red[8][G][2];
@@ -57,6 +64,16 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
   const int64_t key0 = (int64_t)blockIdx.x * kTile;
   if (key0 >= n) return;
   const int64_t nblk_n = (n + kBlock - 1) / kBlock;
+  if (REQ) {
+    // the appended token's block, rebuilt before this tile is staged
+    __shared__ float s_qvm[kBlock];
+    const int64_t lb = (n - 1) / kBlock;
+    if (lb * kBlock >= key0 && lb * kBlock < key0 + kTile) {
+      quantize_block<D, E>(a.K, a.V, a.K4w, a.boundsw, a.vmaxw, a.vnorm2w, a.n_max, a.nblk_max, bg, lb, n, s_qvm);
+      __threadfence();   // the new codes and bounds reach L2 before the copies below read them
+      __syncthreads();
+    }
+  }
 
   // 1. stage the block bounds (first group: the query prep needs them) and
   // the codes (second group: the dot products need them)
@@ -132,30 +149,42 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
     }
     float alpha = 0.f, inv = 0.f;
     if (amax > 0.f) {
-      alpha = fdiv(amax, 127.0f);
-      inv = fdiv(127.0f, amax);
+      alpha = fdiv(amax, QMF);
+      inv = fdiv(QMF, amax);
     }
     float tb[CPT], ta[CPT], tp[CPT], tn[CPT];
     int at[CPT];
 #pragma unroll
     for (int k = 0; k < CPT; ++k) {
       float x = rintf(fmul(av[k], inv));
-      x = fminf(fmaxf(x, -127.0f), 127.0f);
+      x = fminf(fmaxf(x, -QMF), QMF);
       at[k] = (int)x;
-      float r = fsub(av[k], fmul(alpha, x));
       tb[k] = fmul(s_qt[h][c0 + k], mv[k]);
       ta[k] = fabsf(av[k]);
-      tp[k] = fmaxf(r, 0.0f);
-      tn[k] = fmaxf(-r, 0.0f);
+      if (!TWO) {
+        float r = fsub(av[k], fmul(alpha, x));
+        tp[k] = fmaxf(r, 0.0f);
+        tn[k] = fmaxf(-r, 0.0f);
+      }
     }
     float Bq = tree16<CPT>(tb);
     float A1 = tree16<CPT>(ta);
-    float Rp = tree16<CPT>(tp);
-    float Rn = tree16<CPT>(tn);
+    float Rp = 0.f, Rn = 0.f;
+    if (!TWO) {
+      Rp = tree16<CPT>(tp);
+      Rn = tree16<CPT>(tn);
+    }
     if (l16 == 0) {
       float sk = fmul(A1, 0.5000152587890625f);
-      float hi = fadd(sk, fmul(15.0f, Rp));
-      float lo = fadd(sk, fmul(15.0f, Rn));
+      float hi, lo;
+      if (TWO) {
+        const float res = fmul((float)(15 * D), fmul(alpha, 0.515625f));
+        hi = fadd(sk, res);
+        lo = fadd(sk, res);
+      } else {
+        hi = fadd(sk, fmul(15.0f, Rp));
+        lo = fadd(sk, fmul(15.0f, Rn));
+      }
       float mag = fadd(fadd(fmul(s_q1[h], kabs), hi), lo);
       float marg = fmul(mag, 6.103515625e-05f);      // 2^-14
       float bhi = fadd(fadd(Bq, hi), marg);
@@ -169,18 +198,29 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
       if (gblk < nblk_n) a.hw[((int64_t)bg * a.nblk_max + gblk) * G + h] = fmul(0.5f, fsub(bhi, blo));
       if (!isfinite(bhi) || !isfinite(blo) || !isfinite(alpha)) atomicOr(a.status, 1u);
     }
-    // pack the code: word w covers channels 8w..8w+7; even word = channels
-    // 8w, 8w+2, 8w+4, 8w+6 (bytes 0..3), odd word = 8w+1, ..., 8w+7
-    if (CPT == 8) {
-      unsigned ev = (at[0] & 0xFF) | ((at[2] & 0xFF) << 8) | ((at[4] & 0xFF) << 16) | ((unsigned)(at[6] & 0xFF) << 24);
-      unsigned od = (at[1] & 0xFF) | ((at[3] & 0xFF) << 8) | ((at[5] & 0xFF) << 16) | ((unsigned)(at[7] & 0xFF) << 24);
-      s_atw[blk][h][l16] = ev;
-      s_atw[blk][h][WE + l16] = od;
-    } else {
-      unsigned short ev = (unsigned short)((at[0] & 0xFF) | ((at[2] & 0xFF) << 8));
-      unsigned short od = (unsigned short)((at[1] & 0xFF) | ((at[3] & 0xFF) << 8));
-      reinterpret_cast<unsigned short*>(&s_atw[blk][h][0])[l16] = ev;
-      reinterpret_cast<unsigned short*>(&s_atw[blk][h][WE])[l16] = od;
+    // pack the code (each digit): word w covers channels 8w..8w+7; even
+    // word = channels 8w, 8w+2, 8w+4, 8w+6 (bytes 0..3), odd word = 8w+1,
+    // ..., 8w+7.  Two digits: hi = floor((at + 128) / 256) in [-127, 127],
+    // lo = at - 256 hi in [-128, 127].
+#pragma unroll
+    for (int dd = 0; dd < ND; ++dd) {
+      int dg[CPT];
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) {
+        const int hi = (at[k] + 128) >> 8;      // arithmetic shift: floor
+        dg[k] = !TWO ? at[k] : (dd == 0 ? at[k] - 256 * hi : hi);
+      }
+      if (CPT == 8) {
+        unsigned ev = (dg[0] & 0xFF) | ((dg[2] & 0xFF) << 8) | ((dg[4] & 0xFF) << 16) | ((unsigned)(dg[6] & 0xFF) << 24);
+        unsigned od = (dg[1] & 0xFF) | ((dg[3] & 0xFF) << 8) | ((dg[5] & 0xFF) << 16) | ((unsigned)(dg[7] & 0xFF) << 24);
+        s_atw[dd][blk][h][l16] = ev;
+        s_atw[dd][blk][h][WE + l16] = od;
+      } else {
+        unsigned short ev = (unsigned short)((dg[0] & 0xFF) | ((dg[2] & 0xFF) << 8));
+        unsigned short od = (unsigned short)((dg[1] & 0xFF) | ((dg[3] & 0xFF) << 8));
+        reinterpret_cast<unsigned short*>(&s_atw[dd][blk][h][0])[l16] = ev;
+        reinterpret_cast<unsigned short*>(&s_atw[dd][blk][h][WE])[l16] = od;
+      }
     }
   }
   cp_async_wait<0>();            // the codes too
@@ -197,17 +237,21 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
   const int gq = lane >> 2, tq = lane & 3;
   const int blk = w >> 1;
   constexpr int KS = D / 32;
-  unsigned bq[KS][2];
+  unsigned bq[ND][KS][2];
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    bq[ks][0] = gq < G ? s_atw[blk][gq < G ? gq : 0][4 * ks + tq] : 0u;
-    bq[ks][1] = gq < G ? s_atw[blk][gq < G ? gq : 0][WE + 4 * ks + tq] : 0u;
-  }
+  for (int dd = 0; dd < ND; ++dd)
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      bq[dd][ks][0] = gq < G ? s_atw[dd][blk][gq < G ? gq : 0][4 * ks + tq] : 0u;
+      bq[dd][ks][1] = gq < G ? s_atw[dd][blk][gq < G ? gq : 0][WE + 4 * ks + tq] : 0u;
+    }
   float lmax[2] = {-INFINITY, -INFINITY}, umax[2] = {-INFINITY, -INFINITY};   // heads 2tq, 2tq+1
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
     const int r0 = 32 * w + 16 * mt + gq, r1 = r0 + 8;
-    int acc[4] = {0, 0, 0, 0};
+    int acc[ND][4];
+#pragma unroll
+    for (int dd = 0; dd < ND; ++dd) acc[dd][0] = acc[dd][1] = acc[dd][2] = acc[dd][3] = 0;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       // word 4ks+tq of rows r0, r1: chunk ks, word tq (swizzled chunks)
@@ -215,12 +259,18 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
       const unsigned w1 = *reinterpret_cast<const unsigned*>(s_codes + r1 * ROWB + ((ks ^ (r1 & (CHR - 1))) << 4) + 4 * tq);
       const unsigned af0 = w0 & 0x0F0F0F0Fu, af1 = w1 & 0x0F0F0F0Fu;
       const unsigned af2 = (w0 >> 4) & 0x0F0F0F0Fu, af3 = (w1 >> 4) & 0x0F0F0F0Fu;
-      asm volatile(
-          "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-          "{%0,%1,%2,%3};\n"
-          : "+r"(acc[0]), "+r"(acc[1]), "+r"(acc[2]), "+r"(acc[3])
-          : "r"(af0), "r"(af1), "r"(af2), "r"(af3), "r"(bq[ks][0]), "r"(bq[ks][1]));
+#pragma unroll
+      for (int dd = 0; dd < ND; ++dd)
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+r"(acc[dd][0]), "+r"(acc[dd][1]), "+r"(acc[dd][2]), "+r"(acc[dd][3])
+            : "r"(af0), "r"(af1), "r"(af2), "r"(af3), "r"(bq[dd][ks][0]), "r"(bq[dd][ks][1]));
     }
+    // I = 256 I_hi + I_lo (|I| < 2^26: exact in int32)
+    int I4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) I4[e] = TWO ? acc[ND - 1][e] * 256 + acc[0][e] : acc[0][e];
     // acc[0], acc[1]: key r0, heads 2tq, 2tq+1; acc[2], acc[3]: key r1
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -233,7 +283,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
         const int h = 2 * tq + u;
         ubv[u] = 0.f;
         if (h < G) {
-          const float aI = fmul(s_alpha[blk][h], (float)acc[2 * half + u]);
+          const float aI = fmul(s_alpha[blk][h], (float)I4[2 * half + u]);
           const float ub = fadd(aI, s_bhi[blk][h]);
           const float lo = fadd(aI, s_blo[blk][h]);
           ubv[u] = ub;
@@ -278,7 +328,16 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
 template <int D, int G, typename E>
 cudaError_t launch_scan_t(const ScanArgs& a, const SeqArgs& seq, int B, int64_t nmax_live, cudaStream_t st) {
   dim3 grid((unsigned)((nmax_live + kTile - 1) / kTile), (unsigned)(B * a.Hkv));
-  launch_pdl(scan_kernel<D, G, E>, grid, dim3(256), 0, st, a, seq);
+  // REQ: the variant that re-quantises the appended block first (device-
+  // length steps); a separate instantiation keeps the plain scan's
+  // registers (and resident CTAs) as they are
+  if (a.requant) {
+    if (a.two_digit) launch_pdl(scan_kernel<D, G, E, true, true>, grid, dim3(256), 0, st, a, seq);
+    else launch_pdl(scan_kernel<D, G, E, false, true>, grid, dim3(256), 0, st, a, seq);
+  } else {
+    if (a.two_digit) launch_pdl(scan_kernel<D, G, E, true, false>, grid, dim3(256), 0, st, a, seq);
+    else launch_pdl(scan_kernel<D, G, E, false, false>, grid, dim3(256), 0, st, a, seq);
+  }
   return cudaGetLastError();
 }
 

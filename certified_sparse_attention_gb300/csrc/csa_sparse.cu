@@ -189,9 +189,10 @@ constexpr int kCsetTiles = 16;   // 256-key tiles staged between list flushes
 // A CTA covers `span` keys (a multiple of 256) of one group; grids are
 // sized to the resident CTA count so the pass runs in one wave.
 template <int G>
-__global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+__global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
                                                    int span) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   // members are staged in shared memory and take one slot range of the
   // group's list per 16 tiles (a per-warp reservation on the group's
   // counter serialises)
@@ -278,9 +279,10 @@ __host__ __device__ constexpr int rows_smem() {
 }
 
 template <int D, int G, typename E, int MODE>
-__global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+__global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
                                                    int round) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   constexpr int CPL = D / 32;
   constexpr int RB = D * (int)sizeof(E);
   extern __shared__ __align__(16) uint8_t dsm[];
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
       const uint2 e = ck == 0 ? cw[0] : (ck == 1 ? cw[1] : (ck == 2 ? cw[2] : cw[3]));
       bool keep = e.x != ~0u;
       if (MODE == 1 && keep) {
-        const int jm = (int)((e.y >> 8) & 0xFFu);
+        const int jm = a.refine8 ? (int)(a.jkey[(int64_t)bg * a.pcap + e.x] & 0x1FFu) : (int)((e.y >> 8) & 0xFFu);
         keep = jm > lold && jm <= lnew;
       }
       const unsigned bal = __ballot_sync(0xffffffffu, keep);
@@ -527,9 +529,10 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
 constexpr int kRsel = 4096;      // list entries per CTA
 
 template <int G>
-__global__ void __launch_bounds__(256) rsel_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+__global__ void __launch_bounds__(256) rsel_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
                                                    int round) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   __shared__ uint2 s_list[kRsel];
   __shared__ unsigned s_n, s_gbase;
   const int tid = threadIdx.x;
@@ -558,7 +561,7 @@ __global__ void __launch_bounds__(256) rsel_kernel(const SparseArgs a, const __g
     bool keep = false;
     if (i < cnt) {
       e = cl[i];
-      const int jm = (int)((e.y >> 8) & 0xFFu);
+      const int jm = a.refine8 ? (int)(a.jkey[(int64_t)bg * a.pcap + e.x] & 0x1FFu) : (int)((e.y >> 8) & 0xFFu);
       keep = jm > lold && jm <= lnew;
     }
     const int slot = warp_append(&s_n, keep);
@@ -568,6 +571,255 @@ __global__ void __launch_bounds__(256) rsel_kernel(const SparseArgs a, const __g
   if (tid == 0) s_gbase = s_n ? atomicAdd(a.rcnt + round * BG + bg, s_n) : 0u;
   __syncthreads();
   for (unsigned i = tid; i < s_n; i += 256) a.rlist[(int64_t)bg * a.pcap + s_gbase + i] = s_list[i];
+}
+
+// ------------------------------------------------- 8-bit refinement tier
+//
+// picx.dev "Algorithm Components" 4: an 8-bit stage between the 4-bit
+// candidates and the exact 16-bit reads.  Before a round's rescoring, every
+// pool key whose smallest bound level lies in the range the round newly
+// needs also gets the upper bound ubar8 from its 8-bit codes (same blocks
+// and minima, 255 levels, 12-bit query codes: the 4-bit construction with
+// 15 -> 255, 16 -> 256 and QM = 2047), and per head the refined bound level
+//   jref = max(0, ceil(fl(fl(-r xbar) - 2^-10))),
+//   xbar = fl(fl(fl(min(ubar4, ubar8) - cb) * log2e) + t).
+// jbar <= jref <= the exact level, so the sample, the estimates and every
+// result stay the same; the key's smallest level over its heads becomes the
+// smallest jref, and a key whose jref lies past the round's range waits for
+// a later round (or is never read).  keys_read counts jref instead of jbar.
+// One warp per 64-key block with a key to refine: it stages the block's
+// 8-bit rows of those keys, codes the query per head (one lane per four
+// channels, the same adjacent-pair float32 trees as the 4-bit query codes),
+// and takes the exact integer dots on tensor cores (u8 codes x two s8
+// digits of the 12-bit query codes, mma.sync m16n8k32).
+constexpr int kRfW = 4;          // warps per refinement CTA
+
+template <int D, int G>
+struct RfLayout {
+  static constexpr int rows = 0;                         // [64][D] u8, 16-byte chunks swizzled
+  static constexpr int dig = rows + 64 * D;              // [2][8][D] s8 query digits (lo, hi)
+  static constexpr int ub8 = dig + 2 * 8 * D;            // [64][8] float ubar8
+  static constexpr int per_warp = ub8 + 64 * 8 * 4;
+  static constexpr int hist = kRfW * per_warp;           // [G][J1+1] int (after the warps)
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kRfW * 32) refine8_kernel(const SparseArgs a,
+                                                          const __grid_constant__ SeqArgs seq_arg, int round) {
+  pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
+  using Lt = RfLayout<D, G>;
+  constexpr int CPL = D / 32;          // channels per lane in the query code
+  constexpr int CH = D / 16;           // 16-byte chunks per 8-bit row
+  constexpr int KS = D / 32;           // k-steps of the dots
+  extern __shared__ __align__(16) uint8_t dsm[];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int BG = a.B * a.Hkv;
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int64_t n = seq.n[b];
+  if (n <= kWindow) return;
+  const int64_t P = n - kWindow;
+  const int J = seq.J[b];
+  const int JS = a.J1 + 1;
+  const int bh0 = b * a.Hq + g * G;
+  const int lold = a.front[round * BG + bg] - 1;
+  int lnew = -1;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const int* st = a.state + (int64_t)(bh0 + h) * 4;
+    if (!(st[3] & kFlagDone)) lnew = max(lnew, st[1]);
+  }
+  if (lnew <= lold) return;
+  if (a.refine8 == 2 && round == 0 && lnew < a.r) return;   // a group that stops near level 0
+  int* s_hd = reinterpret_cast<int*>(dsm + Lt::hist);
+  for (int i = tid; i < G * JS; i += kRfW * 32) s_hd[i] = 0;
+  __syncthreads();
+  uint8_t* my = dsm + w * Lt::per_warp;
+  uint8_t* s_rows = my + Lt::rows;
+  int8_t* s_dig = reinterpret_cast<int8_t*>(my + Lt::dig);
+  float* s_u8 = reinterpret_cast<float*>(my + Lt::ub8);
+  // per head: the scaled query channels of this lane and tree(|qt|)
+  const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q) + ((int64_t)b * a.Hq + (int64_t)g * G) * D;
+  float qt[G][CPL], q1[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float ab[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      qt[h][c] = fmul(__bfloat162float(qp[(int64_t)h * D + lane * CPL + c]), a.rs);
+      ab[c] = fabsf(qt[h][c]);
+    }
+    float s1 = local_tree<CPL>(ab);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) s1 = fadd(s1, __shfl_xor_sync(0xffffffffu, s1, o));
+    q1[h] = s1;
+  }
+  float clo[G], cbv[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) { clo[h] = cmax_get(a, bh0 + h, 0); cbv[h] = cmax_get(a, bh0 + h, 2); }
+  const float neg_r = -(float)a.r;
+  uint16_t* jk = a.jkey + (int64_t)bg * a.pcap;
+  const int64_t nblk_p = (P + kBlock - 1) / kBlock;
+  const int64_t nwarp = (int64_t)gridDim.x * kRfW;
+  for (int64_t blk = (int64_t)blockIdx.x * kRfW + w; blk < nblk_p; blk += nwarp) {
+    const int64_t k0 = blk * kBlock;
+    // keys of the block to refine in this round
+    bool sel[2];
+    unsigned jkv[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int64_t key = k0 + lane + 32 * x;
+      jkv[x] = key < P ? jk[key] : 0x1FFu;
+      const int jm = (int)(jkv[x] & 0x1FFu);
+      sel[x] = !(jkv[x] & 0x200u) && jm > lold && jm <= lnew;
+    }
+    const unsigned m0 = __ballot_sync(0xffffffffu, sel[0]), m1 = __ballot_sync(0xffffffffu, sel[1]);
+    if (!(m0 | m1)) continue;
+    // stage the selected keys' 8-bit rows (others zero), chunk c of row r
+    // at chunk c ^ (r mod CH)
+    const uint8_t* src = a.K8 + ((int64_t)bg * a.nblk_max * kBlock + k0) * D;
+    for (int c = lane; c < 64 * CH; c += 32) {
+      const int r = c / CH, part = c - r * CH;
+      const bool ok = ((r < 32 ? m0 >> r : m1 >> (r - 32)) & 1u) != 0u;
+      cp_async16(s_rows + r * D + ((part ^ (r & (CH - 1))) << 4), ok ? src + (int64_t)r * D + part * 16 : src, ok);
+    }
+    cp_async_commit();
+    // 12-bit query codes of the block per head, as two s8 digits
+    const float* mins = a.bounds + ((int64_t)bg * a.nblk_max + blk) * 2 * D;
+    const float* dl8 = a.delta8 + ((int64_t)bg * a.nblk_max + blk) * D;
+    float mv[CPL], dv[CPL];
+    float kabs = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      mv[c] = mins[lane * CPL + c];
+      dv[c] = dl8[lane * CPL + c];
+      kabs = fmaxf(kabs, fadd(fabsf(mv[c]), fmul(256.0f, dv[c])));
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) kabs = fmaxf(kabs, __shfl_xor_sync(0xffffffffu, kabs, o));
+    float alpha8[G], bhi8[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float av[CPL], tb[CPL], ta[CPL], tp[CPL], tn[CPL];
+      float amax = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        av[c] = fmul(qt[h][c], dv[c]);
+        amax = fmaxf(amax, fabsf(av[c]));
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      float al = 0.f, inv = 0.f;
+      if (amax > 0.f) {
+        al = fdiv(amax, 2047.0f);
+        inv = fdiv(2047.0f, amax);
+      }
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        float x = rintf(fmul(av[c], inv));
+        x = fminf(fmaxf(x, -2047.0f), 2047.0f);
+        const int at = (int)x;
+        const float r = fsub(av[c], fmul(al, x));
+        tb[c] = fmul(qt[h][c], mv[c]);
+        ta[c] = fabsf(av[c]);
+        tp[c] = fmaxf(r, 0.0f);
+        tn[c] = fmaxf(-r, 0.0f);
+        const int hi = (at + 128) >> 8;           // floor((at + 128) / 256), in [-8, 8]
+        s_dig[(0 * 8 + h) * D + lane * CPL + c] = (int8_t)(at - 256 * hi);
+        s_dig[(1 * 8 + h) * D + lane * CPL + c] = (int8_t)hi;
+      }
+      float Bq = local_tree<CPL>(tb), A1 = local_tree<CPL>(ta), Rp = local_tree<CPL>(tp), Rn = local_tree<CPL>(tn);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        Bq = fadd(Bq, __shfl_xor_sync(0xffffffffu, Bq, o));
+        A1 = fadd(A1, __shfl_xor_sync(0xffffffffu, A1, o));
+        Rp = fadd(Rp, __shfl_xor_sync(0xffffffffu, Rp, o));
+        Rn = fadd(Rn, __shfl_xor_sync(0xffffffffu, Rn, o));
+      }
+      const float sk = fmul(A1, 0.5000152587890625f);
+      const float hi = fadd(sk, fmul(255.0f, Rp));
+      const float lo = fadd(sk, fmul(255.0f, Rn));
+      const float mag = fadd(fadd(fmul(q1[h], kabs), hi), lo);
+      const float marg = fmul(mag, 6.103515625e-05f);     // 2^-14
+      alpha8[h] = al;
+      bhi8[h] = fadd(fadd(Bq, hi), marg);
+    }
+    if (G < 8) {
+      // padding heads: zero digits
+      for (int i = lane; i < (8 - G) * D; i += 32) {
+        s_dig[(0 * 8 + G) * D + i] = 0;
+        s_dig[(1 * 8 + G) * D + i] = 0;
+      }
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+    // exact integer dots: 4 tiles of 16 keys x 8 heads, two digits
+    const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int r0 = 16 * mt + gq, r1 = r0 + 8;
+      int acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        // bytes 32ks + 4tq.. (chunk 2ks) and 32ks + 16 + 4tq.. (chunk 2ks + 1)
+        const unsigned a0 = *reinterpret_cast<const unsigned*>(s_rows + r0 * D + (((2 * ks) ^ (r0 & (CH - 1))) << 4) + 4 * tq);
+        const unsigned a1 = *reinterpret_cast<const unsigned*>(s_rows + r1 * D + (((2 * ks) ^ (r1 & (CH - 1))) << 4) + 4 * tq);
+        const unsigned a2 = *reinterpret_cast<const unsigned*>(s_rows + r0 * D + (((2 * ks + 1) ^ (r0 & (CH - 1))) << 4) + 4 * tq);
+        const unsigned a3 = *reinterpret_cast<const unsigned*>(s_rows + r1 * D + (((2 * ks + 1) ^ (r1 & (CH - 1))) << 4) + 4 * tq);
+#pragma unroll
+        for (int dd = 0; dd < 2; ++dd) {
+          const unsigned b0 = *reinterpret_cast<const unsigned*>(s_dig + (dd * 8 + gq) * D + 32 * ks + 4 * tq);
+          const unsigned b1 = *reinterpret_cast<const unsigned*>(s_dig + (dd * 8 + gq) * D + 32 * ks + 16 + 4 * tq);
+          asm volatile(
+              "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+              "{%0,%1,%2,%3};\n"
+              : "+r"(acc[dd][0]), "+r"(acc[dd][1]), "+r"(acc[dd][2]), "+r"(acc[dd][3])
+              : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = 2 * tq + (e & 1);
+        const int r = (e < 2) ? r0 : r1;
+        if (h < G) {
+          const int I = acc[1][e] * 256 + acc[0][e];
+          s_u8[r * 8 + h] = fadd(fmul(alpha8[h], __int2float_rn(I)), bhi8[h]);
+        }
+      }
+    }
+    __syncwarp();
+    // refined levels of the selected keys
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      if (!sel[x]) continue;
+      const int r = lane + 32 * x;
+      const int64_t key = k0 + r;
+      const float* up = a.ubar + ((int64_t)bg * a.n_max + key) * G;
+      int jm = 0x1FF;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float t = a.per_head ? a.t32[((int64_t)bg * a.pcap + key) * G + h] : a.t32[(int64_t)bg * a.pcap + key];
+        const float u4 = up[h];
+        const int jb = bound_level(u4, cbv[h], t, neg_r, J);
+        if (jb > J || u4 >= clo[h]) continue;          // no candidate, or in the head's exact-max set
+        const int jr = bound_level(fminf(u4, s_u8[r * 8 + h]), cbv[h], t, neg_r, J);
+        a.jref[((int64_t)bg * a.pcap + key) * G + h] = (uint16_t)jr;
+        if (jr != jb) {
+          atomicAdd(&s_hd[h * JS + jb], -1);
+          atomicAdd(&s_hd[h * JS + jr], 1);
+        }
+        jm = min(jm, jr);
+      }
+      jk[key] = (uint16_t)((jkv[x] & 0x400u) | 0x200u | (unsigned)min(jm, 0x1FF));
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int i = tid; i < G * (J + 2); i += kRfW * 32) {
+    const int h = i / (J + 2), l = i - h * (J + 2);
+    const int v = s_hd[h * JS + l];
+    if (v) atomicAdd(a.jrd + (int64_t)(bh0 + h) * (a.J1 + 1) + l, v);
+  }
 }
 
 // ------------------------------------------------------------- candidates
@@ -594,9 +846,10 @@ constexpr int cand_smem(int G, int J1) {
 //    and fixed-point heavy weights per level.  They only size the first
 //    gather round.
 template <int G>
-__global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+__global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
                                                    int span) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   extern __shared__ __align__(16) uint8_t dsm[];
   const int J1 = a.J1, JS = a.J1 + 1;
   // the CTA's candidates, staged here and written out with one global slot
@@ -683,22 +936,30 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
       a.t32[(int64_t)bg * a.pcap + key] = t0;
     }
   }
-  int jmin = 255;
+  int jmin = 255, jmin_out = 0x1FF;   // jmin_out: over the heads not in their exact-max set
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     int jr = -1;
+    bool inc = false;
     if (live) {
       const int jb = bound_level(ub[h], c_b[h], t[h], neg_r, J);
       const bool cand = jb <= J;
-      const bool inc = ub[h] >= c_lo[h];
+      inc = ub[h] >= c_lo[h];
       inset |= inc;
       jr = inc ? 0 : (cand ? jb : J + 1);
       if (cand) { cm |= 1u << h; jmin = min(jmin, jb); }
+      if (cand && !inc) jmin_out = min(jmin_out, jb);
     }
     if (jr >= 0) atomicAdd(&s_jr[h * JS + jr], 1u);
     const unsigned cb = __ballot_sync(0xffffffffu, (cm >> h) & 1u);
     if (lane == 0 && cb) atomicAdd(&s_nc[h], (unsigned)__popc(cb));
+    if (a.refine8) {
+      const unsigned ib = __ballot_sync(0xffffffffu, inc);
+      if (lane == 0 && ib) atomicAdd(a.ninset + bh0 + h, (unsigned)__popc(ib));
+    }
   }
+  if (a.refine8 && live)
+    a.jkey[(int64_t)bg * a.pcap + key] = (uint16_t)(inset ? (0x400u | (unsigned)jmin_out) : (unsigned)jmin_out);
   float* sp = a.s32 + ((int64_t)bg * a.pcap + key) * G;
   // estimated levels (a key that is no candidate of a head has no level
   // up to J for it): one tile in eight with weight 8; when the exact-max
@@ -768,8 +1029,9 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
 // -------------------------------------------- window sums + stop predictor
 
 template <int D, int G, typename E>
-__global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+__global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   constexpr int CPL = D / 32;
   __shared__ float s_nr[G][D];
   __shared__ float s_dr[G], s_hr[G];
@@ -1080,9 +1342,10 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
 }
 
 template <int G, bool PH>
-__global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+__global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
                                                      int round, unsigned tpg, int isz) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   __shared__ unsigned s_item;
   const int BG = a.B * a.Hkv;
   const unsigned total = a.rq[6 * BG + round] * tpg;
@@ -1171,9 +1434,10 @@ constexpr int vgather_smem() {
 }
 
 template <int D, int G, typename E>
-__global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+__global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
                                                       int nent) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   constexpr int CPL = D / 32;
   constexpr int ACC = 2 * D + 8;
   constexpr int RB = D * (int)sizeof(E);
@@ -1680,9 +1944,10 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
 // ------------------------------------------------------------ certificate
 
 template <int D>
-__global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq,
+__global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
                                                       int round) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   constexpr int ACC = 2 * D + 8;
   constexpr int CPL = D / 32;
   constexpr int LB = 32;                   // levels per shared-memory batch
@@ -1822,11 +2087,16 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       for (int c = tid; c < D; c += 256)
         a.o[(int64_t)bh * D + c] = (s_win[c] + s_pre[i][D + c] + tau * s_pre[i][c]) / Dh;
       // rows read up to the stop level: warp 0 sums the bound-level histogram
-      unsigned kr = 0;
+      unsigned kr = 0, kr8 = 0;
       if (w == 0) {
         const unsigned* jr = a.jr_hist + (int64_t)bh * (a.J1 + 1);
-        for (int l = lane; l <= found; l += 32) kr += jr[l];
+        const int* jd = a.refine8 ? a.jrd + (int64_t)bh * (a.J1 + 1) : nullptr;
+        for (int l = lane; l <= found; l += 32) {
+          kr8 += jr[l];
+          kr += jd ? (unsigned)((int)jr[l] + jd[l]) : jr[l];
+        }
         kr = __reduce_add_sync(0xffffffffu, kr);
+        kr8 = __reduce_add_sync(0xffffffffu, kr8);
       }
       if (tid == 0) {
         const int vr = kWindow + (int)s_pre[i][2 * D + 4];
@@ -1836,8 +2106,10 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
         st[2] = found;
         st[3] = flags | kFlagDone;
         if (a.stats) {
+          // 8-bit rows: the candidates outside the head's exact-max set with jbar <= j*
+          const int r8 = a.refine8 ? (int)kr8 - (int)a.ninset[bh] : 0;
           csa_head_stats hs = {found, kWindow + (int)kr, vr, (int)a.ncand[bh], 0, J, round + 1,
-                               kWindow, kWindow, 0};
+                               kWindow, kWindow, r8};
           a.stats[bh] = hs;
         }
       }
@@ -1873,8 +2145,9 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
 // --------------------------------------------------- near-threshold count
 
 template <int G>
-__global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq) {
+__global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg) {
   pdl_entry();
+  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow || !a.stats) return;
@@ -1895,7 +2168,11 @@ __global__ void __launch_bounds__(256) near_kernel(const SparseArgs a, const __g
       if (js > J) { needK = needV = true; continue; }   // exact fallback
       if (js < 0) continue;
       const float u = ub[h];
-      const int jb = bound_level(u, cmax_get(a, bh0 + h, 2), t, neg_r, J);
+      int jb = bound_level(u, cmax_get(a, bh0 + h, 2), t, neg_r, J);
+      // the 8-bit tier: a refined candidate is needed from its refined level
+      if (a.refine8 && jb <= J && u < cmax_get(a, bh0 + h, 0) &&
+          (a.jkey[(int64_t)bg * a.pcap + key] & 0x200u))
+        jb = a.jref[((int64_t)bg * a.pcap + key) * G + h];
       if (u >= cmax_get(a, bh0 + h, 0) || jb <= js) needK = true;
       const float s = sp[h];
       if (!(s > -INFINITY)) continue;
@@ -1985,11 +2262,7 @@ static int per_group(const SparseArgs& a, int64_t target, int64_t cap) {
 template <int D, int G, typename E, int MODE>
 void launch_rows_t(int64_t items, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int round) {
   constexpr int smem = rows_smem<D, G, E>();
-  static bool set = false;
-  if (!set) {
-    cudaFuncSetAttribute(rows_kernel<D, G, E, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    set = true;
-  }
+  cudaFuncSetAttribute(rows_kernel<D, G, E, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   // four CTAs per SM over all groups: more, shorter shares than one wave
   // holds balance the uneven density of wanted entries better
   const int per = per_group(a, 4 * (int64_t)nsm, (items + 8 * kRingW - 1) / (8 * kRingW));
@@ -2007,11 +2280,7 @@ void launch_rows1(int64_t items, int nsm, cudaStream_t st, const SparseArgs& a, 
 template <int G>
 void launch_cand_t(int64_t pmax, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {
   const int smem = cand_smem(G, a.J1);
-  static int set = 0;
-  if (smem > set) {
-    cudaFuncSetAttribute(cand_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    set = smem;
-  }
+  cudaFuncSetAttribute(cand_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   const int64_t span = (int64_t)kTile * kTilesPerCta;
   dim3 grid((unsigned)((pmax + span - 1) / span), (unsigned)(a.B * a.Hkv));
   launch_pdl(cand_kernel<G>, grid, dim3(256), smem, st, a, seq, (int)span);
@@ -2027,24 +2296,18 @@ void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqAr
                       PhaseMark mark) {
   if constexpr (sizeof(E) == 2) {
     constexpr int smem = VsLayout<D, G>::smem;
-    static int per_sm = 0;
-    if (!per_sm) {
-      cudaFuncSetAttribute(vsum_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vsum_kernel<D, G>, kVsW * 32, smem) !=
-              cudaSuccess ||
-          per_sm < 1)
-        per_sm = 1;
-    }
+    cudaFuncSetAttribute(vsum_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vsum_kernel<D, G>, kVsW * 32, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
     launch_pdl(vplan_kernel<true>, dim3(1), dim3(1024), 0, st, a, nent);
     if (mark) mark(7, st);
     launch_pdl(vsum_kernel<D, G>, dim3((unsigned)(nsm * per_sm)), dim3(kVsW * 32), smem, st, a, nent);
   } else {
     constexpr int smem = vgather_smem<D, G, E>();
-    static bool set = false;
-    if (!set) {
-      cudaFuncSetAttribute(vgather_kernel<D, G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      set = true;
-    }
+    cudaFuncSetAttribute(vgather_kernel<D, G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     launch_pdl(vplan_kernel<false>, dim3(1), dim3(1024), 0, st, a, nent);
     if (mark) mark(7, st);
     launch_pdl(vgather_kernel<D, G, E>, dim3((unsigned)(nsm * 2)), dim3(256), smem, st, a, seq, nent);
@@ -2079,8 +2342,37 @@ cudaError_t launch_predict(const SparseArgs& a, const SeqArgs& seq, int d, int G
   CSA_DG_LAUNCH(predict_kernel, grid, dim3(256), 0, st, a, seq)
   return cudaGetLastError();
 }
+template <int D, int G>
+static cudaError_t launch_refine_t(const SparseArgs& a, const SeqArgs& seq, int round, int nsm, cudaStream_t st) {
+  const int smem = RfLayout<D, G>::hist + G * (a.J1 + 1) * 4;
+  const cudaError_t e = cudaFuncSetAttribute(refine8_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int per = per_group(a, 4 * (int64_t)nsm, (a.nblk_max + kRfW - 1) / kRfW);
+  launch_pdl(refine8_kernel<D, G>, dim3((unsigned)per, (unsigned)(a.B * a.Hkv)), dim3(kRfW * 32), smem, st, a, seq,
+             round);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, bool bf16, int64_t pmax_live,
                          int round, int nsm, cudaStream_t st, PhaseMark mark) {
+  if (a.refine8) {
+    // the 8-bit refinement of the round's candidates (bf16 caches only)
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (d * 10 + G) {
+      case 1281: e = launch_refine_t<128, 1>(a, seq, round, nsm, st); break;
+      case 1282: e = launch_refine_t<128, 2>(a, seq, round, nsm, st); break;
+      case 1284: e = launch_refine_t<128, 4>(a, seq, round, nsm, st); break;
+      case 1288: e = launch_refine_t<128, 8>(a, seq, round, nsm, st); break;
+      case 641: e = launch_refine_t<64, 1>(a, seq, round, nsm, st); break;
+      case 642: e = launch_refine_t<64, 2>(a, seq, round, nsm, st); break;
+      case 644: e = launch_refine_t<64, 4>(a, seq, round, nsm, st); break;
+      case 648: e = launch_refine_t<64, 8>(a, seq, round, nsm, st); break;
+      default: break;
+    }
+    if (e != cudaSuccess) return e;
+    add_launches(1);
+    if (mark) mark(12, st);
+  }
   // eight 256-thread CTAs per SM pull work items (isz keys of a group
   // listed for this round) from the round's queue
   const int isz = round == 0 ? kLevItem : kLevItemLate;

@@ -96,8 +96,12 @@ csa_status csa_dense_decode_static(const csa_shape* shape, const void* q, const 
   void* scratch = nullptr;
   const csa_status sa = scratch_address((cudaStream_t)stream, &scratch);
   if (sa != CSA_OK) return sa;
-  DenseArgs a;
-  a.q = q; a.K = K; a.V = V; a.part = (float*)scratch; a.o = o; a.state = nullptr; a.nfall = nullptr;
+  // the array holds the status word, then the partials (the workspace
+  // layout of csa_dense_decode)
+  if (cudaMemsetAsync(scratch, 0, sizeof(unsigned), (cudaStream_t)stream) != cudaSuccess) return CSA_ERR_CUDA;
+  DenseArgs a = {};
+  a.q = q; a.K = K; a.V = V; a.part = (float*)((char*)scratch + 256); a.o = o; a.state = nullptr;
+  a.nfall = nullptr; a.status = (unsigned*)scratch;
   a.B = shape->B; a.Hq = shape->Hq; a.Hkv = shape->Hkv; a.n_max = shape->n_max;
   a.nsplit = dense_nsplit(shape->n_max); a.rs = (float)(1.0 / std::sqrt((double)shape->d));
   add_launches(2);

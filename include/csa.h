@@ -103,6 +103,18 @@ typedef struct {
   int perturb;    /* 0: one perturbation draw per (sequence, KV head, key),
                    * shared by the group's query heads (default); 1: one draw
                    * per query head (stream 2^20 + g G + h of the keying)   */
+  int qcode;      /* query code of the 4-bit bounds: 0 = int8 (QM = 127) with
+                   * the residual summed per channel (default); 1 = two s8
+                   * digits (QM = 127 * 257) with the closed-form residual
+                   * 15 d alpha (1/2 + 2^-6): narrower bounds, fewer
+                   * candidates; results do not depend on it               */
+  int refine8;    /* 8-bit refinement tier (picx.dev "Algorithm Components"
+                   * 4: an 8-bit stage before the exact 16-bit reads); needs
+                   * csa_decode_step_refined and bf16 caches.  0 = off;
+                   * 1 = every group; 2 = groups whose first gather range
+                   * reaches level r (the near-uniform groups, which stop
+                   * near level 0, stay on the 4-bit bounds).  Results do
+                   * not depend on it; keys_read counts the refined levels */
 } csa_params;
 
 /* Optional per-(sequence, query head) diagnostics. */
@@ -118,7 +130,9 @@ typedef struct {
                             /* pool rows counted in keys_read| (one bf16 K  */
                             /* row load serves the whole group)             */
   int32_t group_values_read;/* the same union for values_read              */
-  int32_t reserved;
+  int32_t rows8;            /* refinement tier: 8-bit rows of the head's    */
+                            /* candidates outside its exact-max set with    */
+                            /* jbar <= j* (0 without the tier)              */
 } csa_head_stats;
 
 /* Bytes of workspace csa_decode_step needs for this shape and parameters.
@@ -152,7 +166,8 @@ csa_status csa_quantize_keys(const csa_shape* shape, const void* K,
  *   keys_read  [B][Hq]     see csa_head_stats
  *   stats      [B][Hq]     optional (NULL to skip)
  * workspace: device buffer of at least csa_workspace_size bytes, 256-byte
- * aligned; its contents on entry do not matter.
+ * aligned; its contents on entry do not matter.  params->refine8 must be 0
+ * here (the tier's 8-bit inputs come through csa_decode_step_refined).
  * With sub-batches (csa_params.sub_batches) the call forks onto the
  * library's streams of the current device and joins back onto `stream`
  * before returning control of the outputs; enqueueing is serialised by a
@@ -169,7 +184,73 @@ csa_status csa_decode_step(const csa_shape* shape, const csa_params* params,
                            csa_head_stats* stats, void* workspace,
                            size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace csa_dense_decode needs. */
+/* 8-bit codes of the same blocks, for the refinement tier (picx.dev
+ * "Algorithm Components" 4).  Per block and channel: the same minimum m_c as
+ * csa_quantize_keys, Delta8_c = fl((max - min) / 255) (0 -> 1), code =
+ * clamp(rint(fl(fl(k - m_c) / Delta8_c)), 0, 255), one byte per code.
+ * Rebuilds every block that holds a token at position >= from_token and
+ * < len[b].
+ *   K8      device [B][Hkv][nblk_max * 64][d] uint8
+ *   delta8  device [B][Hkv][nblk_max][d] float
+ * Positions >= len[b] inside a rebuilt block get code 0. */
+csa_status csa_quantize_keys8(const csa_shape* shape, const void* K,
+                              const int64_t* len, int64_t from_token,
+                              uint8_t* K8, float* delta8, void* stream);
+
+/* csa_decode_step with the 8-bit refinement tier (params->refine8 = 1 or 2,
+ * bf16 caches): before each gather round's exact rescoring, the candidates
+ * the round would read also get the upper bound from their 8-bit codes
+ * (K8, delta8 from csa_quantize_keys8, same blocks; query codes of 12 bits
+ * per (block, head)), and a key whose level from the tighter of the two
+ * bounds lies past the round's range is not read in that round.  The
+ * refined level never exceeds the exact one, so o, beta, level and
+ * values_read are those of csa_decode_step; keys_read counts the refined
+ * levels.  Other arguments, results and errors as csa_decode_step. */
+csa_status csa_decode_step_refined(const csa_shape* shape,
+                                   const csa_params* params, const void* q,
+                                   const void* K, const void* V,
+                                   const uint8_t* K4, const float* bounds,
+                                   const float* vmax, const float* vnorm2,
+                                   const uint8_t* K8, const float* delta8,
+                                   const int64_t* len,
+                                   const uint64_t* step_seed, float* o,
+                                   float* beta, int32_t* level,
+                                   int32_t* keys_read, csa_head_stats* stats,
+                                   void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* The same step with the lengths and seeds in device memory, for whole-token
+ * decode captured once into a CUDA graph and replayed every token (the
+ * readsearch.ai abstract: the perturbations are drawn anew at every decode
+ * step, so a replayed step must read the new seeds; picx.dev "CPU Speed":
+ * whole decode steps over all layers are what is timed).
+ *   len        device [B] int64, 1 <= len[b] <= n_max (a value outside is
+ *              clamped and reported by csa_check as CSA_ERR_INVALID_ARG)
+ *   step_seed  device [B] uint64
+ *   requantize_last  1: before scanning, rebuild the 64-token block that
+ *              holds token len[b] - 1 of every sequence (codes, bounds,
+ *              vmax, vnorm2 from K and V: what csa_quantize_keys with
+ *              from_token = len[b] - 1 does), inside the step's first
+ *              kernel; for the token just appended.  0: the caller keeps
+ *              K4, bounds, vmax and vnorm2 current.  With 1, K4, bounds,
+ *              vmax and vnorm2 are written.
+ * Both arrays are read by the step's first kernel, in stream order, so a
+ * kernel or copy earlier on `stream` (or in the same graph) may write them.
+ * Grids are sized from n_max rather than the longest live sequence.  The
+ * refinement tier is not available here (params->refine8 must be 0).  Other
+ * arguments, results and errors as csa_decode_step. */
+csa_status csa_decode_step_device(const csa_shape* shape, const csa_params* params,
+                                  const void* q, const void* K, const void* V,
+                                  uint8_t* K4, float* bounds, float* vmax,
+                                  float* vnorm2, const int64_t* len,
+                                  const uint64_t* step_seed,
+                                  int requantize_last, float* o, float* beta,
+                                  int32_t* level, int32_t* keys_read,
+                                  csa_head_stats* stats, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace csa_dense_decode needs (a status word, then the
+ * split-K partials). */
 size_t csa_dense_workspace_size(const csa_shape* shape);
 
 /* Dense decode attention (the same-build comparator, and the exact formula
@@ -221,7 +302,9 @@ csa_status csa_dense_decode_static(const csa_shape* shape, const void* q,
  *   cmax     uint32 [B][Hq][4]          c*_lo, c*_hi, cb, c32 as ordered
  *            integers (u >= 2^31: float bits u - 2^31; else bits ~u)
  *   s32      float [B][Hkv][n_max-64][G] float32 score of each candidate
- *            pool key for each head, -inf where it is not a candidate
+ *            pool key for each head; after a step called with `stats`,
+ *            -inf where the key is not a candidate of the head or was not
+ *            rescored (without `stats` the other entries are left stale)
  *   jr_hist  uint32 [B][Hq][J+2]        first level at which the key's bf16
  *            row is needed (exact-max set: level 0), J+1 = never
  *   bcnt     uint32 [B][Hkv][J1]        entries appended to each level bucket
@@ -257,7 +340,7 @@ csa_status csa_workspace_layout(const csa_shape* shape,
  * Phases: 0 workspace clear, 1 scan, 2 exact max, 3 candidates (with the
  * value-free level histograms), 4 rescoring of candidate K rows (per
  * round), 5 predictor + window, 6 level buckets, 7 gather plan, 8 V gather,
- * 9 certificate, 10 exact fallback, 11 diagnostics, 12 reserved (0). */
+ * 9 certificate, 10 exact fallback, 11 diagnostics, 12 8-bit refinement. */
 #define CSA_NPHASE 13
 typedef struct {
   float ms[CSA_NPHASE];
@@ -269,9 +352,11 @@ csa_status csa_profile_enable(int on);
 csa_status csa_profile_read(csa_phase_times* out);
 
 /* Synchronises `stream`, then returns the device status word recorded in
- * `workspace` by the last csa_decode_step that used it (CSA_OK, or
- * CSA_ERR_NONFINITE / CSA_ERR_WORKSPACE), or CSA_ERR_CUDA if the stream
- * reports an error. */
+ * `workspace` by the last csa_decode_step, csa_decode_step_device or
+ * csa_dense_decode that used it: CSA_OK, CSA_ERR_NONFINITE,
+ * CSA_ERR_WORKSPACE, CSA_ERR_TIMEOUT (a bounded wait of the dense kernel
+ * gave up) or CSA_ERR_INVALID_ARG (a device length out of range); or
+ * CSA_ERR_CUDA if the stream reports an error. */
 csa_status csa_check(void* workspace, void* stream);
 
 /* Static English description of a status code. */

@@ -17,6 +17,20 @@ TOL = 2e-3      # o and beta, relative
 NEAR = 1e-5     # nats: memberships this close to a threshold may differ
 
 
+def o_close(o_dev, o_ref, tol=TOL):
+    """Element-wise "within tol relative" for an output vector: every channel
+    c satisfies |o_dev_c - o_ref_c| <= tol (|o_ref_c| + rms(o_ref)).  The rms
+    floor keeps channels whose exact value is near zero (where any rounding
+    is large relative to the channel) from failing on float32 rounding,
+    while no single channel can hide an error behind the vector's norm."""
+    o_dev = np.asarray(o_dev, np.float64)
+    o_ref = np.asarray(o_ref, np.float64)
+    rms = float(np.sqrt(np.mean(o_ref * o_ref)))
+    err = np.abs(o_dev - o_ref)
+    lim = tol * (np.abs(o_ref) + rms)
+    return bool(np.all(err <= lim)), float(np.max(err / np.maximum(lim, 1e-300)))
+
+
 def ensure_built():
     import certified_sparse_attention_gb300 as csa
     if not os.path.exists(csa.LIB_PATH):
@@ -36,7 +50,8 @@ class DeviceRun:
 
     def __init__(self, w: synth.Workload, K, V, q, lens, seeds, n_alloc,
                  device="cuda:0", eps=None, delta=None, r=None,
-                 measure=0, J_override=-1, sub_batches=0, perturb=0):
+                 measure=0, J_override=-1, sub_batches=0, perturb=0,
+                 qcode=0, refine8=0):
         import torch
         import certified_sparse_attention_gb300 as csa
         self.csa = csa
@@ -47,7 +62,8 @@ class DeviceRun:
         self.params = csa.make_params(w.eps if eps is None else eps,
                                       w.delta if delta is None else delta,
                                       w.r if r is None else r, measure,
-                                      J_override, sub_batches, perturb)
+                                      J_override, sub_batches, perturb,
+                                      qcode, refine8)
         Kp = np.zeros((w.B, w.Hkv, n_alloc, w.d), np.float32)
         Vp = np.zeros_like(Kp)
         Kp[:, :, :K.shape[2]] = K
@@ -59,9 +75,16 @@ class DeviceRun:
         csa.check(csa.csa_quantize_keys(self.shape, self.K, self.V, self.lens,
                                         0, *self.meta),
                   "csa_quantize_keys")
+        self.meta8 = None
+        if refine8:
+            self.meta8 = csa.meta8_buffers(self.shape, device)
+            csa.check(csa.csa_quantize_keys8(self.shape, self.K, self.lens, 0,
+                                             *self.meta8),
+                      "csa_quantize_keys8")
         self.step = csa.DecodeStep(self.shape, self.params, device,
                                    with_stats=True)
-        self.step(self.q, self.K, self.V, self.meta, self.lens, self.seeds)
+        self.step(self.q, self.K, self.V, self.meta, self.lens, self.seeds,
+                  meta8=self.meta8)
         torch.cuda.synchronize()
         csa.check(csa.csa_check(self.step.ws), "csa_check")
         self.map = csa.csa_workspace_layout(self.shape, self.params)
@@ -72,7 +95,8 @@ class DeviceRun:
         self.lens = [int(x) for x in lens]
         self.seeds = [int(x) for x in seeds]
         self.q = to_dev(q, self.w.dtype, self.q.device)
-        self.step(self.q, self.K, self.V, self.meta, self.lens, self.seeds)
+        self.step(self.q, self.K, self.V, self.meta, self.lens, self.seeds,
+                  meta8=self.meta8)
         torch.cuda.synchronize()
         self.csa.check(self.csa.csa_check(self.step.ws), "csa_check")
 
@@ -172,7 +196,9 @@ def compare_group(run, w, K, V, q, b, g, res, p, report):
         lv = min(int(lvl_g[b, hq]), J)
         scored = np.isfinite(s32[b, g, :P, h])
         assert not np.any(scored & ~cand), (b, g, h)
-        assert np.all(scored[cand & (det["jbar"] <= lv)]), (b, g, h)
+        # (with the 8-bit tier a candidate is read from its refined level)
+        jneed = det["jref"] if p.refine8 else det["jbar"]
+        assert np.all(scored[cand & (jneed <= lv)]), (b, g, h)
         pend = cand & ~scored
         assert np.all(det["jl_c"][pend] > lv), (b, g, h)
         assert stats[b, hq, 3] == res.n_candidates[h]
@@ -223,20 +249,23 @@ def compare_group(run, w, K, V, q, b, g, res, p, report):
             b_ref = cert["beta"][gl]
             assert abs(beta_g[b, hq] - b_ref) <= TOL * b_ref
             kr = 64 + len(np.union1d(det["cset"],
-                                     np.nonzero(det["jbar"] <= gl)[0]))
+                                     np.nonzero(jneed <= gl)[0]))
             assert kr_g[b, hq] == kr
+            if p.refine8:
+                assert stats[b, hq, 9] == res.rows8[h], (b, g, h)
             assert stats[b, hq, 2] == 64 + int((jr <= gl).sum())
         else:
             o_ref, _ = dense_attention(q[b, hq], K[b, g, :n], V[b, g, :n])
             assert beta_g[b, hq] == 0 and kr_g[b, hq] == n
-        err = np.linalg.norm(o_g[b, hq] - o_ref)
-        assert err <= TOL * np.linalg.norm(o_ref) + 1e-6, (b, g, h, err)
+        ok_o, worst = o_close(o_g[b, hq], o_ref)
+        assert ok_o, (b, g, h, worst)
+        report["worst_o"] = max(report.get("worst_o", 0.0), worst)
         report["heads"] += 1
         report["levels"].append(gl)
         # rows the head needs, for the group unions
         if gl <= J:
             needK.update(np.union1d(det["cset"],
-                                    np.nonzero(det["jbar"] <= gl)[0]).tolist())
+                                    np.nonzero(jneed <= gl)[0]).tolist())
             needV.update(np.nonzero(jr <= gl)[0].tolist())
         else:
             needK.update(range(P))
@@ -251,7 +280,9 @@ def run_and_compare(w, K, V, q, lens, seeds, n_alloc, **pover):
     run = DeviceRun(w, K, V, q, lens, seeds, n_alloc, **pover)
     p = Params(run.params.eps, run.params.delta, run.params.r,
                measure=run.params.measure, J_override=run.params.J_override,
-               per_head=bool(run.params.perturb))
+               per_head=bool(run.params.perturb),
+               two_digit=bool(run.params.qcode),
+               refine8=bool(run.params.refine8))
     report = {"flips": 0, "level_flips": 0, "heads": 0, "levels": []}
     for b in range(w.B):
         n = run.lens[b]

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def _declared():
     src = open(os.path.join(ROOT, "include", "csa.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(csa_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(csa_[a-z_0-9]+)\s*\(", src)))
 
 
 @pytest.fixture(scope="module")
@@ -70,7 +70,7 @@ def test_unsupported_shapes(lib, bad):
                                 dict(delta=0.0), dict(r=0), dict(r=5),
                                 dict(measure=4), dict(J_override=300),
                                 dict(sub_batches=5), dict(sub_batches=-1),
-                                dict(perturb=2)])
+                                dict(perturb=2), dict(qcode=2)])
 def test_invalid_params(lib, pk):
     s = csa.make_shape(1, 8, 2, 128, 4096, "bf16")
     kw = dict(eps=0.05, delta=0.05, r=2)
@@ -103,6 +103,24 @@ def test_decode_rejects_bad_arguments_before_launch(lib):
                              fake, None, fake, 16, None)
     assert st == 6                       # workspace too small
     assert csa.status_string(6).startswith("workspace")
+
+
+def test_device_length_step_rejects_bad_arguments_before_launch(lib):
+    # the device-length variant: the same host checks (its lengths are on
+    # the device and checked there), plus the re-quantisation flag
+    s = csa.make_shape(1, 8, 2, 128, 4096, "bf16")
+    p = csa.make_params()
+    fake = 256
+    f = lib.csa_decode_step_device
+    assert f(ctypes.byref(s), ctypes.byref(p), fake, fake, fake, fake, fake,
+             fake, fake, None, fake, 1, fake, fake, fake, fake, None, fake,
+             1 << 30, None) == 1                     # no length array
+    assert f(ctypes.byref(s), ctypes.byref(p), fake, fake, fake, fake, fake,
+             fake, fake, fake, fake, 2, fake, fake, fake, fake, None, fake,
+             1 << 30, None) == 1                     # flag not 0 or 1
+    assert f(ctypes.byref(s), ctypes.byref(p), fake, fake, fake, fake, fake,
+             fake, fake, fake, fake, 1, fake, fake, fake, fake, None, fake,
+             16, None) == 6                          # workspace too small
 
 
 def test_missing_library_fails_loudly(tmp_path):

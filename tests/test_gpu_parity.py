@@ -14,7 +14,7 @@ import pytest
 import synth
 from oracle.quantize import quantize_keys, value_sq_norms_f32, vmax_blocks
 from oracle.step import dense_attention
-from tests.gpu_common import ensure_built, run_and_compare, to_dev
+from tests.gpu_common import DeviceRun, ensure_built, o_close, run_and_compare, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -161,6 +161,18 @@ def test_decode_per_head_perturbations(G, n):
     assert rep["heads"] == 4 * G
 
 
+@pytest.mark.parametrize("G,d,n", [(4, 128, 1500), (2, 64, 1100),
+                                   (8, 128, 4093)])
+def test_decode_two_digit_query_codes(G, d, n):
+    # query codes of two s8 digits with the closed-form residual: the
+    # bounds, maxima and candidate sets bit for bit against the oracle's
+    # two-digit construction, results as always
+    w, K, V, q = _case("llama16k", n, B=2, Hq=2 * G, Hkv=2, d=d)
+    seeds = synth.step_seeds(w, 10)
+    run, rep = run_and_compare(w, K, V, q, [n, n - 61], seeds, n, qcode=1)
+    assert rep["heads"] == 4 * G
+
+
 @pytest.mark.parametrize("G,d", [(1, 128), (2, 64), (8, 128)])
 def test_decode_group_sizes(G, d):
     w, K, V, q = _case("llama16k", 900, Hq=2 * G, Hkv=2, d=d)
@@ -276,3 +288,122 @@ def test_decode_largest_batch_ragged():
             o_ref, _ = dense_attention(q[b, hq], K[b, g, :n], V[b, g, :n])
             assert np.linalg.norm(o_g[b, hq] - o_ref) <= 1e-5 * np.linalg.norm(o_ref) + 1e-6
             assert beta_g[b, hq] == 0 and lvl_g[b, hq] == 0 and kr_g[b, hq] == n
+
+
+def test_decode_degenerate_inputs():
+    # a zero query (every score 0: all keys weigh the same and are heavy at
+    # level 0; the query code is all zeros) and a group whose cached keys
+    # are all equal (every block constant: Delta = 1, codes 0): against the
+    # oracle
+    w, K, V, q = _case("llama16k", 1500, Hq=8, Hkv=2)
+    seeds = synth.step_seeds(w, 13)
+    q0 = q.copy()
+    q0[0, :4] = 0.0
+    run, rep = run_and_compare(w, K, V, q0, [1500], seeds, 1500)
+    assert rep["heads"] == 8
+    K1 = K.copy()
+    K1[0, 1, :] = K[0, 1, :1]
+    run, rep = run_and_compare(w, K1, V, q, [1500], seeds, 1500)
+    assert rep["heads"] == 8
+
+
+def test_decode_metamorphic_relations():
+    # on the device: doubling every value doubles o and beta at the same
+    # stop levels (every scaling is by a power of two, exact in float32; the
+    # per-level sums are float atomics whose order varies from run to run,
+    # so the two runs agree to float32 rounding, not bit for bit), and a
+    # larger eps never stops a head later
+    import torch
+    w, K, V, q = _case("llama16k", 1500, B=2, Hq=8, Hkv=2)
+    seeds = synth.step_seeds(w, 14)
+    run = DeviceRun(w, K, V, q, [1500, 1400], seeds, 1500)
+    o1, b1, l1, k1, _ = run.outputs()
+    run2 = DeviceRun(w, K, 2.0 * V, q, [1500, 1400], seeds, 1500)
+    o2, b2, l2, k2, _ = run2.outputs()
+    assert np.array_equal(l1, l2) and np.array_equal(k1, k2)
+    for b in range(2):
+        for hq in range(8):
+            assert o_close(o2[b, hq], 2.0 * o1[b, hq], tol=1e-5)[0], (b, hq)
+    assert np.allclose(b2, 2.0 * b1, rtol=1e-5, atol=0)
+    prev = None
+    for eps in (0.02, 0.05, 0.2):
+        r = DeviceRun(w, K, V, q, [1500, 1400], seeds, 1500, eps=eps)
+        lv = r.outputs()[2]
+        if prev is not None:
+            assert np.all(lv <= prev)
+        prev = lv
+    torch.cuda.synchronize()
+
+
+# ------------------------------------- the benchmarked grid (r = 4) and eps
+
+@pytest.mark.parametrize("r,n", [(3, 4093), (4, 4093)])
+def test_decode_finer_grids_small(r, n):
+    # grids of r = 3 and 4 levels per octave: the level arithmetic -r x,
+    # J = ceil(r log2 |P|) and the round-1 margin r - 1, on a peaked and a
+    # near-uniform group, through two sub-batches
+    w, K, V, q = _case("llama16k", n, B=2, Hq=8, Hkv=2, r=r)
+    seeds = synth.step_seeds(w, 13)
+    run, rep = run_and_compare(w, K, V, q, [n, n - 333], seeds, n)
+    assert rep["heads"] == 16
+
+
+def test_decode_128k_r4_groups():
+    # the shape of the 128K benchmark (n = 131072, GQA 4, d = 128, bf16,
+    # eps .05, delta .05, r = 4, J = 68): one peaked and one near-uniform
+    # group, every key's bound and candidate, every head's o and beta
+    w, K, V, q = _case("llama128k_b4", 131072, B=1, Hq=8, Hkv=2)
+    assert w.r == 4
+    seeds = synth.step_seeds(w, 1)
+    run, rep = run_and_compare(w, K, V, q, [131072], seeds, 131072)
+    assert rep["heads"] == 8
+    print("128K r=4: levels", rep["levels"], "flips", rep["flips"],
+          "level flips", rep["level_flips"], "worst o", rep["worst_o"])
+
+
+@pytest.mark.parametrize("eps", [0.01, 0.1])
+def test_decode_16k_eps_sweep(eps):
+    # tighter and looser targets than the default on the full 16K length:
+    # eps = 0.01 pushes the stop levels deep (most of the pool sampled)
+    w, K, V, q = _case("llama16k", 16384, Hq=8, Hkv=2, eps=eps)
+    seeds = synth.step_seeds(w, 2)
+    run, rep = run_and_compare(w, K, V, q, [16384], seeds, 16384)
+    assert rep["heads"] == 8
+    print("eps", eps, "levels", rep["levels"], "worst o", rep["worst_o"])
+
+
+# ------------------------------------------------- 8-bit refinement tier
+
+@pytest.mark.parametrize("n,over", [(1337, {"Hq": 8, "Hkv": 2}),
+                                    (130, {"Hq": 4, "Hkv": 4, "d": 64})])
+def test_quantizer8_bit_exact(n, over):
+    import torch
+    import certified_sparse_attention_gb300 as csa
+    from oracle.quantize import quantize_keys8
+    w, K, V, q = _case("llama16k", n, **over)
+    n_alloc = n + 75
+    shape = csa.make_shape(w.B, w.Hq, w.Hkv, w.d, n_alloc, w.dtype)
+    Kp = np.zeros((w.B, w.Hkv, n_alloc, w.d), np.float32)
+    Kp[:, :, :n] = K
+    Kt = to_dev(Kp, w.dtype, "cuda")
+    K8, d8 = csa.meta8_buffers(shape, "cuda")
+    csa.check(csa.csa_quantize_keys8(shape, Kt, [n] * w.B, 0, K8, d8))
+    torch.cuda.synchronize()
+    for g in range(w.Hkv):
+        codes8, mins8, deltas8 = quantize_keys8(K[0, g], n)
+        nb = mins8.shape[0]
+        assert np.array_equal(K8[0, g, :nb * 64].cpu().numpy(), codes8)
+        assert np.array_equal(d8[0, g, :nb].cpu().numpy(), deltas8)
+
+
+@pytest.mark.parametrize("refine8,r,n", [(1, 2, 4093), (1, 4, 4093),
+                                         (2, 4, 4093), (1, 2, 16384)])
+def test_decode_refine8(refine8, r, n):
+    # the 8-bit tier: every refined key's level bit for bit (through the
+    # candidates scored, keys_read, the group unions and the 8-bit rows),
+    # and the same memberships, o, beta and levels as without it
+    w, K, V, q = _case("llama16k", n, B=2, Hq=8, Hkv=2, r=r)
+    seeds = synth.step_seeds(w, 15)
+    run, rep = run_and_compare(w, K, V, q, [n, n - 211], seeds, n,
+                               refine8=refine8)
+    assert rep["heads"] == 16

@@ -290,23 +290,24 @@ def decode_loop(args, csa, w, device, stream):
             step(q_all[t, li], K, V, mt, lens,
                  seeds_for(w, 100 + lid, t), stream)
 
-    with torch.cuda.stream(stream):
+    gs = torch.cuda.Stream(device)           # graphs are captured off the default stream
+    with torch.cuda.stream(gs):
         token_device()                       # warm-up, eager (token 0)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
+    with torch.cuda.graph(graph, stream=gs):
         token_device()
     t_dev.fill_(1)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
+    with torch.cuda.stream(gs):
+        e0.record(gs)
         for t in range(1, T):
             graph.replay()
-        e1.record(stream)
+        e1.record(gs)
     torch.cuda.synchronize()
-    csa.check(csa.csa_check(step.ws, stream), "csa_check (decode loop)")
+    csa.check(csa.csa_check(step.ws, gs), "csa_check (decode loop)")
     us_graph = e0.elapsed_time(e1) / (T - 1) * 1e3
     e0.record(stream)
     for t in range(1, T):
@@ -832,6 +833,91 @@ def context_sweep(args):
         torch.cuda.empty_cache()
 
 
+def stress_sweep(args):
+    """The stress sweep of the pages' setting: batch 1, 8 KV heads, GQA 4,
+    d = 128, bf16, r = 2, n in {256K, 512K, 1M} tokens, eps in {0.01, 0.02,
+    0.05, 0.1}, three attention regimes (flat: q x 0.05; heavy-tailed:
+    Pareto(1.5) boosts along the needle direction; adversarial: ceil(eps^-2)
+    keys sharing one boosted score over a flat background).  Per point: the
+    certified step and the same-build dense decode (CUDA events, 10 steps
+    after 3 warm-up steps), keys and values read per head, stop levels, and
+    certificate coverage of 4 steps against float64 exact attention.  One
+    JSON line per point; not part of the benchmark line."""
+    import torch
+    import synth
+    import certified_sparse_attention_gb300 as csa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    csa.load_library()
+    st = torch.cuda.current_stream(dev)
+    for regime in ("flat", "heavy", "adversarial"):
+        for n in (262144, 524288, 1048576):
+            data = None
+            for eps in (0.01, 0.02, 0.05, 0.1):
+                w = synth.stress(n, eps, regime)
+                if data is None or regime == "adversarial":
+                    data = None
+                    torch.cuda.empty_cache()
+                    shape, data = setup_layers(w, [0], dev, csa)
+                d = data[0]
+                params = csa.make_params(w.eps, w.delta, w.r)
+                step = csa.DecodeStep(shape, params, dev, with_stats=True)
+                dense = csa.DenseDecode(shape, dev)
+                lens = [n]
+                seeds = [seeds_for(w, 0, i) for i in range(14)]
+
+                def run_sparse(i):
+                    step(d["q"][i % 4], d["K"], d["V"], d["meta"], lens,
+                         seeds[i], st)
+
+                def run_dense(i):
+                    dense(d["q"][i % 4], d["K"], d["V"], lens, st)
+
+                res = {}
+                for key, fn in (("sparse_us", run_sparse),
+                                ("dense_us", run_dense)):
+                    for i in range(3):
+                        fn(i)
+                    torch.cuda.synchronize()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(st)
+                    for i in range(3, 13):
+                        fn(i)
+                    e1.record(st)
+                    torch.cuda.synchronize()
+                    res[key] = round(e0.elapsed_time(e1) / 10 * 1e3, 1)
+                cov = Coverage(w)
+                kr, vr, lv = [], [], []
+                for i in range(4):
+                    run_sparse(i)
+                    torch.cuda.synchronize()
+                    csa.check(csa.csa_check(step.ws), "csa_check (stress)")
+                    sts = step.stats.cpu()
+                    kr.append(float(sts[..., 1].float().mean()))
+                    vr.append(float(sts[..., 2].float().mean()))
+                    lv.extend(sts[..., 0].flatten().tolist())
+                    cov.add(d["q"][i % 4], d["K"], d["V"], lens, step)
+                c = cov.summary()
+                print(json.dumps({"stress_sweep": {
+                    "regime": regime, "n": n, "eps": eps, "r": w.r, **res,
+                    "sparse_over_dense": round(res["sparse_us"] / res["dense_us"], 3),
+                    "keys_read_mean": round(sum(kr) / len(kr), 1),
+                    "values_read_mean": round(sum(vr) / len(vr), 1),
+                    "level_mean": round(sum(lv) / len(lv), 2),
+                    "level_max": int(max(lv)),
+                    "head_steps": c["head_steps"],
+                    "beta_violations": c["beta_violations"],
+                    "eps_violations": c["eps_violations"],
+                    "fallbacks": c["fallbacks"],
+                    "err_over_epsM_p90": c["err_over_epsM"]["p90"],
+                    "err_over_epsM_max": c["err_over_epsM"]["max"]}}),
+                    flush=True)
+                del step, dense
+            del data
+            torch.cuda.empty_cache()
+
+
 def synth_workload(name):
     import synth
     return synth.workload(name)
@@ -849,6 +935,10 @@ def main(argv=None):
                     help="override the context length (profiler captures)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch (profiler captures)")
+    ap.add_argument("--stress-sweep", action="store_true",
+                    help="the stress sweep (256K-1M tokens, eps 0.01-0.1, "
+                         "flat / heavy-tailed / adversarial): one JSON line "
+                         "per point instead of the benchmark line")
     ap.add_argument("--context-sweep", action="store_true",
                     help="print step times from 128K to 1M tokens and exit")
     ap.add_argument("--decode-layers", type=int, default=32,
@@ -867,6 +957,10 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank, local)
+        return
+    if args.stress_sweep:
+        if rank == 0:
+            stress_sweep(args)
         return
     if args.context_sweep:
         if rank == 0:

@@ -62,9 +62,9 @@ float normal_quantile_two_sided(double delta) {
 struct Layout {
   int J1;
   int64_t pcap, nblk_max;
-  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, front, rcnt, jrd, ninset,
+  size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, front, jrd, ninset,
       zero_end;
-  size_t jkey, jref, seqd, winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, hw, s32, win, t32, clist, rlist, xlist, cmap,
+  size_t jkey, jref, seqd, winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, hw, s32, win, t32, clist, xlist, cmap,
       buckets, dpart, pref, total;
   int64_t nchunk_cap;
 };
@@ -84,18 +84,17 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.ncand = o; o += up((size_t)BH * 4);
   L.pre_hist = o; o += up((size_t)BH * L.J1 * 4 * 4);
   L.acc = o; o += up((size_t)BH * L.J1 * ACC * 4);
-  L.bcnt = o; o += up((size_t)BG * L.J1 * 4);
+  L.bcnt = o; o += up((size_t)3 * BG * L.J1 * 4);
   L.bcons = o; o += up((size_t)BG * L.J1 * 4);
   L.ccnt = o; o += up((size_t)BG * 4);
   L.xcnt = o; o += up((size_t)BG * 4);
   L.nfall = o; o += up(4);
   L.rq = o; o += up(((size_t)BG * 6 + 6) * 4);
   L.front = o; o += up((size_t)4 * BG * 4);
-  L.rcnt = o; o += up((size_t)3 * BG * 4);
   L.jrd = o; o += up(p->refine8 ? (size_t)BH * (L.J1 + 1) * 4 : 0);
   L.ninset = o; o += up(p->refine8 ? (size_t)BH * 4 : 0);
   L.zero_end = o;
-  L.seqd = o; o += up(sizeof(SeqArgs));
+  L.seqd = o; o += up(sizeof(SeqArgs) + sizeof(ReqPtrs));
   L.jkey = o; o += up(p->refine8 ? (size_t)BG * L.pcap * 2 : 0);
   L.jref = o; o += up(p->refine8 ? (size_t)BG * L.pcap * G * 2 : 0);
   L.winstats = o; o += up((size_t)BH * (D + 4) * 4);
@@ -110,7 +109,6 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.win = o; o += up((size_t)BG * kWindow * G * 4);
   L.t32 = o; o += up((size_t)BG * L.pcap * (p->perturb ? G : 1) * 4);
   L.clist = o; o += up((size_t)BG * L.pcap * 8);
-  L.rlist = o; o += up((size_t)BG * L.pcap * 8);
   L.xlist = o; o += up((size_t)BG * s->n_max * 8);
   L.nchunk_cap = (int64_t)BG * L.J1 + (int64_t)BG * L.pcap * 2 * G / 1024 + 16;
   L.cmap = o; o += up((size_t)L.nchunk_cap * 4);
@@ -312,8 +310,9 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
   prof_step_begin(st);
   if (clear && cudaMemsetAsync(ws, 0, L.zero_end, st) != cudaSuccess) return CSA_ERR_CUDA;
   if (src.dev) {
+    const ReqPtrs req = {K, V, src.K4w, src.boundsw, src.vmaxw, src.vnorm2w};
     if (launch_seq_prep(src.len, src.seed, shape->B, shape->n_max, params->r, params->J_override,
-                        (SeqArgs*)(ws + L.seqd), status, st) != cudaSuccess)
+                        (SeqArgs*)(ws + L.seqd), req, status, st) != cudaSuccess)
       return CSA_ERR_CUDA;
     count_launches(1);
   }
@@ -327,7 +326,6 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
   sa.two_digit = params->qcode == 1;
   sa.seqd = seqd;
   sa.requant = src.dev && src.requant;
-  sa.K = K; sa.V = V; sa.K4w = src.K4w; sa.boundsw = src.boundsw; sa.vmaxw = src.vmaxw; sa.vnorm2w = src.vnorm2w;
   cudaError_t e = launch_scan(sa, seq, shape->B, shape->d, G, bf16, nlive, st);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   count_launches(1);
@@ -345,7 +343,6 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
   a.rq = (unsigned*)(ws + L.rq);
   a.pref = (float*)(ws + L.pref);
   a.hw = (const float*)(ws + L.hw); a.front = (int*)(ws + L.front);
-  a.rlist = (uint2*)(ws + L.rlist); a.rcnt = (unsigned*)(ws + L.rcnt);
   a.xlist = (uint2*)(ws + L.xlist); a.xcnt = (unsigned*)(ws + L.xcnt);
   a.chunk_map = (unsigned*)(ws + L.cmap); a.nchunk_cap = L.nchunk_cap;
   a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);
@@ -378,7 +375,7 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
     if (launch_round(a, seq, shape->d, G, bf16, plive > 0 ? plive : 1, round, nsm, st,
                      g_prof.on ? prof_mark : nullptr) != cudaSuccess)
       return CSA_ERR_CUDA;
-    count_launches(round > 0 ? 6 : 5);
+    count_launches(4);
   }
   // exact attention for heads with no certified level and sequences without a pool
   DenseArgs da = {};

@@ -24,14 +24,21 @@ struct ScanArgs {
   bool two_digit;       // query codes of two s8 digits (QM = 127 * 257)
   // fused re-quantisation (device-length steps): the CTA whose tile holds
   // the block of token n - 1 rebuilds that block's codes, bounds, vmax and
-  // vnorm2 from K and V before it scans it
-  int requant;
+  // vnorm2 from K and V before it scans it (the arrays it writes are named
+  // in the ReqPtrs that follow *seqd in the workspace; a larger argument
+  // block would cost the plain scan registers)
+  bool requant;
+};
+
+// Arrays of the fused re-quantisation, stored right after the device-side
+// SeqArgs of a device-length step.
+struct ReqPtrs {
   const void* K;
   const void* V;
-  uint8_t* K4w;
-  float* boundsw;
-  float* vmaxw;
-  float* vnorm2w;
+  uint8_t* K4;
+  float* bounds;
+  float* vmax;
+  float* vnorm2;
 };
 
 struct SparseArgs {
@@ -72,14 +79,12 @@ struct SparseArgs {
   unsigned* chunk_map;    // [nchunk_cap]         gather work item -> bucket entry
   int64_t nchunk_cap;
   uint2* clist;           // [B*Hkv][pcap]        candidates: key, head mask | min bound level << 8
-  uint2* rlist;           // [B*Hkv][pcap]        a later round's candidates to rescore
-  unsigned* rcnt;         // [3][B*Hkv]
   int* front;             // [4][B*Hkv]           rescored through bound level (+1) before round r
   unsigned* ccnt;         // [B*Hkv]
   unsigned* nfall;        // heads that need the exact fallback
   unsigned* rq;           // round queues: [3][B*Hkv] groups per round, [3][B*Hkv] flags,
                           // [3] group counts, [3] work-item counters
-  unsigned* bcnt;         // [B*Hkv][J1]           entries of the current round
+  unsigned* bcnt;         // [3][B*Hkv][J1]        entries appended in each round
   unsigned* bcons;        // [B*Hkv][J1]           entries over the step (diagnostics)
   uint2* buckets;         // [B*Hkv][J1][pcap]    key, event masks (add | trans<<8 | before<<16)
   unsigned* plan_start;   // [B*Hkv*J1]
@@ -153,7 +158,7 @@ cudaError_t launch_quant8(const QuantArgs&, const SeqArgs&, int B, int d, bool b
                           cudaStream_t);
 int dense_nsplit(int64_t n_max);
 cudaError_t launch_seq_prep(const int64_t* len, const uint64_t* seed, int B, int64_t n_max, int r, int J_override,
-                            SeqArgs* out, unsigned* status, cudaStream_t);
+                            SeqArgs* out, const ReqPtrs& req, unsigned* status, cudaStream_t);
 
 // Launch with programmatic stream serialisation (see pdl_entry).
 template <typename... KArgs, typename... Args>

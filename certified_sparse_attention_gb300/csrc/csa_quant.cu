@@ -50,13 +50,15 @@ cudaError_t launch_quant8(const QuantArgs& a, const SeqArgs& seq, int B, int d, 
 
 // Per-sequence data of a step whose lengths and seeds live in device
 // memory: n, seed and the last grid level J = ceil(r log2 |pool|) (the
-// smallest j with 2^j >= |pool|^r, in exact 128-bit integers).  A length
-// outside [1, n_max] is clamped and flagged in the status word (bit 8).
+// smallest j with 2^j >= |pool|^r, in exact 128-bit integers), followed by
+// the arrays of the fused re-quantisation.  A length outside [1, n_max] is
+// clamped and flagged in the status word (bit 8).
 __global__ void __launch_bounds__(kMaxB) seq_prep_kernel(const int64_t* len, const unsigned long long* seed, int B,
                                                        int64_t n_max, int r, int J_override, SeqArgs* out,
-                                                       unsigned* status) {
+                                                       ReqPtrs req, unsigned* status) {
   pdl_entry();
   const int b = threadIdx.x;
+  if (b == 0) *reinterpret_cast<ReqPtrs*>(out + 1) = req;
   if (b >= kMaxB) return;
   if (b >= B) {
     out->n[b] = 0; out->seed[b] = 0ull; out->J[b] = 0;
@@ -82,9 +84,9 @@ __global__ void __launch_bounds__(kMaxB) seq_prep_kernel(const int64_t* len, con
 }
 
 cudaError_t launch_seq_prep(const int64_t* len, const uint64_t* seed, int B, int64_t n_max, int r, int J_override,
-                            SeqArgs* out, unsigned* status, cudaStream_t st) {
+                            SeqArgs* out, const ReqPtrs& req, unsigned* status, cudaStream_t st) {
   launch_pdl(seq_prep_kernel, dim3(1), dim3(kMaxB), 0, st, len, (const unsigned long long*)seed, B, n_max, r,
-             J_override, out, status);
+             J_override, out, req, status);
   return cudaGetLastError();
 }
 

@@ -39,7 +39,7 @@ __device__ __forceinline__ float tree16(const float* v) {
 // in place of the two residual trees (|a_c - alpha at_c| <= alpha (1/2 +
 // 2^-6) for codes this fine); I = 256 I_hi + I_lo from two products.
 template <int D, int G, typename E, bool TWO, bool REQ>
-__global__ void __launch_bounds__(256, 6) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq_arg) {
+__global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq_arg) {
   pdl_entry();
   const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   constexpr int ND = TWO ? 2 : 1;    // query-code digits
@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(256, 6) scan_kernel(const ScanArgs a, const __
     __shared__ float s_qvm[kBlock];
     const int64_t lb = (n - 1) / kBlock;
     if (lb * kBlock >= key0 && lb * kBlock < key0 + kTile) {
-      quantize_block<D, E>(a.K, a.V, a.K4w, a.boundsw, a.vmaxw, a.vnorm2w, a.n_max, a.nblk_max, bg, lb, n, s_qvm);
+      const ReqPtrs& rp = *reinterpret_cast<const ReqPtrs*>(a.seqd + 1);
+      quantize_block<D, E>(rp.K, rp.V, rp.K4, rp.bounds, rp.vmax, rp.vnorm2, a.n_max, a.nblk_max, bg, lb, n, s_qvm);
       __threadfence();   // the new codes and bounds reach L2 before the copies below read them
       __syncthreads();
     }

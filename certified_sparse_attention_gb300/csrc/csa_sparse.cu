@@ -14,8 +14,6 @@
 //                   (no values, no K rows: for the stop predictor)
 //   predict_kernel  window sums (D_R, N_R, H_R) and a predicted stop level
 //                   per head that sizes the first gather round
-//   rsel_kernel     (rounds after the first) the candidates a round newly
-//                   needs, compacted
 //   rows_kernel<1>  (per round) float32 scores of the listed candidates
 //                   whose smallest bound level lies in the range that the
 //                   round's levels newly need (jbar_i <= j implies
@@ -23,7 +21,9 @@
 //   levels_kernel   (per round) each key that changes a head's sums at a
 //                   level of the round is appended once to the (b, g, level)
 //                   bucket, with per-head event masks
-//   vplan_kernel    (per round) ranges of the new bucket entries
+//   vplan_kernel    (per round, only for large batches) ranges of the new
+//                   bucket entries (otherwise each value-sum CTA computes
+//                   them)
 //   vsum_kernel     (per round, bf16) V rows of the bucketed keys in
 //                   batches of 16 entries of one level; per-level
 //                   Horvitz-Thompson sums (light count, sum v, sum ||v||^2;
@@ -301,12 +301,6 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
   if (MODE == 0) {
     list = a.xlist + (int64_t)bg * a.n_max;
     cnt = (int)a.xcnt[bg];
-  } else if (round > 0) {
-    // later rounds: the wanted entries, compacted by rsel_kernel
-    list = a.rlist + (int64_t)bg * a.pcap;
-    cnt = (int)a.rcnt[round * (a.B * a.Hkv) + bg];
-    lnew = 255;
-    if (cnt == 0) return;
   } else {
     list = a.clist + (int64_t)bg * a.pcap;
     cnt = (int)a.ccnt[bg];
@@ -520,57 +514,6 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
       if (y > -INFINITY) atomic_max_f(a.cmax + (int64_t)(bh0 + tid) * 4 + 3, y);
     }
   }
-}
-
-// Rounds after the first: the candidates of the groups still running whose
-// smallest bound level lies in the range the round newly needs, compacted
-// (one list reservation per CTA) so that the rescoring pass reads only
-// those.  Also advances the group's rescored-through level.
-constexpr int kRsel = 4096;      // list entries per CTA
-
-template <int G>
-__global__ void __launch_bounds__(256) rsel_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
-                                                   int round) {
-  pdl_entry();
-  const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
-  __shared__ uint2 s_list[kRsel];
-  __shared__ unsigned s_n, s_gbase;
-  const int tid = threadIdx.x;
-  const int BG = a.B * a.Hkv;
-  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
-  if (seq.n[b] <= kWindow) return;
-  const int bh0 = b * a.Hq + g * G;
-  const int lold = a.front[round * BG + bg] - 1;
-  int lnew = -1;
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const int* st = a.state + (int64_t)(bh0 + h) * 4;
-    if (!(st[3] & kFlagDone)) lnew = max(lnew, st[1]);
-  }
-  if (blockIdx.x == 0 && tid == 0) a.front[(round + 1) * BG + bg] = max(lold, lnew) + 1;
-  const int cnt = (int)a.ccnt[bg];
-  const int e0 = blockIdx.x * kRsel;
-  if (lnew <= lold || e0 >= cnt) return;
-  if (tid == 0) s_n = 0u;
-  __syncthreads();
-  const uint2* cl = a.clist + (int64_t)bg * a.pcap;
-#pragma unroll 4
-  for (int k = 0; k < kRsel / 256; ++k) {
-    const int i = e0 + k * 256 + tid;
-    uint2 e = make_uint2(0u, 0u);
-    bool keep = false;
-    if (i < cnt) {
-      e = cl[i];
-      const int jm = a.refine8 ? (int)(a.jkey[(int64_t)bg * a.pcap + e.x] & 0x1FFu) : (int)((e.y >> 8) & 0xFFu);
-      keep = jm > lold && jm <= lnew;
-    }
-    const int slot = warp_append(&s_n, keep);
-    if (slot >= 0) s_list[slot] = e;
-  }
-  __syncthreads();
-  if (tid == 0) s_gbase = s_n ? atomicAdd(a.rcnt + round * BG + bg, s_n) : 0u;
-  __syncthreads();
-  for (unsigned i = tid; i < s_n; i += 256) a.rlist[(int64_t)bg * a.pcap + s_gbase + i] = s_list[i];
 }
 
 // ------------------------------------------------- 8-bit refinement tier
@@ -1212,7 +1155,7 @@ constexpr int kLevItemLate = 512; // later rounds: few groups, more and shorter 
 // One work item: keys [k0, k0 + isz) of group bg.
 template <int G, bool PH>
 __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& seq, int bg, int64_t k0,
-                                            int isz) {
+                                            int isz, int round) {
   const int lane = threadIdx.x & 31;
   const int b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
@@ -1236,7 +1179,8 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
 #pragma unroll
   for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
   const float neg_r = -(float)a.r;
-  unsigned* bcnt = a.bcnt + (int64_t)bg * a.J1;
+  // this round's bucket counters (one set per round, zeroed with the step)
+  unsigned* bcnt = a.bcnt + ((int64_t)round * a.B * a.Hkv + bg) * a.J1;
   uint2* bk = a.buckets + (int64_t)bg * a.J1 * a.pcap;
   const float* sb = a.s32 + (int64_t)bg * a.pcap * G;
   const float* tb = a.t32 + (int64_t)bg * a.pcap * (PH ? G : 1);
@@ -1355,7 +1299,7 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
     const unsigned item = s_item;
     __syncthreads();
     if (item >= total) break;
-    levels_item<G, PH>(a, seq, (int)a.rq[round * BG + item / tpg], (int64_t)(item % tpg) * isz, isz);
+    levels_item<G, PH>(a, seq, (int)a.rq[round * BG + item / tpg], (int64_t)(item % tpg) * isz, isz, round);
   }
 }
 
@@ -1365,24 +1309,23 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
 // it into per-warp ranges); otherwise it counts work items of kChunk
 // entries and chunk_map maps each item to its bucket.
 template <bool EV>
-__global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nent) {
+__global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nent, int round) {
   pdl_entry();
   __shared__ unsigned s_part[1024];
   const int tid = threadIdx.x;
   const int per = (nent + 1023) / 1024;
   const int i0 = tid * per, i1 = min(nent, i0 + per);
   unsigned sum = 0;
+  const unsigned* cnt = a.bcnt + (int64_t)round * nent;   // this round's counters
   for (int i = i0; i < i1; ++i) {
-    // this round's entries; the counters restart at 0 for the next round
-    // (a bucket holds at most one entry per key in a round), the step's
-    // cumulative count is kept in bcons (diagnostics)
+    // this round's entries (a bucket holds at most one entry per key in a
+    // round); the step's cumulative count is kept in bcons (diagnostics)
     const unsigned st = 0;
-    unsigned en = a.bcnt[i];
+    unsigned en = cnt[i];
     if (en > (unsigned)a.pcap) en = (unsigned)a.pcap;
     a.plan_start[i] = st;
     a.plan_end[i] = en;
     a.bcons[i] += en;
-    a.bcnt[i] = 0u;
     sum += EV ? en - st : (en - st + kChunk - 1) / kChunk;
   }
   // exclusive prefix of the per-thread sums: a shuffle scan within each
@@ -1673,29 +1616,35 @@ struct VsGen {
 
 // Smallest bucket e' >= e0 whose new entries hold concatenated position x
 // (plan_off non-decreasing, plan_off[nent] > x), with its offsets.
-__device__ __forceinline__ void vs_seek(const SparseArgs& a, int nent, int e0, unsigned x, VsGen& g) {
+// (poff: the exclusive prefix of the round's entries per bucket, in shared
+// memory or in the workspace; every bucket's new entries start at 0)
+__device__ __forceinline__ void vs_seek(const SparseArgs& a, const unsigned* poff, int nent, int e0, unsigned x,
+                                        VsGen& g) {
   const int lane = threadIdx.x & 31;
   for (int base = e0;; base += 32) {
     const int e = base + lane;
     const bool in = e < nent;
-    const unsigned o1 = in ? a.plan_off[e + 1] : 0xffffffffu;
+    const unsigned o1 = in ? poff[e + 1] : 0xffffffffu;
     const unsigned bal = __ballot_sync(0xffffffffu, o1 > x);
     if (bal) {
       const int f = __ffs(bal) - 1;
-      const unsigned o0 = in ? a.plan_off[e] : 0u;
-      const unsigned st = in ? a.plan_start[e] : 0u;
+      const unsigned o0 = in ? poff[e] : 0u;
       g.e = base + f;
       g.bg = g.e / a.J1;
       g.off0 = __shfl_sync(0xffffffffu, o0, f);
       g.off1 = __shfl_sync(0xffffffffu, o1, f);
-      g.start = __shfl_sync(0xffffffffu, st, f);
+      g.start = 0u;
       return;
     }
   }
 }
 
+// Buckets up to this count get their gather plan in each value-sum CTA's
+// shared memory (no separate plan launch); more use vplan_kernel's.
+constexpr int kPlanSmem = 4096;
+
 template <int D, int G>
-__global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int nent) {
+__global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int nent, int round) {
   pdl_entry();
   using Lt = VsLayout<D, G>;
   constexpr int RB = Lt::RB, MT = Lt::MT, NT = D / 8, CH = RB / 16;
@@ -1712,7 +1661,47 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
   uint8_t* s_at = base + Lt::at;
   uint8_t* s_bx = base + Lt::bx;
 
-  const unsigned E = a.plan_off[nent];
+  // the round's entries per bucket and their exclusive prefix over the
+  // buckets: computed here by every CTA (small plans) or read from
+  // vplan_kernel's (large ones)
+  const unsigned* poff = a.plan_off;
+  if (nent <= kPlanSmem) {
+    unsigned* s_plan = reinterpret_cast<unsigned*>(dsm + kVsW * Lt::per_warp);
+    __shared__ unsigned s_wsum[kVsW];
+    const unsigned* cnt = a.bcnt + (int64_t)round * nent;
+    const int nth = kVsW * 32, t = threadIdx.x;
+    const int per = (nent + nth - 1) / nth;
+    const int i0 = t * per, i1 = min(nent, i0 + per);
+    unsigned sum = 0;
+    for (int i = i0; i < i1; ++i) {
+      const unsigned en = min(cnt[i], (unsigned)a.pcap);
+      if (blockIdx.x == 0) a.bcons[i] += en;
+      sum += en;
+    }
+    unsigned inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned x = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += x;
+    }
+    if (lane == 31) s_wsum[w] = inc;
+    __syncthreads();
+    unsigned wbase = 0, tot = 0;
+#pragma unroll
+    for (int x = 0; x < kVsW; ++x) {
+      if (x < w) wbase += s_wsum[x];
+      tot += s_wsum[x];
+    }
+    unsigned run = wbase + inc - sum;
+    for (int i = i0; i < i1; ++i) {
+      s_plan[i] = run;
+      run += min(cnt[i], (unsigned)a.pcap);
+    }
+    if (t == 0) s_plan[nent] = tot;
+    __syncthreads();
+    poff = s_plan;
+  }
+  const unsigned E = poff[nent];
   const unsigned nw = gridDim.x * kVsW, gw = blockIdx.x * kVsW + w;
   VsGen gen;
   gen.pos = (unsigned)(((unsigned long long)E * gw) / nw);
@@ -1723,14 +1712,14 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
     int lo = 0, hi = nent;
     while (hi - lo > 1) {
       const int p = lo + 1 + (int)(((int64_t)(hi - lo - 1) * lane) / 32);
-      const unsigned bal = __ballot_sync(0xffffffffu, a.plan_off[p] <= gen.pos);
+      const unsigned bal = __ballot_sync(0xffffffffu, poff[p] <= gen.pos);
       const int cnt = __popc(bal);
       const int plo = __shfl_sync(0xffffffffu, p, cnt > 0 ? cnt - 1 : 0);
       const int phi = __shfl_sync(0xffffffffu, p, cnt < 32 ? cnt : 31);
       if (cnt == 0) hi = plo;
       else { lo = plo; if (cnt < 32) hi = phi; }
     }
-    vs_seek(a, nent, lo, gen.pos, gen);
+    vs_seek(a, poff, nent, lo, gen.pos, gen);
   }
 
   // next batch descriptor into slot ds; entries and c32 by cp.async
@@ -1739,7 +1728,7 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
     int cnt = 0, e = -1, bg = 0;
     unsigned eoff = 0;
     if (gen.pos < gen.end) {
-      if (gen.pos >= gen.off1) vs_seek(a, nent, gen.e + 1, gen.pos, gen);
+      if (gen.pos >= gen.off1) vs_seek(a, poff, nent, gen.e + 1, gen.pos, gen);
       e = gen.e;
       bg = gen.bg;
       cnt = (int)min(min(gen.off1, gen.end) - gen.pos, (unsigned)kVsB);
@@ -2292,23 +2281,28 @@ void launch_cset_t(int64_t nmax, int nsm, cudaStream_t st, const SparseArgs& a, 
   launch_pdl(cset_kernel<G>, grid, dim3(256), 0, st, a, seq, (int)span);
 }
 template <int D, int G, typename E>
-void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int nent,
+void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int nent, int round,
                       PhaseMark mark) {
   if constexpr (sizeof(E) == 2) {
-    constexpr int smem = VsLayout<D, G>::smem;
+    const bool small = nent <= kPlanSmem;
+    const int smem = VsLayout<D, G>::smem + (small ? (nent + 1) * 4 : 0);
     cudaFuncSetAttribute(vsum_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vsum_kernel<D, G>, kVsW * 32, smem) !=
             cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
-    launch_pdl(vplan_kernel<true>, dim3(1), dim3(1024), 0, st, a, nent);
+    if (!small) {
+      launch_pdl(vplan_kernel<true>, dim3(1), dim3(1024), 0, st, a, nent, round);
+      add_launches(1);
+    }
     if (mark) mark(7, st);
-    launch_pdl(vsum_kernel<D, G>, dim3((unsigned)(nsm * per_sm)), dim3(kVsW * 32), smem, st, a, nent);
+    launch_pdl(vsum_kernel<D, G>, dim3((unsigned)(nsm * per_sm)), dim3(kVsW * 32), smem, st, a, nent, round);
   } else {
     constexpr int smem = vgather_smem<D, G, E>();
     cudaFuncSetAttribute(vgather_kernel<D, G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    launch_pdl(vplan_kernel<false>, dim3(1), dim3(1024), 0, st, a, nent);
+    launch_pdl(vplan_kernel<false>, dim3(1), dim3(1024), 0, st, a, nent, round);
+    add_launches(1);
     if (mark) mark(7, st);
     launch_pdl(vgather_kernel<D, G, E>, dim3((unsigned)(nsm * 2)), dim3(256), smem, st, a, seq, nent);
   }
@@ -2382,10 +2376,6 @@ cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
   if (nct > items) nct = items;
   if (nct < 1) nct = 1;
   dim3 grid((unsigned)nct);
-  if (round > 0) {
-    dim3 rg((unsigned)((pmax_live + kRsel - 1) / kRsel), (unsigned)(a.B * a.Hkv));
-    CSA_G_SWITCH(rsel_kernel, rg, dim3(256), 0, st, a, seq, round)
-  }
   CSA_DG_SWITCH(launch_rows1, (pmax_live, nsm, st, a, seq, round))
   if (mark) mark(4, st);
   switch (G * 2 + (a.per_head ? 1 : 0)) {
@@ -2401,7 +2391,7 @@ cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
   }
   if (mark) mark(6, st);
   const int nent = a.B * a.Hkv * a.J1;
-  CSA_DG_SWITCH(launch_vgather_t, (nsm, st, a, seq, nent, mark))
+  CSA_DG_SWITCH(launch_vgather_t, (nsm, st, a, seq, nent, round, mark))
   if (mark) mark(8, st);
   dim3 cg((unsigned)(a.B * a.Hq));
   if (d == 128) launch_pdl(certify_kernel<128>, cg, dim3(256), 0, st, a, seq, round);

@@ -918,6 +918,44 @@ def stress_sweep(args):
             torch.cuda.empty_cache()
 
 
+def dense_only(args):
+    """The same-build dense decode alone on the benchmark workload (or the
+    --n / --batch reduction), for profiler captures of that kernel: warm-up
+    and timed calls on one resident layer; one JSON line with its time and
+    bytes per second.  Not part of the benchmark line."""
+    import dataclasses
+    import torch
+    import synth
+    import certified_sparse_attention_gb300 as csa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    csa.load_library()
+    w = synth.workload(WORKLOAD)
+    if args.n or args.batch:
+        w = dataclasses.replace(w, n=args.n or w.n, B=args.batch or w.B)
+    shape, data = setup_layers(w, [0], dev, csa)
+    d = data[0]
+    dense = csa.DenseDecode(shape, dev)
+    lens = [w.n] * w.B
+    st = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        dense(d["q"][i % 4], d["K"], d["V"], lens, st)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(args.steps):
+        dense(d["q"][i % 4], d["K"], d["V"], lens, st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    csa.check(csa.csa_check(dense.ws), "csa_check (dense)")
+    us = e0.elapsed_time(e1) / args.steps * 1e3
+    nbytes = 2 * w.B * w.Hkv * w.n * w.d * 2
+    print(json.dumps({"dense_only": {"workload": w.name, "n": w.n, "B": w.B,
+                                     "us": round(us, 1),
+                                     "gbs": round(nbytes / us / 1e3, 1)}}))
+
+
 def synth_workload(name):
     import synth
     return synth.workload(name)
@@ -935,6 +973,9 @@ def main(argv=None):
                     help="override the context length (profiler captures)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch (profiler captures)")
+    ap.add_argument("--dense-only", action="store_true",
+                    help="time the same-build dense decode alone (profiler "
+                         "captures of that kernel)")
     ap.add_argument("--stress-sweep", action="store_true",
                     help="the stress sweep (256K-1M tokens, eps 0.01-0.1, "
                          "flat / heavy-tailed / adversarial): one JSON line "
@@ -957,6 +998,10 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank, local)
+        return
+    if args.dense_only:
+        if rank == 0:
+            dense_only(args)
         return
     if args.stress_sweep:
         if rank == 0:

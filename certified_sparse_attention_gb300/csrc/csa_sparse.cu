@@ -1155,7 +1155,7 @@ constexpr int kLevItemLate = 512; // later rounds: few groups, more and shorter 
 // One work item: keys [k0, k0 + isz) of group bg.
 template <int G, bool PH>
 __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& seq, int bg, int64_t k0,
-                                            int isz, int round) {
+                                            int isz, int round, uint2* sev) {
   const int lane = threadIdx.x & 31;
   const int b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
@@ -1218,70 +1218,64 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
       cs[h] = ns[h];
       ct[h] = nt[h];
     }
-    if (wlo == whi) {
-      // a one-level round (the common case for flat groups): at most one
-      // event per key, slots by a ballot and one atomic per warp
-      const int l = wlo;
+    // the key's entries for the round's levels: for each head a light
+    // entry at jl < hl in its range (bit h) and the move to the heavy sums
+    // at hl in its range (bit 8 + h, and bit 16 + h when the key was light
+    // before), one entry per distinct level with every head's bits merged
+    // (a bucket holds at most one entry per key in a round).  The warp
+    // first packs its lanes' entries into shared memory (the level in bits
+    // 24-31 of the mask word), then takes them 32 at a time: lanes with the
+    // same level share one slot reservation, so a warp makes one round trip
+    // to the counters per 32 entries rather than one per level of a lane.
+    unsigned pa = 0, pt = 0;
+    if (key < kend) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if (jl[h] < hl[h] && jl[h] > lo[h] && jl[h] <= hi[h]) pa |= 1u << h;
+        if (hl[h] <= J && hl[h] > lo[h] && hl[h] <= hi[h]) pt |= 1u << h;
+      }
+    }
+    unsigned nev = 0;
+#pragma unroll
+    for (int k = 0; k < 2 * G; ++k) {
+      if (!__any_sync(0xffffffffu, (pa | pt) != 0u)) break;
+      int cur = 1 << 20;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if ((pa >> h) & 1u) cur = min(cur, jl[h]);
+        if ((pt >> h) & 1u) cur = min(cur, hl[h]);
+      }
       unsigned m = 0;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        if (!(l > lo[h] && l <= hi[h])) continue;
-        if (jl[h] == l && jl[h] < hl[h]) m |= 1u << h;
-        if (hl[h] == l) {
+        if (((pa >> h) & 1u) && jl[h] == cur) { m |= 1u << h; pa &= ~(1u << h); }
+        if (((pt >> h) & 1u) && hl[h] == cur) {
           m |= 1u << (8 + h);
           if (jl[h] < hl[h]) m |= 1u << (16 + h);
+          pt &= ~(1u << h);
         }
       }
       const unsigned bal = __ballot_sync(0xffffffffu, m != 0u);
+      if (m) sev[nev + __popc(bal & ((1u << lane) - 1u))] = make_uint2((unsigned)key, m | ((unsigned)cur << 24));
+      nev += __popc(bal);
+    }
+    __syncwarp();
+    for (unsigned i0 = 0; i0 < nev; i0 += 32) {
+      const bool has = i0 + lane < nev;
+      const uint2 e = has ? sev[i0 + lane] : make_uint2(0u, 0u);
+      const int l = has ? (int)(e.y >> 24) : -1;
+      const unsigned grp = __match_any_sync(0xffffffffu, l);
+      const int leader = __ffs(grp) - 1;
       unsigned p0 = 0;
-      if (lane == 0 && bal) p0 = atomicAdd(bcnt + l, (unsigned)__popc(bal));
-      p0 = __shfl_sync(0xffffffffu, p0, 0);
-      if (m) {
-        const unsigned p = p0 + (unsigned)__popc(bal & ((1u << lane) - 1u));
-        if (p < (unsigned)a.pcap) bk[(int64_t)l * a.pcap + p] = make_uint2((unsigned)key, m);
+      if (lane == leader && l >= 0) p0 = atomicAdd(bcnt + l, (unsigned)__popc(grp));
+      p0 = __shfl_sync(0xffffffffu, p0, leader);
+      if (l >= 0) {
+        const unsigned p = p0 + (unsigned)__popc(grp & ((1u << lane) - 1u));
+        if (p < (unsigned)a.pcap) bk[(int64_t)l * a.pcap + p] = make_uint2(e.x, e.y & 0x00FFFFFFu);
         else atomicOr(a.status, 2u);
       }
-      continue;
     }
-    // events of the key in the round (a light entry at jl < hl, the
-    // light-to-heavy transition at hl), as a mask over 32-level windows
-    for (int base = wlo; base <= whi; base += 32) {
-      unsigned evm = 0;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const int e1 = jl[h] - base, e2 = hl[h] - base;
-        if (jl[h] < hl[h] && jl[h] > lo[h] && jl[h] <= hi[h] && e1 >= 0 && e1 < 32) evm |= 1u << e1;
-        if (hl[h] <= J && hl[h] > lo[h] && hl[h] <= hi[h] && e2 >= 0 && e2 < 32) evm |= 1u << e2;
-      }
-      while (__any_sync(0xffffffffu, evm != 0u)) {
-        int l = -1;
-        if (evm) {
-          l = base + __ffs(evm) - 1;
-          evm &= evm - 1u;
-        }
-        unsigned m = 0;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          if (!(l > lo[h] && l <= hi[h])) continue;
-          if (jl[h] == l && jl[h] < hl[h]) m |= 1u << h;
-          if (hl[h] == l) {
-            m |= 1u << (8 + h);
-            if (jl[h] < hl[h]) m |= 1u << (16 + h);
-          }
-        }
-        // lanes with the same level take consecutive slots of its bucket
-        const unsigned grp = __match_any_sync(0xffffffffu, l);
-        const int leader = __ffs(grp) - 1;
-        unsigned p0 = 0;
-        if (lane == leader && l >= 0) p0 = atomicAdd(bcnt + l, (unsigned)__popc(grp));
-        p0 = __shfl_sync(0xffffffffu, p0, leader);
-        if (l >= 0) {
-          const unsigned p = p0 + (unsigned)__popc(grp & ((1u << lane) - 1u));
-          if (p < (unsigned)a.pcap) bk[(int64_t)l * a.pcap + p] = make_uint2((unsigned)key, m);
-          else atomicOr(a.status, 2u);
-        }
-      }
-    }
+    __syncwarp();
   }
 }
 
@@ -1291,6 +1285,7 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
   pdl_entry();
   const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   __shared__ unsigned s_item;
+  __shared__ uint2 s_ev[8][64 * G];      // per warp: up to 2G entries per lane
   const int BG = a.B * a.Hkv;
   const unsigned total = a.rq[6 * BG + round] * tpg;
   for (;;) {
@@ -1299,7 +1294,8 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
     const unsigned item = s_item;
     __syncthreads();
     if (item >= total) break;
-    levels_item<G, PH>(a, seq, (int)a.rq[round * BG + item / tpg], (int64_t)(item % tpg) * isz, isz, round);
+    levels_item<G, PH>(a, seq, (int)a.rq[round * BG + item / tpg], (int64_t)(item % tpg) * isz, isz, round,
+                       s_ev[threadIdx.x >> 5]);
   }
 }
 

@@ -484,7 +484,8 @@ def run_ours(args, world, rank, local):
     # --sub-batches: profiler captures of the unsplit chain (a scheduling
     # choice only; the reported line uses the default)
     params = csa.make_params(w.eps, w.delta, w.r, sub_batches=args.sub_batches,
-                             qcode=args.qcode, refine8=args.refine8)
+                             qcode=args.qcode, refine8=args.refine8,
+                             dots=args.dots)
     step = csa.DecodeStep(shape, params, device, with_stats=False)
     step_diag = csa.DecodeStep(shape, params, device, with_stats=True)
     dense = csa.DenseDecode(shape, device)
@@ -986,6 +987,8 @@ def main(argv=None):
                     help="layers of the whole-model decode loop (0: skip it)")
     ap.add_argument("--no-modes", action="store_true",
                     help="skip the CLT / other-measure comparisons (profiler captures)")
+    ap.add_argument("--dots", type=int, default=0,
+                    help="the scan's integer dots: 0 tensor cores, 1 dp4a")
     ap.add_argument("--refine8", type=int, default=0,
                     help="8-bit refinement tier: 0 off, 1 every group, 2 "
                          "groups whose first range reaches level r")

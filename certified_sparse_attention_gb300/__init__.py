@@ -65,7 +65,7 @@ class csa_params(ctypes.Structure):
                 ("r", ctypes.c_int), ("measure", ctypes.c_int),
                 ("J_override", ctypes.c_int), ("sub_batches", ctypes.c_int),
                 ("perturb", ctypes.c_int), ("qcode", ctypes.c_int),
-                ("refine8", ctypes.c_int)]
+                ("refine8", ctypes.c_int), ("dots", ctypes.c_int)]
 
 
 class csa_head_stats(ctypes.Structure):
@@ -196,10 +196,10 @@ def make_shape(B, Hq, Hkv, d, n_max, dtype) -> csa_shape:
 
 def make_params(eps=0.05, delta=0.05, r=2, measure=CSA_MEASURE_VALUE,
                 J_override=-1, sub_batches=0, perturb=0,
-                qcode=0, refine8=0) -> csa_params:
+                qcode=0, refine8=0, dots=0) -> csa_params:
     return csa_params(float(eps), float(delta), int(r), int(measure),
                       int(J_override), int(sub_batches), int(perturb),
-                      int(qcode), int(refine8))
+                      int(qcode), int(refine8), int(dots))
 
 
 def csa_workspace_size(shape: csa_shape, params: csa_params) -> int:

@@ -45,7 +45,7 @@ bool params_ok(const csa_params* p) {
   return p && p->eps > 0.f && std::isfinite(p->eps) && p->delta > 0.f && p->delta < 1.f && p->r >= 1 &&
          p->r <= 4 && p->measure >= 0 && p->measure <= 3 && p->J_override >= -1 && p->J_override <= kMaxJ &&
          p->sub_batches >= 0 && p->sub_batches <= kMaxSub && (p->perturb == 0 || p->perturb == 1) &&
-         (p->qcode == 0 || p->qcode == 1) && p->refine8 >= 0 && p->refine8 <= 2;
+         (p->qcode == 0 || p->qcode == 1) && p->refine8 >= 0 && p->refine8 <= 2 && (p->dots == 0 || p->dots == 1);
 }
 
 // z with P(|N(0,1)| > z) = delta, i.e. erfc(z / sqrt 2) = delta: bisection
@@ -326,6 +326,7 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
   sa.two_digit = params->qcode == 1;
   sa.seqd = seqd;
   sa.requant = src.dev && src.requant;
+  sa.dp4a = params->dots == 1;
   cudaError_t e = launch_scan(sa, seq, shape->B, shape->d, G, bf16, nlive, st);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   count_launches(1);

@@ -28,6 +28,7 @@ struct ScanArgs {
   // in the ReqPtrs that follow *seqd in the workspace; a larger argument
   // block would cost the plain scan registers)
   bool requant;
+  bool dp4a;            // integer dots by CUDA-core dp4a instead of tensor cores
 };
 
 // Arrays of the fused re-quantisation, stored right after the device-side

@@ -38,7 +38,7 @@ __device__ __forceinline__ float tree16(const float* v) {
 // and the closed-form residual term fl(fl(15 d) * fl(alpha * (1/2 + 2^-6)))
 // in place of the two residual trees (|a_c - alpha at_c| <= alpha (1/2 +
 // 2^-6) for codes this fine); I = 256 I_hi + I_lo from two products.
-template <int D, int G, typename E, bool TWO, bool REQ>
+template <int D, int G, typename E, bool TWO, bool REQ, bool DP4A = false>
 __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq_arg) {
   pdl_entry();
   const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
 #pragma unroll
     for (int dd = 0; dd < ND; ++dd) acc[dd][0] = acc[dd][1] = acc[dd][2] = acc[dd][3] = 0;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
+    for (int ks = 0; ks < (DP4A ? 0 : KS); ++ks) {
       // word 4ks+tq of rows r0, r1: chunk ks, word tq (swizzled chunks)
       const unsigned w0 = *reinterpret_cast<const unsigned*>(s_codes + r0 * ROWB + ((ks ^ (r0 & (CHR - 1))) << 4) + 4 * tq);
       const unsigned w1 = *reinterpret_cast<const unsigned*>(s_codes + r1 * ROWB + ((ks ^ (r1 & (CHR - 1))) << 4) + 4 * tq);
@@ -272,6 +272,26 @@ __global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __gri
     int I4[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) I4[e] = TWO ? acc[ND - 1][e] * 256 + acc[0][e] : acc[0][e];
+    if constexpr (DP4A) {
+      // the CUDA-core alternative for the same (key, head) pairs: dp4a over
+      // the code words, low nibbles (even channels) with the even query
+      // word, high nibbles with the odd one (kept to compare the two)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = e < 2 ? r0 : r1, h = 2 * tq + (e & 1);
+        int sacc = 0;
+        if (h < G) {
+#pragma unroll
+          for (int k = 0; k < WE; ++k) {
+            const unsigned wv = *reinterpret_cast<const unsigned*>(
+                s_codes + r * ROWB + (((k >> 2) ^ (r & (CHR - 1))) << 4) + 4 * (k & 3));
+            sacc = __dp4a((int)(wv & 0x0F0F0F0Fu), (int)s_atw[0][blk][h][k], sacc);
+            sacc = __dp4a((int)((wv >> 4) & 0x0F0F0F0Fu), (int)s_atw[0][blk][h][WE + k], sacc);
+          }
+        }
+        I4[e] = sacc;
+      }
+    }
     // acc[0], acc[1]: key r0, heads 2tq, 2tq+1; acc[2], acc[3]: key r1
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -332,7 +352,9 @@ cudaError_t launch_scan_t(const ScanArgs& a, const SeqArgs& seq, int B, int64_t 
   // REQ: the variant that re-quantises the appended block first (device-
   // length steps); a separate instantiation keeps the plain scan's
   // registers (and resident CTAs) as they are
-  if (a.requant) {
+  if (a.dp4a && !a.requant && !a.two_digit) {
+    launch_pdl(scan_kernel<D, G, E, false, false, true>, grid, dim3(256), 0, st, a, seq);
+  } else if (a.requant) {
     if (a.two_digit) launch_pdl(scan_kernel<D, G, E, true, true>, grid, dim3(256), 0, st, a, seq);
     else launch_pdl(scan_kernel<D, G, E, false, true>, grid, dim3(256), 0, st, a, seq);
   } else {

@@ -115,6 +115,10 @@ typedef struct {
                    * reaches level r (the near-uniform groups, which stop
                    * near level 0, stay on the 4-bit bounds).  Results do
                    * not depend on it; keys_read counts the refined levels */
+  int dots;       /* the scan's exact integer dot products: 0 = tensor cores
+                   * (mma.sync u8 x s8, default); 1 = CUDA-core dp4a (the
+                   * comparison the choice rests on; int8 query codes only).
+                   * Results are identical                                  */
 } csa_params;
 
 /* Optional per-(sequence, query head) diagnostics. */

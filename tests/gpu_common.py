@@ -51,7 +51,7 @@ class DeviceRun:
     def __init__(self, w: synth.Workload, K, V, q, lens, seeds, n_alloc,
                  device="cuda:0", eps=None, delta=None, r=None,
                  measure=0, J_override=-1, sub_batches=0, perturb=0,
-                 qcode=0, refine8=0):
+                 qcode=0, refine8=0, dots=0):
         import torch
         import certified_sparse_attention_gb300 as csa
         self.csa = csa
@@ -63,7 +63,7 @@ class DeviceRun:
                                       w.delta if delta is None else delta,
                                       w.r if r is None else r, measure,
                                       J_override, sub_batches, perturb,
-                                      qcode, refine8)
+                                      qcode, refine8, dots)
         Kp = np.zeros((w.B, w.Hkv, n_alloc, w.d), np.float32)
         Vp = np.zeros_like(Kp)
         Kp[:, :, :K.shape[2]] = K

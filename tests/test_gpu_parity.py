@@ -407,3 +407,13 @@ def test_decode_refine8(refine8, r, n):
     run, rep = run_and_compare(w, K, V, q, [n, n - 211], seeds, n,
                                refine8=refine8)
     assert rep["heads"] == 16
+
+
+@pytest.mark.parametrize("G,n", [(4, 1500), (8, 4093)])
+def test_decode_scan_dots_on_cuda_cores(G, n):
+    # the scan's integer dot products by dp4a instead of tensor cores: the
+    # same bounds bit for bit, hence the same everything
+    w, K, V, q = _case("llama16k", n, B=2, Hq=2 * G, Hkv=2)
+    seeds = synth.step_seeds(w, 16)
+    run, rep = run_and_compare(w, K, V, q, [n, n - 99], seeds, n, dots=1)
+    assert rep["heads"] == 4 * G

@@ -17,7 +17,10 @@ namespace csa {
 constexpr int kBlock = 64;     // quantisation block (tokens)
 constexpr int kWindow = 64;    // window read exactly (last tokens)
 constexpr int kTile = 256;     // keys per scan / candidate tile
-constexpr int kCandSeg = 4096; // pool keys per candidate-list segment (one candidate CTA)
+#ifndef CSA_CAND_SEG
+#define CSA_CAND_SEG 4096
+#endif
+constexpr int kCandSeg = CSA_CAND_SEG; // pool keys per candidate-list segment (one candidate CTA)
 constexpr int kMaxB = 128;     // sequences per call
 constexpr int kMaxHeads = 1024; // query heads and KV heads per call
 constexpr int kMaxJ = 255;     // last grid level supported

@@ -21,15 +21,21 @@ multiply-add), with the operation order written out in ``bounds.py`` and
 ``fp32.py``.
 
 Parity status per function (the pins live in ``tests/test_oracle_*.py``):
-  * hashing / log2, quantiser, bounds, inclusion law, nestedness,
-    unbiasedness, exact special cases, Chernoff / Bernstein events,
-    coverage, the Theorem 2 error bound and sample size: pinned (closed
-    forms, brute force, Monte Carlo).
-  * which level stops and the exact o / beta values there: parity unpinned by
-    the pages (they print no worked example); pinned only through the
-    statistical and algebraic checks above and metamorphic relations
-    between runs (monotone in eps and delta, homogeneous in the values,
-    invariant to a common score shift).
+  * hashing / log2, quantiser (4- and 8-bit), bounds, inclusion law,
+    nestedness, unbiasedness, exact special cases, the per-level sums (a
+    pool summed by hand, and a per-key event formulation), the Chernoff
+    interval (exact Poisson-binomial coverage, not over-wide), the G and H
+    events, the Pinelis constant (the exact tail of a binomial sum near the
+    bound: a log term 20% smaller or 50% larger fails), beta (the
+    derivation's identity), coverage, the Theorem 2 error bound and sample
+    size: pinned (closed forms, brute force, exact tails, Monte Carlo).
+  * the decode step as a whole: its pieces are pinned as above, and its
+    composition by exact special cases and by metamorphic relations between
+    runs (monotone in eps and delta, homogeneous in the values, invariant
+    to a common score shift).  The pages print no worked example, so no
+    external value fixes which level a given head stops at: the readings
+    the certificate rests on (the event budget, the variance proxy, the
+    Bernstein form) are the pages' open choices, listed with the tests.
 """
 from .fp32 import tree_sum_f32, log2_m53_f32
 from .hashing import mix64, group_key, key_hashes, perturb_t

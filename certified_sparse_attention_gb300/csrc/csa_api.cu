@@ -51,12 +51,25 @@ bool params_ok(const csa_params* p) {
 // z with P(|N(0,1)| > z) = delta, i.e. erfc(z / sqrt 2) = delta: bisection
 // on the decreasing function erfc (double precision, 200 halvings).
 float normal_quantile_two_sided(double delta) {
+  // the last delta's quantile is kept: the bisection costs ~10 us of host
+  // time, and a decode loop asks for the same delta at every step
+  static std::mutex mu;
+  static double last_delta = -1.0;
+  static float last_z = 0.f;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (delta == last_delta) return last_z;
+  }
   double lo = 0.0, hi = 40.0;
   for (int i = 0; i < 200; ++i) {
     const double mid = 0.5 * (lo + hi);
     if (std::erfc(mid / std::sqrt(2.0)) > delta) lo = mid; else hi = mid;
   }
-  return (float)(0.5 * (lo + hi));
+  const float z = (float)(0.5 * (lo + hi));
+  std::lock_guard<std::mutex> lock(mu);
+  last_delta = delta;
+  last_z = z;
+  return z;
 }
 
 struct Layout {
@@ -175,9 +188,11 @@ void count_launches(int k) { g_prof.launches += k; }
 // ------------------------------------------------------------ sub-batches
 //
 // A batch of B >= 2 sequences runs by default as two sub-batches of
-// consecutive sequences on two library-owned streams: the step is a chain
-// of ~20 dependent launches, several of them latency-bound, and two
-// independent chains fill the GPU better than one.  Each sub-batch has its
+// consecutive sequences on library-owned streams: the step is a chain of
+// ~20 dependent launches, several of them latency-bound, and independent
+// chains fill the GPU better than one (128K x 4, chains enqueued stage by
+// stage: one chain 814 us, two 686, four 694; each chain also costs ~50 us
+// of host time to enqueue).  Each sub-batch has its
 // own workspace region (stride `stride`); they share sub-batch 0's status
 // word.
 
@@ -189,7 +204,7 @@ struct SubPlan {
 bool sub_plan(const csa_shape* s, const csa_params* p, SubPlan& sp) {
   Layout whole;
   if (!make_layout(s, p, whole)) return false;
-  sp.nsub = p->sub_batches == 0 ? (s->B >= 2 ? 2 : 1) : std::min(p->sub_batches, s->B);
+  sp.nsub = p->sub_batches == 0 ? std::min(s->B, 2) : std::min(p->sub_batches, s->B);
   if (sp.nsub <= 1) {
     sp.nsub = 1; sp.Bc = s->B; sp.stride = whole.total; sp.total = whole.total;
     return true;
@@ -273,52 +288,70 @@ struct SeqSource {
   const float* delta8;
 };
 
-// One (sub-)batch on one stream.  `status` is the device status word (shared
-// by the sub-batches of a split call); `clear` zeroes the per-step counters
-// (a split call clears sub-batch 0's, which hold the status word, before it
-// forks).
-csa_status decode_batch(const csa_shape* shape, const csa_params* params, const void* q, const void* K,
-                        const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
-                        const float* vnorm2, const SeqSource& src, float* o,
-                        float* beta, int32_t* level, int32_t* keys_read, csa_head_stats* stats, char* ws,
-                        unsigned* status, bool clear, cudaStream_t st) {
+// One (sub-)batch on one stream, as a chain of launch stages.  `status` is
+// the device status word (shared by the sub-batches of a split call);
+// `clear` zeroes the per-step counters (a split call clears sub-batch 0's,
+// which hold the status word, before it forks).  A split call enqueues the
+// chains stage by stage (stage k of every chain, then stage k + 1), so every
+// chain starts on the device while the host is still enqueueing the rest.
+struct Chain {
+  csa_shape shape;
+  const csa_params* params;
+  SeqSource src;
   Layout L;
-  if (!make_layout(shape, params, L)) return CSA_ERR_INVALID_ARG;
-  const int G = shape->Hq / shape->Hkv;
-  const bool bf16 = shape->dtype == CSA_BF16;
   SeqArgs seq;
-  std::memset(&seq, 0, sizeof(seq));
+  ScanArgs sa;
+  SparseArgs a;
+  DenseArgs da;
+  int64_t nlive, plive;
+  int G;
+  bool bf16, clear, stats;
+  char* ws;
+  unsigned* status;
+  cudaStream_t st;
+};
+constexpr int kChainStages = 10;
+
+csa_status chain_prepare(Chain& c, const csa_shape* shape, const csa_params* params, const void* q,
+                         const void* K, const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
+                         const float* vnorm2, const SeqSource& src, float* o, float* beta, int32_t* level,
+                         int32_t* keys_read, csa_head_stats* stats, char* ws, unsigned* status, bool clear,
+                         cudaStream_t st) {
+  c.shape = *shape;
+  c.params = params;
+  c.src = src;
+  c.ws = ws;
+  c.status = status;
+  c.clear = clear;
+  c.st = st;
+  c.stats = stats != nullptr;
+  Layout& L = c.L;
+  if (!make_layout(shape, params, L)) return CSA_ERR_INVALID_ARG;
+  c.G = shape->Hq / shape->Hkv;
+  c.bf16 = shape->dtype == CSA_BF16;
+  std::memset(&c.seq, 0, sizeof(c.seq));
   int64_t nlive = 0;
   const SeqArgs* seqd = nullptr;
   if (!src.dev) {
     for (int b = 0; b < shape->B; ++b) {
       const int64_t n = src.len[b];
       if (n < 1 || n > shape->n_max) return CSA_ERR_INVALID_ARG;
-      seq.n[b] = n;
-      seq.seed[b] = src.seed[b];
+      c.seq.n[b] = n;
+      c.seq.seed[b] = src.seed[b];
       const int64_t P = n > kWindow ? n - kWindow : 0;
-      seq.J[b] = params->J_override >= 0 ? params->J_override : grid_J(P, params->r);
+      c.seq.J[b] = params->J_override >= 0 ? params->J_override : grid_J(P, params->r);
       if (n > nlive) nlive = n;
     }
   } else {
     nlive = shape->n_max;
     seqd = (const SeqArgs*)(ws + L.seqd);
   }
-  const int64_t plive = nlive > kWindow ? nlive - kWindow : 0;
+  c.nlive = nlive;
+  c.plive = nlive > kWindow ? nlive - kWindow : 0;
   const float rs = (float)(1.0 / std::sqrt((double)shape->d));
 
-  prof_step_begin(st);
-  if (clear && cudaMemsetAsync(ws, 0, L.zero_end, st) != cudaSuccess) return CSA_ERR_CUDA;
-  if (src.dev) {
-    const ReqPtrs req = {K, V, src.K4w, src.boundsw, src.vmaxw, src.vnorm2w};
-    if (launch_seq_prep(src.len, src.seed, shape->B, shape->n_max, params->r, params->J_override,
-                        (SeqArgs*)(ws + L.seqd), req, status, st) != cudaSuccess)
-      return CSA_ERR_CUDA;
-    count_launches(1);
-  }
-  prof_mark(0, st);
-
-  ScanArgs sa = {};
+  ScanArgs& sa = c.sa;
+  sa = {};
   sa.q = q; sa.K4 = K4; sa.bounds = bounds; sa.ubar = (float*)(ws + L.ubar);
   sa.hw = (float*)(ws + L.hw);
   sa.cmax = (unsigned*)(ws + L.cmax); sa.status = status;
@@ -327,12 +360,9 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
   sa.seqd = seqd;
   sa.requant = src.dev && src.requant;
   sa.dp4a = params->dots == 1;
-  cudaError_t e = launch_scan(sa, seq, shape->B, shape->d, G, bf16, nlive, st);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
-  count_launches(1);
-  prof_mark(1, st);
 
-  SparseArgs a = {};
+  SparseArgs& a = c.a;
+  a = {};
   a.q = q; a.K = K; a.V = V; a.vmax = vmax; a.vnorm2 = vnorm2; a.ubar = (const float*)(ws + L.ubar);
   a.s32 = (float*)(ws + L.s32); a.win = (float*)(ws + L.win); a.cmax = (unsigned*)(ws + L.cmax);
   a.jr_hist = (unsigned*)(ws + L.jr_hist); a.ncand = (unsigned*)(ws + L.ncand);
@@ -361,40 +391,84 @@ csa_status decode_batch(const csa_shape* shape, const csa_params* params, const 
     a.jref = (uint16_t*)(ws + L.jref);
   }
 
-  const int nsm = sm_count();
-  if (plive > 0) {
-    if (launch_cstar(a, seq, shape->d, G, bf16, nlive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
-    prof_mark(2, st);
-    if (launch_candidates(a, seq, G, plive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
-    prof_mark(3, st);
-    count_launches(3);
-  }
-  if (launch_predict(a, seq, shape->d, G, bf16, st) != cudaSuccess) return CSA_ERR_CUDA;
-  count_launches(1);
-  prof_mark(5, st);
-  for (int round = 0; round < 3; ++round) {
-    if (launch_round(a, seq, shape->d, G, bf16, plive > 0 ? plive : 1, round, nsm, st,
-                     g_prof.on ? prof_mark : nullptr) != cudaSuccess)
-      return CSA_ERR_CUDA;
-    count_launches(4);
-  }
   // exact attention for heads with no certified level and sequences without a pool
-  DenseArgs da = {};
+  DenseArgs& da = c.da;
+  da = {};
   da.q = q; da.K = K; da.V = V; da.part = (float*)(ws + L.dpart); da.o = o; da.state = a.state;
   da.nfall = a.nfall;
   da.status = status;
   da.seqd = seqd;
   da.B = shape->B; da.Hq = shape->Hq; da.Hkv = shape->Hkv; da.n_max = shape->n_max;
   da.nsplit = dense_nsplit(shape->n_max); da.rs = rs;
-  if (launch_dense(da, seq, shape->d, G, bf16, nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
-  count_launches(2);
-  prof_mark(10, st);
-  if (stats && plive > 0) {
-    if (launch_near(a, seq, G, plive, st) != cudaSuccess) return CSA_ERR_CUDA;
-    count_launches(1);
-    prof_mark(11, st);
-  }
   return CSA_OK;
+}
+
+csa_status chain_stage(Chain& c, int stage, int nsm) {
+  const csa_params* params = c.params;
+  cudaStream_t st = c.st;
+  const int d = c.shape.d, G = c.G;
+  switch (stage) {
+    case 0:
+      prof_step_begin(st);
+      if (c.clear && cudaMemsetAsync(c.ws, 0, c.L.zero_end, st) != cudaSuccess) return CSA_ERR_CUDA;
+      if (c.src.dev) {
+        const ReqPtrs req = {c.a.K, c.a.V, c.src.K4w, c.src.boundsw, c.src.vmaxw, c.src.vnorm2w};
+        if (launch_seq_prep(c.src.len, c.src.seed, c.shape.B, c.shape.n_max, params->r, params->J_override,
+                            (SeqArgs*)(c.ws + c.L.seqd), req, c.status, st) != cudaSuccess)
+          return CSA_ERR_CUDA;
+        count_launches(1);
+      }
+      prof_mark(0, st);
+      return CSA_OK;
+    case 1:
+      if (launch_scan(c.sa, c.seq, c.shape.B, d, G, c.bf16, c.nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
+      count_launches(1);
+      prof_mark(1, st);
+      return CSA_OK;
+    case 2:
+      if (c.plive > 0) {
+        if (launch_cstar(c.a, c.seq, d, G, c.bf16, c.nlive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
+        count_launches(2);
+        prof_mark(2, st);
+      }
+      return CSA_OK;
+    case 3:
+      if (c.plive > 0) {
+        if (launch_candidates(c.a, c.seq, G, c.plive, nsm, st) != cudaSuccess) return CSA_ERR_CUDA;
+        count_launches(1);
+        prof_mark(3, st);
+      }
+      return CSA_OK;
+    case 4:
+      if (launch_predict(c.a, c.seq, d, G, c.bf16, st) != cudaSuccess) return CSA_ERR_CUDA;
+      count_launches(1);
+      prof_mark(5, st);
+      return CSA_OK;
+    case 5:
+    case 6:
+    case 7: {
+      const int round = stage - 5;
+      if (launch_round(c.a, c.seq, d, G, c.bf16, c.plive > 0 ? c.plive : 1, round, nsm, st,
+                       g_prof.on ? prof_mark : nullptr) != cudaSuccess)
+        return CSA_ERR_CUDA;
+      count_launches(4);
+      return CSA_OK;
+    }
+    case 8:
+      if (launch_dense(c.da, c.seq, d, G, c.bf16, c.nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
+      count_launches(2);
+      prof_mark(10, st);
+      return CSA_OK;
+    case 9:
+      if (c.stats && c.plive > 0) {
+        if (launch_near(c.a, c.seq, G, c.plive, st) != cudaSuccess) return CSA_ERR_CUDA;
+        count_launches(1);
+        prof_mark(11, st);
+      }
+      return CSA_OK;
+    default:
+      return CSA_OK;
+  }
 }
 
 }  // namespace
@@ -607,10 +681,14 @@ csa_status decode_step_impl(const csa_shape* shape, const csa_params* params, co
   cudaStream_t st = (cudaStream_t)stream;
   char* ws = (char*)workspace;
   unsigned* status = (unsigned*)ws;   // offset 0 of (sub-batch 0's) layout
+  const int nsm = sm_count();
   if (sp.nsub == 1 || g_prof.on) {
     // one stream (phase timing runs unsplit so its events bracket whole phases)
-    return decode_batch(shape, params, q, K, V, K4, bounds, vmax, vnorm2, src, o, beta, level, keys_read, stats,
-                        ws, status, true, st);
+    Chain c;
+    csa_status r = chain_prepare(c, shape, params, q, K, V, K4, bounds, vmax, vnorm2, src, o, beta, level,
+                                 keys_read, stats, ws, status, true, st);
+    for (int k = 0; r == CSA_OK && k < kChainStages; ++k) r = chain_stage(c, k, nsm);
+    return r;
   }
   // sub-batches of consecutive sequences on the library's streams: fork
   // after clearing sub-batch 0's counters (they hold the status word), join
@@ -629,6 +707,8 @@ csa_status decode_step_impl(const csa_shape* shape, const csa_params* params, co
   const size_t esz = shape->dtype == CSA_BF16 ? 2 : 4;
   const int64_t nblk = (shape->n_max + kBlock - 1) / kBlock;
   const int64_t Hq = shape->Hq, Hkv = shape->Hkv, D = shape->d, N = shape->n_max;
+  Chain chains[kMaxSub];
+  int nch = 0;
   for (int c = 0; c < sp.nsub; ++c) {
     const int64_t b0 = (int64_t)c * sp.Bc;
     if (b0 >= shape->B) break;
@@ -649,14 +729,23 @@ csa_status decode_step_impl(const csa_shape* shape, const csa_params* params, co
       sc_src.K8 = src.K8 + b0 * Hkv * nblk * kBlock * D;
       sc_src.delta8 = src.delta8 + b0 * Hkv * nblk * D;
     }
-    csa_status r = decode_batch(
-        &sc, params, (const char*)q + b0 * Hq * D * esz, (const char*)K + b0 * Hkv * N * D * esz,
+    csa_status r = chain_prepare(
+        chains[nch], &sc, params, (const char*)q + b0 * Hq * D * esz, (const char*)K + b0 * Hkv * N * D * esz,
         (const char*)V + b0 * Hkv * N * D * esz, K4 + b0 * Hkv * nblk * kBlock * (D / 2),
         bounds + b0 * Hkv * nblk * 2 * D, vmax + b0 * Hkv * nblk, vnorm2 + b0 * Hkv * N, sc_src,
         o + b0 * Hq * D, beta + b0 * Hq, level + b0 * Hq, keys_read + b0 * Hq,
         stats ? stats + b0 * Hq : nullptr, ws + c * sp.stride, status, c > 0, cs);
     if (r != CSA_OK) return r;
-    if (cudaEventRecord(ss->join[c], cs) != cudaSuccess) return CSA_ERR_CUDA;
+    ++nch;
+  }
+  // stage k of every chain, then stage k + 1
+  for (int k = 0; k < kChainStages; ++k)
+    for (int c = 0; c < nch; ++c) {
+      const csa_status r = chain_stage(chains[c], k, nsm);
+      if (r != CSA_OK) return r;
+    }
+  for (int c = 0; c < nch; ++c) {
+    if (cudaEventRecord(ss->join[c], ss->st[c]) != cudaSuccess) return CSA_ERR_CUDA;
     if (cudaStreamWaitEvent(st, ss->join[c], 0) != cudaSuccess) return CSA_ERR_CUDA;
   }
   return CSA_OK;

@@ -18,7 +18,7 @@ constexpr int kBlock = 64;     // quantisation block (tokens)
 constexpr int kWindow = 64;    // window read exactly (last tokens)
 constexpr int kTile = 256;     // keys per scan / candidate tile
 #ifndef CSA_CAND_SEG
-#define CSA_CAND_SEG 4096
+#define CSA_CAND_SEG 2048
 #endif
 constexpr int kCandSeg = CSA_CAND_SEG; // pool keys per candidate-list segment (one candidate CTA)
 constexpr int kMaxB = 128;     // sequences per call

@@ -39,7 +39,7 @@ __device__ __forceinline__ float tree16(const float* v) {
 // in place of the two residual trees (|a_c - alpha at_c| <= alpha (1/2 +
 // 2^-6) for codes this fine); I = 256 I_hi + I_lo from two products.
 template <int D, int G, typename E, bool TWO, bool REQ, bool DP4A = false>
-__global__ void __launch_bounds__(256) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq_arg) {
+__global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq_arg) {
   pdl_entry();
   const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   constexpr int ND = TWO ? 2 : 1;    // query-code digits

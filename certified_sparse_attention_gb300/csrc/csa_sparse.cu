@@ -2283,11 +2283,21 @@ void launch_vgather_t(int nsm, cudaStream_t st, const SparseArgs& a, const SeqAr
     const bool small = nent <= kPlanSmem;
     const int smem = VsLayout<D, G>::smem + (small ? (nent + 1) * 4 : 0);
     cudaFuncSetAttribute(vsum_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vsum_kernel<D, G>, kVsW * 32, smem) !=
-            cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
+    // resident CTAs per SM: a property of the device and the shared memory
+    // size, looked up once per (device, size) (the query costs host time on
+    // every step otherwise)
+    static int occ_dev[64] = {0}, occ_smem[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    int per_sm = occ_smem[dev] == smem ? occ_dev[dev] : 0;
+    if (per_sm < 1) {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vsum_kernel<D, G>, kVsW * 32, smem) !=
+              cudaSuccess ||
+          per_sm < 1)
+        per_sm = 1;
+      occ_dev[dev] = per_sm;
+      occ_smem[dev] = smem;
+    }
     if (!small) {
       launch_pdl(vplan_kernel<true>, dim3(1), dim3(1024), 0, st, a, nent, round);
       add_launches(1);

@@ -233,7 +233,7 @@ def test_decode_llama16k_full_size():
 
 
 def test_decode_step_in_cuda_graph():
-    # the step (two sub-batches: fork and join by events) captured into a
+    # the step (two sub-batches of one sequence: fork and join by events) captured into a
     # CUDA graph and replayed gives what the eager call gives
     import torch
     import certified_sparse_attention_gb300 as csa

@@ -77,7 +77,7 @@ struct Layout {
   int64_t pcap, nblk_max;
   size_t status, cmax, jr_hist, ncand, pre_hist, acc, bcnt, bcons, ccnt, xcnt, nfall, rq, front, jrd, ninset,
       zero_end;
-  size_t jkey, jref, seqd, winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, hw, s32, win, t32, clist, xlist, cmap,
+  size_t jkey, jref, seqd, winstats, vmaxp, state, plan_start, plan_end, plan_off, ubar, hw, tmax, s32, win, t32, clist, xlist, cmap,
       buckets, dpart, pref, total;
   int64_t nchunk_cap;
 };
@@ -118,6 +118,7 @@ bool make_layout(const csa_shape* s, const csa_params* p, Layout& L) {
   L.plan_off = o; o += up(((size_t)BG * L.J1 + 1) * 4);
   L.ubar = o; o += up((size_t)BG * s->n_max * G * 4);
   L.hw = o; o += up((size_t)BG * L.nblk_max * G * 4);
+  L.tmax = o; o += up((size_t)BG * ((s->n_max + kTile - 1) / kTile) * G * 4);
   L.s32 = o; o += up((size_t)BG * L.pcap * G * 4);
   L.win = o; o += up((size_t)BG * kWindow * G * 4);
   L.t32 = o; o += up((size_t)BG * L.pcap * (p->perturb ? G : 1) * 4);
@@ -354,6 +355,7 @@ csa_status chain_prepare(Chain& c, const csa_shape* shape, const csa_params* par
   sa = {};
   sa.q = q; sa.K4 = K4; sa.bounds = bounds; sa.ubar = (float*)(ws + L.ubar);
   sa.hw = (float*)(ws + L.hw);
+  sa.tmax = (float*)(ws + L.tmax);
   sa.cmax = (unsigned*)(ws + L.cmax); sa.status = status;
   sa.Hq = shape->Hq; sa.Hkv = shape->Hkv; sa.n_max = shape->n_max; sa.nblk_max = L.nblk_max; sa.rs = rs;
   sa.two_digit = params->qcode == 1;
@@ -373,7 +375,7 @@ csa_status chain_prepare(Chain& c, const csa_shape* shape, const csa_params* par
   a.nfall = (unsigned*)(ws + L.nfall);
   a.rq = (unsigned*)(ws + L.rq);
   a.pref = (float*)(ws + L.pref);
-  a.hw = (const float*)(ws + L.hw); a.front = (int*)(ws + L.front);
+  a.hw = (const float*)(ws + L.hw); a.tmax = (const float*)(ws + L.tmax); a.front = (int*)(ws + L.front);
   a.xlist = (uint2*)(ws + L.xlist); a.xcnt = (unsigned*)(ws + L.xcnt);
   a.chunk_map = (unsigned*)(ws + L.cmap); a.nchunk_cap = L.nchunk_cap;
   a.plan_start = (unsigned*)(ws + L.plan_start); a.plan_end = (unsigned*)(ws + L.plan_end);

@@ -16,6 +16,7 @@ struct ScanArgs {
   const float* bounds;
   float* ubar;          // [B*Hkv][n_max][G]
   float* hw;            // [B*Hkv][nblk_max][G] half width (ubar - l) / 2 per block
+  float* tmax;          // [B*Hkv][ntile_max][G] largest ubar of each 256-key tile
   unsigned* cmax;       // [B*Hq][4] ordered floats: c_lo, c_hi, cb, c32
   unsigned* status;
   int Hq, Hkv;
@@ -52,6 +53,7 @@ struct SparseArgs {
   const float* vnorm2;    // [B*Hkv][n_max]        ||v_i||^2 per token
   const float* ubar;      // [B*Hkv][n_max][G]
   const float* hw;        // [B*Hkv][nblk_max][G] half width of the score bound per block
+  const float* tmax;      // [B*Hkv][ntile_max][G] largest ubar of each 256-key tile
   float* s32;             // [B*Hkv][pcap][G]     scores (-inf: not a candidate, or not rescored)
   float* win;             // [B*Hkv][64][G]       window scores
   unsigned* cmax;         // [B*Hq][4]            c_lo, c_hi, cb, c32 (ordered)

@@ -15,7 +15,8 @@
 //      m16n8k32: 16 keys x heads x 32 channels, low and high nibbles as
 //      bytes), and ubar = fl(fl(alpha I) + b_hi), l = fl(fl(alpha I) + b_lo);
 //   4. ubar is stored key-major with the G heads interleaved, and the per-head
-//      maxima of l (c*_lo) and ubar are folded into global atomics.
+//      maxima of l (c*_lo) and ubar are folded into global atomics (the
+//      tile's own maximum of ubar is stored per head as well).
 #include "csa_args.cuh"
 
 namespace csa {
@@ -343,6 +344,8 @@ __global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a
     unsigned* slot = a.cmax + ((int64_t)b * a.Hq + (int64_t)g * G + tid) * 4;
     if (x > -INFINITY) atomic_max_f(slot + 0, x);
     if (y > -INFINITY) atomic_max_f(slot + 1, y);
+    // the tile's largest ubar: the exact-max pass skips tiles below c*_lo
+    a.tmax[((int64_t)bg * ((a.n_max + kTile - 1) / kTile) + blockIdx.x) * G + tid] = y;
   }
 }
 

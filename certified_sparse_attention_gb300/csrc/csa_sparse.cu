@@ -45,8 +45,18 @@ namespace csa {
 constexpr int kFlagFallback = 1;
 constexpr int kFlagDone = 2;
 constexpr int kChunk = 1024;   // bucket entries per gather work item
-constexpr int kRingS = 4;      // ring stages per warp
-constexpr int kRingW = 8;      // warps per CTA of the ring kernels
+#ifndef CSA_RING_S
+#define CSA_RING_S 4
+#endif
+#ifndef CSA_RING_W
+#define CSA_RING_W 8
+#endif
+#ifndef CSA_ROWS_CPS
+#define CSA_ROWS_CPS 4
+#endif
+constexpr int kRingS = CSA_RING_S;   // ring stages per warp (8 rows each)
+constexpr int kRingW = CSA_RING_W;   // warps per CTA of the ring kernels
+constexpr int kRowsCps = CSA_ROWS_CPS;   // ring CTAs launched per SM
 
 // ----------------------------------------------------------- small helpers
 
@@ -100,38 +110,62 @@ __device__ __forceinline__ int warp_append(unsigned* counter, bool want) {
 }
 
 
+// phi(y) = e^y - 1 - y from y and expm1(y) (a series near 0, where
+// expm1(y) - y cancels)
+__device__ __forceinline__ float phi_em1(float y, float em1) {
+  if (fabsf(y) < 0.05f) return y * y * (0.5f + y * (1.0f / 6.0f + y * (1.0f / 24.0f + y * (1.0f / 120.0f))));
+  return em1 - y;
+}
+
 // Chernoff interval for a Poisson-binomial count k (two-sided, budget
-// delta_e / 2 per side): mu = k e^y with phi(y) = e^y - 1 - y = Lz / k.
-// Returns k - mu_lo and mu_hi - k (both >= 0).  phi is convex, so Newton's
+// delta_e / 2 per side): mu = k e^y with phi(y) = Lz / k.  Returns
+// k - mu_lo and mu_hi - k (both >= 0).  phi is convex, so Newton's
 // iteration started outside a root (where phi > Lz / k) stays outside and
 // converges to it monotonically: the iterates are outward ends of the
-// root's bracket, as the certificate needs.
-__device__ __forceinline__ float phi_y(float y) {
-  if (fabsf(y) < 0.05f) return y * y * (0.5f + y * (1.0f / 6.0f + y * (1.0f / 24.0f + y * (1.0f / 120.0f))));
-  return expm1f(y) - y;
-}
+// root's bracket, as the certificate needs.  Each step takes one expm1:
+// its value at the new iterate is both that iterate's phi and the next
+// step's slope.
 __device__ void chernoff_gaps(float k, float Lz, float& below, float& above) {
   if (!(k > 0.f)) { below = 0.f; above = Lz; return; }
   const float c0 = Lz / k;
-  // upper root: start where phi >= c0, step down the tangent
-  float hi = fmaxf(1.0f, logf(3.0f * c0 + 3.0f));
-  for (int it = 0; it < 8 && phi_y(hi) < c0; ++it) hi *= 2.0f;
-  for (int it = 0; it < 12; ++it) {
-    const float f = phi_y(hi) - c0;
-    const float nx = hi - f / expm1f(hi);
-    if (!(nx < hi) || phi_y(nx) < c0) break;   // converged (or rounding crossed the root)
-    hi = nx;
+  // upper root: start where phi >= c0, step down the tangent.  phi(y) >=
+  // y^2 / 2 for y >= 0, so sqrt(2 c0) lies at or past the root (within a
+  // few per cent of it for small c0: large counts then converge in one to
+  // three steps instead of about ten)
+  const float s2 = sqrtf(2.0f * c0);
+  float hi = fminf(s2, fmaxf(1.0f, logf(3.0f * c0 + 3.0f)));
+  float eh = expm1f(hi), ph = phi_em1(hi, eh);
+  for (int it = 0; it < 8 && ph < c0; ++it) {
+    hi *= 2.0f;
+    eh = expm1f(hi);
+    ph = phi_em1(hi, eh);
   }
-  above = k * expm1f(hi);
-  // lower root: start at -(c0 + 1) (phi > c0 there), step up the tangent
-  float lo = -(c0 + 1.0f);
   for (int it = 0; it < 12; ++it) {
-    const float f = phi_y(lo) - c0;
-    const float nx = lo - f / expm1f(lo);
-    if (!(nx > lo) || nx >= 0.f || phi_y(nx) < c0) break;
-    lo = nx;
+    const float nx = hi - (ph - c0) / eh;
+    if (!(nx < hi)) break;                        // converged
+    const float en = expm1f(nx), pn = phi_em1(nx, en);
+    if (pn < c0) break;                           // rounding crossed the root
+    hi = nx; eh = en; ph = pn;
   }
-  below = -k * expm1f(lo);
+  above = k * eh;
+  // lower root: start at -(sqrt(2 c0) + c0) when phi >= c0 there (the
+  // root lies near -(sqrt(2 c0) + c0 / 3) for small c0), else at -(c0 + 1)
+  // (phi > c0 always); step up the tangent
+  float lo = -(s2 + c0);
+  float el = expm1f(lo), pl = phi_em1(lo, el);
+  if (!(pl >= c0)) {
+    lo = -(c0 + 1.0f);
+    el = expm1f(lo);
+    pl = phi_em1(lo, el);
+  }
+  for (int it = 0; it < 12; ++it) {
+    const float nx = lo - (pl - c0) / el;
+    if (!(nx > lo) || nx >= 0.f) break;
+    const float en = expm1f(nx), pn = phi_em1(nx, en);
+    if (pn < c0) break;
+    lo = nx; el = en; pl = pn;
+  }
+  below = -k * el;
 }
 
 // Stage eight rows (row indices ent[0..nvalid).x) of a [rows][D] array into
@@ -184,20 +218,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const unsigned (&a
 
 // ------------------------------------------------------- exact-max set
 
-constexpr int kCsetTiles = 16;   // 256-key tiles staged between list flushes
+constexpr int kCsetTiles = 16;   // 256-key tiles per exact-max-set CTA (at most 32)
 
-// A CTA covers `span` keys (a multiple of 256) of one group; grids are
-// sized to the resident CTA count so the pass runs in one wave.
+// A CTA covers `span` keys (kCsetTiles 256-key tiles) of one group.  A
+// pool tile whose largest ubar (per head, from the scan) lies below c*_lo
+// for every head holds no member and is not read; the others are read four
+// tiles at a time.
 template <int G>
 __global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
                                                    int span) {
   pdl_entry();
   const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   // members are staged in shared memory and take one slot range of the
-  // group's list per 16 tiles (a per-warp reservation on the group's
-  // counter serialises)
+  // group's list per CTA (a per-warp reservation on the group's counter
+  // serialises)
   __shared__ uint2 s_list[256 * kCsetTiles];
-  __shared__ unsigned s_n, s_gbase;
+  __shared__ unsigned s_n, s_live;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int64_t n = seq.n[b];
   if (n <= kWindow) return;
@@ -209,9 +245,26 @@ __global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __g
   float clo[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) clo[h] = cmax_get(a, bh0 + h, 0);
-  if (threadIdx.x == 0) s_n = 0u;
+  // tiles that may hold a member: warp 0, lane = tile
+  if (threadIdx.x < 32) {
+    const int64_t kt = k0 + (int64_t)threadIdx.x * kTile;
+    bool live = false;
+    if (threadIdx.x < kCsetTiles && kt < kstop) {
+      if (kt + kTile > P) live = true;                 // window keys are members
+      else {
+        const float* tm = a.tmax + ((int64_t)bg * ((a.n_max + kTile - 1) / kTile) + kt / kTile) * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h) live |= tm[h] >= clo[h];
+      }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, live);
+    if (threadIdx.x == 0) { s_live = m; s_n = 0u; }
+  }
   __syncthreads();
+  const unsigned lm = s_live;
   auto load = [&](int64_t key, float (&u)[G]) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) u[h] = -INFINITY;
     if (key >= P) return;
     const float* ub = a.ubar + ((int64_t)bg * a.n_max + key) * G;
     if (G == 4) {
@@ -222,37 +275,36 @@ __global__ void __launch_bounds__(256) cset_kernel(const SparseArgs a, const __g
       for (int h = 0; h < G; ++h) u[h] = ub[h];
     }
   };
-  float cu[G], nu[G];
+  for (int t0 = 0; t0 < kCsetTiles; t0 += 4) {
+    if (!((lm >> t0) & 0xFu)) continue;
+    float u[4][G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) { cu[h] = nu[h] = -INFINITY; }
-  load(k0 + threadIdx.x, cu);
-  int t = 0;
-  for (int64_t kt = k0; kt < kstop; kt += 256, ++t) {
-    const int64_t key = kt + threadIdx.x;
-    if (kt + 256 < kstop) load(key + 256, nu);
-    unsigned qm = 0;
-    if (key < kstop) {
-      if (key >= P) qm = (1u << G) - 1u;
-      else {
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          if (cu[h] >= clo[h]) qm |= 1u << h;
-      }
+    for (int j = 0; j < 4; ++j) {
+      const int64_t key = k0 + (int64_t)(t0 + j) * kTile + threadIdx.x;
+      if ((lm >> (t0 + j)) & 1u) load(key, u[j]);
     }
 #pragma unroll
-    for (int h = 0; h < G; ++h) cu[h] = nu[h];
-    const int slot = warp_append(&s_n, qm != 0);
-    if (slot >= 0) s_list[slot] = make_uint2((unsigned)key, qm);
-    if ((t + 1) % kCsetTiles == 0 || kt + 256 >= kstop) {
-      __syncthreads();
-      if (threadIdx.x == 0) s_gbase = s_n ? atomicAdd(a.xcnt + bg, s_n) : 0u;
-      __syncthreads();
-      for (unsigned i = threadIdx.x; i < s_n; i += 256) a.xlist[(int64_t)bg * a.n_max + s_gbase + i] = s_list[i];
-      __syncthreads();
-      if (threadIdx.x == 0) s_n = 0u;
-      __syncthreads();
+    for (int j = 0; j < 4; ++j) {
+      if (!((lm >> (t0 + j)) & 1u)) continue;
+      const int64_t key = k0 + (int64_t)(t0 + j) * kTile + threadIdx.x;
+      unsigned qm = 0;
+      if (key < kstop) {
+        if (key >= P) qm = (1u << G) - 1u;
+        else {
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            if (u[j][h] >= clo[h]) qm |= 1u << h;
+        }
+      }
+      const int slot = warp_append(&s_n, qm != 0);
+      if (slot >= 0) s_list[slot] = make_uint2((unsigned)key, qm);
     }
   }
+  __syncthreads();
+  __shared__ unsigned s_gbase;
+  if (threadIdx.x == 0) s_gbase = s_n ? atomicAdd(a.xcnt + bg, s_n) : 0u;
+  __syncthreads();
+  for (unsigned i = threadIdx.x; i < s_n; i += 256) a.xlist[(int64_t)bg * a.n_max + s_gbase + i] = s_list[i];
 }
 
 // ------------------------------------------------------ ring row scoring
@@ -279,7 +331,7 @@ __host__ __device__ constexpr int rows_smem() {
 }
 
 template <int D, int G, typename E, int MODE>
-__global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
+__global__ void __launch_bounds__(kRingW * 32) rows_kernel(const SparseArgs a, const __grid_constant__ SeqArgs seq_arg,
                                                    int round) {
   pdl_entry();
   const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
@@ -333,8 +385,8 @@ __global__ void __launch_bounds__(256) rows_kernel(const SparseArgs a, const __g
   // rows per ring slot and slots per warp (the same shared memory either
   // way): the tensor-core path scores 16 rows per product chain
   constexpr int NB = TC ? 16 : 8;
-  constexpr int NS = TC ? 2 : kRingS;
-  static_assert(NB * NS == 8 * kRingS, "ring size");
+  constexpr int NS = TC ? kRingS / 2 : (kRingS < 4 ? kRingS : 4);
+  static_assert(NB * NS <= 8 * kRingS && NS >= 2 && NS <= 4, "ring size (slot counts are packed 8 bits each)");
   uint8_t* my = ring + w * kRingS * 8 * RB;
   uint2* me = s_ent + w * kRingS * 8;
   uint2* myq = s_q + w * kQueue;
@@ -882,18 +934,18 @@ __global__ void __launch_bounds__(256) cand_kernel(const SparseArgs a, const __g
   int jmin = 255, jmin_out = 0x1FF;   // jmin_out: over the heads not in their exact-max set
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    int jr = -1;
     bool inc = false;
     if (live) {
       const int jb = bound_level(ub[h], c_b[h], t[h], neg_r, J);
       const bool cand = jb <= J;
       inc = ub[h] >= c_lo[h];
       inset |= inc;
-      jr = inc ? 0 : (cand ? jb : J + 1);
       if (cand) { cm |= 1u << h; jmin = min(jmin, jb); }
       if (cand && !inc) jmin_out = min(jmin_out, jb);
+      // first level the row is needed (keys never needed are not counted:
+      // most keys of a peaked group, all on one shared-memory word)
+      if (inc || cand) atomicAdd(&s_jr[h * JS + (inc ? 0 : jb)], 1u);
     }
-    if (jr >= 0) atomicAdd(&s_jr[h * JS + jr], 1u);
     const unsigned cb = __ballot_sync(0xffffffffu, (cm >> h) & 1u);
     if (lane == 0 && cb) atomicAdd(&s_nc[h], (unsigned)__popc(cb));
     if (a.refine8) {
@@ -1081,13 +1133,20 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
     // 763, 722, 716 and 719 us per 128K x 4 step)
     float runk = 0.f, rundb = 0.f;
     int pred = -1;
-    for (int l0 = 0; l0 <= J; l0 += 32) {
-      const int j = l0 + lane;
-      float dk = 0.f, ddb = 0.f;
-      if (j <= J) {
-        const float* ph = a.pre_hist + ((int64_t)bh * a.J1 + j) * 4;
+    // the histogram of a chunk of 32 levels, loaded one chunk ahead
+    auto load_chunk = [&](int l0, float& dk, float& ddb) {
+      dk = 0.f; ddb = 0.f;
+      if (l0 + lane <= J) {
+        const float* ph = a.pre_hist + ((int64_t)bh * a.J1 + l0 + lane) * 4;
         dk = ph[0]; ddb = ph[1];
       }
+    };
+    float nk, ndb;
+    load_chunk(0, nk, ndb);
+    for (int l0 = 0; l0 <= J; l0 += 32) {
+      const int j = l0 + lane;
+      const float dk = nk, ddb = ndb;
+      load_chunk(l0 + 32, nk, ndb);
       // inclusive scan over the 32 lanes
       float k = dk, db = ddb;
 #pragma unroll
@@ -1978,21 +2037,32 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
   __syncthreads();
   for (int l0 = lo + 1; l0 <= hi && found < 0; l0 += LB) {
     const int nl = min(LB, hi - l0 + 1);
-    for (int x = tid; x < ACC; x += 256) {
-      float run = s_run[x];
-      int i = 0;
-      for (; i + 8 <= nl; i += 8) {
-        float v[8];
+    {
+      // running sums over the batch's levels, columns tid and tid + 256:
+      // every load of the batch issued before the first add
+      static_assert(ACC <= 512, "two columns per thread");
+      const int x0 = tid, x1 = tid + 256;
+      const bool h0 = x0 < ACC, h1 = x1 < ACC;
+      float v0[LB], v1[LB];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = accb[(int64_t)(l0 + i + u) * ACC + x];
+      for (int u = 0; u < LB; ++u) {
+        v0[u] = (h0 && u < nl) ? accb[(int64_t)(l0 + u) * ACC + x0] : 0.f;
+        v1[u] = (h1 && u < nl) ? accb[(int64_t)(l0 + u) * ACC + x1] : 0.f;
+      }
+      float r0 = h0 ? s_run[x0] : 0.f, r1 = h1 ? s_run[x1] : 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) { run += v[u]; s_pre[i + u][x] = run; }
+      for (int u = 0; u < LB; ++u) {
+        if (h0 && u < nl) {
+          r0 += v0[u];
+          s_pre[u][x0] = r0;
+          if (h1) {
+            r1 += v1[u];
+            s_pre[u][x1] = r1;
+          }
+        }
       }
-      for (; i < nl; ++i) {
-        run += accb[(int64_t)(l0 + i) * ACC + x];
-        s_pre[i][x] = run;
-      }
-      s_run[x] = run;
+      if (h0) s_run[x0] = r0;
+      if (h1) s_run[x1] = r1;
     }
     __syncthreads();
     // vector parts, one warp per level
@@ -2250,9 +2320,9 @@ void launch_rows_t(int64_t items, int nsm, cudaStream_t st, const SparseArgs& a,
   cudaFuncSetAttribute(rows_kernel<D, G, E, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   // four CTAs per SM over all groups: more, shorter shares than one wave
   // holds balance the uneven density of wanted entries better
-  const int per = per_group(a, 4 * (int64_t)nsm, (items + 8 * kRingW - 1) / (8 * kRingW));
-  launch_pdl(rows_kernel<D, G, E, MODE>, dim3((unsigned)per, (unsigned)(a.B * a.Hkv)), dim3(256), smem, st, a,
-             seq, round);
+  const int per = per_group(a, kRowsCps * (int64_t)nsm, (items + 8 * kRingW - 1) / (8 * kRingW));
+  launch_pdl(rows_kernel<D, G, E, MODE>, dim3((unsigned)per, (unsigned)(a.B * a.Hkv)), dim3(kRingW * 32), smem, st,
+             a, seq, round);
 }
 template <int D, int G, typename E>
 void launch_rows0(int64_t items, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq) {

@@ -310,7 +310,8 @@ csa_status csa_dense_decode_static(const csa_shape* shape, const void* q,
  *            -inf where the key is not a candidate of the head or was not
  *            rescored (without `stats` the other entries are left stale)
  *   jr_hist  uint32 [B][Hq][J+2]        first level at which the key's bf16
- *            row is needed (exact-max set: level 0), J+1 = never
+ *            row is needed (exact-max set: level 0); keys never needed
+ *            (level J+1) are not counted, that entry stays 0
  *   bcnt     uint32 [B][Hkv][J1]        entries appended to each level bucket
  *            over the step's gather rounds (one per key, level and round at
  *            which the key changes a head's sums; each entry is one

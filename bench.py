@@ -626,10 +626,8 @@ def run_ours(args, world, rank, local):
     qh = torch.empty_like(data[0]["q"][0], device="cpu").pin_memory()
     qh.copy_(data[0]["q"][0].cpu())
     qd = torch.empty_like(data[0]["q"][0])
-    oh = torch.empty_like(step.o, device="cpu").pin_memory()
-    bh = torch.empty_like(step.beta, device="cpu").pin_memory()
-    lh = torch.empty_like(step.level, device="cpu").pin_memory()
-    kh = torch.empty_like(step.keys_read, device="cpu").pin_memory()
+    # o, beta, level and keys_read: one buffer, one copy back per step
+    outh = torch.empty_like(step.outputs, device="cpu").pin_memory()
     ne2e = max(1, min(args.steps, 64))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -640,15 +638,12 @@ def run_ours(args, world, rank, local):
                                         w.n - 1, *d["meta"], stream))
         step(qd, d["K"], d["V"], d["meta"], lens, seed_tab[L][s % nseed],
              stream, meta8=d.get("meta8"))
-        oh.copy_(step.o, non_blocking=True)
-        bh.copy_(step.beta, non_blocking=True)
-        lh.copy_(step.level, non_blocking=True)
-        kh.copy_(step.keys_read, non_blocking=True)
+        outh.copy_(step.outputs, non_blocking=True)
         stream.synchronize()
     ms_e2e = (time.perf_counter() - t0) * 1e3 / ne2e
     ms_e2e = max_over_ranks(ms_e2e, world, device)
     h2d = qh.numel() * qh.element_size()
-    d2h = sum(t.numel() * t.element_size() for t in (oh, bh, lh, kh))
+    d2h = outh.numel() * outh.element_size()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -410,11 +410,17 @@ class DecodeStep:
         self.ws_bytes = nbytes
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
         B, Hq, d = shape.B, shape.Hq, shape.d
-        self.o = torch.empty((B, Hq, d), dtype=torch.float32, device=device)
-        self.beta = torch.empty((B, Hq), dtype=torch.float32, device=device)
-        self.level = torch.empty((B, Hq), dtype=torch.int32, device=device)
-        self.keys_read = torch.empty((B, Hq), dtype=torch.int32,
-                                     device=device)
+        # the four outputs are views of one buffer (``outputs``), so that a
+        # caller reads a step's results back with a single copy
+        nh = B * Hq
+        self.outputs = torch.empty((nh * (d + 3),), dtype=torch.float32,
+                                   device=device)
+        self.o = self.outputs[:nh * d].view(B, Hq, d)
+        self.beta = self.outputs[nh * d:nh * (d + 1)].view(B, Hq)
+        self.level = self.outputs[nh * (d + 1):nh * (d + 2)].view(
+            torch.int32).view(B, Hq)
+        self.keys_read = self.outputs[nh * (d + 2):].view(
+            torch.int32).view(B, Hq)
         self.stats = (torch.zeros((B, Hq, STATS_FIELDS), dtype=torch.int32,
                                   device=device) if with_stats else None)
 

@@ -49,10 +49,10 @@ constexpr int kChunk = 1024;   // bucket entries per gather work item
 #define CSA_RING_S 4
 #endif
 #ifndef CSA_RING_W
-#define CSA_RING_W 8
+#define CSA_RING_W 4
 #endif
 #ifndef CSA_ROWS_CPS
-#define CSA_ROWS_CPS 4
+#define CSA_ROWS_CPS 12
 #endif
 constexpr int kRingS = CSA_RING_S;   // ring stages per warp (8 rows each)
 constexpr int kRingW = CSA_RING_W;   // warps per CTA of the ring kernels
@@ -1425,10 +1425,13 @@ __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nen
 
 // ------------------------------------------------------------- V gather
 
+constexpr int kVgW = 8;   // warps per CTA of the float32 value gather (256 threads)
+constexpr int kVgS = 4;   // its ring stages per warp (8 rows each)
+
 template <int D, int G, typename E>
 constexpr int vgather_smem() {
-  return kRingW * kRingS * 8 * D * (int)sizeof(E) + kRingW * kRingS * 8 * 16 + G * (2 * D + 8) * 4 +
-         kRingW * (kChunk / kRingW) * 8 + kRingW * kRingS * 8 * G * 4;
+  return kVgW * kVgS * 8 * D * (int)sizeof(E) + kVgW * kVgS * 8 * 16 + G * (2 * D + 8) * 4 +
+         kVgW * (kChunk / kVgW) * 8 + kVgW * kVgS * 8 * G * 4;
 }
 
 template <int D, int G, typename E>
@@ -1439,20 +1442,20 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
   constexpr int CPL = D / 32;
   constexpr int ACC = 2 * D + 8;
   constexpr int RB = D * (int)sizeof(E);
-  constexpr int EPW = kChunk / kRingW;          // events per warp per work item
+  constexpr int EPW = kChunk / kVgW;          // events per warp per work item
   extern __shared__ __align__(16) uint8_t dsm[];
   uint8_t* ring = dsm;
-  float* s_sc = reinterpret_cast<float*>(dsm + kRingW * kRingS * 8 * RB);            // [W][S][8][4]
-  float (*s_acc)[ACC] = reinterpret_cast<float (*)[ACC]>(dsm + kRingW * kRingS * 8 * RB + kRingW * kRingS * 8 * 16);
-  uint2* s_ev = reinterpret_cast<uint2*>(dsm + kRingW * kRingS * 8 * RB + kRingW * kRingS * 8 * 16 + G * ACC * 4);
-  float* s_ww = reinterpret_cast<float*>(dsm + kRingW * kRingS * 8 * RB + kRingW * kRingS * 8 * 16 + G * ACC * 4 +
-                                         kRingW * EPW * 8);                       // [W][S][8][G]
+  float* s_sc = reinterpret_cast<float*>(dsm + kVgW * kVgS * 8 * RB);            // [W][S][8][4]
+  float (*s_acc)[ACC] = reinterpret_cast<float (*)[ACC]>(dsm + kVgW * kVgS * 8 * RB + kVgW * kVgS * 8 * 16);
+  uint2* s_ev = reinterpret_cast<uint2*>(dsm + kVgW * kVgS * 8 * RB + kVgW * kVgS * 8 * 16 + G * ACC * 4);
+  float* s_ww = reinterpret_cast<float*>(dsm + kVgW * kVgS * 8 * RB + kVgW * kVgS * 8 * 16 + G * ACC * 4 +
+                                         kVgW * EPW * 8);                       // [W][S][8][G]
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const unsigned total = a.plan_off[nent];
-  uint8_t* my = ring + w * kRingS * 8 * RB;
-  float* msc = s_sc + w * kRingS * 8 * 4;
+  uint8_t* my = ring + w * kVgS * 8 * RB;
+  float* msc = s_sc + w * kVgS * 8 * 4;
   uint2* mev = s_ev + w * EPW;
-  float* mww = s_ww + w * kRingS * 8 * G;
+  float* mww = s_ww + w * kVgS * 8 * G;
   for (unsigned c = blockIdx.x; c < total; c += gridDim.x) {
     const int e = (int)a.chunk_map[c];
     const int bg = e / a.J1, l = e - bg * a.J1;
@@ -1464,12 +1467,12 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
     // work item (balanced over the warps), loaded in one sweep
     const int nev = (int)(ev1 - ev0);
     const int nball = (nev + 7) / 8;
-    const int nmy = nball > w ? (nball - w + kRingW - 1) / kRingW : 0;   // batches of this warp
+    const int nmy = nball > w ? (nball - w + kVgW - 1) / kVgW : 0;   // batches of this warp
     const uint2* bk = a.buckets + (int64_t)e * a.pcap + ev0;
 #pragma unroll
     for (int i = lane; i < EPW; i += 32) {
       const int k = i >> 3, r = i & 7;
-      const int idx = (w + k * kRingW) * 8 + r;
+      const int idx = (w + k * kVgW) * 8 + r;
       mev[i] = (k < nmy && idx < nev) ? bk[idx] : make_uint2(0u, 0u);
     }
     float c32[G];
@@ -1490,7 +1493,7 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
     const float* sb = a.s32 + (int64_t)bg * a.pcap * G;
     const int nbatch = nmy;
     // events in the warp's k-th batch
-    auto bcount = [&](int k) { return k < nmy ? min(8, nev - (w + k * kRingW) * 8) : 0; };
+    auto bcount = [&](int k) { return k < nmy ? min(8, nev - (w + k * kVgW) * 8) : 0; };
     auto issue = [&](int slot, int bt) {
       const int nv = bcount(bt);
       stage8<D, E>(my + slot * 8 * RB, Vb, mev + bt * 8, nv);
@@ -1503,10 +1506,10 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
       cp_async_commit();
     };
 #pragma unroll
-    for (int sl = 0; sl < kRingS; ++sl) issue(sl, sl);
+    for (int sl = 0; sl < kVgS; ++sl) issue(sl, sl);
     for (int bt = 0; bt < nbatch; ++bt) {
-      const int slot = bt & (kRingS - 1);
-      cp_async_wait<kRingS - 1>();
+      const int slot = bt & (kVgS - 1);
+      cp_async_wait<kVgS - 1>();
       __syncwarp();
       const int nv = bcount(bt);
       // transition weights, one lane per event
@@ -1560,7 +1563,7 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
         }
       }
       __syncwarp();
-      issue(slot, bt + kRingS);
+      issue(slot, bt + kVgS);
     }
     cp_async_wait<0>();
 #pragma unroll
@@ -2318,8 +2321,11 @@ template <int D, int G, typename E, int MODE>
 void launch_rows_t(int64_t items, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int round) {
   constexpr int smem = rows_smem<D, G, E>();
   cudaFuncSetAttribute(rows_kernel<D, G, E, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  // four CTAs per SM over all groups: more, shorter shares than one wave
-  // holds balance the uneven density of wanted entries better
+  // kRowsCps (12) CTAs of 4 warps per SM over all groups, several waves:
+  // many short shares balance the uneven density of wanted entries (and
+  // keep more rows in flight) better than one long share per resident warp
+  // (rescoring 168 us per 128K x 4 step against 199 us with 4 CTAs of 8
+  // warps per SM)
   const int per = per_group(a, kRowsCps * (int64_t)nsm, (items + 8 * kRingW - 1) / (8 * kRingW));
   launch_pdl(rows_kernel<D, G, E, MODE>, dim3((unsigned)per, (unsigned)(a.B * a.Hkv)), dim3(kRingW * 32), smem, st,
              a, seq, round);

@@ -45,6 +45,16 @@ namespace csa {
 constexpr int kFlagFallback = 1;
 constexpr int kFlagDone = 2;
 constexpr int kChunk = 1024;   // bucket entries per gather work item
+// Work units a non-empty bucket costs beyond its entries (its partial batch
+// and the flush of its sums): the warps' shares are equal in entries plus
+// this per bucket, so a warp whose range crosses many small buckets (the
+// deep levels of peaked heads) does not become the launch's straggler.
+// (128 x 4 step, value sums of the unsplit chain: 153 us with no bucket
+// cost, 132 us with 32 to 128; the split step 674 -> 662 us at 128.)
+#ifndef CSA_VS_BUCKET_COST
+#define CSA_VS_BUCKET_COST 128
+#endif
+constexpr unsigned kVsBucketCost = CSA_VS_BUCKET_COST;
 #ifndef CSA_RING_S
 #define CSA_RING_S 4
 #endif
@@ -1208,7 +1218,10 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
 
 // --------------------------------------------------------- level buckets
 
-constexpr int kLevItem = 2048;   // keys per work item of the level pass (first round)
+#ifndef CSA_LEV_ITEM
+#define CSA_LEV_ITEM 2048
+#endif
+constexpr int kLevItem = CSA_LEV_ITEM;   // keys per work item of the level pass (first round)
 constexpr int kLevItemLate = 512; // later rounds: few groups, more and shorter items
 
 // One work item: keys [k0, k0 + isz) of group bg.
@@ -1360,9 +1373,10 @@ __global__ void __launch_bounds__(256) levels_kernel(const SparseArgs a, const _
 
 // One CTA: the bucket entries appended in this round, as per-bucket ranges
 // [plan_start, plan_end) and their exclusive prefix plan_off over the
-// buckets.  EV: the prefix counts entries (the tensor-core gather cuts
-// it into per-warp ranges); otherwise it counts work items of kChunk
-// entries and chunk_map maps each item to its bucket.
+// buckets.  EV: the prefix counts work units, the entries plus
+// kVsBucketCost per non-empty bucket (the tensor-core gather cuts it into
+// equal per-warp ranges); otherwise it counts work items of kChunk entries
+// and chunk_map maps each item to its bucket.
 template <bool EV>
 __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nent, int round) {
   pdl_entry();
@@ -1381,7 +1395,7 @@ __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nen
     a.plan_start[i] = st;
     a.plan_end[i] = en;
     a.bcons[i] += en;
-    sum += EV ? en - st : (en - st + kChunk - 1) / kChunk;
+    sum += EV ? en - st + (en > st ? kVsBucketCost : 0u) : (en - st + kChunk - 1) / kChunk;
   }
   // exclusive prefix of the per-thread sums: a shuffle scan within each
   // warp, then one over the 32 warp totals
@@ -1409,7 +1423,8 @@ __global__ void __launch_bounds__(1024) vplan_kernel(const SparseArgs a, int nen
   for (int i = i0; i < i1; ++i) {
     a.plan_off[i] = run;
     if (EV) {
-      run += a.plan_end[i] - a.plan_start[i];
+      const unsigned ne = a.plan_end[i] - a.plan_start[i];
+      run += ne + (ne ? kVsBucketCost : 0u);
     } else {
       const unsigned nch = (a.plan_end[i] - a.plan_start[i] + kChunk - 1) / kChunk;
       for (unsigned k = 0; k < nch; ++k)
@@ -1663,17 +1678,18 @@ __device__ __forceinline__ void red_add2(float* p, float x, float y) {
   if (x != 0.f || y != 0.f) atomicAdd(reinterpret_cast<float2*>(p), make_float2(x, y));
 }
 
-// Batch generator over a warp's range [pos, end) of the concatenated new
-// bucket entries (warp-uniform state).
+// Batch generator over a warp's range [pos, end) of the concatenated work
+// units (per non-empty bucket: kVsBucketCost units, then one per new entry;
+// warp-uniform state).
 struct VsGen {
   int e, bg;          // current bucket and its (sequence, KV head)
-  unsigned pos, end;  // next entry, end of range (concatenated numbering)
-  unsigned off0, off1;  // concatenated offsets of bucket e and e + 1
+  unsigned pos, end;  // next unit, end of range
+  unsigned off0, off1;  // first units of bucket e and e + 1
   unsigned start;     // bucket-local index of the bucket's first new entry
 };
 
-// Smallest bucket e' >= e0 whose new entries hold concatenated position x
-// (plan_off non-decreasing, plan_off[nent] > x), with its offsets.
+// Smallest bucket e' >= e0 whose units hold position x (plan_off
+// non-decreasing, plan_off[nent] > x), with its offsets.
 // (poff: the exclusive prefix of the round's entries per bucket, in shared
 // memory or in the workspace; every bucket's new entries start at 0)
 __device__ __forceinline__ void vs_seek(const SparseArgs& a, const unsigned* poff, int nent, int e0, unsigned x,
@@ -1719,9 +1735,9 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
   uint8_t* s_at = base + Lt::at;
   uint8_t* s_bx = base + Lt::bx;
 
-  // the round's entries per bucket and their exclusive prefix over the
-  // buckets: computed here by every CTA (small plans) or read from
-  // vplan_kernel's (large ones)
+  // the round's work units per bucket (entries plus kVsBucketCost when
+  // non-empty) and their exclusive prefix over the buckets: computed here
+  // by every CTA (small plans) or read from vplan_kernel's (large ones)
   const unsigned* poff = a.plan_off;
   if (nent <= kPlanSmem) {
     unsigned* s_plan = reinterpret_cast<unsigned*>(dsm + kVsW * Lt::per_warp);
@@ -1734,7 +1750,7 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
     for (int i = i0; i < i1; ++i) {
       const unsigned en = min(cnt[i], (unsigned)a.pcap);
       if (blockIdx.x == 0) a.bcons[i] += en;
-      sum += en;
+      sum += en + (en ? kVsBucketCost : 0u);
     }
     unsigned inc = sum;
 #pragma unroll
@@ -1753,7 +1769,8 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
     unsigned run = wbase + inc - sum;
     for (int i = i0; i < i1; ++i) {
       s_plan[i] = run;
-      run += min(cnt[i], (unsigned)a.pcap);
+      const unsigned en = min(cnt[i], (unsigned)a.pcap);
+      run += en + (en ? kVsBucketCost : 0u);
     }
     if (t == 0) s_plan[nent] = tot;
     __syncthreads();
@@ -1787,11 +1804,16 @@ __global__ void __launch_bounds__(kVsW * 32) vsum_kernel(const SparseArgs a, int
     unsigned eoff = 0;
     if (gen.pos < gen.end) {
       if (gen.pos >= gen.off1) vs_seek(a, poff, nent, gen.e + 1, gen.pos, gen);
-      e = gen.e;
-      bg = gen.bg;
-      cnt = (int)min(min(gen.off1, gen.end) - gen.pos, (unsigned)kVsB);
-      eoff = gen.start + (gen.pos - gen.off0);
-      gen.pos += cnt;
+      // a bucket's first kVsBucketCost units hold no entries
+      const unsigned ent0 = gen.off0 + kVsBucketCost;
+      if (gen.pos < ent0) gen.pos = ent0;
+      if (gen.pos < gen.end) {
+        e = gen.e;
+        bg = gen.bg;
+        cnt = (int)min(min(gen.off1, gen.end) - gen.pos, (unsigned)kVsB);
+        eoff = gen.start + (gen.pos - ent0);
+        gen.pos += cnt;
+      }
     }
     if (lane == 0) { dp[0] = e; dp[1] = (int)eoff; dp[2] = cnt; dp[3] = bg; }
     if (cnt > 0) {

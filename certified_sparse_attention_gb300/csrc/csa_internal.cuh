@@ -18,9 +18,13 @@ constexpr int kBlock = 64;     // quantisation block (tokens)
 constexpr int kWindow = 64;    // window read exactly (last tokens)
 constexpr int kTile = 256;     // keys per scan / candidate tile
 #ifndef CSA_CAND_SEG
-#define CSA_CAND_SEG 2048
+#define CSA_CAND_SEG 3072
 #endif
-constexpr int kCandSeg = CSA_CAND_SEG; // pool keys per candidate-list segment (one candidate CTA)
+// pool keys per candidate-list segment (one candidate CTA).  On the 128K x 4
+// step with two sub-batch chains: 2048, 2560, 3072, 3584 and 4096 keys gave
+// 655, 645, 640, 648 and 658 us (the unsplit candidate pass alone is
+// fastest at 2048: 102 against 109 us).
+constexpr int kCandSeg = CSA_CAND_SEG;
 constexpr int kMaxB = 128;     // sequences per call
 constexpr int kMaxHeads = 1024; // query heads and KV heads per call
 constexpr int kMaxJ = 255;     // last grid level supported

@@ -233,7 +233,11 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const unsigned (&a
 
 // ------------------------------------------------------- exact-max set
 
-constexpr int kCsetTiles = 16;   // 256-key tiles per exact-max-set CTA (at most 32)
+#ifndef CSA_CSET_TILES
+#define CSA_CSET_TILES 16
+#endif
+constexpr int kCsetTiles = CSA_CSET_TILES;   // 256-key tiles per exact-max-set CTA (at most 16: static list)
+static_assert(kCsetTiles % 4 == 0 && kCsetTiles <= 16, "tiles are read four at a time; the list is static");
 
 // A CTA covers `span` keys (kCsetTiles 256-key tiles) of one group.  A
 // pool tile whose largest ubar (per head, from the scan) lies below c*_lo
@@ -1228,6 +1232,10 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
 #endif
 constexpr int kLevItem = CSA_LEV_ITEM;   // keys per work item of the level pass (first round)
 constexpr int kLevItemLate = 512; // later rounds: few groups, more and shorter items
+#ifndef CSA_LEV_CPS
+#define CSA_LEV_CPS 8
+#endif
+constexpr int kLevCps = CSA_LEV_CPS;   // level-pass CTAs launched per SM (at most)
 
 // One work item: keys [k0, k0 + isz) of group bg.
 template <int G, bool PH>
@@ -2476,11 +2484,11 @@ cudaError_t launch_round(const SparseArgs& a, const SeqArgs& seq, int d, int G, 
     add_launches(1);
     if (mark) mark(12, st);
   }
-  // eight 256-thread CTAs per SM pull work items (isz keys of a group
+  // kLevCps 256-thread CTAs per SM pull work items (isz keys of a group
   // listed for this round) from the round's queue
   const int isz = round == 0 ? kLevItem : kLevItemLate;
   const unsigned tpg = (unsigned)((pmax_live + isz - 1) / isz);
-  int64_t nct = 8 * (int64_t)nsm;
+  int64_t nct = kLevCps * (int64_t)nsm;
   const int64_t items = (int64_t)tpg * a.B * a.Hkv;
   if (nct > items) nct = items;
   if (nct < 1) nct = 1;

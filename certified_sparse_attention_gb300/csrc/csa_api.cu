@@ -307,11 +307,17 @@ struct Chain {
   int64_t nlive, plive;
   int G;
   bool bf16, clear, stats;
+  bool tm_ok;             // tm_codes holds a tensor map of the code rows
+  CUtensorMap tm_codes;
   char* ws;
   unsigned* status;
   cudaStream_t st;
 };
 constexpr int kChainStages = 10;
+#ifndef CSA_SCAN_TMA
+#define CSA_SCAN_TMA 1
+#endif
+constexpr bool kScanTma = CSA_SCAN_TMA != 0;   // bulk tensor staging of the scan's code tiles
 
 csa_status chain_prepare(Chain& c, const csa_shape* shape, const csa_params* params, const void* q,
                          const void* K, const void* V, const uint8_t* K4, const float* bounds, const float* vmax,
@@ -362,6 +368,13 @@ csa_status chain_prepare(Chain& c, const csa_shape* shape, const csa_params* par
   sa.seqd = seqd;
   sa.requant = src.dev && src.requant;
   sa.dp4a = params->dots == 1;
+  // the plain d = 128 scan stages its code tile with one bulk tensor copy
+  // (64-byte rows, 256-row boxes; the row index must fit in int32)
+  {
+    const uint64_t crows = (uint64_t)shape->B * shape->Hkv * L.nblk_max * kBlock;
+    c.tm_ok = kScanTma && shape->d == 128 && !sa.requant && !sa.two_digit && !sa.dp4a && crows < (1ull << 31) &&
+              make_tmap_2d_u8_sw64(&c.tm_codes, K4, 64, crows, 64, 64, kTile);
+  }
 
   SparseArgs& a = c.a;
   a = {};
@@ -423,7 +436,9 @@ csa_status chain_stage(Chain& c, int stage, int nsm) {
       prof_mark(0, st);
       return CSA_OK;
     case 1:
-      if (launch_scan(c.sa, c.seq, c.shape.B, d, G, c.bf16, c.nlive, st) != cudaSuccess) return CSA_ERR_CUDA;
+      if (launch_scan(c.sa, c.seq, c.shape.B, d, G, c.bf16, c.nlive, c.tm_ok ? &c.tm_codes : nullptr, st) !=
+          cudaSuccess)
+        return CSA_ERR_CUDA;
       count_launches(1);
       prof_mark(1, st);
       return CSA_OK;
@@ -477,8 +492,9 @@ csa_status chain_stage(Chain& c, int stage, int nsm) {
 
 void add_launches(int k) { count_launches(k); }
 
-bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
-                       uint32_t box_inner, uint32_t box_rows) {
+namespace {
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, CUtensorMapSwizzle sw, const void* base, uint64_t inner,
+                  uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows) {
   typedef CUresult (*Encode)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -497,9 +513,21 @@ bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint6
   const cuuint64_t strides[1] = {pitch_bytes};
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                       uint32_t box_inner, uint32_t box_rows) {
+  return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, base, inner, rows,
+                      pitch_bytes, box_inner, box_rows);
+}
+
+bool make_tmap_2d_u8_sw64(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                          uint32_t box_inner, uint32_t box_rows) {
+  return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_64B, base, inner, rows, pitch_bytes,
+                      box_inner, box_rows);
 }
 
 bool current_context_id(unsigned long long* id) {

@@ -143,8 +143,11 @@ struct QuantArgs {
   int64_t blk_from;
 };
 
+// tm_codes: a tensor map over the 4-bit code rows (make_tmap_2d_u8_sw64,
+// box 64 bytes x 256 rows) for the plain d = 128 scan, or null (16-byte
+// cp.async staging)
 cudaError_t launch_scan(const ScanArgs&, const SeqArgs&, int B, int d, int G, bool bf16, int64_t nmax_live,
-                        cudaStream_t);
+                        const CUtensorMap* tm_codes, cudaStream_t);
 cudaError_t launch_cstar(const SparseArgs&, const SeqArgs&, int d, int G, bool bf16, int64_t nmax_live,
                          int nsm, cudaStream_t);
 cudaError_t launch_candidates(const SparseArgs&, const SeqArgs&, int G, int64_t pmax_live, int nsm, cudaStream_t);
@@ -196,5 +199,10 @@ bool current_context_id(unsigned long long* id);
 // (base or pitch not 16-byte aligned, sizes out of range).
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
                        uint32_t box_inner, uint32_t box_rows);
+// The same over `rows` rows of `inner` bytes (8-bit elements), 64-byte
+// swizzle (the 16-byte chunk c of tile row r lands at chunk c ^ ((r / 2) % 4)
+// of a 512-byte-aligned buffer).
+bool make_tmap_2d_u8_sw64(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                          uint32_t box_inner, uint32_t box_rows);
 
 }  // namespace csa

@@ -6,7 +6,8 @@
 // the whole GQA group.  One CTA scans a tile of 256 keys (four 64-token
 // blocks) of one (sequence, KV head) for all G query heads:
 //   1. the packed codes (256 x d/2 bytes) and the four blocks' (m_c, Delta_c)
-//      are staged in shared memory with cp.async;
+//      are staged in shared memory: the codes (d = 128) by one bulk tensor
+//      copy completing on an mbarrier, the bounds with cp.async;
 //   2. per (block, head) the query is coded to int8 with a residual and a
 //      key-rounding slack (16 threads per (block, head), adjacent-pair float32
 //      trees over the channels);
@@ -39,8 +40,13 @@ __device__ __forceinline__ float tree16(const float* v) {
 // and the closed-form residual term fl(fl(15 d) * fl(alpha * (1/2 + 2^-6)))
 // in place of the two residual trees (|a_c - alpha at_c| <= alpha (1/2 +
 // 2^-6) for codes this fine); I = 256 I_hi + I_lo from two products.
-template <int D, int G, typename E, bool TWO, bool REQ, bool DP4A = false>
-__global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq_arg) {
+// TMA: the code tile arrives by one bulk tensor copy (64-byte swizzle,
+// completing on an mbarrier) instead of 16-byte cp.async (plain d = 128
+// scan only).
+template <int D, int G, typename E, bool TWO, bool REQ, bool DP4A = false, bool TMA = false>
+__global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a, const __grid_constant__ SeqArgs seq_arg,
+                                                                const __grid_constant__ CUtensorMap tm_codes) {
+  static_assert(!TMA || (D == 128 && !TWO && !REQ && !DP4A), "bulk tensor staging: plain d = 128 scan");
   pdl_entry();
   const SeqArgs& seq = a.seqd ? *a.seqd : seq_arg;
   constexpr int ND = TWO ? 2 : 1;    // query-code digits
@@ -49,7 +55,8 @@ __global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a
   constexpr int ROWB = D / 2;        // bytes of codes per key
   constexpr int CHR = ROWB / 16;     // 16-byte chunks per key
   constexpr int WE = D / 8;          // even (and odd) code words per key
-  __shared__ __align__(16) uint8_t s_codes[kTile * ROWB];
+  __shared__ __align__(1024) uint8_t s_codes[kTile * ROWB];
+  __shared__ __align__(8) unsigned long long s_bar;   // the code tile's copy (TMA)
   __shared__ __align__(16) float s_bnd[4][2][D];
   __shared__ __align__(16) float s_qt[G][D];
   __shared__ __align__(16) unsigned s_atw[ND][4][G][2 * WE];   // [digit]: lo, hi
@@ -78,7 +85,15 @@ __global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a
   }
 
   // 1. stage the block bounds (first group: the query prep needs them) and
-  // the codes (second group: the dot products need them)
+  // the codes (second group, or the bulk tensor copy: the dot products need
+  // them)
+  // (the copy's swizzle pattern follows shared-memory address bits: the tile
+  // must start on a 1024-byte boundary, else the cp.async staging is taken)
+  const bool tma = TMA && (smem_u32(s_codes) & 1023u) == 0u;
+  if (tma && tid == 0) {
+    mbar_init(smem_u32(&s_bar), 1);
+    fence_barrier_init();
+  }
   {
     const int64_t blk0 = key0 / kBlock;
     const float* bsrc = a.bounds + ((int64_t)bg * a.nblk_max + blk0) * 2 * D;
@@ -88,18 +103,29 @@ __global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a
       cp_async16(reinterpret_cast<float*>(s_bnd) + c * 4, ok ? bsrc + (int64_t)c * 4 : a.bounds, ok);
     }
     cp_async_commit();
-    const uint8_t* src = a.K4 + ((int64_t)bg * a.nblk_max * kBlock + key0) * ROWB;
-    const int64_t rows_valid = nblk_n * kBlock - key0;
+    if (tma) {
+      // rows past the group's last block hold other codes (or zeros past
+      // the array); they belong to keys >= n, whose bounds are never kept
+      __syncthreads();   // the barrier is initialised before anyone waits on it
+      if (tid == 0) {
+        mbar_expect_tx(smem_u32(&s_bar), (unsigned)(kTile * ROWB));
+        tma_load_2d(smem_u32(s_codes), &tm_codes, 0, (int)((int64_t)bg * a.nblk_max * kBlock + key0),
+                    smem_u32(&s_bar));
+      }
+    } else {
+      const uint8_t* src = a.K4 + ((int64_t)bg * a.nblk_max * kBlock + key0) * ROWB;
+      const int64_t rows_valid = nblk_n * kBlock - key0;
 #pragma unroll
-    for (int c = tid; c < kTile * CHR; c += 256) {
-      const int row = c / CHR, part = c - row * CHR;
-      bool ok = row < rows_valid;
-      // chunk `part` of a row at chunk part ^ (row % CHR): the fragment
-      // loads of eight rows then spread over the banks
-      cp_async16(s_codes + row * ROWB + ((part ^ (row & (CHR - 1))) << 4),
-                 ok ? src + (int64_t)c * 16 : a.K4, ok);
+      for (int c = tid; c < kTile * CHR; c += 256) {
+        const int row = c / CHR, part = c - row * CHR;
+        bool ok = row < rows_valid;
+        // chunk `part` of a row at chunk part ^ (row % CHR): the fragment
+        // loads of eight rows then spread over the banks
+        cp_async16(s_codes + row * ROWB + ((part ^ (row & (CHR - 1))) << 4),
+                   ok ? src + (int64_t)c * 16 : a.K4, ok);
+      }
+      cp_async_commit();
     }
-    cp_async_commit();
   }
   // query (scaled by 1/sqrt d) for the group's G heads
   {
@@ -126,7 +152,8 @@ __global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a
       if (lane == 0) s_q1[w] = s;
     }
   }
-  cp_async_wait<1>();            // the bounds group has landed
+  if (tma) cp_async_wait<0>();   // the bounds group has landed
+  else cp_async_wait<1>();
   __syncthreads();
 
   // 2. per (block, head) query code
@@ -225,8 +252,19 @@ __global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a
       }
     }
   }
-  cp_async_wait<0>();            // the codes too
-  __syncthreads();
+  if (tma) {
+    // the codes too (bounded wait; on a timeout the CTA records it, waits
+    // once more for its copy and leaves)
+    const bool ok = mbar_wait(smem_u32(&s_bar), 0);
+    if (!__syncthreads_and(ok)) {
+      if (tid == 0) atomicOr(a.status, 4u);
+      mbar_wait(smem_u32(&s_bar), 0);
+      return;
+    }
+  } else {
+    cp_async_wait<0>();          // the codes too
+    __syncthreads();
+  }
 
   // 3. bounds per key.  The exact integer dot products I = sum_c qcode_c *
   // code_c come from u8 x s8 m16n8k32 tensor-core products: a warp takes its
@@ -257,8 +295,12 @@ __global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a
 #pragma unroll
     for (int ks = 0; ks < (DP4A ? 0 : KS); ++ks) {
       // word 4ks+tq of rows r0, r1: chunk ks, word tq (swizzled chunks)
-      const unsigned w0 = *reinterpret_cast<const unsigned*>(s_codes + r0 * ROWB + ((ks ^ (r0 & (CHR - 1))) << 4) + 4 * tq);
-      const unsigned w1 = *reinterpret_cast<const unsigned*>(s_codes + r1 * ROWB + ((ks ^ (r1 & (CHR - 1))) << 4) + 4 * tq);
+      // (the bulk tensor copy's 64-byte swizzle puts chunk c of row r at
+      // c ^ ((r / 2) % 4); the cp.async staging at c ^ (r % CHR))
+      const int s0 = tma ? ((r0 >> 1) & 3) : (r0 & (CHR - 1));
+      const int s1 = tma ? ((r1 >> 1) & 3) : (r1 & (CHR - 1));
+      const unsigned w0 = *reinterpret_cast<const unsigned*>(s_codes + r0 * ROWB + ((ks ^ s0) << 4) + 4 * tq);
+      const unsigned w1 = *reinterpret_cast<const unsigned*>(s_codes + r1 * ROWB + ((ks ^ s1) << 4) + 4 * tq);
       const unsigned af0 = w0 & 0x0F0F0F0Fu, af1 = w1 & 0x0F0F0F0Fu;
       const unsigned af2 = (w0 >> 4) & 0x0F0F0F0Fu, af3 = (w1 >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
@@ -350,30 +392,37 @@ __global__ void __launch_bounds__(256, REQ ? 6 : 0) scan_kernel(const ScanArgs a
 }
 
 template <int D, int G, typename E>
-cudaError_t launch_scan_t(const ScanArgs& a, const SeqArgs& seq, int B, int64_t nmax_live, cudaStream_t st) {
+cudaError_t launch_scan_t(const ScanArgs& a, const SeqArgs& seq, int B, int64_t nmax_live, const CUtensorMap* tm,
+                          cudaStream_t st) {
   dim3 grid((unsigned)((nmax_live + kTile - 1) / kTile), (unsigned)(B * a.Hkv));
+  static const CUtensorMap none = {};
+  const CUtensorMap& t = tm ? *tm : none;
   // REQ: the variant that re-quantises the appended block first (device-
   // length steps); a separate instantiation keeps the plain scan's
   // registers (and resident CTAs) as they are
   if (a.dp4a && !a.requant && !a.two_digit) {
-    launch_pdl(scan_kernel<D, G, E, false, false, true>, grid, dim3(256), 0, st, a, seq);
+    launch_pdl(scan_kernel<D, G, E, false, false, true>, grid, dim3(256), 0, st, a, seq, t);
   } else if (a.requant) {
-    if (a.two_digit) launch_pdl(scan_kernel<D, G, E, true, true>, grid, dim3(256), 0, st, a, seq);
-    else launch_pdl(scan_kernel<D, G, E, false, true>, grid, dim3(256), 0, st, a, seq);
+    if (a.two_digit) launch_pdl(scan_kernel<D, G, E, true, true>, grid, dim3(256), 0, st, a, seq, t);
+    else launch_pdl(scan_kernel<D, G, E, false, true>, grid, dim3(256), 0, st, a, seq, t);
+  } else if (a.two_digit) {
+    launch_pdl(scan_kernel<D, G, E, true, false>, grid, dim3(256), 0, st, a, seq, t);
+  } else if constexpr (D == 128) {
+    if (tm) launch_pdl(scan_kernel<D, G, E, false, false, false, true>, grid, dim3(256), 0, st, a, seq, t);
+    else launch_pdl(scan_kernel<D, G, E, false, false>, grid, dim3(256), 0, st, a, seq, t);
   } else {
-    if (a.two_digit) launch_pdl(scan_kernel<D, G, E, true, false>, grid, dim3(256), 0, st, a, seq);
-    else launch_pdl(scan_kernel<D, G, E, false, false>, grid, dim3(256), 0, st, a, seq);
+    launch_pdl(scan_kernel<D, G, E, false, false>, grid, dim3(256), 0, st, a, seq, t);
   }
   return cudaGetLastError();
 }
 
 #define CSA_SCAN_CASE(DD, GG)                                                          \
   if (d == DD && G == GG)                                                              \
-    return bf16 ? launch_scan_t<DD, GG, __nv_bfloat16>(a, seq, B, nmax_live, st)       \
-                : launch_scan_t<DD, GG, float>(a, seq, B, nmax_live, st);
+    return bf16 ? launch_scan_t<DD, GG, __nv_bfloat16>(a, seq, B, nmax_live, tm, st)   \
+                : launch_scan_t<DD, GG, float>(a, seq, B, nmax_live, tm, st);
 
 cudaError_t launch_scan(const ScanArgs& a, const SeqArgs& seq, int B, int d, int G, bool bf16,
-                        int64_t nmax_live, cudaStream_t st) {
+                        int64_t nmax_live, const CUtensorMap* tm, cudaStream_t st) {
   CSA_SCAN_CASE(128, 1) CSA_SCAN_CASE(128, 2) CSA_SCAN_CASE(128, 4) CSA_SCAN_CASE(128, 8)
   CSA_SCAN_CASE(64, 1) CSA_SCAN_CASE(64, 2) CSA_SCAN_CASE(64, 4) CSA_SCAN_CASE(64, 8)
   return cudaErrorInvalidValue;

@@ -1069,10 +1069,29 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
   for (int i = tid; i < G * D; i += 256) (&s_nr[0][0])[i] = 0.f;
   if (tid < G) { s_dr[tid] = 0.f; s_hr[tid] = 0.f; }
   __syncthreads();
+  // every load of this phase is issued before its values are used: the
+  // warp's eight window rows and their scores, c32, and (below) the pool's
+  // value-norm bounds
+  constexpr int RPW = kWindow / 8;   // window rows per warp
+  const E* Vb = reinterpret_cast<const E*>(a.V) + ((int64_t)bg * a.n_max + P) * D;
+  float vw[RPW][CPL], sw[RPW][G];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    const int row = w + 8 * i;
+    load_row<D, E>(Vb + (int64_t)row * D, vw[i]);
+    const float* ws = a.win + ((int64_t)bg * kWindow + row) * G;
+#pragma unroll
+    for (int h = 0; h < G; ++h) sw[i][h] = ws[h];
+  }
   float c32[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
-  const E* Vb = reinterpret_cast<const E*>(a.V) + ((int64_t)bg * a.n_max + P) * D;
+  float vmx = 0.f;
+  {
+    const int64_t nbp = (P + kBlock - 1) / kBlock;
+#pragma unroll 8
+    for (int64_t i = tid; i < nbp; i += 256) vmx = fmaxf(vmx, a.vmax[(int64_t)bg * a.nblk_max + i]);
+  }
   float nr[G][CPL], dr[G], hr[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -1081,20 +1100,17 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
     for (int c = 0; c < CPL; ++c) nr[h][c] = 0.f;
   }
 #pragma unroll
-  for (int row = w; row < kWindow; row += 8) {
-    float v[CPL];
-    load_row<D, E>(Vb + (int64_t)row * D, v);
+  for (int i = 0; i < RPW; ++i) {
     float sq = 0.f;
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) sq += v[c] * v[c];
-    const float* ws = a.win + ((int64_t)bg * kWindow + row) * G;
+    for (int c = 0; c < CPL; ++c) sq += vw[i][c] * vw[i][c];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float wt = expf(fsub(ws[h], c32[h]));
+      const float wt = expf(fsub(sw[i][h], c32[h]));
       dr[h] += wt;
       hr[h] += wt * sq;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) nr[h][c] += wt * v[c];
+      for (int c = 0; c < CPL; ++c) nr[h][c] += wt * vw[i][c];
     }
   }
 #pragma unroll
@@ -1106,11 +1122,7 @@ __global__ void __launch_bounds__(256) predict_kernel(const SparseArgs a, const 
   }
   // largest value-norm bound over the pool blocks
   {
-    const int64_t nbp = (P + kBlock - 1) / kBlock;
-    float m = 0.f;
-#pragma unroll 8
-    for (int64_t i = tid; i < nbp; i += 256) m = fmaxf(m, a.vmax[(int64_t)bg * a.nblk_max + i]);
-    m = warp_max(m);
+    const float m = warp_max(vmx);
     if (lane == 0) s_vm[w] = m;
   }
   __syncthreads();
@@ -2034,8 +2046,9 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
   constexpr int CPL = D / 32;
   constexpr int LB = 32;                   // levels per shared-memory batch
   __shared__ float s_pre[LB][ACC];
-  __shared__ float s_run[ACC];
   __shared__ float s_vec[LB][4];           // ||c||^2, ||o_hat - c||^2, c.S1, ||o_hat||^2
+  __shared__ unsigned s_jr[kMaxJ + 2];     // rows first needed per level (and the 8-bit tier's change)
+  __shared__ int s_jd[kMaxJ + 2];
   __shared__ float s_beta[LB], s_dh[LB];
   __shared__ int s_cert[LB];
   __shared__ float s_win[D + 4];
@@ -2062,46 +2075,54 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
   const int64_t n = seq.n[b];
   const int J = seq.J[b];
   const int lo = st[0], hi = st[1];
+  const float* accb = a.acc + (int64_t)bh * a.J1 * ACC;
+  // Thread tid owns columns tid and tid + 256 of the per-level sums: their
+  // running totals stay in its registers (r0, r1) across batches and rounds
+  // (the previous round's are in pref).  A batch's LB levels are loaded at
+  // once, the next batch while this one is evaluated.
+  static_assert(ACC <= 512, "two columns per thread");
+  const int x0 = tid, x1 = tid + 256;
+  const bool h0 = x0 < ACC, h1 = x1 < ACC;
+  float v0[LB], v1[LB];
+  auto load_batch = [&](int l0, int nl) {
+#pragma unroll
+    for (int u = 0; u < LB; ++u) {
+      v0[u] = (h0 && u < nl) ? accb[(int64_t)(l0 + u) * ACC + x0] : 0.f;
+      v1[u] = (h1 && u < nl) ? accb[(int64_t)(l0 + u) * ACC + x1] : 0.f;
+    }
+  };
+  // one round of loads: the first batch, the earlier rounds' sums, the
+  // window sums, the rows-needed histogram up to J, the value-norm bound
+  int l0 = lo + 1;
+  int nl = min(LB, hi - l0 + 1);
+  if (l0 <= hi) load_batch(l0, nl);
+  float r0 = (h0 && lo >= 0) ? a.pref[(int64_t)bh * ACC + x0] : 0.f;
+  float r1 = (h1 && lo >= 0) ? a.pref[(int64_t)bh * ACC + x1] : 0.f;
   for (int i = tid; i < D + 4; i += 256) s_win[i] = a.winstats[(int64_t)bh * (D + 4) + i];
+  for (int l = tid; l <= J; l += 256) {
+    s_jr[l] = a.jr_hist[(int64_t)bh * (a.J1 + 1) + l];
+    s_jd[l] = a.refine8 ? a.jrd[(int64_t)bh * (a.J1 + 1) + l] : 0;
+  }
+  const float Vp = a.vmaxp[bg];
   __syncthreads();
   const float DR = s_win[D], HR = s_win[D + 1];
-  const float Vp = a.vmaxp[bg];
   const float de = a.delta / (4.0f * (float)(J + 1));
   const float L = logf(1.0f / de), Lz = logf(2.0f / de);
-  const float* accb = a.acc + (int64_t)bh * a.J1 * ACC;
   int found = -1;
-  // sums over the levels of earlier rounds: kept by the previous round
-  for (int x = tid; x < ACC; x += 256) s_run[x] = lo >= 0 ? a.pref[(int64_t)bh * ACC + x] : 0.f;
-  __syncthreads();
-  for (int l0 = lo + 1; l0 <= hi && found < 0; l0 += LB) {
-    const int nl = min(LB, hi - l0 + 1);
-    {
-      // running sums over the batch's levels, columns tid and tid + 256:
-      // every load of the batch issued before the first add
-      static_assert(ACC <= 512, "two columns per thread");
-      const int x0 = tid, x1 = tid + 256;
-      const bool h0 = x0 < ACC, h1 = x1 < ACC;
-      float v0[LB], v1[LB];
+  while (l0 <= hi && found < 0) {
 #pragma unroll
-      for (int u = 0; u < LB; ++u) {
-        v0[u] = (h0 && u < nl) ? accb[(int64_t)(l0 + u) * ACC + x0] : 0.f;
-        v1[u] = (h1 && u < nl) ? accb[(int64_t)(l0 + u) * ACC + x1] : 0.f;
-      }
-      float r0 = h0 ? s_run[x0] : 0.f, r1 = h1 ? s_run[x1] : 0.f;
-#pragma unroll
-      for (int u = 0; u < LB; ++u) {
-        if (h0 && u < nl) {
-          r0 += v0[u];
-          s_pre[u][x0] = r0;
-          if (h1) {
-            r1 += v1[u];
-            s_pre[u][x1] = r1;
-          }
+    for (int u = 0; u < LB; ++u) {
+      if (h0 && u < nl) {
+        r0 += v0[u];
+        s_pre[u][x0] = r0;
+        if (h1) {
+          r1 += v1[u];
+          s_pre[u][x1] = r1;
         }
       }
-      if (h0) s_run[x0] = r0;
-      if (h1) s_run[x1] = r1;
     }
+    const int l1 = l0 + LB, nl1 = min(LB, hi - l1 + 1);
+    if (l1 <= hi) load_batch(l1, nl1);
     __syncthreads();
     // vector parts, one warp per level
     for (int i = w; i < nl; i += 8) {
@@ -2182,11 +2203,9 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       // rows read up to the stop level: warp 0 sums the bound-level histogram
       unsigned kr = 0, kr8 = 0;
       if (w == 0) {
-        const unsigned* jr = a.jr_hist + (int64_t)bh * (a.J1 + 1);
-        const int* jd = a.refine8 ? a.jrd + (int64_t)bh * (a.J1 + 1) : nullptr;
         for (int l = lane; l <= found; l += 32) {
-          kr8 += jr[l];
-          kr += jd ? (unsigned)((int)jr[l] + jd[l]) : jr[l];
+          kr8 += s_jr[l];
+          kr += (unsigned)((int)s_jr[l] + s_jd[l]);
         }
         kr = __reduce_add_sync(0xffffffffu, kr);
         kr8 = __reduce_add_sync(0xffffffffu, kr8);
@@ -2208,10 +2227,13 @@ __global__ void __launch_bounds__(256) certify_kernel(const SparseArgs a, const 
       }
     }
     __syncthreads();
+    l0 = l1;
+    nl = nl1;
   }
   if (found < 0 && hi < J) {
     // the head continues: keep its sums through this range for the next round
-    for (int x = tid; x < ACC; x += 256) a.pref[(int64_t)bh * ACC + x] = s_run[x];
+    if (h0) a.pref[(int64_t)bh * ACC + x0] = r0;
+    if (h1) a.pref[(int64_t)bh * ACC + x1] = r1;
   }
   if (found < 0 && tid == 0) {
     if (hi >= J) {

@@ -1652,8 +1652,10 @@ __global__ void __launch_bounds__(256) vgather_kernel(const SparseArgs a, const 
 #define CSA_VS_WARPS 4
 #endif
 #ifndef CSA_VS_STAGES
-#define CSA_VS_STAGES 3
+#define CSA_VS_STAGES 4
 #endif
+// (stages x warps on the 128K x 4 step, two chains: 3 x 4 623-627 us,
+// 4 x 4 620-621, 2 x 8 623-624, 2 x 4 625-628, 3 x 2 635-638)
 constexpr int kVsW = CSA_VS_WARPS;              // warps per CTA
 constexpr int kVsS = CSA_VS_STAGES;             // row stages per warp (>= 2)
 constexpr int kVsE = 2 * kVsS;                  // entry / descriptor slots per warp

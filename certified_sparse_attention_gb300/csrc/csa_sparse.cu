@@ -62,7 +62,7 @@ constexpr unsigned kVsBucketCost = CSA_VS_BUCKET_COST;
 #define CSA_RING_W 4
 #endif
 #ifndef CSA_ROWS_CPS
-#define CSA_ROWS_CPS 12
+#define CSA_ROWS_CPS 16
 #endif
 #ifndef CSA_ROWS0_CPS
 #define CSA_ROWS0_CPS 5
@@ -2380,11 +2380,11 @@ template <int D, int G, typename E, int MODE>
 void launch_rows_t(int64_t items, int nsm, cudaStream_t st, const SparseArgs& a, const SeqArgs& seq, int round) {
   constexpr int smem = rows_smem<D, G, E>();
   cudaFuncSetAttribute(rows_kernel<D, G, E, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  // kRowsCps (12) CTAs of 4 warps per SM over all groups, several waves:
+  // kRowsCps (16) CTAs of 4 warps per SM over all groups, several waves:
   // many short shares balance the uneven density of wanted entries (and
   // keep more rows in flight) better than one long share per resident warp
-  // (rescoring 168 us per 128K x 4 step against 199 us with 4 CTAs of 8
-  // warps per SM)
+  // (rescoring of the unsplit 128K x 4 step: 199 us with 4 CTAs of 8 warps
+  // per SM; 179, 168 and 164 us with 8, 12 and 16 CTAs of 4 warps)
   const int per = per_group(a, (MODE == 0 ? kRows0Cps : kRowsCps) * (int64_t)nsm, (items + 8 * kRingW - 1) / (8 * kRingW));
   launch_pdl(rows_kernel<D, G, E, MODE>, dim3((unsigned)per, (unsigned)(a.B * a.Hkv)), dim3(kRingW * 32), smem, st,
              a, seq, round);

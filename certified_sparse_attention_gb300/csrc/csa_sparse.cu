@@ -1262,23 +1262,6 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
   const int64_t kend = min(P, k0 + isz);
   const int J = seq.J[b];
   const int bh0 = b * a.Hq + g * G;
-  int lo[G], hi[G];
-  int wlo = J + 1, whi = -1;
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const int* st = a.state + (int64_t)(bh0 + h) * 4;
-    lo[h] = st[0];
-    hi[h] = (st[3] & kFlagDone) ? st[0] : st[1];
-    if (hi[h] > lo[h]) { wlo = min(wlo, lo[h] + 1); whi = max(whi, hi[h]); }
-  }
-  if (whi < 0) return;
-  float c32[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
-  const float neg_r = -(float)a.r;
-  // this round's bucket counters (one set per round, zeroed with the step)
-  unsigned* bcnt = a.bcnt + ((int64_t)round * a.B * a.Hkv + bg) * a.J1;
-  uint2* bk = a.buckets + (int64_t)bg * a.J1 * a.pcap;
   const float* sb = a.s32 + (int64_t)bg * a.pcap * G;
   const float* tb = a.t32 + (int64_t)bg * a.pcap * (PH ? G : 1);
   // scores and t of a key, loaded one 256-key step ahead
@@ -1302,8 +1285,27 @@ __device__ __forceinline__ void levels_item(const SparseArgs& a, const SeqArgs& 
       for (int h = 0; h < G; ++h) t[h] = t0;
     }
   };
+  // the item's first keys, c32 and the heads' ranges load together (one
+  // round trip before the first tile, not three)
   float cs[G], ns[G], ct[G], nt[G];
   load_key(k0 + threadIdx.x, cs, ct);
+  float c32[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) c32[h] = cmax_get(a, bh0 + h, 3);
+  int lo[G], hi[G];
+  int whi = -1;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const int* st = a.state + (int64_t)(bh0 + h) * 4;
+    lo[h] = st[0];
+    hi[h] = (st[3] & kFlagDone) ? st[0] : st[1];
+    if (hi[h] > lo[h]) whi = max(whi, hi[h]);
+  }
+  if (whi < 0) return;
+  const float neg_r = -(float)a.r;
+  // this round's bucket counters (one set per round, zeroed with the step)
+  unsigned* bcnt = a.bcnt + ((int64_t)round * a.B * a.Hkv + bg) * a.J1;
+  uint2* bk = a.buckets + (int64_t)bg * a.J1 * a.pcap;
   for (int64_t key0 = k0; key0 < kend; key0 += 256) {
     const int64_t key = key0 + threadIdx.x;
     load_key(key + 256, ns, nt);
